@@ -1,0 +1,238 @@
+"""Python access to the CPU oracle (``oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: this package is imported by ``tests/``, by
+``__graft_entry__.smoke()`` and by the CPU-baseline leg of ``bench.py``; the
+product path (``place_kv_cache_gb300``) never imports, loads or calls it, and
+the two share no code.
+
+Arrays are numpy: bf16 values are ``uint16`` bit patterns, fp32 values are
+``float32``. Attention results are fp64. Every wrapper returns the oracle's
+result or raises ``OracleError`` with the oracle's status code.
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against closed
+forms, invariants and the figures printed on the pages.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+# gcc command that builds the oracle; __graft_entry__.build() runs the same line.
+BUILD_CMD = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+             "-o", _LIB, _SRC, "-lm"]
+
+F32, BF16 = 0, 1
+Q_DYNAMIC, Q_FIXED = 0, 1
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def build(force: bool = False) -> str:
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        subprocess.run(BUILD_CMD, check=True)
+    return _LIB
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB)
+        vp, i32, f64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_float
+        L.orc_visible_range.argtypes = [i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+        L.orc_decode_attention.argtypes = [vp, i32, i32, vp, i32, i32, i32, i32, i32, vp, f64, i32, vp]
+        L.orc_paged_attention.argtypes = [vp, i32, i32, vp, i32, i32, i32, i32, i32, vp, i32, i32, vp,
+                                          f64, i32, vp]
+        L.orc_cache_update.argtypes = [vp, i32, i32, i32, i32, i32, vp, i32, vp]
+        L.orc_paged_update.argtypes = [vp, i32, i32, i32, i32, i32, vp, i32, i32, vp, i32, vp]
+        L.orc_pack_u4.argtypes = [vp, i32, vp]
+        L.orc_pack_u4.restype = None
+        L.orc_unpack_u4.argtypes = [vp, i32, vp]
+        L.orc_unpack_u4.restype = None
+        L.orc_int4_quantize_row.argtypes = [vp, i32, i32, f32, i32, vp, vp, vp]
+        L.orc_int4_dequantize_row.argtypes = [vp, vp, vp, i32, vp]
+        L.orc_int4_append.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, i32, vp, i32, f32, i32]
+        L.orc_int4_attention.argtypes = [vp, i32, vp, vp, vp, i32, i32, i32, i32, vp, vp, f64, i32, vp]
+        L.orc_fp16_to_double.argtypes = [ctypes.c_uint16]
+        L.orc_fp16_to_double.restype = f64
+        L.orc_float_to_fp16.argtypes = [f32]
+        L.orc_float_to_fp16.restype = ctypes.c_uint16
+        _lib = L
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise OracleError(f"{what}: oracle status {rc}")
+
+
+def _dtype_code(a: np.ndarray) -> int:
+    if a.dtype == np.float32:
+        return F32
+    if a.dtype == np.uint16:
+        return BF16
+    raise TypeError(f"oracle takes float32 or uint16 (bf16 bits), got {a.dtype}")
+
+
+def _c(a, dtype=None):
+    return np.ascontiguousarray(a if dtype is None else np.asarray(a, dtype=dtype))
+
+
+def default_scale(head_dim: int) -> float:
+    return 1.0 / float(np.sqrt(head_dim))
+
+
+def visible_range(n: int, window: int = -1):
+    lo, hi = ctypes.c_int(), ctypes.c_int()
+    lib().orc_visible_range(n, window, ctypes.byref(lo), ctypes.byref(hi))
+    return lo.value, hi.value
+
+
+def decode_attention(q, cache, lens, scale: Optional[float] = None, window: int = -1) -> np.ndarray:
+    """q [B, Hq, D]; cache [2, B, Hkv, C, D]; lens [B] -> y [B, Hq, D] fp64."""
+    q, cache, lens = _c(q), _c(cache), _c(lens, np.int32)
+    B, Hq, D = q.shape
+    _, B2, Hkv, C, D2 = cache.shape
+    assert B == B2 and D == D2
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    s = default_scale(D) if scale is None else scale
+    _check(lib().orc_decode_attention(_ptr(q), _dtype_code(q), Hq, _ptr(cache), _dtype_code(cache),
+                                      B, Hkv, C, D, _ptr(lens), s, window, _ptr(out)), "decode_attention")
+    return out
+
+
+def paged_attention(q, pool, block_table, lens, scale: Optional[float] = None, window: int = -1) -> np.ndarray:
+    """q [B, Hq, D]; pool [2, P, Hkv, S, D]; block_table [B, M] -> y [B, Hq, D] fp64."""
+    q, pool, bt, lens = _c(q), _c(pool), _c(block_table, np.int32), _c(lens, np.int32)
+    B, Hq, D = q.shape
+    _, P, Hkv, S, D2 = pool.shape
+    assert D == D2 and bt.shape[0] == B
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    s = default_scale(D) if scale is None else scale
+    _check(lib().orc_paged_attention(_ptr(q), _dtype_code(q), Hq, _ptr(pool), _dtype_code(pool), P, Hkv, S,
+                                     D, _ptr(bt), bt.shape[1], B, _ptr(lens), s, window, _ptr(out)),
+           "paged_attention")
+    return out
+
+
+def cache_update(cache: np.ndarray, values, positions) -> None:
+    """In place: cache [2, B, H, C, D]; values [2, B, H, new_len, D]; positions [B]."""
+    assert cache.flags.c_contiguous
+    values, positions = _c(values, cache.dtype), _c(positions, np.int32)
+    _, B, H, C, D = cache.shape
+    new_len = values.shape[3]
+    assert values.shape == (2, B, H, new_len, D)
+    _check(lib().orc_cache_update(_ptr(cache), _dtype_code(cache), B, H, C, D, _ptr(values), new_len,
+                                  _ptr(positions)), "cache_update")
+
+
+def paged_update(pool: np.ndarray, block_table, values, positions) -> None:
+    """In place: pool [2, P, H, S, D]; block_table [B, M]; values [2, B, H, new_len, D]."""
+    assert pool.flags.c_contiguous
+    bt, values, positions = _c(block_table, np.int32), _c(values, pool.dtype), _c(positions, np.int32)
+    _, P, H, S, D = pool.shape
+    B, M = bt.shape
+    new_len = values.shape[3]
+    assert values.shape == (2, B, H, new_len, D)
+    _check(lib().orc_paged_update(_ptr(pool), _dtype_code(pool), P, H, S, D, _ptr(bt), M, B, _ptr(values),
+                                  new_len, _ptr(positions)), "paged_update")
+
+
+def pack_u4(codes) -> np.ndarray:
+    codes = _c(codes, np.uint8)
+    out = np.zeros((codes.size + 1) // 2, dtype=np.uint8)
+    lib().orc_pack_u4(_ptr(codes), codes.size, _ptr(out))
+    return out
+
+
+def unpack_u4(packed, n: int) -> np.ndarray:
+    packed = _c(packed, np.uint8)
+    out = np.zeros(n, dtype=np.uint8)
+    lib().orc_unpack_u4(_ptr(packed), n, _ptr(out))
+    return out
+
+
+def int4_row_bytes(D: int):
+    """(code bytes, scales, zero-point bytes) of one token row of one head."""
+    return D // 2, D // 32, (D // 32 + 1) // 2
+
+
+def int4_quantize_row(x_bf16, mode: int = Q_DYNAMIC, fixed_scale: float = 0.25, fixed_zp: int = 8):
+    """One token's D bf16 values -> (codes [D/2] u8, scales [D/32] fp16 bits, zps [ceil(D/64)] u8)."""
+    x = _c(x_bf16, np.uint16)
+    D = x.size
+    cb, sb, zb = int4_row_bytes(D)
+    codes = np.zeros(cb, np.uint8)
+    scales = np.zeros(sb, np.uint16)
+    zps = np.zeros(zb, np.uint8)
+    _check(lib().orc_int4_quantize_row(_ptr(x), D, mode, fixed_scale, fixed_zp, _ptr(codes), _ptr(scales),
+                                       _ptr(zps)), "int4_quantize_row")
+    return codes, scales, zps
+
+
+def int4_dequantize_row(codes, scales, zps) -> np.ndarray:
+    codes, scales, zps = _c(codes, np.uint8), _c(scales, np.uint16), _c(zps, np.uint8)
+    D = codes.size * 2
+    out = np.zeros(D, np.float64)
+    _check(lib().orc_int4_dequantize_row(_ptr(codes), _ptr(scales), _ptr(zps), D, _ptr(out)),
+           "int4_dequantize_row")
+    return out
+
+
+def int4_planes(B: int, H: int, C: int, D: int):
+    """Fresh zeroed INT4 planes (codes, scales, zps) for a [2, B, H, C, D] logical cache."""
+    cb, sb, zb = int4_row_bytes(D)
+    return (np.zeros((2, B, H, C, cb), np.uint8), np.zeros((2, B, H, C, sb), np.uint16),
+            np.zeros((2, B, H, C, zb), np.uint8))
+
+
+def int4_append(codes, scales, zps, values_bf16, positions, mode: int = Q_DYNAMIC,
+                fixed_scale: float = 0.25, fixed_zp: int = 8) -> None:
+    """In place on the planes; values [2, B, H, new_len, D] bf16 bits."""
+    for a in (codes, scales, zps):
+        assert a.flags.c_contiguous
+    values, positions = _c(values_bf16, np.uint16), _c(positions, np.int32)
+    _, B, H, new_len, D = values.shape
+    C = codes.shape[3]
+    _check(lib().orc_int4_append(_ptr(codes), _ptr(scales), _ptr(zps), B, H, C, D, _ptr(values), new_len,
+                                 _ptr(positions), mode, fixed_scale, fixed_zp), "int4_append")
+
+
+def int4_attention(q, codes, scales, zps, lens, cur_kv=None, scale: Optional[float] = None,
+                   window: int = -1) -> np.ndarray:
+    """q [B, Hq, D] bf16 bits; planes as from int4_planes; cur_kv [2, B, Hkv, 1, D] bf16 or None."""
+    q, codes, scales, zps, lens = _c(q, np.uint16), _c(codes), _c(scales), _c(zps), _c(lens, np.int32)
+    B, Hq, D = q.shape
+    _, B2, Hkv, C, _cb = codes.shape
+    assert B == B2
+    cur = None if cur_kv is None else _c(cur_kv, np.uint16)
+    out = np.zeros((B, Hq, D), np.float64)
+    s = default_scale(D) if scale is None else scale
+    _check(lib().orc_int4_attention(_ptr(q), Hq, _ptr(codes), _ptr(scales), _ptr(zps), B, Hkv, C, D,
+                                    _ptr(lens), _ptr(cur), s, window, _ptr(out)), "int4_attention")
+    return out
+
+
+def fp16_to_float(bits: int) -> float:
+    return float(lib().orc_fp16_to_double(int(bits)))
+
+
+def float_to_fp16(f: float) -> int:
+    return int(lib().orc_float_to_fp16(float(f)))
