@@ -1,0 +1,463 @@
+"""Decode-step benchmark: achieved HBM GB/s (and % of the measured HBM
+roofline), microseconds per step and rows x tokens / s of the fused decode
+step (in-place append + GQA decode attention) over a caller-owned KV cache.
+
+One step = one ``ol_decode_step`` over the whole batch of the workload: host
+validation, the append of one token per row and attention over every row's
+valid prefix, in one kernel launch. Steps are replayed from CUDA graphs so
+the host never limits a microsecond-scale step; when one step's cache fits in
+L2, consecutive steps rotate over enough independent cache replicas that the
+data of a step is never L2-resident from the previous visit.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                       [--impl ours|reference]
+Under torchrun each rank runs its own replica of the workload on its own GPU
+(independent rows: no collective on the data path; weak scaling); rank 0
+prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import WORKLOADS, bf16_from_f32, make_case  # noqa: E402
+
+METRIC = "decode step: achieved HBM GB/s (% of ~8 TB/s roofline), µs/step, rows·tok/s"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="qwen_b1_gqa7", choices=[k for k in WORKLOADS if k != "tiny_f32"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seconds", type=float, default=1.0, help="target timed seconds when --steps is not given")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def step_bytes(w, lens):
+    """Algorithmic HBM bytes of one step: K/V of every attended token (the new
+    token's K/V read from new_kv), the appended token written, q read, y written."""
+    elt = 2 if w.dtype == "bf16" else 4
+    D = w.head_dim
+    if w.layout == "int4":
+        kv_tok = 2 * (D // 2 + (D // 32) * 2 + D // 64)         # codes + fp16 scales + zero points, K and V
+        hist = float(np.sum(lens - 1)) * w.kv_heads * kv_tok
+        cur = w.batch * w.kv_heads * 2 * D * 2                   # current token read uncompressed (bf16)
+        written = w.batch * w.kv_heads * kv_tok
+    else:
+        hist = float(np.sum(lens - 1)) * w.kv_heads * 2 * D * elt
+        cur = w.batch * w.kv_heads * 2 * D * elt
+        written = w.batch * w.kv_heads * 2 * D * elt
+        if w.layout == "paged":
+            hist += float(np.sum(np.ceil(lens / w.page_size))) * 4   # block-table entries
+    q = w.batch * w.q_heads * D * 2
+    y = w.batch * w.q_heads * D * 2
+    return hist + cur + written + q + y
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------- ours
+
+def to_dev(a, dev):
+    import torch
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+    return torch.from_numpy(a).to(dev)
+
+
+class Setup:
+    """Device-resident inputs for one workload (one rank)."""
+
+    def __init__(self, w, dev, seed_offset=0):
+        import torch
+        import place_kv_cache_gb300 as ol
+        self.ol, self.torch, self.w, self.dev = ol, torch, w, dev
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(w.seed + 1000 * seed_offset)
+        rng = np.random.default_rng(w.seed + 1000 * seed_offset)
+        # lengths and page permutation from the seeded generator; bulk values from a seeded
+        # device generator (N(0,1), rounded to bf16): the benchmark times the path, the tests
+        # check its values against the oracle
+        from workloads import draw_lens
+        self.lens = draw_lens(rng, w)
+        self.lens_d = torch.from_numpy(self.lens).to(dev)
+        D = w.head_dim
+        B, H = w.batch, w.kv_heads
+        self.bytes_per_step = step_bytes(w, self.lens)
+        self.q = torch.randn((B, w.q_heads, D), generator=gen, device=dev).to(torch.bfloat16)
+        self.new_kv = torch.randn((2, B, H, 1, D), generator=gen, device=dev).to(torch.bfloat16)
+        self.out = torch.empty((B, w.q_heads, D), dtype=torch.bfloat16, device=dev)
+        ws_bytes = ol.ol_workspace_size(B, w.q_heads, H, D)
+        self.ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        self.ws_bytes = ws_bytes
+        ol.ol_workspace_init(self.ws, ws_bytes)
+        self.replicas = max(1, math.ceil(2 * L2_BYTES / max(1.0, self.bytes_per_step)))
+        self.replicas = min(self.replicas, 64)
+        self.caches, self.descs, self.updated = [], [], []
+        for r in range(self.replicas):
+            self._make_replica(gen, rng)
+        self.l2_note = (f"{self.replicas} cache replicas rotated, {self.replicas * self.bytes_per_step / 2**20:.0f} MiB "
+                        f"touched per rotation > 2x L2" if self.replicas > 1 else
+                        f"inputs larger than L2 ({self.bytes_per_step / 2**20:.0f} MiB per step)")
+
+    def resident_bytes(self):
+        w = self.w
+        if w.layout == "paged":
+            return 2 * w.num_pages * w.kv_heads * w.page_size * w.head_dim * 2
+        if w.layout == "int4":
+            return 2 * w.batch * w.kv_heads * w.capacity * (w.head_dim // 2 + w.head_dim // 16 + w.head_dim // 64)
+        return 2 * w.batch * w.kv_heads * w.capacity * w.head_dim * 2
+
+    def _make_replica(self, gen, rng):
+        torch, ol, w = self.torch, self.ol, self.w
+        B, H, D = w.batch, w.kv_heads, w.head_dim
+        if w.layout == "contiguous":
+            cache = torch.randn((2, B, H, w.capacity, D), generator=gen, device=self.dev).to(torch.bfloat16)
+            self.caches.append(cache)
+            self.descs.append(ol.kv_cache(cache))
+            self.updated.append(cache)
+            self.layout = ol.OL_LAYOUT_CONTIGUOUS
+        elif w.layout == "paged":
+            pool = torch.empty((2, w.num_pages, H, w.page_size, D), dtype=torch.bfloat16, device=self.dev)
+            for k in range(2):
+                for c0 in range(0, w.num_pages, 4096):
+                    c1 = min(w.num_pages, c0 + 4096)
+                    pool[k, c0:c1] = torch.randn((c1 - c0, H, w.page_size, D), generator=gen,
+                                                 device=self.dev).to(torch.bfloat16)
+            perm = rng.permutation(w.num_pages).astype(np.int32)
+            M = w.max_pages_per_row
+            table = np.ascontiguousarray(perm[: B * M].reshape(B, M))
+            bt_d = torch.from_numpy(table).to(self.dev)
+            self.caches.append((pool, bt_d, table))
+            self.descs.append(ol.paged_kv(pool, bt_d, table))
+            self.updated.append(pool)
+            self.layout = ol.OL_LAYOUT_PAGED
+        else:
+            rows = 2 * B * H * w.capacity
+            codes = torch.randint(0, 256, (2, B, H, w.capacity, D // 2), generator=gen, device=self.dev,
+                                  dtype=torch.int32).to(torch.uint8)
+            scales = (torch.rand((2, B, H, w.capacity, D // 32), generator=gen, device=self.dev) * 0.3 + 0.05)
+            scales = scales.to(torch.float16).view(torch.int16)
+            zps = torch.randint(0, 256, (2, B, H, w.capacity, D // 64), generator=gen, device=self.dev,
+                                dtype=torch.int32).to(torch.uint8)
+            del rows
+            self.caches.append((codes, scales, zps))
+            self.descs.append(ol.int4_kv(codes, scales, zps, head_dim=D))
+            self.updated.append(codes)
+            self.layout = ol.OL_LAYOUT_INT4
+
+    def step(self, r, stream=None):
+        self.ol.ol_decode_step(self.layout, self.descs[r], self.updated[r], self.q, self.w.q_heads, self.new_kv,
+                               self.lens, self.lens_d, 0.0, -1, self.out, self.ol.OL_BF16, self.ws, self.ws_bytes,
+                               stream=stream)
+
+
+def run_ours(args, rank, world, dist):
+    import torch
+    dev = f"cuda:{int(os.environ.get('LOCAL_RANK', 0))}"
+    torch.cuda.set_device(dev)
+    import place_kv_cache_gb300 as ol
+    ol.load()
+    w = WORKLOADS[args.workload]
+    s = Setup(w, dev, seed_offset=rank)
+    stream = torch.cuda.Stream(device=dev)
+    R = s.replicas
+    per_graph = max(R, 32)
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3) * R):
+            s.step(i % R)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(per_graph):
+                s.step(i % R)
+        g.replay()
+        stream.synchronize()
+    # calibrate the step time to size the timed region
+    t = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            g.replay()
+    stream.synchronize()
+    est = (time.perf_counter() - t) / (5 * per_graph)
+    if args.steps is None:
+        K = max(per_graph, int(args.seconds / max(est, 1e-7)) // per_graph * per_graph)
+    else:
+        K = max(per_graph, (args.steps + per_graph - 1) // per_graph * per_graph)
+    n_graphs = K // per_graph
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(int(os.environ.get("LOCAL_RANK", 0))) as clk:
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, int(0.3 / max(est * per_graph, 1e-6)))):
+                g.replay()                       # keep the GPU busy while the sampler settles
+        if dist is not None:
+            dist.barrier()
+        stream.synchronize()
+        clk.mark_start()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(n_graphs):
+                g.replay()
+            e1.record(stream)
+        stream.synchronize()
+        clk.mark_end()
+        if dist is not None:
+            dist.barrier()
+    ms = e0.elapsed_time(e1)
+    if dist is not None:
+        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    status = ol.ol_workspace_status(s.ws, stream=stream)
+    ms_per_step = ms / K
+    total_bytes = s.bytes_per_step * world
+    gbs = total_bytes / (ms_per_step * 1e-3) / 1e9
+    peak, peak_src = measured_peaks()
+    result = {
+        "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.layout != "int4" else "u4+bf16", "data": "synthetic",
+        "us_per_step": round(ms_per_step * 1e3, 3),
+        "rows_tok_per_s": round(w.batch * world / (ms_per_step * 1e-3), 1),
+        "pct_of_hbm_roofline": round(100.0 * gbs / world / peak, 2),
+        "config": {"workload": w.name, "layout": w.layout, "batch": w.batch, "q_heads": w.q_heads,
+                   "kv_heads": w.kv_heads, "head_dim": w.head_dim, "capacity": w.capacity,
+                   "lens_mean": float(np.mean(s.lens)), "bytes_per_step": s.bytes_per_step,
+                   "l2": s.l2_note, "graph_steps": per_graph, "parallelism": f"rows x{world} (independent)"},
+        "roofline": {"bound": "hbm", "achieved": round(gbs / world, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / world / peak, 4), "traffic": None,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else
+                     "fallback 6.8 TB/s"},
+        "gpu_launches": K,
+        "device_status": status,
+        "clocks": clk.summary(),
+    }
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(s, stream, K_e2e=min(K, 200 * R))
+    return result
+
+
+def run_e2e(s, stream, K_e2e):
+    """The same step through the public call with host buffers: per step, q, the
+    new K/V and the lengths are copied from pinned host memory to the device, the
+    step runs, and y is copied back to pinned host memory."""
+    torch = s.torch
+    q_h = s.q.cpu().pin_memory()
+    kv_h = s.new_kv.cpu().pin_memory()
+    lens_h = torch.from_numpy(s.lens).pin_memory()
+    y_h = torch.empty(s.out.shape, dtype=s.out.dtype).pin_memory()
+    h2d = q_h.numel() * 2 + kv_h.numel() * 2 + lens_h.numel() * 4
+    d2h = y_h.numel() * 2
+    R = s.replicas
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for i in range(3 * R):
+            s.q.copy_(q_h, non_blocking=True)
+            s.new_kv.copy_(kv_h, non_blocking=True)
+            s.lens_d.copy_(lens_h, non_blocking=True)
+            s.step(i % R)
+            y_h.copy_(s.out, non_blocking=True)
+        stream.synchronize()
+        e0.record(stream)
+        for i in range(K_e2e):
+            s.q.copy_(q_h, non_blocking=True)
+            s.new_kv.copy_(kv_h, non_blocking=True)
+            s.lens_d.copy_(lens_h, non_blocking=True)
+            s.step(i % R)
+            y_h.copy_(s.out, non_blocking=True)
+        e1.record(stream)
+    stream.synchronize()
+    ms = e0.elapsed_time(e1) / K_e2e
+    return {"value": round(s.bytes_per_step / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "us_per_step": round(ms * 1e3, 3),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": K_e2e}
+
+
+# --------------------------------------------------------------- oracle
+
+def oracle_step_inputs(w, max_rows):
+    """A bounded sample of the workload for the CPU oracle: the first max_rows rows."""
+    import oracle as O
+    from workloads import scaled
+    rows = min(w.batch, max_rows)
+    ws = scaled(w, batch=rows)
+    case = make_case(ws, seed=w.seed)
+    return O, ws, case
+
+
+def run_oracle_steps(w, budget_s, max_rows):
+    """Time the oracle's decode step (append + attention) on a sample of the workload."""
+    from workloads import block_table, contiguous_cache, poisoned_pool
+    O, ws, case = oracle_step_inputs(w, max_rows)
+    if w.layout == "contiguous":
+        cache = contiguous_cache(case)
+
+        def one():
+            O.cache_update(cache, case.new_kv, case.lens - 1)
+            return O.decode_attention(case.q, cache, case.lens)
+    elif w.layout == "paged":
+        pool = poisoned_pool(ws)
+        table = block_table(case)
+        for b, h in enumerate(case.history):
+            if h.shape[2]:
+                O.paged_update(pool, table[b:b + 1], h[:, None], [0])
+
+        def one():
+            O.paged_update(pool, table, case.new_kv, case.lens - 1)
+            return O.paged_attention(case.q, pool, table, case.lens)
+    else:
+        planes = O.int4_planes(ws.batch, ws.kv_heads, ws.capacity, ws.head_dim)
+        for b, h in enumerate(case.history):
+            sub = O.int4_planes(1, ws.kv_heads, ws.capacity, ws.head_dim)
+            O.int4_append(*sub, h[:, None], [0])
+            for full, part in zip(planes, sub):
+                full[:, b] = part[:, 0]
+
+        def one():
+            O.int4_append(*planes, case.new_kv, case.lens - 1)
+            return O.int4_attention(case.q, *planes, case.lens, cur_kv=case.new_kv)
+    times = []
+    t_all = time.perf_counter()
+    while True:
+        t = time.perf_counter()
+        one()
+        times.append(time.perf_counter() - t)
+        if time.perf_counter() - t_all > budget_s or len(times) >= 1000:
+            break
+    sec = statistics.median(times)
+    nbytes = step_bytes(ws, case.lens)
+    return {"value": round(nbytes / sec / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{len(times)} oracle decode steps (append + attention, fp64) on the first {ws.batch} of "
+                      f"{w.batch} rows of {w.name}; median {sec * 1e3:.1f} ms/step",
+            "us_per_step": round(sec * 1e6, 1), "rows_tok_per_s": round(ws.batch / sec, 2)}
+
+
+def run_reference(args, rank, world):
+    w = WORKLOADS[args.workload]
+    max_rows = {"qwen_b1_gqa7": 1, "ragged_b32": 4, "paged_b64": 2, "int4_b16": 1}[w.name]
+    K = args.steps if args.steps is not None else 3
+    budget = 60.0
+    res = run_oracle_steps(w, budget_s=min(budget, 10.0 * max(1, K)), max_rows=max_rows)
+    return {"impl": "reference", "metric": METRIC, "value": res["value"], "unit": "GB/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": res["us_per_step"] / 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "layout": w.layout, "batch": w.batch, "q_heads": w.q_heads,
+                       "kv_heads": w.kv_heads, "head_dim": w.head_dim, "capacity": w.capacity},
+            "cpu_baseline": res,
+            "e2e": {"value": res["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist_mod.init_process_group("nccl")
+        dist = dist_mod
+    result = run_ours(args, rank, world, dist)
+    if rank == 0 and not args.no_cpu_baseline:
+        w = WORKLOADS[args.workload]
+        max_rows = {"qwen_b1_gqa7": 1, "ragged_b32": 4, "paged_b64": 2, "int4_b16": 1}[w.name]
+        result["cpu_baseline"] = run_oracle_steps(w, budget_s=10.0, max_rows=max_rows)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+if __name__ == "__main__":
+    main()

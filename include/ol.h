@@ -1,0 +1,279 @@
+/*
+ * ol.h -- C ABI of the GB300 decode step over a caller-owned KV cache.
+ *
+ * One operation, in three cache layouts: append this step's K/V in place
+ * ("CacheUpdate": page "Mutable execution cache", sections Value model,
+ * Required alias, Model example and Runtime contract) fused with single-token
+ * attention softmax(q K^T * scale) V over the valid prefix (page "Persistent
+ * input/output feedback", section Optional heterogeneous paged KV: causal
+ * masking, left_window_size, grouped-query attention, online softmax, current
+ * K/V attended before they are encoded).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Pointers are DEVICE pointers unless the name ends in `_host`. The caller
+ *   owns every buffer: caches, q, values, outputs, block tables, workspace.
+ *   The library keeps no pointer after a call returns, apart from the
+ *   (base, size, owner) triples of ol_cache_bind.
+ * - The library allocates nothing: no cudaMalloc, no output cache, no copy
+ *   fallback. The only memory it touches is what the caller passes.
+ * - Every call validates everything on the host before any launch. A non-OK
+ *   return means nothing was written and nothing was launched. OL_OK means
+ *   the work was enqueued on `stream` (asynchronous with respect to the host).
+ * - Required alias: `updated_*` must equal the descriptor's data pointer on
+ *   every call (pointer identity), else OL_ERR_ALIAS. The descriptor must be
+ *   OL_READ_WRITE, else OL_ERR_READONLY. Capacity is part of the shape:
+ *   position + new_len > capacity is OL_ERR_CAPACITY, never growth.
+ * - Lengths: lens[b] counts the tokens row b attends, including the token this
+ *   step appends; the append position of a decode step is lens[b] - 1.
+ *   `*_host` arrays drive validation and launch sizing; `*_dev` arrays (same
+ *   values, on the device) drive the kernels. The caller keeps them equal;
+ *   the kernels still check every index they use and skip (never perform) an
+ *   access outside the caller's buffers, recording OL_DEVICE_GUARD in the
+ *   workspace status word where a workspace is passed.
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream). Calls on one workspace must not overlap on the GPU.
+ * - Alignment: every device pointer must be 16-byte aligned (OL_ERR_ALIGN).
+ * - dtype: OL_BF16 (bit pattern of bfloat16) or OL_F32. q and new K/V share
+ *   the cache's dtype; the attention output is OL_BF16 or OL_F32.
+ */
+#ifndef OL_H_
+#define OL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define OL_API __attribute__((visibility("default")))
+#else
+#define OL_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void* ol_stream; /* cudaStream_t */
+
+typedef enum ol_status {
+  OL_OK = 0,
+  OL_ERR_NULL = 1,         /* a required pointer is NULL */
+  OL_ERR_ALIAS = 2,        /* updated pointer != cache pointer, or an input/output overlaps the cache */
+  OL_ERR_READONLY = 3,     /* descriptor access is OL_READ_ONLY but the call writes the cache */
+  OL_ERR_CAPACITY = 4,     /* position + new_len > capacity, or lens[b] outside [0, capacity] */
+  OL_ERR_SHAPE = 5,        /* inconsistent sizes (q_heads not a multiple of kv_heads, ...) */
+  OL_ERR_DTYPE = 6,        /* unknown dtype, or a dtype the layout does not take */
+  OL_ERR_BUSY = 7,         /* the cache range is bound by another owner (ol_cache_bind) */
+  OL_ERR_WORKSPACE = 8,    /* workspace NULL or smaller than ol_workspace_size() */
+  OL_ERR_CUDA = 9,         /* a CUDA runtime call failed (launch error, bad stream, ...) */
+  OL_ERR_UNSUPPORTED = 10, /* a valid request this build does not implement */
+  OL_ERR_INJECTED = 11,    /* host fault injection: env OL_FAULT_INJECT=after_validate */
+  OL_ERR_PAGE = 12,        /* a block-table entry is outside the pool, or two rows append to one slot */
+  OL_ERR_ALIGN = 13        /* a device pointer is not 16-byte aligned */
+} ol_status;
+
+typedef enum ol_dtype { OL_F32 = 0, OL_BF16 = 1 } ol_dtype;
+
+/* ValueInfoProto.access of the cache binding (page "Mutable execution cache", Proto additions). */
+typedef enum ol_access { OL_READ_ONLY = 0, OL_READ_WRITE = 1 } ol_access;
+
+typedef enum ol_layout { OL_LAYOUT_CONTIGUOUS = 0, OL_LAYOUT_PAGED = 1, OL_LAYOUT_INT4 = 2 } ol_layout;
+
+/* How an INT4 append chooses (scale, zero point) per block of 32 values. */
+typedef enum ol_quant_mode {
+  OL_Q_DYNAMIC = 0, /* lo = min(0, min x), hi = max(0, max x), scale = fp16((hi-lo)/15) (1 if 0),
+                       zp = sat(round_half_even(-lo/scale)) */
+  OL_Q_FIXED = 1    /* scale = fp16(fixed_scale), zp = fixed_zp for every block */
+} ol_quant_mode;
+
+/* Device status word values (ol_workspace_status). */
+enum { OL_DEVICE_OK = 0, OL_DEVICE_GUARD = 1 };
+
+/*
+ * Contiguous cache [2, batch, kv_heads, capacity, head_dim], K plane 0,
+ * V plane 1, row-major, dtype OL_BF16 or OL_F32. Capacity is in the shape
+ * (page "Mutable execution cache", Model example: cache
+ * FLOAT16[2, batch, heads, max_length, head_size]).
+ * `owner` identifies the session for ol_cache_bind (0 = none).
+ */
+typedef struct ol_kv_cache {
+  void* data;
+  int32_t dtype;
+  int32_t batch, kv_heads, capacity, head_dim;
+  int32_t access;
+  uint64_t owner;
+} ol_kv_cache;
+
+/*
+ * Paged cache: one fixed pool [2, num_pages, kv_heads, page_size, head_dim]
+ * (K plane 0, V plane 1) and a block table [batch, max_pages] of int32 page
+ * indices: logical token t of row b lives in slot t % page_size of page
+ * block_table[b][t / page_size] (page "Mutable execution cache", ONNX Runtime
+ * GenAI: logical pages map to slices of the num_blocks axis of a pool that
+ * never grows). The capacity of a row is max_pages * page_size.
+ * `block_table_host` is the same table in host memory, used for validation.
+ */
+typedef struct ol_paged_kv {
+  void* data;
+  const int32_t* block_table;
+  const int32_t* block_table_host;
+  int32_t dtype;
+  int32_t num_pages, kv_heads, page_size, head_dim;
+  int32_t batch, max_pages;
+  int32_t access;
+  uint64_t owner;
+} ol_paged_kv;
+
+/*
+ * INT4 blockwise-affine cache, stored as three planes of the logical
+ * [2, batch, kv_heads, capacity, head_dim] cache (head_dim a multiple of 64):
+ *   codes  uint8 [2, batch, kv_heads, capacity, head_dim / 2]   two uint4 codes per byte, low nibble first
+ *   scales fp16  [2, batch, kv_heads, capacity, head_dim / 32]  one scale per block of 32 values
+ *   zps    uint8 [2, batch, kv_heads, capacity, head_dim / 64]  two uint4 zero points per byte, low first
+ * Reconstruction: (code - zp) * scale (page "Custom quantized and persistent
+ * values", Struct types and byte-encodable layouts: blocked affine, packing
+ * least-significant bits first). `codes` is the alias pointer.
+ */
+typedef struct ol_int4_kv {
+  uint8_t* codes;
+  uint16_t* scales;
+  uint8_t* zps;
+  int32_t batch, kv_heads, capacity, head_dim;
+  int32_t quant_mode;
+  float fixed_scale;
+  int32_t fixed_zp;
+  int32_t access;
+  uint64_t owner;
+} ol_int4_kv;
+
+/* Human-readable name of a status code (static string). */
+OL_API const char* ol_status_string(ol_status s);
+
+/* ABI version of this header (major * 100 + minor). */
+OL_API int32_t ol_version(void);
+
+/*
+ * Bytes of workspace the attention and step calls need for these sizes. The
+ * workspace holds the split-K partial results, one ticket counter per
+ * (row, kv head) and the device status word. Zero it once with
+ * ol_workspace_init before its first use; each call leaves its counters at
+ * zero when it completes.
+ */
+OL_API size_t ol_workspace_size(int32_t batch, int32_t q_heads, int32_t kv_heads, int32_t head_dim);
+
+/* Zero a workspace on `stream` (cudaMemsetAsync of the caller's memory). */
+OL_API ol_status ol_workspace_init(void* workspace, size_t ws_bytes, ol_stream stream);
+
+/*
+ * Read and clear the workspace's device status word (synchronizes `stream`).
+ * *status_out is OL_DEVICE_OK, or OL_DEVICE_GUARD if a kernel skipped an
+ * access because a device-side index disagreed with the validated sizes.
+ */
+OL_API ol_status ol_workspace_status(void* workspace, int32_t* status_out, ol_stream stream);
+
+/*
+ * Bind a writable cache range [base, base + bytes) to `owner` (page "Mutable
+ * execution cache", Runtime contract: one writable cache binding cannot be
+ * used concurrently by multiple sessions). Binding a range that overlaps a
+ * range bound by another owner returns OL_ERR_BUSY; rebinding one's own range
+ * is OL_OK. While bound, calls whose descriptor overlaps the range with a
+ * different `owner` return OL_ERR_BUSY. Unbinding a range one does not own
+ * returns OL_ERR_BUSY; unbinding an unbound range is OL_OK.
+ */
+OL_API ol_status ol_cache_bind(const void* base, size_t bytes, uint64_t owner);
+OL_API ol_status ol_cache_unbind(const void* base, uint64_t owner);
+
+/*
+ * CacheUpdate(cache, values, position) -> updated_cache, with updated_cache
+ * aliasing cache (page "Mutable execution cache", Value model and Model
+ * example). values [2, batch, kv_heads, new_len, head_dim] is written to rows
+ * [position, position + new_len) of every (plane, row, head); nothing else is
+ * written. position is the INT64 scalar of the page's example.
+ * Errors: NULL, ALIAS, READONLY, CAPACITY (position < 0 or
+ * position + new_len > capacity), SHAPE, DTYPE, BUSY, ALIGN, CUDA.
+ */
+OL_API ol_status ol_cache_update(const ol_kv_cache* cache, void* updated_cache, const void* values,
+                          int32_t new_len, int64_t position, ol_stream stream);
+
+/* As ol_cache_update with one position per row (positions_host/dev [batch] int32). */
+OL_API ol_status ol_cache_update_rows(const ol_kv_cache* cache, void* updated_cache, const void* values,
+                               int32_t new_len, const int32_t* positions_host,
+                               const int32_t* positions_dev, ol_stream stream);
+
+/*
+ * PagedCacheUpdate(cache, page_id, values, position): write values
+ * [2, batch, kv_heads, new_len, head_dim] to logical tokens
+ * [p_b, p_b + new_len) of each row through the block table, in place
+ * (page "Mutable execution cache", Heterogeneous paged cache and Runtime
+ * contract: existing pages are updated in place, nothing is allocated).
+ * Every page the write reaches must be in [0, num_pages) and no two rows
+ * may write the same slot (OL_ERR_PAGE).
+ */
+OL_API ol_status ol_paged_cache_update(const ol_paged_kv* kv, void* updated_pool, const void* values,
+                                int32_t new_len, const int32_t* positions_host,
+                                const int32_t* positions_dev, ol_stream stream);
+
+/*
+ * Decode attention over a contiguous cache (read-only use of the cache).
+ * q [batch, q_heads, head_dim] (cache dtype); out [batch, q_heads, head_dim]
+ * in out_dtype. Query head h reads kv head h / (q_heads / kv_heads). Row b
+ * attends its visible tokens: [0, lens[b]) if window < 0, else
+ * [max(0, lens[b] - 1 - window), lens[b]). lens[b] == 0 gives out = 0.
+ * scale <= 0 selects 1/sqrt(head_dim).
+ */
+OL_API ol_status ol_decode_attention(const ol_kv_cache* cache, const void* q, int32_t q_heads,
+                              const int32_t* lens_host, const int32_t* lens_dev, float scale,
+                              int32_t window, void* out, int32_t out_dtype, void* workspace,
+                              size_t ws_bytes, ol_stream stream);
+
+/* Decode attention over a paged cache; as ol_decode_attention. */
+OL_API ol_status ol_paged_decode_attention(const ol_paged_kv* kv, const void* q, int32_t q_heads,
+                                    const int32_t* lens_host, const int32_t* lens_dev,
+                                    float scale, int32_t window, void* out, int32_t out_dtype,
+                                    void* workspace, size_t ws_bytes, ol_stream stream);
+
+/*
+ * INT4 append: quantize values_bf16 [2, batch, kv_heads, 1, head_dim] per
+ * block of 32 (round half to even, saturate to [0, 15]; page "Persistent
+ * input/output feedback", quantization paragraph) and write codes, scales and
+ * zero points at row positions[b] of each (plane, row, head). updated_codes
+ * must equal cache->codes.
+ */
+OL_API ol_status ol_int4kv_append(const ol_int4_kv* cache, void* updated_codes, const void* values_bf16,
+                           const int32_t* positions_host, const int32_t* positions_dev,
+                           ol_stream stream);
+
+/*
+ * INT4 decode attention. History is reconstructed from the codes. If cur_kv
+ * ([2, batch, kv_heads, 1, head_dim] bf16) is non-NULL, the token at
+ * lens[b] - 1 takes part uncompressed from cur_kv instead of the codes (the
+ * current K/V are attended before they are encoded: page "Persistent
+ * input/output feedback", section Optional heterogeneous paged KV).
+ * q is bf16; otherwise as ol_decode_attention.
+ */
+OL_API ol_status ol_int4kv_decode_attention(const ol_int4_kv* cache, const void* q, int32_t q_heads,
+                                     const int32_t* lens_host, const int32_t* lens_dev,
+                                     const void* cur_kv, float scale, int32_t window, void* out,
+                                     int32_t out_dtype, void* workspace, size_t ws_bytes,
+                                     ol_stream stream);
+
+/*
+ * The fused decode step in one launch: append new_kv
+ * [2, batch, kv_heads, 1, head_dim] at position lens[b] - 1 of every row
+ * (CacheUpdate / PagedCacheUpdate / INT4 append, in place, `updated` aliasing
+ * the descriptor's data pointer) and attend [visible range of lens[b]] with
+ * the new token included. For OL_LAYOUT_INT4 the new token is attended
+ * uncompressed and stored encoded. `cache_desc` points to the ol_kv_cache,
+ * ol_paged_kv or ol_int4_kv that `layout` names. new_kv has the cache dtype
+ * (bf16 for INT4). Requires lens[b] >= 1.
+ */
+OL_API ol_status ol_decode_step(int32_t layout, const void* cache_desc, void* updated, const void* q,
+                         int32_t q_heads, const void* new_kv, const int32_t* lens_host,
+                         const int32_t* lens_dev, float scale, int32_t window, void* out,
+                         int32_t out_dtype, void* workspace, size_t ws_bytes, ol_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OL_H_ */

@@ -1,0 +1,688 @@
+// ol_api.cpp -- the C ABI declared in include/ol.h: host-side validation,
+// the cache bind registry, the split-K launch plan and kernel dispatch.
+//
+// Every check runs before any launch, so an error return means nothing was
+// written (page "Mutable execution cache", Runtime contract: overflow is an
+// error, never growth; read-only initializers are never mutable caches; one
+// writable binding is not used concurrently by several sessions; Required
+// alias: pointer identity checked, no silent copy fallback).
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "ol_internal.h"
+
+namespace ol {
+namespace {
+
+struct Range {
+  uintptr_t lo, hi;  // [lo, hi)
+  bool empty() const { return hi <= lo; }
+};
+Range range_of(const void* p, size_t bytes) {
+  uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return {a, a + bytes};
+}
+bool overlaps(Range a, Range b) { return !a.empty() && !b.empty() && a.lo < b.hi && b.lo < a.hi; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Binding {
+  uintptr_t lo, hi;
+  uint64_t owner;
+};
+std::mutex g_bind_mu;
+std::vector<Binding> g_bindings;
+
+ol_status check_owner(const Range* ranges, int nranges, uint64_t owner) {
+  std::lock_guard<std::mutex> lk(g_bind_mu);
+  for (const Binding& bd : g_bindings)
+    for (int i = 0; i < nranges; ++i)
+      if (overlaps(ranges[i], Range{bd.lo, bd.hi}) && bd.owner != owner) return OL_ERR_BUSY;
+  return OL_OK;
+}
+
+bool fault_injected() {
+  const char* v = std::getenv("OL_FAULT_INJECT");
+  return v && std::strcmp(v, "after_validate") == 0;
+}
+
+size_t elt_bytes(int dtype) { return dtype == OL_F32 ? 4 : 2; }
+bool valid_dtype(int d) { return d == OL_F32 || d == OL_BF16; }
+
+// Launch tuning: OL_TUNE="waves=<w>,minchunk=<c>,cfg=<variant>,cluster=<cs>,cpu=<k>" (read once).
+struct Tune {
+  int waves = 2;
+  int min_chunk = 16;
+  int cfg = -1;      // tensor-core kernel variant; -1 = default
+  int cluster = -1;  // cluster size cap; -1 = automatic
+  int clusters_per_unit = -1;  // cap on clusters per (row, kv head) for small batches
+};
+const Tune& tune() {
+  static Tune t = [] {
+    Tune x;
+    const char* v = std::getenv("OL_TUNE");
+    if (!v) return x;
+    std::string s(v);
+    size_t pos = 0;
+    while (pos < s.size()) {
+      size_t comma = s.find(',', pos);
+      std::string kv = s.substr(pos, comma == std::string::npos ? std::string::npos : comma - pos);
+      size_t eq = kv.find('=');
+      if (eq != std::string::npos) {
+        std::string k = kv.substr(0, eq);
+        int val = std::atoi(kv.c_str() + eq + 1);
+        if (k == "waves" && val > 0) x.waves = val;
+        if (k == "minchunk" && val >= 16) x.min_chunk = (val + 15) / 16 * 16;
+        if (k == "cfg" && val >= 0 && val <= 3) x.cfg = val;
+        if (k == "cluster" && val >= 1) x.cluster = val;
+        if (k == "cpu" && val >= 1) x.clusters_per_unit = val;
+      }
+      if (comma == std::string::npos) break;
+      pos = comma + 1;
+    }
+    return x;
+  }();
+  return t;
+}
+
+int pow2_floor(long long x) {
+  int r = 1;
+  while ((long long)r * 2 <= x) r *= 2;
+  return r;
+}
+
+// Pick the target split length so that about `target` CTAs cover all
+// (row, kv head) visible token ranges, within the workspace's CTA budget.
+void plan_splits(AttnParams& p, const int32_t* lens_host, long long target, int cluster) {
+  long long tok = 0;
+  for (int b = 0; b < p.batch; ++b) {
+    RowSplit rs = row_split(lens_host[b], p.window, 16);
+    tok += rs.hi - rs.start;
+  }
+  tok *= p.kv_heads;
+  long long chunk = target > 0 ? (tok + target - 1) / target : tok;
+  chunk = (chunk + 15) / 16 * 16;
+  if (chunk < tune().min_chunk) chunk = tune().min_chunk;
+  const long long budget = (long long)max_ctas(p.batch, p.kv_heads);
+  for (;;) {
+    long long total = 0;
+    for (int b = 0; b < p.batch; ++b) total += row_split(lens_host[b], p.window, (int)chunk, cluster).nsplit;
+    total *= p.kv_heads;
+    if (total <= budget || chunk >= (1ll << 30)) {
+      p.chunk = (int)chunk;
+      p.cluster = cluster;
+      p.total_ctas = (int)total;
+      return;
+    }
+    chunk *= 2;
+  }
+}
+
+// Tensor-core path: variant (warps x stages), CTAs per SM, and for batches
+// with fewer (row, kv head) units than SMs one wave of CTAs grouped in
+// clusters that merge their splits through distributed shared memory.
+void plan_fast(AttnParams& p, const int32_t* lens_host, int sms) {
+  const long long units = (long long)p.batch * p.kv_heads;
+  // measured defaults: 8 warps x 2 stages for contiguous caches and small
+  // batches, 4 warps x 2 stages (three CTAs per SM) for paged pools
+  if (tune().cfg >= 0)
+    p.variant = tune().cfg;
+  else
+    p.variant = (units >= sms && p.layout == OL_LAYOUT_PAGED) ? 2 : 3;
+  const int smem = fast_bf16_smem(p.variant) + 1024;
+  const int warps = fast_bf16_warps(p.variant);
+  int per_sm = (227 * 1024) / smem;
+  if (per_sm > 64 / warps) per_sm = 64 / warps;
+  if (per_sm < 1) per_sm = 1;
+  const long long slots = (long long)sms * per_sm;
+  if (units >= sms || units == 0) {
+    plan_splits(p, lens_host, slots * tune().waves, 1);
+    return;
+  }
+  int cs = pow2_floor(slots / units);
+  if (cs > 16) cs = 16;
+  const int cap = fast_bf16_max_cluster(p.variant, p.layout == OL_LAYOUT_PAGED);
+  if (cs > cap) cs = cap;
+  if (tune().cluster > 0 && cs > tune().cluster) cs = pow2_floor(tune().cluster);
+  // k clusters per (row, kv head), all CTAs resident at once: split length from the longest row
+  // one cluster per (row, kv head) by default: a second level of merging
+  // through global memory costs more than the extra CTAs gain
+  long long k = slots / (units * cs);
+  const long long kcap = tune().clusters_per_unit > 0 ? tune().clusters_per_unit : 1;
+  if (k > kcap) k = kcap;
+  if (k < 1) k = 1;
+  int longest = 0;
+  for (int b = 0; b < p.batch; ++b) {
+    RowSplit rs = row_split(lens_host[b], p.window, 16);
+    if (rs.hi - rs.start > longest) longest = rs.hi - rs.start;
+  }
+  long long chunk = (longest + cs * k - 1) / (cs * k);
+  chunk = (chunk + 15) / 16 * 16;
+  if (chunk < 16) chunk = 16;
+  long long total = 0;
+  for (int b = 0; b < p.batch; ++b) total += row_split(lens_host[b], p.window, (int)chunk, cs).nsplit;
+  p.chunk = (int)chunk;
+  p.cluster = cs;
+  p.total_ctas = (int)(total * p.kv_heads);
+}
+
+int sm_count_cached() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+// ----------------------------------------------------------- descriptors
+
+struct CacheView {
+  int layout;
+  int dtype;
+  int batch, kv_heads, head_dim, capacity;
+  int access;
+  uint64_t owner;
+  void* alias_ptr;  // pointer that `updated` must equal
+  Range ranges[3];  // cache storage (INT4: three planes)
+  int nranges;
+};
+
+ol_status view_contiguous(const ol_kv_cache* c, CacheView& v) {
+  if (!c || !c->data) return OL_ERR_NULL;
+  if (!valid_dtype(c->dtype)) return OL_ERR_DTYPE;
+  if (c->batch < 0 || c->kv_heads <= 0 || c->capacity < 0 || c->head_dim <= 0) return OL_ERR_SHAPE;
+  if (!aligned16(c->data)) return OL_ERR_ALIGN;
+  v = {};
+  v.layout = OL_LAYOUT_CONTIGUOUS;
+  v.dtype = c->dtype;
+  v.batch = c->batch;
+  v.kv_heads = c->kv_heads;
+  v.head_dim = c->head_dim;
+  v.capacity = c->capacity;
+  v.access = c->access;
+  v.owner = c->owner;
+  v.alias_ptr = c->data;
+  v.ranges[0] = range_of(c->data, 2ull * c->batch * c->kv_heads * c->capacity * c->head_dim * elt_bytes(c->dtype));
+  v.nranges = 1;
+  return OL_OK;
+}
+
+ol_status view_paged(const ol_paged_kv* c, CacheView& v) {
+  if (!c || !c->data || !c->block_table || !c->block_table_host) return OL_ERR_NULL;
+  if (!valid_dtype(c->dtype)) return OL_ERR_DTYPE;
+  if (c->batch < 0 || c->kv_heads <= 0 || c->num_pages <= 0 || c->page_size <= 0 || c->head_dim <= 0 ||
+      c->max_pages < 0)
+    return OL_ERR_SHAPE;
+  if ((long long)c->max_pages * c->page_size > (1ll << 30)) return OL_ERR_SHAPE;
+  if (!aligned16(c->data) || !aligned16(c->block_table)) return OL_ERR_ALIGN;
+  v = {};
+  v.layout = OL_LAYOUT_PAGED;
+  v.dtype = c->dtype;
+  v.batch = c->batch;
+  v.kv_heads = c->kv_heads;
+  v.head_dim = c->head_dim;
+  v.capacity = c->max_pages * c->page_size;
+  v.access = c->access;
+  v.owner = c->owner;
+  v.alias_ptr = c->data;
+  v.ranges[0] = range_of(c->data, 2ull * c->num_pages * c->kv_heads * c->page_size * c->head_dim *
+                                      elt_bytes(c->dtype));
+  v.nranges = 1;
+  return OL_OK;
+}
+
+ol_status view_int4(const ol_int4_kv* c, CacheView& v) {
+  if (!c || !c->codes || !c->scales || !c->zps) return OL_ERR_NULL;
+  if (c->batch < 0 || c->kv_heads <= 0 || c->capacity < 0 || c->head_dim <= 0) return OL_ERR_SHAPE;
+  if (c->head_dim % 64 != 0) return OL_ERR_SHAPE;
+  if (c->quant_mode != OL_Q_DYNAMIC && c->quant_mode != OL_Q_FIXED) return OL_ERR_SHAPE;
+  if (c->quant_mode == OL_Q_FIXED &&
+      (!(c->fixed_scale > 0.f) || !std::isfinite(c->fixed_scale) || c->fixed_zp < 0 || c->fixed_zp > 15))
+    return OL_ERR_SHAPE;
+  if (!aligned16(c->codes) || !aligned16(c->scales) || !aligned16(c->zps)) return OL_ERR_ALIGN;
+  v = {};
+  v.layout = OL_LAYOUT_INT4;
+  v.dtype = OL_BF16;
+  v.batch = c->batch;
+  v.kv_heads = c->kv_heads;
+  v.head_dim = c->head_dim;
+  v.capacity = c->capacity;
+  v.access = c->access;
+  v.owner = c->owner;
+  v.alias_ptr = c->codes;
+  const unsigned long long rows = 2ull * c->batch * c->kv_heads * c->capacity;
+  v.ranges[0] = range_of(c->codes, rows * (c->head_dim / 2));
+  v.ranges[1] = range_of(c->scales, rows * (c->head_dim / 32) * 2);
+  v.ranges[2] = range_of(c->zps, rows * (c->head_dim / 64));
+  v.nranges = 3;
+  for (int i = 0; i < 3; ++i)
+    for (int j = i + 1; j < 3; ++j)
+      if (overlaps(v.ranges[i], v.ranges[j])) return OL_ERR_ALIAS;
+  return OL_OK;
+}
+
+ol_status view_of(int layout, const void* desc, CacheView& v) {
+  switch (layout) {
+    case OL_LAYOUT_CONTIGUOUS:
+      return view_contiguous(static_cast<const ol_kv_cache*>(desc), v);
+    case OL_LAYOUT_PAGED:
+      return view_paged(static_cast<const ol_paged_kv*>(desc), v);
+    case OL_LAYOUT_INT4:
+      return view_int4(static_cast<const ol_int4_kv*>(desc), v);
+    default:
+      return OL_ERR_UNSUPPORTED;
+  }
+}
+
+// The buffer must not overlap any cache storage range.
+ol_status no_overlap(const CacheView& v, const void* p, size_t bytes) {
+  if (!p || bytes == 0) return OL_OK;
+  Range r = range_of(p, bytes);
+  for (int i = 0; i < v.nranges; ++i)
+    if (overlaps(r, v.ranges[i])) return OL_ERR_ALIAS;
+  return OL_OK;
+}
+
+ol_status writable(const CacheView& v, const void* updated) {
+  if (!updated) return OL_ERR_NULL;
+  if (updated != v.alias_ptr) return OL_ERR_ALIAS;
+  if (v.access != OL_READ_WRITE) return OL_ERR_READONLY;
+  return OL_OK;
+}
+
+// Paged validation: every page a row reads or writes is inside the pool; a
+// page that a row appends into is referenced by no other row.
+ol_status check_pages(const ol_paged_kv* c, const int32_t* lens_or_pos, int new_len, bool append,
+                      int window) {
+  const int S = c->page_size;
+  std::vector<int> first_row(append ? c->num_pages : 0, -1);
+  std::vector<char> shared(append ? c->num_pages : 0, 0);
+  for (int b = 0; b < c->batch; ++b) {
+    int lo, hi;
+    if (append) {  // history [0, p) is read, [p, p + new_len) written
+      lo = 0;
+      hi = lens_or_pos[b] + new_len;
+    } else {
+      RowSplit rs = row_split(lens_or_pos[b], window, 1);
+      lo = rs.lo;
+      hi = rs.hi;
+    }
+    if (hi <= lo) continue;
+    for (int pg = lo / S; pg <= (hi - 1) / S; ++pg) {
+      int page = c->block_table_host[(size_t)b * c->max_pages + pg];
+      if (page < 0 || page >= c->num_pages) return OL_ERR_PAGE;
+      if (append) {
+        if (first_row[page] == -1)
+          first_row[page] = b;
+        else if (first_row[page] != b)
+          shared[page] = 1;
+      }
+    }
+  }
+  if (append)
+    for (int b = 0; b < c->batch; ++b) {
+      int p0 = lens_or_pos[b];
+      for (int t = p0; t < p0 + new_len; ++t)
+        if (shared[c->block_table_host[(size_t)b * c->max_pages + t / S]]) return OL_ERR_PAGE;
+    }
+  return OL_OK;
+}
+
+AttnParams base_params(const CacheView& v, int layout, const void* desc) {
+  AttnParams p = {};
+  p.layout = layout;
+  p.dtype = v.dtype;
+  p.batch = v.batch;
+  p.kv_heads = v.kv_heads;
+  p.head_dim = v.head_dim;
+  p.capacity = v.capacity;
+  if (layout == OL_LAYOUT_CONTIGUOUS) {
+    p.cache = static_cast<const ol_kv_cache*>(desc)->data;
+  } else if (layout == OL_LAYOUT_PAGED) {
+    const ol_paged_kv* c = static_cast<const ol_paged_kv*>(desc);
+    p.pool = c->data;
+    p.block_table = c->block_table;
+    p.num_pages = c->num_pages;
+    p.page_size = c->page_size;
+    p.max_pages = c->max_pages;
+  } else {
+    const ol_int4_kv* c = static_cast<const ol_int4_kv*>(desc);
+    p.codes = c->codes;
+    p.scales = c->scales;
+    p.zps = c->zps;
+    p.quant_mode = c->quant_mode;
+    p.fixed_scale = c->fixed_scale;
+    p.fixed_zp = c->fixed_zp;
+  }
+  return p;
+}
+
+// Shared path of every attention-bearing call.
+ol_status run_attention(int layout, const void* desc, const CacheView& v, const void* q, int q_heads,
+                        const int32_t* lens_host, const int32_t* lens_dev, const void* new_kv, int append,
+                        int cur_from_new, float scale, int window, void* out, int out_dtype, void* workspace,
+                        size_t ws_bytes, cudaStream_t stream) {
+  if (!q || !lens_host || !lens_dev || !out || !workspace) return OL_ERR_NULL;
+  if (q_heads <= 0 || q_heads % v.kv_heads != 0) return OL_ERR_SHAPE;
+  if (v.head_dim > 256) return OL_ERR_UNSUPPORTED;
+  if (!valid_dtype(out_dtype)) return OL_ERR_DTYPE;
+  if (!aligned16(q) || !aligned16(lens_dev) || !aligned16(out) || !aligned16(workspace) ||
+      (new_kv && !aligned16(new_kv)))
+    return OL_ERR_ALIGN;
+  const int D = v.head_dim;
+  for (int b = 0; b < v.batch; ++b) {
+    if (lens_host[b] < (append ? 1 : 0) || lens_host[b] > v.capacity) return OL_ERR_CAPACITY;
+  }
+  const size_t in_elt = v.layout == OL_LAYOUT_INT4 ? 2 : elt_bytes(v.dtype);
+  const size_t q_bytes = (size_t)v.batch * q_heads * D * in_elt;
+  const size_t out_bytes = (size_t)v.batch * q_heads * D * elt_bytes(out_dtype);
+  const size_t kv_bytes = 2ull * v.batch * v.kv_heads * D * in_elt;
+  const size_t need = workspace_bytes(v.batch, q_heads, v.kv_heads, D);
+  if (ws_bytes < need) return OL_ERR_WORKSPACE;
+  ol_status st;
+  if ((st = no_overlap(v, q, q_bytes)) != OL_OK) return st;
+  if ((st = no_overlap(v, out, out_bytes)) != OL_OK) return st;
+  if ((st = no_overlap(v, new_kv, kv_bytes)) != OL_OK) return st;
+  if ((st = no_overlap(v, workspace, need)) != OL_OK) return st;
+  if ((st = no_overlap(v, lens_dev, sizeof(int32_t) * v.batch)) != OL_OK) return st;
+  if (overlaps(range_of(out, out_bytes), range_of(q, q_bytes)) ||
+      overlaps(range_of(out, out_bytes), range_of(workspace, need)) ||
+      (new_kv && overlaps(range_of(out, out_bytes), range_of(new_kv, kv_bytes))))
+    return OL_ERR_ALIAS;
+  if (layout == OL_LAYOUT_PAGED) {
+    const ol_paged_kv* c = static_cast<const ol_paged_kv*>(desc);
+    if ((st = no_overlap(v, c->block_table, sizeof(int32_t) * (size_t)c->batch * c->max_pages)) != OL_OK) return st;
+    if (append) {
+      std::vector<int32_t> pos(v.batch);
+      for (int b = 0; b < v.batch; ++b) pos[b] = lens_host[b] - 1;
+      if ((st = check_pages(c, pos.data(), 1, true, window)) != OL_OK) return st;
+    } else if ((st = check_pages(c, lens_host, 0, false, window)) != OL_OK) {
+      return st;
+    }
+  }
+  if ((st = check_owner(v.ranges, v.nranges, v.owner)) != OL_OK) return st;
+  if (fault_injected()) return OL_ERR_INJECTED;
+
+  AttnParams p = base_params(v, layout, desc);
+  p.q_heads = q_heads;
+  p.group = q_heads / v.kv_heads;
+  p.q = q;
+  p.lens = lens_dev;
+  p.new_kv = new_kv;
+  p.append = append;
+  p.cur_from_new = cur_from_new;
+  p.scale = scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
+  p.scale_log2 = p.scale * 1.4426950408889634f;
+  p.window = window < 0 ? -1 : window;
+  p.out = out;
+  p.out_dtype = out_dtype;
+  char* ws = static_cast<char*>(workspace);
+  p.status = reinterpret_cast<int32_t*>(ws);
+  p.counters = reinterpret_cast<uint32_t*>(ws + kStatusBytes);
+  p.partials = reinterpret_cast<float*>(ws + partials_offset(v.batch, v.kv_heads));
+
+  const int sms = sm_count_cached();
+  cudaError_t e;
+  if (layout != OL_LAYOUT_INT4 && fast_bf16_supported(p)) {
+    plan_fast(p, lens_host, sms);
+    e = launch_fast_bf16(p, stream);
+  } else if (layout == OL_LAYOUT_INT4 && fast_int4_supported(p)) {
+    plan_splits(p, lens_host, (long long)sms * 2 * tune().waves, 1);
+    e = launch_fast_int4(p, stream);
+  } else {
+    plan_splits(p, lens_host, (long long)sms * 4, 1);
+    p.variant = 0;
+    e = launch_generic_attention(p, stream);
+  }
+  return e == cudaSuccess ? OL_OK : OL_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace ol
+
+using namespace ol;
+
+extern "C" {
+
+const char* ol_status_string(ol_status s) {
+  switch (s) {
+    case OL_OK: return "OL_OK";
+    case OL_ERR_NULL: return "OL_ERR_NULL: a required pointer is NULL";
+    case OL_ERR_ALIAS: return "OL_ERR_ALIAS: updated pointer differs from the cache, or a buffer overlaps the cache";
+    case OL_ERR_READONLY: return "OL_ERR_READONLY: the cache descriptor is read-only";
+    case OL_ERR_CAPACITY: return "OL_ERR_CAPACITY: position + length exceeds the cache capacity";
+    case OL_ERR_SHAPE: return "OL_ERR_SHAPE: inconsistent or invalid sizes";
+    case OL_ERR_DTYPE: return "OL_ERR_DTYPE: unsupported dtype";
+    case OL_ERR_BUSY: return "OL_ERR_BUSY: the cache is bound by another owner";
+    case OL_ERR_WORKSPACE: return "OL_ERR_WORKSPACE: workspace missing or too small";
+    case OL_ERR_CUDA: return "OL_ERR_CUDA: a CUDA call failed";
+    case OL_ERR_UNSUPPORTED: return "OL_ERR_UNSUPPORTED: not implemented for these sizes";
+    case OL_ERR_INJECTED: return "OL_ERR_INJECTED: host fault injection after validation";
+    case OL_ERR_PAGE: return "OL_ERR_PAGE: invalid block-table entry or shared append page";
+    case OL_ERR_ALIGN: return "OL_ERR_ALIGN: device pointer not 16-byte aligned";
+  }
+  return "unknown ol_status";
+}
+
+int32_t ol_version(void) { return 100; }
+
+size_t ol_workspace_size(int32_t batch, int32_t q_heads, int32_t kv_heads, int32_t head_dim) {
+  if (batch < 0 || kv_heads <= 0 || q_heads <= 0 || q_heads % kv_heads != 0 || head_dim <= 0) return 0;
+  return workspace_bytes(batch, q_heads, kv_heads, head_dim);
+}
+
+ol_status ol_workspace_init(void* workspace, size_t ws_bytes, ol_stream stream) {
+  if (!workspace) return OL_ERR_NULL;
+  return cudaMemsetAsync(workspace, 0, ws_bytes, static_cast<cudaStream_t>(stream)) == cudaSuccess ? OL_OK
+                                                                                                    : OL_ERR_CUDA;
+}
+
+ol_status ol_workspace_status(void* workspace, int32_t* status_out, ol_stream stream) {
+  if (!workspace || !status_out) return OL_ERR_NULL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess) return OL_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return OL_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, sizeof v, s) != cudaSuccess) return OL_ERR_CUDA;
+  *status_out = v;
+  return OL_OK;
+}
+
+ol_status ol_cache_bind(const void* base, size_t bytes, uint64_t owner) {
+  if (!base || bytes == 0) return OL_ERR_NULL;
+  Range r = range_of(base, bytes);
+  std::lock_guard<std::mutex> lk(g_bind_mu);
+  for (const Binding& bd : g_bindings)
+    if (overlaps(r, Range{bd.lo, bd.hi}) && bd.owner != owner) return OL_ERR_BUSY;
+  for (Binding& bd : g_bindings)
+    if (bd.lo == r.lo && bd.owner == owner) {
+      bd.hi = r.hi > bd.hi ? r.hi : bd.hi;
+      return OL_OK;
+    }
+  g_bindings.push_back({r.lo, r.hi, owner});
+  return OL_OK;
+}
+
+ol_status ol_cache_unbind(const void* base, uint64_t owner) {
+  if (!base) return OL_ERR_NULL;
+  uintptr_t a = reinterpret_cast<uintptr_t>(base);
+  std::lock_guard<std::mutex> lk(g_bind_mu);
+  for (size_t i = 0; i < g_bindings.size(); ++i)
+    if (g_bindings[i].lo == a) {
+      if (g_bindings[i].owner != owner) return OL_ERR_BUSY;
+      g_bindings.erase(g_bindings.begin() + (long)i);
+      return OL_OK;
+    }
+  return OL_OK;
+}
+
+static ol_status append_common(const CacheView& v, const void* updated, const void* values, int32_t new_len,
+                               const int32_t* positions_host, const int32_t* positions_dev) {
+  ol_status st;
+  if ((st = writable(v, updated)) != OL_OK) return st;
+  if (!values || !positions_host || !positions_dev) return OL_ERR_NULL;
+  if (new_len < 0) return OL_ERR_SHAPE;
+  if (!aligned16(values) || !aligned16(positions_dev)) return OL_ERR_ALIGN;
+  for (int b = 0; b < v.batch; ++b)
+    if (positions_host[b] < 0 || (long long)positions_host[b] + new_len > v.capacity) return OL_ERR_CAPACITY;
+  const size_t in_elt = v.layout == OL_LAYOUT_INT4 ? 2 : elt_bytes(v.dtype);
+  if ((st = no_overlap(v, values, 2ull * v.batch * v.kv_heads * new_len * v.head_dim * in_elt)) != OL_OK) return st;
+  if ((st = no_overlap(v, positions_dev, sizeof(int32_t) * v.batch)) != OL_OK) return st;
+  return OL_OK;
+}
+
+static ol_status launch_append_view(const CacheView& v, int layout, const void* desc, const void* values,
+                                    int32_t new_len, const int32_t* positions_dev, cudaStream_t s) {
+  AppendParams p = {};
+  p.layout = layout;
+  p.dtype = v.dtype;
+  p.batch = v.batch;
+  p.kv_heads = v.kv_heads;
+  p.head_dim = v.head_dim;
+  p.capacity = v.capacity;
+  p.new_len = new_len;
+  p.values = values;
+  p.positions = positions_dev;
+  if (layout == OL_LAYOUT_CONTIGUOUS) {
+    p.cache = static_cast<const ol_kv_cache*>(desc)->data;
+  } else if (layout == OL_LAYOUT_PAGED) {
+    const ol_paged_kv* c = static_cast<const ol_paged_kv*>(desc);
+    p.pool = c->data;
+    p.block_table = c->block_table;
+    p.num_pages = c->num_pages;
+    p.page_size = c->page_size;
+    p.max_pages = c->max_pages;
+  } else {
+    const ol_int4_kv* c = static_cast<const ol_int4_kv*>(desc);
+    p.codes = c->codes;
+    p.scales = c->scales;
+    p.zps = c->zps;
+    p.quant_mode = c->quant_mode;
+    p.fixed_scale = c->fixed_scale;
+    p.fixed_zp = c->fixed_zp;
+  }
+  return launch_append(p, s) == cudaSuccess ? OL_OK : OL_ERR_CUDA;
+}
+
+ol_status ol_cache_update_rows(const ol_kv_cache* cache, void* updated_cache, const void* values, int32_t new_len,
+                               const int32_t* positions_host, const int32_t* positions_dev, ol_stream stream) {
+  CacheView v;
+  ol_status st = view_contiguous(cache, v);
+  if (st != OL_OK) return st;
+  if ((st = append_common(v, updated_cache, values, new_len, positions_host, positions_dev)) != OL_OK) return st;
+  if ((st = check_owner(v.ranges, v.nranges, v.owner)) != OL_OK) return st;
+  if (fault_injected()) return OL_ERR_INJECTED;
+  return launch_append_view(v, OL_LAYOUT_CONTIGUOUS, cache, values, new_len, positions_dev,
+                            static_cast<cudaStream_t>(stream));
+}
+
+ol_status ol_cache_update(const ol_kv_cache* cache, void* updated_cache, const void* values, int32_t new_len,
+                          int64_t position, ol_stream stream) {
+  // One position for every row (the INT64 scalar of CacheUpdate), passed by value.
+  CacheView v;
+  ol_status st = view_contiguous(cache, v);
+  if (st != OL_OK) return st;
+  if (position < 0 || position > (int64_t)v.capacity) return OL_ERR_CAPACITY;
+  if ((st = writable(v, updated_cache)) != OL_OK) return st;
+  if (!values) return OL_ERR_NULL;
+  if (new_len < 0) return OL_ERR_SHAPE;
+  if (!aligned16(values)) return OL_ERR_ALIGN;
+  if (position + new_len > (int64_t)v.capacity) return OL_ERR_CAPACITY;
+  if ((st = no_overlap(v, values, 2ull * v.batch * v.kv_heads * new_len * v.head_dim * elt_bytes(v.dtype))) != OL_OK)
+    return st;
+  if ((st = check_owner(v.ranges, v.nranges, v.owner)) != OL_OK) return st;
+  if (fault_injected()) return OL_ERR_INJECTED;
+  AppendParams p = {};
+  p.layout = OL_LAYOUT_CONTIGUOUS;
+  p.dtype = v.dtype;
+  p.batch = v.batch;
+  p.kv_heads = v.kv_heads;
+  p.head_dim = v.head_dim;
+  p.capacity = v.capacity;
+  p.new_len = new_len;
+  p.values = values;
+  p.positions = nullptr;
+  p.cache = cache->data;
+  p.scalar_position = static_cast<int32_t>(position);
+  return launch_append(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? OL_OK : OL_ERR_CUDA;
+}
+
+ol_status ol_paged_cache_update(const ol_paged_kv* kv, void* updated_pool, const void* values, int32_t new_len,
+                                const int32_t* positions_host, const int32_t* positions_dev, ol_stream stream) {
+  CacheView v;
+  ol_status st = view_paged(kv, v);
+  if (st != OL_OK) return st;
+  if ((st = append_common(v, updated_pool, values, new_len, positions_host, positions_dev)) != OL_OK) return st;
+  if ((st = no_overlap(v, kv->block_table, sizeof(int32_t) * (size_t)kv->batch * kv->max_pages)) != OL_OK) return st;
+  if ((st = check_pages(kv, positions_host, new_len, true, -1)) != OL_OK) return st;
+  if ((st = check_owner(v.ranges, v.nranges, v.owner)) != OL_OK) return st;
+  if (fault_injected()) return OL_ERR_INJECTED;
+  return launch_append_view(v, OL_LAYOUT_PAGED, kv, values, new_len, positions_dev, static_cast<cudaStream_t>(stream));
+}
+
+ol_status ol_int4kv_append(const ol_int4_kv* cache, void* updated_codes, const void* values_bf16,
+                           const int32_t* positions_host, const int32_t* positions_dev, ol_stream stream) {
+  CacheView v;
+  ol_status st = view_int4(cache, v);
+  if (st != OL_OK) return st;
+  if ((st = append_common(v, updated_codes, values_bf16, 1, positions_host, positions_dev)) != OL_OK) return st;
+  if ((st = check_owner(v.ranges, v.nranges, v.owner)) != OL_OK) return st;
+  if (fault_injected()) return OL_ERR_INJECTED;
+  return launch_append_view(v, OL_LAYOUT_INT4, cache, values_bf16, 1, positions_dev, static_cast<cudaStream_t>(stream));
+}
+
+ol_status ol_decode_attention(const ol_kv_cache* cache, const void* q, int32_t q_heads, const int32_t* lens_host,
+                              const int32_t* lens_dev, float scale, int32_t window, void* out, int32_t out_dtype,
+                              void* workspace, size_t ws_bytes, ol_stream stream) {
+  CacheView v;
+  ol_status st = view_contiguous(cache, v);
+  if (st != OL_OK) return st;
+  return run_attention(OL_LAYOUT_CONTIGUOUS, cache, v, q, q_heads, lens_host, lens_dev, nullptr, 0, 0, scale, window,
+                       out, out_dtype, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+ol_status ol_paged_decode_attention(const ol_paged_kv* kv, const void* q, int32_t q_heads, const int32_t* lens_host,
+                                    const int32_t* lens_dev, float scale, int32_t window, void* out,
+                                    int32_t out_dtype, void* workspace, size_t ws_bytes, ol_stream stream) {
+  CacheView v;
+  ol_status st = view_paged(kv, v);
+  if (st != OL_OK) return st;
+  return run_attention(OL_LAYOUT_PAGED, kv, v, q, q_heads, lens_host, lens_dev, nullptr, 0, 0, scale, window, out,
+                       out_dtype, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+ol_status ol_int4kv_decode_attention(const ol_int4_kv* cache, const void* q, int32_t q_heads,
+                                     const int32_t* lens_host, const int32_t* lens_dev, const void* cur_kv,
+                                     float scale, int32_t window, void* out, int32_t out_dtype, void* workspace,
+                                     size_t ws_bytes, ol_stream stream) {
+  CacheView v;
+  ol_status st = view_int4(cache, v);
+  if (st != OL_OK) return st;
+  if (cur_kv && lens_host)
+    for (int b = 0; b < v.batch; ++b)
+      if (lens_host[b] < 1) return OL_ERR_CAPACITY;
+  return run_attention(OL_LAYOUT_INT4, cache, v, q, q_heads, lens_host, lens_dev, cur_kv, 0, cur_kv ? 1 : 0, scale,
+                       window, out, out_dtype, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+ol_status ol_decode_step(int32_t layout, const void* cache_desc, void* updated, const void* q, int32_t q_heads,
+                         const void* new_kv, const int32_t* lens_host, const int32_t* lens_dev, float scale,
+                         int32_t window, void* out, int32_t out_dtype, void* workspace, size_t ws_bytes,
+                         ol_stream stream) {
+  CacheView v;
+  ol_status st = view_of(layout, cache_desc, v);
+  if (st != OL_OK) return st;
+  if ((st = writable(v, updated)) != OL_OK) return st;
+  if (!new_kv) return OL_ERR_NULL;
+  return run_attention(layout, cache_desc, v, q, q_heads, lens_host, lens_dev, new_kv, 1, 1, scale, window, out,
+                       out_dtype, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,398 @@
+// ol_common.cuh -- device helpers shared by the decode-step kernels:
+// inline-PTX wrappers (mbarrier, bulk/tensor copies, ldmatrix, mma.sync,
+// movmatrix, programmatic dependent launch), bf16/fp16 bit helpers, the
+// CTA -> (row, kv head, split) mapping and the split-K merge.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "ol_internal.h"
+
+namespace ol {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr long long kWaitLimitCycles = 4000000000LL;  // ~2 s at 2 GHz: bounded spin on mbarriers
+
+// ------------------------------------------------------------------ PTX
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: returns false (and the caller records a device status) if the
+// phase did not complete within kWaitLimitCycles.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  }
+  return true;
+}
+
+// 2D tiled tensor copy global -> shared, completion on an mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+// Contiguous bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                              uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// D = A(16x16, row) * B(16x8, col) + D, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ------------------------------------------------------------ bit helpers
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t h) {
+  return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
+  __nv_bfloat16 b = __float2bfloat16_rn(f);
+  return *reinterpret_cast<uint16_t*>(&b);
+}
+__device__ __forceinline__ float fp16_bits_to_float(uint16_t h) {
+  return __half2float(__ushort_as_half(h));
+}
+
+__device__ __forceinline__ void set_status(int32_t* status, int32_t v) {
+  if (status) atomicOr(reinterpret_cast<int*>(status), v);
+}
+
+// --------------------------------------------------------- CTA -> work map
+
+// The work of one CTA: kv head g of row b, split s of nsplit; the tokens of
+// the split's 16-token tiles (see row_split) clipped to the visible range
+// [lo, hi); t_begin is a multiple of 16. A split may be empty when a short
+// row's split count was rounded up to a whole cluster.
+struct Work {
+  int b, g, s, nsplit;
+  int lo, hi;            // visible range of the row
+  int t_begin, t_end;    // token range of this split (t_begin a multiple of 16)
+  int first_cta;         // CTA index of split 0 of (b, g)
+  int valid;
+};
+
+// Computed by one full warp; every lane returns the same Work.
+__device__ __forceinline__ Work map_cta_warp(const int32_t* __restrict__ lens, int batch, int kv_heads,
+                                             int capacity, int window, int chunk, int cta,
+                                             int32_t* status, int cluster = 1) {
+  const int lane = threadIdx.x & 31;
+  Work w;
+  w.valid = 0;
+  w.b = w.g = w.s = 0;
+  w.nsplit = 1;
+  w.lo = w.hi = w.t_begin = w.t_end = 0;
+  w.first_cta = 0;
+  int running = 0;
+  for (int base = 0; base < batch; base += 32) {
+    int b = base + lane;
+    int n = 0;
+    if (b < batch) {
+      n = lens[b];
+      if (n < 0 || n > capacity) {
+        set_status(status, OL_DEVICE_GUARD);
+        n = n < 0 ? 0 : capacity;
+      }
+    }
+    RowSplit rs = row_split(n, window, chunk, cluster);
+    int cnt = (b < batch) ? rs.nsplit * kv_heads : 0;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (cta < running + total) {
+      int excl = incl - cnt;
+      unsigned hit = __ballot_sync(0xffffffffu, cnt > 0 && cta >= running + excl && cta < running + incl);
+      int src = __ffs(hit) - 1;
+      int within = cta - running - __shfl_sync(0xffffffffu, excl, src);
+      w.b = base + src;
+      w.nsplit = __shfl_sync(0xffffffffu, rs.nsplit, src);
+      w.lo = __shfl_sync(0xffffffffu, rs.lo, src);
+      w.hi = __shfl_sync(0xffffffffu, rs.hi, src);
+      int start = __shfl_sync(0xffffffffu, rs.start, src);
+      int ntiles = __shfl_sync(0xffffffffu, rs.ntiles, src);
+      w.g = within / w.nsplit;
+      w.s = within % w.nsplit;
+      w.t_begin = min(start + 16 * split_tile(w.s, ntiles, w.nsplit), w.hi);
+      w.t_end = min(start + 16 * split_tile(w.s + 1, ntiles, w.nsplit), w.hi);
+      w.first_cta = cta - w.s;
+      w.valid = 1;
+      return w;
+    }
+    running += total;
+  }
+  set_status(status, OL_DEVICE_GUARD);  // grid larger than the device-side plan
+  return w;
+}
+
+// -------------------------------------------------------- output + merge
+
+__device__ __forceinline__ void store_out(void* out, int out_dtype, size_t idx, float v) {
+  if (out_dtype == OL_F32)
+    reinterpret_cast<float*>(out)[idx] = v;
+  else
+    reinterpret_cast<uint16_t*>(out)[idx] = float_to_bf16_bits(v);
+}
+
+// Split-K completion. A CTA holds, in shared memory, its merged state for the
+// query heads [h0, h1) of its group and the dimensions [d0, d1):
+// m[jl] (log2 domain), l[jl], o[jl * o_stride + (d - d0)] with jl = j - h0.
+// Its result goes to partial slot `slot` of the `nslots` slots of (row, kv
+// head), which start at `first_slot`. With one slot the CTA writes
+// y = o / l directly; otherwise it stores the partial, takes a ticket, and the
+// last of the `arrivals` CTAs of (row, kv head) merges all slots:
+//   M = max_s m_s, L = sum_s l_s 2^(m_s - M), y = sum_s o_s 2^(m_s - M) / L.
+// The merge first reduces (M, L) per head (one warp per head, lanes over the
+// slots), then each output element reads its slots with independent loads.
+// `scratch` is shared memory for 2 * group floats.
+// Block-wide: every thread of the CTA must call it.
+__device__ __forceinline__ void finish_split(const AttnParams& p, const Work& w, const float* sm_m,
+                                             const float* sm_l, const float* sm_o, int o_stride, int h0,
+                                             int h1, int d0, int d1, int slot, int first_slot, int nslots,
+                                             int arrivals, int* sm_flag, float* scratch) {
+  const int D = p.head_dim;
+  const int G = p.group;
+  const int tid = threadIdx.x;
+  const int nthreads = blockDim.x;
+  const int nh = h1 - h0, nd = d1 - d0;
+  const size_t out_base = ((size_t)w.b * p.q_heads + (size_t)w.g * G) * D;
+  if (nslots == 1) {
+    for (int i = tid; i < nh * nd; i += nthreads) {
+      const int jl = i / nd, d = d0 + i % nd;
+      const float l = sm_l[jl];
+      const float y = l > 0.f ? sm_o[jl * o_stride + (d - d0)] / l : 0.f;
+      store_out(p.out, p.out_dtype, out_base + (size_t)(h0 + jl) * D + d, y);
+    }
+    return;
+  }
+  float* sl = p.partials + (size_t)slot * G * (D + 2);
+  for (int i = tid; i < nh * (nd + 2); i += nthreads) {
+    const int jl = i / (nd + 2), e = i % (nd + 2);
+    if (e < 2) {
+      if (d0 == 0) sl[(size_t)(h0 + jl) * (D + 2) + e] = e == 0 ? sm_m[jl] : sm_l[jl];
+    } else {
+      sl[(size_t)(h0 + jl) * (D + 2) + 2 + d0 + (e - 2)] = sm_o[jl * o_stride + (e - 2)];
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    unsigned* ctr = p.counters + (size_t)w.b * p.kv_heads + w.g;
+    const unsigned prev = atomicAdd(ctr, 1u);
+    const int last = (prev == (unsigned)(arrivals - 1));
+    if (last) atomicExch(ctr, 0u);  // leave the ticket at zero for the next call
+    *sm_flag = last;
+  }
+  __syncthreads();
+  if (!*sm_flag) return;
+  __threadfence();
+  const float* base = p.partials + (size_t)first_slot * G * (D + 2);
+  const size_t stride = (size_t)G * (D + 2);
+  const int warp = tid >> 5, lane = tid & 31, nwarps = nthreads >> 5;
+  for (int j = warp; j < G; j += nwarps) {
+    float M = -INFINITY;
+    for (int s = lane; s < nslots; s += 32) M = fmaxf(M, __ldcg(base + s * stride + (size_t)j * (D + 2)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float L = 0.f;
+    if (M != -INFINITY)
+      for (int s = lane; s < nslots; s += 32) {
+        const float* ps = base + s * stride + (size_t)j * (D + 2);
+        const float ms = __ldcg(ps);
+        L += ms == -INFINITY ? 0.f : __ldcg(ps + 1) * fast_exp2(ms - M);
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (lane == 0) {
+      scratch[2 * j] = M;
+      scratch[2 * j + 1] = L;
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < G * D; i += nthreads) {
+    const int j = i / D, d = i % D;
+    const float M = scratch[2 * j], L = scratch[2 * j + 1];
+    float acc = 0.f;
+    if (M != -INFINITY) {
+      const float* pj = base + (size_t)j * (D + 2);
+#pragma unroll 8
+      for (int s = 0; s < nslots; ++s) {
+        const float ms = __ldcg(pj + s * stride);
+        const float ov = __ldcg(pj + s * stride + 2 + d);
+        acc += ms == -INFINITY ? 0.f : ov * fast_exp2(ms - M);
+      }
+    }
+    store_out(p.out, p.out_dtype, out_base + (size_t)j * D + d, L > 0.f ? acc / L : 0.f);
+  }
+}
+
+// ------------------------------------------------------- thread-block clusters
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory variable in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t map_shared_rank(uint32_t local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+  return remote;
+}
+__device__ __forceinline__ float ld_shared_cluster(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// ----------------------------------------------------- INT4 quantization
+
+// Quantize one token's D bf16 values (D a multiple of 32) into one INT4 row:
+// per block of 32, fp16 scale and uint4 zero point (dynamic min-max or fixed
+// parameters), code = sat[0,15](round_half_even(x / scale) + zp) in IEEE fp32.
+// Executed by one full warp; lane i handles element i of each block.
+__device__ __forceinline__ void int4_quantize_row_warp(const uint16_t* __restrict__ x, int D, int mode,
+                                                       float fixed_scale, int fixed_zp,
+                                                       uint8_t* __restrict__ codes_row,
+                                                       uint16_t* __restrict__ scales_row,
+                                                       uint8_t* __restrict__ zps_row) {
+  const int lane = threadIdx.x & 31;
+  const int nb = D / 32;
+  uint32_t zp_acc = 0;  // lane 0 collects the packed zero points
+  for (int blk = 0; blk < nb; ++blk) {
+    float v = bf16_bits_to_float(x[blk * 32 + lane]);
+    float s;
+    int zp;
+    uint16_t sbits;
+    if (mode == OL_Q_FIXED) {
+      sbits = __half_as_ushort(__float2half_rn(fixed_scale));
+      s = fp16_bits_to_float(sbits);
+      zp = fixed_zp;
+    } else {
+      float lo = fminf(v, 0.f), hi = fmaxf(v, 0.f);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+      }
+      float s32 = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
+      sbits = __half_as_ushort(__float2half_rn(s32));
+      s = fp16_bits_to_float(sbits);
+      if (s == 0.f) {
+        sbits = __half_as_ushort(__float2half_rn(1.0f));
+        s = 1.0f;
+      }
+      float z = rintf(__fdiv_rn(-lo, s));
+      z = fminf(fmaxf(z, 0.f), 15.f);
+      zp = static_cast<int>(z);
+    }
+    float r = __fadd_rn(rintf(__fdiv_rn(v, s)), static_cast<float>(zp));
+    r = fminf(fmaxf(r, 0.f), 15.f);
+    uint32_t code = static_cast<uint32_t>(r);
+    uint32_t hi_code = __shfl_down_sync(0xffffffffu, code, 1);
+    if ((lane & 1) == 0) codes_row[blk * 16 + lane / 2] = static_cast<uint8_t>(code | (hi_code << 4));
+    if (lane == 0) {
+      scales_row[blk] = sbits;
+      zp_acc |= static_cast<uint32_t>(zp) << (4 * (blk & 1));
+      if ((blk & 1) == 1 || blk == nb - 1) {
+        zps_row[blk / 2] = static_cast<uint8_t>(zp_acc);
+        zp_acc = 0;
+      }
+    }
+  }
+}
+
+}  // namespace ol

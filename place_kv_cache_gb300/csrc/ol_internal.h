@@ -1,0 +1,151 @@
+// ol_internal.h -- parameter blocks passed from the host-side ABI layer
+// (ol_api.cpp) to the kernel launchers (*.cu). Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime_api.h>
+
+#include "../../include/ol.h"
+
+namespace ol {
+
+// Workspace layout (all offsets in bytes from the workspace base):
+//   [0, 256)                     int32 device status word (+ padding)
+//   [256, 256 + counters)        uint32 ticket counter per (row, kv head)
+//   [partials_off, ...)          float partial results, one slot per CTA and query head:
+//                                {m (log2 domain), l, o[head_dim]}
+constexpr size_t kStatusBytes = 256;
+constexpr int kMaxExtraSplits = 4096;  // CTAs beyond one per (row, kv head)
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline size_t counters_bytes(int batch, int kv_heads) {
+  return align_up(sizeof(uint32_t) * (size_t)batch * (size_t)kv_heads, 256);
+}
+inline size_t partials_offset(int batch, int kv_heads) {
+  return kStatusBytes + counters_bytes(batch, kv_heads);
+}
+inline size_t max_ctas(int batch, int kv_heads) {
+  return (size_t)batch * (size_t)kv_heads + kMaxExtraSplits;
+}
+inline size_t workspace_bytes(int batch, int q_heads, int kv_heads, int head_dim) {
+  int group = q_heads / kv_heads;
+  return partials_offset(batch, kv_heads) +
+         max_ctas(batch, kv_heads) * (size_t)group * (size_t)(head_dim + 2) * sizeof(float);
+}
+
+// One attention / decode-step launch, fully validated on the host.
+struct AttnParams {
+  int layout;      // ol_layout
+  int dtype;       // cache dtype (OL_F32 / OL_BF16; INT4 history with bf16 q)
+  int batch, q_heads, kv_heads, group, head_dim;
+  int capacity;    // tokens per row: C (contiguous / INT4) or max_pages * page_size (paged)
+
+  // contiguous cache [2, B, Hkv, C, D]
+  void* cache;
+  // paged pool [2, P, Hkv, S, D] and block table [B, M]
+  void* pool;
+  const int32_t* block_table;
+  int num_pages, page_size, max_pages;
+  // INT4 planes
+  uint8_t* codes;
+  uint16_t* scales;
+  uint8_t* zps;
+  int quant_mode;
+  float fixed_scale;
+  int fixed_zp;
+
+  const void* q;        // [B, Hq, D]
+  const int32_t* lens;  // device [B]
+  const void* new_kv;   // [2, B, Hkv, 1, D]: appended (fused step) and attended at lens-1
+  int append;           // 1: write new_kv into the cache at lens[b]-1 (fused step)
+  int cur_from_new;     // 1: the token at lens[b]-1 is taken from new_kv, not the cache
+  float scale;          // softmax scale
+  float scale_log2;     // scale * log2(e)
+  int window;           // < 0: unbounded
+  void* out;            // [B, Hq, D]
+  int out_dtype;
+
+  int32_t* status;      // device status word
+  uint32_t* counters;   // [B * Hkv]
+  float* partials;      // [max_ctas][G][D + 2]
+
+  // split plan (host computes it from lens_host; kernels recompute the mapping from lens)
+  int chunk;            // target tokens per split, a multiple of 16
+  int cluster;          // CTAs per thread-block cluster (1 = no cluster)
+  int variant;          // tensor-core kernel variant (warps x stages)
+  int total_ctas;
+};
+
+// Append-only launches (CacheUpdate, PagedCacheUpdate, INT4 append).
+struct AppendParams {
+  int layout;
+  int dtype;
+  int batch, kv_heads, head_dim, capacity, new_len;
+  void* cache;
+  void* pool;
+  const int32_t* block_table;
+  int num_pages, page_size, max_pages;
+  uint8_t* codes;
+  uint16_t* scales;
+  uint8_t* zps;
+  int quant_mode;
+  float fixed_scale;
+  int fixed_zp;
+  const void* values;        // [2, B, Hkv, new_len, D]
+  const int32_t* positions;  // device [B], or NULL: every row uses scalar_position
+  int scalar_position;
+};
+
+// Launchers (return cudaSuccess or the launch error).
+cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
+cudaError_t launch_generic_attention(const AttnParams& p, cudaStream_t s);
+// Tensor-core paths; return cudaErrorNotSupported when the shape is outside them.
+bool fast_bf16_supported(const AttnParams& p);
+int fast_bf16_smem(int variant);
+int fast_bf16_warps(int variant);
+int fast_bf16_max_cluster(int variant, bool paged);
+cudaError_t launch_fast_bf16(const AttnParams& p, cudaStream_t s);
+bool fast_int4_supported(const AttnParams& p);
+cudaError_t launch_fast_int4(const AttnParams& p, cudaStream_t s);
+
+// Visible range and split plan of one row, shared by the host planner and the
+// kernels. The tokens [start, hi) (start = lo rounded down to 16) form
+// ntiles 16-token tiles; they are cut into nsplit splits, split s taking tiles
+// [s * ntiles / nsplit, (s + 1) * ntiles / nsplit), so splits differ by at most
+// one tile. nsplit = ceil(tokens / chunk), rounded up to a multiple of
+// `cluster` so that a cluster never straddles two (row, kv head).
+struct RowSplit {
+  int lo, hi, start, ntiles, nsplit;
+};
+#if defined(__CUDACC__)
+__host__ __device__
+#endif
+inline RowSplit row_split(int n, int window, int chunk, int cluster = 1) {
+  RowSplit r;
+  if (n <= 0) {
+    r.lo = r.hi = r.start = r.ntiles = 0;
+    r.nsplit = cluster;
+    return r;
+  }
+  r.hi = n;
+  r.lo = window < 0 ? 0 : ((n - 1 - window) > 0 ? (n - 1 - window) : 0);
+  r.start = r.lo & ~15;
+  const int len = r.hi - r.start;
+  r.ntiles = (len + 15) / 16;
+  int ns = (len + chunk - 1) / chunk;
+  r.nsplit = (ns + cluster - 1) / cluster * cluster;
+  return r;
+}
+
+// First tile of split s (s in [0, nsplit]).
+#if defined(__CUDACC__)
+__host__ __device__
+#endif
+inline int split_tile(int s, int ntiles, int nsplit) {
+  return (int)(((long long)s * ntiles) / nsplit);
+}
+
+}  // namespace ol

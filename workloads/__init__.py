@@ -148,8 +148,10 @@ def make_case(w: Workload, *, lens: Optional[np.ndarray] = None, seed: Optional[
     """Draw one case. ``history_len_offset`` tokens of each row are left for the
     append (1 for a decode step); use 0 to get a history of ``lens[b]`` tokens."""
     rng = np.random.default_rng(w.seed if seed is None else seed)
-    drawn = draw_lens(rng, w)
-    lens = drawn if lens is None else np.asarray(lens, dtype=np.int32)
+    if lens is None:
+        lens = draw_lens(rng, w)       # explicit lengths skip this draw
+    else:
+        lens = np.asarray(lens, dtype=np.int32)
     perm = None
     if w.layout == "paged":
         perm = rng.permutation(w.num_pages).astype(np.int32)
