@@ -272,6 +272,34 @@ OL_API ol_status ol_decode_step(int32_t layout, const void* cache_desc, void* up
                          const int32_t* lens_dev, float scale, int32_t window, void* out,
                          int32_t out_dtype, void* workspace, size_t ws_bytes, ol_stream stream);
 
+/*
+ * The fused decode step with no allocation by anyone: no workspace argument.
+ * The paper has no counterpart; it exists for callers that cannot call
+ * cudaMalloc -- code running inside a host engine that owns all device memory
+ * and forbids allocation while it executes (an inference-engine plugin's
+ * enqueue, a fixed-arena runtime), or a latency-critical decode loop that
+ * cannot afford an allocation's implicit synchronization.
+ *
+ * Its scratch (split-K partials, ticket counters, status word) is one
+ * file-scope device array of OL_NOALLOC_SCRATCH_BYTES inside this library;
+ * every GPU that loads the library holds it until the process exits. The
+ * first call on a device looks up that array's device address (with the
+ * device current); make that first call before any stream capture. Every call
+ * clears the counters and status word on `stream` (cudaMemsetAsync of the
+ * array itself, no allocation) and then runs ol_decode_step with the array as
+ * its workspace. Requests whose worst-case workspace,
+ * ol_workspace_size(batch, q_heads, kv_heads, head_dim), exceeds
+ * OL_NOALLOC_SCRATCH_BYTES are rejected with OL_ERR_WORKSPACE before anything
+ * runs. All calls share the one array: calls that overlap on the GPU (on
+ * different streams, or from different threads) race on it and must not be
+ * issued. Arguments and errors are otherwise those of ol_decode_step.
+ */
+#define OL_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+OL_API ol_status ol_decode_step_noalloc(int32_t layout, const void* cache_desc, void* updated, const void* q,
+                                        int32_t q_heads, const void* new_kv, const int32_t* lens_host,
+                                        const int32_t* lens_dev, float scale, int32_t window, void* out,
+                                        int32_t out_dtype, ol_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -30,7 +30,7 @@ OL_DEVICE_OK, OL_DEVICE_GUARD = 0, 1
 SYMBOLS = ("ol_status_string", "ol_version", "ol_workspace_size", "ol_workspace_init", "ol_workspace_status",
            "ol_cache_bind", "ol_cache_unbind", "ol_cache_update", "ol_cache_update_rows",
            "ol_paged_cache_update", "ol_decode_attention", "ol_paged_decode_attention", "ol_int4kv_append",
-           "ol_int4kv_decode_attention", "ol_decode_step")
+           "ol_int4kv_decode_attention", "ol_decode_step", "ol_decode_step_noalloc")
 
 
 class OlError(RuntimeError):
@@ -100,6 +100,7 @@ def load(build_if_missing: bool = True):
         "ol_int4kv_decode_attention": (st, [ctypes.POINTER(Int4KV), vp, i32, vp, vp, vp, f32, i32, vp, i32, vp, sz,
                                             vp]),
         "ol_decode_step": (st, [i32, vp, vp, vp, i32, vp, vp, vp, f32, i32, vp, i32, vp, sz, vp]),
+        "ol_decode_step_noalloc": (st, [i32, vp, vp, vp, i32, vp, vp, vp, f32, i32, vp, i32, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -292,3 +293,13 @@ def ol_decode_step(layout: int, desc, updated, q, q_heads: int, new_kv, lens_hos
     _check(load().ol_decode_step(layout, ctypes.byref(desc), _ptr(updated), _ptr(q), q_heads, _ptr(new_kv), _ptr(lh),
                                  _ptr(lens_dev), scale, window, _ptr(out), out_dtype, _ptr(workspace), ws_bytes,
                                  _stream(stream)), "ol_decode_step")
+
+
+def ol_decode_step_noalloc(layout: int, desc, updated, q, q_heads: int, new_kv, lens_host, lens_dev, scale: float,
+                           window: int, out, out_dtype: int, stream=None):
+    """ol_decode_step without a workspace argument, for callers that cannot
+    allocate: the library's own static device scratch serves as workspace."""
+    lh = _host_i32(lens_host)
+    _check(load().ol_decode_step_noalloc(layout, ctypes.byref(desc), _ptr(updated), _ptr(q), q_heads, _ptr(new_kv),
+                                         _ptr(lh), _ptr(lens_dev), scale, window, _ptr(out), out_dtype,
+                                         _stream(stream)), "ol_decode_step_noalloc")
