@@ -166,10 +166,15 @@ class Setup:
         # check its values against the oracle
         from workloads import draw_lens
         self.lens = draw_lens(rng, w)
-        self.lens_d = torch.from_numpy(self.lens).to(dev)
+        # a chained workload advances every row by one token per step (append at
+        # lens - 1, lens + 1 next step); the others repeat the same step shape
+        self.chain = w.steps if w.steps > 1 else 1
+        self.lens_list = [self.lens + i for i in range(self.chain)]
+        self.lens_d_list = [torch.from_numpy(l).to(dev) for l in self.lens_list]
+        self.lens_d = self.lens_d_list[0]
         D = w.head_dim
         B, H = w.batch, w.kv_heads
-        self.bytes_per_step = step_bytes(w, self.lens)
+        self.bytes_per_step = float(np.mean([step_bytes(w, l) for l in self.lens_list]))
         self.q = torch.randn((B, w.q_heads, D), generator=gen, device=dev).to(torch.bfloat16)
         self.new_kv = torch.randn((2, B, H, 1, D), generator=gen, device=dev).to(torch.bfloat16)
         self.out = torch.empty((B, w.q_heads, D), dtype=torch.bfloat16, device=dev)
@@ -232,10 +237,12 @@ class Setup:
             self.updated.append(codes)
             self.layout = ol.OL_LAYOUT_INT4
 
-    def step(self, r, stream=None):
+    def step(self, i, stream=None):
+        """Step i of the rotation: replica i % replicas, chain position i % chain."""
+        r, c = i % self.replicas, i % self.chain
         self.ol.ol_decode_step(self.layout, self.descs[r], self.updated[r], self.q, self.w.q_heads, self.new_kv,
-                               self.lens, self.lens_d, 0.0, -1, self.out, self.ol.OL_BF16, self.ws, self.ws_bytes,
-                               stream=stream)
+                               self.lens_list[c], self.lens_d_list[c], 0.0, -1, self.out, self.ol.OL_BF16, self.ws,
+                               self.ws_bytes, stream=stream)
 
 
 def run_ours(args, rank, world, dist):
@@ -248,15 +255,16 @@ def run_ours(args, rank, world, dist):
     s = Setup(w, dev, seed_offset=rank)
     stream = torch.cuda.Stream(device=dev)
     R = s.replicas
-    per_graph = max(R, 32)
+    per_graph = max(R * s.chain, 32)
+    per_graph = (per_graph + R * s.chain - 1) // (R * s.chain) * (R * s.chain)
     with torch.cuda.stream(stream):
-        for i in range(max(args.warmup, 3) * R):
-            s.step(i % R)
+        for i in range(max(args.warmup, 3) * R * s.chain):
+            s.step(i)
         stream.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for i in range(per_graph):
-                s.step(i % R)
+                s.step(i)
         g.replay()
         stream.synchronize()
     # calibrate the step time to size the timed region
@@ -310,7 +318,8 @@ def run_ours(args, rank, world, dist):
         "config": {"workload": w.name, "layout": w.layout, "batch": w.batch, "q_heads": w.q_heads,
                    "kv_heads": w.kv_heads, "head_dim": w.head_dim, "capacity": w.capacity,
                    "lens_mean": float(np.mean(s.lens)), "bytes_per_step": s.bytes_per_step,
-                   "l2": s.l2_note, "graph_steps": per_graph, "parallelism": f"rows x{world} (independent)"},
+                   "l2": s.l2_note, "graph_steps": per_graph, "chained_steps": s.chain,
+                   "parallelism": f"rows x{world} (independent)"},
         "roofline": {"bound": "hbm", "achieved": round(gbs / world, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(gbs / world / peak, 4), "traffic": None,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else
@@ -331,28 +340,29 @@ def run_e2e(s, stream, K_e2e):
     torch = s.torch
     q_h = s.q.cpu().pin_memory()
     kv_h = s.new_kv.cpu().pin_memory()
-    lens_h = torch.from_numpy(s.lens).pin_memory()
     y_h = torch.empty(s.out.shape, dtype=s.out.dtype).pin_memory()
-    h2d = q_h.numel() * 2 + kv_h.numel() * 2 + lens_h.numel() * 4
+    h2d = q_h.numel() * 2 + kv_h.numel() * 2 + s.lens.size * 4
     d2h = y_h.numel() * 2
     R = s.replicas
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    lens_h = [torch.from_numpy(l).pin_memory() for l in s.lens_list]
+
+    def one(i):
+        c = i % s.chain
+        s.q.copy_(q_h, non_blocking=True)
+        s.new_kv.copy_(kv_h, non_blocking=True)
+        s.lens_d_list[c].copy_(lens_h[c], non_blocking=True)
+        s.step(i)
+        y_h.copy_(s.out, non_blocking=True)
+
     with torch.cuda.stream(stream):
-        for i in range(3 * R):
-            s.q.copy_(q_h, non_blocking=True)
-            s.new_kv.copy_(kv_h, non_blocking=True)
-            s.lens_d.copy_(lens_h, non_blocking=True)
-            s.step(i % R)
-            y_h.copy_(s.out, non_blocking=True)
+        for i in range(3 * R * s.chain):
+            one(i)
         stream.synchronize()
         e0.record(stream)
         for i in range(K_e2e):
-            s.q.copy_(q_h, non_blocking=True)
-            s.new_kv.copy_(kv_h, non_blocking=True)
-            s.lens_d.copy_(lens_h, non_blocking=True)
-            s.step(i % R)
-            y_h.copy_(s.out, non_blocking=True)
+            one(i)
         e1.record(stream)
     stream.synchronize()
     ms = e0.elapsed_time(e1) / K_e2e

@@ -121,20 +121,25 @@ void plan_splits(AttnParams& p, const int32_t* lens_host, long long target, int 
   }
 }
 
-// Tensor-core path: variant (warps x stages), CTAs per SM, and for batches
-// with fewer (row, kv head) units than SMs one wave of CTAs grouped in
+// Tensor-core paths: kernel variant (warps x stages), CTAs per SM, and for
+// batches with fewer (row, kv head) units than SMs one wave of CTAs grouped in
 // clusters that merge their splits through distributed shared memory.
 void plan_fast(AttnParams& p, const int32_t* lens_host, int sms) {
   const long long units = (long long)p.batch * p.kv_heads;
+  const bool int4 = p.layout == OL_LAYOUT_INT4;
   // measured defaults: 8 warps x 2 stages for contiguous caches and small
-  // batches, 4 warps x 2 stages (three CTAs per SM) for paged pools
+  // batches, 4 warps x 2 stages (three CTAs per SM) for paged pools; INT4:
+  // 8 warps x 4 stages
   if (tune().cfg >= 0)
     p.variant = tune().cfg;
+  else if (int4)
+    p.variant = 0;
   else
     p.variant = (units >= sms && p.layout == OL_LAYOUT_PAGED) ? 2 : 3;
-  const int smem = fast_bf16_smem(p.variant) + 1024;
-  const int warps = fast_bf16_warps(p.variant);
-  int per_sm = (227 * 1024) / smem;
+  if (int4 && p.variant > 2) p.variant = 0;
+  const int smem = (int4 ? fast_int4_smem(p.variant) : fast_bf16_smem(p.variant)) + 1024;
+  const int warps = int4 ? fast_int4_warps(p.variant) : fast_bf16_warps(p.variant);
+  int per_sm = (228 * 1024) / smem;
   if (per_sm > 64 / warps) per_sm = 64 / warps;
   if (per_sm < 1) per_sm = 1;
   const long long slots = (long long)sms * per_sm;
@@ -144,10 +149,9 @@ void plan_fast(AttnParams& p, const int32_t* lens_host, int sms) {
   }
   int cs = pow2_floor(slots / units);
   if (cs > 16) cs = 16;
-  const int cap = fast_bf16_max_cluster(p.variant, p.layout == OL_LAYOUT_PAGED);
+  const int cap = int4 ? fast_int4_max_cluster(p.variant) : fast_bf16_max_cluster(p.variant, p.layout == OL_LAYOUT_PAGED);
   if (cs > cap) cs = cap;
   if (tune().cluster > 0 && cs > tune().cluster) cs = pow2_floor(tune().cluster);
-  // k clusters per (row, kv head), all CTAs resident at once: split length from the longest row
   // one cluster per (row, kv head) by default: a second level of merging
   // through global memory costs more than the extra CTAs gain
   long long k = slots / (units * cs);
@@ -434,7 +438,7 @@ ol_status run_attention(int layout, const void* desc, const CacheView& v, const 
     plan_fast(p, lens_host, sms);
     e = launch_fast_bf16(p, stream);
   } else if (layout == OL_LAYOUT_INT4 && fast_int4_supported(p)) {
-    plan_splits(p, lens_host, (long long)sms * 2 * tune().waves, 1);
+    plan_fast(p, lens_host, sms);
     e = launch_fast_int4(p, stream);
   } else {
     plan_splits(p, lens_host, (long long)sms * 4, 1);

@@ -18,7 +18,7 @@
 //   O^T[128 dims x 8 heads] += V^T[128 x 16] * P^T  8 mma, V via ldmatrix.trans
 // Warps merge in shared memory; CTAs of one (row, kv head) merge through
 // fp32 partials in the workspace and an atomic ticket (finish_split).
-#include "ol_common.cuh"
+#include "ol_merge.cuh"
 
 namespace ol {
 namespace {
@@ -27,7 +27,6 @@ constexpr int kTok = 16;                    // tokens per tile
 constexpr int kHalfBytes = kTok * 128;      // 16 rows x 64 bf16 (one SWIZZLE_128B box)
 constexpr int kPlaneBytes = 2 * kHalfBytes; // K or V tile: 4 KB
 constexpr int kStageBytes = 2 * kPlaneBytes;// K + V: 8 KB
-constexpr int kOStride = 132;               // fp32 row stride of per-warp O in shared memory
 
 template <int NWARPS, int STAGES>
 struct FastLayout {
@@ -59,16 +58,18 @@ __global__ void __launch_bounds__(NWARPS * 32)
   uint8_t* stages = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kStages);
   Work* sw = reinterpret_cast<Work*>(smem + L::kStages + L::kBars);
-  float* sm_wm = reinterpret_cast<float*>(smem + L::kStages + L::kBars + 256);  // [NWARPS][8]
-  float* sm_wl = sm_wm + NWARPS * 8;                                               // [NWARPS][8]
-  float* sm_m = sm_wl + NWARPS * 8;                                                // [8] CTA merge
-  float* sm_l = sm_m + 8;                                                          // [8]
-  float* sm_cm = sm_l + 8;                                                         // [8] cluster merge
-  float* sm_cl = sm_cm + 8;                                                        // [8]
-  float* sm_scr = sm_cl + 8;                                                       // [16] final-merge scratch
-  float* sm_cw = sm_scr + 16;                                                      // [16][8] cluster weights
-  float* sm_cwl = sm_cw + 16 * 8;                                                  // [16][8] weighted l
-  int* sm_flag = reinterpret_cast<int*>(sm_cwl + 16 * 8);
+  float* misc = reinterpret_cast<float*>(smem + L::kStages + L::kBars + 256);
+  MergeScratch ms;
+  ms.wm = misc;                 // [NWARPS][8]
+  ms.wl = ms.wm + NWARPS * 8;   // [NWARPS][8]
+  ms.m = ms.wl + NWARPS * 8;    // [8]
+  ms.l = ms.m + 8;
+  ms.cm = ms.l + 8;
+  ms.cl = ms.cm + 8;
+  ms.scr = ms.cl + 8;           // [16]
+  ms.cw = ms.scr + 16;          // [16][8]
+  ms.cwl = ms.cw + 16 * 8;      // [16][8]
+  ms.flag = reinterpret_cast<int*>(ms.cwl + 16 * 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int CS = p.cluster;
@@ -248,107 +249,14 @@ __global__ void __launch_bounds__(NWARPS * 32)
     }
   }
 
-  // per-warp state: l summed over the 8 lanes that share a head pair
-#pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    l_run0 += __shfl_xor_sync(0xffffffffu, l_run0, off);
-    l_run1 += __shfl_xor_sync(0xffffffffu, l_run1, off);
-  }
-  float* so = reinterpret_cast<float*>(my_stages);  // [8 heads][kOStride]
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    so[(2 * c) * kOStride + 16 * mt + n] = o[mt][0];
-    so[(2 * c + 1) * kOStride + 16 * mt + n] = o[mt][1];
-    so[(2 * c) * kOStride + 16 * mt + n + 8] = o[mt][2];
-    so[(2 * c + 1) * kOStride + 16 * mt + n + 8] = o[mt][3];
-  }
-  if (n == 0) {
-    sm_wm[warp * 8 + 2 * c] = m_run0;
-    sm_wm[warp * 8 + 2 * c + 1] = m_run1;
-    sm_wl[warp * 8 + 2 * c] = l_run0;
-    sm_wl[warp * 8 + 2 * c + 1] = l_run1;
-  }
-  __syncthreads();
-  if (threadIdx.x < 8) {
-    const int j = threadIdx.x;
-    float M = -INFINITY;
-    for (int ww = 0; ww < NWARPS; ++ww) M = fmaxf(M, sm_wm[ww * 8 + j]);
-    float Lsum = 0.f;
-    if (M != -INFINITY)
-      for (int ww = 0; ww < NWARPS; ++ww) {
-        const float mw = sm_wm[ww * 8 + j];
-        if (mw != -INFINITY) Lsum += sm_wl[ww * 8 + j] * fast_exp2(mw - M);
-      }
-    sm_m[j] = M;
-    sm_l[j] = Lsum;
-  }
-  __syncthreads();
-  float* merged = reinterpret_cast<float*>(stages + kStageBytes);  // warp 0's second stage: [8][kOStride]
-  for (int idx = threadIdx.x; idx < G * 128; idx += NWARPS * 32) {
-    const int j = idx >> 7, d = idx & 127;
-    const float M = sm_m[j];
-    float acc = 0.f;
-    if (M != -INFINITY)
-      for (int ww = 0; ww < NWARPS; ++ww) {
-        const float mw = sm_wm[ww * 8 + j];
-        if (mw != -INFINITY)
-          acc += reinterpret_cast<const float*>(stages + ww * STAGES * kStageBytes)[j * kOStride + d] *
-                 fast_exp2(mw - M);
-      }
-    merged[j * kOStride + d] = acc;
-  }
-  __syncthreads();
-  if (CS == 1) {
-    finish_split(p, w, sm_m, sm_l, merged, kOStride, 0, G, 0, 128, blockIdx.x, w.first_cta, w.nsplit, w.nsplit,
-                 sm_flag, sm_scr);
-    return;
-  }
-
-  // Cluster merge: the CS CTAs of a cluster hold consecutive splits of one
-  // (row, kv head). After a cluster barrier, every CTA reads the CS (m, l)
-  // pairs of each head (one remote load per thread), and CTA rank r merges
-  // dimensions [r*128/CS, (r+1)*128/CS) of every head from the CS CTAs' shared
-  // memory with independent remote loads.
-  cluster_sync();
-  const uint32_t rank = cluster_ctarank();
-  const int dspan = 128 / CS, d0 = (int)rank * dspan;
-  float* cmerged = reinterpret_cast<float*>(stages + kStageBytes) + 8 * kOStride;  // [8][dspan]
-  if (threadIdx.x < CS * 8) {  // (m, l) of head j in cluster CTA q
-    const int q = threadIdx.x >> 3, j = threadIdx.x & 7;
-    sm_cw[threadIdx.x] = ld_shared_cluster(map_shared_rank(smem_u32(sm_m + j), q));
-    sm_cwl[threadIdx.x] = ld_shared_cluster(map_shared_rank(smem_u32(sm_l + j), q));
-  }
-  __syncthreads();
-  if (threadIdx.x < 8) {
-    float M = -INFINITY;
-    for (int q = 0; q < CS; ++q) M = fmaxf(M, sm_cw[q * 8 + threadIdx.x]);
-    sm_cm[threadIdx.x] = M;
-  }
-  __syncthreads();
-  if (threadIdx.x < CS * 8) {  // weights 2^(m_q - M), zero for empty splits
-    const float M = sm_cm[threadIdx.x & 7], mq = sm_cw[threadIdx.x];
-    const float wq = (M == -INFINITY || mq == -INFINITY) ? 0.f : fast_exp2(mq - M);
-    sm_cw[threadIdx.x] = wq;
-    sm_cwl[threadIdx.x] *= wq;
-  }
-  __syncthreads();
-  if (threadIdx.x < 8) {
-    float Lsum = 0.f;
-    for (int q = 0; q < CS; ++q) Lsum += sm_cwl[q * 8 + threadIdx.x];
-    sm_cl[threadIdx.x] = Lsum;
-  }
-  for (int idx = threadIdx.x; idx < G * dspan; idx += NWARPS * 32) {
-    const int j = idx / dspan, d = d0 + idx % dspan;
-    const uint32_t local = smem_u32(merged + j * kOStride + d);
-    float acc = 0.f;
-#pragma unroll 4
-    for (int q = 0; q < CS; ++q) acc += ld_shared_cluster(map_shared_rank(local, q)) * sm_cw[q * 8 + j];
-    cmerged[j * dspan + (d - d0)] = acc;
-  }
-  cluster_sync();  // every remote read is done before any CTA of the cluster exits
-  if (!w.valid) return;
-  finish_split(p, w, sm_cm, sm_cl, cmerged, dspan, 0, G, d0, d0 + dspan, (int)(blockIdx.x / CS),
-               w.first_cta / CS, w.nsplit / CS, w.nsplit, sm_flag, sm_scr);
+  // per-warp state into the warp's own first stage, then the CTA / cluster / split merge
+  store_warp_state(reinterpret_cast<float*>(my_stages), ms, warp, o, m_run0, m_run1, l_run0, l_run1);
+  float* merged = reinterpret_cast<float*>(stages + kStageBytes);  // warp 0's second stage
+  float* cmerged = merged + 8 * kOStride;
+  merge_and_finish(
+      p, w, NWARPS,
+      [&](int st) { return reinterpret_cast<const float*>(stages + st * STAGES * kStageBytes); }, merged,
+      cmerged, ms);
 }
 
 // ------------------------------------------------------------------ host

@@ -109,6 +109,9 @@ int fast_bf16_warps(int variant);
 int fast_bf16_max_cluster(int variant, bool paged);
 cudaError_t launch_fast_bf16(const AttnParams& p, cudaStream_t s);
 bool fast_int4_supported(const AttnParams& p);
+int fast_int4_smem(int variant);
+int fast_int4_warps(int variant);
+int fast_int4_max_cluster(int variant);
 cudaError_t launch_fast_int4(const AttnParams& p, cudaStream_t s);
 
 // Visible range and split plan of one row, shared by the host planner and the
