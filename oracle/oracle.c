@@ -22,7 +22,7 @@
  *   - INT4 blockwise affine: per block of 32 elements one fp16 scale and one
  *     uint4 zero point, code = saturate(round_half_even(x / scale) + zp),
  *     two codes per byte with the first in the low nibble, reconstruction
- *     (code - zp) * scale (page "Custom quantized and persistent values",
+ *     (code - zp) * scale (page "Custom, quantized, and persistent values",
  *     section Struct types and byte-encodable layouts; page "Persistent
  *     input/output feedback", rounding and tolerance paragraph).
  *
