@@ -202,10 +202,15 @@ class Setup:
     def _make_replica(self, gen, rng):
         torch, ol, w = self.torch, self.ol, self.w
         B, H, D = w.batch, w.kv_heads, w.head_dim
+        # consecutive steps either use other caches (replicas, like the layers of
+        # a model) or rewrite only their own new row: the history is stable and
+        # the first tiles may be requested before the previous step completes.
+        # A chained workload appends where the next step reads: no such promise.
+        acc = ol.OL_READ_WRITE | (ol.OL_HISTORY_STABLE if self.chain == 1 else 0)
         if w.layout == "contiguous":
             cache = torch.randn((2, B, H, w.capacity, D), generator=gen, device=self.dev).to(torch.bfloat16)
             self.caches.append(cache)
-            self.descs.append(ol.kv_cache(cache))
+            self.descs.append(ol.kv_cache(cache, access=acc))
             self.updated.append(cache)
             self.layout = ol.OL_LAYOUT_CONTIGUOUS
         elif w.layout == "paged":
@@ -220,7 +225,7 @@ class Setup:
             table = np.ascontiguousarray(perm[: B * M].reshape(B, M))
             bt_d = torch.from_numpy(table).to(self.dev)
             self.caches.append((pool, bt_d, table))
-            self.descs.append(ol.paged_kv(pool, bt_d, table))
+            self.descs.append(ol.paged_kv(pool, bt_d, table, access=acc))
             self.updated.append(pool)
             self.layout = ol.OL_LAYOUT_PAGED
         else:
@@ -233,7 +238,7 @@ class Setup:
                                 dtype=torch.int32).to(torch.uint8)
             del rows
             self.caches.append((codes, scales, zps))
-            self.descs.append(ol.int4_kv(codes, scales, zps, head_dim=D))
+            self.descs.append(ol.int4_kv(codes, scales, zps, head_dim=D, access=acc))
             self.updated.append(codes)
             self.layout = ol.OL_LAYOUT_INT4
 
@@ -319,6 +324,7 @@ def run_ours(args, rank, world, dist):
                    "kv_heads": w.kv_heads, "head_dim": w.head_dim, "capacity": w.capacity,
                    "lens_mean": float(np.mean(s.lens)), "bytes_per_step": s.bytes_per_step,
                    "l2": s.l2_note, "graph_steps": per_graph, "chained_steps": s.chain,
+                   "history_stable": s.chain == 1,
                    "parallelism": f"rows x{world} (independent)"},
         "roofline": {"bound": "hbm", "achieved": round(gbs / world, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(gbs / world / peak, 4), "traffic": None,

@@ -30,7 +30,10 @@
  *   values, on the device) drive the kernels. The caller keeps them equal;
  *   the kernels still check every index they use and skip (never perform) an
  *   access outside the caller's buffers, recording OL_DEVICE_GUARD in the
- *   workspace status word where a workspace is passed.
+ *   workspace status word where a workspace is passed. For attention and
+ *   step calls on batches of at most 160 rows the launch carries lens_host by
+ *   value and the kernels read no lens_dev; a call captured in a CUDA graph
+ *   replays the lengths (and launch size) it was captured with.
  * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *   stream). Calls on one workspace must not overlap on the GPU.
  * - Alignment: every device pointer must be 16-byte aligned (OL_ERR_ALIGN).
@@ -76,6 +79,19 @@ typedef enum ol_dtype { OL_F32 = 0, OL_BF16 = 1 } ol_dtype;
 
 /* ValueInfoProto.access of the cache binding (page "Mutable execution cache", Proto additions). */
 typedef enum ol_access { OL_READ_ONLY = 0, OL_READ_WRITE = 1 } ol_access;
+
+/*
+ * Optional bit ORed into a descriptor's `access`: the caller guarantees that
+ * no work enqueued earlier on the same stream is still writing this cache's
+ * history rows [0, lens[b] - 1) of any row (nor, for a paged cache, the block
+ * table entries that cover them). Attention-bearing calls may then start
+ * reading those rows while the preceding kernel finishes (programmatic
+ * dependent launch); q, new K/V, lengths, outputs and workspace are still
+ * touched only after it completes. Typical use: consecutive layers of a model,
+ * each with its own cache. Not valid for a step that immediately follows a
+ * step on the same cache (that step wrote row lens[b] - 2).
+ */
+enum { OL_HISTORY_STABLE = 0x100 };
 
 typedef enum ol_layout { OL_LAYOUT_CONTIGUOUS = 0, OL_LAYOUT_PAGED = 1, OL_LAYOUT_INT4 = 2 } ol_layout;
 

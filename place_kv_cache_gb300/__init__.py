@@ -23,6 +23,7 @@ OL_OK, OL_ERR_NULL, OL_ERR_ALIAS, OL_ERR_READONLY, OL_ERR_CAPACITY, OL_ERR_SHAPE
     OL_ERR_WORKSPACE, OL_ERR_CUDA, OL_ERR_UNSUPPORTED, OL_ERR_INJECTED, OL_ERR_PAGE, OL_ERR_ALIGN = range(14)
 OL_F32, OL_BF16 = 0, 1
 OL_READ_ONLY, OL_READ_WRITE = 0, 1
+OL_HISTORY_STABLE = 0x100
 OL_LAYOUT_CONTIGUOUS, OL_LAYOUT_PAGED, OL_LAYOUT_INT4 = 0, 1, 2
 OL_Q_DYNAMIC, OL_Q_FIXED = 0, 1
 OL_DEVICE_OK, OL_DEVICE_GUARD = 0, 1

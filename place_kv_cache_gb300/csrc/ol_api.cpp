@@ -192,6 +192,7 @@ struct CacheView {
   int dtype;
   int batch, kv_heads, head_dim, capacity;
   int access;
+  bool history_stable;
   uint64_t owner;
   void* alias_ptr;  // pointer that `updated` must equal
   Range ranges[3];  // cache storage (INT4: three planes)
@@ -210,7 +211,8 @@ ol_status view_contiguous(const ol_kv_cache* c, CacheView& v) {
   v.kv_heads = c->kv_heads;
   v.head_dim = c->head_dim;
   v.capacity = c->capacity;
-  v.access = c->access;
+  v.access = c->access & ~OL_HISTORY_STABLE;
+  v.history_stable = (c->access & OL_HISTORY_STABLE) != 0;
   v.owner = c->owner;
   v.alias_ptr = c->data;
   v.ranges[0] = range_of(c->data, 2ull * c->batch * c->kv_heads * c->capacity * c->head_dim * elt_bytes(c->dtype));
@@ -233,7 +235,8 @@ ol_status view_paged(const ol_paged_kv* c, CacheView& v) {
   v.kv_heads = c->kv_heads;
   v.head_dim = c->head_dim;
   v.capacity = c->max_pages * c->page_size;
-  v.access = c->access;
+  v.access = c->access & ~OL_HISTORY_STABLE;
+  v.history_stable = (c->access & OL_HISTORY_STABLE) != 0;
   v.owner = c->owner;
   v.alias_ptr = c->data;
   v.ranges[0] = range_of(c->data, 2ull * c->num_pages * c->kv_heads * c->page_size * c->head_dim *
@@ -258,7 +261,8 @@ ol_status view_int4(const ol_int4_kv* c, CacheView& v) {
   v.kv_heads = c->kv_heads;
   v.head_dim = c->head_dim;
   v.capacity = c->capacity;
-  v.access = c->access;
+  v.access = c->access & ~OL_HISTORY_STABLE;
+  v.history_stable = (c->access & OL_HISTORY_STABLE) != 0;
   v.owner = c->owner;
   v.alias_ptr = c->codes;
   const unsigned long long rows = 2ull * c->batch * c->kv_heads * c->capacity;
@@ -427,6 +431,10 @@ ol_status run_attention(int layout, const void* desc, const CacheView& v, const 
   p.window = window < 0 ? -1 : window;
   p.out = out;
   p.out_dtype = out_dtype;
+  p.inline_lens = v.batch <= kInlineRows ? 1 : 0;
+  if (p.inline_lens)
+    for (int b = 0; b < v.batch; ++b) p.lens_inline[b] = lens_host[b];
+  p.early = (v.history_stable && p.inline_lens) ? 1 : 0;
   char* ws = static_cast<char*>(workspace);
   p.status = reinterpret_cast<int32_t*>(ws);
   p.counters = reinterpret_cast<uint32_t*>(ws + kStatusBytes);

@@ -33,9 +33,10 @@ struct FastLayout {
   static constexpr int kStages = NWARPS * STAGES * kStageBytes;
   static constexpr int kBars = NWARPS * STAGES * 8;
   static constexpr int kMisc = 256 + NWARPS * 8 * 4 * 2 + 8 * 4 * 6 + 2 * 16 * 8 * 4 + 16;
-  static constexpr int kTotal = 1024 /* alignment slack */ + kStages + kBars + kMisc;
+  static constexpr int kRecv = (1024 + 2 * 128 + 8 * 64) * 4;  // cluster receive buffers + cmerged
+  static constexpr int kTotal = 1024 /* alignment slack */ + kStages + kRecv + kBars + kMisc;
   static_assert(STAGES >= 2, "the merged O lives in warp 0's second stage");
-  static_assert(8 * kOStride * 4 + 8 * 64 * 4 <= kStageBytes, "CTA and cluster merge buffers fit one stage");
+  static_assert(8 * kOStride * 4 <= kStageBytes, "the CTA state fits one stage");
 };
 
 __device__ __forceinline__ int tile_row(const AttnParams& p, bool paged, int plane, int b, int g, int t0,
@@ -51,14 +52,15 @@ __device__ __forceinline__ int tile_row(const AttnParams& p, bool paged, int pla
 
 template <int NWARPS, int STAGES, bool PAGED>
 __global__ void __launch_bounds__(NWARPS * 32)
-    fast_bf16_kernel(const __grid_constant__ CUtensorMap tmap, const AttnParams p) {
+    fast_bf16_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ AttnParams p) {
   using L = FastLayout<NWARPS, STAGES>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = align1024(smem_raw);
   uint8_t* stages = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kStages);
-  Work* sw = reinterpret_cast<Work*>(smem + L::kStages + L::kBars);
-  float* misc = reinterpret_cast<float*>(smem + L::kStages + L::kBars + 256);
+  float* recv = reinterpret_cast<float*>(smem + L::kStages);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kStages + L::kRecv);
+  Work* sw = reinterpret_cast<Work*>(smem + L::kStages + L::kRecv + L::kBars);
+  float* misc = reinterpret_cast<float*>(smem + L::kStages + L::kRecv + L::kBars + 256);
   MergeScratch ms;
   ms.wm = misc;                 // [NWARPS][8]
   ms.wl = ms.wm + NWARPS * 8;   // [NWARPS][8]
@@ -68,8 +70,12 @@ __global__ void __launch_bounds__(NWARPS * 32)
   ms.cl = ms.cm + 8;
   ms.scr = ms.cl + 8;           // [16]
   ms.cw = ms.scr + 16;          // [16][8]
-  ms.cwl = ms.cw + 16 * 8;      // [16][8]
-  ms.flag = reinterpret_cast<int*>(ms.cwl + 16 * 8);
+  ms.wt = ms.cw + 16 * 8;       // [16][8] (>= nstates x 8)
+  ms.flag = reinterpret_cast<int*>(ms.wt + 16 * 8);
+  ms.recv_o = recv;             // [1024]
+  ms.recv_m = recv + 1024;      // [128]
+  ms.recv_l = recv + 1024 + 128;
+  float* cmerged = recv + 1024 + 256;  // [8][64]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int CS = p.cluster;
@@ -79,17 +85,25 @@ __global__ void __launch_bounds__(NWARPS * 32)
     for (int st = 0; st < STAGES; ++st) mbar_init(bar0 + 8 * st, 1);
     fence_mbar_init();
   }
-  pdl_wait();
-  pdl_launch_dependents();
+  // With the lengths carried in the launch the CTA mapping needs no memory
+  // written by earlier work and runs before the dependency wait; so do the
+  // first TMA requests when the caller declared the history stable.
+  if (!p.inline_lens) pdl_wait();
   if (warp == 0) {
-    Work w = map_cta_warp(p.lens, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, blockIdx.x, p.status, CS);
+    Work w = p.inline_lens
+                 ? map_cta_warp(p.lens_inline, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, blockIdx.x,
+                                nullptr, CS)
+                 : map_cta_warp(p.lens, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, blockIdx.x, p.status, CS);
     if (lane == 0) *sw = w;
   }
   __syncthreads();
   const Work w = *sw;
   // Without a cluster an unmapped CTA can leave now; in a cluster every CTA
   // must reach the cluster barriers, so it runs with an empty token range.
-  if (!w.valid && CS == 1) return;
+  if (!w.valid && CS == 1) {
+    if (p.inline_lens) pdl_wait();
+    return;
+  }
 
   const int G = p.group;
   const int nsub = w.valid ? (w.t_end - w.t_begin + kTok - 1) / kTok : 0;
@@ -113,10 +127,13 @@ __global__ void __launch_bounds__(NWARPS * 32)
     tma_load_2d(dst + kPlaneBytes, &tmap, 0, rv, bar, pol);
     tma_load_2d(dst + kPlaneBytes + kHalfBytes, &tmap, 64, rv, bar, pol);
   };
-  if (lane == 0) {
-    const int pre = my_n < STAGES ? my_n : STAGES;
+  const int pre = my_n < STAGES ? my_n : STAGES;
+  if (p.early && lane == 0)
     for (int i = 0; i < pre; ++i) issue(i);
-  }
+  if (p.inline_lens) pdl_wait();
+  pdl_launch_dependents();
+  if (!p.early && lane == 0)
+    for (int i = 0; i < pre; ++i) issue(i);
 
   // q^T as the B operand (16 dims x 8 heads per k-step): lane (c, n) holds
   // q[n][16kk + 2c, +1] and q[n][16kk + 2c + 8, +9]; heads n >= G are zero.
@@ -251,8 +268,7 @@ __global__ void __launch_bounds__(NWARPS * 32)
 
   // per-warp state into the warp's own first stage, then the CTA / cluster / split merge
   store_warp_state(reinterpret_cast<float*>(my_stages), ms, warp, o, m_run0, m_run1, l_run0, l_run1);
-  float* merged = reinterpret_cast<float*>(stages + kStageBytes);  // warp 0's second stage
-  float* cmerged = merged + 8 * kOStride;
+  float* merged = reinterpret_cast<float*>(stages + kStageBytes);  // warp 0's second stage (no cluster)
   merge_and_finish(
       p, w, NWARPS,
       [&](int st) { return reinterpret_cast<const float*>(stages + st * STAGES * kStageBytes); }, merged,

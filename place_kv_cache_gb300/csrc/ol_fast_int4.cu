@@ -10,8 +10,8 @@
 // and 2 x 128 B of scales and 2 x 32 B of zero points by bulk copies.
 // Dequantization happens in registers: a nibble c becomes the exact bf16
 // value 128 + c with one mask-and-or per pair.
-//   S^T: one accumulator per 32-dim block b, fed (128 + c) codes; then
-//        s = sum_b scale_K[t,b] * (acc_b - (128 + zp_K[t,b]) * qsum_b)
+//   S^T: one accumulator per 32-dim block b, fed the exact bf16 values
+//        (128 + c) - (128 + zp_K) = c - zp_K; then s = sum_b scale_K[t,b] * acc_b
 //   O^T: V^T as exact bf16 (c - zp_V) per token, the V scale folded into
 //        P^T per block, P^T carried as bf16 hi + lo.
 // The token being appended (fused step) takes part uncompressed from new_kv as
@@ -35,7 +35,11 @@ constexpr uint32_t kMagic = 0x43004300u;  // bf16 pair (128, 128)
 template <int NWARPS, int STAGES>
 struct Int4Layout {
   static constexpr int kStages = NWARPS * STAGES * kStage;
-  static constexpr int kExtra = 3 * 8 * kOStride * 4;  // extra state O, merged, cmerged (<= 8 x 64)
+  // extra state O, then one region that is either the CTA-merged state (no
+  // cluster) or the cluster receive buffers + cmerged (cluster): never both
+  static constexpr int kUnion = (1024 + 2 * 128 + 8 * 64) * 4 > 8 * kOStride * 4 ? (1024 + 2 * 128 + 8 * 64) * 4
+                                                                               : 8 * kOStride * 4;
+  static constexpr int kExtra = 8 * kOStride * 4 + kUnion;
   static constexpr int kBars = NWARPS * STAGES * 8;
   static constexpr int kMisc = 256 + (NWARPS + 1) * 8 * 4 * 2 + 8 * 4 * 6 + 16 * 4 + 2 * 16 * 8 * 4 + 16;
   static constexpr int kTotal = 1024 + kStages + kExtra + kBars + kMisc;
@@ -54,21 +58,18 @@ __device__ __forceinline__ uint32_t hsub2_bf16(uint32_t a, uint32_t b) {
 __device__ __forceinline__ int swz64(int r, int x) {
   return r * 64 + ((((x >> 4) ^ (r >> 1)) & 3) << 4) + (x & 15);
 }
-__device__ __forceinline__ int zp_of(const uint8_t* zrow, int b) {
-  const uint8_t z = zrow[b >> 1];
-  return (b & 1) ? (z >> 4) : (z & 0xF);
-}
 
 template <int NWARPS, int STAGES>
 __global__ void __launch_bounds__(NWARPS * 32)
-    fast_int4_kernel(const __grid_constant__ CUtensorMap tmap, const AttnParams p) {
+    fast_int4_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ AttnParams p) {
   using L = Int4Layout<NWARPS, STAGES>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = align1024(smem_raw);
   uint8_t* stages = smem;
   float* extra_o = reinterpret_cast<float*>(smem + L::kStages);
-  float* merged = extra_o + 8 * kOStride;
-  float* cmerged = merged + 8 * kOStride;
+  float* merged = extra_o + 8 * kOStride;  // no cluster: the CTA state
+  float* recv = merged;                    // cluster: receive buffers, then cmerged
+  float* cmerged = recv + 1024 + 256;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kStages + L::kExtra);
   Work* sw = reinterpret_cast<Work*>(smem + L::kStages + L::kExtra + L::kBars);
   float* misc = reinterpret_cast<float*>(smem + L::kStages + L::kExtra + L::kBars + 256);
@@ -81,8 +82,11 @@ __global__ void __launch_bounds__(NWARPS * 32)
   ms.cl = ms.cm + 8;
   ms.scr = ms.cl + 8;
   ms.cw = ms.scr + 16;
-  ms.cwl = ms.cw + 16 * 8;
-  ms.flag = reinterpret_cast<int*>(ms.cwl + 16 * 8);
+  ms.wt = ms.cw + 16 * 8;
+  ms.flag = reinterpret_cast<int*>(ms.wt + 16 * 8);
+  ms.recv_o = recv;
+  ms.recv_m = recv + 1024;
+  ms.recv_l = recv + 1024 + 128;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int CS = p.cluster;
@@ -92,15 +96,20 @@ __global__ void __launch_bounds__(NWARPS * 32)
     for (int st = 0; st < STAGES; ++st) mbar_init(bar0 + 8 * st, 1);
     fence_mbar_init();
   }
-  pdl_wait();
-  pdl_launch_dependents();
+  if (!p.inline_lens) pdl_wait();
   if (warp == 0) {
-    Work w = map_cta_warp(p.lens, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, blockIdx.x, p.status, CS);
+    Work w = p.inline_lens
+                 ? map_cta_warp(p.lens_inline, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, blockIdx.x,
+                                nullptr, CS)
+                 : map_cta_warp(p.lens, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, blockIdx.x, p.status, CS);
     if (lane == 0) *sw = w;
   }
   __syncthreads();
   const Work w = *sw;
-  if (!w.valid && CS == 1) return;
+  if (!w.valid && CS == 1) {
+    if (p.inline_lens) pdl_wait();
+    return;
+  }
 
   const int G = p.group;
   const int C = p.capacity;
@@ -124,17 +133,19 @@ __global__ void __launch_bounds__(NWARPS * 32)
     bulk_load(smem_u32(dst + kOffZk), p.zps + (size_t)(rowK0 + t0) * 2, kZpBytes, bar, pol);
     bulk_load(smem_u32(dst + kOffZv), p.zps + (size_t)(rowV0 + t0) * 2, kZpBytes, bar, pol);
   };
-  if (lane == 0) {
-    const int pre = my_n < STAGES ? my_n : STAGES;
+  const int pre = my_n < STAGES ? my_n : STAGES;
+  if (p.early && lane == 0)
     for (int i = 0; i < pre; ++i) issue(i);
-  }
+  if (p.inline_lens) pdl_wait();
+  pdl_launch_dependents();
+  if (!p.early && lane == 0)
+    for (int i = 0; i < pre; ++i) issue(i);
 
   // q as the B operand of the four blocks' k-steps, in the dims order of the
   // code words: lane (c, n) holds q[n][32b + 8c .. +7] as e0..e7;
   // k-step (b, hh): b0 = {e(2hh), e(2hh+4)}, b1 = {e(2hh+1), e(2hh+5)}.
   const int c = lane & 3, n = lane >> 2;
   uint32_t qf[4][2][2];
-  float qs[4];  // per block: sum of this lane's 8 q values
   {
     const bool live = n < G && w.valid;
     const uint16_t* qp = reinterpret_cast<const uint16_t*>(p.q) +
@@ -146,22 +157,8 @@ __global__ void __launch_bounds__(NWARPS * 32)
       qf[b][0][1] = __byte_perm(v.x, v.z, 0x7632);
       qf[b][1][0] = __byte_perm(v.y, v.w, 0x5410);
       qf[b][1][1] = __byte_perm(v.y, v.w, 0x7632);
-      qs[b] = __uint_as_float(v.x << 16) + __uint_as_float(v.x & 0xffff0000u) + __uint_as_float(v.y << 16) +
-              __uint_as_float(v.y & 0xffff0000u) + __uint_as_float(v.z << 16) + __uint_as_float(v.z & 0xffff0000u) +
-              __uint_as_float(v.w << 16) + __uint_as_float(v.w & 0xffff0000u);
     }
   }
-  // qsum[b] of head n, then the values for this lane's S^T heads 2c and 2c+1
-  float qsum0[4], qsum1[4];
-#pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    float t = qs[b];
-    t += __shfl_xor_sync(0xffffffffu, t, 1);
-    t += __shfl_xor_sync(0xffffffffu, t, 2);
-    qsum0[b] = __shfl_sync(0xffffffffu, t, 8 * c);
-    qsum1[b] = __shfl_sync(0xffffffffu, t, 8 * c + 4);
-  }
-
   float o[8][4];
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
@@ -176,43 +173,43 @@ __global__ void __launch_bounds__(NWARPS * 32)
       break;
     }
     const int t0 = w.t_begin + (warp + i * NWARPS) * kTok;
-    const uint8_t* sg = my_stages + st * kStage;
-    const uint8_t* kc = sg;
-    const uint8_t* vc = sg + kOffVc;
-    const uint16_t* ksc = reinterpret_cast<const uint16_t*>(sg + kOffSk);
-    const uint16_t* vsc = reinterpret_cast<const uint16_t*>(sg + kOffSv);
-    const uint8_t* kz = sg + kOffZk;
-    const uint8_t* vz = sg + kOffZv;
+    const uint32_t sg = smem_u32(my_stages + st * kStage);
+    const uint32_t kc = sg, vc = sg + kOffVc, ksc = sg + kOffSk, vsc = sg + kOffSv, kz = sg + kOffZk, vz = sg + kOffZv;
 
     const int ra = n, rb = n + 8;  // the lane's S^T rows (tokens) in this tile
     const bool va = t0 + ra >= w.lo && t0 + ra < t_stop;
     const bool vb = t0 + rb >= w.lo && t0 + rb < t_stop;
 
-    // ---- S^T = K q^T, one accumulator per 32-dim block
+    // ---- S^T = K q^T, one accumulator per 32-dim block, A = exact (c - zp)
+    // zero points of rows ra / rb, duplicated in both 16-bit halves
+    const uint32_t za = lds_u16(kz + 2 * ra), zb = lds_u16(kz + 2 * rb);
+    const uint32_t zda = za | (za << 16), zdb = zb | (zb << 16);
     float sacc[4][4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       sacc[b][0] = sacc[b][1] = sacc[b][2] = sacc[b][3] = 0.f;
-      const uint32_t wa = *reinterpret_cast<const uint32_t*>(kc + swz64(ra, 16 * b + 4 * c));
-      const uint32_t wb = *reinterpret_cast<const uint32_t*>(kc + swz64(rb, 16 * b + 4 * c));
-      mma_bf16_16816(sacc[b], code_pair(wa, 0), code_pair(wb, 0), code_pair(wa, 4), code_pair(wb, 4), qf[b][0][0],
+      const uint32_t wa = lds_u32(kc + swz64(ra, 16 * b + 4 * c));
+      const uint32_t wb = lds_u32(kc + swz64(rb, 16 * b + 4 * c));
+      const uint32_t zpa = code_pair(zda, 4 * b), zpb = code_pair(zdb, 4 * b);  // (128 + zp, 128 + zp)
+      mma_bf16_16816(sacc[b], hsub2_bf16(code_pair(wa, 0), zpa), hsub2_bf16(code_pair(wb, 0), zpb),
+                     hsub2_bf16(code_pair(wa, 4), zpa), hsub2_bf16(code_pair(wb, 4), zpb), qf[b][0][0],
                      qf[b][0][1]);
-      mma_bf16_16816(sacc[b], code_pair(wa, 8), code_pair(wb, 8), code_pair(wa, 12), code_pair(wb, 12), qf[b][1][0],
+      mma_bf16_16816(sacc[b], hsub2_bf16(code_pair(wa, 8), zpa), hsub2_bf16(code_pair(wb, 8), zpb),
+                     hsub2_bf16(code_pair(wa, 12), zpa), hsub2_bf16(code_pair(wb, 12), zpb), qf[b][1][0],
                      qf[b][1][1]);
     }
-    const uint2 ska = *reinterpret_cast<const uint2*>(ksc + 4 * ra);
-    const uint2 skb = *reinterpret_cast<const uint2*>(ksc + 4 * rb);
+    const uint2 ska = lds_v2(ksc + 8 * ra);
+    const uint2 skb = lds_v2(ksc + 8 * rb);
     float s00 = 0.f, s01 = 0.f, s10 = 0.f, s11 = 0.f;
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       const uint32_t pa = b < 2 ? ska.x : ska.y, pb = b < 2 ? skb.x : skb.y;
       const float sca = fp16_bits_to_float((b & 1) ? (pa >> 16) : (pa & 0xffff));
       const float scb = fp16_bits_to_float((b & 1) ? (pb >> 16) : (pb & 0xffff));
-      const float za = 128.f + zp_of(kz + 2 * ra, b), zb = 128.f + zp_of(kz + 2 * rb, b);
-      s00 += sca * (sacc[b][0] - za * qsum0[b]);
-      s01 += sca * (sacc[b][1] - za * qsum1[b]);
-      s10 += scb * (sacc[b][2] - zb * qsum0[b]);
-      s11 += scb * (sacc[b][3] - zb * qsum1[b]);
+      s00 += sca * sacc[b][0];
+      s01 += sca * sacc[b][1];
+      s10 += scb * sacc[b][2];
+      s11 += scb * sacc[b][3];
     }
     s00 = va ? s00 * p.scale_log2 : -INFINITY;
     s01 = va ? s01 * p.scale_log2 : -INFINITY;
@@ -244,9 +241,12 @@ __global__ void __launch_bounds__(NWARPS * 32)
     }
 
     // ---- O^T += V^T P^T, block by block
-    const uint2 sva = *reinterpret_cast<const uint2*>(vsc + 4 * ra);
-    const uint2 svb = *reinterpret_cast<const uint2*>(vsc + 4 * rb);
+    const uint2 sva = lds_v2(vsc + 8 * ra);
+    const uint2 svb = lds_v2(vsc + 8 * rb);
     const int r0 = 2 * c, r1 = 2 * c + 1, r8 = 2 * c + 8, r9 = 2 * c + 9;  // V^T columns (tokens) of this lane
+    // zero points of those tokens: tokens (r0, r1) in the two 16-bit halves, likewise (r8, r9)
+    const uint32_t zv01 = lds_u16(vz + 2 * r0) | (lds_u16(vz + 2 * r1) << 16);
+    const uint32_t zv89 = lds_u16(vz + 2 * r8) | (lds_u16(vz + 2 * r9) << 16);
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       const uint32_t pa = b < 2 ? sva.x : sva.y, pb = b < 2 ? svb.x : svb.y;
@@ -260,12 +260,9 @@ __global__ void __launch_bounds__(NWARPS * 32)
       const uint32_t pl0 = movmatrix_trans(l0), pl1 = movmatrix_trans(l1);
       // V codes of this lane's dims (32b + 4n .. +3) for tokens r0, r1, r8, r9
       const int x = 16 * b + 2 * n;
-      const uint32_t w01 = *reinterpret_cast<const uint16_t*>(vc + swz64(r0, x)) |
-                           (uint32_t(*reinterpret_cast<const uint16_t*>(vc + swz64(r1, x))) << 16);
-      const uint32_t w89 = *reinterpret_cast<const uint16_t*>(vc + swz64(r8, x)) |
-                           (uint32_t(*reinterpret_cast<const uint16_t*>(vc + swz64(r9, x))) << 16);
-      const uint32_t z01 = (0x4300u | zp_of(vz + 2 * r0, b)) | ((0x4300u | zp_of(vz + 2 * r1, b)) << 16);
-      const uint32_t z89 = (0x4300u | zp_of(vz + 2 * r8, b)) | ((0x4300u | zp_of(vz + 2 * r9, b)) << 16);
+      const uint32_t w01 = lds_u16(vc + swz64(r0, x)) | (lds_u16(vc + swz64(r1, x)) << 16);
+      const uint32_t w89 = lds_u16(vc + swz64(r8, x)) | (lds_u16(vc + swz64(r9, x)) << 16);
+      const uint32_t z01 = code_pair(zv01, 4 * b), z89 = code_pair(zv89, 4 * b);  // (128 + zp) per token
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint32_t a0 = hsub2_bf16(code_pair(w01, 8 * h), z01);

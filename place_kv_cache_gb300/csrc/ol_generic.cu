@@ -90,7 +90,7 @@ __device__ void append_token_warp(const AttnParams& p, int b, int g, int pos) {
   }
 }
 
-__global__ void __launch_bounds__(kGenWarps * 32) generic_attn_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kGenWarps * 32) generic_attn_kernel(const __grid_constant__ AttnParams p) {
   __shared__ Work sw;
   __shared__ int sm_flag;
   __shared__ float sm_wm[kGenWarps][kGenHeads], sm_wl[kGenWarps][kGenHeads];
@@ -103,7 +103,10 @@ __global__ void __launch_bounds__(kGenWarps * 32) generic_attn_kernel(const Attn
   pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 0) {
-    Work w = map_cta_warp(p.lens, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, blockIdx.x, p.status);
+    Work w = p.inline_lens ? map_cta_warp(p.lens_inline, p.batch, p.kv_heads, p.capacity, p.window, p.chunk,
+                                          blockIdx.x, nullptr)
+                           : map_cta_warp(p.lens, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, blockIdx.x,
+                                          p.status);
     if (lane == 0) sw = w;
   }
   __syncthreads();

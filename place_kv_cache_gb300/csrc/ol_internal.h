@@ -17,6 +17,7 @@ namespace ol {
 //   [partials_off, ...)          float partial results, one slot per CTA and query head:
 //                                {m (log2 domain), l, o[head_dim]}
 constexpr size_t kStatusBytes = 256;
+constexpr int kInlineRows = 160;  // batches up to this size carry their lengths in the launch
 constexpr int kMaxExtraSplits = 4096;  // CTAs beyond one per (row, kv head)
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -67,6 +68,10 @@ struct AttnParams {
   int window;           // < 0: unbounded
   void* out;            // [B, Hq, D]
   int out_dtype;
+
+  int inline_lens;      // 1: lengths are lens_inline (the host array, by value), lens is not read
+  int early;            // 1: history rows are stable: tiles may be requested before the dependency wait
+  int32_t lens_inline[kInlineRows];
 
   int32_t* status;      // device status word
   uint32_t* counters;   // [B * Hkv]

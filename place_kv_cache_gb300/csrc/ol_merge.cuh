@@ -13,12 +13,15 @@ constexpr int kOStride = 132;  // fp32 row stride of an [8 heads][128 dims] stat
 struct MergeScratch {
   float* wm;      // [nstates][8] per-state maxima (log2 domain)
   float* wl;      // [nstates][8] per-state sums
+  float* wt;      // [nstates][8] per-state weights 2^(m_s - M)
   float* m;       // [8] CTA state
   float* l;       // [8]
   float* cm;      // [8] cluster state
   float* cl;      // [8]
   float* cw;      // [16][8] cluster weights
-  float* cwl;     // [16][8] weighted cluster sums
+  float* recv_o;  // [CS][8][128/CS] slices pushed by the cluster's CTAs (1024 floats)
+  float* recv_m;  // [CS][8] their maxima
+  float* recv_l;  // [CS][8] their sums
   float* scr;     // [16] final-merge scratch
   int* flag;
 };
@@ -55,89 +58,132 @@ __device__ __forceinline__ void store_warp_state(float* so, const MergeScratch& 
   }
 }
 
-// Merge `nstates` states (state s has O at state_o(s)) into the CTA state
-// `merged` ([8][kOStride]) and ms.m / ms.l, then finish: with p.cluster == 1
-// through finish_split; otherwise through the cluster merge (CTA rank r
-// merges dims [r*128/CS, (r+1)*128/CS) of every head from all CS CTAs) and
-// then finish_split on those dims. Every thread of every CTA of the cluster
-// must call it (it contains cluster barriers when p.cluster > 1).
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ void st_shared_cluster(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_shared_cluster_v4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// Merge `nstates` (<= 32) states (state s has O at state_o(s)) into the CTA
+// state and finish. Weights 2^(m_s - M) are formed once per (state, head).
+//   p.cluster == 1: the CTA state goes to `merged` ([8][kOStride]) and
+//     finish_split.
+//   p.cluster == CS > 1: the CTAs of a cluster hold consecutive splits of one
+//     (row, kv head); CTA r owns dims [r*128/CS, (r+1)*128/CS). Each CTA pushes
+//     its state straight into the owners' receive buffers (remote shared-memory
+//     stores), one cluster barrier makes them visible, and every CTA merges its
+//     own slice from local shared memory. No remote loads, one barrier; after
+//     the barrier a CTA touches only its own shared memory and may exit.
+// Every thread of every CTA of the cluster must call it.
 template <typename StateO>
 __device__ __forceinline__ void merge_and_finish(const AttnParams& p, const Work& w, int nstates, StateO state_o,
                                                  float* merged, float* cmerged, const MergeScratch& ms) {
   const int G = p.group;
   const int CS = p.cluster;
   __syncthreads();
-  if (threadIdx.x < 8) {
+  if (threadIdx.x < 8) {  // one thread per head: maximum, weights 2^(m_s - M), sum
     const int j = threadIdx.x;
     float M = -INFINITY;
     for (int s = 0; s < nstates; ++s) M = fmaxf(M, ms.wm[s * 8 + j]);
     float L = 0.f;
-    if (M != -INFINITY)
-      for (int s = 0; s < nstates; ++s) {
-        const float mw = ms.wm[s * 8 + j];
-        if (mw != -INFINITY) L += ms.wl[s * 8 + j] * fast_exp2(mw - M);
-      }
+    for (int s = 0; s < nstates; ++s) {
+      const float mw = ms.wm[s * 8 + j];
+      const float wt = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
+      ms.wt[s * 8 + j] = wt;
+      L += wt * ms.wl[s * 8 + j];
+    }
     ms.m[j] = M;
     ms.l[j] = L;
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < G * 128; idx += blockDim.x) {
-    const int j = idx >> 7, d = idx & 127;
-    const float M = ms.m[j];
-    float acc = 0.f;
-    if (M != -INFINITY)
-      for (int s = 0; s < nstates; ++s) {
-        const float mw = ms.wm[s * 8 + j];
-        if (mw != -INFINITY) acc += state_o(s)[j * kOStride + d] * fast_exp2(mw - M);
-      }
-    merged[j * kOStride + d] = acc;
+  const uint32_t rank = CS > 1 ? cluster_ctarank() : 0;
+  const int dspan = 128 / CS;
+  if (CS > 1 && threadIdx.x < CS * 8) {  // (m, l) of head j to CTA q
+    const int q = threadIdx.x >> 3, j = threadIdx.x & 7;
+    st_shared_cluster(map_shared_rank(smem_u32(ms.recv_m + rank * 8 + j), q), ms.m[j]);
+    st_shared_cluster(map_shared_rank(smem_u32(ms.recv_l + rank * 8 + j), q), ms.l[j]);
   }
-  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * 32; idx += blockDim.x) {
+    const int j = idx >> 5, d = (idx & 31) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < nstates; ++s) {
+      const float wt = ms.wt[s * 8 + j];
+      if (wt != 0.f) {
+        const float4 v = *reinterpret_cast<const float4*>(state_o(s) + j * kOStride + d);
+        acc.x += wt * v.x;
+        acc.y += wt * v.y;
+        acc.z += wt * v.z;
+        acc.w += wt * v.w;
+      }
+    }
+    if (CS == 1) {
+      *reinterpret_cast<float4*>(merged + j * kOStride + d) = acc;
+    } else {
+      const int owner = d / dspan;
+      const uint32_t dst = smem_u32(ms.recv_o + (rank * 8 + j) * dspan + (d - owner * dspan));
+      st_shared_cluster_v4(map_shared_rank(dst, owner), acc);
+    }
+  }
   if (CS == 1) {
+    __syncthreads();
     if (!w.valid) return;
     finish_split(p, w, ms.m, ms.l, merged, kOStride, 0, G, 0, 128, blockIdx.x, w.first_cta, w.nsplit, w.nsplit,
                  ms.flag, ms.scr);
     return;
   }
-  // Cluster merge: after a cluster barrier every CTA reads the CS (m, l) pairs
-  // of each head (one remote load per thread) and merges its slice of dims
-  // from the CS CTAs' `merged` with independent remote loads.
-  cluster_sync();
-  const uint32_t rank = cluster_ctarank();
-  const int dspan = 128 / CS, d0 = (int)rank * dspan;
-  if (threadIdx.x < CS * 8) {
-    const int q = threadIdx.x >> 3, j = threadIdx.x & 7;
-    ms.cw[threadIdx.x] = ld_shared_cluster(map_shared_rank(smem_u32(ms.m + j), q));
-    ms.cwl[threadIdx.x] = ld_shared_cluster(map_shared_rank(smem_u32(ms.l + j), q));
-  }
-  __syncthreads();
+  cluster_sync();  // every push of every CTA of the cluster is visible
+  const int d0 = (int)rank * dspan;
   if (threadIdx.x < 8) {
+    const int j = threadIdx.x;
     float M = -INFINITY;
-    for (int q = 0; q < CS; ++q) M = fmaxf(M, ms.cw[q * 8 + threadIdx.x]);
-    ms.cm[threadIdx.x] = M;
-  }
-  __syncthreads();
-  if (threadIdx.x < CS * 8) {  // weights 2^(m_q - M), zero for empty splits
-    const float M = ms.cm[threadIdx.x & 7], mq = ms.cw[threadIdx.x];
-    const float wq = (M == -INFINITY || mq == -INFINITY) ? 0.f : fast_exp2(mq - M);
-    ms.cw[threadIdx.x] = wq;
-    ms.cwl[threadIdx.x] *= wq;
-  }
-  __syncthreads();
-  if (threadIdx.x < 8) {
+    for (int q = 0; q < CS; ++q) M = fmaxf(M, ms.recv_m[q * 8 + j]);
     float L = 0.f;
-    for (int q = 0; q < CS; ++q) L += ms.cwl[q * 8 + threadIdx.x];
-    ms.cl[threadIdx.x] = L;
+    for (int q = 0; q < CS; ++q) {
+      const float mq = ms.recv_m[q * 8 + j];
+      const float wq = (mq == -INFINITY) ? 0.f : fast_exp2(mq - M);
+      ms.cw[q * 8 + j] = wq;
+      L += wq * ms.recv_l[q * 8 + j];
+    }
+    ms.cm[j] = M;
+    ms.cl[j] = L;
   }
-  for (int idx = threadIdx.x; idx < G * dspan; idx += blockDim.x) {
-    const int j = idx / dspan, d = d0 + idx % dspan;
-    const uint32_t local = smem_u32(merged + j * kOStride + d);
-    float acc = 0.f;
-#pragma unroll 4
-    for (int q = 0; q < CS; ++q) acc += ld_shared_cluster(map_shared_rank(local, q)) * ms.cw[q * 8 + j];
-    cmerged[j * dspan + (d - d0)] = acc;
+  __syncthreads();
+  const int nd4 = dspan / 4;
+  for (int idx = threadIdx.x; idx < G * nd4; idx += blockDim.x) {
+    const int j = idx / nd4, dd = (idx % nd4) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < CS; ++q) {
+      const float wq = ms.cw[q * 8 + j];
+      const float4 v = *reinterpret_cast<const float4*>(ms.recv_o + (q * 8 + j) * dspan + dd);
+      acc.x += wq * v.x;
+      acc.y += wq * v.y;
+      acc.z += wq * v.z;
+      acc.w += wq * v.w;
+    }
+    *reinterpret_cast<float4*>(cmerged + j * dspan + dd) = acc;
   }
-  cluster_sync();  // every remote read is done before any CTA of the cluster exits
+  __syncthreads();
   if (!w.valid) return;
   finish_split(p, w, ms.cm, ms.cl, cmerged, dspan, 0, G, d0, d0 + dspan, (int)(blockIdx.x / CS), w.first_cta / CS,
                w.nsplit / CS, w.nsplit, ms.flag, ms.scr);

@@ -234,3 +234,10 @@ def test_int4_descriptor_rules():
 
 def test_unknown_layout():
     assert status_of(step, layout=9) == ol.OL_ERR_UNSUPPORTED
+
+
+def test_history_stable_bit_keeps_write_access():
+    desc = ol.kv_cache(CACHE, dims=(B, HKV, C, D), dtype=ol.OL_BF16, access=ol.OL_READ_WRITE | ol.OL_HISTORY_STABLE)
+    assert status_of(step, desc=desc) == ol.OL_ERR_INJECTED
+    desc = ol.kv_cache(CACHE, dims=(B, HKV, C, D), dtype=ol.OL_BF16, access=ol.OL_READ_ONLY | ol.OL_HISTORY_STABLE)
+    assert status_of(step, desc=desc) == ol.OL_ERR_READONLY

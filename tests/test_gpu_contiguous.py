@@ -22,11 +22,11 @@ pytestmark = pytest.mark.gpu
 TOL = 2e-3
 
 
-def run_step(case, cache_np, out_dtype=ol.OL_F32, window=-1, scale=0.0):
+def run_step(case, cache_np, out_dtype=ol.OL_F32, window=-1, scale=0.0, access=ol.OL_READ_WRITE):
     w = case.workload
     cache_d = to_dev(cache_np)
     ptr0 = cache_d.data_ptr()
-    desc = ol.kv_cache(cache_d)
+    desc = ol.kv_cache(cache_d, access=access)
     ws, n = workspace(w.batch, w.q_heads, w.kv_heads, w.head_dim)
     out = out_tensor(w.batch, w.q_heads, w.head_dim, out_dtype)
     lens_d = to_dev(case.lens)
@@ -177,3 +177,30 @@ def test_fault_injection_leaves_cache_untouched(monkeypatch):
     torch.cuda.synchronize()
     np.testing.assert_array_equal(to_host(cache_d).view(np.uint8), cache.view(np.uint8))
     assert torch.isnan(out).all()
+
+
+@pytest.mark.parametrize("shape", [SHAPES[0], SHAPES[1], SHAPES[4], SHAPES[8]], ids=lambda s: s[0])
+def test_history_stable_flag_gives_the_same_step(shape):
+    # the caller's promise that the history is stable only moves the first tile
+    # requests before the dependency wait; results are those of a plain step
+    name, dt, B, Hq, Hkv, D, C, lens = shape
+    w = Workload(name, dt, B, Hq, Hkv, D, C, "contiguous", seed=zlib.crc32(name.encode()) % 1000)
+    case = make_case(w, lens=np.array(lens, np.int32))
+    cache = contiguous_cache(case)
+    got_cache, got = run_step(case, cache, access=ol.OL_READ_WRITE | ol.OL_HISTORY_STABLE)
+    ref_cache, want = expected(case, cache)
+    np.testing.assert_array_equal(got_cache.view(np.uint8), ref_cache.view(np.uint8))
+    check_out(got, want, ol.OL_F32)
+
+
+def test_large_batch_reads_lengths_from_device():
+    # more than 160 rows: the kernels map CTAs from lens_dev rather than from the launch
+    rng = np.random.default_rng(21)
+    lens = rng.integers(1, 65, size=200).astype(np.int32)
+    w = Workload("bigb", "bf16", 200, 8, 2, 128, 64, "contiguous", seed=21)
+    case = make_case(w, lens=lens)
+    cache = contiguous_cache(case)
+    got_cache, got = run_step(case, cache)
+    ref_cache, want = expected(case, cache)
+    np.testing.assert_array_equal(got_cache.view(np.uint8), ref_cache.view(np.uint8))
+    check_out(got, want, ol.OL_F32)

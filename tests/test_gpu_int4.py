@@ -41,7 +41,7 @@ def host_planes(dplanes):
     return tuple(to_host(p) for p in dplanes)
 
 
-def desc_of(dplanes, w, mode, access=ol.OL_READ_WRITE):
+def desc_of(dplanes, w, mode, access=ol.OL_READ_WRITE):  # noqa: D401
     return ol.int4_kv(*dplanes, head_dim=w.head_dim, quant_mode=mode, access=access)
 
 
@@ -140,3 +140,21 @@ def test_int4_chained_steps():
         lens = lens + 1
     for g, r in zip(host_planes(dplanes), planes):
         np.testing.assert_array_equal(g, r)
+
+
+def test_int4_history_stable_flag():
+    B, Hq, Hkv, D, C = 3, 32, 8, 128, 300
+    w = Workload("i4flag", "bf16", B, Hq, Hkv, D, C, "int4", seed=36)
+    case = make_case(w, lens=np.array([1, 17, 300], np.int32))
+    planes = oracle_planes(case, O.Q_DYNAMIC)
+    dplanes = dev_planes(planes)
+    ws, n = workspace(B, Hq, Hkv, D)
+    out = out_tensor(B, Hq, D, ol.OL_F32)
+    desc = desc_of(dplanes, w, O.Q_DYNAMIC, access=ol.OL_READ_WRITE | ol.OL_HISTORY_STABLE)
+    ol.ol_decode_step(ol.OL_LAYOUT_INT4, desc, dplanes[0], to_dev(case.q), Hq, to_dev(case.new_kv), case.lens,
+                      to_dev(case.lens), 0.0, -1, out, ol.OL_F32, ws, n)
+    torch.cuda.synchronize()
+    O.int4_append(*planes, case.new_kv, case.lens - 1)
+    for g, r in zip(host_planes(dplanes), planes):
+        np.testing.assert_array_equal(g, r)
+    check_out(out_as_f64(out), O.int4_attention(case.q, *planes, case.lens, cur_kv=case.new_kv), ol.OL_F32)

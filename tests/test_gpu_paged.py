@@ -36,12 +36,12 @@ def paged_workload(name, dt, B, Hq, Hkv, D, P, S, M):
                     page_size=S, num_pages=P, lens_range=(1, M * S))
 
 
-def run(case, pool, table, out_dtype=ol.OL_F32, window=-1, step=True):
+def run(case, pool, table, out_dtype=ol.OL_F32, window=-1, step=True, flags=0):
     w = case.workload
     pool_d = to_dev(pool)
     ptr0 = pool_d.data_ptr()
     bt_d = to_dev(table)
-    desc = ol.paged_kv(pool_d, bt_d, table, access=ol.OL_READ_WRITE if step else ol.OL_READ_ONLY)
+    desc = ol.paged_kv(pool_d, bt_d, table, access=(ol.OL_READ_WRITE if step else ol.OL_READ_ONLY) | flags)
     ws, n = workspace(w.batch, w.q_heads, w.kv_heads, w.head_dim)
     out = out_tensor(w.batch, w.q_heads, w.head_dim, out_dtype)
     lens_d = to_dev(case.lens)
@@ -126,3 +126,15 @@ def test_paged_cache_update_standalone():
     ref = pool.copy()
     O.paged_update(ref, table, vals, pos)
     np.testing.assert_array_equal(to_host(pool_d).view(np.uint8), ref.view(np.uint8))
+
+
+def test_paged_history_stable_flag():
+    name, dt, B, Hq, Hkv, D, P, S, M, lens = SHAPES[0]
+    w = paged_workload(name, dt, B, Hq, Hkv, D, P, S, M)
+    case = make_case(w, lens=np.array(lens, np.int32))
+    pool, table = build_pool(case)
+    got_pool, got = run(case, pool, table, flags=ol.OL_HISTORY_STABLE)
+    ref = pool.copy()
+    O.paged_update(ref, table, case.new_kv, case.lens - 1)
+    np.testing.assert_array_equal(got_pool.view(np.uint8), ref.view(np.uint8))
+    check_out(got, O.paged_attention(case.q, ref, table, case.lens), ol.OL_F32)
