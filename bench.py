@@ -141,6 +141,22 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ------------------------------------------------------------- multi-rank
+
+def combine_ranks(ms_total, steps, bytes_per_step, world, dist=None, device="cpu"):
+    """Whole-job result of a weak-scaling run: every rank processes its own copy
+    of the workload (independent rows: no collective on the data path); the job
+    time is the slowest rank's (max over ranks) and the job moves world x the
+    per-rank bytes. Returns (ms_per_step, whole-job GB/s)."""
+    if dist is not None and world > 1:
+        import torch
+        t = torch.tensor([ms_total], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_per_step = ms_total / steps
+    return ms_per_step, bytes_per_step * world / (ms_per_step * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------- ours
 
 def to_dev(a, dev):
@@ -304,14 +320,8 @@ def run_ours(args, rank, world, dist):
         if dist is not None:
             dist.barrier()
     ms = e0.elapsed_time(e1)
-    if dist is not None:
-        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms_per_step, gbs = combine_ranks(ms, K, s.bytes_per_step, world, dist, device=dev)
     status = ol.ol_workspace_status(s.ws, stream=stream)
-    ms_per_step = ms / K
-    total_bytes = s.bytes_per_step * world
-    gbs = total_bytes / (ms_per_step * 1e-3) / 1e9
     peak, peak_src = measured_peaks()
     result = {
         "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": K,

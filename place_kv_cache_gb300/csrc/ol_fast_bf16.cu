@@ -35,6 +35,8 @@ struct FastLayout {
   static constexpr int kMisc = 256 + NWARPS * 8 * 4 * 2 + 8 * 4 * 6 + 2 * 16 * 8 * 4 + 16;
   static constexpr int kRecv = (1024 + 2 * 128 + 8 * 64) * 4;  // cluster receive buffers + cmerged
   static constexpr int kTotal = 1024 /* alignment slack */ + kStages + kRecv + kBars + kMisc;
+  // CTAs per SM that shared memory allows (1 KB per CTA is reserved by the driver)
+  static constexpr int kPerSm = (228 * 1024) / (kTotal + 1024) > 0 ? (228 * 1024) / (kTotal + 1024) : 1;
   static_assert(STAGES >= 2, "the merged O lives in warp 0's second stage");
   static_assert(8 * kOStride * 4 <= kStageBytes, "the CTA state fits one stage");
 };
@@ -51,7 +53,7 @@ __device__ __forceinline__ int tile_row(const AttnParams& p, bool paged, int pla
 }
 
 template <int NWARPS, int STAGES, bool PAGED>
-__global__ void __launch_bounds__(NWARPS * 32)
+__global__ void __launch_bounds__(NWARPS * 32, FastLayout<NWARPS, STAGES>::kPerSm)
     fast_bf16_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ AttnParams p) {
   using L = FastLayout<NWARPS, STAGES>;
   extern __shared__ uint8_t smem_raw[];
@@ -234,15 +236,19 @@ __global__ void __launch_bounds__(NWARPS * 32)
     const float p10 = fast_exp2(s10 - b0), p11 = fast_exp2(s11 - b1);
     l_run0 = l_run0 * al0 + (p00 + p10);
     l_run1 = l_run1 * al1 + (p01 + p11);
+    // rescale O only when some lane's running maximum moved (otherwise every
+    // factor is exactly 1)
+    if (__any_sync(0xffffffffu, mn0 != m_run0 || mn1 != m_run1)) {
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        o[mt][0] *= al0;
+        o[mt][1] *= al1;
+        o[mt][2] *= al0;
+        o[mt][3] *= al1;
+      }
+    }
     m_run0 = mn0;
     m_run1 = mn1;
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      o[mt][0] *= al0;
-      o[mt][1] *= al1;
-      o[mt][2] *= al0;
-      o[mt][3] *= al1;
-    }
     // P^T as the B operand (16 tokens x 8 heads), carried as bf16 hi + bf16 lo
     // (p - hi) so the P.V product keeps ~16 significant bits of each weight
     const uint32_t h0 = pack_bf16x2(p00, p01), h1 = pack_bf16x2(p10, p11);

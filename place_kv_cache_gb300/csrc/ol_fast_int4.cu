@@ -43,6 +43,7 @@ struct Int4Layout {
   static constexpr int kBars = NWARPS * STAGES * 8;
   static constexpr int kMisc = 256 + (NWARPS + 1) * 8 * 4 * 2 + 8 * 4 * 6 + 16 * 4 + 2 * 16 * 8 * 4 + 16;
   static constexpr int kTotal = 1024 + kStages + kExtra + kBars + kMisc;
+  static constexpr int kPerSm = (228 * 1024) / (kTotal + 1024) > 0 ? (228 * 1024) / (kTotal + 1024) : 1;
   static_assert(STAGES * kStage >= 8 * kOStride * 4, "a warp's state fits its stages");
 };
 
@@ -60,7 +61,7 @@ __device__ __forceinline__ int swz64(int r, int x) {
 }
 
 template <int NWARPS, int STAGES>
-__global__ void __launch_bounds__(NWARPS * 32)
+__global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerSm)
     fast_int4_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ AttnParams p) {
   using L = Int4Layout<NWARPS, STAGES>;
   extern __shared__ uint8_t smem_raw[];
@@ -230,15 +231,19 @@ __global__ void __launch_bounds__(NWARPS * 32)
     const float p10 = fast_exp2(s10 - b0), p11 = fast_exp2(s11 - b1);
     l_run0 = l_run0 * al0 + (p00 + p10);
     l_run1 = l_run1 * al1 + (p01 + p11);
+    // rescale O only when some lane's running maximum moved (otherwise every
+    // factor is exactly 1)
+    if (__any_sync(0xffffffffu, mn0 != m_run0 || mn1 != m_run1)) {
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        o[mt][0] *= al0;
+        o[mt][1] *= al1;
+        o[mt][2] *= al0;
+        o[mt][3] *= al1;
+      }
+    }
     m_run0 = mn0;
     m_run1 = mn1;
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      o[mt][0] *= al0;
-      o[mt][1] *= al1;
-      o[mt][2] *= al0;
-      o[mt][3] *= al1;
-    }
 
     // ---- O^T += V^T P^T, block by block
     const uint2 sva = lds_v2(vsc + 8 * ra);
