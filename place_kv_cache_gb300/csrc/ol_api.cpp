@@ -141,6 +141,7 @@ void plan_fast(AttnParams& p, const int32_t* lens_host, int sms) {
   const int warps = int4 ? fast_int4_warps(p.variant) : fast_bf16_warps(p.variant);
   int per_sm = (228 * 1024) / smem;
   if (per_sm > 64 / warps) per_sm = 64 / warps;
+  if (int4 && per_sm > 16 / warps) per_sm = 16 / warps;  // 128 registers per thread
   if (per_sm < 1) per_sm = 1;
   const long long slots = (long long)sms * per_sm;
   if (units >= sms || units == 0) {

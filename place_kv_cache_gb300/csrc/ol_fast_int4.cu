@@ -5,18 +5,25 @@
 // per byte), one (scale, zero point) per block of 32 dims.
 //
 // Same decomposition as the bf16 kernel (one CTA per (row, kv head, split),
-// per-warp rings of 16-token tiles, shared merge). Per tile a warp receives
-// 2 x 1 KB of codes by TMA (SWIZZLE_64B, 64-byte rows: conflict-free reads)
-// and 2 x 128 B of scales and 2 x 32 B of zero points by bulk copies.
-// Dequantization happens in registers: a nibble c becomes the exact bf16
-// value 128 + c with one mask-and-or per pair.
-//   S^T: one accumulator per 32-dim block b, fed the exact bf16 values
-//        (128 + c) - (128 + zp_K) = c - zp_K; then s = sum_b scale_K[t,b] * acc_b
-//   O^T: V^T as exact bf16 (c - zp_V) per token, the V scale folded into
-//        P^T per block, P^T carried as bf16 hi + lo.
+// warps over 16-token tiles, shared merge). A ring of stages holds NWARPS
+// consecutive tiles each, one per warp; a stage arrives by three 3-D tensor
+// copies that each cover the K and the V plane: codes (SWIZZLE_64B, 64-byte
+// rows: conflict-free reads), scales and zero points. The last warp to finish
+// with a stage issues its refill.
+// Dequantization happens in registers and is exact:
+//   S^T: one fp32 accumulator per 32-dim block b. The codes are fp16
+//        operands as they lie in memory (a masked nibble is the subnormal
+//        c * 2^-24, or 16c * 2^-24 one nibble up, which q absorbs as q / 16);
+//        one more k-step adds zp_K * (-sum of the block's q). Then
+//        s = sum_b scale_K[t,b] * acc_b.
+//   O^T: V^T as exact bf16 (128 + c) - (128 + zp_V) per token, the V scale
+//        folded into P^T per block, P^T carried as bf16 hi + lo.
 // The token being appended (fused step) takes part uncompressed from new_kv as
 // one extra merge state, and is quantized into the cache by the same CTA.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <type_traits>
 
 #include "ol_merge.cuh"
 
@@ -24,27 +31,37 @@ namespace ol {
 namespace {
 
 constexpr int kTok = 16;
-constexpr int kCodesBytes = kTok * 64;    // one plane's codes of a tile
-constexpr int kScaleBytes = kTok * 8;     // 4 fp16 per row
-constexpr int kZpBytes = kTok * 2;        // 4 nibbles per row
-constexpr int kTileTx = 2 * (kCodesBytes + kScaleBytes + kZpBytes);  // 2368
-constexpr int kStage = 3072;              // 1024-aligned stage stride
-constexpr int kOffVc = 1024, kOffSk = 2048, kOffSv = 2048 + 128, kOffZk = 2304, kOffZv = 2336;
 constexpr uint32_t kMagic = 0x43004300u;  // bf16 pair (128, 128)
+constexpr uint32_t kLoNib = 0x000F000Fu;  // nibble in bits 0..3 of both 16-bit halves
+constexpr uint32_t kHiNib = 0x00F000F0u;  // nibble in bits 4..7 of both halves
+constexpr int kStateBytes = 8 * kOStride * 4;  // one warp's [8][kOStride] fp32 state
+
+// A stage: NWARPS tiles of 16 tokens. Byte offsets (NW = NWARPS):
+//   K codes [16NW][64] @0, V codes @1024NW, K scales [16NW][4] fp16 @2048NW,
+//   V scales @2176NW, K zero points [16NW][2] @2304NW, V zero points @2336NW.
+template <int NW>
+struct Int4Stage {
+  static constexpr int kCodes = 1024 * NW;  // one plane's codes
+  static constexpr int kOffSk = 2048 * NW, kOffSv = 2176 * NW, kOffZk = 2304 * NW, kOffZv = 2336 * NW;
+  static constexpr int kTx = 2368 * NW;                   // bytes the three copies deliver
+  static constexpr int kBytes = (kTx + 1023) / 1024 * 1024;  // 1024-aligned stride
+};
 
 template <int NWARPS, int STAGES>
 struct Int4Layout {
-  static constexpr int kStages = NWARPS * STAGES * kStage;
+  static constexpr int kStages = STAGES * Int4Stage<NWARPS>::kBytes;
   // extra state O, then one region that is either the CTA-merged state (no
   // cluster) or the cluster receive buffers + cmerged (cluster): never both
-  static constexpr int kUnion = (1024 + 2 * 128 + 8 * 64) * 4 > 8 * kOStride * 4 ? (1024 + 2 * 128 + 8 * 64) * 4
-                                                                               : 8 * kOStride * 4;
-  static constexpr int kExtra = 8 * kOStride * 4 + kUnion;
-  static constexpr int kBars = NWARPS * STAGES * 8;
+  static constexpr int kUnion = (1024 + 2 * 128 + 8 * 64) * 4 > kStateBytes ? (1024 + 2 * 128 + 8 * 64) * 4
+                                                                         : kStateBytes;
+  static constexpr int kExtra = kStateBytes + kUnion;
+  static constexpr int kBars = STAGES * 8 + STAGES * 4;  // full barriers, release counters
   static constexpr int kMisc = 256 + (NWARPS + 1) * 8 * 4 * 2 + 8 * 4 * 6 + 16 * 4 + 2 * 16 * 8 * 4 + 16;
-  static constexpr int kTotal = 1024 + kStages + kExtra + kBars + kMisc;
-  static constexpr int kPerSm = (228 * 1024) / (kTotal + 1024) > 0 ? (228 * 1024) / (kTotal + 1024) : 1;
-  static_assert(STAGES * kStage >= 8 * kOStride * 4, "a warp's state fits its stages");
+  static constexpr int kTotal = 1024 + kStages + kExtra + (kBars + 15) / 16 * 16 + kMisc;
+  // CTAs per SM: shared memory, and 128 registers per thread
+  static constexpr int kBySmem = (228 * 1024) / (kTotal + 1024) > 0 ? (228 * 1024) / (kTotal + 1024) : 1;
+  static constexpr int kPerSm = kBySmem < 16 / NWARPS ? kBySmem : 16 / NWARPS;
+  static_assert(kStages >= NWARPS * kStateBytes, "the warps' states fit in the stages");
 };
 
 __device__ __forceinline__ uint32_t code_pair(uint32_t w, int shift) {
@@ -55,6 +72,13 @@ __device__ __forceinline__ uint32_t hsub2_bf16(uint32_t a, uint32_t b) {
   __nv_bfloat162 r = __hsub2(x, y);
   return *reinterpret_cast<uint32_t*>(&r);
 }
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ float2 half2_bits_to_float2(uint32_t x) {
+  return __half22float2(*reinterpret_cast<__half2*>(&x));
+}
 // byte offset of logical byte x of 64-byte row r in a SWIZZLE_64B tile
 __device__ __forceinline__ int swz64(int r, int x) {
   return r * 64 + ((((x >> 4) ^ (r >> 1)) & 3) << 4) + (x & 15);
@@ -62,8 +86,10 @@ __device__ __forceinline__ int swz64(int r, int x) {
 
 template <int NWARPS, int STAGES>
 __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerSm)
-    fast_int4_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ AttnParams p) {
+    fast_int4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
+                     const __grid_constant__ CUtensorMap tm_zps, const __grid_constant__ AttnParams p) {
   using L = Int4Layout<NWARPS, STAGES>;
+  using S = Int4Stage<NWARPS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* stages = smem;
@@ -72,8 +98,9 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
   float* recv = merged;                    // cluster: receive buffers, then cmerged
   float* cmerged = recv + 1024 + 256;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kStages + L::kExtra);
-  Work* sw = reinterpret_cast<Work*>(smem + L::kStages + L::kExtra + L::kBars);
-  float* misc = reinterpret_cast<float*>(smem + L::kStages + L::kExtra + L::kBars + 256);
+  int* freed = reinterpret_cast<int*>(smem + L::kStages + L::kExtra + STAGES * 8);  // warps done per stage
+  Work* sw = reinterpret_cast<Work*>(smem + L::kStages + L::kExtra + (L::kBars + 15) / 16 * 16);
+  float* misc = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(sw) + 256);
   MergeScratch ms;
   ms.wm = misc;                        // [NWARPS + 1][8]
   ms.wl = ms.wm + (NWARPS + 1) * 8;    // [NWARPS + 1][8]
@@ -91,10 +118,15 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int CS = p.cluster;
-  if (threadIdx.x == 0) prefetch_tensormap(&tmap);
-  const uint32_t bar0 = smem_u32(bars + warp * STAGES);
-  if (lane == 0) {
-    for (int st = 0; st < STAGES; ++st) mbar_init(bar0 + 8 * st, 1);
+  const uint32_t bar0 = smem_u32(bars);
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&tm_codes);
+    prefetch_tensormap(&tm_scales);
+    prefetch_tensormap(&tm_zps);
+    for (int st = 0; st < STAGES; ++st) {
+      mbar_init(bar0 + 8 * st, 1);
+      freed[st] = 0;
+    }
     fence_mbar_init();
   }
   if (!p.inline_lens) pdl_wait();
@@ -114,52 +146,104 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
 
   const int G = p.group;
   const int C = p.capacity;
-  const int nsub = w.valid ? (w.t_end - w.t_begin + kTok - 1) / kTok : 0;
-  const int my_n = nsub > warp ? (nsub - warp + NWARPS - 1) / NWARPS : 0;
-  uint8_t* my_stages = stages + warp * STAGES * kStage;
+  const int nsub = w.valid ? (w.t_end - w.t_begin + kTok - 1) / kTok : 0;  // tiles of the CTA
+  const int nstage = (nsub + NWARPS - 1) / NWARPS;                              // stages of the CTA
   const uint64_t pol = policy_evict_first();
-  const int rowK0 = ((0 * p.batch + w.b) * p.kv_heads + w.g) * C;  // row of token 0, K plane
-  const int rowV0 = ((1 * p.batch + w.b) * p.kv_heads + w.g) * C;
+  const int row0 = (w.b * p.kv_heads + w.g) * C;  // row of token 0 within a plane
+  const int rowK0 = row0, rowV0 = p.batch * p.kv_heads * C + row0;
 
-  auto issue = [&](int i) {
-    const int st = i % STAGES;
-    const int t0 = w.t_begin + (warp + i * NWARPS) * kTok;
-    uint8_t* dst = my_stages + st * kStage;
+  // Stage j (tiles NWARPS*j ..) into ring slot j % STAGES: codes, scales and
+  // zero points of tokens t .. t + 16*NWARPS - 1 of both planes. Boxes that run
+  // past the CTA's range read tokens nobody uses (or the fill value past the
+  // end of the arrays).
+  auto issue = [&](int j) {
+    const int st = j % STAGES;
+    const uint32_t dst = smem_u32(stages + st * S::kBytes);
     const uint32_t bar = bar0 + 8 * st;
-    mbar_arrive_expect_tx(bar, kTileTx);
-    tma_load_2d(smem_u32(dst), &tmap, 0, rowK0 + t0, bar, pol);
-    tma_load_2d(smem_u32(dst + kOffVc), &tmap, 0, rowV0 + t0, bar, pol);
-    bulk_load(smem_u32(dst + kOffSk), p.scales + (size_t)(rowK0 + t0) * 4, kScaleBytes, bar, pol);
-    bulk_load(smem_u32(dst + kOffSv), p.scales + (size_t)(rowV0 + t0) * 4, kScaleBytes, bar, pol);
-    bulk_load(smem_u32(dst + kOffZk), p.zps + (size_t)(rowK0 + t0) * 2, kZpBytes, bar, pol);
-    bulk_load(smem_u32(dst + kOffZv), p.zps + (size_t)(rowV0 + t0) * 2, kZpBytes, bar, pol);
+    const int r = row0 + w.t_begin + j * NWARPS * kTok;  // multiple of 16
+    mbar_arrive_expect_tx(bar, S::kTx);
+    tma_load_3d(dst, &tm_codes, 0, r, 0, bar, pol);
+    tma_load_3d(dst + S::kOffSk, &tm_scales, 0, r >> 1, 0, bar, pol);
+    tma_load_3d(dst + S::kOffZk, &tm_zps, 0, r >> 3, 0, bar, pol);
   };
-  const int pre = my_n < STAGES ? my_n : STAGES;
-  if (p.early && lane == 0)
-    for (int i = 0; i < pre; ++i) issue(i);
+  const int pre = nstage < STAGES ? nstage : STAGES;
+  if (p.early && threadIdx.x == 0)
+    for (int j = 0; j < pre; ++j) issue(j);
   if (p.inline_lens) pdl_wait();
   pdl_launch_dependents();
-  if (!p.early && lane == 0)
-    for (int i = 0; i < pre; ++i) issue(i);
+  if (!p.early && threadIdx.x == 0)
+    for (int j = 0; j < pre; ++j) issue(j);
 
-  // q as the B operand of the four blocks' k-steps, in the dims order of the
-  // code words: lane (c, n) holds q[n][32b + 8c .. +7] as e0..e7;
-  // k-step (b, hh): b0 = {e(2hh), e(2hh+4)}, b1 = {e(2hh+1), e(2hh+5)}.
+  // K side operands. The codes enter the tensor cores as fp16 subnormals: a
+  // 16-bit lane holding c in bits 0..3 is c * 2^-24, in bits 4..7 it is
+  // 16c * 2^-24, both exact, so one mask yields two operands. q is converted
+  // to fp16 scaled by 2^eq, with eq chosen to put max |q| in [2^9, 2^10)
+  // (exact: bf16 values are fp16 values times a power of two, unless tiny).
+  // Lane (c, n) holds q[n][32b + 8c + i], i = 0..7, in the nibble order of a
+  // code word:  k-step 0 of block b: b0 = (i0, i4), b1 = (i1, i5) / 16,
+  //             k-step 1:            b0 = (i2, i6), b1 = (i3, i7) / 16.
+  // A third k-step per block adds zp * (-Q_b), Q_b the sum of the block's
+  // fp16 q carried as two fp16 (rows 0 and 1 of lane c = 0).
   const int c = lane & 3, n = lane >> 2;
-  uint32_t qf[4][2][2];
+  uint32_t qf[4][2][2], qz[4];
+  float sfac;  // converts an accumulator (units 2^-24 * 2^eq) to the exp2 domain
   {
     const bool live = n < G && w.valid;
     const uint16_t* qp = reinterpret_cast<const uint16_t*>(p.q) +
                          ((size_t)w.b * p.q_heads + (size_t)w.g * G + (n < G ? n : 0)) * 128;
+    float qv[4][8];
+    float mx = 0.f;
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      uint4 v = live ? __ldg(reinterpret_cast<const uint4*>(qp + 32 * b + 8 * c)) : make_uint4(0, 0, 0, 0);
-      qf[b][0][0] = __byte_perm(v.x, v.z, 0x5410);
-      qf[b][0][1] = __byte_perm(v.x, v.z, 0x7632);
-      qf[b][1][0] = __byte_perm(v.y, v.w, 0x5410);
-      qf[b][1][1] = __byte_perm(v.y, v.w, 0x7632);
+      const uint4 v = live ? __ldg(reinterpret_cast<const uint4*>(qp + 32 * b + 8 * c)) : make_uint4(0, 0, 0, 0);
+      const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        qv[b][2 * k] = __uint_as_float(wd[k] << 16);
+        qv[b][2 * k + 1] = __uint_as_float(wd[k] & 0xffff0000u);
+        mx = fmaxf(mx, fmaxf(fabsf(qv[b][2 * k]), fabsf(qv[b][2 * k + 1])));
+      }
+    }
+    mx = warp_max(mx);
+    int eq = 0;
+    if (mx > 0.f && mx <= 3.0e38f) {
+      int e2;
+      frexpf(mx, &e2);  // mx = f * 2^e2, f in [0.5, 1)
+      eq = min(100, max(-100, 10 - e2));
+    }
+    const float qscale = ldexpf(1.f, eq);
+    sfac = ldexpf(p.scale_log2, 24 - eq);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      float qh[8];
+      float qs = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        qh[i] = __half2float(__float2half_rn(qv[b][i] * qscale));
+        qs += qh[i];
+      }
+      qf[b][0][0] = pack_f16x2(qh[0], qh[4]);
+      qf[b][0][1] = pack_f16x2(qh[1] * 0.0625f, qh[5] * 0.0625f);
+      qf[b][1][0] = pack_f16x2(qh[2], qh[6]);
+      qf[b][1][1] = pack_f16x2(qh[3] * 0.0625f, qh[7] * 0.0625f);
+      qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+      qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+      const float qhi = __half2float(__float2half_rn(qs));
+      qz[b] = c == 0 ? pack_f16x2(-qhi, -(qs - qhi)) : 0u;
     }
   }
+  // loop-invariant shared-memory offsets of the lane's reads from a stage:
+  // K word of token n, block b (token n + 8: +512); V half-words of tokens
+  // 2c, 2c+1, 2c+8, 2c+9 at dims 32b + 4n .. +3 (+0, +64, +512, +576); the
+  // warp's tile is rows 16*warp .. +15 of each plane (the 64-byte swizzle
+  // pattern repeats every 8 rows, so a tile's offsets do not depend on warp)
+  uint32_t koff[4], voff[4];
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    koff[b] = 1024 * warp + swz64(n, 16 * b + 4 * c);
+    voff[b] = S::kCodes + 1024 * warp + swz64(2 * c, 16 * b + 2 * n);
+  }
+
   float o[8][4];
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
@@ -167,55 +251,48 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
   const int codes_hi = p.cur_from_new ? w.hi - 1 : w.hi;  // tokens below this come from the codes
   const int t_stop = min(w.t_end, codes_hi);
 
-  for (int i = 0; i < my_n; ++i) {
-    const int st = i % STAGES;
-    if (!mbar_wait_bounded(bar0 + 8 * st, (i / STAGES) & 1)) {
-      if (lane == 0) set_status(p.status, OL_DEVICE_GUARD);
-      break;
+  // One 16-token tile in stage base sg. FULL: every token of the tile is
+  // visible (no masking of scores or scales).
+  auto tile = [&](const uint32_t sg, const int t0, auto full_tag) {
+    constexpr bool FULL = decltype(full_tag)::value;
+    const uint32_t ksc = sg + S::kOffSk + 128 * warp, vsc = sg + S::kOffSv + 128 * warp;
+    const uint32_t kz = sg + S::kOffZk + 32 * warp, vz = sg + S::kOffZv + 32 * warp;
+    bool va = true, vb = true;  // the lane's S^T rows (tokens n, n + 8) are visible
+    if (!FULL) {
+      va = t0 + n >= w.lo && t0 + n < t_stop;
+      vb = t0 + n + 8 >= w.lo && t0 + n + 8 < t_stop;
     }
-    const int t0 = w.t_begin + (warp + i * NWARPS) * kTok;
-    const uint32_t sg = smem_u32(my_stages + st * kStage);
-    const uint32_t kc = sg, vc = sg + kOffVc, ksc = sg + kOffSk, vsc = sg + kOffSv, kz = sg + kOffZk, vz = sg + kOffZv;
 
-    const int ra = n, rb = n + 8;  // the lane's S^T rows (tokens) in this tile
-    const bool va = t0 + ra >= w.lo && t0 + ra < t_stop;
-    const bool vb = t0 + rb >= w.lo && t0 + rb < t_stop;
-
-    // ---- S^T = K q^T, one accumulator per 32-dim block, A = exact (c - zp)
-    // zero points of rows ra / rb, duplicated in both 16-bit halves
-    const uint32_t za = lds_u16(kz + 2 * ra), zb = lds_u16(kz + 2 * rb);
-    const uint32_t zda = za | (za << 16), zdb = zb | (zb << 16);
+    // ---- S^T = K q^T, one accumulator per 32-dim block
+    const uint32_t zda = lds_u16(kz + 2 * n) * 0x10001u, zdb = lds_u16(kz + 2 * n + 16) * 0x10001u;
     float sacc[4][4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       sacc[b][0] = sacc[b][1] = sacc[b][2] = sacc[b][3] = 0.f;
-      const uint32_t wa = lds_u32(kc + swz64(ra, 16 * b + 4 * c));
-      const uint32_t wb = lds_u32(kc + swz64(rb, 16 * b + 4 * c));
-      const uint32_t zpa = code_pair(zda, 4 * b), zpb = code_pair(zdb, 4 * b);  // (128 + zp, 128 + zp)
-      mma_bf16_16816(sacc[b], hsub2_bf16(code_pair(wa, 0), zpa), hsub2_bf16(code_pair(wb, 0), zpb),
-                     hsub2_bf16(code_pair(wa, 4), zpa), hsub2_bf16(code_pair(wb, 4), zpb), qf[b][0][0],
-                     qf[b][0][1]);
-      mma_bf16_16816(sacc[b], hsub2_bf16(code_pair(wa, 8), zpa), hsub2_bf16(code_pair(wb, 8), zpb),
-                     hsub2_bf16(code_pair(wa, 12), zpa), hsub2_bf16(code_pair(wb, 12), zpb), qf[b][1][0],
-                     qf[b][1][1]);
+      const uint32_t wa = lds_u32(sg + koff[b]), wb = lds_u32(sg + koff[b] + 512);
+      const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
+      mma_f16_16816(sacc[b], wa & kLoNib, wb & kLoNib, wa & kHiNib, wb & kHiNib, qf[b][0][0], qf[b][0][1]);
+      mma_f16_16816(sacc[b], wa8 & kLoNib, wb8 & kLoNib, wa8 & kHiNib, wb8 & kHiNib, qf[b][1][0], qf[b][1][1]);
+      const uint32_t za = (zda >> (4 * b)) & kLoNib, zb = (zdb >> (4 * b)) & kLoNib;
+      mma_f16_16816(sacc[b], za, zb, za, zb, qz[b], 0u);
     }
-    const uint2 ska = lds_v2(ksc + 8 * ra);
-    const uint2 skb = lds_v2(ksc + 8 * rb);
-    float s00 = 0.f, s01 = 0.f, s10 = 0.f, s11 = 0.f;
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const uint32_t pa = b < 2 ? ska.x : ska.y, pb = b < 2 ? skb.x : skb.y;
-      const float sca = fp16_bits_to_float((b & 1) ? (pa >> 16) : (pa & 0xffff));
-      const float scb = fp16_bits_to_float((b & 1) ? (pb >> 16) : (pb & 0xffff));
-      s00 += sca * sacc[b][0];
-      s01 += sca * sacc[b][1];
-      s10 += scb * sacc[b][2];
-      s11 += scb * sacc[b][3];
+    const uint2 ska = lds_v2(ksc + 8 * n), skb = lds_v2(ksc + 8 * n + 64);
+    const float2 ka01 = half2_bits_to_float2(ska.x), ka23 = half2_bits_to_float2(ska.y);
+    const float2 kb01 = half2_bits_to_float2(skb.x), kb23 = half2_bits_to_float2(skb.y);
+    float s00 = ka01.x * sacc[0][0] + ka01.y * sacc[1][0] + ka23.x * sacc[2][0] + ka23.y * sacc[3][0];
+    float s01 = ka01.x * sacc[0][1] + ka01.y * sacc[1][1] + ka23.x * sacc[2][1] + ka23.y * sacc[3][1];
+    float s10 = kb01.x * sacc[0][2] + kb01.y * sacc[1][2] + kb23.x * sacc[2][2] + kb23.y * sacc[3][2];
+    float s11 = kb01.x * sacc[0][3] + kb01.y * sacc[1][3] + kb23.x * sacc[2][3] + kb23.y * sacc[3][3];
+    s00 *= sfac;
+    s01 *= sfac;
+    s10 *= sfac;
+    s11 *= sfac;
+    if (!FULL) {
+      s00 = va ? s00 : -INFINITY;
+      s01 = va ? s01 : -INFINITY;
+      s10 = vb ? s10 : -INFINITY;
+      s11 = vb ? s11 : -INFINITY;
     }
-    s00 = va ? s00 * p.scale_log2 : -INFINITY;
-    s01 = va ? s01 * p.scale_log2 : -INFINITY;
-    s10 = vb ? s10 * p.scale_log2 : -INFINITY;
-    s11 = vb ? s11 * p.scale_log2 : -INFINITY;
 
     // ---- online softmax (exp2 domain)
     float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
@@ -226,14 +303,14 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
     }
     const float mn0 = fmaxf(m_run0, mx0), mn1 = fmaxf(m_run1, mx1);
     const float b0 = mn0 == -INFINITY ? 0.f : mn0, b1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float al0 = fast_exp2(m_run0 - b0), al1 = fast_exp2(m_run1 - b1);
     const float p00 = fast_exp2(s00 - b0), p01 = fast_exp2(s01 - b1);
     const float p10 = fast_exp2(s10 - b0), p11 = fast_exp2(s11 - b1);
-    l_run0 = l_run0 * al0 + (p00 + p10);
-    l_run1 = l_run1 * al1 + (p01 + p11);
     // rescale O only when some lane's running maximum moved (otherwise every
     // factor is exactly 1)
     if (__any_sync(0xffffffffu, mn0 != m_run0 || mn1 != m_run1)) {
+      const float al0 = fast_exp2(m_run0 - b0), al1 = fast_exp2(m_run1 - b1);
+      l_run0 *= al0;
+      l_run1 *= al1;
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         o[mt][0] *= al0;
@@ -242,31 +319,36 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
         o[mt][3] *= al1;
       }
     }
+    l_run0 += p00 + p10;
+    l_run1 += p01 + p11;
     m_run0 = mn0;
     m_run1 = mn1;
 
-    // ---- O^T += V^T P^T, block by block
-    const uint2 sva = lds_v2(vsc + 8 * ra);
-    const uint2 svb = lds_v2(vsc + 8 * rb);
-    const int r0 = 2 * c, r1 = 2 * c + 1, r8 = 2 * c + 8, r9 = 2 * c + 9;  // V^T columns (tokens) of this lane
-    // zero points of those tokens: tokens (r0, r1) in the two 16-bit halves, likewise (r8, r9)
-    const uint32_t zv01 = lds_u16(vz + 2 * r0) | (lds_u16(vz + 2 * r1) << 16);
-    const uint32_t zv89 = lds_u16(vz + 2 * r8) | (lds_u16(vz + 2 * r9) << 16);
+    // ---- O^T += V^T P^T, block by block: A = exact bf16 (c - zp_V), the V
+    // scale folded into P^T, P^T carried as bf16 hi + lo
+    const uint2 sva = lds_v2(vsc + 8 * n), svb = lds_v2(vsc + 8 * n + 64);
+    float2 va01 = half2_bits_to_float2(sva.x), va23 = half2_bits_to_float2(sva.y);
+    float2 vb01 = half2_bits_to_float2(svb.x), vb23 = half2_bits_to_float2(svb.y);
+    if (!FULL) {  // a hidden token's scale may be anything: its weight is exactly 0
+      if (!va) va01 = va23 = make_float2(0.f, 0.f);
+      if (!vb) vb01 = vb23 = make_float2(0.f, 0.f);
+    }
+    // zero points of the lane's V^T columns: tokens (2c, 2c+1) and (2c+8, 2c+9)
+    // in the two 16-bit halves
+    const uint32_t zv01 = lds_u32(vz + 4 * c), zv89 = lds_u32(vz + 4 * c + 16);
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      const uint32_t pa = b < 2 ? sva.x : sva.y, pb = b < 2 ? svb.x : svb.y;
-      const float sca = va ? fp16_bits_to_float((b & 1) ? (pa >> 16) : (pa & 0xffff)) : 0.f;
-      const float scb = vb ? fp16_bits_to_float((b & 1) ? (pb >> 16) : (pb & 0xffff)) : 0.f;
+      const float sca = b == 0 ? va01.x : b == 1 ? va01.y : b == 2 ? va23.x : va23.y;
+      const float scb = b == 0 ? vb01.x : b == 1 ? vb01.y : b == 2 ? vb23.x : vb23.y;
       const float q00 = p00 * sca, q01 = p01 * sca, q10 = p10 * scb, q11 = p11 * scb;
       const uint32_t h0 = pack_bf16x2(q00, q01), h1 = pack_bf16x2(q10, q11);
       const uint32_t l0 = pack_bf16x2(q00 - __uint_as_float(h0 << 16), q01 - __uint_as_float(h0 & 0xffff0000u));
       const uint32_t l1 = pack_bf16x2(q10 - __uint_as_float(h1 << 16), q11 - __uint_as_float(h1 & 0xffff0000u));
       const uint32_t ph0 = movmatrix_trans(h0), ph1 = movmatrix_trans(h1);
       const uint32_t pl0 = movmatrix_trans(l0), pl1 = movmatrix_trans(l1);
-      // V codes of this lane's dims (32b + 4n .. +3) for tokens r0, r1, r8, r9
-      const int x = 16 * b + 2 * n;
-      const uint32_t w01 = lds_u16(vc + swz64(r0, x)) | (lds_u16(vc + swz64(r1, x)) << 16);
-      const uint32_t w89 = lds_u16(vc + swz64(r8, x)) | (lds_u16(vc + swz64(r9, x)) << 16);
+      const uint32_t vrow = sg + voff[b];
+      const uint32_t w01 = __byte_perm(lds_u16(vrow), lds_u16(vrow + 64), 0x5410);
+      const uint32_t w89 = __byte_perm(lds_u16(vrow + 512), lds_u16(vrow + 576), 0x5410);
       const uint32_t z01 = code_pair(zv01, 4 * b), z89 = code_pair(zv89, 4 * b);  // (128 + zp) per token
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -278,14 +360,37 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
         mma_bf16_16816(o[2 * b + h], a0, a1, a2, a3, pl0, pl1);
       }
     }
-    __syncwarp();
-    if (lane == 0 && i + STAGES < my_n) {
-      fence_proxy_async_smem();  // this stage's generic reads before the async-proxy refill
-      issue(i + STAGES);
+  };
+
+  for (int j = 0; j < nstage; ++j) {
+    const int tile_idx = j * NWARPS + warp;
+    if (tile_idx >= nsub) break;  // the last stage may hold fewer tiles
+    const int st = j % STAGES;
+    if (!mbar_wait_bounded(bar0 + 8 * st, (j / STAGES) & 1)) {
+      if (lane == 0) set_status(p.status, OL_DEVICE_GUARD);
+      break;
+    }
+    const int t0 = w.t_begin + tile_idx * kTok;
+    const uint32_t sg = smem_u32(stages + st * S::kBytes);
+    if (t0 >= w.lo && t0 + kTok <= t_stop)
+      tile(sg, t0, std::true_type{});
+    else
+      tile(sg, t0, std::false_type{});
+    if (j + STAGES < nstage) {  // every warp has a tile in this stage
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();  // this warp's reads of the stage come first
+        if (atomicAdd(freed + st, 1) == NWARPS - 1) {
+          freed[st] = 0;
+          fence_proxy_async_smem();  // the generic reads before the async-proxy refill
+          issue(j + STAGES);
+        }
+      }
     }
   }
+  __syncthreads();  // all stages consumed: they now hold the warps' states
 
-  store_warp_state<true>(reinterpret_cast<float*>(my_stages), ms, warp, o, m_run0, m_run1, l_run0, l_run1);
+  store_warp_state<true>(reinterpret_cast<float*>(stages + warp * kStateBytes), ms, warp, o, m_run0, m_run1, l_run0, l_run1);
 
   // The token being appended (if this CTA's range holds it): attended from
   // new_kv uncompressed as one more merge state, and quantized into the cache.
@@ -319,7 +424,7 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
       }
     }
   }
-  __syncthreads();  // every warp's tiles are consumed: the appended row may be rewritten
+  __syncthreads();  // every tile is consumed: the appended row may be rewritten
   if (has_cur && p.append && warp < 2) {
     const int plane = warp;
     const size_t row = (size_t)(plane == 0 ? rowK0 : rowV0) + cur;
@@ -331,7 +436,7 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
   merge_and_finish(
       p, w, has_cur ? NWARPS + 1 : NWARPS,
       [&](int s) {
-        return s < NWARPS ? reinterpret_cast<const float*>(stages + s * STAGES * kStage)
+        return s < NWARPS ? reinterpret_cast<const float*>(stages + s * kStateBytes)
                           : static_cast<const float*>(extra_o);
       },
       merged, cmerged, ms);
@@ -356,17 +461,28 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// codes plane as rows of 64 bytes; boxes of 16 rows, 64-byte swizzle
-bool encode_codes(CUtensorMap* map, void* base, uint64_t rows) {
+// A [2 planes][rows][inner] byte array as a 3-D tensor map whose boxes span
+// `box_rows` rows of both planes.
+bool encode_planes(CUtensorMap* map, void* base, uint64_t inner, uint64_t rows, uint32_t box_rows,
+                   CUtensorMapSwizzle swizzle) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {64, rows};
-  cuuint64_t strides[1] = {64};
-  cuuint32_t box[2] = {64, kTok};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  cuuint64_t dims[3] = {inner, rows, 2};
+  cuuint64_t strides[2] = {inner, inner * rows};
+  cuuint32_t box[3] = {(cuuint32_t)inner, box_rows, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The three maps of a stage of NWARPS tiles: codes as 64-byte rows, scales as
+// 16-byte rows of two tokens, zero points as 16-byte rows of eight tokens.
+bool encode_int4_maps(CUtensorMap (&maps)[3], const AttnParams& p, int nwarps) {
+  const uint64_t rows = (uint64_t)p.batch * p.kv_heads * p.capacity;  // per plane
+  const uint32_t tok = 16u * nwarps;
+  return encode_planes(&maps[0], p.codes, 64, rows, tok, CU_TENSOR_MAP_SWIZZLE_64B) &&
+         encode_planes(&maps[1], p.scales, 16, rows / 2, tok / 2, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+         encode_planes(&maps[2], p.zps, 16, rows / 8, tok / 8, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 template <int NWARPS, int STAGES>
@@ -408,7 +524,9 @@ int max_cluster() {
 }
 
 template <int NWARPS, int STAGES>
-cudaError_t launch_cfg(const CUtensorMap& map, const AttnParams& p, cudaStream_t s) {
+cudaError_t launch_cfg(const AttnParams& p, cudaStream_t s) {
+  CUtensorMap maps[3];
+  if (!encode_int4_maps(maps, p, NWARPS)) return cudaErrorInvalidValue;
   cudaError_t e = ensure_attrs<NWARPS, STAGES>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -425,15 +543,15 @@ cudaError_t launch_cfg(const CUtensorMap& map, const AttnParams& p, cudaStream_t
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, fast_int4_kernel<NWARPS, STAGES>, map, p);
+  return cudaLaunchKernelEx(&cfg, fast_int4_kernel<NWARPS, STAGES>, maps[0], maps[1], maps[2], p);
 }
 
 }  // namespace
 
 bool fast_int4_supported(const AttnParams& p) {
   if (p.layout != OL_LAYOUT_INT4 || p.head_dim != 128 || p.group > 8) return false;
-  // tiles never cross a row's capacity (the bulk copies of scales and zero
-  // points have no out-of-bounds fill) and start 16-byte aligned
+  // every (row, kv head) starts on a 16-token boundary, so a stage's scale
+  // and zero-point boxes start on whole 16-byte rows of their maps
   if (p.capacity % 16 != 0) return false;
   const unsigned long long rows = 2ull * p.batch * p.kv_heads * p.capacity;
   return rows < (1ull << 31);
@@ -457,12 +575,10 @@ int fast_int4_max_cluster(int variant) {
 
 cudaError_t launch_fast_int4(const AttnParams& p, cudaStream_t s) {
   if (p.total_ctas <= 0) return cudaSuccess;
-  CUtensorMap map;
-  if (!encode_codes(&map, p.codes, 2ull * p.batch * p.kv_heads * p.capacity)) return cudaErrorInvalidValue;
   switch (p.variant) {
-    case 1: return launch_cfg<4, 4>(map, p, s);
-    case 2: return launch_cfg<8, 2>(map, p, s);
-    default: return launch_cfg<8, 4>(map, p, s);
+    case 1: return launch_cfg<4, 4>(p, s);
+    case 2: return launch_cfg<8, 2>(p, s);
+    default: return launch_cfg<8, 4>(p, s);
   }
 }
 
