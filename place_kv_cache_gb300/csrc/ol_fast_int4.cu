@@ -35,6 +35,7 @@ constexpr uint32_t kMagic = 0x43004300u;  // bf16 pair (128, 128)
 constexpr uint32_t kLoNib = 0x000F000Fu;  // nibble in bits 0..3 of both 16-bit halves
 constexpr uint32_t kHiNib = 0x00F000F0u;  // nibble in bits 4..7 of both halves
 constexpr int kStateBytes = 8 * kOStride * 4;  // one warp's [8][kOStride] fp32 state
+constexpr float kLazy = 8.f;  // log2 headroom of the lazy softmax maximum
 
 // A stage: NWARPS tiles of 16 tokens. Byte offsets (NW = NWARPS):
 //   K codes [16NW][64] @0, V codes @1024NW, K scales [16NW][4] fp16 @2048NW,
@@ -294,21 +295,20 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
       s11 = vb ? s11 : -INFINITY;
     }
 
-    // ---- online softmax (exp2 domain)
-    float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+    // ---- online softmax (exp2 domain) with a lazy maximum: the weights are
+    // taken against the running maximum m as long as no score exceeds it by
+    // more than kLazy (weights stay below 2^kLazy); only then is the tile's
+    // maximum reduced across the lanes and the state rescaled
+    if (__any_sync(0xffffffffu, fmaxf(s00, s10) > m_run0 + kLazy || fmaxf(s01, s11) > m_run1 + kLazy)) {
+      float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-    }
-    const float mn0 = fmaxf(m_run0, mx0), mn1 = fmaxf(m_run1, mx1);
-    const float b0 = mn0 == -INFINITY ? 0.f : mn0, b1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float p00 = fast_exp2(s00 - b0), p01 = fast_exp2(s01 - b1);
-    const float p10 = fast_exp2(s10 - b0), p11 = fast_exp2(s11 - b1);
-    // rescale O only when some lane's running maximum moved (otherwise every
-    // factor is exactly 1)
-    if (__any_sync(0xffffffffu, mn0 != m_run0 || mn1 != m_run1)) {
-      const float al0 = fast_exp2(m_run0 - b0), al1 = fast_exp2(m_run1 - b1);
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(m_run0, mx0), mn1 = fmaxf(m_run1, mx1);
+      const float al0 = mn0 == m_run0 ? 1.f : fast_exp2(m_run0 - mn0);
+      const float al1 = mn1 == m_run1 ? 1.f : fast_exp2(m_run1 - mn1);
       l_run0 *= al0;
       l_run1 *= al1;
 #pragma unroll
@@ -318,11 +318,14 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
         o[mt][2] *= al0;
         o[mt][3] *= al1;
       }
+      m_run0 = mn0;
+      m_run1 = mn1;
     }
+    const float r0 = m_run0 == -INFINITY ? 0.f : m_run0, r1 = m_run1 == -INFINITY ? 0.f : m_run1;
+    const float p00 = fast_exp2(s00 - r0), p01 = fast_exp2(s01 - r1);
+    const float p10 = fast_exp2(s10 - r0), p11 = fast_exp2(s11 - r1);
     l_run0 += p00 + p10;
     l_run1 += p01 + p11;
-    m_run0 = mn0;
-    m_run1 = mn1;
 
     // ---- O^T += V^T P^T, block by block: A = exact bf16 (c - zp_V), the V
     // scale folded into P^T, P^T carried as bf16 hi + lo
