@@ -144,6 +144,28 @@ void plan_fast(AttnParams& p, const int32_t* lens_host, int sms) {
   if (int4 && per_sm > 16 / warps) per_sm = 16 / warps;  // 128 registers per thread
   if (per_sm < 1) per_sm = 1;
   const long long slots = (long long)sms * per_sm;
+  p.streamk = 0;
+  if (int4 && units > 0 && slots <= 4096 && tune().cluster <= 0) {
+    // Stream-K: the INT4 kernel is bound by instruction throughput, so every
+    // SM gets the same number of tiles (whole CTAs per (row, kv head) leave
+    // some SMs with more). Used when every row has tiles and a CTA gets at
+    // least 64 of them (its extra segment costs little against that).
+    long long tiles = 0;
+    bool empty_row = false;
+    for (int b = 0; b < p.batch; ++b) {
+      const int nt = row_split(lens_host[b], p.window, 16).ntiles;
+      empty_row |= nt == 0;
+      tiles += nt;
+    }
+    tiles *= p.kv_heads;
+    if (!empty_row && tiles >= 64 * slots) {
+      p.streamk = 1;
+      p.cluster = 1;
+      p.chunk = 16;
+      p.total_ctas = (int)slots;
+      return;
+    }
+  }
   if (units >= sms || units == 0) {
     plan_splits(p, lens_host, slots * tune().waves, 1);
     return;

@@ -195,7 +195,9 @@ struct Work {
   int b, g, s, nsplit;
   int lo, hi;            // visible range of the row
   int t_begin, t_end;    // token range of this split (t_begin a multiple of 16)
-  int first_cta;         // CTA index of split 0 of (b, g)
+  int first_cta;         // partial slot of split 0 of (b, g)
+  int slot;              // this split's partial slot
+  int next;              // stream-K: global tile of the CTA's next segment, -1 = none
   int valid;
 };
 
@@ -209,7 +211,8 @@ __device__ __forceinline__ Work map_cta_warp(const int32_t* __restrict__ lens, i
   w.b = w.g = w.s = 0;
   w.nsplit = 1;
   w.lo = w.hi = w.t_begin = w.t_end = 0;
-  w.first_cta = 0;
+  w.first_cta = w.slot = 0;
+  w.next = -1;
   int running = 0;
   for (int base = 0; base < batch; base += 32) {
     int b = base + lane;
@@ -246,12 +249,103 @@ __device__ __forceinline__ Work map_cta_warp(const int32_t* __restrict__ lens, i
       w.t_begin = min(start + 16 * split_tile(w.s, ntiles, w.nsplit), w.hi);
       w.t_end = min(start + 16 * split_tile(w.s + 1, ntiles, w.nsplit), w.hi);
       w.first_cta = cta - w.s;
+      w.slot = cta;
       w.valid = 1;
       return w;
     }
     running += total;
   }
   set_status(status, OL_DEVICE_GUARD);  // grid larger than the device-side plan
+  return w;
+}
+
+// Length of row b as the kernels read it: clamped to [0, capacity], with a
+// device status when it was out of range.
+__device__ __forceinline__ int read_len(const int32_t* __restrict__ lens, int b, int capacity, int32_t* status) {
+  int n = lens[b];
+  if (n < 0 || n > capacity) {
+    set_status(status, OL_DEVICE_GUARD);
+    n = n < 0 ? 0 : capacity;
+  }
+  return n;
+}
+
+// Stream-K work. The 16-token tiles of all (row, kv head) units, in unit
+// order u = b * kv_heads + g, are cut into `nctas` contiguous ranges of equal
+// size; CTA c takes tiles [c*T/nctas, (c+1)*T/nctas) of the T tiles. Where its
+// range crosses units it works in segments, one per unit. This returns the
+// segment that starts at global tile x (x < 0: the CTA's first), with
+//   slot = c + u (increasing along the tile order, so the segments of one
+//   unit hold consecutive slots), first_cta = the slot of the unit's first
+//   segment, nsplit = the unit's segment count, next = the start of the CTA's
+//   following segment (-1: none).
+// Computed by one full warp; every lane returns the same Work.
+__device__ __forceinline__ Work map_streamk_warp(const int32_t* __restrict__ lens, int batch, int kv_heads,
+                                                 int capacity, int window, int nctas, int cta, int x,
+                                                 int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  Work w;
+  w.valid = 0;
+  w.b = w.g = w.s = 0;
+  w.nsplit = 1;
+  w.lo = w.hi = w.t_begin = w.t_end = 0;
+  w.first_cta = w.slot = 0;
+  w.next = -1;
+  long long T = 0;
+  for (int base = 0; base < batch; base += 32) {
+    const int b = base + lane;
+    int nt = b < batch ? row_split(read_len(lens, b, capacity, status), window, 16).ntiles : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) nt += __shfl_xor_sync(0xffffffffu, nt, o);
+    T += nt;
+  }
+  T *= kv_heads;
+  const long long g0 = (long long)cta * T / nctas, g1 = (long long)(cta + 1) * T / nctas;
+  const long long xx = x < 0 ? g0 : x;
+  if (xx >= g1) return w;  // an empty range, or past the CTA's last segment
+  long long running = 0;  // first global tile of the chunk's first row
+  for (int base = 0; base < batch; base += 32) {
+    const int b = base + lane;
+    RowSplit rs;
+    rs.lo = rs.hi = rs.start = rs.ntiles = rs.nsplit = 0;
+    if (b < batch) rs = row_split(read_len(lens, b, capacity, nullptr), window, 16);
+    const long long cnt = b < batch ? (long long)rs.ntiles * kv_heads : 0;
+    long long incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const long long total = __shfl_sync(0xffffffffu, incl, 31);
+    if (xx < running + total) {
+      const long long excl = incl - cnt;
+      const unsigned hit = __ballot_sync(0xffffffffu, cnt > 0 && xx >= running + excl && xx < running + incl);
+      const int src = __ffs(hit) - 1;
+      const int nt = __shfl_sync(0xffffffffu, rs.ntiles, src);
+      const int start = __shfl_sync(0xffffffffu, rs.start, src);
+      const long long rb = running + __shfl_sync(0xffffffffu, excl, src);  // first tile of row b
+      w.b = base + src;
+      w.lo = __shfl_sync(0xffffffffu, rs.lo, src);
+      w.hi = __shfl_sync(0xffffffffu, rs.hi, src);
+      w.g = (int)((xx - rb) / nt);
+      const long long au = rb + (long long)w.g * nt, bu = au + nt;  // the unit's tiles
+      const long long se = bu < g1 ? bu : g1;
+      w.t_begin = min(start + 16 * (int)(xx - au), w.hi);
+      w.t_end = min(start + 16 * (int)(se - au), w.hi);
+      const int cf = (int)(((au + 1) * nctas - 1) / T);  // CTA holding the unit's first tile
+      const int cl = (int)((bu * nctas - 1) / T);        // and its last
+      const int u = w.b * kv_heads + w.g;
+      w.s = cta - cf;
+      w.nsplit = cl - cf + 1;
+      w.slot = cta + u;
+      w.first_cta = cf + u;
+      w.next = se < g1 ? (int)se : -1;
+      w.valid = 1;
+      return w;
+    }
+    running += total;
+  }
+  set_status(status, OL_DEVICE_GUARD);
   return w;
 }
 

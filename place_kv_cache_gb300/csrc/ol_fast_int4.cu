@@ -131,17 +131,25 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
     fence_mbar_init();
   }
   if (!p.inline_lens) pdl_wait();
+  const int32_t* lens = p.inline_lens ? p.lens_inline : p.lens;
+  int32_t* const lens_status = p.inline_lens ? nullptr : p.status;
+  int jbase = 0;  // stages consumed by earlier segments: ring slot and mbarrier phase
+  int next = -1;  // stream-K: global tile where the next segment starts
+  // One pass per segment: a split of one (row, kv head). Without stream-K a
+  // CTA has one segment.
+  for (int seg = 0;; ++seg) {
+  if (seg > 0) __syncthreads();  // the previous segment's Work and states are done with
   if (warp == 0) {
-    Work w = p.inline_lens
-                 ? map_cta_warp(p.lens_inline, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, blockIdx.x,
-                                nullptr, CS)
-                 : map_cta_warp(p.lens, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, blockIdx.x, p.status, CS);
+    Work w = p.streamk ? map_streamk_warp(lens, p.batch, p.kv_heads, p.capacity, p.window, p.total_ctas,
+                                          blockIdx.x, next, lens_status)
+                       : map_cta_warp(lens, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, blockIdx.x,
+                                      lens_status, CS);
     if (lane == 0) *sw = w;
   }
   __syncthreads();
   const Work w = *sw;
-  if (!w.valid && CS == 1) {
-    if (p.inline_lens) pdl_wait();
+  if (!w.valid && (seg > 0 || CS == 1)) {  // a cluster's idle CTAs still take part in its merge
+    if (seg == 0 && p.inline_lens) pdl_wait();
     return;
   }
 
@@ -158,7 +166,7 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
   // past the CTA's range read tokens nobody uses (or the fill value past the
   // end of the arrays).
   auto issue = [&](int j) {
-    const int st = j % STAGES;
+    const int st = (jbase + j) % STAGES;
     const uint32_t dst = smem_u32(stages + st * S::kBytes);
     const uint32_t bar = bar0 + 8 * st;
     const int r = row0 + w.t_begin + j * NWARPS * kTok;  // multiple of 16
@@ -168,12 +176,17 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
     tma_load_3d(dst + S::kOffZk, &tm_zps, 0, r >> 3, 0, bar, pol);
   };
   const int pre = nstage < STAGES ? nstage : STAGES;
-  if (p.early && threadIdx.x == 0)
+  if (seg == 0) {
+    if (p.early && threadIdx.x == 0)
+      for (int j = 0; j < pre; ++j) issue(j);
+    if (p.inline_lens) pdl_wait();
+    pdl_launch_dependents();
+    if (!p.early && threadIdx.x == 0)
+      for (int j = 0; j < pre; ++j) issue(j);
+  } else if (threadIdx.x == 0) {
+    fence_proxy_async_smem();  // the previous segment's generic use of the stages first
     for (int j = 0; j < pre; ++j) issue(j);
-  if (p.inline_lens) pdl_wait();
-  pdl_launch_dependents();
-  if (!p.early && threadIdx.x == 0)
-    for (int j = 0; j < pre; ++j) issue(j);
+  }
 
   // K side operands. The codes enter the tensor cores as fp16 subnormals: a
   // 16-bit lane holding c in bits 0..3 is c * 2^-24, in bits 4..7 it is
@@ -368,8 +381,8 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
   for (int j = 0; j < nstage; ++j) {
     const int tile_idx = j * NWARPS + warp;
     if (tile_idx >= nsub) break;  // the last stage may hold fewer tiles
-    const int st = j % STAGES;
-    if (!mbar_wait_bounded(bar0 + 8 * st, (j / STAGES) & 1)) {
+    const int st = (jbase + j) % STAGES;
+    if (!mbar_wait_bounded(bar0 + 8 * st, ((jbase + j) / STAGES) & 1)) {
       if (lane == 0) set_status(p.status, OL_DEVICE_GUARD);
       break;
     }
@@ -443,6 +456,10 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
                           : static_cast<const float*>(extra_o);
       },
       merged, cmerged, ms);
+  jbase += nstage;
+  if (!p.streamk || w.next < 0) break;
+  next = w.next;
+  }  // segments
 }
 
 // ------------------------------------------------------------------ host

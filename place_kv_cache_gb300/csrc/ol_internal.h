@@ -82,6 +82,7 @@ struct AttnParams {
   int cluster;          // CTAs per thread-block cluster (1 = no cluster)
   int variant;          // tensor-core kernel variant (warps x stages)
   int total_ctas;
+  int streamk;          // 1: the CTAs split the concatenated tiles of all (row, kv head) evenly
 };
 
 // Append-only launches (CacheUpdate, PagedCacheUpdate, INT4 append).

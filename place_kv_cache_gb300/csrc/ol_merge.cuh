@@ -148,7 +148,7 @@ __device__ __forceinline__ void merge_and_finish(const AttnParams& p, const Work
   if (CS == 1) {
     __syncthreads();
     if (!w.valid) return;
-    finish_split(p, w, ms.m, ms.l, merged, kOStride, 0, G, 0, 128, blockIdx.x, w.first_cta, w.nsplit, w.nsplit,
+    finish_split(p, w, ms.m, ms.l, merged, kOStride, 0, G, 0, 128, w.slot, w.first_cta, w.nsplit, w.nsplit,
                  ms.flag, ms.scr);
     return;
   }

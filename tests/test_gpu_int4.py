@@ -158,3 +158,30 @@ def test_int4_history_stable_flag():
     for g, r in zip(host_planes(dplanes), planes):
         np.testing.assert_array_equal(g, r)
     check_out(out_as_f64(out), O.int4_attention(case.q, *planes, case.lens, cur_kv=case.new_kv), ol.OL_F32)
+
+
+@pytest.mark.parametrize("shape", [
+    # long rows and one short one: each of the ~300 CTAs takes ~70 tiles of the
+    # concatenated rows, so ranges cross (row, kv head) boundaries and the
+    # short row's units share CTAs (several segments per CTA)
+    ("ragged", 6, [16384, 16384, 16000, 700, 16000, 16000], -1),
+    ("window", 8, [16384] * 7 + [700], 12000),
+], ids=lambda s: s[0])
+def test_int4_streamk_matches_oracle(shape):
+    name, B, lens, window = shape
+    Hq, Hkv, D, C = 16, 4, 128, 16384
+    w = Workload("sk_" + name, "bf16", B, Hq, Hkv, D, C, "int4", seed=36)
+    case = make_case(w, lens=np.array(lens, np.int32))
+    planes = oracle_planes(case, O.Q_DYNAMIC)
+    dplanes = dev_planes(planes)
+    ws, n = workspace(B, Hq, Hkv, D)
+    out = out_tensor(B, Hq, D, ol.OL_F32)
+    ol.ol_decode_step(ol.OL_LAYOUT_INT4, desc_of(dplanes, w, O.Q_DYNAMIC), dplanes[0], to_dev(case.q), Hq,
+                      to_dev(case.new_kv), case.lens, to_dev(case.lens), 0.0, window, out, ol.OL_F32, ws, n)
+    torch.cuda.synchronize()
+    assert ol.ol_workspace_status(ws) == ol.OL_DEVICE_OK
+    O.int4_append(*planes, case.new_kv, case.lens - 1, mode=O.Q_DYNAMIC)
+    for g, r in zip(host_planes(dplanes), planes):
+        np.testing.assert_array_equal(g, r)
+    want = O.int4_attention(case.q, *planes, case.lens, cur_kv=case.new_kv, window=window)
+    assert max_abs_err(out_as_f64(out), want) <= TOL
