@@ -59,6 +59,37 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def kernel_sources_sha() -> str:
+    """sha256 over the library's CUDA/C++ sources (file name and content, in name
+    order): a recorded DRAM traffic figure holds only for the sources it was
+    measured on."""
+    import hashlib
+    d = os.path.join(ROOT, "place_kv_cache_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
+            h.update(name.encode() + b"\0")
+            with open(os.path.join(d, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes (read + write) per launch of the workload's kernel from one ncu
+    capture, as listed in profiles/dram_traffic.txt; None when none was recorded
+    or it was recorded on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    sha = kernel_sources_sha()
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) == 4 and not line.startswith("#") and parts[0] == workload and parts[3] == sha:
+                return int(parts[2])
+    return None
+
+
 def step_bytes(w, lens):
     """Algorithmic HBM bytes of one step: K/V of every attended token (the new
     token's K/V read from new_kv), the appended token written, q read, y written."""
@@ -337,7 +368,7 @@ def run_ours(args, rank, world, dist):
                    "history_stable": s.chain == 1,
                    "parallelism": f"rows x{world} (independent)"},
         "roofline": {"bound": "hbm", "achieved": round(gbs / world, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(gbs / world / peak, 4), "traffic": None,
+                     "frac": round(gbs / world / peak, 4), "traffic": recorded_traffic(w.name),
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else
                      "fallback 6.8 TB/s"},
         "gpu_launches": K,
