@@ -289,6 +289,36 @@ OL_API ol_status ol_decode_step(int32_t layout, const void* cache_desc, void* up
                          int32_t out_dtype, void* workspace, size_t ws_bytes, ol_stream stream);
 
 /*
+ * Workspace bytes for ol_decode_step_host: those of ol_workspace_size plus
+ * device staging for q, new_kv, the lengths and y (sized for 4-byte elements,
+ * so one size serves every dtype). 0 on invalid sizes.
+ */
+OL_API size_t ol_workspace_size_host(int32_t batch, int32_t q_heads, int32_t kv_heads, int32_t head_dim);
+
+/*
+ * The fused decode step with host-resident inputs and output: q_host
+ * [batch, q_heads, head_dim], new_kv_host [2, batch, kv_heads, 1, head_dim]
+ * (dtypes as for ol_decode_step) and lens_host [batch] are copied into the
+ * workspace's staging area (host-to-device copies on `stream`), the step runs
+ * as ol_decode_step on those device copies, and y is copied to out_host
+ * [batch, q_heads, head_dim] of out_dtype (device-to-host on `stream`).
+ * Everything is asynchronous: out_host holds y once `stream` has been
+ * synchronized, and the host buffers must stay valid until then; pinned host
+ * memory keeps the copies asynchronous (pageable memory works, at the
+ * driver's pace). The cache stays in device memory, described as for
+ * ol_decode_step. ws_bytes must be at least
+ * ol_workspace_size_host(batch, q_heads, kv_heads, head_dim).
+ * Errors: those of ol_decode_step (the descriptor, host pointers, lengths and
+ * workspace size are checked before any copy is enqueued; a call that fails
+ * later has written only the staging area), or OL_ERR_CUDA if a copy cannot
+ * be enqueued. The cache is never touched by a failing call.
+ */
+OL_API ol_status ol_decode_step_host(int32_t layout, const void* cache_desc, void* updated, const void* q_host,
+                                     int32_t q_heads, const void* new_kv_host, const int32_t* lens_host,
+                                     float scale, int32_t window, void* out_host, int32_t out_dtype,
+                                     void* workspace, size_t ws_bytes, ol_stream stream);
+
+/*
  * The fused decode step with no allocation by anyone: no workspace argument.
  * The paper has no counterpart; it exists for callers that cannot call
  * cudaMalloc -- code running inside a host engine that owns all device memory

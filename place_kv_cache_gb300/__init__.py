@@ -31,7 +31,8 @@ OL_DEVICE_OK, OL_DEVICE_GUARD = 0, 1
 SYMBOLS = ("ol_status_string", "ol_version", "ol_workspace_size", "ol_workspace_init", "ol_workspace_status",
            "ol_cache_bind", "ol_cache_unbind", "ol_cache_update", "ol_cache_update_rows",
            "ol_paged_cache_update", "ol_decode_attention", "ol_paged_decode_attention", "ol_int4kv_append",
-           "ol_int4kv_decode_attention", "ol_decode_step", "ol_decode_step_noalloc")
+           "ol_int4kv_decode_attention", "ol_decode_step", "ol_decode_step_noalloc", "ol_workspace_size_host",
+           "ol_decode_step_host")
 
 
 class OlError(RuntimeError):
@@ -102,6 +103,8 @@ def load(build_if_missing: bool = True):
                                             vp]),
         "ol_decode_step": (st, [i32, vp, vp, vp, i32, vp, vp, vp, f32, i32, vp, i32, vp, sz, vp]),
         "ol_decode_step_noalloc": (st, [i32, vp, vp, vp, i32, vp, vp, vp, f32, i32, vp, i32, vp]),
+        "ol_workspace_size_host": (sz, [i32, i32, i32, i32]),
+        "ol_decode_step_host": (st, [i32, vp, vp, vp, i32, vp, vp, f32, i32, vp, i32, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -294,6 +297,21 @@ def ol_decode_step(layout: int, desc, updated, q, q_heads: int, new_kv, lens_hos
     _check(load().ol_decode_step(layout, ctypes.byref(desc), _ptr(updated), _ptr(q), q_heads, _ptr(new_kv), _ptr(lh),
                                  _ptr(lens_dev), scale, window, _ptr(out), out_dtype, _ptr(workspace), ws_bytes,
                                  _stream(stream)), "ol_decode_step")
+
+
+def ol_workspace_size_host(batch: int, q_heads: int, kv_heads: int, head_dim: int) -> int:
+    return load().ol_workspace_size_host(batch, q_heads, kv_heads, head_dim)
+
+
+def ol_decode_step_host(layout: int, desc, updated, q_host, q_heads: int, new_kv_host, lens_host, scale: float,
+                        window: int, out_host, out_dtype: int, workspace, ws_bytes: int, stream=None):
+    """ol_decode_step with q, new K/V, lengths and y in host memory (numpy arrays
+    or CPU tensors, pinned for asynchronous copies); y is in out_host once the
+    stream has been synchronized."""
+    lh = _host_i32(lens_host)
+    _check(load().ol_decode_step_host(layout, ctypes.byref(desc), _ptr(updated), _ptr(q_host), q_heads,
+                                      _ptr(new_kv_host), _ptr(lh), scale, window, _ptr(out_host), out_dtype,
+                                      _ptr(workspace), ws_bytes, _stream(stream)), "ol_decode_step_host")
 
 
 def ol_decode_step_noalloc(layout: int, desc, updated, q, q_heads: int, new_kv, lens_host, lens_dev, scale: float,

@@ -720,4 +720,64 @@ ol_status ol_decode_step(int32_t layout, const void* cache_desc, void* updated, 
                        out_dtype, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
+// Staging offsets inside the workspace for ol_decode_step_host, after the
+// bytes ol_decode_step needs; every buffer 256-byte aligned and sized for
+// 4-byte elements.
+struct HostStaging {
+  size_t q, kv, lens, out, total;
+};
+static HostStaging host_staging(int32_t batch, int32_t q_heads, int32_t kv_heads, int32_t head_dim) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  HostStaging h;
+  h.q = up(workspace_bytes(batch, q_heads, kv_heads, head_dim));
+  h.kv = h.q + up((size_t)batch * q_heads * head_dim * 4);
+  h.lens = h.kv + up(2ull * batch * kv_heads * head_dim * 4);
+  h.out = h.lens + up((size_t)batch * 4);
+  h.total = h.out + up((size_t)batch * q_heads * head_dim * 4);
+  return h;
+}
+
+size_t ol_workspace_size_host(int32_t batch, int32_t q_heads, int32_t kv_heads, int32_t head_dim) {
+  if (batch < 0 || kv_heads <= 0 || q_heads <= 0 || q_heads % kv_heads != 0 || head_dim <= 0) return 0;
+  return host_staging(batch, q_heads, kv_heads, head_dim).total;
+}
+
+ol_status ol_decode_step_host(int32_t layout, const void* cache_desc, void* updated, const void* q_host,
+                              int32_t q_heads, const void* new_kv_host, const int32_t* lens_host, float scale,
+                              int32_t window, void* out_host, int32_t out_dtype, void* workspace, size_t ws_bytes,
+                              ol_stream stream) {
+  CacheView v;
+  ol_status st = view_of(layout, cache_desc, v);
+  if (st != OL_OK) return st;
+  if ((st = writable(v, updated)) != OL_OK) return st;
+  if (!q_host || !new_kv_host || !lens_host || !out_host || !workspace) return OL_ERR_NULL;
+  if (q_heads <= 0 || q_heads % v.kv_heads != 0) return OL_ERR_SHAPE;
+  if (!valid_dtype(out_dtype)) return OL_ERR_DTYPE;
+  if (!aligned16(workspace)) return OL_ERR_ALIGN;
+  const HostStaging h = host_staging(v.batch, q_heads, v.kv_heads, v.head_dim);
+  if (ws_bytes < h.total) return OL_ERR_WORKSPACE;
+  if ((st = no_overlap(v, workspace, h.total)) != OL_OK) return st;
+  for (int b = 0; b < v.batch; ++b)
+    if (lens_host[b] < 1 || lens_host[b] > v.capacity) return OL_ERR_CAPACITY;
+  const size_t in_elt = v.layout == OL_LAYOUT_INT4 ? 2 : elt_bytes(v.dtype);
+  const size_t q_bytes = (size_t)v.batch * q_heads * v.head_dim * in_elt;
+  const size_t kv_bytes = 2ull * v.batch * v.kv_heads * v.head_dim * in_elt;
+  const size_t out_bytes = (size_t)v.batch * q_heads * v.head_dim * elt_bytes(out_dtype);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(ws + h.q, q_host, q_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(ws + h.kv, new_kv_host, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return OL_ERR_CUDA;
+  // the kernels take the lengths by value for batches of up to kInlineRows
+  // rows and never read the device copy then
+  if (v.batch > kInlineRows &&
+      cudaMemcpyAsync(ws + h.lens, lens_host, sizeof(int32_t) * v.batch, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return OL_ERR_CUDA;
+  st = run_attention(layout, cache_desc, v, ws + h.q, q_heads, lens_host, reinterpret_cast<int32_t*>(ws + h.lens),
+                     ws + h.kv, 1, 1, scale, window, ws + h.out, out_dtype, workspace, h.q, s);
+  if (st != OL_OK) return st;
+  return cudaMemcpyAsync(out_host, ws + h.out, out_bytes, cudaMemcpyDeviceToHost, s) == cudaSuccess ? OL_OK
+                                                                                                 : OL_ERR_CUDA;
+}
+
 }  // extern "C"

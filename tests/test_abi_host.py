@@ -241,3 +241,40 @@ def test_history_stable_bit_keeps_write_access():
     assert status_of(step, desc=desc) == ol.OL_ERR_INJECTED
     desc = ol.kv_cache(CACHE, dims=(B, HKV, C, D), dtype=ol.OL_BF16, access=ol.OL_READ_ONLY | ol.OL_HISTORY_STABLE)
     assert status_of(step, desc=desc) == ol.OL_ERR_READONLY
+
+
+# ------------------------------------------------- host-buffer decode step
+
+def test_host_step_workspace_holds_the_staging():
+    plain = ol.ol_workspace_size(B, HQ, HKV, D)
+    host = ol.ol_workspace_size_host(B, HQ, HKV, D)
+    assert host >= plain + (B * HQ * D * 4) * 2 + 2 * B * HKV * D * 4 + B * 4
+    assert ol.ol_workspace_size_host(1, 7, 4, 128) == 0
+
+
+def host_step(updated=CACHE, q=None, kv=None, lens=(10, 64), out=None, ws=WS, ws_bytes=None, desc=None):
+    desc = ol.kv_cache(CACHE, dims=(B, HKV, C, D), dtype=ol.OL_BF16) if desc is None else desc
+    q = np.zeros((B, HQ, D), np.uint16) if q is None else q
+    kv = np.zeros((2, B, HKV, 1, D), np.uint16) if kv is None else kv
+    out = np.zeros((B, HQ, D), np.uint16) if out is None else out
+    ws_bytes = ol.ol_workspace_size_host(B, HQ, HKV, D) if ws_bytes is None else ws_bytes
+    ol.ol_decode_step_host(ol.OL_LAYOUT_CONTIGUOUS, desc, updated, q, HQ, kv, np.array(lens, np.int32), 0.0, -1,
+                           out, ol.OL_BF16, ws, ws_bytes, stream=0)
+
+
+def test_host_step_rejects_before_any_copy():
+    # every one of these fails on the host before a copy is enqueued (no GPU here)
+    assert status_of(host_step, updated=CACHE + 256) == ol.OL_ERR_ALIAS
+    assert status_of(host_step, ws_bytes=ol.ol_workspace_size(B, HQ, HKV, D)) == ol.OL_ERR_WORKSPACE
+    assert status_of(host_step, lens=(10, C + 1)) == ol.OL_ERR_CAPACITY
+    assert status_of(host_step, lens=(0, 5)) == ol.OL_ERR_CAPACITY
+    assert status_of(host_step, ws=CACHE + 64) == ol.OL_ERR_ALIAS          # staging inside the cache
+    assert status_of(host_step, ws=WS + 8) == ol.OL_ERR_ALIGN
+    ro = ol.kv_cache(CACHE, dims=(B, HKV, C, D), dtype=ol.OL_BF16, access=ol.OL_READ_ONLY)
+    assert status_of(host_step, desc=ro) == ol.OL_ERR_READONLY
+    lib = ol.load()
+    d = ol.kv_cache(CACHE, dims=(B, HKV, C, D), dtype=ol.OL_BF16)
+    import ctypes
+    assert lib.ol_decode_step_host(ol.OL_LAYOUT_CONTIGUOUS, ctypes.byref(d), CACHE, None, HQ, None, None, 0.0, -1,
+                                   None, ol.OL_BF16, WS, ol.ol_workspace_size_host(B, HQ, HKV, D), None) \
+        == ol.OL_ERR_NULL
