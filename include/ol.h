@@ -289,6 +289,37 @@ OL_API ol_status ol_decode_step(int32_t layout, const void* cache_desc, void* up
                          int32_t out_dtype, void* workspace, size_t ws_bytes, ol_stream stream);
 
 /*
+ * Storage statistics of a call (page "Persistent input/output feedback",
+ * sections Opt-in storage auditing through runtime events and Optional
+ * heterogeneous paged KV: the storage_* reports and the direct call's
+ * copied / dequantized byte counts). The library records them, on the
+ * calling host thread, for every append, attention or decode-step call that
+ * passes validation (also when the launch then fails: the counts describe the
+ * work the call requested). They are host arithmetic on the call's sizes; no
+ * device work is added.
+ */
+typedef struct {
+  int64_t calls;                       /* calls summed into this record */
+  int64_t storage_allocations;         /* KV storage allocations: always 0 (caches are caller-owned, never grown) */
+  int64_t storage_allocated_bytes;     /* KV storage bytes requested: always 0 */
+  int64_t storage_prefix_copied_bytes; /* bytes of the valid prefix copied: always 0 (appends write in place) */
+  int64_t storage_append_copied_bytes; /* new payload bytes stored by appends (INT4: codes + scales + zero points) */
+  int64_t storage_reuse_count;         /* K / V storage tensors appended in place (2 per appending call) */
+  int64_t dequantized_bytes;           /* FLOAT bytes decoded from quantized history: 4 per element per (token,
+                                          kv head, K or V), the current uncompressed token excluded; one decode
+                                          serves the whole query group */
+  int64_t attended_tokens;             /* sum over rows and kv heads of the visible tokens, current one included */
+  int64_t kv_payload_bytes_read;       /* K/V payload bytes read from the cache for the visible history */
+  int64_t workspace_bytes;             /* workspace bytes the call's shapes require (bound on its scratch) */
+} ol_stats;
+
+/* The record of the last validated call on this thread (zeros before the first). */
+OL_API ol_status ol_last_call_stats(ol_stats* out);
+/* Sums of every record on this thread since the last ol_reset_stats (calls > 1). */
+OL_API ol_status ol_total_stats(ol_stats* out);
+OL_API void ol_reset_stats(void);
+
+/*
  * Workspace bytes for ol_decode_step_host: those of ol_workspace_size plus
  * device staging for q, new_kv, the lengths and y (sized for 4-byte elements,
  * so one size serves every dtype). 0 on invalid sizes.

@@ -32,7 +32,18 @@ SYMBOLS = ("ol_status_string", "ol_version", "ol_workspace_size", "ol_workspace_
            "ol_cache_bind", "ol_cache_unbind", "ol_cache_update", "ol_cache_update_rows",
            "ol_paged_cache_update", "ol_decode_attention", "ol_paged_decode_attention", "ol_int4kv_append",
            "ol_int4kv_decode_attention", "ol_decode_step", "ol_decode_step_noalloc", "ol_workspace_size_host",
-           "ol_decode_step_host")
+           "ol_decode_step_host", "ol_last_call_stats", "ol_total_stats", "ol_reset_stats")
+
+
+class Stats(ctypes.Structure):
+    """ol_stats: storage statistics of a call (see include/ol.h)."""
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "calls", "storage_allocations", "storage_allocated_bytes", "storage_prefix_copied_bytes",
+        "storage_append_copied_bytes", "storage_reuse_count", "dequantized_bytes", "attended_tokens",
+        "kv_payload_bytes_read", "workspace_bytes")]
+
+    def as_dict(self) -> dict:
+        return {n: getattr(self, n) for n, _ in self._fields_}
 
 
 class OlError(RuntimeError):
@@ -104,6 +115,9 @@ def load(build_if_missing: bool = True):
         "ol_decode_step": (st, [i32, vp, vp, vp, i32, vp, vp, vp, f32, i32, vp, i32, vp, sz, vp]),
         "ol_decode_step_noalloc": (st, [i32, vp, vp, vp, i32, vp, vp, vp, f32, i32, vp, i32, vp]),
         "ol_workspace_size_host": (sz, [i32, i32, i32, i32]),
+        "ol_last_call_stats": (st, [vp]),
+        "ol_total_stats": (st, [vp]),
+        "ol_reset_stats": (None, []),
         "ol_decode_step_host": (st, [i32, vp, vp, vp, i32, vp, vp, f32, i32, vp, i32, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
@@ -215,6 +229,24 @@ def int4_kv(codes, scales, zps, *, head_dim: Optional[int] = None, quant_mode: i
 
 def ol_version() -> int:
     return load().ol_version()
+
+
+def ol_last_call_stats() -> dict:
+    """Storage statistics of the last call on this thread that passed validation."""
+    st = Stats()
+    _check(load().ol_last_call_stats(ctypes.byref(st)), "ol_last_call_stats")
+    return st.as_dict()
+
+
+def ol_total_stats() -> dict:
+    """Sums of the statistics of this thread's calls since ol_reset_stats."""
+    st = Stats()
+    _check(load().ol_total_stats(ctypes.byref(st)), "ol_total_stats")
+    return st.as_dict()
+
+
+def ol_reset_stats() -> None:
+    load().ol_reset_stats()
 
 
 def ol_status_string(status: int) -> str:

@@ -7,6 +7,7 @@
 // writable binding is not used concurrently by several sessions; Required
 // alias: pointer identity checked, no silent copy fallback).
 #include <cmath>
+#include <algorithm>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -396,6 +397,65 @@ AttnParams base_params(const CacheView& v, int layout, const void* desc) {
 }
 
 // Shared path of every attention-bearing call.
+// ----------------------------------------------------- storage statistics
+
+thread_local ol_stats t_last = {};
+thread_local ol_stats t_total = {};
+
+void record(const ol_stats& s) {
+  t_last = s;
+  t_total.calls += s.calls;
+  t_total.storage_allocations += s.storage_allocations;
+  t_total.storage_allocated_bytes += s.storage_allocated_bytes;
+  t_total.storage_prefix_copied_bytes += s.storage_prefix_copied_bytes;
+  t_total.storage_append_copied_bytes += s.storage_append_copied_bytes;
+  t_total.storage_reuse_count += s.storage_reuse_count;
+  t_total.dequantized_bytes += s.dequantized_bytes;
+  t_total.attended_tokens += s.attended_tokens;
+  t_total.kv_payload_bytes_read += s.kv_payload_bytes_read;
+  t_total.workspace_bytes = std::max(t_total.workspace_bytes, s.workspace_bytes);
+}
+
+// Stored payload bytes of one token of one kv head in one plane (K or V).
+int64_t token_payload(const CacheView& v) {
+  return v.layout == OL_LAYOUT_INT4 ? v.head_dim / 2 + (v.head_dim / 32) * 2 + v.head_dim / 64
+                                    : (int64_t)v.head_dim * (int64_t)elt_bytes(v.dtype);
+}
+
+// An append of new_len tokens to every row: written in place, nothing else copied.
+void record_append(const CacheView& v, int new_len) {
+  ol_stats s = {};
+  s.calls = 1;
+  s.storage_append_copied_bytes = 2ll * v.batch * v.kv_heads * new_len * token_payload(v);
+  s.storage_reuse_count = new_len > 0 && v.batch > 0 ? 2 : 0;
+  record(s);
+}
+
+// An attention call (with the fused append when `append`): history read from
+// the cache is the visible range minus the current token when that one comes
+// from new_kv.
+void record_attention(const CacheView& v, const int32_t* lens_host, int window, int append, int cur_from_new,
+                      size_t ws_need) {
+  ol_stats s = {};
+  s.calls = 1;
+  int64_t visible = 0, hist = 0;
+  for (int b = 0; b < v.batch; ++b) {
+    const RowSplit rs = row_split(lens_host[b], window < 0 ? -1 : window, 16);
+    const int vis = rs.hi - rs.lo;
+    visible += vis;
+    hist += (cur_from_new && vis > 0) ? vis - 1 : vis;
+  }
+  s.attended_tokens = visible * v.kv_heads;
+  s.kv_payload_bytes_read = 2 * hist * v.kv_heads * token_payload(v);
+  if (v.layout == OL_LAYOUT_INT4) s.dequantized_bytes = 2 * hist * v.kv_heads * v.head_dim * 4;
+  if (append) {
+    s.storage_append_copied_bytes = 2ll * v.batch * v.kv_heads * token_payload(v);
+    s.storage_reuse_count = v.batch > 0 ? 2 : 0;
+  }
+  s.workspace_bytes = (int64_t)ws_need;
+  record(s);
+}
+
 ol_status run_attention(int layout, const void* desc, const CacheView& v, const void* q, int q_heads,
                         const int32_t* lens_host, const int32_t* lens_dev, const void* new_kv, int append,
                         int cur_from_new, float scale, int window, void* out, int out_dtype, void* workspace,
@@ -439,6 +499,7 @@ ol_status run_attention(int layout, const void* desc, const CacheView& v, const 
     }
   }
   if ((st = check_owner(v.ranges, v.nranges, v.owner)) != OL_OK) return st;
+  record_attention(v, lens_host, window, append, cur_from_new, need);
   if (fault_injected()) return OL_ERR_INJECTED;
 
   AttnParams p = base_params(v, layout, desc);
@@ -507,6 +568,23 @@ const char* ol_status_string(ol_status s) {
 }
 
 int32_t ol_version(void) { return 100; }
+
+ol_status ol_last_call_stats(ol_stats* out) {
+  if (!out) return OL_ERR_NULL;
+  *out = t_last;
+  return OL_OK;
+}
+
+ol_status ol_total_stats(ol_stats* out) {
+  if (!out) return OL_ERR_NULL;
+  *out = t_total;
+  return OL_OK;
+}
+
+void ol_reset_stats(void) {
+  t_last = ol_stats{};
+  t_total = ol_stats{};
+}
 
 size_t ol_workspace_size(int32_t batch, int32_t q_heads, int32_t kv_heads, int32_t head_dim) {
   if (batch < 0 || kv_heads <= 0 || q_heads <= 0 || q_heads % kv_heads != 0 || head_dim <= 0) return 0;
@@ -613,6 +691,7 @@ ol_status ol_cache_update_rows(const ol_kv_cache* cache, void* updated_cache, co
   if (st != OL_OK) return st;
   if ((st = append_common(v, updated_cache, values, new_len, positions_host, positions_dev)) != OL_OK) return st;
   if ((st = check_owner(v.ranges, v.nranges, v.owner)) != OL_OK) return st;
+  record_append(v, new_len);
   if (fault_injected()) return OL_ERR_INJECTED;
   return launch_append_view(v, OL_LAYOUT_CONTIGUOUS, cache, values, new_len, positions_dev,
                             static_cast<cudaStream_t>(stream));
@@ -633,6 +712,7 @@ ol_status ol_cache_update(const ol_kv_cache* cache, void* updated_cache, const v
   if ((st = no_overlap(v, values, 2ull * v.batch * v.kv_heads * new_len * v.head_dim * elt_bytes(v.dtype))) != OL_OK)
     return st;
   if ((st = check_owner(v.ranges, v.nranges, v.owner)) != OL_OK) return st;
+  record_append(v, new_len);
   if (fault_injected()) return OL_ERR_INJECTED;
   AppendParams p = {};
   p.layout = OL_LAYOUT_CONTIGUOUS;
@@ -658,6 +738,7 @@ ol_status ol_paged_cache_update(const ol_paged_kv* kv, void* updated_pool, const
   if ((st = no_overlap(v, kv->block_table, sizeof(int32_t) * (size_t)kv->batch * kv->max_pages)) != OL_OK) return st;
   if ((st = check_pages(kv, positions_host, new_len, true, -1)) != OL_OK) return st;
   if ((st = check_owner(v.ranges, v.nranges, v.owner)) != OL_OK) return st;
+  record_append(v, new_len);
   if (fault_injected()) return OL_ERR_INJECTED;
   return launch_append_view(v, OL_LAYOUT_PAGED, kv, values, new_len, positions_dev, static_cast<cudaStream_t>(stream));
 }
@@ -669,6 +750,7 @@ ol_status ol_int4kv_append(const ol_int4_kv* cache, void* updated_codes, const v
   if (st != OL_OK) return st;
   if ((st = append_common(v, updated_codes, values_bf16, 1, positions_host, positions_dev)) != OL_OK) return st;
   if ((st = check_owner(v.ranges, v.nranges, v.owner)) != OL_OK) return st;
+  record_append(v, 1);
   if (fault_injected()) return OL_ERR_INJECTED;
   return launch_append_view(v, OL_LAYOUT_INT4, cache, values_bf16, 1, positions_dev, static_cast<cudaStream_t>(stream));
 }

@@ -81,3 +81,23 @@ def test_host_step_int4():
         np.testing.assert_array_equal(g, r)
     want = O.int4_attention(case.q, *planes, case.lens, cur_kv=case.new_kv)
     assert max_abs_err(out_h.numpy().astype(np.float64), want) <= TOL
+
+
+def test_stats_describe_a_real_step():
+    # the storage statistics of a step that ran on the GPU: no prefix copy, no
+    # allocation, the appended bytes and the history bytes read
+    B, Hq, Hkv, D, C = 2, 8, 2, 128, 64
+    w = Workload("st", "bf16", B, Hq, Hkv, D, C, "contiguous", seed=43)
+    case = make_case(w, lens=np.array([5, 64], np.int32))
+    cache_d = to_dev(contiguous_cache(case))
+    ws, n = host_workspace(B, Hq, Hkv, D)
+    out_h = pinned(np.zeros((B, Hq, D), np.float32))
+    ol.ol_reset_stats()
+    ol.ol_decode_step_host(ol.OL_LAYOUT_CONTIGUOUS, ol.kv_cache(cache_d), cache_d, pinned(case.q), Hq,
+                           pinned(case.new_kv), case.lens, 0.0, -1, out_h, ol.OL_F32, ws, n)
+    torch.cuda.synchronize()
+    s = ol.ol_last_call_stats()
+    assert s["storage_prefix_copied_bytes"] == 0 and s["storage_allocations"] == 0
+    assert s["storage_append_copied_bytes"] == 2 * B * Hkv * D * 2
+    assert s["kv_payload_bytes_read"] == 2 * (4 + 63) * Hkv * D * 2
+    assert ol.ol_total_stats()["calls"] == 1
