@@ -92,9 +92,16 @@ def recorded_traffic(workload: str):
 
 def step_bytes(w, lens):
     """Algorithmic HBM bytes of one step: K/V of every attended token (the new
-    token's K/V read from new_kv), the appended token written, q read, y written."""
+    token's K/V read from new_kv), the appended token written, q read, y written.
+    A chunked step appends T = w.chunk tokens per row and reads the union of its
+    query tokens' ranges once: history, the chunk's K/V, T queries and outputs."""
     elt = 2 if w.dtype == "bf16" else 4
     D = w.head_dim
+    T = w.chunk
+    if T > 1:
+        hist = float(np.sum(lens - T)) * w.kv_heads * 2 * D * elt
+        new = w.batch * w.kv_heads * T * 2 * D * elt
+        return hist + 2 * new + 2 * w.batch * w.q_heads * T * D * 2   # new K/V written and read; q and y
     if w.layout == "int4":
         kv_tok = 2 * (D // 2 + (D // 32) * 2 + D // 64)         # codes + fp16 scales + zero points, K and V
         hist = float(np.sum(lens - 1)) * w.kv_heads * kv_tok
@@ -222,10 +229,13 @@ class Setup:
         D = w.head_dim
         B, H = w.batch, w.kv_heads
         self.bytes_per_step = float(np.mean([step_bytes(w, l) for l in self.lens_list]))
-        self.q = torch.randn((B, w.q_heads, D), generator=gen, device=dev).to(torch.bfloat16)
-        self.new_kv = torch.randn((2, B, H, 1, D), generator=gen, device=dev).to(torch.bfloat16)
-        self.out = torch.empty((B, w.q_heads, D), dtype=torch.bfloat16, device=dev)
-        ws_bytes = ol.ol_workspace_size(B, w.q_heads, H, D)
+        T = w.chunk
+        qshape = (B, w.q_heads, T, D) if T > 1 else (B, w.q_heads, D)
+        self.q = torch.randn(qshape, generator=gen, device=dev).to(torch.bfloat16)
+        self.new_kv = torch.randn((2, B, H, T, D), generator=gen, device=dev).to(torch.bfloat16)
+        self.out = torch.empty(qshape, dtype=torch.bfloat16, device=dev)
+        ws_bytes = (ol.ol_workspace_size_chunk(B, w.q_heads, H, D, T) if T > 1 else
+                    ol.ol_workspace_size(B, w.q_heads, H, D))
         self.ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         self.ws_bytes = ws_bytes
         ol.ol_workspace_init(self.ws, ws_bytes)
@@ -292,6 +302,11 @@ class Setup:
     def step(self, i, stream=None):
         """Step i of the rotation: replica i % replicas, chain position i % chain."""
         r, c = i % self.replicas, i % self.chain
+        if self.w.chunk > 1:
+            self.ol.ol_chunk_step(self.layout, self.descs[r], self.updated[r], self.q, self.w.q_heads, self.w.chunk,
+                                  self.new_kv, self.lens_list[c], self.lens_d_list[c], 0.0, -1, self.out,
+                                  self.ol.OL_BF16, self.ws, self.ws_bytes, stream=stream)
+            return
         self.ol.ol_decode_step(self.layout, self.descs[r], self.updated[r], self.q, self.w.q_heads, self.new_kv,
                                self.lens_list[c], self.lens_d_list[c], 0.0, -1, self.out, self.ol.OL_BF16, self.ws,
                                self.ws_bytes, stream=stream)
@@ -375,8 +390,12 @@ def run_ours(args, rank, world, dist):
         "device_status": status,
         "clocks": clk.summary(),
     }
-    if not args.no_e2e:
+    if not args.no_e2e and w.chunk == 1:
         result["e2e"] = run_e2e(s, stream, K_e2e=min(K, 200 * R))
+    elif not args.no_e2e:
+        result["e2e"] = None  # the host-buffer call is a decode step; chunked steps run from device buffers
+    if w.chunk > 1:
+        result["config"]["chunk"] = w.chunk
     return result
 
 
@@ -428,7 +447,7 @@ def oracle_step_inputs(w, max_rows):
     from workloads import scaled
     rows = min(w.batch, max_rows)
     ws = scaled(w, batch=rows)
-    case = make_case(ws, seed=w.seed)
+    case = make_case(ws, seed=w.seed, history_len_offset=w.chunk)
     return O, ws, case
 
 
@@ -436,7 +455,17 @@ def run_oracle_steps(w, budget_s, max_rows):
     """Time the oracle's decode step (append + attention) on a sample of the workload."""
     from workloads import block_table, contiguous_cache, poisoned_pool
     O, ws, case = oracle_step_inputs(w, max_rows)
-    if w.layout == "contiguous":
+    if w.layout == "contiguous" and w.chunk > 1:
+        cache = contiguous_cache(case)
+        T = w.chunk
+        rng = np.random.default_rng(w.seed + 7)
+        q = bf16_from_f32(rng.standard_normal((ws.batch, ws.q_heads, T, ws.head_dim)).astype(np.float32))
+        kv = bf16_from_f32(rng.standard_normal((2, ws.batch, ws.kv_heads, T, ws.head_dim)).astype(np.float32))
+
+        def one():
+            O.cache_update(cache, kv, case.lens - T)
+            return O.chunk_attention(q, cache, case.lens, T)
+    elif w.layout == "contiguous":
         cache = contiguous_cache(case)
 
         def one():
@@ -474,14 +503,15 @@ def run_oracle_steps(w, budget_s, max_rows):
     sec = statistics.median(times)
     nbytes = step_bytes(ws, case.lens)
     return {"value": round(nbytes / sec / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{len(times)} oracle decode steps (append + attention, fp64) on the first {ws.batch} of "
+            "sample": f"{len(times)} oracle {'chunked' if w.chunk > 1 else 'decode'} steps (append + attention, "
+                      f"fp64) on the first {ws.batch} of "
                       f"{w.batch} rows of {w.name}; median {sec * 1e3:.1f} ms/step",
             "us_per_step": round(sec * 1e6, 1), "rows_tok_per_s": round(ws.batch / sec, 2)}
 
 
 def run_reference(args, rank, world):
     w = WORKLOADS[args.workload]
-    max_rows = {"qwen_b1_gqa7": 1, "ragged_b32": 4, "paged_b64": 2, "int4_b16": 1}[w.name]
+    max_rows = {"qwen_b1_gqa7": 1, "ragged_b32": 4, "paged_b64": 2, "int4_b16": 1, "chunk4_b32": 1}[w.name]
     K = args.steps if args.steps is not None else 3
     budget = 60.0
     res = run_oracle_steps(w, budget_s=min(budget, 10.0 * max(1, K)), max_rows=max_rows)
@@ -510,7 +540,7 @@ def main():
     result = run_ours(args, rank, world, dist)
     if rank == 0 and not args.no_cpu_baseline:
         w = WORKLOADS[args.workload]
-        max_rows = {"qwen_b1_gqa7": 1, "ragged_b32": 4, "paged_b64": 2, "int4_b16": 1}[w.name]
+        max_rows = {"qwen_b1_gqa7": 1, "ragged_b32": 4, "paged_b64": 2, "int4_b16": 1, "chunk4_b32": 1}[w.name]
         result["cpu_baseline"] = run_oracle_steps(w, budget_s=10.0, max_rows=max_rows)
     if dist is not None:
         dist.barrier()

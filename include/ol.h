@@ -289,6 +289,31 @@ OL_API ol_status ol_decode_step(int32_t layout, const void* cache_desc, void* up
                          int32_t out_dtype, void* workspace, size_t ws_bytes, ol_stream stream);
 
 /*
+ * Chunked step: multi-token append with causal attention inside the chunk
+ * (the Attention contract of page "Persistent input/output feedback", section
+ * Optional heterogeneous paged KV: causal by default, left window, every new
+ * token visible to itself and to the later tokens of the chunk). For every
+ * row b: write new_kv [2, batch, kv_heads, new_len, head_dim] at positions
+ * lens[b] - new_len .. lens[b] - 1 (in place, `updated` aliasing the
+ * descriptor's data pointer), then for every query token i of
+ * q [batch, q_heads, new_len, head_dim] attend positions
+ * [max(0, pos_i - window), pos_i] with pos_i = lens[b] - new_len + i
+ * (window < 0: [0, pos_i]) into out [batch, q_heads, new_len, head_dim].
+ * new_len = 1 is ol_decode_step. Contiguous and paged caches;
+ * OL_LAYOUT_INT4 returns OL_ERR_UNSUPPORTED. Requires
+ * new_len <= lens[b] <= capacity and ws_bytes >=
+ * ol_workspace_size_chunk(batch, q_heads, kv_heads, head_dim, new_len).
+ * Two launches on `stream` (the append, then one attention launch whose
+ * grid slice z serves query token z); every check runs before the first.
+ */
+OL_API size_t ol_workspace_size_chunk(int32_t batch, int32_t q_heads, int32_t kv_heads, int32_t head_dim,
+                                      int32_t new_len);
+OL_API ol_status ol_chunk_step(int32_t layout, const void* cache_desc, void* updated, const void* q,
+                               int32_t q_heads, int32_t new_len, const void* new_kv, const int32_t* lens_host,
+                               const int32_t* lens_dev, float scale, int32_t window, void* out, int32_t out_dtype,
+                               void* workspace, size_t ws_bytes, ol_stream stream);
+
+/*
  * Storage statistics of a call (page "Persistent input/output feedback",
  * sections Opt-in storage auditing through runtime events and Optional
  * heterogeneous paged KV: the storage_* reports and the direct call's
@@ -308,8 +333,10 @@ typedef struct {
   int64_t dequantized_bytes;           /* FLOAT bytes decoded from quantized history: 4 per element per (token,
                                           kv head, K or V), the current uncompressed token excluded; one decode
                                           serves the whole query group */
-  int64_t attended_tokens;             /* sum over rows and kv heads of the visible tokens, current one included */
-  int64_t kv_payload_bytes_read;       /* K/V payload bytes read from the cache for the visible history */
+  int64_t attended_tokens;             /* sum over query tokens, rows and kv heads of the visible tokens, the
+                                          current one included */
+  int64_t kv_payload_bytes_read;       /* K/V payload bytes of the visible history read from the cache, summed
+                                          over query tokens (a chunk's query tokens share most of it) */
   int64_t workspace_bytes;             /* workspace bytes the call's shapes require (bound on its scratch) */
 } ol_stats;
 

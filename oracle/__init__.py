@@ -132,6 +132,28 @@ def paged_attention(q, pool, block_table, lens, scale: Optional[float] = None, w
     return out
 
 
+def chunk_attention(q, cache, lens, new_len: int, scale: Optional[float] = None, window: int = -1) -> np.ndarray:
+    """Causal attention inside a chunk of new_len appended tokens (the Attention
+    contract of page "Persistent input/output feedback", section Optional
+    heterogeneous paged KV: causal masking by default, left window). Query
+    token i of row b sits at position p_i = lens[b] - new_len + i and attends
+    the visible range of that position, which is exactly a decode attention
+    over a prefix of p_i + 1 tokens. q [B, Hq, new_len, D]; the cache already
+    holds the appended tokens -> y [B, Hq, new_len, D] fp64."""
+    lens = _c(lens, np.int32)
+    return np.stack([decode_attention(np.ascontiguousarray(q[:, :, i, :]), cache, lens - new_len + i + 1,
+                                      scale=scale, window=window) for i in range(new_len)], axis=2)
+
+
+def paged_chunk_attention(q, pool, block_table, lens, new_len: int, scale: Optional[float] = None,
+                          window: int = -1) -> np.ndarray:
+    """chunk_attention over a paged pool."""
+    lens = _c(lens, np.int32)
+    return np.stack([paged_attention(np.ascontiguousarray(q[:, :, i, :]), pool, block_table,
+                                     lens - new_len + i + 1, scale=scale, window=window)
+                     for i in range(new_len)], axis=2)
+
+
 def cache_update(cache: np.ndarray, values, positions) -> None:
     """In place: cache [2, B, H, C, D]; values [2, B, H, new_len, D]; positions [B]."""
     assert cache.flags.c_contiguous

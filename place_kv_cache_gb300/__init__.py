@@ -32,7 +32,8 @@ SYMBOLS = ("ol_status_string", "ol_version", "ol_workspace_size", "ol_workspace_
            "ol_cache_bind", "ol_cache_unbind", "ol_cache_update", "ol_cache_update_rows",
            "ol_paged_cache_update", "ol_decode_attention", "ol_paged_decode_attention", "ol_int4kv_append",
            "ol_int4kv_decode_attention", "ol_decode_step", "ol_decode_step_noalloc", "ol_workspace_size_host",
-           "ol_decode_step_host", "ol_last_call_stats", "ol_total_stats", "ol_reset_stats")
+           "ol_decode_step_host", "ol_last_call_stats", "ol_total_stats", "ol_reset_stats",
+           "ol_workspace_size_chunk", "ol_chunk_step")
 
 
 class Stats(ctypes.Structure):
@@ -115,6 +116,8 @@ def load(build_if_missing: bool = True):
         "ol_decode_step": (st, [i32, vp, vp, vp, i32, vp, vp, vp, f32, i32, vp, i32, vp, sz, vp]),
         "ol_decode_step_noalloc": (st, [i32, vp, vp, vp, i32, vp, vp, vp, f32, i32, vp, i32, vp]),
         "ol_workspace_size_host": (sz, [i32, i32, i32, i32]),
+        "ol_workspace_size_chunk": (sz, [i32, i32, i32, i32, i32]),
+        "ol_chunk_step": (st, [i32, vp, vp, vp, i32, i32, vp, vp, vp, f32, i32, vp, i32, vp, sz, vp]),
         "ol_last_call_stats": (st, [vp]),
         "ol_total_stats": (st, [vp]),
         "ol_reset_stats": (None, []),
@@ -329,6 +332,20 @@ def ol_decode_step(layout: int, desc, updated, q, q_heads: int, new_kv, lens_hos
     _check(load().ol_decode_step(layout, ctypes.byref(desc), _ptr(updated), _ptr(q), q_heads, _ptr(new_kv), _ptr(lh),
                                  _ptr(lens_dev), scale, window, _ptr(out), out_dtype, _ptr(workspace), ws_bytes,
                                  _stream(stream)), "ol_decode_step")
+
+
+def ol_workspace_size_chunk(batch: int, q_heads: int, kv_heads: int, head_dim: int, new_len: int) -> int:
+    return load().ol_workspace_size_chunk(batch, q_heads, kv_heads, head_dim, new_len)
+
+
+def ol_chunk_step(layout: int, desc, updated, q, q_heads: int, new_len: int, new_kv, lens_host, lens_dev,
+                  scale: float, window: int, out, out_dtype: int, workspace, ws_bytes: int, stream=None):
+    """Append new_len tokens per row and attend causally inside the chunk:
+    q and out [B, Hq, new_len, D], new_kv [2, B, Hkv, new_len, D]."""
+    lh = _host_i32(lens_host)
+    _check(load().ol_chunk_step(layout, ctypes.byref(desc), _ptr(updated), _ptr(q), q_heads, new_len, _ptr(new_kv),
+                                _ptr(lh), _ptr(lens_dev), scale, window, _ptr(out), out_dtype, _ptr(workspace),
+                                ws_bytes, _stream(stream)), "ol_chunk_step")
 
 
 def ol_workspace_size_host(batch: int, q_heads: int, kv_heads: int, head_dim: int) -> int:

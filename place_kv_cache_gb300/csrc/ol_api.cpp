@@ -435,16 +435,17 @@ void record_append(const CacheView& v, int new_len) {
 // the cache is the visible range minus the current token when that one comes
 // from new_kv.
 void record_attention(const CacheView& v, const int32_t* lens_host, int window, int append, int cur_from_new,
-                      size_t ws_need) {
+                      size_t ws_need, int nq) {
   ol_stats s = {};
   s.calls = 1;
   int64_t visible = 0, hist = 0;
-  for (int b = 0; b < v.batch; ++b) {
-    const RowSplit rs = row_split(lens_host[b], window < 0 ? -1 : window, 16);
-    const int vis = rs.hi - rs.lo;
-    visible += vis;
-    hist += (cur_from_new && vis > 0) ? vis - 1 : vis;
-  }
+  for (int z = 0; z < nq; ++z)  // query token z of a chunk sees up to lens - nq + z
+    for (int b = 0; b < v.batch; ++b) {
+      const RowSplit rs = row_split(lens_host[b] - (nq - 1 - z), window < 0 ? -1 : window, 16);
+      const int vis = rs.hi - rs.lo;
+      visible += vis;
+      hist += (cur_from_new && vis > 0) ? vis - 1 : vis;
+    }
   s.attended_tokens = visible * v.kv_heads;
   s.kv_payload_bytes_read = 2 * hist * v.kv_heads * token_payload(v);
   if (v.layout == OL_LAYOUT_INT4) s.dequantized_bytes = 2 * hist * v.kv_heads * v.head_dim * 4;
@@ -456,10 +457,13 @@ void record_attention(const CacheView& v, const int32_t* lens_host, int window, 
   record(s);
 }
 
+// nq > 1: a chunked step's attention (query tokens z = 0..nq-1 per row, token z
+// at position lens - nq + z; q and y are [B, Hq, nq, D]). check_only: stop
+// after validation (nothing recorded, nothing launched).
 ol_status run_attention(int layout, const void* desc, const CacheView& v, const void* q, int q_heads,
                         const int32_t* lens_host, const int32_t* lens_dev, const void* new_kv, int append,
                         int cur_from_new, float scale, int window, void* out, int out_dtype, void* workspace,
-                        size_t ws_bytes, cudaStream_t stream) {
+                        size_t ws_bytes, cudaStream_t stream, int nq = 1, bool check_only = false) {
   if (!q || !lens_host || !lens_dev || !out || !workspace) return OL_ERR_NULL;
   if (q_heads <= 0 || q_heads % v.kv_heads != 0) return OL_ERR_SHAPE;
   if (v.head_dim > 256) return OL_ERR_UNSUPPORTED;
@@ -468,14 +472,15 @@ ol_status run_attention(int layout, const void* desc, const CacheView& v, const 
       (new_kv && !aligned16(new_kv)))
     return OL_ERR_ALIGN;
   const int D = v.head_dim;
+  const int min_len = nq > 1 ? nq : (append ? 1 : 0);
   for (int b = 0; b < v.batch; ++b) {
-    if (lens_host[b] < (append ? 1 : 0) || lens_host[b] > v.capacity) return OL_ERR_CAPACITY;
+    if (lens_host[b] < min_len || lens_host[b] > v.capacity) return OL_ERR_CAPACITY;
   }
   const size_t in_elt = v.layout == OL_LAYOUT_INT4 ? 2 : elt_bytes(v.dtype);
-  const size_t q_bytes = (size_t)v.batch * q_heads * D * in_elt;
-  const size_t out_bytes = (size_t)v.batch * q_heads * D * elt_bytes(out_dtype);
+  const size_t q_bytes = (size_t)v.batch * q_heads * nq * D * in_elt;
+  const size_t out_bytes = (size_t)v.batch * q_heads * nq * D * elt_bytes(out_dtype);
   const size_t kv_bytes = 2ull * v.batch * v.kv_heads * D * in_elt;
-  const size_t need = workspace_bytes(v.batch, q_heads, v.kv_heads, D);
+  const size_t need = workspace_bytes(v.batch, q_heads, v.kv_heads, D, nq);
   if (ws_bytes < need) return OL_ERR_WORKSPACE;
   ol_status st;
   if ((st = no_overlap(v, q, q_bytes)) != OL_OK) return st;
@@ -494,12 +499,13 @@ ol_status run_attention(int layout, const void* desc, const CacheView& v, const 
       std::vector<int32_t> pos(v.batch);
       for (int b = 0; b < v.batch; ++b) pos[b] = lens_host[b] - 1;
       if ((st = check_pages(c, pos.data(), 1, true, window)) != OL_OK) return st;
-    } else if ((st = check_pages(c, lens_host, 0, false, window)) != OL_OK) {
+    } else if ((st = check_pages(c, lens_host, 0, false, window < 0 ? -1 : window + nq - 1)) != OL_OK) {
       return st;
     }
   }
   if ((st = check_owner(v.ranges, v.nranges, v.owner)) != OL_OK) return st;
-  record_attention(v, lens_host, window, append, cur_from_new, need);
+  if (check_only) return OL_OK;
+  record_attention(v, lens_host, window, append, cur_from_new, need, nq);
   if (fault_injected()) return OL_ERR_INJECTED;
 
   AttnParams p = base_params(v, layout, desc);
@@ -512,7 +518,9 @@ ol_status run_attention(int layout, const void* desc, const CacheView& v, const 
   p.cur_from_new = cur_from_new;
   p.scale = scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
   p.scale_log2 = p.scale * 1.4426950408889634f;
-  p.window = window < 0 ? -1 : window;
+  p.window_q = window < 0 ? -1 : window;
+  p.window = window < 0 ? -1 : window + nq - 1;  // the union of the query tokens' ranges
+  p.nq = nq;
   p.out = out;
   p.out_dtype = out_dtype;
   p.inline_lens = v.batch <= kInlineRows ? 1 : 0;
@@ -522,7 +530,7 @@ ol_status run_attention(int layout, const void* desc, const CacheView& v, const 
   char* ws = static_cast<char*>(workspace);
   p.status = reinterpret_cast<int32_t*>(ws);
   p.counters = reinterpret_cast<uint32_t*>(ws + kStatusBytes);
-  p.partials = reinterpret_cast<float*>(ws + partials_offset(v.batch, v.kv_heads));
+  p.partials = reinterpret_cast<float*>(ws + partials_offset(v.batch, v.kv_heads, nq));
 
   const int sms = sm_count_cached();
   cudaError_t e;
@@ -652,8 +660,10 @@ static ol_status append_common(const CacheView& v, const void* updated, const vo
 }
 
 static ol_status launch_append_view(const CacheView& v, int layout, const void* desc, const void* values,
-                                    int32_t new_len, const int32_t* positions_dev, cudaStream_t s) {
+                                    int32_t new_len, const int32_t* positions_dev, cudaStream_t s,
+                                    int positions_are_lens = 0) {
   AppendParams p = {};
+  p.positions_are_lens = positions_are_lens;
   p.layout = layout;
   p.dtype = v.dtype;
   p.batch = v.batch;
@@ -817,6 +827,59 @@ static HostStaging host_staging(int32_t batch, int32_t q_heads, int32_t kv_heads
   h.out = h.lens + up((size_t)batch * 4);
   h.total = h.out + up((size_t)batch * q_heads * head_dim * 4);
   return h;
+}
+
+size_t ol_workspace_size_chunk(int32_t batch, int32_t q_heads, int32_t kv_heads, int32_t head_dim,
+                               int32_t new_len) {
+  if (batch < 0 || kv_heads <= 0 || q_heads <= 0 || q_heads % kv_heads != 0 || head_dim <= 0 || new_len < 1)
+    return 0;
+  return workspace_bytes(batch, q_heads, kv_heads, head_dim, new_len);
+}
+
+ol_status ol_chunk_step(int32_t layout, const void* cache_desc, void* updated, const void* q, int32_t q_heads,
+                        int32_t new_len, const void* new_kv, const int32_t* lens_host, const int32_t* lens_dev,
+                        float scale, int32_t window, void* out, int32_t out_dtype, void* workspace, size_t ws_bytes,
+                        ol_stream stream) {
+  CacheView v;
+  ol_status st = view_of(layout, cache_desc, v);
+  if (st != OL_OK) return st;
+  if (layout == OL_LAYOUT_INT4) return OL_ERR_UNSUPPORTED;
+  if (new_len < 1) return OL_ERR_SHAPE;
+  if (!lens_host) return OL_ERR_NULL;
+  // the append writes positions lens - new_len .. lens - 1 of every row
+  std::vector<int32_t> pos(v.batch);
+  for (int b = 0; b < v.batch; ++b) {
+    if (lens_host[b] < new_len || lens_host[b] > v.capacity) return OL_ERR_CAPACITY;
+    pos[b] = lens_host[b] - new_len;
+  }
+  if ((st = append_common(v, updated, new_kv, new_len, pos.data(), lens_dev)) != OL_OK) return st;
+  if (layout == OL_LAYOUT_PAGED) {
+    const ol_paged_kv* c = static_cast<const ol_paged_kv*>(cache_desc);
+    if ((st = no_overlap(v, c->block_table, sizeof(int32_t) * (size_t)c->batch * c->max_pages)) != OL_OK) return st;
+    if ((st = check_pages(c, pos.data(), new_len, true, -1)) != OL_OK) return st;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // every check of the attention first: an error return means nothing was written
+  if ((st = run_attention(layout, cache_desc, v, q, q_heads, lens_host, lens_dev, nullptr, 0, 0, scale, window, out,
+                          out_dtype, workspace, ws_bytes, s, new_len, true)) != OL_OK)
+    return st;
+  const size_t in_elt = elt_bytes(v.dtype);
+  if ((st = no_overlap(v, new_kv, 2ull * v.batch * v.kv_heads * new_len * v.head_dim * in_elt)) != OL_OK) return st;
+  if (overlaps(range_of(out, (size_t)v.batch * q_heads * new_len * v.head_dim * elt_bytes(out_dtype)),
+               range_of(new_kv, 2ull * v.batch * v.kv_heads * new_len * v.head_dim * in_elt)))
+    return OL_ERR_ALIAS;
+  if ((st = check_owner(v.ranges, v.nranges, v.owner)) != OL_OK) return st;
+  if (fault_injected()) return OL_ERR_INJECTED;
+  if ((st = launch_append_view(v, layout, cache_desc, new_kv, new_len, lens_dev, s, 1)) != OL_OK) return st;
+  st = run_attention(layout, cache_desc, v, q, q_heads, lens_host, lens_dev, nullptr, 0, 0, scale, window, out,
+                     out_dtype, workspace, ws_bytes, s, new_len);
+  // the call's one record: the attention's counts (recorded by run_attention) and the append's
+  const int64_t appended = 2ll * v.batch * v.kv_heads * new_len * token_payload(v);
+  for (ol_stats* r : {&t_last, &t_total}) {
+    r->storage_append_copied_bytes += appended;
+    r->storage_reuse_count += v.batch > 0 ? 2 : 0;
+  }
+  return st;
 }
 
 size_t ol_workspace_size_host(int32_t batch, int32_t q_heads, int32_t kv_heads, int32_t head_dim) {

@@ -16,7 +16,8 @@ __global__ void copy_rows_kernel(const AppendParams p) {
   const int b = blockIdx.x / (p.new_len * p.kv_heads);
   const int plane = blockIdx.y;
   const int D = p.head_dim;
-  const int pos = p.positions ? p.positions[b] : p.scalar_position;
+  int pos = p.positions ? p.positions[b] : p.scalar_position;
+  if (p.positions_are_lens) pos -= p.new_len;
   if (pos < 0 || (long long)pos + p.new_len > p.capacity) return;  // device guard
   const int t = pos + j;
   size_t dst;

@@ -119,6 +119,11 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -259,6 +264,29 @@ __device__ __forceinline__ Work map_cta_warp(const int32_t* __restrict__ lens, i
   return w;
 }
 
+// Grid roles. A decode step: x = CTA of the plan (clusters along x), y = the
+// CUDA-core kernel's query-head block. A chunked step (nq > 1): x = query
+// token, y = CTA of the plan (clusters along y), z = query-head block: the
+// query tokens of one split are adjacent in launch order, so they run side by
+// side and share the split's K/V tiles through L2.
+__device__ __forceinline__ int cta_index(const AttnParams& p) { return p.nq > 1 ? blockIdx.y : blockIdx.x; }
+__device__ __forceinline__ int query_index(const AttnParams& p) { return p.nq > 1 ? blockIdx.x : 0; }
+__device__ __forceinline__ int head_block(const AttnParams& p) { return p.nq > 1 ? blockIdx.z : blockIdx.y; }
+
+// Chunked steps: query token z = query_index of every row sits at position
+// hi - nq + z. Its visible range ends there (causal inside the chunk) and
+// starts window_q tokens before it; the plan's split stays and only the CTA's
+// range is clipped.
+__device__ __forceinline__ void slice_query(Work& w, const AttnParams& p) {
+  if (p.nq <= 1 || !w.valid) return;
+  const int hi = w.hi - (p.nq - 1 - query_index(p));
+  const int lo = p.window_q < 0 ? w.lo : max(hi - 1 - p.window_q, 0);
+  w.hi = hi;
+  w.lo = max(w.lo, lo);
+  w.t_end = min(w.t_end, hi);
+  if (w.t_end < w.t_begin) w.t_end = w.t_begin;
+}
+
 // Length of row b as the kernels read it: clamped to [0, capacity], with a
 // device status when it was out of range.
 __device__ __forceinline__ int read_len(const int32_t* __restrict__ lens, int b, int capacity, int32_t* status) {
@@ -379,17 +407,23 @@ __device__ __forceinline__ void finish_split(const AttnParams& p, const Work& w,
   const int tid = threadIdx.x;
   const int nthreads = blockDim.x;
   const int nh = h1 - h0, nd = d1 - d0;
-  const size_t out_base = ((size_t)w.b * p.q_heads + (size_t)w.g * G) * D;
+  // query token z of a chunked step: its own output rows, counters and partial slots
+  const int nq = p.nq > 1 ? p.nq : 1, z = query_index(p);
+  const size_t hstride = (size_t)nq * D;  // between query heads in y [B, Hq, nq, D]
+  const size_t out_base = (((size_t)w.b * p.q_heads + (size_t)w.g * G) * nq + z) * D;
+  float* const partials =
+      p.partials + (size_t)z * ((size_t)p.batch * p.kv_heads + kMaxExtraSplits) * G * (D + 2);  // max_ctas slots
+  uint32_t* const counters = p.counters + (size_t)z * p.batch * p.kv_heads;
   if (nslots == 1) {
     for (int i = tid; i < nh * nd; i += nthreads) {
       const int jl = i / nd, d = d0 + i % nd;
       const float l = sm_l[jl];
       const float y = l > 0.f ? sm_o[jl * o_stride + (d - d0)] / l : 0.f;
-      store_out(p.out, p.out_dtype, out_base + (size_t)(h0 + jl) * D + d, y);
+      store_out(p.out, p.out_dtype, out_base + (size_t)(h0 + jl) * hstride + d, y);
     }
     return;
   }
-  float* sl = p.partials + (size_t)slot * G * (D + 2);
+  float* sl = partials + (size_t)slot * G * (D + 2);
   for (int i = tid; i < nh * (nd + 2); i += nthreads) {
     const int jl = i / (nd + 2), e = i % (nd + 2);
     if (e < 2) {
@@ -401,7 +435,7 @@ __device__ __forceinline__ void finish_split(const AttnParams& p, const Work& w,
   __threadfence();
   __syncthreads();
   if (tid == 0) {
-    unsigned* ctr = p.counters + (size_t)w.b * p.kv_heads + w.g;
+    unsigned* ctr = counters + (size_t)w.b * p.kv_heads + w.g;
     const unsigned prev = atomicAdd(ctr, 1u);
     const int last = (prev == (unsigned)(arrivals - 1));
     if (last) atomicExch(ctr, 0u);  // leave the ticket at zero for the next call
@@ -410,7 +444,7 @@ __device__ __forceinline__ void finish_split(const AttnParams& p, const Work& w,
   __syncthreads();
   if (!*sm_flag) return;
   __threadfence();
-  const float* base = p.partials + (size_t)first_slot * G * (D + 2);
+  const float* base = partials + (size_t)first_slot * G * (D + 2);
   const size_t stride = (size_t)G * (D + 2);
   const int warp = tid >> 5, lane = tid & 31, nwarps = nthreads >> 5;
   for (int j = warp; j < G; j += nwarps) {
@@ -446,7 +480,7 @@ __device__ __forceinline__ void finish_split(const AttnParams& p, const Work& w,
         acc += ms == -INFINITY ? 0.f : ov * fast_exp2(ms - M);
       }
     }
-    store_out(p.out, p.out_dtype, out_base + (size_t)j * D + d, L > 0.f ? acc / L : 0.f);
+    store_out(p.out, p.out_dtype, out_base + (size_t)j * hstride + d, L > 0.f ? acc / L : 0.f);
   }
 }
 

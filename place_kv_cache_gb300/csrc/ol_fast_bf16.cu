@@ -93,9 +93,11 @@ __global__ void __launch_bounds__(NWARPS * 32, FastLayout<NWARPS, STAGES>::kPerS
   if (!p.inline_lens) pdl_wait();
   if (warp == 0) {
     Work w = p.inline_lens
-                 ? map_cta_warp(p.lens_inline, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, blockIdx.x,
+                 ? map_cta_warp(p.lens_inline, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, cta_index(p),
                                 nullptr, CS)
-                 : map_cta_warp(p.lens, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, blockIdx.x, p.status, CS);
+                 : map_cta_warp(p.lens, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, cta_index(p), p.status,
+                                CS);
+    slice_query(w, p);
     if (lane == 0) *sw = w;
   }
   __syncthreads();
@@ -111,7 +113,8 @@ __global__ void __launch_bounds__(NWARPS * 32, FastLayout<NWARPS, STAGES>::kPerS
   const int nsub = w.valid ? (w.t_end - w.t_begin + kTok - 1) / kTok : 0;
   const int my_n = nsub > warp ? (nsub - warp + NWARPS - 1) / NWARPS : 0;
   uint8_t* my_stages = stages + warp * STAGES * kStageBytes;
-  const uint64_t pol = policy_evict_first();
+  // a decode step reads each K/V byte once; a chunk's query tokens re-read it from L2
+  const uint64_t pol = p.nq > 1 ? policy_evict_normal() : policy_evict_first();
 
   // lane 0 issues the four TMA boxes of this warp's i-th tile into stage i % STAGES
   auto issue = [&](int i) {
@@ -143,7 +146,8 @@ __global__ void __launch_bounds__(NWARPS * 32, FastLayout<NWARPS, STAGES>::kPerS
   uint32_t qf[8][2];
   {
     const uint16_t* qp = reinterpret_cast<const uint16_t*>(p.q) +
-                         ((size_t)w.b * p.q_heads + (size_t)w.g * G + (n < G ? n : 0)) * 128;
+                         (((size_t)w.b * p.q_heads + (size_t)w.g * G + (n < G ? n : 0)) * (p.nq > 1 ? p.nq : 1) +
+                          query_index(p)) * 128;
     const bool live = n < G && w.valid;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
@@ -359,7 +363,8 @@ cudaError_t launch_cfg(const CUtensorMap& map, const AttnParams& p, cudaStream_t
   cudaError_t e = ensure_attrs<NWARPS, STAGES, PAGED>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.total_ctas, 1, 1);
+  const bool chunk = p.nq > 1;  // query tokens along x, the plan's CTAs (and clusters) along y
+  cfg.gridDim = chunk ? dim3(p.nq, p.total_ctas, 1) : dim3(p.total_ctas, 1, 1);
   cfg.blockDim = dim3(NWARPS * 32, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -367,8 +372,8 @@ cudaError_t launch_cfg(const CUtensorMap& map, const AttnParams& p, cudaStream_t
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = p.cluster;
-  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.x = chunk ? 1 : p.cluster;
+  attr[1].val.clusterDim.y = chunk ? p.cluster : 1;
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;

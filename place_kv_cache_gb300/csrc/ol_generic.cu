@@ -104,9 +104,10 @@ __global__ void __launch_bounds__(kGenWarps * 32) generic_attn_kernel(const __gr
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 0) {
     Work w = p.inline_lens ? map_cta_warp(p.lens_inline, p.batch, p.kv_heads, p.capacity, p.window, p.chunk,
-                                          blockIdx.x, nullptr)
-                           : map_cta_warp(p.lens, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, blockIdx.x,
+                                          cta_index(p), nullptr)
+                           : map_cta_warp(p.lens, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, cta_index(p),
                                           p.status);
+    slice_query(w, p);
     if (lane == 0) sw = w;
   }
   __syncthreads();
@@ -115,7 +116,7 @@ __global__ void __launch_bounds__(kGenWarps * 32) generic_attn_kernel(const __gr
 
   const int D = p.head_dim;
   const int G = p.group;
-  const int heads_lo = blockIdx.y * kGenHeads;
+  const int heads_lo = head_block(p) * kGenHeads;
   const int heads_hi = min(G, heads_lo + kGenHeads);
   const int nh = heads_hi - heads_lo;
   const int cur = p.cur_from_new ? w.hi - 1 : -1;
@@ -132,7 +133,8 @@ __global__ void __launch_bounds__(kGenWarps * 32) generic_attn_kernel(const __gr
       int d = lane + 32 * i;
       float qv = 0.f;
       if (j < nh && d < D) {
-        size_t qi = ((size_t)w.b * p.q_heads + (size_t)w.g * G + heads_lo + j) * D + d;
+        size_t qi = (((size_t)w.b * p.q_heads + (size_t)w.g * G + heads_lo + j) * (p.nq > 1 ? p.nq : 1) +
+                     query_index(p)) * D + d;
         qv = (p.dtype == OL_F32 && p.layout != OL_LAYOUT_INT4)
                  ? reinterpret_cast<const float*>(p.q)[qi]
                  : bf16_bits_to_float(reinterpret_cast<const uint16_t*>(p.q)[qi]);
@@ -215,11 +217,11 @@ __global__ void __launch_bounds__(kGenWarps * 32) generic_attn_kernel(const __gr
 
   // The fused append: the last split of (b, g) writes the new token. Nothing
   // in this launch reads that cache row (the attention takes it from new_kv).
-  if (p.append && w.s == w.nsplit - 1 && blockIdx.y == 0 && warp == 0 && w.hi >= 1)
+  if (p.append && w.s == w.nsplit - 1 && head_block(p) == 0 && warp == 0 && w.hi >= 1)
     append_token_warp(p, w.b, w.g, w.hi - 1);
 
-  finish_split(p, w, sm_m, sm_l, &sm_o[0][0], 256, heads_lo, heads_hi, 0, D, blockIdx.x, w.first_cta, w.nsplit,
-               w.nsplit * gridDim.y, &sm_flag, sm_scratch);
+  finish_split(p, w, sm_m, sm_l, &sm_o[0][0], 256, heads_lo, heads_hi, 0, D, cta_index(p), w.first_cta, w.nsplit,
+               w.nsplit * (p.nq > 1 ? gridDim.z : gridDim.y), &sm_flag, sm_scratch);
 }
 
 }  // namespace
@@ -227,7 +229,8 @@ __global__ void __launch_bounds__(kGenWarps * 32) generic_attn_kernel(const __gr
 cudaError_t launch_generic_attention(const AttnParams& p, cudaStream_t s) {
   if (p.total_ctas <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.total_ctas, (p.group + kGenHeads - 1) / kGenHeads, 1);
+  const int hb = (p.group + kGenHeads - 1) / kGenHeads;
+  cfg.gridDim = p.nq > 1 ? dim3(p.nq, p.total_ctas, hb) : dim3(p.total_ctas, hb, 1);
   cfg.blockDim = dim3(kGenWarps * 32, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;

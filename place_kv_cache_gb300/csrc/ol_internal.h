@@ -22,19 +22,21 @@ constexpr int kMaxExtraSplits = 4096;  // CTAs beyond one per (row, kv head)
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline size_t counters_bytes(int batch, int kv_heads) {
-  return align_up(sizeof(uint32_t) * (size_t)batch * (size_t)kv_heads, 256);
+// nq: query tokens per row (1 for a decode step, the chunk length for a
+// chunked step); every query token has its own counters and partial slots.
+inline size_t counters_bytes(int batch, int kv_heads, int nq = 1) {
+  return align_up(sizeof(uint32_t) * (size_t)nq * (size_t)batch * (size_t)kv_heads, 256);
 }
-inline size_t partials_offset(int batch, int kv_heads) {
-  return kStatusBytes + counters_bytes(batch, kv_heads);
+inline size_t partials_offset(int batch, int kv_heads, int nq = 1) {
+  return kStatusBytes + counters_bytes(batch, kv_heads, nq);
 }
 inline size_t max_ctas(int batch, int kv_heads) {
   return (size_t)batch * (size_t)kv_heads + kMaxExtraSplits;
 }
-inline size_t workspace_bytes(int batch, int q_heads, int kv_heads, int head_dim) {
+inline size_t workspace_bytes(int batch, int q_heads, int kv_heads, int head_dim, int nq = 1) {
   int group = q_heads / kv_heads;
-  return partials_offset(batch, kv_heads) +
-         max_ctas(batch, kv_heads) * (size_t)group * (size_t)(head_dim + 2) * sizeof(float);
+  return partials_offset(batch, kv_heads, nq) +
+         (size_t)nq * max_ctas(batch, kv_heads) * (size_t)group * (size_t)(head_dim + 2) * sizeof(float);
 }
 
 // One attention / decode-step launch, fully validated on the host.
@@ -65,7 +67,10 @@ struct AttnParams {
   int cur_from_new;     // 1: the token at lens[b]-1 is taken from new_kv, not the cache
   float scale;          // softmax scale
   float scale_log2;     // scale * log2(e)
-  int window;           // < 0: unbounded
+  int window;           // < 0: unbounded; with nq > 1 the window of the first query token
+                        // widened by nq - 1 (the union of the query tokens' ranges), for the plan
+  int nq;               // query tokens per row (grid z): token z attends up to position lens - nq + z
+  int window_q;         // the caller's window, per query token (< 0: unbounded)
   void* out;            // [B, Hq, D]
   int out_dtype;
 
@@ -103,6 +108,7 @@ struct AppendParams {
   const void* values;        // [2, B, Hkv, new_len, D]
   const int32_t* positions;  // device [B], or NULL: every row uses scalar_position
   int scalar_position;
+  int positions_are_lens;    // 1: positions[b] is a length and the append starts at positions[b] - new_len
 };
 
 // Launchers (return cudaSuccess or the launch error).

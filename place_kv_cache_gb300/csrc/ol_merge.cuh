@@ -185,7 +185,7 @@ __device__ __forceinline__ void merge_and_finish(const AttnParams& p, const Work
   }
   __syncthreads();
   if (!w.valid) return;
-  finish_split(p, w, ms.cm, ms.cl, cmerged, dspan, 0, G, d0, d0 + dspan, (int)(blockIdx.x / CS), w.first_cta / CS,
+  finish_split(p, w, ms.cm, ms.cl, cmerged, dspan, 0, G, d0, d0 + dspan, cta_index(p) / CS, w.first_cta / CS,
                w.nsplit / CS, w.nsplit, ms.flag, ms.scr);
 }
 

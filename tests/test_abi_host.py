@@ -278,3 +278,23 @@ def test_host_step_rejects_before_any_copy():
     assert lib.ol_decode_step_host(ol.OL_LAYOUT_CONTIGUOUS, ctypes.byref(d), CACHE, None, HQ, None, None, 0.0, -1,
                                    None, ol.OL_BF16, WS, ol.ol_workspace_size_host(B, HQ, HKV, D), None) \
         == ol.OL_ERR_NULL
+
+
+# ------------------------------------------------------------ chunked step
+
+def chunk(lens=(10, 64), new_len=4, ws_bytes=None, layout=ol.OL_LAYOUT_CONTIGUOUS, desc=None, updated=CACHE):
+    desc = ol.kv_cache(CACHE, dims=(B, HKV, C, D), dtype=ol.OL_BF16) if desc is None else desc
+    n = ol.ol_workspace_size_chunk(B, HQ, HKV, D, new_len) if ws_bytes is None else ws_bytes
+    ol.ol_chunk_step(layout, desc, updated, Q, HQ, new_len, NEWKV, np.array(lens, np.int32), LENS_DEV, 0.0, -1, OUT,
+                     ol.OL_BF16, WS, n, stream=0)
+
+
+def test_chunk_step_validation():
+    assert status_of(chunk) == ol.OL_ERR_INJECTED
+    assert status_of(chunk, lens=(3, 64)) == ol.OL_ERR_CAPACITY          # a row shorter than the chunk
+    assert status_of(chunk, lens=(10, C + 1)) == ol.OL_ERR_CAPACITY
+    assert status_of(chunk, new_len=0) == ol.OL_ERR_SHAPE
+    assert status_of(chunk, ws_bytes=ol.ol_workspace_size(B, HQ, HKV, D)) == ol.OL_ERR_WORKSPACE
+    assert status_of(chunk, updated=CACHE + 256) == ol.OL_ERR_ALIAS
+    assert status_of(chunk, desc=int4_desc(), updated=CODES, layout=ol.OL_LAYOUT_INT4) == ol.OL_ERR_UNSUPPORTED
+    assert ol.ol_workspace_size_chunk(B, HQ, HKV, D, 4) > ol.ol_workspace_size(B, HQ, HKV, D)

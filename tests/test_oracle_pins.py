@@ -488,3 +488,70 @@ def test_four_step_fixture_tolerance():
         worst = max(worst, float(np.abs(y4h - yd).max()))
     assert worst <= 0.15
     assert worst > 0.0                                  # quantization did change the values
+
+
+# ------------------------------------------------------------ chunked steps
+
+def _causal_brute_force(q, k, v, pos, scale, window):
+    """Full score matrix with a causal (and left-window) mask, row softmax,
+    weighted sum: written independently of the oracle, in float64.
+    q [T, D] for one (row, head); k, v [C, D]; pos [T] query positions."""
+    s = (q @ k.T) * scale
+    t = np.arange(k.shape[0])[None, :]
+    lo = pos[:, None] - (window if window >= 0 else 10 ** 9)
+    mask = (t <= pos[:, None]) & (t >= lo)
+    s = np.where(mask, s, -np.inf)
+    w = np.exp(s - s.max(axis=1, keepdims=True))
+    w /= w.sum(axis=1, keepdims=True)
+    return w @ v
+
+
+@pytest.mark.parametrize("window", [-1, 0, 3])
+def test_chunk_attention_equals_masked_brute_force(window):
+    rng = np.random.default_rng(71)
+    B, Hq, Hkv, D, C, T = 2, 4, 2, 8, 12, 3
+    cache = rng.standard_normal((2, B, Hkv, C, D)).astype(np.float32)
+    q = rng.standard_normal((B, Hq, T, D)).astype(np.float32)
+    lens = np.array([T, 10], np.int32)              # row 0: the chunk is the whole row
+    y = O.chunk_attention(q, cache, lens, T, window=window)
+    scale = 1.0 / math.sqrt(D)
+    for b in range(B):
+        pos = lens[b] - T + np.arange(T)
+        for h in range(Hq):
+            g = h // (Hq // Hkv)
+            want = _causal_brute_force(q[b, h].astype(np.float64), cache[0, b, g].astype(np.float64),
+                                       cache[1, b, g].astype(np.float64), pos, scale, window)
+            np.testing.assert_allclose(y[b, h], want, rtol=0, atol=1e-12)
+
+
+def test_chunk_first_query_ignores_later_chunk_tokens():
+    # causality inside the chunk: changing the K/V of chunk tokens 1.. leaves
+    # query token 0 unchanged, and changes query token 1
+    rng = np.random.default_rng(72)
+    B, Hq, Hkv, D, C, T = 1, 2, 1, 8, 16, 3
+    cache = rng.standard_normal((2, B, Hkv, C, D)).astype(np.float32)
+    q = rng.standard_normal((B, Hq, T, D)).astype(np.float32)
+    lens = np.array([9], np.int32)
+    y0 = O.chunk_attention(q, cache, lens, T)
+    cache2 = cache.copy()
+    cache2[:, 0, 0, 7:9] += 5.0                      # chunk tokens 1 and 2 (positions 7, 8)
+    y1 = O.chunk_attention(q, cache2, lens, T)
+    np.testing.assert_array_equal(y0[:, :, 0], y1[:, :, 0])
+    assert np.abs(y0[:, :, 1] - y1[:, :, 1]).max() > 1e-3
+
+
+def test_paged_chunk_equals_contiguous_chunk():
+    rng = np.random.default_rng(73)
+    B, Hq, Hkv, D, S, M, T = 2, 4, 2, 8, 4, 5, 4
+    C = S * M
+    cache = rng.standard_normal((2, B, Hkv, C, D)).astype(np.float32)
+    q = rng.standard_normal((B, Hq, T, D)).astype(np.float32)
+    perm = rng.permutation(B * M).astype(np.int32)
+    table = perm.reshape(B, M)
+    pool = np.zeros((2, B * M, Hkv, S, D), np.float32)
+    for b in range(B):
+        for j in range(M):
+            pool[:, table[b, j]] = cache[:, b, :, j * S:(j + 1) * S]
+    lens = np.array([7, 20], np.int32)
+    np.testing.assert_array_equal(O.paged_chunk_attention(q, pool, table, lens, T, window=5),
+                                  O.chunk_attention(q, cache, lens, T, window=5))

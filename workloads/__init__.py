@@ -67,6 +67,7 @@ class Workload:
     steps: int = 1                             # chained decode steps
     dist: str = "normal"                       # "normal" (N(0,1)) or "uniform" (U[-1,1])
     block: int = 32                            # INT4 block along head_dim
+    chunk: int = 1                             # tokens appended and attended per row per step
 
     @property
     def group(self) -> int:
@@ -92,6 +93,11 @@ WORKLOADS = {
                           lens_range=(1, 16384), page_size=16, num_pages=65536),
     "int4_b16": Workload("int4_b16", "bf16", 16, 32, 8, 128, 32768, "int4", seed=5,
                          lens_fixed=16385, steps=64),
+    # chunked step (multi-token append, causal inside the chunk): the ragged
+    # shape with 4 tokens per row per step, as a speculative-decoding verifier
+    # appends and scores its drafted tokens
+    "chunk4_b32": Workload("chunk4_b32", "bf16", 32, 32, 8, 128, 8192, "contiguous",
+                           seed=6, lens_range=(512, 8192), chunk=4),
 }
 
 
