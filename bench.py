@@ -60,14 +60,14 @@ def measured_peaks():
 
 
 def kernel_sources_sha() -> str:
-    """sha256 over the library's device-code sources (.cu, .cuh, .h: file name
+    """sha256 over the library's device-code sources (.cu, .cuh, .h, .inc: file name
     and content, in name order): a recorded DRAM traffic figure holds only for
     the kernel sources it was measured on."""
     import hashlib
     d = os.path.join(ROOT, "place_kv_cache_gb300", "csrc")
     h = hashlib.sha256()
     for name in sorted(os.listdir(d)):
-        if name.endswith((".cu", ".cuh", ".h")):
+        if name.endswith((".cu", ".cuh", ".h", ".inc")):
             h.update(name.encode() + b"\0")
             with open(os.path.join(d, name), "rb") as f:
                 h.update(f.read())

@@ -138,6 +138,7 @@ void plan_fast(AttnParams& p, const int32_t* lens_host, int sms) {
   else
     p.variant = (units >= sms && p.layout == OL_LAYOUT_PAGED) ? 2 : 3;
   if (int4 && p.variant > 2) p.variant = 0;
+  if (!int4 && p.nq > 1 && p.variant != 2) p.variant = 3;  // chunked steps: the variants built for them
   const int smem = (int4 ? fast_int4_smem(p.variant) : fast_bf16_smem(p.variant)) + 1024;
   const int warps = int4 ? fast_int4_warps(p.variant) : fast_bf16_warps(p.variant);
   int per_sm = (228 * 1024) / smem;
@@ -534,7 +535,10 @@ ol_status run_attention(int layout, const void* desc, const CacheView& v, const 
 
   const int sms = sm_count_cached();
   cudaError_t e;
+  p.tq = 1;
   if (layout != OL_LAYOUT_INT4 && fast_bf16_supported(p)) {
+    // a chunk's query tokens share a CTA as extra MMA columns: 8 / group of them
+    if (nq > 1) p.tq = std::max(1, std::min(nq, 8 / p.group));
     plan_fast(p, lens_host, sms);
     e = launch_fast_bf16(p, stream);
   } else if (layout == OL_LAYOUT_INT4 && fast_int4_supported(p)) {

@@ -273,17 +273,29 @@ __device__ __forceinline__ int cta_index(const AttnParams& p) { return p.nq > 1 
 __device__ __forceinline__ int query_index(const AttnParams& p) { return p.nq > 1 ? blockIdx.x : 0; }
 __device__ __forceinline__ int head_block(const AttnParams& p) { return p.nq > 1 ? blockIdx.z : blockIdx.y; }
 
-// Chunked steps: query token z = query_index of every row sits at position
-// hi - nq + z. Its visible range ends there (causal inside the chunk) and
-// starts window_q tokens before it; the plan's split stays and only the CTA's
-// range is clipped.
+// A CTA's state columns: column c is query token c / group of the CTA's slice
+// (tq tokens from slice_first) and head c % group; group * tq columns.
+__device__ __forceinline__ int slice_tq(const AttnParams& p) { return p.nq > 1 && p.tq > 1 ? p.tq : 1; }
+__device__ __forceinline__ int state_cols(const AttnParams& p) { return p.group * slice_tq(p); }
+__device__ __forceinline__ int slice_first(const AttnParams& p) { return query_index(p) * slice_tq(p); }
+__device__ __forceinline__ int slice_tokens(const AttnParams& p) {
+  return p.nq > 1 ? min(slice_tq(p), p.nq - slice_first(p)) : 1;
+}
+
+// Chunked steps: query token z of every row sits at position hi - nq + z; its
+// visible range ends there (causal inside the chunk) and starts window_q
+// tokens before it. A CTA serves the slice's tokens: its range is clipped to
+// the union of theirs (the first token's start to the last token's end), and
+// the kernel masks each column to its own token's range. The plan's split
+// stays.
 __device__ __forceinline__ void slice_query(Work& w, const AttnParams& p) {
   if (p.nq <= 1 || !w.valid) return;
-  const int hi = w.hi - (p.nq - 1 - query_index(p));
-  const int lo = p.window_q < 0 ? w.lo : max(hi - 1 - p.window_q, 0);
-  w.hi = hi;
+  const int hi_first = w.hi - (p.nq - 1 - slice_first(p));
+  const int hi_last = hi_first + slice_tokens(p) - 1;
+  const int lo = p.window_q < 0 ? w.lo : max(hi_first - 1 - p.window_q, 0);
+  w.hi = hi_last;
   w.lo = max(w.lo, lo);
-  w.t_end = min(w.t_end, hi);
+  w.t_end = min(w.t_end, hi_last);
   if (w.t_end < w.t_begin) w.t_end = w.t_begin;
 }
 
@@ -396,7 +408,8 @@ __device__ __forceinline__ void store_out(void* out, int out_dtype, size_t idx, 
 //   M = max_s m_s, L = sum_s l_s 2^(m_s - M), y = sum_s o_s 2^(m_s - M) / L.
 // The merge first reduces (M, L) per head (one warp per head, lanes over the
 // slots), then each output element reads its slots with independent loads.
-// `scratch` is shared memory for 2 * group floats.
+// `scratch` is shared memory for 2 * state_cols(p) floats. The state's
+// columns are (query token, head) pairs (see state_cols).
 // Block-wide: every thread of the CTA must call it.
 __device__ __forceinline__ void finish_split(const AttnParams& p, const Work& w, const float* sm_m,
                                              const float* sm_l, const float* sm_o, int o_stride, int h0,
@@ -404,26 +417,32 @@ __device__ __forceinline__ void finish_split(const AttnParams& p, const Work& w,
                                              int arrivals, int* sm_flag, float* scratch) {
   const int D = p.head_dim;
   const int G = p.group;
+  const int NC = state_cols(p);  // state columns: (query token, head) pairs
   const int tid = threadIdx.x;
   const int nthreads = blockDim.x;
   const int nh = h1 - h0, nd = d1 - d0;
-  // query token z of a chunked step: its own output rows, counters and partial slots
-  const int nq = p.nq > 1 ? p.nq : 1, z = query_index(p);
-  const size_t hstride = (size_t)nq * D;  // between query heads in y [B, Hq, nq, D]
-  const size_t out_base = (((size_t)w.b * p.q_heads + (size_t)w.g * G) * nq + z) * D;
+  // a chunked step's slice zs: its own counters and partial slots; column c
+  // goes to query token z0 + c / G, head c % G of y [B, Hq, nq, D]
+  const int nq = p.nq > 1 ? p.nq : 1, zs = query_index(p), z0 = slice_first(p);
+  const size_t head_base = (size_t)w.b * p.q_heads + (size_t)w.g * G;
+  auto out_at = [&](int c, int d) -> size_t {
+    if (nq == 1) return (head_base + c) * D + d;  // a decode step: column = head
+    return ((head_base + c % G) * nq + z0 + c / G) * D + d;
+  };
+  const int c_live = G * slice_tokens(p);  // columns past it belong to tokens beyond the chunk
   float* const partials =
-      p.partials + (size_t)z * ((size_t)p.batch * p.kv_heads + kMaxExtraSplits) * G * (D + 2);  // max_ctas slots
-  uint32_t* const counters = p.counters + (size_t)z * p.batch * p.kv_heads;
+      p.partials + (size_t)zs * ((size_t)p.batch * p.kv_heads + kMaxExtraSplits) * NC * (D + 2);  // max_ctas slots
+  uint32_t* const counters = p.counters + (size_t)zs * p.batch * p.kv_heads;
   if (nslots == 1) {
     for (int i = tid; i < nh * nd; i += nthreads) {
       const int jl = i / nd, d = d0 + i % nd;
       const float l = sm_l[jl];
       const float y = l > 0.f ? sm_o[jl * o_stride + (d - d0)] / l : 0.f;
-      store_out(p.out, p.out_dtype, out_base + (size_t)(h0 + jl) * hstride + d, y);
+      if (h0 + jl < c_live) store_out(p.out, p.out_dtype, out_at(h0 + jl, d), y);
     }
     return;
   }
-  float* sl = partials + (size_t)slot * G * (D + 2);
+  float* sl = partials + (size_t)slot * NC * (D + 2);
   for (int i = tid; i < nh * (nd + 2); i += nthreads) {
     const int jl = i / (nd + 2), e = i % (nd + 2);
     if (e < 2) {
@@ -444,10 +463,10 @@ __device__ __forceinline__ void finish_split(const AttnParams& p, const Work& w,
   __syncthreads();
   if (!*sm_flag) return;
   __threadfence();
-  const float* base = partials + (size_t)first_slot * G * (D + 2);
-  const size_t stride = (size_t)G * (D + 2);
+  const float* base = partials + (size_t)first_slot * NC * (D + 2);
+  const size_t stride = (size_t)NC * (D + 2);
   const int warp = tid >> 5, lane = tid & 31, nwarps = nthreads >> 5;
-  for (int j = warp; j < G; j += nwarps) {
+  for (int j = warp; j < NC; j += nwarps) {
     float M = -INFINITY;
     for (int s = lane; s < nslots; s += 32) M = fmaxf(M, __ldcg(base + s * stride + (size_t)j * (D + 2)));
 #pragma unroll
@@ -467,7 +486,7 @@ __device__ __forceinline__ void finish_split(const AttnParams& p, const Work& w,
     }
   }
   __syncthreads();
-  for (int i = tid; i < G * D; i += nthreads) {
+  for (int i = tid; i < c_live * D; i += nthreads) {
     const int j = i / D, d = i % D;
     const float M = scratch[2 * j], L = scratch[2 * j + 1];
     float acc = 0.f;
@@ -480,7 +499,7 @@ __device__ __forceinline__ void finish_split(const AttnParams& p, const Work& w,
         acc += ms == -INFINITY ? 0.f : ov * fast_exp2(ms - M);
       }
     }
-    store_out(p.out, p.out_dtype, out_base + (size_t)j * hstride + d, L > 0.f ? acc / L : 0.f);
+    store_out(p.out, p.out_dtype, out_at(j, d), L > 0.f ? acc / L : 0.f);
   }
 }
 

@@ -33,10 +33,14 @@ inline size_t partials_offset(int batch, int kv_heads, int nq = 1) {
 inline size_t max_ctas(int batch, int kv_heads) {
   return (size_t)batch * (size_t)kv_heads + kMaxExtraSplits;
 }
+// A partial slot holds one CTA's state columns: the query group's heads, or for
+// a chunked step up to 8 (query token, head) pairs (never more than nq * group
+// columns over all of a chunk's slices, and never more than 8 per slice).
 inline size_t workspace_bytes(int batch, int q_heads, int kv_heads, int head_dim, int nq = 1) {
   int group = q_heads / kv_heads;
+  const size_t cols = nq > 1 ? (size_t)nq * (size_t)(group > 8 ? group : 8) : (size_t)group;
   return partials_offset(batch, kv_heads, nq) +
-         (size_t)nq * max_ctas(batch, kv_heads) * (size_t)group * (size_t)(head_dim + 2) * sizeof(float);
+         cols * max_ctas(batch, kv_heads) * (size_t)(head_dim + 2) * sizeof(float);
 }
 
 // One attention / decode-step launch, fully validated on the host.
@@ -69,7 +73,9 @@ struct AttnParams {
   float scale_log2;     // scale * log2(e)
   int window;           // < 0: unbounded; with nq > 1 the window of the first query token
                         // widened by nq - 1 (the union of the query tokens' ranges), for the plan
-  int nq;               // query tokens per row (grid z): token z attends up to position lens - nq + z
+  int nq;               // query tokens per row: token z attends up to position lens - nq + z
+  int tq;               // query tokens per CTA slice (state columns = group * tq, at most 8 for the
+                        // tensor-core kernel); a chunked step has ceil(nq / tq) slices
   int window_q;         // the caller's window, per query token (< 0: unbounded)
   void* out;            // [B, Hq, D]
   int out_dtype;

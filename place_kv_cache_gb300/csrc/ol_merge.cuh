@@ -99,7 +99,7 @@ __device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t addr) {
 template <typename StateO>
 __device__ __forceinline__ void merge_and_finish(const AttnParams& p, const Work& w, int nstates, StateO state_o,
                                                  float* merged, float* cmerged, const MergeScratch& ms) {
-  const int G = p.group;
+  const int G = state_cols(p);  // state columns: the heads, or (query token, head) pairs
   const int CS = p.cluster;
   __syncthreads();
   if (threadIdx.x < 8) {  // one thread per head: maximum, weights 2^(m_s - M), sum
