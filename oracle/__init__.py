@@ -70,6 +70,11 @@ def lib():
         L.orc_fp16_to_double.restype = f64
         L.orc_float_to_fp16.argtypes = [f32]
         L.orc_float_to_fp16.restype = ctypes.c_uint16
+        L.orc_hf_encode_row.argtypes = [vp, i32, vp, vp]
+        L.orc_hf_decode_row.argtypes = [vp, i32, vp, vp]
+        L.orc_hpaged_append.argtypes = [vp, vp, i32, i32, i32, i32, vp, i32, i32, vp, i32, vp, vp]
+        L.orc_hpaged_attention.argtypes = [vp, i32, vp, vp, i32, i32, i32, i32, vp, i32, i32, vp, vp, f64, i32, vp]
+        L.orc_hpaged_quantize.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, i32, vp]
         _lib = L
     return _lib
 
@@ -258,3 +263,90 @@ def fp16_to_float(bits: int) -> float:
 
 def float_to_fp16(f: float) -> int:
     return int(lib().orc_float_to_fp16(float(f)))
+
+
+# ------------------------------------------------ heterogeneous paged pages
+
+# Page formats (the oracle's own numbering, which the library's enumeration
+# mirrors): dense FLOAT, FLOAT16, BFLOAT16; affine INT8, UINT8, INT4, UINT4,
+# INT2, UINT2.
+HF_F32, HF_F16, HF_BF16, HF_I8, HF_U8, HF_I4, HF_U4, HF_I2, HF_U2 = range(9)
+HF_BITS = {HF_F32: 32, HF_F16: 16, HF_BF16: 16, HF_I8: 8, HF_U8: 8, HF_I4: 4, HF_U4: 4, HF_I2: 2, HF_U2: 2}
+HF_RANGE = {HF_I8: (-128, 127), HF_U8: (0, 255), HF_I4: (-8, 7), HF_U4: (0, 15), HF_I2: (-2, 1), HF_U2: (0, 3)}
+
+# one page's descriptor: (format, scale, zero point) of K, then of V
+PAGE_DESC = np.dtype([("kf", "<i4"), ("ks", "<f4"), ("kz", "<i4"), ("vf", "<i4"), ("vs", "<f4"), ("vz", "<i4")])
+
+
+def page_desc(k=(HF_BF16, 1.0, 0), v=(HF_BF16, 1.0, 0)) -> np.ndarray:
+    """A one-element descriptor array for K format k and V format v."""
+    d = np.zeros(1, PAGE_DESC)
+    d["kf"], d["ks"], d["kz"] = k
+    d["vf"], d["vs"], d["vz"] = v
+    return d
+
+
+def hpaged_pool(P: int, H: int, S: int, D: int):
+    """Zeroed page slots [P, 2 * H * S * D * 4] bytes and descriptors [P] (all BFLOAT16)."""
+    desc = np.zeros(P, PAGE_DESC)
+    desc["kf"] = HF_BF16
+    desc["vf"] = HF_BF16
+    return np.zeros((P, 2 * H * S * D * 4), np.uint8), desc
+
+
+def hf_encode_row(x_bf16, fmt) -> np.ndarray:
+    """Codes of one row of D bf16 values in plane format fmt = (format, scale, zp)."""
+    x = _c(x_bf16, np.uint16)
+    D = x.shape[0]
+    out = np.zeros((D * HF_BITS[fmt[0]] + 7) // 8, np.uint8)
+    f = page_desc(k=fmt)
+    _check(lib().orc_hf_encode_row(_ptr(x), D, _ptr(f), _ptr(out)), "hf_encode_row")
+    return out
+
+
+def hf_decode_row(row, D: int, fmt) -> np.ndarray:
+    """fp32 reconstructions (as fp64) of one row of D elements in format fmt."""
+    r = _c(row, np.uint8)
+    out = np.zeros(D, np.float64)
+    f = page_desc(k=fmt)
+    _check(lib().orc_hf_decode_row(_ptr(r), D, _ptr(f), _ptr(out)), "hf_decode_row")
+    return out
+
+
+def hpaged_append(pool, desc, block_table, values, positions, new_fmt) -> None:
+    """In place: values [2, B, H, new_len, D] bf16 at positions [B]; new_fmt a
+    one-element PAGE_DESC array for pages the append starts."""
+    assert pool.flags.c_contiguous and desc.flags.c_contiguous
+    bt, values, positions = _c(block_table, np.int32), _c(values, np.uint16), _c(positions, np.int32)
+    _, B, H, new_len, D = values.shape
+    P = pool.shape[0]
+    S = pool.shape[1] // (2 * H * D * 4)
+    _check(lib().orc_hpaged_append(_ptr(pool), _ptr(desc), P, H, S, D, _ptr(bt), bt.shape[1], B, _ptr(values),
+                                   new_len, _ptr(positions), _ptr(_c(new_fmt, PAGE_DESC))), "hpaged_append")
+
+
+def hpaged_attention(q, pool, desc, block_table, lens, H: int, cur_kv=None, scale: Optional[float] = None,
+                     window: int = -1) -> np.ndarray:
+    """q [B, Hq, D] bf16 over the heterogeneous pages (H kv heads) -> y fp64."""
+    q, bt, lens = _c(q, np.uint16), _c(block_table, np.int32), _c(lens, np.int32)
+    B, Hq, D = q.shape
+    P = pool.shape[0]
+    S = pool.shape[1] // (2 * H * D * 4)
+    out = np.zeros((B, Hq, D), np.float64)
+    s = default_scale(D) if scale is None else scale
+    cur = None if cur_kv is None else _c(cur_kv, np.uint16)
+    _check(lib().orc_hpaged_attention(_ptr(q), Hq, _ptr(_c(pool, np.uint8)), _ptr(_c(desc, PAGE_DESC)), P, H, S,
+                                      D, _ptr(bt), bt.shape[1], B, _ptr(lens), _ptr(cur), s, window, _ptr(out)),
+           "hpaged_attention")
+    return out
+
+
+def hpaged_quantize(pool, desc, H: int, D: int, pages, valid, to_fmt) -> None:
+    """In place (QuantizePagedCache): the selected pages' valid prefixes converted
+    to to_fmt (a one-element PAGE_DESC array), the rest zero in that format."""
+    assert pool.flags.c_contiguous and desc.flags.c_contiguous
+    pg, va = _c(pages, np.int32), _c(valid, np.int32)
+    P = pool.shape[0]
+    S = pool.shape[1] // (2 * H * D * 4)
+    _check(lib().orc_hpaged_quantize(_ptr(pool), _ptr(desc), P, H, S, D, _ptr(pg), _ptr(va), pg.shape[0],
+                                     _ptr(_c(to_fmt, PAGE_DESC))), "hpaged_quantize")

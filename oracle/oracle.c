@@ -488,3 +488,321 @@ int orc_int4_attention(const uint16_t* q, int Hq, const uint8_t* codes, const ui
   free(V);
   return rc;
 }
+
+/* ------------------------------------------- heterogeneous paged pages */
+
+/*
+ * A paged cache whose pages each carry their own K and V storage formats
+ * (page "Persistent input/output feedback", sections Optional heterogeneous
+ * paged KV and Selected-block quantization; the code packing of page "Custom,
+ * quantized, and persistent values", affine branch: four-bit codes two per
+ * byte and two-bit codes four per byte, least-significant bits first).
+ *
+ * Layout (the same one the library documents): num_pages slots of
+ * 2 * Hkv * S * D * 4 bytes; plane k (0 = K, 1 = V) of page p starts at
+ * p * slot + k * Hkv * S * D * 4; within a plane of format f the codes of
+ * (head h, slot s) start at (h * S + s) * row_bytes(f) and hold the D
+ * elements in order. Descriptor of a plane: format, scale, zero point.
+ *
+ * Formats: dense FLOAT, FLOAT16, BFLOAT16; affine INT8, UINT8, INT4, UINT4,
+ * INT2, UINT2 with value = (code - zero_point) * scale.
+ *   encode (QuantizeLinear): code = saturate(round_half_even(x / scale) + zp)
+ *     to the type's range, in IEEE fp32; dense: the value rounded to nearest
+ *     even in the dense type.
+ *   decode (DequantizeLinear): (code - zp) * scale in fp32; dense: exact.
+ */
+enum { ORC_HF_F32 = 0, ORC_HF_F16, ORC_HF_BF16, ORC_HF_I8, ORC_HF_U8, ORC_HF_I4, ORC_HF_U4, ORC_HF_I2, ORC_HF_U2 };
+
+typedef struct {
+  int32_t format;
+  float scale;
+  int32_t zero_point;
+} orc_plane_fmt;
+
+typedef struct {
+  orc_plane_fmt k, v;
+} orc_page_desc;
+
+int orc_hf_bits(int f) {
+  switch (f) {
+    case ORC_HF_F32: return 32;
+    case ORC_HF_F16: case ORC_HF_BF16: return 16;
+    case ORC_HF_I8: case ORC_HF_U8: return 8;
+    case ORC_HF_I4: case ORC_HF_U4: return 4;
+    case ORC_HF_I2: case ORC_HF_U2: return 2;
+  }
+  return 0;
+}
+static int hf_affine(int f) { return f >= ORC_HF_I8 && f <= ORC_HF_U2; }
+static int hf_signed(int f) { return f == ORC_HF_I8 || f == ORC_HF_I4 || f == ORC_HF_I2; }
+/* code range of an affine format */
+void orc_hf_range(int f, int* qmin, int* qmax) {
+  int bits = orc_hf_bits(f);
+  if (hf_signed(f)) {
+    *qmin = -(1 << (bits - 1));
+    *qmax = (1 << (bits - 1)) - 1;
+  } else {
+    *qmin = 0;
+    *qmax = (1 << bits) - 1;
+  }
+}
+long long orc_hf_row_bytes(int f, int D) { return ((long long)D * orc_hf_bits(f) + 7) / 8; }
+
+static uint16_t float_to_bf16_rne(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x40); /* quiet NaN */
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+/* Encode one row of D bf16 values into `row` (row_bytes(format) bytes). */
+static void hf_encode_row(const uint16_t* x, int D, const orc_plane_fmt* pf, uint8_t* row) {
+  const int f = pf->format;
+  memset(row, 0, (size_t)orc_hf_row_bytes(f, D));
+  for (int d = 0; d < D; ++d) {
+    float v = bf16_to_float(x[d]);
+    if (f == ORC_HF_F32) {
+      memcpy(row + 4 * (size_t)d, &v, 4);
+    } else if (f == ORC_HF_F16) {
+      uint16_t h = float_to_fp16_bits(v);
+      memcpy(row + 2 * (size_t)d, &h, 2);
+    } else if (f == ORC_HF_BF16) {
+      uint16_t h = float_to_bf16_rne(v);
+      memcpy(row + 2 * (size_t)d, &h, 2);
+    } else {
+      int qmin, qmax;
+      orc_hf_range(f, &qmin, &qmax);
+      float r = rintf(v / pf->scale) + (float)pf->zero_point;
+      if (r < (float)qmin) r = (float)qmin;
+      if (r > (float)qmax) r = (float)qmax;
+      int code = (int)r;
+      int bits = orc_hf_bits(f);
+      unsigned u = (unsigned)code & ((1u << bits) - 1u); /* two's complement in `bits` */
+      if (bits == 8)
+        row[d] = (uint8_t)u;
+      else
+        row[(size_t)d * bits / 8] |= (uint8_t)(u << ((d * bits) % 8));
+    }
+  }
+}
+
+/* Decode one row into fp64 (each element is the fp32 reconstruction). */
+static void hf_decode_row(const uint8_t* row, int D, const orc_plane_fmt* pf, double* out) {
+  const int f = pf->format;
+  for (int d = 0; d < D; ++d) {
+    if (f == ORC_HF_F32) {
+      float v;
+      memcpy(&v, row + 4 * (size_t)d, 4);
+      out[d] = v;
+    } else if (f == ORC_HF_F16) {
+      uint16_t h;
+      memcpy(&h, row + 2 * (size_t)d, 2);
+      out[d] = fp16_bits_to_double(h);
+    } else if (f == ORC_HF_BF16) {
+      uint16_t h;
+      memcpy(&h, row + 2 * (size_t)d, 2);
+      out[d] = bf16_to_double(h);
+    } else {
+      int bits = orc_hf_bits(f);
+      unsigned u = bits == 8 ? row[d] : (row[(size_t)d * bits / 8] >> ((d * bits) % 8)) & ((1u << bits) - 1u);
+      int code = (int)u;
+      if (hf_signed(f) && code >= (1 << (bits - 1))) code -= (1 << bits);
+      float v = (float)(code - pf->zero_point) * pf->scale;
+      out[d] = v;
+    }
+  }
+}
+
+static int hf_check_fmt(const orc_plane_fmt* pf) {
+  if (pf->format < ORC_HF_F32 || pf->format > ORC_HF_U2) return ORC_ERR_SHAPE;
+  if (hf_affine(pf->format)) {
+    int qmin, qmax;
+    orc_hf_range(pf->format, &qmin, &qmax);
+    if (!(pf->scale > 0.0f) || !isfinite(pf->scale)) return ORC_ERR_SHAPE;
+    if (pf->zero_point < qmin || pf->zero_point > qmax) return ORC_ERR_SHAPE;
+  }
+  return ORC_OK;
+}
+
+int orc_hf_encode_row(const uint16_t* x, int D, const orc_plane_fmt* pf, uint8_t* row) {
+  int rc = hf_check_fmt(pf);
+  if (rc != ORC_OK) return rc;
+  hf_encode_row(x, D, pf, row);
+  return ORC_OK;
+}
+int orc_hf_decode_row(const uint8_t* row, int D, const orc_plane_fmt* pf, double* out) {
+  int rc = hf_check_fmt(pf);
+  if (rc != ORC_OK) return rc;
+  hf_decode_row(row, D, pf, out);
+  return ORC_OK;
+}
+
+static uint8_t* hf_row_ptr(uint8_t* pool, int Hkv, int S, int D, int page, int plane, int h, int s, int f) {
+  size_t plane_bytes = (size_t)Hkv * S * D * 4;
+  return pool + (size_t)page * 2 * plane_bytes + (size_t)plane * plane_bytes +
+         ((size_t)h * S + s) * (size_t)orc_hf_row_bytes(f, D);
+}
+
+/*
+ * Append new_len tokens per row at positions[b] (values [2, B, Hkv, new_len, D]
+ * bf16). A token that lands in slot 0 of its page starts the page: the page
+ * takes the formats `new_fmt` (K, V). Any other token is encoded in its page's
+ * existing formats. Rejects bad positions, pages or formats before writing.
+ */
+int orc_hpaged_append(uint8_t* pool, orc_page_desc* desc, int P, int Hkv, int S, int D,
+                      const int32_t* block_table, int M, int B, const uint16_t* values, int new_len,
+                      const int32_t* positions, const orc_page_desc* new_fmt) {
+  if (B < 0 || Hkv <= 0 || D <= 0 || S <= 0 || M < 0 || new_len < 0 || D % 4) return ORC_ERR_SHAPE;
+  if (hf_check_fmt(&new_fmt->k) || hf_check_fmt(&new_fmt->v)) return ORC_ERR_SHAPE;
+  for (int b = 0; b < B; ++b) {
+    if (positions[b] < 0 || (long long)positions[b] + new_len > (long long)M * S) return ORC_ERR_CAPACITY;
+    for (int j = 0; j < new_len; ++j) {
+      int t = positions[b] + j;
+      int page = block_table[(size_t)b * M + t / S];
+      if (page < 0 || page >= P) return ORC_ERR_PAGE;
+    }
+  }
+  for (int b = 0; b < B; ++b)
+    for (int j = 0; j < new_len; ++j) {
+      int t = positions[b] + j;
+      int page = block_table[(size_t)b * M + t / S];
+      int s = t % S;
+      if (s == 0) desc[page] = *new_fmt;
+      for (int plane = 0; plane < 2; ++plane) {
+        const orc_plane_fmt* pf = plane == 0 ? &desc[page].k : &desc[page].v;
+        for (int h = 0; h < Hkv; ++h) {
+          const uint16_t* x = values + ((((size_t)plane * B + b) * Hkv + h) * new_len + j) * D;
+          hf_encode_row(x, D, pf, hf_row_ptr(pool, Hkv, S, D, page, plane, h, s, pf->format));
+        }
+      }
+    }
+  return ORC_OK;
+}
+
+/*
+ * Decode attention over the heterogeneous pages: the visible tokens of row b
+ * decoded by their pages' formats; with cur_kv ([2, B, Hkv, 1, D] bf16) the
+ * token at lens[b] - 1 takes part uncompressed from cur_kv (the current K/V
+ * are attended before they are encoded). q [B, Hq, D] bf16; out fp64.
+ */
+int orc_hpaged_attention(const uint16_t* q, int Hq, const uint8_t* pool, const orc_page_desc* desc, int P,
+                         int Hkv, int S, int D, const int32_t* block_table, int M, int B, const int32_t* lens,
+                         const uint16_t* cur_kv, double scale, int window, double* out) {
+  if (B < 0 || Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0 || D <= 0 || S <= 0 || M < 0 || D % 4) return ORC_ERR_SHAPE;
+  long long cap = (long long)M * S;
+  for (int b = 0; b < B; ++b) {
+    if (lens[b] < 0 || lens[b] > cap) return ORC_ERR_CAPACITY;
+    for (int t = 0; t < lens[b]; ++t) {
+      int page = block_table[(size_t)b * M + t / S];
+      if (page < 0 || page >= P) return ORC_ERR_PAGE;
+      if (hf_check_fmt(&desc[page].k) || hf_check_fmt(&desc[page].v)) return ORC_ERR_SHAPE;
+    }
+  }
+  int G = Hq / Hkv;
+  double* K = (double*)malloc(((size_t)cap + 1) * D * sizeof(double));
+  double* V = (double*)malloc(((size_t)cap + 1) * D * sizeof(double));
+  if (!K || !V) {
+    free(K);
+    free(V);
+    return ORC_ERR_ALLOC;
+  }
+  int rc = ORC_OK;
+  for (int b = 0; b < B && rc == ORC_OK; ++b) {
+    int lo, hi;
+    int n = orc_visible_range(lens[b], window, &lo, &hi);
+    for (int g = 0; g < Hkv && rc == ORC_OK; ++g) {
+      for (int t = 0; t < n; ++t) {
+        int logical = lo + t;
+        if (cur_kv && logical == lens[b] - 1) {
+          for (int d = 0; d < D; ++d) {
+            K[(size_t)t * D + d] = bf16_to_double(cur_kv[(((size_t)0 * B + b) * Hkv + g) * D + d]);
+            V[(size_t)t * D + d] = bf16_to_double(cur_kv[(((size_t)1 * B + b) * Hkv + g) * D + d]);
+          }
+          continue;
+        }
+        int page = block_table[(size_t)b * M + logical / S];
+        int s = logical % S;
+        hf_decode_row(hf_row_ptr((uint8_t*)pool, Hkv, S, D, page, 0, g, s, desc[page].k.format), D,
+                      &desc[page].k, K + (size_t)t * D);
+        hf_decode_row(hf_row_ptr((uint8_t*)pool, Hkv, S, D, page, 1, g, s, desc[page].v.format), D,
+                      &desc[page].v, V + (size_t)t * D);
+      }
+      rc = attend_group(q, ORC_BF16, Hq, G, b, g, D, K, V, n, scale, out);
+    }
+  }
+  free(K);
+  free(V);
+  return rc;
+}
+
+/*
+ * QuantizePagedCache on the selected pages (unique indices): each page's valid
+ * prefix of valid[i] slots is decoded in its current formats and encoded in
+ * `to` (K, V independently); the other slots become the destination format's
+ * zeros (encode of 0). Every index, length and format is checked before any
+ * page changes.
+ */
+int orc_hpaged_quantize(uint8_t* pool, orc_page_desc* desc, int P, int Hkv, int S, int D, const int32_t* pages,
+                        const int32_t* valid, int n, const orc_page_desc* to) {
+  if (Hkv <= 0 || D <= 0 || S <= 0 || n < 0 || D % 4) return ORC_ERR_SHAPE;
+  if (hf_check_fmt(&to->k) || hf_check_fmt(&to->v)) return ORC_ERR_SHAPE;
+  for (int i = 0; i < n; ++i) {
+    if (pages[i] < 0 || pages[i] >= P) return ORC_ERR_PAGE;
+    if (valid[i] < 0 || valid[i] > S) return ORC_ERR_CAPACITY;
+    for (int j = 0; j < i; ++j)
+      if (pages[j] == pages[i]) return ORC_ERR_SHAPE;
+  }
+  double* vals = (double*)malloc((size_t)Hkv * S * D * sizeof(double));
+  float* x = (float*)malloc((size_t)D * sizeof(float));
+  if (!vals || !x) {
+    free(vals);
+    free(x);
+    return ORC_ERR_ALLOC;
+  }
+  for (int i = 0; i < n; ++i) {
+    int page = pages[i];
+    for (int plane = 0; plane < 2; ++plane) {
+      orc_plane_fmt* from = plane == 0 ? &desc[page].k : &desc[page].v;
+      const orc_plane_fmt* dst = plane == 0 ? &to->k : &to->v;
+      /* the whole plane is decoded before any of it is rewritten: source and
+         destination rows share the page's bytes */
+      for (int h = 0; h < Hkv; ++h)
+        for (int s = 0; s < valid[i]; ++s)
+          hf_decode_row(hf_row_ptr(pool, Hkv, S, D, page, plane, h, s, from->format), D, from,
+                        vals + ((size_t)h * S + s) * D);
+      for (int h = 0; h < Hkv; ++h)
+        for (int s = 0; s < S; ++s) {
+          uint8_t* row = hf_row_ptr(pool, Hkv, S, D, page, plane, h, s, dst->format);
+          for (int d = 0; d < D; ++d) x[d] = s < valid[i] ? (float)vals[((size_t)h * S + s) * D + d] : 0.0f;
+          /* encode from the fp32 reconstruction (a float, not rounded to bf16 first) */
+          if (dst->format == ORC_HF_F32) {
+            memcpy(row, x, (size_t)D * 4);
+          } else if (dst->format == ORC_HF_F16 || dst->format == ORC_HF_BF16) {
+            for (int d = 0; d < D; ++d) {
+              uint16_t hb = dst->format == ORC_HF_F16 ? float_to_fp16_bits(x[d]) : float_to_bf16_rne(x[d]);
+              memcpy(row + 2 * (size_t)d, &hb, 2);
+            }
+          } else {
+            int qmin, qmax, bits = orc_hf_bits(dst->format);
+            orc_hf_range(dst->format, &qmin, &qmax);
+            memset(row, 0, (size_t)orc_hf_row_bytes(dst->format, D));
+            for (int d = 0; d < D; ++d) {
+              float r = rintf(x[d] / dst->scale) + (float)dst->zero_point;
+              if (r < (float)qmin) r = (float)qmin;
+              if (r > (float)qmax) r = (float)qmax;
+              unsigned u = (unsigned)(int)r & ((1u << bits) - 1u);
+              if (bits == 8)
+                row[d] = (uint8_t)u;
+              else
+                row[(size_t)d * bits / 8] |= (uint8_t)(u << ((d * bits) % 8));
+            }
+          }
+        }
+      *from = *dst;
+    }
+  }
+  free(vals);
+  free(x);
+  return ORC_OK;
+}

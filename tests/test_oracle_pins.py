@@ -555,3 +555,161 @@ def test_paged_chunk_equals_contiguous_chunk():
     lens = np.array([7, 20], np.int32)
     np.testing.assert_array_equal(O.paged_chunk_attention(q, pool, table, lens, T, window=5),
                                   O.chunk_attention(q, cache, lens, T, window=5))
+
+
+# --------------------------------------------------- heterogeneous pages
+
+def test_hf_two_bit_codes_by_hand():
+    # INT2, scale 1, zero point 0: saturate(round_half_even(x)) to [-2, 1],
+    # two's complement in two bits, four codes per byte, least-significant first
+    x = bf16_from_f32(np.array([-3, -2, -1, 0, 1, 2, 0.5, 1.5], np.float32))
+    row = O.hf_encode_row(x, (O.HF_I2, 1.0, 0))
+    # codes -2 -2 -1 0 -> 0b00_11_10_10 ; codes 1 1 0 1 (0.5 -> 0, 1.5 -> 2 -> 1) -> 0b01_00_01_01
+    assert row.tolist() == [0x3A, 0x45]
+    np.testing.assert_array_equal(O.hf_decode_row(row, 8, (O.HF_I2, 1.0, 0)), [-2, -2, -1, 0, 1, 1, 0, 1])
+
+
+def test_hf_four_bit_unsigned_packing_by_hand():
+    # UINT4, scale 0.25, zero point 8 (the selector example of the pages): x / 0.25 + 8
+    x = bf16_from_f32(np.array([0.0, 0.25, -2.0, 1.75, 5.0, -5.0, 0.125, 0.375], np.float32))
+    row = O.hf_encode_row(x, (O.HF_U4, 0.25, 8))
+    # codes 8, 9, 0, 15, 15 (sat), 0 (sat), 8 (0.5 -> 0), 10 (1.5 -> 2); low nibble first
+    assert row.tolist() == [0x98, 0xF0, 0x0F, 0xA8]
+
+
+@pytest.mark.parametrize("fmt", ["I8", "U8", "I4", "U4", "I2", "U2"])
+def test_hf_ties_to_even_and_saturation(fmt):
+    f = getattr(O, "HF_" + fmt)
+    qmin, qmax = O.HF_RANGE[f]
+    zp = (qmin + qmax + 1) // 2 if qmin == 0 else 0
+    scale = 0.5
+    # x / scale = k + 0.5 rounds to the even neighbour; beyond the range saturates
+    ks = np.arange(qmin - zp - 3, qmax - zp + 3)
+    x = (ks + 0.5) * scale
+    codes = O.hf_decode_row(O.hf_encode_row(bf16_from_f32(x.astype(np.float32)), (f, scale, zp)), len(x),
+                            (f, scale, zp)) / scale + zp
+    for k, c in zip(ks, codes):
+        want = min(max(int(k) + (int(k) % 2), qmin - zp), qmax - zp) + zp   # even of k, k + 1
+        assert c == want, (fmt, k, c, want)
+
+
+@pytest.mark.parametrize("fmt", ["I8", "U8", "I4", "U4", "I2", "U2"])
+def test_hf_reconstruction_within_half_scale(fmt):
+    # "each affine reconstruction differs from its source by at most half its scale"
+    f = getattr(O, "HF_" + fmt)
+    qmin, qmax = O.HF_RANGE[f]
+    zp, scale = (qmin + qmax + 1) // 2, 0.125
+    rng = np.random.default_rng(81)
+    x = rng.uniform((qmin - zp) * scale, (qmax - zp) * scale, 64).astype(np.float32)
+    xb = bf16_from_f32(x)
+    y = O.hf_decode_row(O.hf_encode_row(xb, (f, scale, zp)), 64, (f, scale, zp))
+    assert np.abs(y - bf16_to_f32(xb)).max() <= scale / 2 + 1e-9
+
+
+def test_hf_dense_formats():
+    rng = np.random.default_rng(82)
+    x = bf16_from_f32(rng.standard_normal(32).astype(np.float32))
+    xf = bf16_to_f32(x).astype(np.float64)
+    for f in (O.HF_F32, O.HF_BF16):                  # bf16 values are exact in both
+        np.testing.assert_array_equal(O.hf_decode_row(O.hf_encode_row(x, (f, 0, 0)), 32, (f, 0, 0)), xf)
+    h = O.hf_decode_row(O.hf_encode_row(x, (O.HF_F16, 0, 0)), 32, (O.HF_F16, 0, 0))
+    np.testing.assert_array_equal(h, xf.astype(np.float16).astype(np.float64))   # nearest fp16
+
+
+def _hetero_case(B=2, H=2, S=4, M=4, D=8, seed=83):
+    rng = np.random.default_rng(seed)
+    P = B * M
+    table = rng.permutation(P).astype(np.int32).reshape(B, M)
+    pool, desc = O.hpaged_pool(P, H, S, D)
+    return rng, P, table, pool, desc
+
+
+def test_hpaged_all_bf16_equals_paged_oracle():
+    rng, P, table, pool, desc = _hetero_case()
+    B, H, S, M, D = 2, 2, 4, 4, 8
+    lens = np.array([16, 7], np.int32)
+    hist = bf16_from_f32(rng.standard_normal((2, B, H, 16, D)).astype(np.float32))
+    O.hpaged_append(pool, desc, table, hist, [0, 0], O.page_desc())
+    dense = np.zeros((2, P, H, S, D), np.uint16)
+    O.paged_update(dense, table, hist, [0, 0])
+    q = bf16_from_f32(rng.standard_normal((B, 4, D)).astype(np.float32))
+    for window in (-1, 2):
+        np.testing.assert_array_equal(O.hpaged_attention(q, pool, desc, table, lens, H, window=window),
+                                      O.paged_attention(q, dense, table, lens, window=window))
+
+
+def test_hpaged_pages_keep_their_formats():
+    # a token that starts a page stamps the call's formats on it; later tokens of
+    # that page use the page's formats; earlier pages keep theirs
+    rng, P, table, pool, desc = _hetero_case()
+    D, H = 8, 2
+    vals = bf16_from_f32(rng.standard_normal((2, 2, H, 6, D)).astype(np.float32))
+    O.hpaged_append(pool, desc, table, vals, [0, 0], O.page_desc(k=(O.HF_I8, 0.01, 0), v=(O.HF_U4, 0.25, 8)))
+    more = bf16_from_f32(rng.standard_normal((2, 2, H, 3, D)).astype(np.float32))
+    O.hpaged_append(pool, desc, table, more, [6, 6], O.page_desc(k=(O.HF_F32, 1, 0), v=(O.HF_I2, 0.5, 0)))
+    for b in range(2):
+        assert desc["kf"][table[b, 0]] == O.HF_I8 and desc["vf"][table[b, 1]] == O.HF_U4   # slots 0..3, 4..7
+        assert desc["kf"][table[b, 2]] == O.HF_F32 and desc["vf"][table[b, 2]] == O.HF_I2  # started at 8
+
+
+@pytest.mark.parametrize("fmt,scale,zps,tol", [("I8", 0.01, 0, 0.01), ("U8", 0.01, 128, 0.01),
+                                               ("I4", 0.25, 0, 0.15), ("U4", 0.25, 8, 0.15)])
+def test_hpaged_four_step_fixture_tolerance(fmt, scale, zps, tol):
+    # the pages' tolerance table: Q/K/V components +/-(0.173 * step), four steps,
+    # K and V stored in `fmt` with scalar (scale, zero point); the current token
+    # attended uncompressed; within `tol` of unquantized dense attention
+    B, H, Hq, S, M, D = 1, 1, 2, 4, 2, 64
+    f = (getattr(O, "HF_" + fmt), scale, zps)
+    table = np.arange(M, dtype=np.int32).reshape(1, M)
+    pool, desc = O.hpaged_pool(M, H, S, D)
+    dense = np.full((2, B, H, S * M, D), np.nan, np.float32)
+    worst = 0.0
+    for step in range(1, 5):
+        kv = bf16_from_f32(np.stack([fixture_signed_ramp(B, H, 1, D, step), fixture_signed_ramp(B, H, 1, D, step)]))
+        q = bf16_from_f32(fixture_signed_ramp(B, Hq, 1, D, step)[:, :, 0])
+        yq = O.hpaged_attention(q, pool, desc, table, [step], H, cur_kv=kv)
+        O.hpaged_append(pool, desc, table, kv, [step - 1], O.page_desc(k=f, v=f))
+        O.cache_update(dense, bf16_to_f32(kv), [step - 1])
+        yd = O.decode_attention(bf16_to_f32(q), dense, [step])
+        worst = max(worst, float(np.abs(yq - yd).max()),
+                    float(np.abs(O.hpaged_attention(q, pool, desc, table, [step], H) - yd).max()))
+    assert worst <= tol
+    assert worst > 0.0
+
+
+def test_hpaged_quantize_selected_pages_only():
+    rng, P, table, pool, desc = _hetero_case()
+    B, H, S, M, D = 2, 2, 4, 4, 8
+    hist = bf16_from_f32(rng.standard_normal((2, B, H, 14, D)).astype(np.float32))
+    O.hpaged_append(pool, desc, table, hist, [0, 0], O.page_desc(k=(O.HF_F32, 1, 0), v=(O.HF_BF16, 1, 0)))
+    before, dbefore = pool.copy(), desc.copy()
+    sel = np.array([table[0, 1], table[1, 3]], np.int32)          # a full page and a half-full one
+    valid = np.array([4, 2], np.int32)                            # row 1 holds 14 tokens: page 3 has 2
+    to = O.page_desc(k=(O.HF_I4, 0.125, 0), v=(O.HF_U2, 0.5, 2))
+    O.hpaged_quantize(pool, desc, H, D, sel, valid, to)
+    for p in range(P):
+        if p not in sel:
+            np.testing.assert_array_equal(pool[p], before[p])
+            assert desc[p] == dbefore[p]
+    assert desc["kf"][sel[0]] == O.HF_I4 and desc["vf"][sel[1]] == O.HF_U2
+    # valid rows reconstruct within half a scale of the source; unused rows are the
+    # destination's zeros (code = zero point)
+    for p, n in zip(sel, valid):
+        for h in range(H):
+            for s in range(S):
+                for plane, (f, sc, zp) in ((0, (O.HF_I4, 0.125, 0)), (1, (O.HF_U2, 0.5, 2))):
+                    rb = D * O.HF_BITS[f] // 8
+                    off = plane * H * S * D * 4 + (h * S + s) * rb
+                    got = O.hf_decode_row(pool[p, off:off + rb], D, (f, sc, zp))
+                    if s >= n:
+                        np.testing.assert_array_equal(got, np.zeros(D))
+                    else:
+                        f0 = (O.HF_F32, 1, 0) if plane == 0 else (O.HF_BF16, 1, 0)
+                        rb0 = D * O.HF_BITS[f0[0]] // 8
+                        off0 = plane * H * S * D * 4 + (h * S + s) * rb0
+                        src = O.hf_decode_row(before[p, off0:off0 + rb0], D, f0)
+                        lo, hi = (O.HF_RANGE[f][0] - zp) * sc, (O.HF_RANGE[f][1] - zp) * sc
+                        expect = np.clip(src, lo, hi)
+                        assert np.abs(got - expect).max() <= sc / 2 + 1e-9
+    with pytest.raises(O.OracleError):                             # duplicate index
+        O.hpaged_quantize(pool, desc, H, D, np.array([1, 1], np.int32), np.array([4, 4], np.int32), to)
