@@ -93,7 +93,12 @@ typedef enum ol_access { OL_READ_ONLY = 0, OL_READ_WRITE = 1 } ol_access;
  */
 enum { OL_HISTORY_STABLE = 0x100 };
 
-typedef enum ol_layout { OL_LAYOUT_CONTIGUOUS = 0, OL_LAYOUT_PAGED = 1, OL_LAYOUT_INT4 = 2 } ol_layout;
+typedef enum ol_layout {
+  OL_LAYOUT_CONTIGUOUS = 0,
+  OL_LAYOUT_PAGED = 1,
+  OL_LAYOUT_INT4 = 2,
+  OL_LAYOUT_HPAGED = 3 /* ol_hpaged_kv: paged, every page with its own K and V formats */
+} ol_layout;
 
 /* How an INT4 append chooses (scale, zero point) per block of 32 values. */
 typedef enum ol_quant_mode {
@@ -161,6 +166,62 @@ typedef struct ol_int4_kv {
   int32_t access;
   uint64_t owner;
 } ol_int4_kv;
+
+/*
+ * Heterogeneous paged cache: every page stores its K and its V in its own
+ * format (page "Persistent input/output feedback", sections Optional
+ * heterogeneous paged KV and Selected-block quantization). Formats: dense
+ * FLOAT, FLOAT16, BFLOAT16; affine INT8, UINT8, INT4, UINT4, INT2, UINT2 with
+ * value = (code - zero_point) * scale, one scalar (scale, zero point) per page
+ * and plane. Encoding is QuantizeLinear in IEEE fp32:
+ * code = saturate(round_half_even(x / scale) + zero_point); dense formats
+ * round to nearest even. Codes of four and two bits pack two and four per
+ * byte, least-significant bits first (page "Custom, quantized, and persistent
+ * values", affine branch).
+ */
+typedef enum ol_page_format_id {
+  OL_FMT_F32 = 0, OL_FMT_F16 = 1, OL_FMT_BF16 = 2,
+  OL_FMT_I8 = 3, OL_FMT_U8 = 4, OL_FMT_I4 = 5, OL_FMT_U4 = 6, OL_FMT_I2 = 7, OL_FMT_U2 = 8
+} ol_page_format_id;
+
+/* One plane's format; scale and zero_point are ignored by dense formats. Affine
+   formats need a positive finite scale and a zero point inside the code range. */
+typedef struct ol_plane_format {
+  int32_t format;
+  float scale;
+  int32_t zero_point;
+} ol_plane_format;
+
+typedef struct ol_page_format {
+  ol_plane_format k, v;
+} ol_page_format;
+
+/*
+ * The heterogeneous pool: num_pages slots of 2 * kv_heads * page_size *
+ * head_dim * 4 bytes (room for the widest format). Plane k (0 = K, 1 = V) of
+ * page p starts at byte p * slot + k * slot / 2; in a plane of format f the
+ * codes of (head h, page slot s) start at (h * page_size + s) * row_bytes(f)
+ * and hold head_dim elements (row_bytes = head_dim * bits / 8). head_dim must
+ * be a multiple of 4. Logical token t of row b lives in slot t % page_size of
+ * page block_table[b][t / page_size].
+ *   formats       device [num_pages]: each page's formats, read by the kernels
+ *   formats_host  host [num_pages]: the same table, read by the host to
+ *                 validate and plan. Calls that start or convert a page update
+ *                 both: the host entry when the call is made, the device entry
+ *                 in stream order.
+ * `pool` is the alias pointer.
+ */
+typedef struct ol_hpaged_kv {
+  void* pool;
+  ol_page_format* formats;
+  ol_page_format* formats_host;
+  const int32_t* block_table;
+  const int32_t* block_table_host;
+  int32_t num_pages, kv_heads, page_size, head_dim;
+  int32_t batch, max_pages;
+  int32_t access;
+  uint64_t owner;
+} ol_hpaged_kv;
 
 /* Human-readable name of a status code (static string). */
 OL_API const char* ol_status_string(ol_status s);
@@ -287,6 +348,58 @@ OL_API ol_status ol_decode_step(int32_t layout, const void* cache_desc, void* up
                          int32_t q_heads, const void* new_kv, const int32_t* lens_host,
                          const int32_t* lens_dev, float scale, int32_t window, void* out,
                          int32_t out_dtype, void* workspace, size_t ws_bytes, ol_stream stream);
+
+/*
+ * Append new_len tokens per row to a heterogeneous paged cache: values
+ * [2, batch, kv_heads, new_len, head_dim] bf16 at positions[b].. of every row.
+ * A token that lands in slot 0 of its page starts that page: the page takes
+ * the formats *new_pages (the caller's format selection for this call, chosen
+ * from anything it likes, e.g. the retained length); every other token is
+ * encoded in its page's existing formats, so earlier pages are never converted
+ * and a partially filled page keeps its format. `updated` must equal
+ * cache->pool. Writes only the appended slots and the started pages' formats.
+ */
+OL_API ol_status ol_hpaged_append(const ol_hpaged_kv* cache, void* updated, const void* values_bf16,
+                                  int32_t new_len, const int32_t* positions_host, const int32_t* positions_dev,
+                                  const ol_page_format* new_pages, ol_stream stream);
+
+/*
+ * Decode attention over a heterogeneous paged cache: every visible token is
+ * decoded with its page's formats. If cur_kv ([2, batch, kv_heads, 1,
+ * head_dim] bf16) is non-NULL the token at lens[b] - 1 takes part
+ * uncompressed from cur_kv (current K/V attended before they are encoded).
+ * q bf16 [batch, q_heads, head_dim]; otherwise as ol_decode_attention.
+ */
+OL_API ol_status ol_hpaged_decode_attention(const ol_hpaged_kv* cache, const void* q, int32_t q_heads,
+                                            const int32_t* lens_host, const int32_t* lens_dev, const void* cur_kv,
+                                            float scale, int32_t window, void* out, int32_t out_dtype,
+                                            void* workspace, size_t ws_bytes, ol_stream stream);
+
+/*
+ * The fused step on a heterogeneous paged cache: append new_kv
+ * [2, batch, kv_heads, 1, head_dim] bf16 at lens[b] - 1 (as ol_hpaged_append,
+ * pages started by it taking *new_pages) and attend with the new token
+ * uncompressed, in one launch.
+ */
+OL_API ol_status ol_hpaged_decode_step(const ol_hpaged_kv* cache, void* updated, const void* q, int32_t q_heads,
+                                       const void* new_kv, const ol_page_format* new_pages,
+                                       const int32_t* lens_host, const int32_t* lens_dev, float scale,
+                                       int32_t window, void* out, int32_t out_dtype, void* workspace,
+                                       size_t ws_bytes, ol_stream stream);
+
+/*
+ * QuantizePagedCache on selected pages (page "Persistent input/output
+ * feedback", section Selected-block quantization): for each of the n pages
+ * (unique indices), the first valid[i] slots of every head are decoded in the
+ * page's current formats and encoded in *to (K and V independently; dense
+ * targets dequantize), the other slots become the target format's zeros, and
+ * the page's formats become *to. Unselected pages are untouched. Every index,
+ * length and format is checked before anything is written. pages and valid are
+ * given in host memory (validation) and device memory (the kernel), equal.
+ */
+OL_API ol_status ol_hpaged_quantize(const ol_hpaged_kv* cache, void* updated, const int32_t* pages_host,
+                                    const int32_t* pages_dev, const int32_t* valid_host, const int32_t* valid_dev,
+                                    int32_t n, const ol_page_format* to, ol_stream stream);
 
 /*
  * Chunked step: multi-token append with causal attention inside the chunk

@@ -24,7 +24,12 @@ OL_OK, OL_ERR_NULL, OL_ERR_ALIAS, OL_ERR_READONLY, OL_ERR_CAPACITY, OL_ERR_SHAPE
 OL_F32, OL_BF16 = 0, 1
 OL_READ_ONLY, OL_READ_WRITE = 0, 1
 OL_HISTORY_STABLE = 0x100
-OL_LAYOUT_CONTIGUOUS, OL_LAYOUT_PAGED, OL_LAYOUT_INT4 = 0, 1, 2
+OL_LAYOUT_CONTIGUOUS, OL_LAYOUT_PAGED, OL_LAYOUT_INT4, OL_LAYOUT_HPAGED = 0, 1, 2, 3
+# ol_page_format_id: per-page element formats of the heterogeneous paged cache
+OL_FMT_F32, OL_FMT_F16, OL_FMT_BF16, OL_FMT_I8, OL_FMT_U8, OL_FMT_I4, OL_FMT_U4, OL_FMT_I2, OL_FMT_U2 = range(9)
+# host mirror of ol_page_format: (format, scale, zero point) of K, then of V
+PAGE_FORMAT_DTYPE = np.dtype([("kf", "<i4"), ("ks", "<f4"), ("kz", "<i4"), ("vf", "<i4"), ("vs", "<f4"),
+                              ("vz", "<i4")])
 OL_Q_DYNAMIC, OL_Q_FIXED = 0, 1
 OL_DEVICE_OK, OL_DEVICE_GUARD = 0, 1
 
@@ -33,7 +38,8 @@ SYMBOLS = ("ol_status_string", "ol_version", "ol_workspace_size", "ol_workspace_
            "ol_paged_cache_update", "ol_decode_attention", "ol_paged_decode_attention", "ol_int4kv_append",
            "ol_int4kv_decode_attention", "ol_decode_step", "ol_decode_step_noalloc", "ol_workspace_size_host",
            "ol_decode_step_host", "ol_last_call_stats", "ol_total_stats", "ol_reset_stats",
-           "ol_workspace_size_chunk", "ol_chunk_step")
+           "ol_workspace_size_chunk", "ol_chunk_step", "ol_hpaged_append", "ol_hpaged_decode_attention",
+           "ol_hpaged_decode_step", "ol_hpaged_quantize")
 
 
 class Stats(ctypes.Structure):
@@ -74,6 +80,25 @@ class Int4KV(ctypes.Structure):
                 ("batch", ctypes.c_int32), ("kv_heads", ctypes.c_int32), ("capacity", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("quant_mode", ctypes.c_int32), ("fixed_scale", ctypes.c_float),
                 ("fixed_zp", ctypes.c_int32), ("access", ctypes.c_int32), ("owner", ctypes.c_uint64)]
+
+
+class PlaneFormat(ctypes.Structure):
+    """ol_plane_format: element format of one plane (K or V) of a page."""
+    _fields_ = [("format", ctypes.c_int32), ("scale", ctypes.c_float), ("zero_point", ctypes.c_int32)]
+
+
+class PageFormat(ctypes.Structure):
+    """ol_page_format: the K and V formats of a page."""
+    _fields_ = [("k", PlaneFormat), ("v", PlaneFormat)]
+
+
+class HPagedKV(ctypes.Structure):
+    """ol_hpaged_kv: page slots of 2 * kv_heads * page_size * head_dim * 4 bytes, per-page formats, block table."""
+    _fields_ = [("pool", ctypes.c_void_p), ("formats", ctypes.c_void_p), ("formats_host", ctypes.c_void_p),
+                ("block_table", ctypes.c_void_p), ("block_table_host", ctypes.c_void_p),
+                ("num_pages", ctypes.c_int32), ("kv_heads", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("batch", ctypes.c_int32), ("max_pages", ctypes.c_int32),
+                ("access", ctypes.c_int32), ("owner", ctypes.c_uint64)]
 
 
 _lib = None
@@ -122,6 +147,13 @@ def load(build_if_missing: bool = True):
         "ol_total_stats": (st, [vp]),
         "ol_reset_stats": (None, []),
         "ol_decode_step_host": (st, [i32, vp, vp, vp, i32, vp, vp, f32, i32, vp, i32, vp, sz, vp]),
+        "ol_hpaged_append": (st, [ctypes.POINTER(HPagedKV), vp, vp, i32, vp, vp, ctypes.POINTER(PageFormat), vp]),
+        "ol_hpaged_decode_attention": (st, [ctypes.POINTER(HPagedKV), vp, i32, vp, vp, vp, f32, i32, vp, i32, vp, sz,
+                                            vp]),
+        "ol_hpaged_decode_step": (st, [ctypes.POINTER(HPagedKV), vp, vp, i32, vp, ctypes.POINTER(PageFormat), vp, vp,
+                                       f32, i32, vp, i32, vp, sz, vp]),
+        "ol_hpaged_quantize": (st, [ctypes.POINTER(HPagedKV), vp, vp, vp, vp, vp, i32, ctypes.POINTER(PageFormat),
+                                    vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -225,6 +257,33 @@ def int4_kv(codes, scales, zps, *, head_dim: Optional[int] = None, quant_mode: i
         B, H, C, D = dims
     d = Int4KV(_ptr(codes), _ptr(scales), _ptr(zps), B, H, C, D, quant_mode, fixed_scale, fixed_zp, access, owner)
     d._refs = (codes, scales, zps)  # the descriptor keeps the buffers it points to alive
+    return d
+
+
+def page_format(k=(OL_FMT_BF16, 1.0, 0), v=(OL_FMT_BF16, 1.0, 0)) -> PageFormat:
+    """A page's formats: k and v are (format, scale, zero point)."""
+    return PageFormat(PlaneFormat(*k), PlaneFormat(*v))
+
+
+def hpaged_kv(pool, formats, formats_host, block_table, block_table_host, *, kv_heads: int, page_size: int,
+              head_dim: int, access: int = OL_READ_WRITE, owner: int = 0) -> HPagedKV:
+    """Descriptor of a heterogeneous paged cache.
+
+    pool: device bytes, num_pages slots of 2 * kv_heads * page_size * head_dim * 4;
+    formats: device table of num_pages ol_page_format (24 bytes each);
+    formats_host: the host mirror, a C-contiguous numpy array of PAGE_FORMAT_DTYPE
+    that the library updates in place when a call starts or converts a page;
+    block_table / block_table_host: [batch, max_pages] int32 on device / host.
+    """
+    if not (isinstance(formats_host, np.ndarray) and formats_host.dtype == PAGE_FORMAT_DTYPE
+            and formats_host.flags.c_contiguous):
+        raise TypeError("formats_host must be a C-contiguous numpy array of PAGE_FORMAT_DTYPE")
+    bt_host = _host_i32(block_table_host)
+    B, M = bt_host.shape
+    P = formats_host.shape[0]
+    d = HPagedKV(_ptr(pool), _ptr(formats), _ptr(formats_host), _ptr(block_table), _ptr(bt_host), P, kv_heads,
+                 page_size, head_dim, B, M, access, owner)
+    d._refs = (pool, formats, formats_host, block_table, bt_host)  # keeps the buffers alive
     return d
 
 
@@ -371,3 +430,37 @@ def ol_decode_step_noalloc(layout: int, desc, updated, q, q_heads: int, new_kv, 
     _check(load().ol_decode_step_noalloc(layout, ctypes.byref(desc), _ptr(updated), _ptr(q), q_heads, _ptr(new_kv),
                                          _ptr(lh), _ptr(lens_dev), scale, window, _ptr(out), out_dtype,
                                          _stream(stream)), "ol_decode_step_noalloc")
+
+
+def ol_hpaged_append(kv: HPagedKV, updated, values, new_len: int, positions_host, positions_dev,
+                     new_pages: PageFormat, stream=None):
+    """values [2, B, Hkv, new_len, D] bf16 at positions[b]; pages the append starts take new_pages."""
+    ph = _host_i32(positions_host)
+    _check(load().ol_hpaged_append(ctypes.byref(kv), _ptr(updated), _ptr(values), new_len, _ptr(ph),
+                                   _ptr(positions_dev), ctypes.byref(new_pages), _stream(stream)), "ol_hpaged_append")
+
+
+def ol_hpaged_decode_attention(kv: HPagedKV, q, q_heads: int, lens_host, lens_dev, cur_kv, scale: float, window: int,
+                               out, out_dtype: int, workspace, ws_bytes: int, stream=None):
+    lh = _host_i32(lens_host)
+    _check(load().ol_hpaged_decode_attention(ctypes.byref(kv), _ptr(q), q_heads, _ptr(lh), _ptr(lens_dev),
+                                             _ptr(cur_kv), scale, window, _ptr(out), out_dtype, _ptr(workspace),
+                                             ws_bytes, _stream(stream)), "ol_hpaged_decode_attention")
+
+
+def ol_hpaged_decode_step(kv: HPagedKV, updated, q, q_heads: int, new_kv, new_pages: PageFormat, lens_host, lens_dev,
+                          scale: float, window: int, out, out_dtype: int, workspace, ws_bytes: int, stream=None):
+    lh = _host_i32(lens_host)
+    _check(load().ol_hpaged_decode_step(ctypes.byref(kv), _ptr(updated), _ptr(q), q_heads, _ptr(new_kv),
+                                        ctypes.byref(new_pages), _ptr(lh), _ptr(lens_dev), scale, window, _ptr(out),
+                                        out_dtype, _ptr(workspace), ws_bytes, _stream(stream)),
+           "ol_hpaged_decode_step")
+
+
+def ol_hpaged_quantize(kv: HPagedKV, updated, pages_host, pages_dev, valid_host, valid_dev, to: PageFormat,
+                       stream=None):
+    """QuantizePagedCache on the selected pages: valid prefixes converted to `to`, the rest zero."""
+    ph, vh = _host_i32(pages_host), _host_i32(valid_host)
+    _check(load().ol_hpaged_quantize(ctypes.byref(kv), _ptr(updated), _ptr(ph), _ptr(pages_dev), _ptr(vh),
+                                     _ptr(valid_dev), len(ph), ctypes.byref(to), _stream(stream)),
+           "ol_hpaged_quantize")

@@ -301,6 +301,96 @@ ol_status view_int4(const ol_int4_kv* c, CacheView& v) {
   return OL_OK;
 }
 
+bool valid_plane_format(const ol_plane_format& f) {
+  if (f.format < OL_FMT_F32 || f.format > OL_FMT_U2) return false;
+  if (!fmt_affine(f.format)) return true;
+  return f.scale > 0.f && std::isfinite(f.scale) && f.zero_point >= fmt_qmin(f.format) &&
+         f.zero_point <= fmt_qmax(f.format);
+}
+bool valid_page_format(const ol_page_format& f) { return valid_plane_format(f.k) && valid_plane_format(f.v); }
+
+// Bytes of one page slot of a heterogeneous pool: room for both planes in fp32.
+size_t hpaged_slot_bytes(const ol_hpaged_kv* c) { return 2ull * c->kv_heads * c->page_size * c->head_dim * 4; }
+
+ol_status view_hpaged(const ol_hpaged_kv* c, CacheView& v) {
+  if (!c || !c->pool || !c->formats || !c->formats_host || !c->block_table || !c->block_table_host)
+    return OL_ERR_NULL;
+  if (c->batch < 0 || c->kv_heads <= 0 || c->num_pages <= 0 || c->page_size <= 0 || c->head_dim <= 0 ||
+      c->max_pages < 0 || c->head_dim % 4 != 0)
+    return OL_ERR_SHAPE;
+  if ((long long)c->max_pages * c->page_size > (1ll << 30)) return OL_ERR_SHAPE;
+  if (!aligned16(c->pool) || !aligned16(c->block_table) || (reinterpret_cast<uintptr_t>(c->formats) & 3u))
+    return OL_ERR_ALIGN;
+  v = {};
+  v.layout = OL_LAYOUT_HPAGED;
+  v.dtype = OL_BF16;  // q, new tokens and outputs' input side are bf16
+  v.batch = c->batch;
+  v.kv_heads = c->kv_heads;
+  v.head_dim = c->head_dim;
+  v.capacity = c->max_pages * c->page_size;
+  v.access = c->access & ~OL_HISTORY_STABLE;
+  v.history_stable = (c->access & OL_HISTORY_STABLE) != 0;
+  v.owner = c->owner;
+  v.alias_ptr = c->pool;
+  v.ranges[0] = range_of(c->pool, (size_t)c->num_pages * hpaged_slot_bytes(c));
+  v.ranges[1] = range_of(c->formats, sizeof(ol_page_format) * (size_t)c->num_pages);
+  v.nranges = 2;
+  if (overlaps(v.ranges[0], v.ranges[1])) return OL_ERR_ALIAS;
+  return OL_OK;
+}
+
+// The same pool seen as a plain paged cache, for the block-table checks.
+ol_paged_kv paged_shape_of(const ol_hpaged_kv* c) {
+  ol_paged_kv k = {};
+  k.data = c->pool;
+  k.block_table = c->block_table;
+  k.block_table_host = c->block_table_host;
+  k.num_pages = c->num_pages;
+  k.kv_heads = c->kv_heads;
+  k.page_size = c->page_size;
+  k.head_dim = c->head_dim;
+  k.batch = c->batch;
+  k.max_pages = c->max_pages;
+  k.dtype = OL_BF16;
+  return k;
+}
+
+// Formats in force for token t of row b during an append that starts at pos:
+// the started pages' (slot 0 inside the append) new formats, else the page's.
+const ol_page_format& hpaged_token_format(const ol_hpaged_kv* c, int b, int t, int pos, const ol_page_format& nf) {
+  const int page = c->block_table_host[(size_t)b * c->max_pages + t / c->page_size];
+  return t - t % c->page_size >= pos ? nf : c->formats_host[page];
+}
+
+// Heterogeneous page checks (after check_pages on the block table): every page
+// that a call reads, or appends into without starting it, has valid formats.
+// read_hi[b]: tokens [lo, read_hi) of row b are read from the cache, lo from
+// the window; pos/new_len: the append (new_len 0 for none).
+ol_status check_hpaged_formats(const ol_hpaged_kv* c, const int32_t* lens, int window, const int32_t* read_hi,
+                               const int32_t* pos, int new_len) {
+  const int S = c->page_size;
+  for (int b = 0; b < c->batch; ++b) {
+    if (lens) {
+      const RowSplit rs = row_split(lens[b], window, 1);
+      for (int t = rs.lo; t < read_hi[b]; t += S - t % S)
+        if (!valid_page_format(c->formats_host[c->block_table_host[(size_t)b * c->max_pages + t / S]]))
+          return OL_ERR_SHAPE;
+    }
+    if (new_len > 0 && pos[b] % S != 0 &&
+        !valid_page_format(c->formats_host[c->block_table_host[(size_t)b * c->max_pages + pos[b] / S]]))
+      return OL_ERR_SHAPE;
+  }
+  return OL_OK;
+}
+
+// After a validated append: the host mirror takes the started pages' formats.
+void hpaged_start_pages(const ol_hpaged_kv* c, const int32_t* pos, int new_len, const ol_page_format& nf) {
+  const int S = c->page_size;
+  for (int b = 0; b < c->batch; ++b)
+    for (int t = (pos[b] + S - 1) / S * S; t < pos[b] + new_len; t += S)
+      c->formats_host[c->block_table_host[(size_t)b * c->max_pages + t / S]] = nf;
+}
+
 ol_status view_of(int layout, const void* desc, CacheView& v) {
   switch (layout) {
     case OL_LAYOUT_CONTIGUOUS:
@@ -385,6 +475,14 @@ AttnParams base_params(const CacheView& v, int layout, const void* desc) {
     p.num_pages = c->num_pages;
     p.page_size = c->page_size;
     p.max_pages = c->max_pages;
+  } else if (layout == OL_LAYOUT_HPAGED) {
+    const ol_hpaged_kv* c = static_cast<const ol_hpaged_kv*>(desc);
+    p.pool = c->pool;
+    p.block_table = c->block_table;
+    p.num_pages = c->num_pages;
+    p.page_size = c->page_size;
+    p.max_pages = c->max_pages;
+    p.page_fmt = c->formats;
   } else {
     const ol_int4_kv* c = static_cast<const ol_int4_kv*>(desc);
     p.codes = c->codes;
@@ -458,13 +556,47 @@ void record_attention(const CacheView& v, const int32_t* lens_host, int window, 
   record(s);
 }
 
+// Heterogeneous pages: payload and dequantized bytes follow each page's formats.
+// read_lo/read_hi: the tokens read from the cache per row; nf: formats of the
+// pages a fused append starts (or NULL); append_pos: the fused append's
+// position per row (or NULL).
+void record_hpaged(const ol_hpaged_kv* c, const int32_t* read_lo, const int32_t* read_hi, int64_t attended,
+                   const int32_t* append_pos, int new_len, const ol_page_format* nf, size_t ws_need) {
+  ol_stats s = {};
+  s.calls = 1;
+  const int S = c->page_size, D = c->head_dim;
+  auto plane_bytes = [&](const ol_plane_format& f, int64_t n) {
+    s.kv_payload_bytes_read += n * (int64_t)fmt_row_bytes(f.format, D);
+    if (fmt_affine(f.format)) s.dequantized_bytes += n * D * 4;
+  };
+  for (int b = 0; read_lo && b < c->batch; ++b)
+    for (int t = read_lo[b]; t < read_hi[b];) {
+      const int end = std::min(read_hi[b], (t / S + 1) * S);
+      const ol_page_format& f = c->formats_host[c->block_table_host[(size_t)b * c->max_pages + t / S]];
+      plane_bytes(f.k, (int64_t)(end - t) * c->kv_heads);
+      plane_bytes(f.v, (int64_t)(end - t) * c->kv_heads);
+      t = end;
+    }
+  for (int b = 0; append_pos && b < c->batch; ++b)
+    for (int t = append_pos[b]; t < append_pos[b] + new_len; ++t) {
+      const ol_page_format& f = hpaged_token_format(c, b, t, append_pos[b], *nf);
+      s.storage_append_copied_bytes +=
+          (int64_t)c->kv_heads * (int64_t)(fmt_row_bytes(f.k.format, D) + fmt_row_bytes(f.v.format, D));
+    }
+  if (append_pos && new_len > 0 && c->batch > 0) s.storage_reuse_count = 2;
+  s.attended_tokens = attended * c->kv_heads;
+  s.workspace_bytes = (int64_t)ws_need;
+  record(s);
+}
+
 // nq > 1: a chunked step's attention (query tokens z = 0..nq-1 per row, token z
 // at position lens - nq + z; q and y are [B, Hq, nq, D]). check_only: stop
 // after validation (nothing recorded, nothing launched).
 ol_status run_attention(int layout, const void* desc, const CacheView& v, const void* q, int q_heads,
                         const int32_t* lens_host, const int32_t* lens_dev, const void* new_kv, int append,
                         int cur_from_new, float scale, int window, void* out, int out_dtype, void* workspace,
-                        size_t ws_bytes, cudaStream_t stream, int nq = 1, bool check_only = false) {
+                        size_t ws_bytes, cudaStream_t stream, int nq = 1, bool check_only = false,
+                        const ol_page_format* new_fmt = nullptr) {
   if (!q || !lens_host || !lens_dev || !out || !workspace) return OL_ERR_NULL;
   if (q_heads <= 0 || q_heads % v.kv_heads != 0) return OL_ERR_SHAPE;
   if (v.head_dim > 256) return OL_ERR_UNSUPPORTED;
@@ -504,9 +636,42 @@ ol_status run_attention(int layout, const void* desc, const CacheView& v, const 
       return st;
     }
   }
-  if ((st = check_owner(v.ranges, v.nranges, v.owner)) != OL_OK) return st;
-  if (check_only) return OL_OK;
-  record_attention(v, lens_host, window, append, cur_from_new, need, nq);
+  std::vector<int32_t> read_lo, read_hi, append_pos;
+  if (layout == OL_LAYOUT_HPAGED) {
+    const ol_hpaged_kv* c = static_cast<const ol_hpaged_kv*>(desc);
+    if (nq != 1) return OL_ERR_UNSUPPORTED;
+    if ((st = no_overlap(v, c->block_table, sizeof(int32_t) * (size_t)c->batch * c->max_pages)) != OL_OK) return st;
+    const ol_paged_kv k = paged_shape_of(c);
+    if (append) {
+      if (!new_fmt) return OL_ERR_NULL;
+      if (!valid_page_format(*new_fmt)) return OL_ERR_SHAPE;
+      append_pos.resize(v.batch);
+      for (int b = 0; b < v.batch; ++b) append_pos[b] = lens_host[b] - 1;
+      if ((st = check_pages(&k, append_pos.data(), 1, true, window)) != OL_OK) return st;
+    } else if ((st = check_pages(&k, lens_host, 0, false, window < 0 ? -1 : window)) != OL_OK) {
+      return st;
+    }
+    read_lo.resize(v.batch);
+    read_hi.resize(v.batch);
+    int64_t attended = 0;
+    for (int b = 0; b < v.batch; ++b) {
+      const RowSplit rs = row_split(lens_host[b], window < 0 ? -1 : window, 1);
+      read_lo[b] = rs.lo;
+      read_hi[b] = rs.hi - ((cur_from_new && rs.hi > rs.lo) ? 1 : 0);
+      attended += rs.hi - rs.lo;
+    }
+    if ((st = check_hpaged_formats(c, lens_host, window < 0 ? -1 : window, read_hi.data(),
+                                   append ? append_pos.data() : nullptr, append ? 1 : 0)) != OL_OK)
+      return st;
+    if ((st = check_owner(v.ranges, v.nranges, v.owner)) != OL_OK) return st;
+    if (check_only) return OL_OK;
+    record_hpaged(c, read_lo.data(), read_hi.data(), attended, append ? append_pos.data() : nullptr, 1, new_fmt,
+                  need);
+  } else {
+    if ((st = check_owner(v.ranges, v.nranges, v.owner)) != OL_OK) return st;
+    if (check_only) return OL_OK;
+    record_attention(v, lens_host, window, append, cur_from_new, need, nq);
+  }
   if (fault_injected()) return OL_ERR_INJECTED;
 
   AttnParams p = base_params(v, layout, desc);
@@ -522,6 +687,7 @@ ol_status run_attention(int layout, const void* desc, const CacheView& v, const 
   p.window_q = window < 0 ? -1 : window;
   p.window = window < 0 ? -1 : window + nq - 1;  // the union of the query tokens' ranges
   p.nq = nq;
+  if (new_fmt) p.new_fmt = *new_fmt;
   p.out = out;
   p.out_dtype = out_dtype;
   p.inline_lens = v.batch <= kInlineRows ? 1 : 0;
@@ -927,6 +1093,140 @@ ol_status ol_decode_step_host(int32_t layout, const void* cache_desc, void* upda
   if (st != OL_OK) return st;
   return cudaMemcpyAsync(out_host, ws + h.out, out_bytes, cudaMemcpyDeviceToHost, s) == cudaSuccess ? OL_OK
                                                                                                  : OL_ERR_CUDA;
+}
+
+// ------------------------------------------------ heterogeneous paged cache
+
+ol_status ol_hpaged_append(const ol_hpaged_kv* cache, void* updated, const void* values_bf16, int32_t new_len,
+                           const int32_t* positions_host, const int32_t* positions_dev,
+                           const ol_page_format* new_pages, ol_stream stream) {
+  CacheView v;
+  ol_status st = view_hpaged(cache, v);
+  if (st != OL_OK) return st;
+  if ((st = append_common(v, updated, values_bf16, new_len, positions_host, positions_dev)) != OL_OK) return st;
+  if (!new_pages) return OL_ERR_NULL;
+  if (!valid_page_format(*new_pages)) return OL_ERR_SHAPE;
+  if ((st = no_overlap(v, cache->block_table, sizeof(int32_t) * (size_t)cache->batch * cache->max_pages)) != OL_OK)
+    return st;
+  const ol_paged_kv k = paged_shape_of(cache);
+  if ((st = check_pages(&k, positions_host, new_len, true, -1)) != OL_OK) return st;
+  if (new_len > 0 &&
+      (st = check_hpaged_formats(cache, nullptr, -1, nullptr, positions_host, new_len)) != OL_OK)
+    return st;
+  if ((st = check_owner(v.ranges, v.nranges, v.owner)) != OL_OK) return st;
+  record_hpaged(cache, nullptr, nullptr, 0, positions_host, new_len, new_pages, 0);
+  if (fault_injected()) return OL_ERR_INJECTED;
+  AppendParams p = {};
+  p.layout = OL_LAYOUT_HPAGED;
+  p.dtype = OL_BF16;
+  p.batch = v.batch;
+  p.kv_heads = v.kv_heads;
+  p.head_dim = v.head_dim;
+  p.capacity = v.capacity;
+  p.new_len = new_len;
+  p.values = values_bf16;
+  p.positions = positions_dev;
+  p.pool = cache->pool;
+  p.block_table = cache->block_table;
+  p.num_pages = cache->num_pages;
+  p.page_size = cache->page_size;
+  p.max_pages = cache->max_pages;
+  p.page_fmt = cache->formats;
+  p.new_fmt = *new_pages;
+  if (launch_hpaged_append(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return OL_ERR_CUDA;
+  if (new_len > 0) hpaged_start_pages(cache, positions_host, new_len, *new_pages);
+  return OL_OK;
+}
+
+ol_status ol_hpaged_decode_attention(const ol_hpaged_kv* cache, const void* q, int32_t q_heads,
+                                     const int32_t* lens_host, const int32_t* lens_dev, const void* cur_kv,
+                                     float scale, int32_t window, void* out, int32_t out_dtype, void* workspace,
+                                     size_t ws_bytes, ol_stream stream) {
+  CacheView v;
+  ol_status st = view_hpaged(cache, v);
+  if (st != OL_OK) return st;
+  if (cur_kv && lens_host)
+    for (int b = 0; b < v.batch; ++b)
+      if (lens_host[b] < 1) return OL_ERR_CAPACITY;
+  return run_attention(OL_LAYOUT_HPAGED, cache, v, q, q_heads, lens_host, lens_dev, cur_kv, 0, cur_kv ? 1 : 0,
+                       scale, window, out, out_dtype, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+ol_status ol_hpaged_decode_step(const ol_hpaged_kv* cache, void* updated, const void* q, int32_t q_heads,
+                                const void* new_kv, const ol_page_format* new_pages, const int32_t* lens_host,
+                                const int32_t* lens_dev, float scale, int32_t window, void* out, int32_t out_dtype,
+                                void* workspace, size_t ws_bytes, ol_stream stream) {
+  CacheView v;
+  ol_status st = view_hpaged(cache, v);
+  if (st != OL_OK) return st;
+  if ((st = writable(v, updated)) != OL_OK) return st;
+  if (!new_kv || !new_pages) return OL_ERR_NULL;
+  st = run_attention(OL_LAYOUT_HPAGED, cache, v, q, q_heads, lens_host, lens_dev, new_kv, 1, 1, scale, window, out,
+                     out_dtype, workspace, ws_bytes, static_cast<cudaStream_t>(stream), 1, false, new_pages);
+  if (st != OL_OK) return st;
+  std::vector<int32_t> pos(v.batch);
+  for (int b = 0; b < v.batch; ++b) pos[b] = lens_host[b] - 1;
+  hpaged_start_pages(cache, pos.data(), 1, *new_pages);
+  return OL_OK;
+}
+
+ol_status ol_hpaged_quantize(const ol_hpaged_kv* cache, void* updated, const int32_t* pages_host,
+                             const int32_t* pages_dev, const int32_t* valid_host, const int32_t* valid_dev, int32_t n,
+                             const ol_page_format* to, ol_stream stream) {
+  CacheView v;
+  ol_status st = view_hpaged(cache, v);
+  if (st != OL_OK) return st;
+  if ((st = writable(v, updated)) != OL_OK) return st;
+  if (!to) return OL_ERR_NULL;
+  if (n < 0) return OL_ERR_SHAPE;
+  if (n > 0 && (!pages_host || !pages_dev || !valid_host || !valid_dev)) return OL_ERR_NULL;
+  if (!valid_page_format(*to)) return OL_ERR_SHAPE;
+  // one head's page rows are staged in shared memory as fp32
+  if ((size_t)cache->page_size * cache->head_dim * 4 > 200 * 1024) return OL_ERR_UNSUPPORTED;
+  if (n > 0 && (!aligned16(pages_dev) || !aligned16(valid_dev))) return OL_ERR_ALIGN;
+  std::vector<char> seen(cache->num_pages, 0);
+  for (int i = 0; i < n; ++i) {
+    const int page = pages_host[i];
+    if (page < 0 || page >= cache->num_pages) return OL_ERR_PAGE;
+    if (seen[page]) return OL_ERR_SHAPE;
+    seen[page] = 1;
+    if (valid_host[i] < 0 || valid_host[i] > cache->page_size) return OL_ERR_CAPACITY;
+    if (!valid_page_format(cache->formats_host[page])) return OL_ERR_SHAPE;
+  }
+  if ((st = no_overlap(v, pages_dev, sizeof(int32_t) * (size_t)n)) != OL_OK) return st;
+  if ((st = no_overlap(v, valid_dev, sizeof(int32_t) * (size_t)n)) != OL_OK) return st;
+  if ((st = check_owner(v.ranges, v.nranges, v.owner)) != OL_OK) return st;
+  {
+    // statistics: the converted rows are read in the old formats and written in the new
+    ol_stats s = {};
+    s.calls = 1;
+    const int D = cache->head_dim;
+    for (int i = 0; i < n; ++i) {
+      const ol_page_format& f = cache->formats_host[pages_host[i]];
+      const int64_t rows = (int64_t)valid_host[i] * cache->kv_heads;
+      s.kv_payload_bytes_read += rows * (int64_t)(fmt_row_bytes(f.k.format, D) + fmt_row_bytes(f.v.format, D));
+      s.dequantized_bytes += rows * D * 4 * ((fmt_affine(f.k.format) ? 1 : 0) + (fmt_affine(f.v.format) ? 1 : 0));
+      s.storage_append_copied_bytes += (int64_t)cache->page_size * cache->kv_heads *
+                                       (int64_t)(fmt_row_bytes(to->k.format, D) + fmt_row_bytes(to->v.format, D));
+    }
+    s.storage_reuse_count = n > 0 ? 2 : 0;
+    record(s);
+  }
+  if (fault_injected()) return OL_ERR_INJECTED;
+  QuantizeParams p = {};
+  p.pool = static_cast<uint8_t*>(cache->pool);
+  p.page_fmt = cache->formats;
+  p.num_pages = cache->num_pages;
+  p.kv_heads = cache->kv_heads;
+  p.page_size = cache->page_size;
+  p.head_dim = cache->head_dim;
+  p.pages = pages_dev;
+  p.valid = valid_dev;
+  p.n = n;
+  p.to = *to;
+  if (launch_hpaged_quantize(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return OL_ERR_CUDA;
+  for (int i = 0; i < n; ++i) cache->formats_host[pages_host[i]] = *to;
+  return OL_OK;
 }
 
 }  // extern "C"

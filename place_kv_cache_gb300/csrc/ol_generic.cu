@@ -1,6 +1,6 @@
 // ol_generic.cu -- CUDA-core decode attention for every layout and dtype:
-// contiguous fp32/bf16, paged fp32/bf16 and INT4, any head_dim up to 256, any
-// GQA group. It serves the shapes the tensor-core kernels do not take (for
+// contiguous fp32/bf16, paged fp32/bf16, INT4 and heterogeneous pages (each
+// page decoded by its own formats), any head_dim up to 256, any GQA group. It serves the shapes the tensor-core kernels do not take (for
 // example fp32 caches with head_dim 4) with the same split plan, merge and
 // fused append as they use.
 //
@@ -9,7 +9,7 @@
 // dimensions; per token the warp reduces q.k with shuffles and updates an
 // online-softmax state (m, l, o) per query head. Warps merge in shared memory
 // and the CTA finishes through the split-K ticket (finish_split).
-#include "ol_common.cuh"
+#include "ol_hpaged.cuh"
 
 namespace ol {
 namespace {
@@ -36,6 +36,17 @@ __device__ __forceinline__ float load_kv(const AttnParams& p, int plane, int b, 
                   t % p.page_size) * D + d;
     return p.dtype == OL_F32 ? reinterpret_cast<const float*>(p.pool)[idx]
                              : bf16_bits_to_float(reinterpret_cast<const uint16_t*>(p.pool)[idx]);
+  }
+  if (p.layout == OL_LAYOUT_HPAGED) {
+    int page = p.block_table[(size_t)b * p.max_pages + t / p.page_size];
+    if (page < 0 || page >= p.num_pages) {
+      set_status(p.status, OL_DEVICE_GUARD);
+      return 0.f;
+    }
+    const ol_plane_format pf = plane == 0 ? p.page_fmt[page].k : p.page_fmt[page].v;
+    return hp_decode(hp_row(reinterpret_cast<uint8_t*>(p.pool), p.kv_heads, p.page_size, D, page, plane, g,
+                            t % p.page_size, pf.format),
+                     d, pf);
   }
   // INT4: (code - zp) * scale
   size_t row = (((size_t)plane * p.batch + b) * p.kv_heads + g) * p.capacity + t;
@@ -66,6 +77,28 @@ __device__ void append_token_warp(const AttnParams& p, int b, int g, int pos) {
       int4_quantize_row_warp(reinterpret_cast<const uint16_t*>(p.new_kv) + src, D, p.quant_mode,
                              p.fixed_scale, p.fixed_zp, p.codes + row * (D / 2),
                              p.scales + row * (D / 32), p.zps + row * (D / 64));
+      continue;
+    }
+    if (p.layout == OL_LAYOUT_HPAGED) {
+      int page = p.block_table[(size_t)b * p.max_pages + pos / p.page_size];
+      if (page < 0 || page >= p.num_pages) {
+        if (lane == 0) set_status(p.status, OL_DEVICE_GUARD);
+        return;
+      }
+      const int slot = pos % p.page_size;
+      // a token in slot 0 starts its page, which takes the step's formats
+      const ol_plane_format pf = slot == 0 ? (plane == 0 ? p.new_fmt.k : p.new_fmt.v)
+                                           : (plane == 0 ? p.page_fmt[page].k : p.page_fmt[page].v);
+      const uint16_t* x = reinterpret_cast<const uint16_t*>(p.new_kv) + src;
+      hp_encode_row_warp([&](int d) { return bf16_bits_to_float(x[d]); }, D, pf,
+                         hp_row(reinterpret_cast<uint8_t*>(p.pool), p.kv_heads, p.page_size, D, page, plane, g,
+                                slot, pf.format));
+      if (slot == 0 && g == 0 && lane == 0) {
+        if (plane == 0)
+          p.page_fmt[page].k = pf;
+        else
+          p.page_fmt[page].v = pf;
+      }
       continue;
     }
     size_t dst;

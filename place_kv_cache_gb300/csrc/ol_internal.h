@@ -63,6 +63,9 @@ struct AttnParams {
   int quant_mode;
   float fixed_scale;
   int fixed_zp;
+  // heterogeneous pages (pool, block_table, num_pages, page_size, max_pages as for paged)
+  ol_page_format* page_fmt;  // device [num_pages]
+  ol_page_format new_fmt;    // formats of the pages a fused append starts
 
   const void* q;        // [B, Hq, D]
   const int32_t* lens;  // device [B]
@@ -115,7 +118,22 @@ struct AppendParams {
   const int32_t* positions;  // device [B], or NULL: every row uses scalar_position
   int scalar_position;
   int positions_are_lens;    // 1: positions[b] is a length and the append starts at positions[b] - new_len
+  ol_page_format* page_fmt;  // heterogeneous pages: device [num_pages]
+  ol_page_format new_fmt;    // formats of the pages the append starts
 };
+
+// Selected-page conversion of a heterogeneous paged cache.
+struct QuantizeParams {
+  uint8_t* pool;
+  ol_page_format* page_fmt;  // device [num_pages]
+  int num_pages, kv_heads, page_size, head_dim;
+  const int32_t* pages;      // device [n]
+  const int32_t* valid;      // device [n]
+  int n;
+  ol_page_format to;
+};
+cudaError_t launch_hpaged_quantize(const QuantizeParams& p, cudaStream_t s);
+cudaError_t launch_hpaged_append(const AppendParams& p, cudaStream_t s);
 
 // Launchers (return cudaSuccess or the launch error).
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
@@ -168,5 +186,25 @@ __host__ __device__
 inline int split_tile(int s, int ntiles, int nsplit) {
   return (int)(((long long)s * ntiles) / nsplit);
 }
+
+// Element formats of the heterogeneous paged cache (host and device).
+#if defined(__CUDACC__)
+#define OL_HD __host__ __device__
+#else
+#define OL_HD
+#endif
+OL_HD inline int fmt_bits(int f) {
+  return f == OL_FMT_F32 ? 32 : (f == OL_FMT_F16 || f == OL_FMT_BF16) ? 16
+                                : (f == OL_FMT_I8 || f == OL_FMT_U8)  ? 8
+                                : (f == OL_FMT_I4 || f == OL_FMT_U4)  ? 4
+                                                                      : 2;
+}
+OL_HD inline bool fmt_affine(int f) { return f >= OL_FMT_I8 && f <= OL_FMT_U2; }
+OL_HD inline bool fmt_signed(int f) { return f == OL_FMT_I8 || f == OL_FMT_I4 || f == OL_FMT_I2; }
+OL_HD inline int fmt_qmin(int f) { return fmt_signed(f) ? -(1 << (fmt_bits(f) - 1)) : 0; }
+OL_HD inline int fmt_qmax(int f) { return fmt_signed(f) ? (1 << (fmt_bits(f) - 1)) - 1 : (1 << fmt_bits(f)) - 1; }
+// bytes of one row of D elements (D a multiple of 4)
+OL_HD inline size_t fmt_row_bytes(int f, int D) { return (size_t)D * fmt_bits(f) / 8; }
+#undef OL_HD
 
 }  // namespace ol

@@ -58,7 +58,7 @@ class Workload:
     kv_heads: int
     head_dim: int
     capacity: int              # tokens per row (contiguous / INT4) or pages*page_size (paged)
-    layout: str                # "contiguous" | "paged" | "int4"
+    layout: str                # "contiguous" | "paged" | "int4" | "hpaged" (per-page formats)
     seed: int
     lens_fixed: Optional[int] = None          # every row has this length
     lens_range: Optional[tuple] = None        # inclusive uniform range, drawn per row
@@ -98,7 +98,34 @@ WORKLOADS = {
     # appends and scores its drafted tokens
     "chunk4_b32": Workload("chunk4_b32", "bf16", 32, 32, 8, 128, 8192, "contiguous",
                            seed=6, lens_range=(512, 8192), chunk=4),
+    # heterogeneous pages: the paged shape with every page's K/V formats chosen
+    # by its age (AGE_FORMATS): recent pages BFLOAT16, older INT8, oldest 4-bit
+    "hpaged_b64": Workload("hpaged_b64", "bf16", 64, 32, 8, 128, 16384, "hpaged", seed=7,
+                           lens_range=(1, 16384), page_size=16, num_pages=65536),
 }
+
+# Page formats of the heterogeneous workloads, as (format, scale, zero point)
+# for K and for V; format codes FLOAT 0, FLOAT16 1, BFLOAT16 2, INT8 3, UINT8 4,
+# INT4 5, UINT4 6, INT2 7, UINT2 8. The formats are a caller's policy (page
+# "Persistent input/output feedback", §Optional heterogeneous paged KV: the
+# caller picks each page's format, for example from the retained length): a
+# page whose last slot is fewer than `age` tokens behind the row's end takes
+# the first entry that admits it. Scales fit N(0, 1) values: INT8 at 1/32
+# covers +/-3.97, INT4 and UINT4 (zero point 8) at 0.5 cover -4..3.5.
+AGE_FORMATS = ((1024, ((2, 1.0, 0), (2, 1.0, 0))),
+               (4096, ((3, 0.03125, 0), (3, 0.03125, 0))),
+               (None, ((5, 0.5, 0), (6, 0.5, 8))))
+
+
+def page_format_classes(lens: np.ndarray, page_size: int, max_pages: int, ages=AGE_FORMATS) -> np.ndarray:
+    """[B, max_pages] index into ``ages`` of each logical page's format (pages
+    past a row's end get the class of age 0, the format a new page starts in)."""
+    out = np.zeros((len(lens), max_pages), np.int32)
+    for b, n in enumerate(lens):
+        for j in range(max_pages):
+            age = max(int(n) - (j + 1) * page_size, 0)
+            out[b, j] = next(i for i, (lim, _) in enumerate(ages) if lim is None or age < lim)
+    return out
 
 
 def _draw(rng: np.random.Generator, shape, dist: str) -> np.ndarray:
@@ -159,7 +186,7 @@ def make_case(w: Workload, *, lens: Optional[np.ndarray] = None, seed: Optional[
     else:
         lens = np.asarray(lens, dtype=np.int32)
     perm = None
-    if w.layout == "paged":
+    if w.layout in ("paged", "hpaged"):
         perm = rng.permutation(w.num_pages).astype(np.int32)
     D = w.head_dim
     q = _store(_draw(rng, (w.batch, w.q_heads, D), w.dist), w.dtype)
