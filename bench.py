@@ -31,7 +31,9 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from workloads import WORKLOADS, bf16_from_f32, make_case  # noqa: E402
+from workloads import AGE_FORMATS, WORKLOADS, bf16_from_f32, make_case, page_format_classes  # noqa: E402
+
+FORMAT_BITS = {0: 32, 1: 16, 2: 16, 3: 8, 4: 8, 5: 4, 6: 4, 7: 2, 8: 2}   # heterogeneous page formats
 
 METRIC = "decode step: achieved HBM GB/s (% of ~8 TB/s roofline), µs/step, rows·tok/s"
 L2_BYTES = 129 * 1024 * 1024
@@ -102,6 +104,22 @@ def step_bytes(w, lens):
         hist = float(np.sum(lens - T)) * w.kv_heads * 2 * D * elt
         new = w.batch * w.kv_heads * T * 2 * D * elt
         return hist + 2 * new + 2 * w.batch * w.q_heads * T * D * 2   # new K/V written and read; q and y
+    if w.layout == "hpaged":
+        # each history token in its page's formats (K and V rows of D * bits / 8
+        # bytes), plus a block-table entry and a 24-byte format pair per page
+        S, M = w.page_size, w.max_pages_per_row
+        cls = page_format_classes(lens, S, M)
+        row = [D * (FORMAT_BITS[k[0]] + FORMAT_BITS[v[0]]) // 8 for _, (k, v) in AGE_FORMATS]
+        hist = 0.0
+        for b, n in enumerate(lens):
+            h = int(n) - 1
+            for j in range((h + S - 1) // S):
+                hist += min(S, h - j * S) * row[cls[b, j]]
+        hist = hist * w.kv_heads + float(np.sum(np.ceil(lens / S))) * (4 + 24)
+        cur = w.batch * w.kv_heads * 2 * D * 2
+        written = w.batch * w.kv_heads * row[0]
+        q = w.batch * w.q_heads * D * 2
+        return hist + cur + written + q + q
     if w.layout == "int4":
         kv_tok = 2 * (D // 2 + (D // 32) * 2 + D // 64)         # codes + fp16 scales + zero points, K and V
         hist = float(np.sum(lens - 1)) * w.kv_heads * kv_tok
@@ -252,6 +270,8 @@ class Setup:
         w = self.w
         if w.layout == "paged":
             return 2 * w.num_pages * w.kv_heads * w.page_size * w.head_dim * 2
+        if w.layout == "hpaged":
+            return 2 * w.num_pages * w.kv_heads * w.page_size * w.head_dim * 4
         if w.layout == "int4":
             return 2 * w.batch * w.kv_heads * w.capacity * (w.head_dim // 2 + w.head_dim // 16 + w.head_dim // 64)
         return 2 * w.batch * w.kv_heads * w.capacity * w.head_dim * 2
@@ -285,6 +305,8 @@ class Setup:
             self.descs.append(ol.paged_kv(pool, bt_d, table, access=acc))
             self.updated.append(pool)
             self.layout = ol.OL_LAYOUT_PAGED
+        elif w.layout == "hpaged":
+            self._make_hpaged_replica(gen, rng, acc)
         else:
             rows = 2 * B * H * w.capacity
             codes = torch.randint(0, 256, (2, B, H, w.capacity, D // 2), generator=gen, device=self.dev,
@@ -299,6 +321,45 @@ class Setup:
             self.updated.append(codes)
             self.layout = ol.OL_LAYOUT_INT4
 
+    def _make_hpaged_replica(self, gen, rng, acc):
+        """Every row's history (lens - 1 tokens) appended through the library in
+        the formats of its pages' ages: one append per run of pages of one class."""
+        torch, ol, w = self.torch, self.ol, self.w
+        B, H, D, S, M, P = w.batch, w.kv_heads, w.head_dim, w.page_size, w.max_pages_per_row, w.num_pages
+        pool = torch.empty(P * 2 * H * S * D * 4, dtype=torch.uint8, device=self.dev)
+        mirror = np.zeros(P, ol.PAGE_FORMAT_DTYPE)
+        (kf, ks, kz), (vf, vs, vz) = AGE_FORMATS[0][1]
+        mirror["kf"], mirror["ks"], mirror["kz"], mirror["vf"], mirror["vs"], mirror["vz"] = kf, ks, kz, vf, vs, vz
+        fmt_d = torch.from_numpy(mirror.view(np.uint8).copy()).to(self.dev)
+        perm = rng.permutation(P).astype(np.int32)
+        table = np.ascontiguousarray(perm[: B * M].reshape(B, M))
+        bt_d = torch.from_numpy(table).to(self.dev)
+        cls = page_format_classes(self.lens, S, M)
+        for b in range(B):
+            hist = int(self.lens[b]) - 1
+            row_t = np.ascontiguousarray(table[b:b + 1])
+            row_kv = ol.hpaged_kv(pool, fmt_d, mirror, bt_d[b:b + 1], row_t, kv_heads=H, page_size=S, head_dim=D)
+            j = 0
+            npages = (hist + S - 1) // S
+            while j < npages:
+                j1 = j
+                while j1 < npages and cls[b, j1] == cls[b, j]:
+                    j1 += 1
+                t0, t1 = j * S, min(j1 * S, hist)
+                vals = torch.randn((2, 1, H, t1 - t0, D), generator=gen, device=self.dev).to(torch.bfloat16)
+                k, v = AGE_FORMATS[cls[b, j]][1]
+                pos = np.array([t0], np.int32)
+                ol.ol_hpaged_append(row_kv, pool, vals, t1 - t0, pos, torch.from_numpy(pos).to(self.dev),
+                                    ol.page_format(k=k, v=v))
+                j = j1
+        torch.cuda.synchronize()
+        self.new_pages = ol.page_format(*AGE_FORMATS[0][1])
+        self.caches.append((pool, fmt_d, mirror, bt_d, table))
+        self.descs.append(ol.hpaged_kv(pool, fmt_d, mirror, bt_d, table, kv_heads=H, page_size=S, head_dim=D,
+                                       access=acc))
+        self.updated.append(pool)
+        self.layout = ol.OL_LAYOUT_HPAGED
+
     def step(self, i, stream=None):
         """Step i of the rotation: replica i % replicas, chain position i % chain."""
         r, c = i % self.replicas, i % self.chain
@@ -306,6 +367,11 @@ class Setup:
             self.ol.ol_chunk_step(self.layout, self.descs[r], self.updated[r], self.q, self.w.q_heads, self.w.chunk,
                                   self.new_kv, self.lens_list[c], self.lens_d_list[c], 0.0, -1, self.out,
                                   self.ol.OL_BF16, self.ws, self.ws_bytes, stream=stream)
+            return
+        if self.w.layout == "hpaged":
+            self.ol.ol_hpaged_decode_step(self.descs[r], self.updated[r], self.q, self.w.q_heads, self.new_kv,
+                                          self.new_pages, self.lens_list[c], self.lens_d_list[c], 0.0, -1, self.out,
+                                          self.ol.OL_BF16, self.ws, self.ws_bytes, stream=stream)
             return
         self.ol.ol_decode_step(self.layout, self.descs[r], self.updated[r], self.q, self.w.q_heads, self.new_kv,
                                self.lens_list[c], self.lens_d_list[c], 0.0, -1, self.out, self.ol.OL_BF16, self.ws,
@@ -372,7 +438,7 @@ def run_ours(args, rank, world, dist):
     result = {
         "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if w.layout != "int4" else "u4+bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": {"int4": "u4+bf16", "hpaged": "bf16+i8+i4/u4 pages, f32 math"}.get(w.layout, "bf16"), "data": "synthetic",
         "us_per_step": round(ms_per_step * 1e3, 3),
         "rows_tok_per_s": round(w.batch * world / (ms_per_step * 1e-3), 1),
         "pct_of_hbm_roofline": round(100.0 * gbs / world / peak, 2),
@@ -390,10 +456,12 @@ def run_ours(args, rank, world, dist):
         "device_status": status,
         "clocks": clk.summary(),
     }
-    if not args.no_e2e and w.chunk == 1:
+    if not args.no_e2e and w.chunk == 1 and w.layout != "hpaged":
         result["e2e"] = run_e2e(s, stream, K_e2e=min(K, 200 * R))
     elif not args.no_e2e:
-        result["e2e"] = None  # the host-buffer call is a decode step; chunked steps run from device buffers
+        # the host-buffer call serves the decode step of the uniform layouts; chunked
+        # steps and heterogeneous pages run from device buffers
+        result["e2e"] = None
     if w.chunk > 1:
         result["config"]["chunk"] = w.chunk
     return result
@@ -447,6 +515,8 @@ def oracle_step_inputs(w, max_rows):
     from workloads import scaled
     rows = min(w.batch, max_rows)
     ws = scaled(w, batch=rows)
+    if w.layout == "hpaged":   # the sample's rows own their pages; a pool of the full size is not needed
+        ws = scaled(ws, num_pages=rows * w.max_pages_per_row)
     case = make_case(ws, seed=w.seed, history_len_offset=w.chunk)
     return O, ws, case
 
@@ -481,6 +551,22 @@ def run_oracle_steps(w, budget_s, max_rows):
         def one():
             O.paged_update(pool, table, case.new_kv, case.lens - 1)
             return O.paged_attention(case.q, pool, table, case.lens)
+    elif w.layout == "hpaged":
+        S, M, H, D = ws.page_size, ws.max_pages_per_row, ws.kv_heads, ws.head_dim
+        pool, desc = O.hpaged_pool(ws.num_pages, H, S, D)
+        table = block_table(case)
+        cls = page_format_classes(case.lens, S, M)
+        for b, h in enumerate(case.history):
+            for j in range((h.shape[2] + S - 1) // S):
+                k, v = AGE_FORMATS[cls[b, j]][1]
+                O.hpaged_append(pool, desc, table[b:b + 1], h[:, None, :, j * S:(j + 1) * S], [j * S],
+                                O.page_desc(k=k, v=v))
+        new_fmt = O.page_desc(*AGE_FORMATS[0][1])
+
+        def one():
+            y = O.hpaged_attention(case.q, pool, desc, table, case.lens, H, cur_kv=case.new_kv)
+            O.hpaged_append(pool, desc, table, case.new_kv, case.lens - 1, new_fmt)
+            return y
     else:
         planes = O.int4_planes(ws.batch, ws.kv_heads, ws.capacity, ws.head_dim)
         for b, h in enumerate(case.history):
@@ -511,7 +597,8 @@ def run_oracle_steps(w, budget_s, max_rows):
 
 def run_reference(args, rank, world):
     w = WORKLOADS[args.workload]
-    max_rows = {"qwen_b1_gqa7": 1, "ragged_b32": 4, "paged_b64": 2, "int4_b16": 1, "chunk4_b32": 1}[w.name]
+    max_rows = {"qwen_b1_gqa7": 1, "ragged_b32": 4, "paged_b64": 2, "int4_b16": 1, "chunk4_b32": 1,
+                "hpaged_b64": 2}[w.name]
     K = args.steps if args.steps is not None else 3
     budget = 60.0
     res = run_oracle_steps(w, budget_s=min(budget, 10.0 * max(1, K)), max_rows=max_rows)
@@ -540,7 +627,8 @@ def main():
     result = run_ours(args, rank, world, dist)
     if rank == 0 and not args.no_cpu_baseline:
         w = WORKLOADS[args.workload]
-        max_rows = {"qwen_b1_gqa7": 1, "ragged_b32": 4, "paged_b64": 2, "int4_b16": 1, "chunk4_b32": 1}[w.name]
+        max_rows = {"qwen_b1_gqa7": 1, "ragged_b32": 4, "paged_b64": 2, "int4_b16": 1, "chunk4_b32": 1,
+                "hpaged_b64": 2}[w.name]
         result["cpu_baseline"] = run_oracle_steps(w, budget_s=10.0, max_rows=max_rows)
     if dist is not None:
         dist.barrier()

@@ -14,7 +14,7 @@ CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_objs")
 LIB = os.path.join(HERE, "libol.so")
 SOURCES = ["ol_api.cpp", "ol_append.cu", "ol_generic.cu", "ol_fast_bf16.cu", "ol_fast_int4.cu", "ol_noalloc.cu",
-           "ol_hpaged.cu"]
+           "ol_hpaged.cu", "ol_fast_hpaged.cu"]
 HEADERS = ["ol_internal.h", "ol_common.cuh", "ol_merge.cuh", "ol_fast_bf16_kernel.inc", "ol_hpaged.cuh",
            os.path.join("..", "..", "include", "ol.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -53,13 +53,14 @@ bool fault_injected() {
 size_t elt_bytes(int dtype) { return dtype == OL_F32 ? 4 : 2; }
 bool valid_dtype(int d) { return d == OL_F32 || d == OL_BF16; }
 
-// Launch tuning: OL_TUNE="waves=<w>,minchunk=<c>,cfg=<variant>,cluster=<cs>,cpu=<k>" (read once).
+// Launch tuning: OL_TUNE="waves=<w>,minchunk=<c>,cfg=<variant>,cluster=<cs>,cpu=<k>,generic=<0|1>" (read once).
 struct Tune {
   int waves = 2;
   int min_chunk = 16;
   int cfg = -1;      // tensor-core kernel variant; -1 = default
   int cluster = -1;  // cluster size cap; -1 = automatic
   int clusters_per_unit = -1;  // cap on clusters per (row, kv head) for small batches
+  bool generic = false;        // heterogeneous pages: the CUDA-core kernel even where the tensor-core one applies
 };
 const Tune& tune() {
   static Tune t = [] {
@@ -80,6 +81,7 @@ const Tune& tune() {
         if (k == "cfg" && val >= 0 && val <= 3) x.cfg = val;
         if (k == "cluster" && val >= 1) x.cluster = val;
         if (k == "cpu" && val >= 1) x.clusters_per_unit = val;
+        if (k == "generic") x.generic = val != 0;
       }
       if (comma == std::string::npos) break;
       pos = comma + 1;
@@ -710,6 +712,10 @@ ol_status run_attention(int layout, const void* desc, const CacheView& v, const 
   } else if (layout == OL_LAYOUT_INT4 && fast_int4_supported(p)) {
     plan_fast(p, lens_host, sms);
     e = launch_fast_int4(p, stream);
+  } else if (layout == OL_LAYOUT_HPAGED && fast_hpaged_supported(p) && !tune().generic) {
+    plan_splits(p, lens_host, (long long)sms * fast_hpaged_ctas_per_sm() * tune().waves, 1);
+    p.variant = 0;
+    e = launch_fast_hpaged(p, stream);
   } else {
     plan_splits(p, lens_host, (long long)sms * 4, 1);
     p.variant = 0;

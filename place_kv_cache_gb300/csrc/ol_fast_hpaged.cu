@@ -1,0 +1,772 @@
+// ol_fast_hpaged.cu -- tensor-core decode attention (and fused append) over
+// the heterogeneous paged cache, for head_dim 128, a GQA group of at most 8
+// and pages of a multiple of 16 slots: every 16-token tile lies in one page
+// and takes that page's K and V formats.
+//
+// Decomposition as in the bf16 kernel: one CTA per (row, kv head, split),
+// warps over 16-token tiles with their own STAGES-deep rings, the shared
+// merge. A tile's K and V arrive as the bytes they occupy in the pool: TMA
+// 2-D copies of 16 rows through one tensor map per row width (256, 128, 64
+// and 32 bytes) whose swizzle keeps the reads below free of bank conflicts.
+// FLOAT planes (512-byte rows) are read by the warp from global memory.
+//
+// Dequantization is exact, inside the MMA operands:
+//   S^T = K q^T
+//     BFLOAT16: K against bf16 q.  FLOAT: bf16 hi + lo of K against bf16 q.
+//     FLOAT16: K against fp16 q * 2^e[col] (e puts the column's largest |q|
+//     in [2^14, 2^15), so the conversion of q is exact).
+//     Affine codes: the code bits themselves as fp16 subnormals c' * 2^-24
+//     (c' = c + 2^(bits-1) for signed formats, so c' >= 0) against the same
+//     fp16 q, then s = scale * (2^(24 - e) acc - zp' * sum(q)), zp' the
+//     zero point with the same offset. The code formats take q in a permuted
+//     dimension order: the order in which a lane finds its codes in the tile.
+//   O^T += V^T P^T
+//     Dense formats: V as stored (FLOAT as bf16 hi + lo) against P^T as
+//     bf16 (FLOAT16: fp16) hi + lo.  Affine codes: V^T as the exact fp16
+//     difference (1024 + c') - (1024 + zp') against fp16 P^T hi + lo into a
+//     per-tile accumulator that is added to O times the V scale.
+//     Every format writes O^T in one permuted dimension order (m-tile 2b + h,
+//     row r: dimension 32b + 4r + 2h; row r + 8: the next one), put back in
+//     order when the warp state is stored.
+// The token being appended takes part uncompressed from new_kv after the tile
+// loop; the fused step encodes it into its page in that page's formats.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ol_hpaged.cuh"
+#include "ol_merge.cuh"
+
+namespace ol {
+namespace {
+
+constexpr int kTok = 16;
+constexpr int kRegion = 4096;         // one plane of a tile in a stage: 16 rows of up to 256 bytes
+constexpr int kStage = 2 * kRegion;   // K region, V region
+constexpr int kHalf = 2048;           // a 16-bit tile's second 64-dimension half
+constexpr int kInfo = 8;              // ints of tile information per stage
+
+template <int NWARPS, int STAGES>
+struct HpLayout {
+  static constexpr int kStages = NWARPS * STAGES * kStage;
+  static constexpr int kInfoBytes = NWARPS * STAGES * kInfo * 4;
+  static constexpr int kBars = NWARPS * STAGES * 8;
+  static constexpr int kMisc = 256 + NWARPS * 8 * 4 * 2 + 8 * 4 * 6 + 2 * 16 * 8 * 4 + 16;
+  static constexpr int kTotal = 1024 + kStages + kInfoBytes + kBars + kMisc;
+  static constexpr int kBySmem = (228 * 1024) / (kTotal + 1024) > 0 ? (228 * 1024) / (kTotal + 1024) : 1;
+  static constexpr int kPerSm = kBySmem < 2 ? kBySmem : 2;  // and registers: up to 255 per thread
+  static_assert(STAGES >= 2, "the merged O lives in warp 0's second stage");
+  static_assert(8 * kOStride * 4 <= kStage, "a warp state fits one stage");
+};
+
+// ---------------------------------------------------------------- helpers
+
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) { return __byte_perm(a, b, sel); }
+// (a & b) ^ c in one instruction
+__device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t hsub2_f16(uint32_t a, uint32_t b) {
+  __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+// bf16 pair of (x, y) and the pair of their remainders
+__device__ __forceinline__ void split_bf16(float x, float y, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16x2(x, y);
+  lo = pack_bf16x2(x - __uint_as_float(hi << 16), y - __uint_as_float(hi & 0xffff0000u));
+}
+__device__ __forceinline__ void split_f16(float x, float y, uint32_t& hi, uint32_t& lo) {
+  hi = pack_f16x2(x, y);
+  const float2 h = __half22float2(*reinterpret_cast<__half2*>(&hi));
+  lo = pack_f16x2(x - h.x, y - h.y);
+}
+
+// Code offset of a signed format (its codes are read as c + 2^(bits-1)).
+__device__ __forceinline__ int code_offset(int f) { return fmt_signed(f) ? 1 << (fmt_bits(f) - 1) : 0; }
+
+// Row of the tensor map of row width fmt_row_bytes(f, 128) that holds
+// (page, plane, head g, page slot s).
+__device__ __forceinline__ int map_row(const AttnParams& p, int page, int plane, int g, int s, int f) {
+  const int per_plane = p.kv_heads * p.page_size * (32 / fmt_bits(f));  // rows of this width per plane
+  return (page * 2 + plane) * per_plane + g * p.page_size + s;
+}
+
+// -------------------------------------------------------------- the kernel
+
+template <int NWARPS, int STAGES>
+__global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
+    fast_hpaged_kernel(const __grid_constant__ CUtensorMap tm16, const __grid_constant__ CUtensorMap tm8,
+                       const __grid_constant__ CUtensorMap tm4, const __grid_constant__ CUtensorMap tm2,
+                       const __grid_constant__ AttnParams p) {
+  using L = HpLayout<NWARPS, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* stages = smem;
+  int* info = reinterpret_cast<int*>(smem + L::kStages);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kStages + L::kInfoBytes);
+  Work* sw = reinterpret_cast<Work*>(smem + L::kStages + L::kInfoBytes + L::kBars);
+  float* misc = reinterpret_cast<float*>(smem + L::kStages + L::kInfoBytes + L::kBars + 256);
+  MergeScratch ms;
+  ms.wm = misc;
+  ms.wl = ms.wm + NWARPS * 8;
+  ms.m = ms.wl + NWARPS * 8;
+  ms.l = ms.m + 8;
+  ms.cm = ms.l + 8;
+  ms.cl = ms.cm + 8;
+  ms.scr = ms.cl + 8;
+  ms.cw = ms.scr + 16;
+  ms.wt = ms.cw + 16 * 8;
+  ms.flag = reinterpret_cast<int*>(ms.wt + 16 * 8);
+  ms.recv_o = ms.recv_m = ms.recv_l = nullptr;  // no cluster
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&tm16);
+    prefetch_tensormap(&tm8);
+    prefetch_tensormap(&tm4);
+    prefetch_tensormap(&tm2);
+  }
+  const uint32_t bar0 = smem_u32(bars + warp * STAGES);
+  if (lane == 0) {
+    for (int st = 0; st < STAGES; ++st) mbar_init(bar0 + 8 * st, 1);
+    fence_mbar_init();
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  if (warp == 0) {
+    Work w = p.inline_lens ? map_cta_warp(p.lens_inline, p.batch, p.kv_heads, p.capacity, p.window, p.chunk,
+                                          blockIdx.x, nullptr)
+                           : map_cta_warp(p.lens, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, blockIdx.x,
+                                          p.status);
+    if (lane == 0) *sw = w;
+  }
+  __syncthreads();
+  const Work w = *sw;
+  if (!w.valid) return;
+
+  const int G = p.group;
+  const int cur = p.cur_from_new ? w.hi - 1 : -1;
+  // history tiles: [t_begin, tend); the current token (from new_kv) is not read from the cache
+  const int hist_end = p.cur_from_new ? w.hi - 1 : w.hi;
+  const int tend = min(w.t_end, hist_end);
+  const int nsub = tend > w.t_begin ? (tend - w.t_begin + kTok - 1) / kTok : 0;
+  const int my_n = nsub > warp ? (nsub - warp + NWARPS - 1) / NWARPS : 0;
+  uint8_t* my_stages = stages + warp * STAGES * kStage;
+  int* my_info = info + warp * STAGES * kInfo;
+  const uint64_t pol = policy_evict_first();
+  const ol_page_format* __restrict__ fmts = p.page_fmt;
+
+  // lane 0: look up tile i's page and formats, record them, request its bytes
+  auto issue = [&](int i) {
+    const int st = i % STAGES;
+    const int t0 = w.t_begin + (warp + i * NWARPS) * kTok;
+    int page = __ldg(p.block_table + (size_t)w.b * p.max_pages + t0 / p.page_size);
+    if (page < 0 || page >= p.num_pages) {
+      set_status(p.status, OL_DEVICE_GUARD);
+      page = 0;
+    }
+    const int s0 = t0 % p.page_size;
+    const ol_page_format f = fmts[page];
+    int* inf = my_info + st * kInfo;
+    inf[0] = page;
+    inf[1] = f.k.format;
+    inf[2] = __float_as_int(f.k.scale);
+    inf[3] = f.k.zero_point;
+    inf[4] = f.v.format;
+    inf[5] = __float_as_int(f.v.scale);
+    inf[6] = f.v.zero_point;
+    const int fk = min(max(f.k.format, 0), (int)OL_FMT_U2), fv = min(max(f.v.format, 0), (int)OL_FMT_U2);
+    const uint32_t bk = fk == OL_FMT_F32 ? 0u : kTok * (uint32_t)fmt_row_bytes(fk, 128);
+    const uint32_t bv = fv == OL_FMT_F32 ? 0u : kTok * (uint32_t)fmt_row_bytes(fv, 128);
+    const uint32_t dst = smem_u32(my_stages + st * kStage);
+    const uint32_t bar = bar0 + 8 * st;
+    mbar_arrive_expect_tx(bar, bk + bv);
+    for (int plane = 0; plane < 2; ++plane) {
+      const int fmt = plane == 0 ? fk : fv;
+      if (fmt == OL_FMT_F32) continue;
+      const uint32_t d = dst + plane * kRegion;
+      const int row = map_row(p, page, plane, w.g, s0, fmt);
+      switch (fmt_bits(fmt)) {
+        case 16:
+          tma_load_2d(d, &tm16, 0, row, bar, pol);
+          tma_load_2d(d + kHalf, &tm16, 64, row, bar, pol);
+          break;
+        case 8: tma_load_2d(d, &tm8, 0, row, bar, pol); break;
+        case 4: tma_load_2d(d, &tm4, 0, row, bar, pol); break;
+        default: tma_load_2d(d, &tm2, 0, row, bar, pol); break;
+      }
+    }
+  };
+  if (lane == 0)
+    for (int i = 0; i < min(my_n, STAGES); ++i) issue(i);
+
+  // ---- q in three operand forms (lane: c = lane % 4, n = lane / 4 = head)
+  const int c = lane & 3, n = lane >> 2;
+  const bool live = n < G;
+  const uint16_t* qp = reinterpret_cast<const uint16_t*>(p.q) + ((size_t)w.b * p.q_heads + (size_t)w.g * G +
+                                                                 (live ? n : 0)) * 128;
+  // this lane's 32 dims 32c .. 32c + 31 of head n: per-head scale exponent and sum
+  uint32_t qraw[16];
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(qp + 32 * c);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 v = live ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
+      qraw[4 * k] = v.x;
+      qraw[4 * k + 1] = v.y;
+      qraw[4 * k + 2] = v.z;
+      qraw[4 * k + 3] = v.w;
+    }
+  }
+  float qmax = 0.f, qsum = 0.f;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const float lo = __uint_as_float(qraw[k] << 16), hi = __uint_as_float(qraw[k] & 0xffff0000u);
+    qmax = fmaxf(qmax, fmaxf(fabsf(lo), fabsf(hi)));
+    qsum += lo + hi;
+  }
+  qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 1));
+  qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 2));
+  qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+  qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+  const int qe = qmax > 0.f ? 14 - ilogbf(qmax) : 0;  // head n's exponent e
+  // B operands: standard order (dims 16kk + 2c, +1 | +8, +9) in bf16 (the
+  // fp16 copy for FLOAT16 pages is made per tile from it), code order
+  // (kk = 2i + h: dims 32c + 8i + {2h, 2h+4} | {2h+1, 2h+5}) in fp16
+  const float s2e = ldexpf(1.f, qe);  // 2^e, exact
+  uint32_t qb[8][2], qc[8][2];
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    qb[kk][0] = live ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * kk + 2 * c)) : 0u;
+    qb[kk][1] = live ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * kk + 2 * c + 8)) : 0u;
+    const int i = kk >> 1, h = kk & 1;
+    // qraw[4i + m] holds dims 32c + 8i + 2m, + 1
+    auto qv = [&](int j) {  // element e_j of block i as float
+      const uint32_t wd = qraw[4 * i + (j >> 1)];
+      return (j & 1) ? __uint_as_float(wd & 0xffff0000u) : __uint_as_float(wd << 16);
+    };
+    qc[kk][0] = pack_f16x2(qv(2 * h) * s2e, qv(2 * h + 4) * s2e);
+    qc[kk][1] = pack_f16x2(qv(2 * h + 1) * s2e, qv(2 * h + 5) * s2e);
+  }
+  // exponent and sum of q for this lane's state columns 2c, 2c + 1
+  const int e0 = __shfl_sync(0xffffffffu, qe, 8 * c), e1 = __shfl_sync(0xffffffffu, qe, 8 * c + 4);
+  const float qs0 = __shfl_sync(0xffffffffu, qsum, 8 * c), qs1 = __shfl_sync(0xffffffffu, qsum, 8 * c + 4);
+
+  float o[8][4];
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+  float m_run0 = -INFINITY, m_run1 = -INFINITY, l_run0 = 0.f, l_run1 = 0.f;
+
+  const int mi = lane >> 3, r8 = lane & 7;
+  const int rK = r8 + 8 * (mi & 1), cK = mi >> 1;  // ldmatrix roles for 16-bit K
+  const float sl2 = p.scale_log2;
+  const uint8_t* pool = reinterpret_cast<const uint8_t*>(p.pool);
+  const size_t slot_bytes = (size_t)p.kv_heads * p.page_size * 128 * 8;  // 2 planes x 128 dims x 4 bytes
+
+  for (int i = 0; i < my_n; ++i) {
+    const int st = i % STAGES;
+    if (!mbar_wait_bounded(bar0 + 8 * st, (i / STAGES) & 1)) {
+      if (lane == 0) set_status(p.status, OL_DEVICE_GUARD);
+      break;
+    }
+    const int t0 = w.t_begin + (warp + i * NWARPS) * kTok;
+    const int* inf = my_info + st * kInfo;
+    const int page = inf[0];
+    const int fk = min(max(inf[1], 0), (int)OL_FMT_U2), fv = min(max(inf[4], 0), (int)OL_FMT_U2);
+    const float ks = __int_as_float(inf[2]), vs = __int_as_float(inf[5]);
+    const int kz = inf[3] + code_offset(fk), vz = inf[6] + code_offset(fv);
+    const uint32_t sK = smem_u32(my_stages + st * kStage), sV = sK + kRegion;
+    const int s0 = t0 % p.page_size;
+    const uint8_t* gK = pool + (size_t)page * slot_bytes + ((size_t)w.g * p.page_size + s0) * 512;
+    const uint8_t* gV = gK + slot_bytes / 2;
+
+    // V rows at or past the history end hold no data: zero their bytes
+    const int vhi = hist_end - t0;
+    if (vhi < kTok && fv != OL_FMT_F32) {
+      const int rb = (int)fmt_row_bytes(fv, 128), cpr = rb / 16;
+      uint8_t* v = my_stages + st * kStage + kRegion;
+      for (int idx = lane; idx < (kTok - vhi) * cpr; idx += 32) {
+        const int r = vhi + idx / cpr, ch = idx % cpr;
+        const int off = rb == 256 ? (ch >> 3) * kHalf + r * 128 + (ch & 7) * 16 : r * rb + ch * 16;
+        *reinterpret_cast<uint4*>(v + off) = make_uint4(0, 0, 0, 0);
+      }
+    }
+    __syncwarp();
+
+    // ---- S^T = K q^T
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    float kmul0 = sl2, kmul1 = sl2, kb0 = 0.f, kb1 = 0.f;
+    if (fk == OL_FMT_BF16 || fk == OL_FMT_F16) {
+      const bool h16 = fk == OL_FMT_F16;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const int ch = 2 * kk + cK;
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(sK + (ch >> 3) * kHalf + rK * 128 + (((ch & 7) ^ r8) << 4), a0, a1, a2, a3);
+        if (h16) {
+          const uint32_t b0 = pack_f16x2(__uint_as_float(qb[kk][0] << 16) * s2e,
+                                         __uint_as_float(qb[kk][0] & 0xffff0000u) * s2e);
+          const uint32_t b1 = pack_f16x2(__uint_as_float(qb[kk][1] << 16) * s2e,
+                                         __uint_as_float(qb[kk][1] & 0xffff0000u) * s2e);
+          mma_f16_16816(s, a0, a1, a2, a3, b0, b1);
+        } else
+          mma_bf16_16816(s, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+      }
+      if (h16) {
+        kmul0 = ldexpf(sl2, -e0);
+        kmul1 = ldexpf(sl2, -e1);
+      }
+    } else if (fk == OL_FMT_F32) {
+      const float* ra = reinterpret_cast<const float*>(gK + (size_t)n * 512);
+      const float* rb = reinterpret_cast<const float*>(gK + (size_t)(n + 8) * 512);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const int d = 16 * kk + 2 * c;
+        const float2 x0 = *reinterpret_cast<const float2*>(ra + d), x1 = *reinterpret_cast<const float2*>(rb + d);
+        const float2 x2 = *reinterpret_cast<const float2*>(ra + d + 8);
+        const float2 x3 = *reinterpret_cast<const float2*>(rb + d + 8);
+        uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
+        split_bf16(x0.x, x0.y, h0, l0);
+        split_bf16(x1.x, x1.y, h1, l1);
+        split_bf16(x2.x, x2.y, h2, l2);
+        split_bf16(x3.x, x3.y, h3, l3);
+        mma_bf16_16816(s, h0, h1, h2, h3, qb[kk][0], qb[kk][1]);
+        mma_bf16_16816(s, l0, l1, l2, l3, qb[kk][0], qb[kk][1]);
+      }
+    } else {
+      // affine codes: A = code bits as fp16 subnormals, in code order
+      const int bits = fmt_bits(fk);
+      const bool sgn = fmt_signed(fk);
+      uint32_t ya[8], yb[8];  // row n and row n + 8: this lane's 32 dims 32c .. 32c + 31
+      if (bits == 8) {
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const uint4 va = lds_v4(sK + n * 128 + (((2 * c + m) ^ (n & 7)) << 4));
+          const uint4 vb = lds_v4(sK + (n + 8) * 128 + (((2 * c + m) ^ (n & 7)) << 4));
+          ya[4 * m] = va.x; ya[4 * m + 1] = va.y; ya[4 * m + 2] = va.z; ya[4 * m + 3] = va.w;
+          yb[4 * m] = vb.x; yb[4 * m + 1] = vb.y; yb[4 * m + 2] = vb.z; yb[4 * m + 3] = vb.w;
+        }
+        if (sgn) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            ya[k] ^= 0x80808080u;
+            yb[k] ^= 0x80808080u;
+          }
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int ii = kk >> 1, h = kk & 1;
+          const uint32_t slo = (2 * h) | ((4 + 2 * h) << 8), shi = (2 * h + 1) | ((5 + 2 * h) << 8);
+          const uint32_t a0 = prmt(ya[2 * ii], ya[2 * ii + 1], slo) & 0x00FF00FFu;
+          const uint32_t a1 = prmt(yb[2 * ii], yb[2 * ii + 1], slo) & 0x00FF00FFu;
+          const uint32_t a2 = prmt(ya[2 * ii], ya[2 * ii + 1], shi) & 0x00FF00FFu;
+          const uint32_t a3 = prmt(yb[2 * ii], yb[2 * ii + 1], shi) & 0x00FF00FFu;
+          mma_f16_16816(s, a0, a1, a2, a3, qc[kk][0], qc[kk][1]);
+        }
+      } else if (bits == 4) {
+        const int sw = (n >> 1) & 3;  // rows n and n + 8 share the 64-byte swizzle phase
+        const uint4 va = lds_v4(sK + n * 64 + ((c ^ sw) << 4));
+        const uint4 vb = lds_v4(sK + (n + 8) * 64 + ((c ^ sw) << 4));
+        ya[0] = va.x; ya[1] = va.y; ya[2] = va.z; ya[3] = va.w;
+        yb[0] = vb.x; yb[1] = vb.y; yb[2] = vb.z; yb[3] = vb.w;
+        if (sgn) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            ya[k] ^= 0x88888888u;
+            yb[k] ^= 0x88888888u;
+          }
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int ii = kk >> 1, h = kk & 1;
+          const uint32_t a0 = (ya[ii] >> (8 * h)) & 0x000F000Fu, a1 = (yb[ii] >> (8 * h)) & 0x000F000Fu;
+          const uint32_t a2 = (ya[ii] >> (8 * h + 4)) & 0x000F000Fu, a3 = (yb[ii] >> (8 * h + 4)) & 0x000F000Fu;
+          mma_f16_16816(s, a0, a1, a2, a3, qc[kk][0], qc[kk][1]);
+        }
+      } else {
+        const int sw = (n >> 2) & 1;  // rows n and n + 8 share the 32-byte swizzle phase
+        const uint2 va = lds_v2(sK + n * 32 + ((((c >> 1) ^ sw)) << 4) + 8 * (c & 1));
+        const uint2 vb = lds_v2(sK + (n + 8) * 32 + ((((c >> 1) ^ sw)) << 4) + 8 * (c & 1));
+        ya[0] = va.x; ya[1] = va.y;
+        yb[0] = vb.x; yb[1] = vb.y;
+        if (sgn) {
+          ya[0] ^= 0xAAAAAAAAu; ya[1] ^= 0xAAAAAAAAu;
+          yb[0] ^= 0xAAAAAAAAu; yb[1] ^= 0xAAAAAAAAu;
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int ii = kk >> 1, h = kk & 1;
+          // block ii: 16 bits of word ii / 2, spread to one byte per 16-bit half
+          const uint32_t sel = (ii & 1) ? 0x4342u : 0x4140u;
+          const uint32_t ua = prmt(ya[ii >> 1], 0u, sel), ub = prmt(yb[ii >> 1], 0u, sel);
+          const uint32_t a0 = (ua >> (4 * h)) & 0x00030003u, a1 = (ub >> (4 * h)) & 0x00030003u;
+          const uint32_t a2 = (ua >> (4 * h + 2)) & 0x00030003u, a3 = (ub >> (4 * h + 2)) & 0x00030003u;
+          mma_f16_16816(s, a0, a1, a2, a3, qc[kk][0], qc[kk][1]);
+        }
+      }
+      kmul0 = ldexpf(ks * sl2, 24 - e0);
+      kmul1 = ldexpf(ks * sl2, 24 - e1);
+      kb0 = ks * sl2 * (float)kz * qs0;
+      kb1 = ks * sl2 * (float)kz * qs1;
+    }
+
+    // ---- online softmax on the S^T columns (exp2 domain)
+    const int ta = t0 + n, tb = ta + 8;
+    const bool va_ = ta >= w.lo && ta < tend, vb_ = tb >= w.lo && tb < tend;
+    const float s00 = va_ ? fmaf(s[0], kmul0, -kb0) : -INFINITY;
+    const float s01 = va_ ? fmaf(s[1], kmul1, -kb1) : -INFINITY;
+    const float s10 = vb_ ? fmaf(s[2], kmul0, -kb0) : -INFINITY;
+    const float s11 = vb_ ? fmaf(s[3], kmul1, -kb1) : -INFINITY;
+    float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(m_run0, mx0), mn1 = fmaxf(m_run1, mx1);
+    const float b0 = mn0 == -INFINITY ? 0.f : mn0, b1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float al0 = fast_exp2(m_run0 - b0), al1 = fast_exp2(m_run1 - b1);
+    const float p00 = fast_exp2(s00 - b0), p01 = fast_exp2(s01 - b1);
+    const float p10 = fast_exp2(s10 - b0), p11 = fast_exp2(s11 - b1);
+    l_run0 = l_run0 * al0 + (p00 + p10);
+    l_run1 = l_run1 * al1 + (p01 + p11);
+    if (__any_sync(0xffffffffu, mn0 != m_run0 || mn1 != m_run1)) {
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        o[mt][0] *= al0;
+        o[mt][1] *= al1;
+        o[mt][2] *= al0;
+        o[mt][3] *= al1;
+      }
+    }
+    m_run0 = mn0;
+    m_run1 = mn1;
+
+    // ---- O^T += V^T P^T (dimension order: m-tile 2bb + hh, row n -> 32bb + 4n + 2hh, row n + 8 -> + 1)
+    const int TA = 2 * c, TB = 2 * c + 1, TC = 2 * c + 8, TD = 2 * c + 9;  // this lane's tokens (k rows)
+    if (fv == OL_FMT_BF16 || fv == OL_FMT_F16 || fv == OL_FMT_F32) {
+      const bool h16 = fv == OL_FMT_F16;
+      uint32_t ph0, ph1, pl0, pl1;
+      {
+        uint32_t h0, l0, h1, l1;
+        if (h16) {
+          split_f16(p00, p01, h0, l0);
+          split_f16(p10, p11, h1, l1);
+        } else {
+          split_bf16(p00, p01, h0, l0);
+          split_bf16(p10, p11, h1, l1);
+        }
+        ph0 = movmatrix_trans(h0);
+        ph1 = movmatrix_trans(h1);
+        pl0 = movmatrix_trans(l0);
+        pl1 = movmatrix_trans(l1);
+      }
+      if (fv == OL_FMT_F32) {
+        // V from global memory; rows at or past the history end count as zero
+        const int vrow[4] = {TA, TB, TC, TD};
+#pragma unroll
+        for (int bb = 0; bb < 4; ++bb) {
+          float4 x[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            x[k] = vrow[k] < vhi ? *reinterpret_cast<const float4*>(gV + (size_t)vrow[k] * 512 +
+                                                                    (32 * bb + 4 * n) * 4)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const float xa0 = hh ? x[0].z : x[0].x, xa1 = hh ? x[0].w : x[0].y;
+            const float xb0 = hh ? x[1].z : x[1].x, xb1 = hh ? x[1].w : x[1].y;
+            const float xc0 = hh ? x[2].z : x[2].x, xc1 = hh ? x[2].w : x[2].y;
+            const float xd0 = hh ? x[3].z : x[3].x, xd1 = hh ? x[3].w : x[3].y;
+            uint32_t a0h, a0l, a1h, a1l, a2h, a2l, a3h, a3l;
+            split_bf16(xa0, xb0, a0h, a0l);
+            split_bf16(xa1, xb1, a1h, a1l);
+            split_bf16(xc0, xd0, a2h, a2l);
+            split_bf16(xc1, xd1, a3h, a3l);
+            mma_bf16_16816(o[2 * bb + hh], a0h, a1h, a2h, a3h, ph0, ph1);
+            mma_bf16_16816(o[2 * bb + hh], a0h, a1h, a2h, a3h, pl0, pl1);
+            mma_bf16_16816(o[2 * bb + hh], a0l, a1l, a2l, a3l, ph0, ph1);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int bb = 0; bb < 4; ++bb) {
+          // 8 bytes (dims 32bb + 4n .. + 3) of each of the four token rows
+          const int e = 32 * (bb & 1) + 4 * n;  // element within the 64-dim half
+          const int ch = e >> 3, sub = (e & 7) * 2;
+          const uint32_t hb = sV + (bb >> 1) * kHalf + sub;
+          const uint2 wa = lds_v2(hb + TA * 128 + ((ch ^ (TA & 7)) << 4));
+          const uint2 wb = lds_v2(hb + TB * 128 + ((ch ^ (TB & 7)) << 4));
+          const uint2 wc = lds_v2(hb + TC * 128 + ((ch ^ (TC & 7)) << 4));
+          const uint2 wd = lds_v2(hb + TD * 128 + ((ch ^ (TD & 7)) << 4));
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint32_t xa = hh ? wa.y : wa.x, xb = hh ? wb.y : wb.x;
+            const uint32_t xc = hh ? wc.y : wc.x, xd = hh ? wd.y : wd.x;
+            const uint32_t a0 = prmt(xa, xb, 0x5410u), a1 = prmt(xa, xb, 0x7632u);
+            const uint32_t a2 = prmt(xc, xd, 0x5410u), a3 = prmt(xc, xd, 0x7632u);
+            if (h16) {
+              mma_f16_16816(o[2 * bb + hh], a0, a1, a2, a3, ph0, ph1);
+              mma_f16_16816(o[2 * bb + hh], a0, a1, a2, a3, pl0, pl1);
+            } else {
+              mma_bf16_16816(o[2 * bb + hh], a0, a1, a2, a3, ph0, ph1);
+              mma_bf16_16816(o[2 * bb + hh], a0, a1, a2, a3, pl0, pl1);
+            }
+          }
+        }
+      }
+    } else {
+      // affine codes: V^T as exact fp16 (1024 + c') - (1024 + zp'), P^T in fp16 hi + lo
+      uint32_t ph0, ph1, pl0, pl1;
+      {
+        uint32_t h0, l0, h1, l1;
+        split_f16(p00, p01, h0, l0);
+        split_f16(p10, p11, h1, l1);
+        ph0 = movmatrix_trans(h0);
+        ph1 = movmatrix_trans(h1);
+        pl0 = movmatrix_trans(l0);
+        pl1 = movmatrix_trans(l1);
+      }
+      const int bits = fmt_bits(fv);
+      const bool sgn = fmt_signed(fv);
+      const uint32_t zf = (uint32_t)__half_as_ushort(__int2half_rn(1024 + vz));
+      const uint32_t zpair = zf | (zf << 16);
+      auto add_tile = [&](int mt, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
+        float t4[4] = {0.f, 0.f, 0.f, 0.f};
+        a0 = hsub2_f16(a0, zpair);
+        a1 = hsub2_f16(a1, zpair);
+        a2 = hsub2_f16(a2, zpair);
+        a3 = hsub2_f16(a3, zpair);
+        mma_f16_16816(t4, a0, a1, a2, a3, ph0, ph1);
+        mma_f16_16816(t4, a0, a1, a2, a3, pl0, pl1);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[mt][j] = fmaf(t4[j], vs, o[mt][j]);
+      };
+      if (bits == 8) {
+        const uint32_t magic = sgn ? 0x64806480u : 0x64006400u;
+#pragma unroll
+        for (int bb = 0; bb < 4; ++bb) {
+          const int ch = 2 * bb + (n >> 2), sub = 4 * (n & 3);
+          const uint32_t xa = lds_u32(sV + TA * 128 + ((ch ^ (TA & 7)) << 4) + sub);
+          const uint32_t xb = lds_u32(sV + TB * 128 + ((ch ^ (TB & 7)) << 4) + sub);
+          const uint32_t xc = lds_u32(sV + TC * 128 + ((ch ^ (TC & 7)) << 4) + sub);
+          const uint32_t xd = lds_u32(sV + TD * 128 + ((ch ^ (TD & 7)) << 4) + sub);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint32_t s0_ = (2 * hh) | ((4 + 2 * hh) << 8), s1_ = (2 * hh + 1) | ((5 + 2 * hh) << 8);
+            add_tile(2 * bb + hh, and_xor(prmt(xa, xb, s0_), 0x00FF00FFu, magic),
+                     and_xor(prmt(xa, xb, s1_), 0x00FF00FFu, magic), and_xor(prmt(xc, xd, s0_), 0x00FF00FFu, magic),
+                     and_xor(prmt(xc, xd, s1_), 0x00FF00FFu, magic));
+          }
+        }
+      } else if (bits == 4) {
+        const uint32_t magic = sgn ? 0x64086408u : 0x64006400u;
+#pragma unroll
+        for (int bp = 0; bp < 2; ++bp) {
+          // matrices (tokens 0-7 | 8-15) x (32-dim blocks 2bp | 2bp + 1)
+          const int t = r8 + 8 * (mi & 1), cb = 2 * bp + (mi >> 1);
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4_trans(sV + t * 64 + ((cb ^ ((t >> 1) & 3)) << 4), r0, r1, r2, r3);
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const uint32_t x01 = q ? r2 : r0, x89 = q ? r3 : r1;  // tokens 2c, 2c+1 | 2c+8, 2c+9
+            const int bb = 2 * bp + q;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+              add_tile(2 * bb + hh, and_xor(x01 >> (8 * hh), 0x000F000Fu, magic),
+                       and_xor(x01 >> (8 * hh + 4), 0x000F000Fu, magic),
+                       and_xor(x89 >> (8 * hh), 0x000F000Fu, magic),
+                       and_xor(x89 >> (8 * hh + 4), 0x000F000Fu, magic));
+          }
+        }
+      } else {
+        const uint32_t magic = sgn ? 0x64026402u : 0x64006400u;
+#pragma unroll
+        for (int bb = 0; bb < 4; ++bb) {
+          // byte 8bb + n of each token row: dims 32bb + 4n .. + 3
+          const int x = 8 * bb + n, ch = x >> 4, sub = x & 15;
+          const uint32_t ba = lds_u8(sV + TA * 32 + ((ch ^ ((TA >> 2) & 1)) << 4) + sub);
+          const uint32_t bbv = lds_u8(sV + TB * 32 + ((ch ^ ((TB >> 2) & 1)) << 4) + sub);
+          const uint32_t bc = lds_u8(sV + TC * 32 + ((ch ^ ((TC >> 2) & 1)) << 4) + sub);
+          const uint32_t bd = lds_u8(sV + TD * 32 + ((ch ^ ((TD >> 2) & 1)) << 4) + sub);
+          const uint32_t xab = prmt(ba, bbv, 0x1410u), xcd = prmt(bc, bd, 0x1410u);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+            add_tile(2 * bb + hh, and_xor(xab >> (4 * hh), 0x00030003u, magic),
+                     and_xor(xab >> (4 * hh + 2), 0x00030003u, magic), and_xor(xcd >> (4 * hh), 0x00030003u, magic),
+                     and_xor(xcd >> (4 * hh + 2), 0x00030003u, magic));
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && i + STAGES < my_n) {
+      fence_proxy_async_smem();  // generic writes to this stage (zeroed rows) before the async-proxy refill
+      issue(i + STAGES);
+    }
+    __syncwarp();
+  }
+
+  // ---- the current token, uncompressed from new_kv, in warp 0's state; the
+  // fused step also encodes it into its page
+  if (cur >= w.t_begin && cur < w.t_end && cur >= 0) {
+    const uint16_t* nk = reinterpret_cast<const uint16_t*>(p.new_kv) + ((size_t)w.b * p.kv_heads + w.g) * 128;
+    const uint16_t* nv = reinterpret_cast<const uint16_t*>(p.new_kv) +
+                         (((size_t)p.batch + w.b) * p.kv_heads + w.g) * 128;
+    if (warp == 0) {
+      float part = 0.f;
+      if (live) {
+#pragma unroll 8
+        for (int d = 32 * c; d < 32 * c + 32; ++d) part = fmaf(bf16_bits_to_float(qp[d]), bf16_bits_to_float(nk[d]), part);
+      }
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
+      // head n's score sits in lanes 4n .. 4n + 3; this lane's columns are 2c, 2c + 1
+      const float sc0 = __shfl_sync(0xffffffffu, part, 8 * c) * sl2;
+      const float sc1 = __shfl_sync(0xffffffffu, part, 8 * c + 4) * sl2;
+      const float s0c = 2 * c < G ? sc0 : -INFINITY, s1c = 2 * c + 1 < G ? sc1 : -INFINITY;
+      const float mn0 = fmaxf(m_run0, s0c), mn1 = fmaxf(m_run1, s1c);
+      const float b0 = mn0 == -INFINITY ? 0.f : mn0, b1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float al0 = fast_exp2(m_run0 - b0), al1 = fast_exp2(m_run1 - b1);
+      const float pc0 = fast_exp2(s0c - b0), pc1 = fast_exp2(s1c - b1);
+      // l is summed over the 8 lanes of a column when the state is stored: add p once
+      l_run0 = l_run0 * al0 + (n == 0 ? pc0 : 0.f);
+      l_run1 = l_run1 * al1 + (n == 0 ? pc1 : 0.f);
+      m_run0 = mn0;
+      m_run1 = mn1;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        const int da = 32 * (mt >> 1) + 4 * n + 2 * (mt & 1);
+        const float va = bf16_bits_to_float(nv[da]), vb = bf16_bits_to_float(nv[da + 1]);
+        o[mt][0] = fmaf(pc0, va, o[mt][0] * al0);
+        o[mt][1] = fmaf(pc1, va, o[mt][1] * al1);
+        o[mt][2] = fmaf(pc0, vb, o[mt][2] * al0);
+        o[mt][3] = fmaf(pc1, vb, o[mt][3] * al1);
+      }
+    } else if (warp == 1 && p.append) {
+      const int page = __ldg(p.block_table + (size_t)w.b * p.max_pages + cur / p.page_size);
+      if (page >= 0 && page < p.num_pages) {
+        const int slot = cur % p.page_size;
+        for (int plane = 0; plane < 2; ++plane) {
+          // a token in slot 0 starts its page, which takes the step's formats
+          const ol_plane_format pf = slot == 0 ? (plane == 0 ? p.new_fmt.k : p.new_fmt.v)
+                                               : (plane == 0 ? fmts[page].k : fmts[page].v);
+          const uint16_t* x = plane == 0 ? nk : nv;
+          hp_encode_row_warp([&](int d) { return bf16_bits_to_float(x[d]); }, 128, pf,
+                             hp_row(reinterpret_cast<uint8_t*>(p.pool), p.kv_heads, p.page_size, 128, page, plane,
+                                    w.g, slot, pf.format));
+          if (slot == 0 && w.g == 0 && lane == 0) {
+            if (plane == 0)
+              p.page_fmt[page].k = pf;
+            else
+              p.page_fmt[page].v = pf;
+          }
+        }
+      } else if (lane == 0) {
+        set_status(p.status, OL_DEVICE_GUARD);
+      }
+    }
+  }
+
+  store_warp_state<true>(reinterpret_cast<float*>(my_stages), ms, warp, o, m_run0, m_run1, l_run0, l_run1);
+  float* merged = reinterpret_cast<float*>(stages + kStage);  // warp 0's second stage
+  merge_and_finish(
+      p, w, NWARPS, [&](int st) { return reinterpret_cast<const float*>(stages + st * STAGES * kStage); }, merged,
+      nullptr, ms);
+}
+
+// ------------------------------------------------------------------ host
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// The pool as rows of `width` bytes (16-bit elements for width 256), boxes of 16 rows.
+bool encode_width(CUtensorMap* map, void* base, uint64_t pool_bytes, int width) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const bool wide = width == 256;
+  cuuint64_t dims[2] = {wide ? 128u : (cuuint64_t)width, pool_bytes / width};
+  cuuint64_t strides[1] = {(cuuint64_t)width};
+  cuuint32_t box[2] = {wide ? 64u : (cuuint32_t)width, kTok};
+  cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle sw = width >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : width == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                              : CU_TENSOR_MAP_SWIZZLE_32B;
+  return fn(map, wide ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int kWarps = 4, kStages = 3;
+
+cudaError_t ensure_attrs() {
+  static cudaError_t state = cudaFuncSetAttribute(fast_hpaged_kernel<kWarps, kStages>,
+                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  HpLayout<kWarps, kStages>::kTotal);
+  return state;
+}
+
+}  // namespace
+
+bool fast_hpaged_supported(const AttnParams& p) {
+  if (p.layout != OL_LAYOUT_HPAGED || p.head_dim != 128 || p.group > 8 || p.nq != 1) return false;
+  if (p.page_size % kTok != 0) return false;
+  // TMA row coordinates are 32-bit: the 32-byte-row view has the most rows
+  const unsigned long long rows32 = (unsigned long long)p.num_pages * p.kv_heads * p.page_size * 128 * 8 / 32;
+  return rows32 < (1ull << 31);
+}
+
+int fast_hpaged_ctas_per_sm() { return HpLayout<kWarps, kStages>::kPerSm; }
+
+cudaError_t launch_fast_hpaged(const AttnParams& p, cudaStream_t s) {
+  if (p.total_ctas <= 0) return cudaSuccess;
+  const uint64_t bytes = (uint64_t)p.num_pages * p.kv_heads * p.page_size * 128 * 8;
+  CUtensorMap maps[4];
+  if (!encode_width(&maps[0], p.pool, bytes, 256) || !encode_width(&maps[1], p.pool, bytes, 128) ||
+      !encode_width(&maps[2], p.pool, bytes, 64) || !encode_width(&maps[3], p.pool, bytes, 32))
+    return cudaErrorInvalidValue;
+  cudaError_t e = ensure_attrs();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.total_ctas, 1, 1);
+  cfg.blockDim = dim3(kWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = HpLayout<kWarps, kStages>::kTotal;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fast_hpaged_kernel<kWarps, kStages>, maps[0], maps[1], maps[2], maps[3], p);
+}
+
+}  // namespace ol

@@ -149,6 +149,9 @@ int fast_int4_smem(int variant);
 int fast_int4_warps(int variant);
 int fast_int4_max_cluster(int variant);
 cudaError_t launch_fast_int4(const AttnParams& p, cudaStream_t s);
+bool fast_hpaged_supported(const AttnParams& p);
+int fast_hpaged_ctas_per_sm();
+cudaError_t launch_fast_hpaged(const AttnParams& p, cudaStream_t s);
 
 // Visible range and split plan of one row, shared by the host planner and the
 // kernels. The tokens [start, hi) (start = lo rounded down to 16) form

@@ -208,3 +208,41 @@ def test_empty_calls_write_nothing():
     ol.ol_hpaged_decode_step(empty, pr.pool_d, to_dev(np.zeros(16, np.uint16)), 4, to_dev(np.zeros(16, np.uint16)), gd,
                              e, to_dev(np.zeros(4, np.int32)), 0.0, -1, out, ol.OL_F32, ws, n)
     pr.check_state()
+
+
+LONG = [  # B, H, S, Hq, lens: several tiles per warp and several splits per (row, kv head)
+    (2, 2, 32, 16, [2500, 1700]),
+    (3, 1, 16, 1, [4096, 33, 1]),
+    (1, 4, 64, 20, [3001]),
+]
+
+
+@pytest.mark.parametrize("shape", LONG, ids=[f"b{s[0]}h{s[1]}s{s[2]}g{s[3] // s[1]}" for s in LONG])
+def test_long_rows_with_every_format_match_oracle(shape):
+    B, H, S, Hq, lens = shape
+    D = 128
+    lens = np.array(lens, np.int32)
+    M = int(-(-lens.max() // S)) + 1
+    pr = Pair(B, H, S, D, M, B * M, seed=606 + S)
+    pr.fill(lens, lambda b, j: (5 * j + 3 * b) % 7 + (j % 3 == 0))
+    q = bf16_from_f32(pr.rng.standard_normal((B, Hq, D)).astype(np.float32))
+    ws, n = workspace(B, Hq, H, D)
+    for window in (-1, 700):
+        out = out_tensor(B, Hq, D, ol.OL_BF16)
+        ol.ol_hpaged_decode_attention(pr.kv, to_dev(q), Hq, lens, to_dev(lens), None, 0.0, window, out, ol.OL_BF16,
+                                      ws, n)
+        torch.cuda.synchronize()
+        check_out(out_as_f64(out), O.hpaged_attention(q, pr.pool, pr.desc, pr.table, lens, H, window=window),
+                  ol.OL_BF16)
+    # a fused step on top: the new token starts or continues its page
+    new_kv = pr.values(1)
+    od, gd = fmt_pair(4)
+    want = O.hpaged_attention(q, pr.pool, pr.desc, pr.table, lens + 1, H, cur_kv=new_kv)
+    O.hpaged_append(pr.pool, pr.desc, pr.table, new_kv, lens, od)
+    out = out_tensor(B, Hq, D, ol.OL_F32)
+    ol.ol_hpaged_decode_step(pr.kv, pr.pool_d, to_dev(q), Hq, to_dev(new_kv), gd, lens + 1, to_dev(lens + 1), 0.0, -1,
+                             out, ol.OL_F32, ws, n)
+    torch.cuda.synchronize()
+    check_out(out_as_f64(out), want, ol.OL_F32)
+    pr.check_state()
+    assert ol.ol_workspace_status(ws) == ol.OL_DEVICE_OK
