@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seconds", type=float, default=1.0, help="target timed seconds when --steps is not given")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="the workload's first ROWS rows only (a smaller device footprint, for profiling)")
     return ap.parse_args()
 
 
@@ -378,13 +380,24 @@ class Setup:
                                self.ws_bytes, stream=stream)
 
 
+def workload_of(args):
+    """The named workload, or its first --rows rows (pages sized to those rows)."""
+    from workloads import scaled
+    w = WORKLOADS[args.workload]
+    if args.rows is not None and args.rows < w.batch:
+        w = scaled(w, batch=args.rows)
+        if w.layout in ("paged", "hpaged"):
+            w = scaled(w, num_pages=args.rows * w.max_pages_per_row)
+    return w
+
+
 def run_ours(args, rank, world, dist):
     import torch
     dev = f"cuda:{int(os.environ.get('LOCAL_RANK', 0))}"
     torch.cuda.set_device(dev)
     import place_kv_cache_gb300 as ol
     ol.load()
-    w = WORKLOADS[args.workload]
+    w = workload_of(args)
     s = Setup(w, dev, seed_offset=rank)
     stream = torch.cuda.Stream(device=dev)
     R = s.replicas

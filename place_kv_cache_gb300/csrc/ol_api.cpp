@@ -53,7 +53,8 @@ bool fault_injected() {
 size_t elt_bytes(int dtype) { return dtype == OL_F32 ? 4 : 2; }
 bool valid_dtype(int d) { return d == OL_F32 || d == OL_BF16; }
 
-// Launch tuning: OL_TUNE="waves=<w>,minchunk=<c>,cfg=<variant>,cluster=<cs>,cpu=<k>,generic=<0|1>" (read once).
+// Launch tuning: OL_TUNE="waves=<w>,minchunk=<c>,cfg=<variant>,cluster=<cs>,cpu=<k>,generic=<0|1>,hpwaves=<w>"
+// (read once).
 struct Tune {
   int waves = 2;
   int min_chunk = 16;
@@ -61,6 +62,7 @@ struct Tune {
   int cluster = -1;  // cluster size cap; -1 = automatic
   int clusters_per_unit = -1;  // cap on clusters per (row, kv head) for small batches
   bool generic = false;        // heterogeneous pages: the CUDA-core kernel even where the tensor-core one applies
+  int hp_waves = 4;            // heterogeneous pages: CTA waves of the split plan (measured best on hpaged_b64)
 };
 const Tune& tune() {
   static Tune t = [] {
@@ -82,6 +84,7 @@ const Tune& tune() {
         if (k == "cluster" && val >= 1) x.cluster = val;
         if (k == "cpu" && val >= 1) x.clusters_per_unit = val;
         if (k == "generic") x.generic = val != 0;
+        if (k == "hpwaves" && val > 0) x.hp_waves = val;
       }
       if (comma == std::string::npos) break;
       pos = comma + 1;
@@ -713,7 +716,7 @@ ol_status run_attention(int layout, const void* desc, const CacheView& v, const 
     plan_fast(p, lens_host, sms);
     e = launch_fast_int4(p, stream);
   } else if (layout == OL_LAYOUT_HPAGED && fast_hpaged_supported(p) && !tune().generic) {
-    plan_splits(p, lens_host, (long long)sms * fast_hpaged_ctas_per_sm() * tune().waves, 1);
+    plan_splits(p, lens_host, (long long)sms * fast_hpaged_ctas_per_sm() * tune().hp_waves, 1);
     p.variant = 0;
     e = launch_fast_hpaged(p, stream);
   } else {

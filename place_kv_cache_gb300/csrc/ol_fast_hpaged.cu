@@ -15,19 +15,23 @@
 //     BFLOAT16: K against bf16 q.  FLOAT: bf16 hi + lo of K against bf16 q.
 //     FLOAT16: K against fp16 q * 2^e[col] (e puts the column's largest |q|
 //     in [2^14, 2^15), so the conversion of q is exact).
-//     Affine codes: the code bits themselves as fp16 subnormals c' * 2^-24
-//     (c' = c + 2^(bits-1) for signed formats, so c' >= 0) against the same
-//     fp16 q, then s = scale * (2^(24 - e) acc - zp' * sum(q)), zp' the
-//     zero point with the same offset. The code formats take q in a permuted
-//     dimension order: the order in which a lane finds its codes in the tile.
+//     Affine codes: the code bits themselves, masked in place, as fp16
+//     subnormals c' * 2^(p - 24) (c' = c + 2^(bits-1) for signed formats, so
+//     c' >= 0; p the code's bit position in its 16-bit half, at most 8)
+//     against the same fp16 q times 2^-p, then
+//     s = scale * (2^(24 - e) acc - zp' * sum(q)), zp' the zero point with
+//     the same offset. Each code width takes q in its own permuted dimension
+//     order: the order in which a lane finds its codes in the tile.
 //   O^T += V^T P^T
 //     Dense formats: V as stored (FLOAT as bf16 hi + lo) against P^T as
 //     bf16 (FLOAT16: fp16) hi + lo.  Affine codes: V^T as the exact fp16
-//     difference (1024 + c') - (1024 + zp') against fp16 P^T hi + lo into a
-//     per-tile accumulator that is added to O times the V scale.
+//     difference (1024 + c') - (1024 + zp') against fp16 (P * m)^T hi + lo,
+//     where the V scale is m * 2^k (m in [1, 2)): O is held in units of 2^k
+//     of the tile's k, rescaled by a power of two when k changes.
 //     Every format writes O^T in one permuted dimension order (m-tile 2b + h,
 //     row r: dimension 32b + 4r + 2h; row r + 8: the next one), put back in
 //     order when the warp state is stored.
+// The q operands in their four orders live in shared memory, once per CTA.
 // The token being appended takes part uncompressed from new_kv after the tile
 // loop; the fused step encodes it into its page in that page's formats.
 #include <cuda_bf16.h>
@@ -48,12 +52,14 @@ constexpr int kInfo = 8;              // ints of tile information per stage
 template <int NWARPS, int STAGES>
 struct HpLayout {
   static constexpr int kStages = NWARPS * STAGES * kStage;
+  static constexpr int kQ = 4 * 8 * 32 * 8;  // q operands: 4 orders x 8 k-steps x 32 lanes x 2 registers
+  static constexpr int kQAux = 2 * 8 * 4;    // per head: exponent e and sum of q
   static constexpr int kInfoBytes = NWARPS * STAGES * kInfo * 4;
   static constexpr int kBars = NWARPS * STAGES * 8;
   static constexpr int kMisc = 256 + NWARPS * 8 * 4 * 2 + 8 * 4 * 6 + 2 * 16 * 8 * 4 + 16;
-  static constexpr int kTotal = 1024 + kStages + kInfoBytes + kBars + kMisc;
+  static constexpr int kTotal = 1024 + kStages + kQ + kQAux + kInfoBytes + kBars + kMisc;
   static constexpr int kBySmem = (228 * 1024) / (kTotal + 1024) > 0 ? (228 * 1024) / (kTotal + 1024) : 1;
-  static constexpr int kPerSm = kBySmem < 2 ? kBySmem : 2;  // and registers: up to 255 per thread
+  static constexpr int kPerSm = kBySmem < 2 ? kBySmem : 2;
   static_assert(STAGES >= 2, "the merged O lives in warp 0's second stage");
   static_assert(8 * kOStride * 4 <= kStage, "a warp state fits one stage");
 };
@@ -68,6 +74,18 @@ __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
 __device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
   uint16_t v;
   asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+// FLOAT-page loads in program order (volatile: not hoisted across the MMAs,
+// which keeps their registers few)
+__device__ __forceinline__ float2 ldg_f2(const float* ptr) {
+  float2 v;
+  asm volatile("ld.global.nc.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(ptr));
+  return v;
+}
+__device__ __forceinline__ float4 ldg_f4(const float* ptr) {
+  float4 v;
+  asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(ptr));
   return v;
 }
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) { return __byte_perm(a, b, sel); }
@@ -96,6 +114,39 @@ __device__ __forceinline__ void split_f16(float x, float y, uint32_t& hi, uint32
   lo = pack_f16x2(x - h.x, y - h.y);
 }
 
+// 2^k as a float: the exponent field directly where it is in range
+__device__ __forceinline__ float pow2f(int k) {
+  return (k >= -126 && k <= 127) ? __int_as_float((k + 127) << 23) : ldexpf(1.f, k);
+}
+// floor(log2(x)) of a positive finite x
+__device__ __forceinline__ int log2_floor(float x) {
+  const int e = (__float_as_int(x) >> 23) & 0xFF;
+  return e != 0 ? e - 127 : ilogbf(x);
+}
+
+// Bounded wait that lets the warp sleep (suspend-time hint) instead of spinning
+// while its tile is in flight; false if the phase did not complete within
+// kWaitLimitCycles.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(1000000u)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait_sleep(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait_sleep(bar, parity)) {
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  }
+  return true;
+}
+
 // Code offset of a signed format (its codes are read as c + 2^(bits-1)).
 __device__ __forceinline__ int code_offset(int f) { return fmt_signed(f) ? 1 << (fmt_bits(f) - 1) : 0; }
 
@@ -117,10 +168,14 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* stages = smem;
-  int* info = reinterpret_cast<int*>(smem + L::kStages);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kStages + L::kInfoBytes);
-  Work* sw = reinterpret_cast<Work*>(smem + L::kStages + L::kInfoBytes + L::kBars);
-  float* misc = reinterpret_cast<float*>(smem + L::kStages + L::kInfoBytes + L::kBars + 256);
+  uint2* qsm = reinterpret_cast<uint2*>(smem + L::kStages);            // [order][kk][lane]
+  int* qexp = reinterpret_cast<int*>(smem + L::kStages + L::kQ);       // [8] per head
+  float* qsum_h = reinterpret_cast<float*>(qexp + 8);                  // [8] per head
+  uint8_t* after_q = smem + L::kStages + L::kQ + L::kQAux;
+  int* info = reinterpret_cast<int*>(after_q);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(after_q + L::kInfoBytes);
+  Work* sw = reinterpret_cast<Work*>(after_q + L::kInfoBytes + L::kBars);
+  float* misc = reinterpret_cast<float*>(after_q + L::kInfoBytes + L::kBars + 256);
   MergeScratch ms;
   ms.wm = misc;
   ms.wl = ms.wm + NWARPS * 8;
@@ -171,30 +226,57 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
   const uint64_t pol = policy_evict_first();
   const ol_page_format* __restrict__ fmts = p.page_fmt;
 
-  // lane 0: look up tile i's page and formats, record them, request its bytes
+  // Look-ahead: lane j holds the page and formats of the warp's tile la_base + j,
+  // so one round of dependent lookups (block table, then format table) serves
+  // 32 tiles instead of stalling the issuing lane on every tile.
+  int la_base = -64, la_page = 0, la_kf = 0, la_ks = 0, la_kz = 0, la_vf = 0, la_vs = 0, la_vz = 0;
+  auto look_ahead = [&](int base) {  // whole warp
+    la_base = base;
+    const int ti = base + lane;
+    if (ti < my_n) {
+      const int t0 = w.t_begin + (warp + ti * NWARPS) * kTok;
+      int page = __ldg(p.block_table + (size_t)w.b * p.max_pages + t0 / p.page_size);
+      if (page < 0 || page >= p.num_pages) {
+        set_status(p.status, OL_DEVICE_GUARD);
+        page = 0;
+      }
+      const int* f = reinterpret_cast<const int*>(fmts + page);
+      la_page = page;
+      la_kf = f[0];
+      la_ks = f[1];
+      la_kz = f[2];
+      la_vf = f[3];
+      la_vs = f[4];
+      la_vz = f[5];
+    }
+  };
+  // whole warp: tile i's page and formats from the look-ahead; lane 0 records
+  // them for the compute phase and requests the tile's bytes
   auto issue = [&](int i) {
+    if (i >= la_base + 32) look_ahead(i);
+    const int src = i - la_base;
+    const int page = __shfl_sync(0xffffffffu, la_page, src);
+    const int kf = __shfl_sync(0xffffffffu, la_kf, src), ks = __shfl_sync(0xffffffffu, la_ks, src);
+    const int kz = __shfl_sync(0xffffffffu, la_kz, src), vf = __shfl_sync(0xffffffffu, la_vf, src);
+    const int vsb = __shfl_sync(0xffffffffu, la_vs, src), vz = __shfl_sync(0xffffffffu, la_vz, src);
+    if (lane != 0) return;
     const int st = i % STAGES;
     const int t0 = w.t_begin + (warp + i * NWARPS) * kTok;
-    int page = __ldg(p.block_table + (size_t)w.b * p.max_pages + t0 / p.page_size);
-    if (page < 0 || page >= p.num_pages) {
-      set_status(p.status, OL_DEVICE_GUARD);
-      page = 0;
-    }
     const int s0 = t0 % p.page_size;
-    const ol_page_format f = fmts[page];
     int* inf = my_info + st * kInfo;
     inf[0] = page;
-    inf[1] = f.k.format;
-    inf[2] = __float_as_int(f.k.scale);
-    inf[3] = f.k.zero_point;
-    inf[4] = f.v.format;
-    inf[5] = __float_as_int(f.v.scale);
-    inf[6] = f.v.zero_point;
-    const int fk = min(max(f.k.format, 0), (int)OL_FMT_U2), fv = min(max(f.v.format, 0), (int)OL_FMT_U2);
+    inf[1] = kf;
+    inf[2] = ks;
+    inf[3] = kz;
+    inf[4] = vf;
+    inf[5] = vsb;
+    inf[6] = vz;
+    const int fk = min(max(kf, 0), (int)OL_FMT_U2), fv = min(max(vf, 0), (int)OL_FMT_U2);
     const uint32_t bk = fk == OL_FMT_F32 ? 0u : kTok * (uint32_t)fmt_row_bytes(fk, 128);
     const uint32_t bv = fv == OL_FMT_F32 ? 0u : kTok * (uint32_t)fmt_row_bytes(fv, 128);
     const uint32_t dst = smem_u32(my_stages + st * kStage);
     const uint32_t bar = bar0 + 8 * st;
+    fence_proxy_async_smem();  // generic writes to this stage (zeroed rows) before the async-proxy refill
     mbar_arrive_expect_tx(bar, bk + bv);
     for (int plane = 0; plane < 2; ++plane) {
       const int fmt = plane == 0 ? fk : fv;
@@ -212,17 +294,16 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
       }
     }
   };
-  if (lane == 0)
-    for (int i = 0; i < min(my_n, STAGES); ++i) issue(i);
+  for (int i = 0; i < min(my_n, STAGES); ++i) issue(i);
 
-  // ---- q in three operand forms (lane: c = lane % 4, n = lane / 4 = head)
+  // ---- q operands (lane: c = lane % 4, n = lane / 4 = head), written once per CTA by warp 0
   const int c = lane & 3, n = lane >> 2;
   const bool live = n < G;
   const uint16_t* qp = reinterpret_cast<const uint16_t*>(p.q) + ((size_t)w.b * p.q_heads + (size_t)w.g * G +
                                                                  (live ? n : 0)) * 128;
-  // this lane's 32 dims 32c .. 32c + 31 of head n: per-head scale exponent and sum
-  uint32_t qraw[16];
-  {
+  if (warp == 0) {
+    // this lane's 32 dims 32c .. 32c + 31 of head n: head n's exponent e and sum
+    uint32_t qraw[16];
     const uint4* src = reinterpret_cast<const uint4*>(qp + 32 * c);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -232,45 +313,69 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
       qraw[4 * k + 2] = v.z;
       qraw[4 * k + 3] = v.w;
     }
-  }
-  float qmax = 0.f, qsum = 0.f;
+    float qmax = 0.f, qsum = 0.f;
 #pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    const float lo = __uint_as_float(qraw[k] << 16), hi = __uint_as_float(qraw[k] & 0xffff0000u);
-    qmax = fmaxf(qmax, fmaxf(fabsf(lo), fabsf(hi)));
-    qsum += lo + hi;
-  }
-  qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 1));
-  qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 2));
-  qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
-  qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
-  const int qe = qmax > 0.f ? 14 - ilogbf(qmax) : 0;  // head n's exponent e
-  // B operands: standard order (dims 16kk + 2c, +1 | +8, +9) in bf16 (the
-  // fp16 copy for FLOAT16 pages is made per tile from it), code order
-  // (kk = 2i + h: dims 32c + 8i + {2h, 2h+4} | {2h+1, 2h+5}) in fp16
-  const float s2e = ldexpf(1.f, qe);  // 2^e, exact
-  uint32_t qb[8][2], qc[8][2];
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    qb[kk][0] = live ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * kk + 2 * c)) : 0u;
-    qb[kk][1] = live ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * kk + 2 * c + 8)) : 0u;
-    const int i = kk >> 1, h = kk & 1;
-    // qraw[4i + m] holds dims 32c + 8i + 2m, + 1
-    auto qv = [&](int j) {  // element e_j of block i as float
-      const uint32_t wd = qraw[4 * i + (j >> 1)];
-      return (j & 1) ? __uint_as_float(wd & 0xffff0000u) : __uint_as_float(wd << 16);
+    for (int k = 0; k < 16; ++k) {
+      const float lo = __uint_as_float(qraw[k] << 16), hi = __uint_as_float(qraw[k] & 0xffff0000u);
+      qmax = fmaxf(qmax, fmaxf(fabsf(lo), fabsf(hi)));
+      qsum += lo + hi;
+    }
+    qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 1));
+    qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 2));
+    qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+    qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+    const int qe = qmax > 0.f ? 14 - log2_floor(qmax) : 0;  // head n's largest |q| * 2^e in [2^14, 2^15)
+    const float s2e_n = pow2f(qe);
+    if (c == 0) {
+      qexp[n] = qe;
+      qsum_h[n] = qsum;
+    }
+    auto qd = [&](int j) {  // q[n][32c + j] * 2^e as float (j < 32)
+      const uint32_t wd = qraw[j >> 1];
+      return ((j & 1) ? __uint_as_float(wd & 0xffff0000u) : __uint_as_float(wd << 16)) * s2e_n;
     };
-    qc[kk][0] = pack_f16x2(qv(2 * h) * s2e, qv(2 * h + 4) * s2e);
-    qc[kk][1] = pack_f16x2(qv(2 * h + 1) * s2e, qv(2 * h + 5) * s2e);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      // order 0, standard: dims 16kk + 2c, +1 | +8, +9 (bf16 as stored)
+      uint2 b;
+      b.x = live ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * kk + 2 * c)) : 0u;
+      b.y = live ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * kk + 2 * c + 8)) : 0u;
+      qsm[(0 * 8 + kk) * 32 + lane] = b;
+      // order 1, 4-bit codes: kk = 2i + h, e_j = 8i + j: (e_2h, e_2h+4) | (e_2h+1, e_2h+5) / 16
+      {
+        const int i = kk >> 1, h = kk & 1, e = 8 * i;
+        b.x = pack_f16x2(qd(e + 2 * h), qd(e + 2 * h + 4));
+        b.y = pack_f16x2(qd(e + 2 * h + 1) * 0.0625f, qd(e + 2 * h + 5) * 0.0625f);
+        qsm[(1 * 8 + kk) * 32 + lane] = b;
+      }
+      // order 2, 8-bit codes: d_j = 4kk + j: (d0, d2) | (d1, d3)
+      b.x = pack_f16x2(qd(4 * kk), qd(4 * kk + 2));
+      b.y = pack_f16x2(qd(4 * kk + 1), qd(4 * kk + 3));
+      qsm[(2 * 8 + kk) * 32 + lane] = b;
+      // order 3, 2-bit codes: word w = kk / 4, pairs j = 2(kk % 4) (+1): (16w + j, 16w + j + 8) / 4^f(j),
+      // f(j) = j below 5, j - 5 from 5 (the bit position / 2 of the masked code)
+      {
+        const int wv = kk >> 2, j0 = 2 * (kk & 3), j1 = j0 + 1;
+        const float f0 = pow2f(-2 * (j0 < 5 ? j0 : j0 - 5)), f1 = pow2f(-2 * (j1 < 5 ? j1 : j1 - 5));
+        b.x = pack_f16x2(qd(16 * wv + j0) * f0, qd(16 * wv + j0 + 8) * f0);
+        b.y = pack_f16x2(qd(16 * wv + j1) * f1, qd(16 * wv + j1 + 8) * f1);
+        qsm[(3 * 8 + kk) * 32 + lane] = b;
+      }
+    }
   }
-  // exponent and sum of q for this lane's state columns 2c, 2c + 1
-  const int e0 = __shfl_sync(0xffffffffu, qe, 8 * c), e1 = __shfl_sync(0xffffffffu, qe, 8 * c + 4);
-  const float qs0 = __shfl_sync(0xffffffffu, qsum, 8 * c), qs1 = __shfl_sync(0xffffffffu, qsum, 8 * c + 4);
+  __syncthreads();
+  const int e_own = qexp[n];                                      // this lane's head (B-operand column n)
+  const float s2e = pow2f(e_own);
+  const int e0 = qexp[2 * c], e1 = qexp[2 * c + 1];               // this lane's state columns 2c, 2c + 1
+  const float qs0 = qsum_h[2 * c], qs1 = qsum_h[2 * c + 1];
+  const uint32_t qbase = smem_u32(qsm) + lane * 8;
+  auto qop = [&](int order, int kk) { return lds_v2(qbase + (order * 8 + kk) * 256); };
 
   float o[8][4];
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   float m_run0 = -INFINITY, m_run1 = -INFINITY, l_run0 = 0.f, l_run1 = 0.f;
+  int ko = 0;  // O is held in units of 2^ko
 
   const int mi = lane >> 3, r8 = lane & 7;
   const int rK = r8 + 8 * (mi & 1), cK = mi >> 1;  // ldmatrix roles for 16-bit K
@@ -280,7 +385,7 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
 
   for (int i = 0; i < my_n; ++i) {
     const int st = i % STAGES;
-    if (!mbar_wait_bounded(bar0 + 8 * st, (i / STAGES) & 1)) {
+    if (!mbar_wait_sleep(bar0 + 8 * st, (i / STAGES) & 1)) {
       if (lane == 0) set_status(p.status, OL_DEVICE_GUARD);
       break;
     }
@@ -308,8 +413,8 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
     }
     __syncwarp();
 
-    // ---- S^T = K q^T
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    // ---- S^T = K q^T, even and odd k-steps in two accumulators (shorter MMA chains)
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
     float kmul0 = sl2, kmul1 = sl2, kb0 = 0.f, kb1 = 0.f;
     if (fk == OL_FMT_BF16 || fk == OL_FMT_F16) {
       const bool h16 = fk == OL_FMT_F16;
@@ -318,18 +423,19 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
         const int ch = 2 * kk + cK;
         uint32_t a0, a1, a2, a3;
         ldsm_x4(sK + (ch >> 3) * kHalf + rK * 128 + (((ch & 7) ^ r8) << 4), a0, a1, a2, a3);
+        const uint2 q = qop(0, kk);
+        float(&acc)[4] = (kk & 1) ? sb : sa;
         if (h16) {
-          const uint32_t b0 = pack_f16x2(__uint_as_float(qb[kk][0] << 16) * s2e,
-                                         __uint_as_float(qb[kk][0] & 0xffff0000u) * s2e);
-          const uint32_t b1 = pack_f16x2(__uint_as_float(qb[kk][1] << 16) * s2e,
-                                         __uint_as_float(qb[kk][1] & 0xffff0000u) * s2e);
-          mma_f16_16816(s, a0, a1, a2, a3, b0, b1);
-        } else
-          mma_bf16_16816(s, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+          const uint32_t b0 = pack_f16x2(__uint_as_float(q.x << 16) * s2e, __uint_as_float(q.x & 0xffff0000u) * s2e);
+          const uint32_t b1 = pack_f16x2(__uint_as_float(q.y << 16) * s2e, __uint_as_float(q.y & 0xffff0000u) * s2e);
+          mma_f16_16816(acc, a0, a1, a2, a3, b0, b1);
+        } else {
+          mma_bf16_16816(acc, a0, a1, a2, a3, q.x, q.y);
+        }
       }
       if (h16) {
-        kmul0 = ldexpf(sl2, -e0);
-        kmul1 = ldexpf(sl2, -e1);
+        kmul0 = sl2 * pow2f(-e0);
+        kmul1 = sl2 * pow2f(-e1);
       }
     } else if (fk == OL_FMT_F32) {
       const float* ra = reinterpret_cast<const float*>(gK + (size_t)n * 512);
@@ -337,23 +443,24 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const int d = 16 * kk + 2 * c;
-        const float2 x0 = *reinterpret_cast<const float2*>(ra + d), x1 = *reinterpret_cast<const float2*>(rb + d);
-        const float2 x2 = *reinterpret_cast<const float2*>(ra + d + 8);
-        const float2 x3 = *reinterpret_cast<const float2*>(rb + d + 8);
+        const float2 x0 = ldg_f2(ra + d), x1 = ldg_f2(rb + d);
+        const float2 x2 = ldg_f2(ra + d + 8), x3 = ldg_f2(rb + d + 8);
         uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
         split_bf16(x0.x, x0.y, h0, l0);
         split_bf16(x1.x, x1.y, h1, l1);
         split_bf16(x2.x, x2.y, h2, l2);
         split_bf16(x3.x, x3.y, h3, l3);
-        mma_bf16_16816(s, h0, h1, h2, h3, qb[kk][0], qb[kk][1]);
-        mma_bf16_16816(s, l0, l1, l2, l3, qb[kk][0], qb[kk][1]);
+        const uint2 q = qop(0, kk);
+        mma_bf16_16816(sa, h0, h1, h2, h3, q.x, q.y);
+        mma_bf16_16816(sb, l0, l1, l2, l3, q.x, q.y);
       }
     } else {
-      // affine codes: A = code bits as fp16 subnormals, in code order
+      // affine codes: A = the code bits masked in place (fp16 subnormals), in the width's q order
       const int bits = fmt_bits(fk);
       const bool sgn = fmt_signed(fk);
-      uint32_t ya[8], yb[8];  // row n and row n + 8: this lane's 32 dims 32c .. 32c + 31
       if (bits == 8) {
+        // rows n and n + 8: this lane's 32 bytes (dims 32c .. 32c + 31) as 8 words of 4 dims
+        uint32_t ya[8], yb[8];
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
           const uint4 va = lds_v4(sK + n * 128 + (((2 * c + m) ^ (n & 7)) << 4));
@@ -361,77 +468,65 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
           ya[4 * m] = va.x; ya[4 * m + 1] = va.y; ya[4 * m + 2] = va.z; ya[4 * m + 3] = va.w;
           yb[4 * m] = vb.x; yb[4 * m + 1] = vb.y; yb[4 * m + 2] = vb.z; yb[4 * m + 3] = vb.w;
         }
-        if (sgn) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            ya[k] ^= 0x80808080u;
-            yb[k] ^= 0x80808080u;
-          }
-        }
+        const uint32_t flip = sgn ? 0x80808080u : 0u;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const int ii = kk >> 1, h = kk & 1;
-          const uint32_t slo = (2 * h) | ((4 + 2 * h) << 8), shi = (2 * h + 1) | ((5 + 2 * h) << 8);
-          const uint32_t a0 = prmt(ya[2 * ii], ya[2 * ii + 1], slo) & 0x00FF00FFu;
-          const uint32_t a1 = prmt(yb[2 * ii], yb[2 * ii + 1], slo) & 0x00FF00FFu;
-          const uint32_t a2 = prmt(ya[2 * ii], ya[2 * ii + 1], shi) & 0x00FF00FFu;
-          const uint32_t a3 = prmt(yb[2 * ii], yb[2 * ii + 1], shi) & 0x00FF00FFu;
-          mma_f16_16816(s, a0, a1, a2, a3, qc[kk][0], qc[kk][1]);
+          const uint32_t x = ya[kk] ^ flip, y = yb[kk] ^ flip;
+          const uint2 q = qop(2, kk);
+          mma_f16_16816((kk & 1) ? sb : sa, x & 0x00FF00FFu, y & 0x00FF00FFu, (x >> 8) & 0x00FF00FFu,
+                        (y >> 8) & 0x00FF00FFu, q.x, q.y);
         }
       } else if (bits == 4) {
         const int sw = (n >> 1) & 3;  // rows n and n + 8 share the 64-byte swizzle phase
         const uint4 va = lds_v4(sK + n * 64 + ((c ^ sw) << 4));
         const uint4 vb = lds_v4(sK + (n + 8) * 64 + ((c ^ sw) << 4));
-        ya[0] = va.x; ya[1] = va.y; ya[2] = va.z; ya[3] = va.w;
-        yb[0] = vb.x; yb[1] = vb.y; yb[2] = vb.z; yb[3] = vb.w;
-        if (sgn) {
+        const uint32_t flip = sgn ? 0x88888888u : 0u;
+        const uint32_t xa[4] = {va.x ^ flip, va.y ^ flip, va.z ^ flip, va.w ^ flip};
+        const uint32_t xb[4] = {vb.x ^ flip, vb.y ^ flip, vb.z ^ flip, vb.w ^ flip};
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            ya[k] ^= 0x88888888u;
-            yb[k] ^= 0x88888888u;
-          }
-        }
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const int ii = kk >> 1, h = kk & 1;
-          const uint32_t a0 = (ya[ii] >> (8 * h)) & 0x000F000Fu, a1 = (yb[ii] >> (8 * h)) & 0x000F000Fu;
-          const uint32_t a2 = (ya[ii] >> (8 * h + 4)) & 0x000F000Fu, a3 = (yb[ii] >> (8 * h + 4)) & 0x000F000Fu;
-          mma_f16_16816(s, a0, a1, a2, a3, qc[kk][0], qc[kk][1]);
+        for (int ii = 0; ii < 4; ++ii) {
+          // nibbles j = 0, 4 | 1, 5 (x16) in place; then 2, 6 | 3, 7 (x16) after a shift by 8
+          const uint2 q0 = qop(1, 2 * ii), q1 = qop(1, 2 * ii + 1);
+          mma_f16_16816(sa, xa[ii] & 0x000F000Fu, xb[ii] & 0x000F000Fu, xa[ii] & 0x00F000F0u, xb[ii] & 0x00F000F0u,
+                        q0.x, q0.y);
+          const uint32_t ta = xa[ii] >> 8, tb = xb[ii] >> 8;
+          mma_f16_16816(sb, ta & 0x000F000Fu, tb & 0x000F000Fu, ta & 0x00F000F0u, tb & 0x00F000F0u, q1.x, q1.y);
         }
       } else {
         const int sw = (n >> 2) & 1;  // rows n and n + 8 share the 32-byte swizzle phase
-        const uint2 va = lds_v2(sK + n * 32 + ((((c >> 1) ^ sw)) << 4) + 8 * (c & 1));
-        const uint2 vb = lds_v2(sK + (n + 8) * 32 + ((((c >> 1) ^ sw)) << 4) + 8 * (c & 1));
-        ya[0] = va.x; ya[1] = va.y;
-        yb[0] = vb.x; yb[1] = vb.y;
-        if (sgn) {
-          ya[0] ^= 0xAAAAAAAAu; ya[1] ^= 0xAAAAAAAAu;
-          yb[0] ^= 0xAAAAAAAAu; yb[1] ^= 0xAAAAAAAAu;
-        }
+        const uint2 va = lds_v2(sK + n * 32 + (((c >> 1) ^ sw) << 4) + 8 * (c & 1));
+        const uint2 vb = lds_v2(sK + (n + 8) * 32 + (((c >> 1) ^ sw) << 4) + 8 * (c & 1));
+        const uint32_t flip = sgn ? 0xAAAAAAAAu : 0u;
+        const uint32_t za[2] = {va.x ^ flip, va.y ^ flip}, zb[2] = {vb.x ^ flip, vb.y ^ flip};
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const int ii = kk >> 1, h = kk & 1;
-          // block ii: 16 bits of word ii / 2, spread to one byte per 16-bit half
-          const uint32_t sel = (ii & 1) ? 0x4342u : 0x4140u;
-          const uint32_t ua = prmt(ya[ii >> 1], 0u, sel), ub = prmt(yb[ii >> 1], 0u, sel);
-          const uint32_t a0 = (ua >> (4 * h)) & 0x00030003u, a1 = (ub >> (4 * h)) & 0x00030003u;
-          const uint32_t a2 = (ua >> (4 * h + 2)) & 0x00030003u, a3 = (ub >> (4 * h + 2)) & 0x00030003u;
-          mma_f16_16816(s, a0, a1, a2, a3, qc[kk][0], qc[kk][1]);
+        for (int wv = 0; wv < 2; ++wv) {
+          // code pairs (j, j + 8) of the word: j < 5 masked in place (bit 2j), j >= 5 after a shift by 10
+          const uint32_t ta = za[wv] >> 10, tb = zb[wv] >> 10;
+#pragma unroll
+          for (int k2 = 0; k2 < 4; ++k2) {
+            const int j0 = 2 * k2, j1 = j0 + 1;
+            const uint32_t m0 = 0x00030003u << (2 * (j0 < 5 ? j0 : j0 - 5));
+            const uint32_t m1 = 0x00030003u << (2 * (j1 < 5 ? j1 : j1 - 5));
+            const uint32_t a0 = (j0 < 5 ? za[wv] : ta) & m0, a1 = (j0 < 5 ? zb[wv] : tb) & m0;
+            const uint32_t a2 = (j1 < 5 ? za[wv] : ta) & m1, a3 = (j1 < 5 ? zb[wv] : tb) & m1;
+            const uint2 q = qop(3, 4 * wv + k2);
+            mma_f16_16816((k2 & 1) ? sb : sa, a0, a1, a2, a3, q.x, q.y);
+          }
         }
       }
-      kmul0 = ldexpf(ks * sl2, 24 - e0);
-      kmul1 = ldexpf(ks * sl2, 24 - e1);
+      kmul0 = ks * sl2 * pow2f(24 - e0);
+      kmul1 = ks * sl2 * pow2f(24 - e1);
       kb0 = ks * sl2 * (float)kz * qs0;
       kb1 = ks * sl2 * (float)kz * qs1;
     }
 
     // ---- online softmax on the S^T columns (exp2 domain)
-    const int ta = t0 + n, tb = ta + 8;
-    const bool va_ = ta >= w.lo && ta < tend, vb_ = tb >= w.lo && tb < tend;
-    const float s00 = va_ ? fmaf(s[0], kmul0, -kb0) : -INFINITY;
-    const float s01 = va_ ? fmaf(s[1], kmul1, -kb1) : -INFINITY;
-    const float s10 = vb_ ? fmaf(s[2], kmul0, -kb0) : -INFINITY;
-    const float s11 = vb_ ? fmaf(s[3], kmul1, -kb1) : -INFINITY;
+    const int ta_ = t0 + n, tb_ = ta_ + 8;
+    const bool va_ = ta_ >= w.lo && ta_ < tend, vb_ = tb_ >= w.lo && tb_ < tend;
+    const float s00 = va_ ? fmaf(sa[0] + sb[0], kmul0, -kb0) : -INFINITY;
+    const float s01 = va_ ? fmaf(sa[1] + sb[1], kmul1, -kb1) : -INFINITY;
+    const float s10 = vb_ ? fmaf(sa[2] + sb[2], kmul0, -kb0) : -INFINITY;
+    const float s11 = vb_ ? fmaf(sa[3] + sb[3], kmul1, -kb1) : -INFINITY;
     float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
@@ -445,118 +540,114 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
     const float p10 = fast_exp2(s10 - b0), p11 = fast_exp2(s11 - b1);
     l_run0 = l_run0 * al0 + (p00 + p10);
     l_run1 = l_run1 * al1 + (p01 + p11);
-    if (__any_sync(0xffffffffu, mn0 != m_run0 || mn1 != m_run1)) {
+    // the V scale exponent of this tile (affine formats; dense: 0): O is held in its units
+    int kv = 0;
+    float mv = 1.f;
+    if (fmt_affine(fv)) {
+      kv = log2_floor(vs);
+      mv = vs * pow2f(-kv);
+    }
+    const bool moved = __any_sync(0xffffffffu, mn0 != m_run0 || mn1 != m_run1);
+    if (moved || kv != ko) {
+      const float f = pow2f(ko - kv);
+      const float r0 = al0 * f, r1 = al1 * f;
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
-        o[mt][0] *= al0;
-        o[mt][1] *= al1;
-        o[mt][2] *= al0;
-        o[mt][3] *= al1;
+        o[mt][0] *= r0;
+        o[mt][1] *= r1;
+        o[mt][2] *= r0;
+        o[mt][3] *= r1;
       }
+      ko = kv;
     }
     m_run0 = mn0;
     m_run1 = mn1;
 
     // ---- O^T += V^T P^T (dimension order: m-tile 2bb + hh, row n -> 32bb + 4n + 2hh, row n + 8 -> + 1)
     const int TA = 2 * c, TB = 2 * c + 1, TC = 2 * c + 8, TD = 2 * c + 9;  // this lane's tokens (k rows)
-    if (fv == OL_FMT_BF16 || fv == OL_FMT_F16 || fv == OL_FMT_F32) {
-      const bool h16 = fv == OL_FMT_F16;
-      uint32_t ph0, ph1, pl0, pl1;
-      {
-        uint32_t h0, l0, h1, l1;
-        if (h16) {
-          split_f16(p00, p01, h0, l0);
-          split_f16(p10, p11, h1, l1);
-        } else {
-          split_bf16(p00, p01, h0, l0);
-          split_bf16(p10, p11, h1, l1);
-        }
-        ph0 = movmatrix_trans(h0);
-        ph1 = movmatrix_trans(h1);
-        pl0 = movmatrix_trans(l0);
-        pl1 = movmatrix_trans(l1);
-      }
-      if (fv == OL_FMT_F32) {
-        // V from global memory; rows at or past the history end count as zero
-        const int vrow[4] = {TA, TB, TC, TD};
-#pragma unroll
-        for (int bb = 0; bb < 4; ++bb) {
-          float4 x[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            x[k] = vrow[k] < vhi ? *reinterpret_cast<const float4*>(gV + (size_t)vrow[k] * 512 +
-                                                                    (32 * bb + 4 * n) * 4)
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const float xa0 = hh ? x[0].z : x[0].x, xa1 = hh ? x[0].w : x[0].y;
-            const float xb0 = hh ? x[1].z : x[1].x, xb1 = hh ? x[1].w : x[1].y;
-            const float xc0 = hh ? x[2].z : x[2].x, xc1 = hh ? x[2].w : x[2].y;
-            const float xd0 = hh ? x[3].z : x[3].x, xd1 = hh ? x[3].w : x[3].y;
-            uint32_t a0h, a0l, a1h, a1l, a2h, a2l, a3h, a3l;
-            split_bf16(xa0, xb0, a0h, a0l);
-            split_bf16(xa1, xb1, a1h, a1l);
-            split_bf16(xc0, xd0, a2h, a2l);
-            split_bf16(xc1, xd1, a3h, a3l);
-            mma_bf16_16816(o[2 * bb + hh], a0h, a1h, a2h, a3h, ph0, ph1);
-            mma_bf16_16816(o[2 * bb + hh], a0h, a1h, a2h, a3h, pl0, pl1);
-            mma_bf16_16816(o[2 * bb + hh], a0l, a1l, a2l, a3l, ph0, ph1);
-          }
-        }
+    const bool half_p = fv != OL_FMT_BF16 && fv != OL_FMT_F32;  // P^T in fp16 (else bf16)
+    uint32_t ph0, ph1, pl0, pl1;
+    {
+      uint32_t h0, l0, h1, l1;
+      if (half_p) {
+        split_f16(p00 * mv, p01 * mv, h0, l0);
+        split_f16(p10 * mv, p11 * mv, h1, l1);
       } else {
+        split_bf16(p00, p01, h0, l0);
+        split_bf16(p10, p11, h1, l1);
+      }
+      ph0 = movmatrix_trans(h0);
+      ph1 = movmatrix_trans(h1);
+      pl0 = movmatrix_trans(l0);
+      pl1 = movmatrix_trans(l1);
+    }
+    if (fv == OL_FMT_F32) {
+      // V from global memory; rows at or past the history end count as zero
+      const int vrow[4] = {TA, TB, TC, TD};
 #pragma unroll
-        for (int bb = 0; bb < 4; ++bb) {
-          // 8 bytes (dims 32bb + 4n .. + 3) of each of the four token rows
-          const int e = 32 * (bb & 1) + 4 * n;  // element within the 64-dim half
-          const int ch = e >> 3, sub = (e & 7) * 2;
-          const uint32_t hb = sV + (bb >> 1) * kHalf + sub;
-          const uint2 wa = lds_v2(hb + TA * 128 + ((ch ^ (TA & 7)) << 4));
-          const uint2 wb = lds_v2(hb + TB * 128 + ((ch ^ (TB & 7)) << 4));
-          const uint2 wc = lds_v2(hb + TC * 128 + ((ch ^ (TC & 7)) << 4));
-          const uint2 wd = lds_v2(hb + TD * 128 + ((ch ^ (TD & 7)) << 4));
+      for (int bb = 0; bb < 4; ++bb) {
+        float4 x[4];
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const uint32_t xa = hh ? wa.y : wa.x, xb = hh ? wb.y : wb.x;
-            const uint32_t xc = hh ? wc.y : wc.x, xd = hh ? wd.y : wd.x;
-            const uint32_t a0 = prmt(xa, xb, 0x5410u), a1 = prmt(xa, xb, 0x7632u);
-            const uint32_t a2 = prmt(xc, xd, 0x5410u), a3 = prmt(xc, xd, 0x7632u);
-            if (h16) {
-              mma_f16_16816(o[2 * bb + hh], a0, a1, a2, a3, ph0, ph1);
-              mma_f16_16816(o[2 * bb + hh], a0, a1, a2, a3, pl0, pl1);
-            } else {
-              mma_bf16_16816(o[2 * bb + hh], a0, a1, a2, a3, ph0, ph1);
-              mma_bf16_16816(o[2 * bb + hh], a0, a1, a2, a3, pl0, pl1);
-            }
+        for (int k = 0; k < 4; ++k) {
+          x[k] = ldg_f4(reinterpret_cast<const float*>(gV + (size_t)vrow[k] * 512) + 32 * bb + 4 * n);
+          if (vrow[k] >= vhi) x[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const float xa0 = hh ? x[0].z : x[0].x, xa1 = hh ? x[0].w : x[0].y;
+          const float xb0 = hh ? x[1].z : x[1].x, xb1 = hh ? x[1].w : x[1].y;
+          const float xc0 = hh ? x[2].z : x[2].x, xc1 = hh ? x[2].w : x[2].y;
+          const float xd0 = hh ? x[3].z : x[3].x, xd1 = hh ? x[3].w : x[3].y;
+          uint32_t a0h, a0l, a1h, a1l, a2h, a2l, a3h, a3l;
+          split_bf16(xa0, xb0, a0h, a0l);
+          split_bf16(xa1, xb1, a1h, a1l);
+          split_bf16(xc0, xd0, a2h, a2l);
+          split_bf16(xc1, xd1, a3h, a3l);
+          mma_bf16_16816(o[2 * bb + hh], a0h, a1h, a2h, a3h, ph0, ph1);
+          mma_bf16_16816(o[2 * bb + hh], a0h, a1h, a2h, a3h, pl0, pl1);
+          mma_bf16_16816(o[2 * bb + hh], a0l, a1l, a2l, a3l, ph0, ph1);
+        }
+      }
+    } else if (fv == OL_FMT_BF16 || fv == OL_FMT_F16) {
+      const bool h16 = fv == OL_FMT_F16;
+#pragma unroll
+      for (int bb = 0; bb < 4; ++bb) {
+        // 8 bytes (dims 32bb + 4n .. + 3) of each of the four token rows
+        const int e = 32 * (bb & 1) + 4 * n;  // element within the 64-dim half
+        const int ch = e >> 3, sub = (e & 7) * 2;
+        const uint32_t hb = sV + (bb >> 1) * kHalf + sub;
+        const uint2 wa = lds_v2(hb + TA * 128 + ((ch ^ (TA & 7)) << 4));
+        const uint2 wb = lds_v2(hb + TB * 128 + ((ch ^ (TB & 7)) << 4));
+        const uint2 wc = lds_v2(hb + TC * 128 + ((ch ^ (TC & 7)) << 4));
+        const uint2 wd = lds_v2(hb + TD * 128 + ((ch ^ (TD & 7)) << 4));
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const uint32_t xa = hh ? wa.y : wa.x, xb = hh ? wb.y : wb.x;
+          const uint32_t xc = hh ? wc.y : wc.x, xd = hh ? wd.y : wd.x;
+          const uint32_t a0 = prmt(xa, xb, 0x5410u), a1 = prmt(xa, xb, 0x7632u);
+          const uint32_t a2 = prmt(xc, xd, 0x5410u), a3 = prmt(xc, xd, 0x7632u);
+          if (h16) {
+            mma_f16_16816(o[2 * bb + hh], a0, a1, a2, a3, ph0, ph1);
+            mma_f16_16816(o[2 * bb + hh], a0, a1, a2, a3, pl0, pl1);
+          } else {
+            mma_bf16_16816(o[2 * bb + hh], a0, a1, a2, a3, ph0, ph1);
+            mma_bf16_16816(o[2 * bb + hh], a0, a1, a2, a3, pl0, pl1);
           }
         }
       }
     } else {
-      // affine codes: V^T as exact fp16 (1024 + c') - (1024 + zp'), P^T in fp16 hi + lo
-      uint32_t ph0, ph1, pl0, pl1;
-      {
-        uint32_t h0, l0, h1, l1;
-        split_f16(p00, p01, h0, l0);
-        split_f16(p10, p11, h1, l1);
-        ph0 = movmatrix_trans(h0);
-        ph1 = movmatrix_trans(h1);
-        pl0 = movmatrix_trans(l0);
-        pl1 = movmatrix_trans(l1);
-      }
+      // affine codes: V^T as exact fp16 (1024 + c') - (1024 + zp') against (P * m)^T
       const int bits = fmt_bits(fv);
       const bool sgn = fmt_signed(fv);
       const uint32_t zf = (uint32_t)__half_as_ushort(__int2half_rn(1024 + vz));
       const uint32_t zpair = zf | (zf << 16);
       auto add_tile = [&](int mt, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
-        float t4[4] = {0.f, 0.f, 0.f, 0.f};
         a0 = hsub2_f16(a0, zpair);
         a1 = hsub2_f16(a1, zpair);
         a2 = hsub2_f16(a2, zpair);
         a3 = hsub2_f16(a3, zpair);
-        mma_f16_16816(t4, a0, a1, a2, a3, ph0, ph1);
-        mma_f16_16816(t4, a0, a1, a2, a3, pl0, pl1);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) o[mt][j] = fmaf(t4[j], vs, o[mt][j]);
+        mma_f16_16816(o[mt], a0, a1, a2, a3, ph0, ph1);
+        mma_f16_16816(o[mt], a0, a1, a2, a3, pl0, pl1);
       };
       if (bits == 8) {
         const uint32_t magic = sgn ? 0x64806480u : 0x64006400u;
@@ -615,11 +706,16 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
       }
     }
     __syncwarp();
-    if (lane == 0 && i + STAGES < my_n) {
-      fence_proxy_async_smem();  // generic writes to this stage (zeroed rows) before the async-proxy refill
-      issue(i + STAGES);
-    }
+    if (i + STAGES < my_n) issue(i + STAGES);
     __syncwarp();
+  }
+
+  if (ko != 0) {
+    const float f = pow2f(ko);
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o[mt][j] *= f;
   }
 
   // ---- the current token, uncompressed from new_kv, in warp 0's state; the
@@ -726,7 +822,7 @@ bool encode_width(CUtensorMap* map, void* base, uint64_t pool_bytes, int width) 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr int kWarps = 4, kStages = 3;
+constexpr int kWarps = 6, kStages = 2;
 
 cudaError_t ensure_attrs() {
   static cudaError_t state = cudaFuncSetAttribute(fast_hpaged_kernel<kWarps, kStages>,
