@@ -412,12 +412,16 @@ OL_API ol_status ol_hpaged_quantize(const ol_hpaged_kv* cache, void* updated, co
  * q [batch, q_heads, new_len, head_dim] attend positions
  * [max(0, pos_i - window), pos_i] with pos_i = lens[b] - new_len + i
  * (window < 0: [0, pos_i]) into out [batch, q_heads, new_len, head_dim].
- * new_len = 1 is ol_decode_step. Contiguous and paged caches;
- * OL_LAYOUT_INT4 returns OL_ERR_UNSUPPORTED. Requires
- * new_len <= lens[b] <= capacity and ws_bytes >=
+ * new_len = 1 is ol_decode_step. Contiguous, paged and INT4 caches (not the
+ * heterogeneous pool: OL_ERR_UNSUPPORTED). INT4: the chunk's tokens take
+ * part uncompressed from new_kv (bf16) and are quantized into the cache only
+ * after the attention (the same section: current K/V are attended as
+ * uncompressed values and encoded afterwards); history comes from the codes.
+ * Requires new_len <= lens[b] <= capacity and ws_bytes >=
  * ol_workspace_size_chunk(batch, q_heads, kv_heads, head_dim, new_len).
- * Two launches on `stream` (the append, then one attention launch whose
- * grid slice z serves query token z); every check runs before the first.
+ * Two launches on `stream` (contiguous and paged: the append, then one
+ * attention launch whose grid slice z serves query token z; INT4: the
+ * attention, then the append); every check runs before the first.
  */
 OL_API size_t ol_workspace_size_chunk(int32_t batch, int32_t q_heads, int32_t kv_heads, int32_t head_dim,
                                       int32_t new_len);

@@ -257,6 +257,35 @@ def int4_attention(q, codes, scales, zps, lens, cur_kv=None, scale: Optional[flo
     return out
 
 
+def int4_chunk_attention(q, codes, scales, zps, lens, new_len: int, new_kv, scale: Optional[float] = None,
+                         window: int = -1) -> np.ndarray:
+    """Chunked step over the INT4 cache: query token i of row b sits at
+    p_i = lens[b] - new_len + i and attends its causal, windowed range; the
+    history [0, lens[b] - new_len) is read from the codes (decoded), the
+    chunk's own tokens take part uncompressed from new_kv (page "Persistent
+    input/output feedback", Optional heterogeneous paged KV: current K/V are
+    attended as uncompressed values and encoded only afterwards).
+    q [B, Hq, new_len, D] bf16 bits; new_kv [2, B, Hkv, new_len, D] bf16 bits
+    -> y [B, Hq, new_len, D] fp64. Built as the pinned chunk_attention over a
+    float32 cache holding exactly those values (each decoded value (c - zp) *
+    scale is exact in float32)."""
+    codes, scales, zps, lens = _c(codes), _c(scales), _c(zps), _c(lens, np.int32)
+    new_kv = _c(new_kv, np.uint16)
+    _, B, H, C, _cb = codes.shape
+    D = new_kv.shape[4]
+    dense = np.full((2, B, H, C, D), np.nan, np.float32)
+    for b in range(B):
+        hist = int(lens[b]) - new_len
+        for plane in range(2):
+            for h in range(H):
+                for t in range(hist):
+                    dense[plane, b, h, t] = int4_dequantize_row(codes[plane, b, h, t], scales[plane, b, h, t],
+                                                                zps[plane, b, h, t])
+                bits = new_kv[plane, b, h].astype(np.uint32) << 16
+                dense[plane, b, h, hist:hist + new_len] = bits.view(np.float32)
+    return chunk_attention(q, dense, lens, new_len, scale=scale, window=window)
+
+
 def fp16_to_float(bits: int) -> float:
     return float(lib().orc_fp16_to_double(int(bits)))
 

@@ -548,7 +548,9 @@ void record_attention(const CacheView& v, const int32_t* lens_host, int window, 
       const RowSplit rs = row_split(lens_host[b] - (nq - 1 - z), window < 0 ? -1 : window, 16);
       const int vis = rs.hi - rs.lo;
       visible += vis;
-      hist += (cur_from_new && vis > 0) ? vis - 1 : vis;
+      // tokens taken from new_kv instead of the cache: the chunk's first z + 1
+      const int fresh = cur_from_new ? std::min(z + 1, vis) : 0;
+      hist += vis - fresh;
     }
   s.attended_tokens = visible * v.kv_heads;
   s.kv_payload_bytes_read = 2 * hist * v.kv_heads * token_payload(v);
@@ -617,7 +619,7 @@ ol_status run_attention(int layout, const void* desc, const CacheView& v, const 
   const size_t in_elt = v.layout == OL_LAYOUT_INT4 ? 2 : elt_bytes(v.dtype);
   const size_t q_bytes = (size_t)v.batch * q_heads * nq * D * in_elt;
   const size_t out_bytes = (size_t)v.batch * q_heads * nq * D * elt_bytes(out_dtype);
-  const size_t kv_bytes = 2ull * v.batch * v.kv_heads * D * in_elt;
+  const size_t kv_bytes = 2ull * v.batch * v.kv_heads * nq * D * in_elt;
   const size_t need = workspace_bytes(v.batch, q_heads, v.kv_heads, D, nq);
   if (ws_bytes < need) return OL_ERR_WORKSPACE;
   ol_status st;
@@ -1022,7 +1024,8 @@ ol_status ol_chunk_step(int32_t layout, const void* cache_desc, void* updated, c
   CacheView v;
   ol_status st = view_of(layout, cache_desc, v);
   if (st != OL_OK) return st;
-  if (layout == OL_LAYOUT_INT4) return OL_ERR_UNSUPPORTED;
+  // INT4: the chunk's tokens are attended uncompressed from new_kv, then encoded
+  const bool int4 = layout == OL_LAYOUT_INT4;
   if (new_len < 1) return OL_ERR_SHAPE;
   if (!lens_host) return OL_ERR_NULL;
   // the append writes positions lens - new_len .. lens - 1 of every row
@@ -1039,8 +1042,8 @@ ol_status ol_chunk_step(int32_t layout, const void* cache_desc, void* updated, c
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // every check of the attention first: an error return means nothing was written
-  if ((st = run_attention(layout, cache_desc, v, q, q_heads, lens_host, lens_dev, nullptr, 0, 0, scale, window, out,
-                          out_dtype, workspace, ws_bytes, s, new_len, true)) != OL_OK)
+  if ((st = run_attention(layout, cache_desc, v, q, q_heads, lens_host, lens_dev, int4 ? new_kv : nullptr, 0,
+                          int4 ? 1 : 0, scale, window, out, out_dtype, workspace, ws_bytes, s, new_len, true)) != OL_OK)
     return st;
   const size_t in_elt = elt_bytes(v.dtype);
   if ((st = no_overlap(v, new_kv, 2ull * v.batch * v.kv_heads * new_len * v.head_dim * in_elt)) != OL_OK) return st;
@@ -1049,9 +1052,15 @@ ol_status ol_chunk_step(int32_t layout, const void* cache_desc, void* updated, c
     return OL_ERR_ALIAS;
   if ((st = check_owner(v.ranges, v.nranges, v.owner)) != OL_OK) return st;
   if (fault_injected()) return OL_ERR_INJECTED;
-  if ((st = launch_append_view(v, layout, cache_desc, new_kv, new_len, lens_dev, s, 1)) != OL_OK) return st;
-  st = run_attention(layout, cache_desc, v, q, q_heads, lens_host, lens_dev, nullptr, 0, 0, scale, window, out,
-                     out_dtype, workspace, ws_bytes, s, new_len);
+  if (int4) {
+    st = run_attention(layout, cache_desc, v, q, q_heads, lens_host, lens_dev, new_kv, 0, 1, scale, window, out,
+                       out_dtype, workspace, ws_bytes, s, new_len);
+    if (st == OL_OK) st = launch_append_view(v, layout, cache_desc, new_kv, new_len, lens_dev, s, 1);
+  } else {
+    if ((st = launch_append_view(v, layout, cache_desc, new_kv, new_len, lens_dev, s, 1)) != OL_OK) return st;
+    st = run_attention(layout, cache_desc, v, q, q_heads, lens_host, lens_dev, nullptr, 0, 0, scale, window, out,
+                       out_dtype, workspace, ws_bytes, s, new_len);
+  }
   // the call's one record: the attention's counts (recorded by run_attention) and the append's
   const int64_t appended = 2ll * v.batch * v.kv_heads * new_len * token_payload(v);
   for (ol_stats* r : {&t_last, &t_total}) {

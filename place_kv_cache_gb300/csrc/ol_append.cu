@@ -36,16 +36,18 @@ __global__ void copy_rows_kernel(const AppendParams p) {
   for (int d = threadIdx.x; d < D; d += blockDim.x) base[dst + d] = in[src + d];
 }
 
-// One warp per (plane, row, head): quantize the new token and store its INT4 row.
+// One warp per (plane, row, head, new token): quantize the token and store its INT4 row.
 __global__ void int4_append_kernel(const AppendParams p) {
-  const int h = blockIdx.x % p.kv_heads;
-  const int b = blockIdx.x / p.kv_heads;
+  const int j = blockIdx.x % p.new_len;
+  const int h = (blockIdx.x / p.new_len) % p.kv_heads;
+  const int b = blockIdx.x / (p.new_len * p.kv_heads);
   const int plane = blockIdx.y;
   const int D = p.head_dim;
-  const int pos = p.positions[b];
-  if (pos < 0 || pos >= p.capacity) return;  // device guard
-  const size_t row = (((size_t)plane * p.batch + b) * p.kv_heads + h) * p.capacity + pos;
-  const size_t src = (((size_t)plane * p.batch + b) * p.kv_heads + h) * D;
+  int pos = p.positions[b];
+  if (p.positions_are_lens) pos -= p.new_len;
+  if (pos < 0 || (long long)pos + p.new_len > p.capacity) return;  // device guard
+  const size_t row = (((size_t)plane * p.batch + b) * p.kv_heads + h) * p.capacity + pos + j;
+  const size_t src = ((((size_t)plane * p.batch + b) * p.kv_heads + h) * p.new_len + j) * D;
   int4_quantize_row_warp(reinterpret_cast<const uint16_t*>(p.values) + src, D, p.quant_mode, p.fixed_scale,
                          p.fixed_zp, p.codes + row * (D / 2), p.scales + row * (D / 32),
                          p.zps + row * (D / 64));
@@ -56,7 +58,7 @@ __global__ void int4_append_kernel(const AppendParams p) {
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s) {
   if (p.batch == 0 || p.new_len == 0) return cudaSuccess;
   if (p.layout == OL_LAYOUT_INT4) {
-    dim3 grid(p.batch * p.kv_heads, 2);
+    dim3 grid(p.batch * p.kv_heads * p.new_len, 2);
     int4_append_kernel<<<grid, 32, 0, s>>>(p);
     return cudaGetLastError();
   }

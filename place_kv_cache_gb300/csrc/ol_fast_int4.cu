@@ -569,7 +569,7 @@ cudaError_t launch_cfg(const AttnParams& p, cudaStream_t s) {
 }  // namespace
 
 bool fast_int4_supported(const AttnParams& p) {
-  if (p.layout != OL_LAYOUT_INT4 || p.head_dim != 128 || p.group > 8) return false;
+  if (p.layout != OL_LAYOUT_INT4 || p.head_dim != 128 || p.group > 8 || p.nq != 1) return false;
   // every (row, kv head) starts on a 16-token boundary, so a stage's scale
   // and zero-point boxes start on whole 16-byte rows of their maps
   if (p.capacity % 16 != 0) return false;

@@ -9,6 +9,8 @@
 // dimensions; per token the warp reduces q.k with shuffles and updates an
 // online-softmax state (m, l, o) per query head. Warps merge in shared memory
 // and the CTA finishes through the split-K ticket (finish_split).
+#include <climits>
+
 #include "ol_hpaged.cuh"
 
 namespace ol {
@@ -59,9 +61,10 @@ __device__ __forceinline__ float load_kv(const AttnParams& p, int plane, int b, 
   return static_cast<float>(code - zp) * s;
 }
 
-// The token being appended by a fused step, from new_kv [2, B, Hkv, 1, D].
-__device__ __forceinline__ float load_new(const AttnParams& p, int plane, int b, int g, int d) {
-  size_t idx = (((size_t)plane * p.batch + b) * p.kv_heads + g) * p.head_dim + d;
+// New token j of row b (the one a fused step appends, or token j of a chunk
+// whose tokens are attended uncompressed), from new_kv [2, B, Hkv, nq, D].
+__device__ __forceinline__ float load_new(const AttnParams& p, int plane, int b, int g, int j, int d) {
+  size_t idx = ((((size_t)plane * p.batch + b) * p.kv_heads + g) * (p.nq > 1 ? p.nq : 1) + j) * p.head_dim + d;
   if (p.dtype == OL_F32 && p.layout != OL_LAYOUT_INT4) return reinterpret_cast<const float*>(p.new_kv)[idx];
   return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(p.new_kv)[idx]);
 }
@@ -125,7 +128,7 @@ __device__ void append_token_warp(const AttnParams& p, int b, int g, int pos) {
 
 __global__ void __launch_bounds__(kGenWarps * 32) generic_attn_kernel(const __grid_constant__ AttnParams p) {
   __shared__ Work sw;
-  __shared__ int sm_flag;
+  __shared__ int sm_flag, sm_new_lo;
   __shared__ float sm_wm[kGenWarps][kGenHeads], sm_wl[kGenWarps][kGenHeads];
   __shared__ float sm_wo[kGenWarps][kGenHeads][256];
   __shared__ float sm_m[kGenHeads], sm_l[kGenHeads];
@@ -140,8 +143,12 @@ __global__ void __launch_bounds__(kGenWarps * 32) generic_attn_kernel(const __gr
                                           cta_index(p), nullptr)
                            : map_cta_warp(p.lens, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, cta_index(p),
                                           p.status);
+    const int row_hi = w.hi;  // the row's length: its new tokens are the last max(nq, 1)
     slice_query(w, p);
-    if (lane == 0) sw = w;
+    if (lane == 0) {
+      sw = w;
+      sm_new_lo = row_hi - (p.nq > 1 ? p.nq : 1);
+    }
   }
   __syncthreads();
   const Work w = sw;
@@ -152,7 +159,9 @@ __global__ void __launch_bounds__(kGenWarps * 32) generic_attn_kernel(const __gr
   const int heads_lo = head_block(p) * kGenHeads;
   const int heads_hi = min(G, heads_lo + kGenHeads);
   const int nh = heads_hi - heads_lo;
-  const int cur = p.cur_from_new ? w.hi - 1 : -1;
+  // tokens from new_lo on come from new_kv when cur_from_new (the decode step's
+  // current token, or every token of a chunk)
+  const int new_lo = p.cur_from_new ? sm_new_lo : INT_MAX;
 
   float q[kGenHeads][kMaxDpl];
   float m[kGenHeads], l[kGenHeads], o[kGenHeads][kMaxDpl];
@@ -185,9 +194,9 @@ __global__ void __launch_bounds__(kGenWarps * 32) generic_attn_kernel(const __gr
       k[i] = 0.f;
       v[i] = 0.f;
       if (d < D) {
-        if (t == cur) {
-          k[i] = load_new(p, 0, w.b, w.g, d);
-          v[i] = load_new(p, 1, w.b, w.g, d);
+        if (t >= new_lo) {
+          k[i] = load_new(p, 0, w.b, w.g, t - new_lo, d);
+          v[i] = load_new(p, 1, w.b, w.g, t - new_lo, d);
         } else {
           k[i] = load_kv(p, 0, w.b, w.g, t, d);
           v[i] = load_kv(p, 1, w.b, w.g, t, d);

@@ -296,5 +296,6 @@ def test_chunk_step_validation():
     assert status_of(chunk, new_len=0) == ol.OL_ERR_SHAPE
     assert status_of(chunk, ws_bytes=ol.ol_workspace_size(B, HQ, HKV, D)) == ol.OL_ERR_WORKSPACE
     assert status_of(chunk, updated=CACHE + 256) == ol.OL_ERR_ALIAS
-    assert status_of(chunk, desc=int4_desc(), updated=CODES, layout=ol.OL_LAYOUT_INT4) == ol.OL_ERR_UNSUPPORTED
+    assert status_of(chunk, desc=int4_desc(), updated=CODES, layout=ol.OL_LAYOUT_INT4) == ol.OL_ERR_INJECTED
+    assert status_of(chunk, desc=int4_desc(), updated=SCALES, layout=ol.OL_LAYOUT_INT4) == ol.OL_ERR_ALIAS
     assert ol.ol_workspace_size_chunk(B, HQ, HKV, D, 4) > ol.ol_workspace_size(B, HQ, HKV, D)

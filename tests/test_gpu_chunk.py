@@ -3,7 +3,9 @@ row and attended causally inside the chunk, against the oracle (cache bytes
 bit-exact, outputs within 2e-3). Covers the tensor-core kernel (head_dim 128,
 GQA <= 8) and the CUDA-core kernel (fp32, head_dim 64, GQA 16), contiguous and
 paged caches, chunk lengths 1..8, rows whose chunk is the whole row, finite
-windows, and the chunk of one token against the decode step."""
+windows, and the chunk of one token against the decode step. INT4 caches: the
+chunk attended uncompressed and quantized afterwards, codes / scales / zero
+points bit-exact against the oracle's append."""
 import zlib
 
 import numpy as np
@@ -125,3 +127,40 @@ def test_chunk_of_one_token_is_the_decode_step():
     # the decode step attends its new token from new_kv, the chunk from the cache it just
     # wrote: the same bf16 values, so the results agree to rounding
     assert np.abs(outs[0][1] - outs[1][1]).max() <= 1e-5
+
+
+INT4 = [
+    # name, B, Hq, Hkv, D, C, lens, T, quant mode
+    ("int4_gqa4_t4", 3, 16, 4, 128, 96, [4, 37, 96], 4, ol.OL_Q_DYNAMIC),
+    ("int4_gqa7_t2_fixed", 1, 28, 4, 128, 64, [50], 2, ol.OL_Q_FIXED),
+    ("int4_d64_t8", 2, 8, 2, 64, 48, [8, 48], 8, ol.OL_Q_DYNAMIC),
+]
+
+
+@pytest.mark.parametrize("window", [-1, 0, 9])
+@pytest.mark.parametrize("shape", INT4, ids=lambda s: s[0])
+def test_chunk_step_int4(shape, window):
+    name, B, Hq, Hkv, D, C, lens, T, mode = shape
+    w = Workload(name, "bf16", B, Hq, Hkv, D, C, "int4", seed=zlib.crc32(name.encode()) % 1000)
+    case, q, kv = chunk_inputs(w, lens, T, seed=52)
+    qm = dict(mode=O.Q_FIXED if mode == ol.OL_Q_FIXED else O.Q_DYNAMIC)
+    planes = O.int4_planes(B, Hkv, C, D)
+    for b, h in enumerate(case.history):
+        if h.shape[2]:
+            sub = O.int4_planes(1, Hkv, C, D)
+            O.int4_append(*sub, h[:, None], [0], **qm)
+            for full, part in zip(planes, sub):
+                full[:, b] = part[:, 0]
+    dev = [to_dev(a) for a in planes]
+    desc = ol.int4_kv(dev[0], dev[1].view(torch.int16), dev[2], head_dim=D, quant_mode=mode)
+    ws, n = ws_for(w, T)
+    out = out_for(w, T, ol.OL_F32)
+    ol.ol_chunk_step(ol.OL_LAYOUT_INT4, desc, dev[0], to_dev(q), Hq, T, to_dev(kv), case.lens, to_dev(case.lens), 0.0,
+                     window, out, ol.OL_F32, ws, n)
+    torch.cuda.synchronize()
+    assert ol.ol_workspace_status(ws) == ol.OL_DEVICE_OK
+    want = O.int4_chunk_attention(q, *planes, case.lens, T, kv, window=window)
+    assert max_abs_err(out_as_f64(out), want) <= TOL
+    O.int4_append(*planes, kv, case.lens - T, **qm)
+    for got, ref in zip(dev, planes):
+        np.testing.assert_array_equal(to_host(got).view(ref.dtype), ref)

@@ -465,6 +465,50 @@ def test_int4_current_token_is_attended_uncompressed():
     np.testing.assert_array_equal(y0[0, 0], bf16_to_f32(cur[1, 0, 0, 0]).astype(np.float64))
 
 
+def test_int4_chunk_of_one_token_is_the_decode_step():
+    # a chunk of one token is the decode step with the current token uncompressed
+    rng = np.random.default_rng(19)
+    B, Hkv, Hq, C, D = 2, 2, 6, 16, 64
+    lens = np.array([9, 1], np.int32)
+    codes, scales, zps = O.int4_planes(B, Hkv, C, D)
+    hist = bf16_from_f32(rng.standard_normal((2, B, Hkv, 8, D)).astype(np.float32))
+    O.int4_append(codes, scales, zps, hist, [0, 0])
+    cur = bf16_from_f32(rng.standard_normal((2, B, Hkv, 1, D)).astype(np.float32))
+    q = bf16_from_f32(rng.standard_normal((B, Hq, D)).astype(np.float32))
+    for w in (-1, 0, 3):
+        y = O.int4_chunk_attention(q[:, :, None, :], codes, scales, zps, lens, 1, cur, window=w)
+        np.testing.assert_array_equal(y[:, :, 0], O.int4_attention(q, codes, scales, zps, lens, cur_kv=cur,
+                                                                      window=w))
+
+
+def test_int4_chunk_reads_history_from_codes_and_the_chunk_uncompressed():
+    # chunk values on the fixed-parameter grid ((k - 8) * 0.25) survive quantization
+    # exactly, so attending them uncompressed must equal quantizing the chunk first
+    # and attending every token from the codes, one query token at a time
+    rng = np.random.default_rng(20)
+    B, Hkv, Hq, C, D, T = 2, 2, 4, 20, 64, 4
+    lens = np.array([12, 4], np.int32)
+    mode = dict(mode=O.Q_FIXED, fixed_scale=0.25, fixed_zp=8)
+    codes, scales, zps = O.int4_planes(B, Hkv, C, D)
+    hist = bf16_from_f32(rng.standard_normal((2, B, Hkv, 8, D)).astype(np.float32))
+    O.int4_append(codes, scales, zps, hist, [0, 0], **mode)
+    grid = ((rng.integers(0, 16, (2, B, Hkv, T, D)) - 8) * 0.25).astype(np.float32)
+    chunk = bf16_from_f32(grid)
+    q = bf16_from_f32(rng.standard_normal((B, Hq, T, D)).astype(np.float32))
+    for w in (-1, 2):
+        y = O.int4_chunk_attention(q, codes, scales, zps, lens, T, chunk, window=w)
+        after = [a.copy() for a in (codes, scales, zps)]
+        O.int4_append(*after, chunk, lens - T, **mode)
+        for i in range(T):
+            yi = O.int4_attention(np.ascontiguousarray(q[:, :, i]), *after, lens - T + i + 1, window=w)
+            np.testing.assert_allclose(y[:, :, i], yi, rtol=0, atol=1e-12)
+    # query token 0 of the chunk does not see the chunk's later tokens
+    moved = chunk.copy()
+    moved[:, :, :, 1:] = bf16_from_f32(rng.standard_normal((2, B, Hkv, T - 1, D)).astype(np.float32))
+    y0 = O.int4_chunk_attention(q, codes, scales, zps, lens, T, chunk)[:, :, 0]
+    np.testing.assert_array_equal(O.int4_chunk_attention(q, codes, scales, zps, lens, T, moved)[:, :, 0], y0)
+
+
 def test_four_step_fixture_tolerance():
     # page "Persistent input/output feedback", tolerance table: Q/K/V components +/-(0.173*step),
     # UINT4 scale 0.25 / zero point 8, four steps; quantized attention within 0.15 of the
