@@ -435,16 +435,27 @@ def run_ours(args, rank, world, dist):
             dist.barrier()
         stream.synchronize()
         clk.mark_start()
+        # one event between consecutive graphs (recorded on the same stream, no
+        # synchronization between them): per-graph step times for the spread
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(n_graphs - 1)]
         with torch.cuda.stream(stream):
             e0.record(stream)
-            for _ in range(n_graphs):
+            for k in range(n_graphs):
                 g.replay()
+                if k < n_graphs - 1:
+                    marks[k].record(stream)
             e1.record(stream)
         stream.synchronize()
         clk.mark_end()
         if dist is not None:
             dist.barrier()
     ms = e0.elapsed_time(e1)
+    bounds = [e0] + marks + [e1]
+    per_graph_us = sorted(bounds[k].elapsed_time(bounds[k + 1]) * 1e3 / per_graph for k in range(n_graphs))
+    spread = {"graphs": n_graphs,
+              "p10": round(float(np.percentile(per_graph_us, 10)), 3),
+              "median": round(float(np.percentile(per_graph_us, 50)), 3),
+              "p90": round(float(np.percentile(per_graph_us, 90)), 3)}
     ms_per_step, gbs = combine_ranks(ms, K, s.bytes_per_step, world, dist, device=dev)
     status = ol.ol_workspace_status(s.ws, stream=stream)
     peak, peak_src = measured_peaks()
@@ -453,6 +464,7 @@ def run_ours(args, rank, world, dist):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": {"int4": "u4+bf16", "hpaged": "bf16+i8+i4/u4 pages, f32 math"}.get(w.layout, "bf16"), "data": "synthetic",
         "us_per_step": round(ms_per_step * 1e3, 3),
+        "us_per_step_spread": dict(spread, note=f"per graph of {per_graph} steps, rank {rank}"),
         "rows_tok_per_s": round(w.batch * world / (ms_per_step * 1e-3), 1),
         "pct_of_hbm_roofline": round(100.0 * gbs / world / peak, 2),
         "config": {"workload": w.name, "layout": w.layout, "batch": w.batch, "q_heads": w.q_heads,
