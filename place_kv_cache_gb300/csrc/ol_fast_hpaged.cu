@@ -48,6 +48,7 @@ constexpr int kRegion = 4096;         // one plane of a tile in a stage: 16 rows
 constexpr int kStage = 2 * kRegion;   // K region, V region
 constexpr int kHalf = 2048;           // a 16-bit tile's second 64-dimension half
 constexpr int kInfo = 8;              // ints of tile information per stage
+constexpr float kLazy = 8.f;          // log2 headroom of the lazy softmax maximum
 
 template <int NWARPS, int STAGES>
 struct HpLayout {
@@ -226,10 +227,17 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
   const uint64_t pol = policy_evict_first();
   const ol_page_format* __restrict__ fmts = p.page_fmt;
 
-  // Look-ahead: lane j holds the page and formats of the warp's tile la_base + j,
-  // so one round of dependent lookups (block table, then format table) serves
-  // 32 tiles instead of stalling the issuing lane on every tile.
-  int la_base = -64, la_page = 0, la_kf = 0, la_ks = 0, la_kz = 0, la_vf = 0, la_vs = 0, la_vz = 0;
+  // Look-ahead: lane j holds what the warp needs of its tile la_base + j, so one
+  // round of dependent lookups (block table, then format table) serves 32
+  // tiles, and the per-tile constants are computed once, 32 tiles at a time:
+  //   page, the tile's TMA rows of K and V (-1: a FLOAT plane),
+  //   w0 = K format | V format << 4 | (V scale exponent + 256) << 8 | V zero point' << 18,
+  //   kbase: S scale (exp2 domain; codes: K scale * 2^24, FLOAT16: 1; times 2^-e per column after),
+  //   kbias: K scale * zero point' (exp2 domain; times sum(q) per column after),
+  //   mv: the V scale's mantissa in [1, 2) (dense: 1).
+  const float sl2 = p.scale_log2;
+  int la_base = -64, la_page = 0, la_w0 = 0, la_rowk = 0, la_rowv = 0;
+  float la_kbase = 0.f, la_kbias = 0.f, la_mv = 1.f;
   auto look_ahead = [&](int base) {  // whole warp
     la_base = base;
     const int ti = base + lane;
@@ -240,50 +248,60 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
         set_status(p.status, OL_DEVICE_GUARD);
         page = 0;
       }
-      const int* f = reinterpret_cast<const int*>(fmts + page);
+      const ol_plane_format fk_ = fmts[page].k, fv_ = fmts[page].v;
+      const int fk = min(max(fk_.format, 0), (int)OL_FMT_U2), fv = min(max(fv_.format, 0), (int)OL_FMT_U2);
+      const int s0 = t0 % p.page_size;
+      int kv = 0, vz = 0;
+      float mv = 1.f;
+      if (fmt_affine(fv)) {
+        kv = log2_floor(fv_.scale);
+        mv = fv_.scale * pow2f(-kv);
+        vz = fv_.zero_point + code_offset(fv);
+      }
       la_page = page;
-      la_kf = f[0];
-      la_ks = f[1];
-      la_kz = f[2];
-      la_vf = f[3];
-      la_vs = f[4];
-      la_vz = f[5];
+      la_w0 = fk | fv << 4 | (kv + 256) << 8 | vz << 18;
+      la_rowk = fk == OL_FMT_F32 ? -1 : map_row(p, page, 0, w.g, s0, fk);
+      la_rowv = fv == OL_FMT_F32 ? -1 : map_row(p, page, 1, w.g, s0, fv);
+      if (fmt_affine(fk)) {
+        la_kbase = fk_.scale * sl2 * 16777216.f;
+        la_kbias = fk_.scale * sl2 * (float)(fk_.zero_point + code_offset(fk));
+      } else {
+        la_kbase = sl2;
+        la_kbias = 0.f;
+      }
+      la_mv = mv;
     }
   };
-  // whole warp: tile i's page and formats from the look-ahead; lane 0 records
-  // them for the compute phase and requests the tile's bytes
+  // whole warp: tile i's constants from the look-ahead; lane 0 records them
+  // for the compute phase and requests the tile's bytes
   auto issue = [&](int i) {
     if (i >= la_base + 32) look_ahead(i);
     const int src = i - la_base;
-    const int page = __shfl_sync(0xffffffffu, la_page, src);
-    const int kf = __shfl_sync(0xffffffffu, la_kf, src), ks = __shfl_sync(0xffffffffu, la_ks, src);
-    const int kz = __shfl_sync(0xffffffffu, la_kz, src), vf = __shfl_sync(0xffffffffu, la_vf, src);
-    const int vsb = __shfl_sync(0xffffffffu, la_vs, src), vz = __shfl_sync(0xffffffffu, la_vz, src);
+    const int page = __shfl_sync(0xffffffffu, la_page, src), w0 = __shfl_sync(0xffffffffu, la_w0, src);
+    const int rowk = __shfl_sync(0xffffffffu, la_rowk, src), rowv = __shfl_sync(0xffffffffu, la_rowv, src);
+    const float kbase = __shfl_sync(0xffffffffu, la_kbase, src), kbias = __shfl_sync(0xffffffffu, la_kbias, src);
+    const float mv = __shfl_sync(0xffffffffu, la_mv, src);
     if (lane != 0) return;
     const int st = i % STAGES;
-    const int t0 = w.t_begin + (warp + i * NWARPS) * kTok;
-    const int s0 = t0 % p.page_size;
     int* inf = my_info + st * kInfo;
     inf[0] = page;
-    inf[1] = kf;
-    inf[2] = ks;
-    inf[3] = kz;
-    inf[4] = vf;
-    inf[5] = vsb;
-    inf[6] = vz;
-    const int fk = min(max(kf, 0), (int)OL_FMT_U2), fv = min(max(vf, 0), (int)OL_FMT_U2);
+    inf[1] = w0;
+    inf[2] = __float_as_int(kbase);
+    inf[3] = __float_as_int(kbias);
+    inf[4] = __float_as_int(mv);
+    const int fk = w0 & 15, fv = (w0 >> 4) & 15;
     const uint32_t bk = fk == OL_FMT_F32 ? 0u : kTok * (uint32_t)fmt_row_bytes(fk, 128);
     const uint32_t bv = fv == OL_FMT_F32 ? 0u : kTok * (uint32_t)fmt_row_bytes(fv, 128);
     const uint32_t dst = smem_u32(my_stages + st * kStage);
     const uint32_t bar = bar0 + 8 * st;
     fence_proxy_async_smem();  // generic writes to this stage (zeroed rows) before the async-proxy refill
     mbar_arrive_expect_tx(bar, bk + bv);
+#pragma unroll
     for (int plane = 0; plane < 2; ++plane) {
-      const int fmt = plane == 0 ? fk : fv;
-      if (fmt == OL_FMT_F32) continue;
+      const int row = plane == 0 ? rowk : rowv;
+      if (row < 0) continue;
       const uint32_t d = dst + plane * kRegion;
-      const int row = map_row(p, page, plane, w.g, s0, fmt);
-      switch (fmt_bits(fmt)) {
+      switch (fmt_bits(plane == 0 ? fk : fv)) {
         case 16:
           tma_load_2d(d, &tm16, 0, row, bar, pol);
           tma_load_2d(d + kHalf, &tm16, 64, row, bar, pol);
@@ -368,6 +386,7 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
   const float s2e = pow2f(e_own);
   const int e0 = qexp[2 * c], e1 = qexp[2 * c + 1];               // this lane's state columns 2c, 2c + 1
   const float qs0 = qsum_h[2 * c], qs1 = qsum_h[2 * c + 1];
+  const float pne0 = pow2f(-e0), pne1 = pow2f(-e1);  // 2^-e of this lane's state columns
   const uint32_t qbase = smem_u32(qsm) + lane * 8;
   auto qop = [&](int order, int kk) { return lds_v2(qbase + (order * 8 + kk) * 256); };
 
@@ -379,7 +398,6 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
 
   const int mi = lane >> 3, r8 = lane & 7;
   const int rK = r8 + 8 * (mi & 1), cK = mi >> 1;  // ldmatrix roles for 16-bit K
-  const float sl2 = p.scale_log2;
   const uint8_t* pool = reinterpret_cast<const uint8_t*>(p.pool);
   const size_t slot_bytes = (size_t)p.kv_heads * p.page_size * 128 * 8;  // 2 planes x 128 dims x 4 bytes
 
@@ -391,14 +409,15 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
     }
     const int t0 = w.t_begin + (warp + i * NWARPS) * kTok;
     const int* inf = my_info + st * kInfo;
-    const int page = inf[0];
-    const int fk = min(max(inf[1], 0), (int)OL_FMT_U2), fv = min(max(inf[4], 0), (int)OL_FMT_U2);
-    const float ks = __int_as_float(inf[2]), vs = __int_as_float(inf[5]);
-    const int kz = inf[3] + code_offset(fk), vz = inf[6] + code_offset(fv);
+    const int w0 = inf[1];
+    const int fk = w0 & 15, fv = (w0 >> 4) & 15, kv = ((w0 >> 8) & 1023) - 256, vz = w0 >> 18;
+    const float kbase = __int_as_float(inf[2]), kbias = __int_as_float(inf[3]), mv = __int_as_float(inf[4]);
     const uint32_t sK = smem_u32(my_stages + st * kStage), sV = sK + kRegion;
-    const int s0 = t0 % p.page_size;
-    const uint8_t* gK = pool + (size_t)page * slot_bytes + ((size_t)w.g * p.page_size + s0) * 512;
-    const uint8_t* gV = gK + slot_bytes / 2;
+    // a FLOAT plane's rows in global memory (page slot s0 of head g)
+    auto gplane = [&](int plane) {
+      return pool + (size_t)inf[0] * slot_bytes + (size_t)plane * (slot_bytes / 2) +
+             ((size_t)w.g * p.page_size + t0 % p.page_size) * 512;
+    };
 
     // V rows at or past the history end hold no data: zero their bytes
     const int vhi = hist_end - t0;
@@ -415,7 +434,10 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
 
     // ---- S^T = K q^T, even and odd k-steps in two accumulators (shorter MMA chains)
     float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-    float kmul0 = sl2, kmul1 = sl2, kb0 = 0.f, kb1 = 0.f;
+    // S scale per column: kbase, times 2^-e for fp16-q formats; codes subtract kbias * sum(q)
+    const bool kq16 = fk != OL_FMT_BF16 && fk != OL_FMT_F32;
+    const float kmul0 = kq16 ? kbase * pne0 : kbase, kmul1 = kq16 ? kbase * pne1 : kbase;
+    const float kb0 = kbias * qs0, kb1 = kbias * qs1;
     if (fk == OL_FMT_BF16 || fk == OL_FMT_F16) {
       const bool h16 = fk == OL_FMT_F16;
 #pragma unroll
@@ -433,11 +455,8 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
           mma_bf16_16816(acc, a0, a1, a2, a3, q.x, q.y);
         }
       }
-      if (h16) {
-        kmul0 = sl2 * pow2f(-e0);
-        kmul1 = sl2 * pow2f(-e1);
-      }
     } else if (fk == OL_FMT_F32) {
+      const uint8_t* gK = gplane(0);
       const float* ra = reinterpret_cast<const float*>(gK + (size_t)n * 512);
       const float* rb = reinterpret_cast<const float*>(gK + (size_t)(n + 8) * 512);
 #pragma unroll
@@ -514,54 +533,53 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
           }
         }
       }
-      kmul0 = ks * sl2 * pow2f(24 - e0);
-      kmul1 = ks * sl2 * pow2f(24 - e1);
-      kb0 = ks * sl2 * (float)kz * qs0;
-      kb1 = ks * sl2 * (float)kz * qs1;
     }
 
-    // ---- online softmax on the S^T columns (exp2 domain)
+    // ---- online softmax on the S^T columns (exp2 domain), lazy maximum: the
+    // running maximum moves only when a score passes it by more than kLazy, so
+    // most tiles skip the warp reduction and the rescale (weights stay <= 2^kLazy)
     const int ta_ = t0 + n, tb_ = ta_ + 8;
     const bool va_ = ta_ >= w.lo && ta_ < tend, vb_ = tb_ >= w.lo && tb_ < tend;
     const float s00 = va_ ? fmaf(sa[0] + sb[0], kmul0, -kb0) : -INFINITY;
     const float s01 = va_ ? fmaf(sa[1] + sb[1], kmul1, -kb1) : -INFINITY;
     const float s10 = vb_ ? fmaf(sa[2] + sb[2], kmul0, -kb0) : -INFINITY;
     const float s11 = vb_ ? fmaf(sa[3] + sb[3], kmul1, -kb1) : -INFINITY;
-    float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+    if (__any_sync(0xffffffffu, fmaxf(s00, s10) > m_run0 + kLazy || fmaxf(s01, s11) > m_run1 + kLazy)) {
+      float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-    }
-    const float mn0 = fmaxf(m_run0, mx0), mn1 = fmaxf(m_run1, mx1);
-    const float b0 = mn0 == -INFINITY ? 0.f : mn0, b1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float al0 = fast_exp2(m_run0 - b0), al1 = fast_exp2(m_run1 - b1);
-    const float p00 = fast_exp2(s00 - b0), p01 = fast_exp2(s01 - b1);
-    const float p10 = fast_exp2(s10 - b0), p11 = fast_exp2(s11 - b1);
-    l_run0 = l_run0 * al0 + (p00 + p10);
-    l_run1 = l_run1 * al1 + (p01 + p11);
-    // the V scale exponent of this tile (affine formats; dense: 0): O is held in its units
-    int kv = 0;
-    float mv = 1.f;
-    if (fmt_affine(fv)) {
-      kv = log2_floor(vs);
-      mv = vs * pow2f(-kv);
-    }
-    const bool moved = __any_sync(0xffffffffu, mn0 != m_run0 || mn1 != m_run1);
-    if (moved || kv != ko) {
-      const float f = pow2f(ko - kv);
-      const float r0 = al0 * f, r1 = al1 * f;
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(m_run0, mx0), mn1 = fmaxf(m_run1, mx1);
+      const float b0 = mn0 == -INFINITY ? 0.f : mn0, b1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float al0 = fast_exp2(m_run0 - b0), al1 = fast_exp2(m_run1 - b1);
+      l_run0 *= al0;
+      l_run1 *= al1;
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
-        o[mt][0] *= r0;
-        o[mt][1] *= r1;
-        o[mt][2] *= r0;
-        o[mt][3] *= r1;
+        o[mt][0] *= al0;
+        o[mt][1] *= al1;
+        o[mt][2] *= al0;
+        o[mt][3] *= al1;
       }
+      m_run0 = mn0;
+      m_run1 = mn1;
+    }
+    const float b0 = m_run0 == -INFINITY ? 0.f : m_run0, b1 = m_run1 == -INFINITY ? 0.f : m_run1;
+    const float p00 = fast_exp2(s00 - b0), p01 = fast_exp2(s01 - b1);
+    const float p10 = fast_exp2(s10 - b0), p11 = fast_exp2(s11 - b1);
+    l_run0 += p00 + p10;
+    l_run1 += p01 + p11;
+    // O is held in units of 2^kv of the tile's V scale exponent (dense: 0)
+    if (kv != ko) {
+      const float f = pow2f(ko - kv);
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[mt][j] *= f;
       ko = kv;
     }
-    m_run0 = mn0;
-    m_run1 = mn1;
 
     // ---- O^T += V^T P^T (dimension order: m-tile 2bb + hh, row n -> 32bb + 4n + 2hh, row n + 8 -> + 1)
     const int TA = 2 * c, TB = 2 * c + 1, TC = 2 * c + 8, TD = 2 * c + 9;  // this lane's tokens (k rows)
@@ -583,6 +601,7 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
     }
     if (fv == OL_FMT_F32) {
       // V from global memory; rows at or past the history end count as zero
+      const uint8_t* gV = gplane(1);
       const int vrow[4] = {TA, TB, TC, TD};
 #pragma unroll
       for (int bb = 0; bb < 4; ++bb) {
