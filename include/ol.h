@@ -388,6 +388,22 @@ OL_API ol_status ol_hpaged_decode_step(const ol_hpaged_kv* cache, void* updated,
                                        size_t ws_bytes, ol_stream stream);
 
 /*
+ * Chunked step on a heterogeneous paged cache (as ol_chunk_step): query token
+ * i of row b at lens[b] - new_len + i attends its causal, windowed range; the
+ * chunk's tokens take part uncompressed from new_kv [2, batch, kv_heads,
+ * new_len, head_dim] bf16 and are then encoded into their pages (as
+ * ol_hpaged_append at lens[b] - new_len: pages the chunk starts take
+ * *new_pages). q and out [batch, q_heads, new_len, head_dim]. Two launches:
+ * the attention, then the append; every check runs before the first.
+ * ws_bytes >= ol_workspace_size_chunk(batch, q_heads, kv_heads, head_dim, new_len).
+ */
+OL_API ol_status ol_hpaged_chunk_step(const ol_hpaged_kv* cache, void* updated, const void* q, int32_t q_heads,
+                                      int32_t new_len, const void* new_kv, const ol_page_format* new_pages,
+                                      const int32_t* lens_host, const int32_t* lens_dev, float scale,
+                                      int32_t window, void* out, int32_t out_dtype, void* workspace,
+                                      size_t ws_bytes, ol_stream stream);
+
+/*
  * QuantizePagedCache on selected pages (page "Persistent input/output
  * feedback", section Selected-block quantization): for each of the n pages
  * (unique indices), the first valid[i] slots of every head are decoded in the

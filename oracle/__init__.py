@@ -370,6 +370,38 @@ def hpaged_attention(q, pool, desc, block_table, lens, H: int, cur_kv=None, scal
     return out
 
 
+def hpaged_chunk_attention(q, pool, desc, block_table, lens, H: int, new_len: int, new_kv,
+                           scale: Optional[float] = None, window: int = -1) -> np.ndarray:
+    """Chunked step over the heterogeneous pages: query token i of row b at
+    p_i = lens[b] - new_len + i attends its causal, windowed range; history
+    [0, lens[b] - new_len) decoded by each page's formats, the chunk's tokens
+    uncompressed from new_kv (page "Persistent input/output feedback",
+    Optional heterogeneous paged KV: current K/V attended uncompressed, encoded
+    afterwards). q [B, Hq, new_len, D], new_kv [2, B, H, new_len, D] bf16 bits
+    -> y [B, Hq, new_len, D] fp64: the pinned chunk_attention over a float32
+    cache holding exactly those values (every decoded value is an fp32)."""
+    bt, lens, new_kv = _c(block_table, np.int32), _c(lens, np.int32), _c(new_kv, np.uint16)
+    B, M = bt.shape
+    D = new_kv.shape[4]
+    S = pool.shape[1] // (2 * H * D * 4)
+    plane_bytes = H * S * D * 4
+    dense = np.full((2, B, H, M * S, D), np.nan, np.float32)
+    for b in range(B):
+        hist = int(lens[b]) - new_len
+        for t in range(hist):
+            page, slot = int(bt[b, t // S]), t % S
+            for plane, (f, sc, zp) in enumerate(((desc["kf"][page], desc["ks"][page], desc["kz"][page]),
+                                                  (desc["vf"][page], desc["vs"][page], desc["vz"][page]))):
+                rb = D * HF_BITS[int(f)] // 8
+                for h in range(H):
+                    off = plane * plane_bytes + (h * S + slot) * rb
+                    dense[plane, b, h, t] = hf_decode_row(pool[page, off:off + rb], D, (int(f), float(sc), int(zp)))
+        for plane in range(2):
+            bits = new_kv[plane, b].astype(np.uint32) << 16
+            dense[plane, b, :, hist:hist + new_len] = bits.view(np.float32)
+    return chunk_attention(q, dense, lens, new_len, scale=scale, window=window)
+
+
 def hpaged_quantize(pool, desc, H: int, D: int, pages, valid, to_fmt) -> None:
     """In place (QuantizePagedCache): the selected pages' valid prefixes converted
     to to_fmt (a one-element PAGE_DESC array), the rest zero in that format."""

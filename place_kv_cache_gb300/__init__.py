@@ -39,7 +39,7 @@ SYMBOLS = ("ol_status_string", "ol_version", "ol_workspace_size", "ol_workspace_
            "ol_int4kv_decode_attention", "ol_decode_step", "ol_decode_step_noalloc", "ol_workspace_size_host",
            "ol_decode_step_host", "ol_last_call_stats", "ol_total_stats", "ol_reset_stats",
            "ol_workspace_size_chunk", "ol_chunk_step", "ol_hpaged_append", "ol_hpaged_decode_attention",
-           "ol_hpaged_decode_step", "ol_hpaged_quantize")
+           "ol_hpaged_decode_step", "ol_hpaged_quantize", "ol_hpaged_chunk_step")
 
 
 class Stats(ctypes.Structure):
@@ -154,6 +154,8 @@ def load(build_if_missing: bool = True):
                                        f32, i32, vp, i32, vp, sz, vp]),
         "ol_hpaged_quantize": (st, [ctypes.POINTER(HPagedKV), vp, vp, vp, vp, vp, i32, ctypes.POINTER(PageFormat),
                                     vp]),
+        "ol_hpaged_chunk_step": (st, [ctypes.POINTER(HPagedKV), vp, vp, i32, i32, vp, ctypes.POINTER(PageFormat), vp,
+                                      vp, f32, i32, vp, i32, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -464,3 +466,13 @@ def ol_hpaged_quantize(kv: HPagedKV, updated, pages_host, pages_dev, valid_host,
     _check(load().ol_hpaged_quantize(ctypes.byref(kv), _ptr(updated), _ptr(ph), _ptr(pages_dev), _ptr(vh),
                                      _ptr(valid_dev), len(ph), ctypes.byref(to), _stream(stream)),
            "ol_hpaged_quantize")
+
+
+def ol_hpaged_chunk_step(kv: HPagedKV, updated, q, q_heads: int, new_len: int, new_kv, new_pages: PageFormat,
+                         lens_host, lens_dev, scale: float, window: int, out, out_dtype: int, workspace,
+                         ws_bytes: int, stream=None):
+    """Chunked step on heterogeneous pages: q and out [B, Hq, new_len, D], new_kv [2, B, Hkv, new_len, D]."""
+    lh = _host_i32(lens_host)
+    _check(load().ol_hpaged_chunk_step(ctypes.byref(kv), _ptr(updated), _ptr(q), q_heads, new_len, _ptr(new_kv),
+                                       ctypes.byref(new_pages), _ptr(lh), _ptr(lens_dev), scale, window, _ptr(out),
+                                       out_dtype, _ptr(workspace), ws_bytes, _stream(stream)), "ol_hpaged_chunk_step")

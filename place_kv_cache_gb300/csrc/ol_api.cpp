@@ -567,8 +567,9 @@ void record_attention(const CacheView& v, const int32_t* lens_host, int window, 
 // read_lo/read_hi: the tokens read from the cache per row; nf: formats of the
 // pages a fused append starts (or NULL); append_pos: the fused append's
 // position per row (or NULL).
-void record_hpaged(const ol_hpaged_kv* c, const int32_t* read_lo, const int32_t* read_hi, int64_t attended,
-                   const int32_t* append_pos, int new_len, const ol_page_format* nf, size_t ws_need) {
+void record_hpaged(const ol_hpaged_kv* c, const int32_t* read_lo, const int32_t* read_hi, int nranges,
+                   int64_t attended, const int32_t* append_pos, int new_len, const ol_page_format* nf,
+                   size_t ws_need) {
   ol_stats s = {};
   s.calls = 1;
   const int S = c->page_size, D = c->head_dim;
@@ -576,14 +577,16 @@ void record_hpaged(const ol_hpaged_kv* c, const int32_t* read_lo, const int32_t*
     s.kv_payload_bytes_read += n * (int64_t)fmt_row_bytes(f.format, D);
     if (fmt_affine(f.format)) s.dequantized_bytes += n * D * 4;
   };
-  for (int b = 0; read_lo && b < c->batch; ++b)
-    for (int t = read_lo[b]; t < read_hi[b];) {
-      const int end = std::min(read_hi[b], (t / S + 1) * S);
+  for (int r = 0; read_lo && r < c->batch * nranges; ++r) {
+    const int b = r % c->batch;
+    for (int t = read_lo[r]; t < read_hi[r];) {
+      const int end = std::min(read_hi[r], (t / S + 1) * S);
       const ol_page_format& f = c->formats_host[c->block_table_host[(size_t)b * c->max_pages + t / S]];
       plane_bytes(f.k, (int64_t)(end - t) * c->kv_heads);
       plane_bytes(f.v, (int64_t)(end - t) * c->kv_heads);
       t = end;
     }
+  }
   for (int b = 0; append_pos && b < c->batch; ++b)
     for (int t = append_pos[b]; t < append_pos[b] + new_len; ++t) {
       const ol_page_format& f = hpaged_token_format(c, b, t, append_pos[b], *nf);
@@ -646,8 +649,10 @@ ol_status run_attention(int layout, const void* desc, const CacheView& v, const 
   std::vector<int32_t> read_lo, read_hi, append_pos;
   if (layout == OL_LAYOUT_HPAGED) {
     const ol_hpaged_kv* c = static_cast<const ol_hpaged_kv*>(desc);
-    if (nq != 1) return OL_ERR_UNSUPPORTED;
+    if (nq != 1 && append) return OL_ERR_UNSUPPORTED;  // the fused append is the decode step's
     if ((st = no_overlap(v, c->block_table, sizeof(int32_t) * (size_t)c->batch * c->max_pages)) != OL_OK) return st;
+    const int wq = window < 0 ? -1 : window;              // one query token's window
+    const int wu = window < 0 ? -1 : window + nq - 1;     // the union of a chunk's query tokens' ranges
     const ol_paged_kv k = paged_shape_of(c);
     if (append) {
       if (!new_fmt) return OL_ERR_NULL;
@@ -655,24 +660,32 @@ ol_status run_attention(int layout, const void* desc, const CacheView& v, const 
       append_pos.resize(v.batch);
       for (int b = 0; b < v.batch; ++b) append_pos[b] = lens_host[b] - 1;
       if ((st = check_pages(&k, append_pos.data(), 1, true, window)) != OL_OK) return st;
-    } else if ((st = check_pages(&k, lens_host, 0, false, window < 0 ? -1 : window)) != OL_OK) {
+    } else if ((st = check_pages(&k, lens_host, 0, false, wu)) != OL_OK) {
       return st;
     }
-    read_lo.resize(v.batch);
-    read_hi.resize(v.batch);
-    int64_t attended = 0;
+    // tokens taken from new_kv instead of the pages: the decode step's current
+    // token, or a chunk's tokens (query token z sees the first z + 1 of them)
+    std::vector<int32_t> union_hi(v.batch);
     for (int b = 0; b < v.batch; ++b) {
-      const RowSplit rs = row_split(lens_host[b], window < 0 ? -1 : window, 1);
-      read_lo[b] = rs.lo;
-      read_hi[b] = rs.hi - ((cur_from_new && rs.hi > rs.lo) ? 1 : 0);
-      attended += rs.hi - rs.lo;
+      const RowSplit rs = row_split(lens_host[b], wu, 1);
+      union_hi[b] = rs.hi - (cur_from_new ? std::min(nq, rs.hi - rs.lo) : 0);
     }
-    if ((st = check_hpaged_formats(c, lens_host, window < 0 ? -1 : window, read_hi.data(),
-                                   append ? append_pos.data() : nullptr, append ? 1 : 0)) != OL_OK)
+    if ((st = check_hpaged_formats(c, lens_host, wu, union_hi.data(), append ? append_pos.data() : nullptr,
+                                   append ? 1 : 0)) != OL_OK)
       return st;
+    read_lo.resize((size_t)v.batch * nq);
+    read_hi.resize((size_t)v.batch * nq);
+    int64_t attended = 0;
+    for (int z = 0; z < nq; ++z)
+      for (int b = 0; b < v.batch; ++b) {
+        const RowSplit rs = row_split(lens_host[b] - (nq - 1 - z), wq, 1);
+        read_lo[(size_t)z * v.batch + b] = rs.lo;
+        read_hi[(size_t)z * v.batch + b] = rs.hi - (cur_from_new ? std::min(z + 1, rs.hi - rs.lo) : 0);
+        attended += rs.hi - rs.lo;
+      }
     if ((st = check_owner(v.ranges, v.nranges, v.owner)) != OL_OK) return st;
     if (check_only) return OL_OK;
-    record_hpaged(c, read_lo.data(), read_hi.data(), attended, append ? append_pos.data() : nullptr, 1, new_fmt,
+    record_hpaged(c, read_lo.data(), read_hi.data(), nq, attended, append ? append_pos.data() : nullptr, 1, new_fmt,
                   need);
   } else {
     if ((st = check_owner(v.ranges, v.nranges, v.owner)) != OL_OK) return st;
@@ -1132,7 +1145,7 @@ ol_status ol_hpaged_append(const ol_hpaged_kv* cache, void* updated, const void*
       (st = check_hpaged_formats(cache, nullptr, -1, nullptr, positions_host, new_len)) != OL_OK)
     return st;
   if ((st = check_owner(v.ranges, v.nranges, v.owner)) != OL_OK) return st;
-  record_hpaged(cache, nullptr, nullptr, 0, positions_host, new_len, new_pages, 0);
+  record_hpaged(cache, nullptr, nullptr, 1, 0, positions_host, new_len, new_pages, 0);
   if (fault_injected()) return OL_ERR_INJECTED;
   AppendParams p = {};
   p.layout = OL_LAYOUT_HPAGED;
@@ -1185,6 +1198,71 @@ ol_status ol_hpaged_decode_step(const ol_hpaged_kv* cache, void* updated, const 
   std::vector<int32_t> pos(v.batch);
   for (int b = 0; b < v.batch; ++b) pos[b] = lens_host[b] - 1;
   hpaged_start_pages(cache, pos.data(), 1, *new_pages);
+  return OL_OK;
+}
+
+ol_status ol_hpaged_chunk_step(const ol_hpaged_kv* cache, void* updated, const void* q, int32_t q_heads,
+                               int32_t new_len, const void* new_kv, const ol_page_format* new_pages,
+                               const int32_t* lens_host, const int32_t* lens_dev, float scale, int32_t window,
+                               void* out, int32_t out_dtype, void* workspace, size_t ws_bytes, ol_stream stream) {
+  CacheView v;
+  ol_status st = view_hpaged(cache, v);
+  if (st != OL_OK) return st;
+  if (new_len < 1) return OL_ERR_SHAPE;
+  if (!lens_host || !new_pages) return OL_ERR_NULL;
+  // the append writes positions lens - new_len .. lens - 1 of every row
+  std::vector<int32_t> pos(v.batch);
+  for (int b = 0; b < v.batch; ++b) {
+    if (lens_host[b] < new_len || lens_host[b] > v.capacity) return OL_ERR_CAPACITY;
+    pos[b] = lens_host[b] - new_len;
+  }
+  if ((st = append_common(v, updated, new_kv, new_len, pos.data(), lens_dev)) != OL_OK) return st;
+  if (!valid_page_format(*new_pages)) return OL_ERR_SHAPE;
+  const ol_paged_kv k = paged_shape_of(cache);
+  if ((st = check_pages(&k, pos.data(), new_len, true, -1)) != OL_OK) return st;
+  if ((st = check_hpaged_formats(cache, nullptr, -1, nullptr, pos.data(), new_len)) != OL_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // every check of the attention first: an error return means nothing was written
+  if ((st = run_attention(OL_LAYOUT_HPAGED, cache, v, q, q_heads, lens_host, lens_dev, new_kv, 0, 1, scale, window,
+                          out, out_dtype, workspace, ws_bytes, s, new_len, true)) != OL_OK)
+    return st;
+  if (fault_injected()) return OL_ERR_INJECTED;
+  // the chunk attended uncompressed, then encoded into its pages
+  st = run_attention(OL_LAYOUT_HPAGED, cache, v, q, q_heads, lens_host, lens_dev, new_kv, 0, 1, scale, window, out,
+                     out_dtype, workspace, ws_bytes, s, new_len);
+  if (st != OL_OK) return st;
+  AppendParams p = {};
+  p.layout = OL_LAYOUT_HPAGED;
+  p.dtype = OL_BF16;
+  p.batch = v.batch;
+  p.kv_heads = v.kv_heads;
+  p.head_dim = v.head_dim;
+  p.capacity = v.capacity;
+  p.new_len = new_len;
+  p.values = new_kv;
+  p.positions = lens_dev;
+  p.positions_are_lens = 1;
+  p.pool = cache->pool;
+  p.block_table = cache->block_table;
+  p.num_pages = cache->num_pages;
+  p.page_size = cache->page_size;
+  p.max_pages = cache->max_pages;
+  p.page_fmt = cache->formats;
+  p.new_fmt = *new_pages;
+  if (launch_hpaged_append(p, s) != cudaSuccess) return OL_ERR_CUDA;
+  // the call's one record: the attention's counts (recorded by run_attention) and the append's
+  int64_t appended = 0;
+  for (int b = 0; b < v.batch; ++b)
+    for (int t = pos[b]; t < pos[b] + new_len; ++t) {
+      const ol_page_format& f = hpaged_token_format(cache, b, t, pos[b], *new_pages);
+      appended += (int64_t)v.kv_heads *
+                  (int64_t)(fmt_row_bytes(f.k.format, v.head_dim) + fmt_row_bytes(f.v.format, v.head_dim));
+    }
+  for (ol_stats* r : {&t_last, &t_total}) {
+    r->storage_append_copied_bytes += appended;
+    r->storage_reuse_count += v.batch > 0 ? 2 : 0;
+  }
+  hpaged_start_pages(cache, pos.data(), new_len, *new_pages);
   return OL_OK;
 }
 

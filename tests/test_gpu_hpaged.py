@@ -246,3 +246,36 @@ def test_long_rows_with_every_format_match_oracle(shape):
     check_out(out_as_f64(out), want, ol.OL_F32)
     pr.check_state()
     assert ol.ol_workspace_status(ws) == ol.OL_DEVICE_OK
+
+
+CHUNKS = [  # B, H, S, D, Hq, lens (before the chunk is counted in), chunk length
+    (3, 2, 16, 128, 8, [16, 21, 40], 4),
+    (2, 1, 4, 64, 4, [3, 9], 5),
+    (1, 2, 16, 128, 14, [100], 16),
+]
+
+
+@pytest.mark.parametrize("window", [-1, 0, 7])
+@pytest.mark.parametrize("shape", CHUNKS, ids=[f"b{s[0]}s{s[2]}d{s[3]}t{s[6]}" for s in CHUNKS])
+def test_chunk_step_matches_oracle(shape, window):
+    B, H, S, D, Hq, hist, T = shape
+    hist = np.array(hist, np.int32)
+    M = int(-(-(hist.max() + T) // S)) + 1
+    pr = Pair(B, H, S, D, M, B * M + 1, seed=707 + D + T)
+    pr.fill(hist, lambda b, j: 2 * j + b + 1)
+    lens = hist + T
+    q = bf16_from_f32(pr.rng.standard_normal((B, Hq, T, D)).astype(np.float32))
+    new_kv = pr.values(T)
+    od, gd = fmt_pair(5)
+    want = O.hpaged_chunk_attention(q, pr.pool, pr.desc, pr.table, lens, H, T, new_kv, window=window)
+    O.hpaged_append(pr.pool, pr.desc, pr.table, new_kv, hist, od)
+    n = ol.ol_workspace_size_chunk(B, Hq, H, D, T)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda:0")
+    ol.ol_workspace_init(ws, n)
+    out = torch.full((B, Hq, T, D), float("nan"), dtype=torch.float32, device="cuda:0")
+    ol.ol_hpaged_chunk_step(pr.kv, pr.pool_d, to_dev(q), Hq, T, to_dev(new_kv), gd, lens, to_dev(lens), 0.0, window,
+                            out, ol.OL_F32, ws, n)
+    torch.cuda.synchronize()
+    check_out(out_as_f64(out), want, ol.OL_F32)
+    pr.check_state()
+    assert ol.ol_workspace_status(ws) == ol.OL_DEVICE_OK

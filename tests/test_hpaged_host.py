@@ -231,3 +231,27 @@ def test_statistics_follow_the_page_formats():
     # row 0 starts page 2 at token 32 (new formats I8 / U4); row 1 continues page 1 at 17 (BF16 / U4)
     assert s["storage_append_copied_bytes"] == HKV * ((128 + 64) + (256 + 64))
     assert s["storage_allocations"] == 0 and s["storage_prefix_copied_bytes"] == 0
+
+
+def chunk(d=None, lens=(10, 100), new_len=4, new_pages=None, updated=POOL, window=-1, ws_bytes=None):
+    d = desc() if d is None else d
+    n = ol.ol_workspace_size_chunk(B, HQ, HKV, D, new_len) if ws_bytes is None else ws_bytes
+    ol.ol_hpaged_chunk_step(d, updated, Q, HQ, new_len, NEWKV, ol.page_format() if new_pages is None else new_pages,
+                            np.array(lens, np.int32), LENS_DEV, 0.0, window, OUT, ol.OL_BF16, WS, n, stream=0)
+
+
+def test_chunk_step_validation():
+    assert status_of(chunk) == ol.OL_ERR_INJECTED
+    assert status_of(chunk, lens=(3, 100)) == ol.OL_ERR_CAPACITY          # a row shorter than the chunk
+    assert status_of(chunk, lens=(10, M * S + 1)) == ol.OL_ERR_CAPACITY
+    assert status_of(chunk, new_len=0) == ol.OL_ERR_SHAPE
+    assert status_of(chunk, ws_bytes=WS_BYTES) == ol.OL_ERR_WORKSPACE      # the decode step's size is too small
+    assert status_of(chunk, updated=POOL + 16) == ol.OL_ERR_ALIAS
+    assert status_of(chunk, d=desc(access=ol.OL_READ_ONLY)) == ol.OL_ERR_READONLY
+    assert status_of(chunk, new_pages=ol.page_format(k=(ol.OL_FMT_U4, 0.5, 16))) == ol.OL_ERR_SHAPE
+    m = mirror()
+    m["vf"][2] = 42                           # row 0's page 2 (tokens 32..47)
+    assert status_of(chunk, d=desc(m), lens=(36, 5)) == ol.OL_ERR_INJECTED  # the chunk 32..35 starts page 2
+    assert status_of(chunk, d=desc(m), lens=(40, 5)) == ol.OL_ERR_SHAPE     # 32..35 are history: page 2 is read
+    assert status_of(chunk, d=desc(m), lens=(40, 8), new_len=8) == ol.OL_ERR_INJECTED  # 32..39 start page 2
+    np.testing.assert_array_equal(m["vf"][2], 42)                          # validation never touches the mirror

@@ -721,6 +721,44 @@ def test_hpaged_four_step_fixture_tolerance(fmt, scale, zps, tol):
     assert worst > 0.0
 
 
+def test_hpaged_chunk_of_one_token_is_the_decode_step():
+    rng, P, table, pool, desc = _hetero_case()
+    B, H, S, M, D = 2, 2, 4, 4, 8
+    hist = bf16_from_f32(rng.standard_normal((2, B, H, 9, D)).astype(np.float32))
+    O.hpaged_append(pool, desc, table, hist[:, :, :, :5], [0, 0], O.page_desc(k=(O.HF_I8, 0.02, 3), v=(O.HF_U4, 0.3, 8)))
+    O.hpaged_append(pool, desc, table, hist[:, :, :, 5:], [5, 5], O.page_desc(k=(O.HF_F16, 1, 0), v=(O.HF_I2, 0.9, 0)))
+    cur = bf16_from_f32(rng.standard_normal((2, B, H, 1, D)).astype(np.float32))
+    q = bf16_from_f32(rng.standard_normal((B, 4, D)).astype(np.float32))
+    lens = np.array([10, 6], np.int32)
+    for w in (-1, 0, 3):
+        y = O.hpaged_chunk_attention(q[:, :, None, :], pool, desc, table, lens, H, 1, cur, window=w)
+        np.testing.assert_array_equal(y[:, :, 0], O.hpaged_attention(q, pool, desc, table, lens, H, cur_kv=cur,
+                                                                       window=w))
+
+
+def test_hpaged_chunk_reads_history_by_page_and_the_chunk_uncompressed():
+    # a BFLOAT16 page stores bf16 values exactly: appending the chunk in BFLOAT16 and
+    # attending every token from the pages equals attending the chunk uncompressed
+    rng, P, table, pool, desc = _hetero_case()
+    B, H, S, M, D, T = 2, 2, 4, 4, 8, 3
+    hist = bf16_from_f32(rng.standard_normal((2, B, H, 8, D)).astype(np.float32))
+    O.hpaged_append(pool, desc, table, hist, [0, 0], O.page_desc(k=(O.HF_U4, 0.4, 7), v=(O.HF_I8, 0.03, -2)))
+    chunk = bf16_from_f32(rng.standard_normal((2, B, H, T, D)).astype(np.float32))
+    q = bf16_from_f32(rng.standard_normal((B, 4, T, D)).astype(np.float32))
+    lens = np.array([11, 7], np.int32)  # both chunks start a page (slot 0), which takes BFLOAT16
+    for w in (-1, 2):
+        y = O.hpaged_chunk_attention(q, pool, desc, table, lens, H, T, chunk, window=w)
+        p2, d2 = pool.copy(), desc.copy()
+        O.hpaged_append(p2, d2, table, chunk, lens - T, O.page_desc())
+        for i in range(T):
+            yi = O.hpaged_attention(np.ascontiguousarray(q[:, :, i]), p2, d2, table, lens - T + i + 1, H, window=w)
+            np.testing.assert_allclose(y[:, :, i], yi, rtol=0, atol=1e-12)
+    moved = chunk.copy()
+    moved[:, :, :, 1:] = bf16_from_f32(rng.standard_normal((2, B, H, T - 1, D)).astype(np.float32))
+    y0 = O.hpaged_chunk_attention(q, pool, desc, table, lens, H, T, chunk)[:, :, 0]
+    np.testing.assert_array_equal(O.hpaged_chunk_attention(q, pool, desc, table, lens, H, T, moved)[:, :, 0], y0)
+
+
 def test_hpaged_quantize_selected_pages_only():
     rng, P, table, pool, desc = _hetero_case()
     B, H, S, M, D = 2, 2, 4, 4, 8
