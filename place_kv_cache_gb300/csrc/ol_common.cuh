@@ -277,10 +277,13 @@ __device__ __forceinline__ int head_block(const AttnParams& p) { return p.nq > 1
 // (tq tokens from slice_first) and head c % group; group * tq columns.
 __device__ __forceinline__ int slice_tq(const AttnParams& p) { return p.nq > 1 && p.tq > 1 ? p.tq : 1; }
 __device__ __forceinline__ int state_cols(const AttnParams& p) { return p.group * slice_tq(p); }
-__device__ __forceinline__ int slice_first(const AttnParams& p) { return query_index(p) * slice_tq(p); }
-__device__ __forceinline__ int slice_tokens(const AttnParams& p) {
-  return p.nq > 1 ? min(slice_tq(p), p.nq - slice_first(p)) : 1;
+// slice zs (by default the launch's own, query_index)
+__device__ __forceinline__ int slice_first(const AttnParams& p, int zs) { return zs * slice_tq(p); }
+__device__ __forceinline__ int slice_first(const AttnParams& p) { return slice_first(p, query_index(p)); }
+__device__ __forceinline__ int slice_tokens(const AttnParams& p, int zs) {
+  return p.nq > 1 ? min(slice_tq(p), p.nq - slice_first(p, zs)) : 1;
 }
+__device__ __forceinline__ int slice_tokens(const AttnParams& p) { return slice_tokens(p, query_index(p)); }
 
 // Chunked steps: query token z of every row sits at position hi - nq + z; its
 // visible range ends there (causal inside the chunk) and starts window_q
@@ -288,15 +291,19 @@ __device__ __forceinline__ int slice_tokens(const AttnParams& p) {
 // the union of theirs (the first token's start to the last token's end), and
 // the kernel masks each column to its own token's range. The plan's split
 // stays.
-__device__ __forceinline__ void slice_query(Work& w, const AttnParams& p) {
+// (A CTA serving slices za..zb takes the union of their ranges.)
+__device__ __forceinline__ void slice_query(Work& w, const AttnParams& p, int za, int zb) {
   if (p.nq <= 1 || !w.valid) return;
-  const int hi_first = w.hi - (p.nq - 1 - slice_first(p));
-  const int hi_last = hi_first + slice_tokens(p) - 1;
+  const int hi_first = w.hi - (p.nq - 1 - slice_first(p, za));
+  const int hi_last = w.hi - (p.nq - 1 - (slice_first(p, zb) + slice_tokens(p, zb) - 1));
   const int lo = p.window_q < 0 ? w.lo : max(hi_first - 1 - p.window_q, 0);
   w.hi = hi_last;
   w.lo = max(w.lo, lo);
   w.t_end = min(w.t_end, hi_last);
   if (w.t_end < w.t_begin) w.t_end = w.t_begin;
+}
+__device__ __forceinline__ void slice_query(Work& w, const AttnParams& p) {
+  slice_query(w, p, query_index(p), query_index(p));
 }
 
 // Length of row b as the kernels read it: clamped to [0, capacity], with a
@@ -414,7 +421,7 @@ __device__ __forceinline__ void store_out(void* out, int out_dtype, size_t idx, 
 __device__ __forceinline__ void finish_split(const AttnParams& p, const Work& w, const float* sm_m,
                                              const float* sm_l, const float* sm_o, int o_stride, int h0,
                                              int h1, int d0, int d1, int slot, int first_slot, int nslots,
-                                             int arrivals, int* sm_flag, float* scratch) {
+                                             int arrivals, int* sm_flag, float* scratch, int zs = -1) {
   const int D = p.head_dim;
   const int G = p.group;
   const int NC = state_cols(p);  // state columns: (query token, head) pairs
@@ -423,13 +430,14 @@ __device__ __forceinline__ void finish_split(const AttnParams& p, const Work& w,
   const int nh = h1 - h0, nd = d1 - d0;
   // a chunked step's slice zs: its own counters and partial slots; column c
   // goes to query token z0 + c / G, head c % G of y [B, Hq, nq, D]
-  const int nq = p.nq > 1 ? p.nq : 1, zs = query_index(p), z0 = slice_first(p);
+  if (zs < 0) zs = query_index(p);  // the slice whose columns these are
+  const int nq = p.nq > 1 ? p.nq : 1, z0 = slice_first(p, zs);
   const size_t head_base = (size_t)w.b * p.q_heads + (size_t)w.g * G;
   auto out_at = [&](int c, int d) -> size_t {
     if (nq == 1) return (head_base + c) * D + d;  // a decode step: column = head
     return ((head_base + c % G) * nq + z0 + c / G) * D + d;
   };
-  const int c_live = G * slice_tokens(p);  // columns past it belong to tokens beyond the chunk
+  const int c_live = G * slice_tokens(p, zs);  // columns past it belong to tokens beyond the chunk
   float* const partials =
       p.partials + (size_t)zs * ((size_t)p.batch * p.kv_heads + kMaxExtraSplits) * NC * (D + 2);  // max_ctas slots
   uint32_t* const counters = p.counters + (size_t)zs * p.batch * p.kv_heads;

@@ -152,7 +152,7 @@ cudaError_t launch_cfg(const CUtensorMap& map, const AttnParams& p, cudaStream_t
   cudaLaunchConfig_t cfg = {};
   constexpr bool chunk = CHUNK;  // query-token slices along x, the plan's CTAs (and clusters) along y
   const int slices = chunk ? (p.nq + (p.tq > 1 ? p.tq : 1) - 1) / (p.tq > 1 ? p.tq : 1) : 1;
-  cfg.gridDim = chunk ? dim3(slices, p.total_ctas, 1) : dim3(p.total_ctas, 1, 1);
+  cfg.gridDim = chunk ? dim3((slices + 1) / 2, p.total_ctas, 1) : dim3(p.total_ctas, 1, 1);  // 2 slices per CTA
   cfg.blockDim = dim3(NWARPS * 32, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;

@@ -98,7 +98,8 @@ __device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t addr) {
 // Every thread of every CTA of the cluster must call it.
 template <typename StateO>
 __device__ __forceinline__ void merge_and_finish(const AttnParams& p, const Work& w, int nstates, StateO state_o,
-                                                 float* merged, float* cmerged, const MergeScratch& ms) {
+                                                 float* merged, float* cmerged, const MergeScratch& ms,
+                                                 int zs = -1) {
   const int G = state_cols(p);  // state columns: the heads, or (query token, head) pairs
   const int CS = p.cluster;
   __syncthreads();
@@ -149,7 +150,7 @@ __device__ __forceinline__ void merge_and_finish(const AttnParams& p, const Work
     __syncthreads();
     if (!w.valid) return;
     finish_split(p, w, ms.m, ms.l, merged, kOStride, 0, G, 0, 128, w.slot, w.first_cta, w.nsplit, w.nsplit,
-                 ms.flag, ms.scr);
+                 ms.flag, ms.scr, zs);
     return;
   }
   cluster_sync();  // every push of every CTA of the cluster is visible
@@ -186,7 +187,7 @@ __device__ __forceinline__ void merge_and_finish(const AttnParams& p, const Work
   __syncthreads();
   if (!w.valid) return;
   finish_split(p, w, ms.cm, ms.cl, cmerged, dspan, 0, G, d0, d0 + dspan, cta_index(p) / CS, w.first_cta / CS,
-               w.nsplit / CS, w.nsplit, ms.flag, ms.scr);
+               w.nsplit / CS, w.nsplit, ms.flag, ms.scr, zs);
 }
 
 }  // namespace ol
