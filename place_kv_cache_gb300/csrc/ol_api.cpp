@@ -53,8 +53,8 @@ bool fault_injected() {
 size_t elt_bytes(int dtype) { return dtype == OL_F32 ? 4 : 2; }
 bool valid_dtype(int d) { return d == OL_F32 || d == OL_BF16; }
 
-// Launch tuning: OL_TUNE="waves=<w>,minchunk=<c>,cfg=<variant>,cluster=<cs>,cpu=<k>,generic=<0|1>,hpwaves=<w>"
-// (read once).
+// Launch tuning: OL_TUNE="waves=<w>,minchunk=<c>,cfg=<variant>,cluster=<cs>,cpu=<k>,generic=<0|1>,hpwaves=<w>,
+// cwaves=<w>" (read once).
 struct Tune {
   int waves = 2;
   int min_chunk = 16;
@@ -63,6 +63,7 @@ struct Tune {
   int clusters_per_unit = -1;  // cap on clusters per (row, kv head) for small batches
   bool generic = false;        // heterogeneous pages: the CUDA-core kernel even where the tensor-core one applies
   int hp_waves = 4;            // heterogeneous pages: CTA waves of the split plan (measured best on hpaged_b64)
+  int chunk_waves = 1;         // chunked steps on tensor cores (measured best on chunk4_b32)
 };
 const Tune& tune() {
   static Tune t = [] {
@@ -85,6 +86,7 @@ const Tune& tune() {
         if (k == "cpu" && val >= 1) x.clusters_per_unit = val;
         if (k == "generic") x.generic = val != 0;
         if (k == "hpwaves" && val > 0) x.hp_waves = val;
+        if (k == "cwaves" && val > 0) x.chunk_waves = val;
       }
       if (comma == std::string::npos) break;
       pos = comma + 1;
@@ -174,7 +176,7 @@ void plan_fast(AttnParams& p, const int32_t* lens_host, int sms) {
     }
   }
   if (units >= sms || units == 0) {
-    plan_splits(p, lens_host, slots * tune().waves, 1);
+    plan_splits(p, lens_host, slots * (p.nq > 1 ? tune().chunk_waves : tune().waves), 1);
     return;
   }
   int cs = pow2_floor(slots / units);
