@@ -494,10 +494,12 @@ def run_ours(args, rank, world, dist):
 
 def run_e2e(s, stream, K_e2e):
     """The same step through the public host-buffer call, ol_decode_step_host:
-    every step copies q, the new K/V (and the lengths when the launch cannot
-    carry them by value) from pinned host memory to the device, runs the step
-    on the device-resident cache and copies y back to pinned host memory, all
-    enqueued by that one call on the timed stream."""
+    every step moves q and the new K/V from pinned host memory to the device
+    (and the lengths when the launch cannot carry them by value), runs the step
+    on the device-resident cache and moves y back into pinned host memory, all
+    enqueued by that one call on the timed stream. Pinned buffers are mapped
+    into the device's address space, so the step's kernels load the inputs and
+    store y across the CPU-GPU link themselves (no copy-engine copies)."""
     torch, ol, w = s.torch, s.ol, s.w
     q_h = s.q.cpu().pin_memory()
     kv_h = s.new_kv.cpu().pin_memory()
@@ -529,7 +531,8 @@ def run_e2e(s, stream, K_e2e):
     ms = e0.elapsed_time(e1) / K_e2e
     return {"value": round(s.bytes_per_step / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "us_per_step": round(ms * 1e3, 3),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": K_e2e,
-            "call": "ol_decode_step_host (one C-ABI call per step, pinned host buffers)"}
+            "call": "ol_decode_step_host (one C-ABI call per step, pinned host buffers)",
+            "transfer": "q, new K/V loaded and y stored by the step's kernels from/to mapped pinned host memory"}
 
 
 # --------------------------------------------------------------- oracle

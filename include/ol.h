@@ -489,15 +489,19 @@ OL_API size_t ol_workspace_size_host(int32_t batch, int32_t q_heads, int32_t kv_
 /*
  * The fused decode step with host-resident inputs and output: q_host
  * [batch, q_heads, head_dim], new_kv_host [2, batch, kv_heads, 1, head_dim]
- * (dtypes as for ol_decode_step) and lens_host [batch] are copied into the
- * workspace's staging area (host-to-device copies on `stream`), the step runs
- * as ol_decode_step on those device copies, and y is copied to out_host
- * [batch, q_heads, head_dim] of out_dtype (device-to-host on `stream`).
+ * (dtypes as for ol_decode_step), lens_host [batch] and y in out_host
+ * [batch, q_heads, head_dim] of out_dtype. Each of q_host, new_kv_host and
+ * out_host that is page-locked host memory mapped into the device's address
+ * space (cudaHostAlloc'd or pinned tensors; registered memory with mapping)
+ * and 16-byte aligned is used in place: the step's kernels load from it and
+ * store y into it across the CPU-GPU link, with no copy. Any other host
+ * buffer goes through the workspace's staging area with host-to-device /
+ * device-to-host copies on `stream` (pageable memory at the driver's pace).
+ * The lengths travel in the launch for up to 160 rows, else by one copy.
  * Everything is asynchronous: out_host holds y once `stream` has been
- * synchronized, and the host buffers must stay valid until then; pinned host
- * memory keeps the copies asynchronous (pageable memory works, at the
- * driver's pace). The cache stays in device memory, described as for
- * ol_decode_step. ws_bytes must be at least
+ * synchronized, and the host buffers must stay valid and unchanged until
+ * then; out_host must not overlap q_host or new_kv_host. The cache stays in
+ * device memory, described as for ol_decode_step. ws_bytes must be at least
  * ol_workspace_size_host(batch, q_heads, kv_heads, head_dim).
  * Errors: those of ol_decode_step (the descriptor, host pointers, lengths and
  * workspace size are checked before any copy is enqueued; a call that fails

@@ -1090,6 +1090,19 @@ size_t ol_workspace_size_host(int32_t batch, int32_t q_heads, int32_t kv_heads, 
   return host_staging(batch, q_heads, kv_heads, head_dim).total;
 }
 
+// The device address of page-locked host memory mapped into the device's
+// address space (cudaHostAlloc'd, or registered with mapping), 16-byte
+// aligned; nullptr for any other pointer (pageable memory, device memory).
+static void* mapped_host(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the error the query left behind
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || !a.devicePointer || !aligned16(a.devicePointer)) return nullptr;
+  return a.devicePointer;
+}
+
 ol_status ol_decode_step_host(int32_t layout, const void* cache_desc, void* updated, const void* q_host,
                               int32_t q_heads, const void* new_kv_host, const int32_t* lens_host, float scale,
                               int32_t window, void* out_host, int32_t out_dtype, void* workspace, size_t ws_bytes,
@@ -1113,17 +1126,31 @@ ol_status ol_decode_step_host(int32_t layout, const void* cache_desc, void* upda
   const size_t out_bytes = (size_t)v.batch * q_heads * v.head_dim * elt_bytes(out_dtype);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(ws + h.q, q_host, q_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(ws + h.kv, new_kv_host, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return OL_ERR_CUDA;
+  // Mapped page-locked buffers are used in place: the step's kernels load q
+  // and the new K/V from host memory and store y there, over the CPU-GPU
+  // link, with no copy-engine copy (a few microseconds of GPU time each, the
+  // larger part of a small step). Other buffers go through the workspace's
+  // staging area with stream-ordered copies.
+  const void* q_in = mapped_host(q_host);
+  const void* kv_in = mapped_host(new_kv_host);
+  void* out_to = mapped_host(out_host);
+  if (!q_in) {
+    if (cudaMemcpyAsync(ws + h.q, q_host, q_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return OL_ERR_CUDA;
+    q_in = ws + h.q;
+  }
+  if (!kv_in) {
+    if (cudaMemcpyAsync(ws + h.kv, new_kv_host, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return OL_ERR_CUDA;
+    kv_in = ws + h.kv;
+  }
   // the kernels take the lengths by value for batches of up to kInlineRows
   // rows and never read the device copy then
   if (v.batch > kInlineRows &&
       cudaMemcpyAsync(ws + h.lens, lens_host, sizeof(int32_t) * v.batch, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return OL_ERR_CUDA;
-  st = run_attention(layout, cache_desc, v, ws + h.q, q_heads, lens_host, reinterpret_cast<int32_t*>(ws + h.lens),
-                     ws + h.kv, 1, 1, scale, window, ws + h.out, out_dtype, workspace, h.q, s);
-  if (st != OL_OK) return st;
+  st = run_attention(layout, cache_desc, v, q_in, q_heads, lens_host, reinterpret_cast<int32_t*>(ws + h.lens),
+                     kv_in, 1, 1, scale, window, out_to ? out_to : ws + h.out, out_dtype, workspace, h.q, s);
+  if (st != OL_OK || out_to) return st;
   return cudaMemcpyAsync(out_host, ws + h.out, out_bytes, cudaMemcpyDeviceToHost, s) == cudaSuccess ? OL_OK
                                                                                                  : OL_ERR_CUDA;
 }
