@@ -504,7 +504,7 @@ def run_e2e(s, stream, K_e2e):
     q_h = s.q.cpu().pin_memory()
     kv_h = s.new_kv.cpu().pin_memory()
     y_h = torch.empty(s.out.shape, dtype=s.out.dtype).pin_memory()
-    lens_h = [np.ascontiguousarray(l, dtype=np.int32) for l in s.lens_list]
+    lens_h = [torch.from_numpy(np.ascontiguousarray(l, dtype=np.int32)) for l in s.lens_list]  # host int32
     h2d = q_h.numel() * 2 + kv_h.numel() * 2 + (s.lens.size * 4 if w.batch > 160 else 0)
     d2h = y_h.numel() * 2
     n = ol.ol_workspace_size_host(w.batch, w.q_heads, w.kv_heads, w.head_dim)

@@ -172,8 +172,18 @@ def _status_string(s: int) -> str:
         return f"status {s}"
 
 
+# address getter per tensor type seen (torch.Tensor and subclasses): one dict
+# lookup instead of the generic checks on every call of a per-step function
+_PTR_OF_TYPE = {}
+_I32 = np.dtype(np.int32)
+_TORCH_I32 = None  # torch.int32, once torch is in use
+
+
 def _ptr(x) -> Optional[int]:
     """Address of a torch tensor / numpy array / int (None stays NULL)."""
+    get = _PTR_OF_TYPE.get(type(x))
+    if get is not None:
+        return get(x)
     if x is None:
         return None
     if isinstance(x, int):
@@ -181,13 +191,26 @@ def _ptr(x) -> Optional[int]:
     if isinstance(x, np.ndarray):
         return x.ctypes.data
     if hasattr(x, "data_ptr"):
+        _PTR_OF_TYPE[type(x)] = type(x).data_ptr
         return x.data_ptr()
     raise TypeError(f"cannot take the address of {type(x)}")
 
 
-def _host_i32(a) -> Optional[np.ndarray]:
+def _host_i32(a):
+    """Host int32 C-contiguous lengths/positions: the argument itself when it
+    already is one (numpy array or CPU tensor), else a converted copy."""
     if a is None:
         return None
+    global _TORCH_I32
+    if type(a) is np.ndarray:
+        if a.dtype == _I32 and a.flags.c_contiguous:
+            return a
+    elif type(a) in _PTR_OF_TYPE or hasattr(a, "data_ptr"):
+        if _TORCH_I32 is None:
+            import torch
+            _TORCH_I32 = torch.int32
+        if not a.is_cuda and a.dtype is _TORCH_I32 and a.is_contiguous():
+            return a
     return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
 
 

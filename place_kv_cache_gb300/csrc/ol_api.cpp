@@ -608,7 +608,7 @@ ol_status run_attention(int layout, const void* desc, const CacheView& v, const 
                         const int32_t* lens_host, const int32_t* lens_dev, const void* new_kv, int append,
                         int cur_from_new, float scale, int window, void* out, int out_dtype, void* workspace,
                         size_t ws_bytes, cudaStream_t stream, int nq = 1, bool check_only = false,
-                        const ol_page_format* new_fmt = nullptr) {
+                        const ol_page_format* new_fmt = nullptr, bool inputs_ready = false) {
   if (!q || !lens_host || !lens_dev || !out || !workspace) return OL_ERR_NULL;
   if (q_heads <= 0 || q_heads % v.kv_heads != 0) return OL_ERR_SHAPE;
   if (v.head_dim > 256) return OL_ERR_UNSUPPORTED;
@@ -716,6 +716,7 @@ ol_status run_attention(int layout, const void* desc, const CacheView& v, const 
   if (p.inline_lens)
     for (int b = 0; b < v.batch; ++b) p.lens_inline[b] = lens_host[b];
   p.early = (v.history_stable && p.inline_lens) ? 1 : 0;
+  p.inputs_ready = inputs_ready ? 1 : 0;
   char* ws = static_cast<char*>(workspace);
   p.status = reinterpret_cast<int32_t*>(ws);
   p.counters = reinterpret_cast<uint32_t*>(ws + kStatusBytes);
@@ -1148,8 +1149,12 @@ ol_status ol_decode_step_host(int32_t layout, const void* cache_desc, void* upda
   if (v.batch > kInlineRows &&
       cudaMemcpyAsync(ws + h.lens, lens_host, sizeof(int32_t) * v.batch, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return OL_ERR_CUDA;
+  // q and the new K/V are the caller's host data, written before this call, or
+  // copies ordered before the launch: the kernels may read them before they
+  // wait for the previous launch to complete
   st = run_attention(layout, cache_desc, v, q_in, q_heads, lens_host, reinterpret_cast<int32_t*>(ws + h.lens),
-                     kv_in, 1, 1, scale, window, out_to ? out_to : ws + h.out, out_dtype, workspace, h.q, s);
+                     kv_in, 1, 1, scale, window, out_to ? out_to : ws + h.out, out_dtype, workspace, h.q, s, 1,
+                     false, nullptr, /*inputs_ready=*/true);
   if (st != OL_OK || out_to) return st;
   return cudaMemcpyAsync(out_host, ws + h.out, out_bytes, cudaMemcpyDeviceToHost, s) == cudaSuccess ? OL_OK
                                                                                                  : OL_ERR_CUDA;

@@ -85,6 +85,8 @@ struct AttnParams {
 
   int inline_lens;      // 1: lengths are lens_inline (the host array, by value), lens is not read
   int early;            // 1: history rows are stable: tiles may be requested before the dependency wait
+  int inputs_ready;     // 1: q and new_kv are complete at launch (host data, or written by copies
+                        // ordered before the launch), so they may be read before the dependency wait
   int32_t lens_inline[kInlineRows];
 
   int32_t* status;      // device status word
