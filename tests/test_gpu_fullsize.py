@@ -17,25 +17,44 @@ from tests.gpu_util import check_out, out_as_f64, out_tensor, to_dev, to_host, w
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
+# the access bits bench.py gives its non-chained caches: history rows stable,
+# so the first K/V tiles are requested before the dependency wait
+STABLE = ol.OL_READ_WRITE | ol.OL_HISTORY_STABLE
 
-def _step_contiguous(case, cache):
+
+def _pinned(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+
+
+def _step_contiguous(case, cache, host):
     w = case.workload
     cache_d = to_dev(cache)
-    ws, n = workspace(w.batch, w.q_heads, w.kv_heads, w.head_dim)
-    out = out_tensor(w.batch, w.q_heads, w.head_dim, ol.OL_BF16)
-    ol.ol_decode_step(ol.OL_LAYOUT_CONTIGUOUS, ol.kv_cache(cache_d), cache_d, to_dev(case.q), w.q_heads,
-                      to_dev(case.new_kv), case.lens, to_dev(case.lens), 0.0, -1, out, ol.OL_BF16, ws, n)
-    torch.cuda.synchronize()
+    desc = ol.kv_cache(cache_d, access=STABLE)
+    if host:  # the host-buffer call bench.py's e2e times: pinned q, new K/V and y used in place
+        n = ol.ol_workspace_size_host(w.batch, w.q_heads, w.kv_heads, w.head_dim)
+        ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+        ol.ol_workspace_init(ws, n)
+        out = torch.full((w.batch, w.q_heads, w.head_dim), float("nan"), dtype=torch.bfloat16).pin_memory()
+        ol.ol_decode_step_host(ol.OL_LAYOUT_CONTIGUOUS, desc, cache_d, _pinned(case.q), w.q_heads,
+                               _pinned(case.new_kv), torch.from_numpy(case.lens), 0.0, -1, out, ol.OL_BF16, ws, n)
+        torch.cuda.synchronize()
+    else:
+        ws, n = workspace(w.batch, w.q_heads, w.kv_heads, w.head_dim)
+        out = out_tensor(w.batch, w.q_heads, w.head_dim, ol.OL_BF16)
+        ol.ol_decode_step(ol.OL_LAYOUT_CONTIGUOUS, desc, cache_d, to_dev(case.q), w.q_heads, to_dev(case.new_kv),
+                          case.lens, to_dev(case.lens), 0.0, -1, out, ol.OL_BF16, ws, n)
+        torch.cuda.synchronize()
     assert ol.ol_workspace_status(ws) == ol.OL_DEVICE_OK
     return cache_d, out_as_f64(out)
 
 
+@pytest.mark.parametrize("host", [False, True], ids=["device_buffers", "host_buffers"])
 @pytest.mark.parametrize("name", ["qwen_b1_gqa7", "ragged_b32"])
-def test_contiguous_full_size(name):
+def test_contiguous_full_size(name, host):
     w = WORKLOADS[name]
     case = make_case(w)
     cache = contiguous_cache(case)
-    cache_d, got = _step_contiguous(case, cache)
+    cache_d, got = _step_contiguous(case, cache, host)
     O.cache_update(cache, case.new_kv, case.lens - 1)          # the expected cache, in place
     np.testing.assert_array_equal(to_host(cache_d), cache)
     del cache_d
@@ -56,7 +75,8 @@ def test_paged_full_size_sampled_rows():
     bt_d = to_dev(table)
     ws, n = workspace(w.batch, w.q_heads, w.kv_heads, w.head_dim)
     out = out_tensor(w.batch, w.q_heads, w.head_dim, ol.OL_BF16)
-    ol.ol_decode_step(ol.OL_LAYOUT_PAGED, ol.paged_kv(pool_d, bt_d, table), pool_d, to_dev(case.q), w.q_heads,
+    ol.ol_decode_step(ol.OL_LAYOUT_PAGED, ol.paged_kv(pool_d, bt_d, table, access=STABLE), pool_d, to_dev(case.q),
+                      w.q_heads,
                       to_dev(case.new_kv), case.lens, to_dev(case.lens), 0.0, -1, out, ol.OL_BF16, ws, n)
     torch.cuda.synchronize()
     assert ol.ol_workspace_status(ws) == ol.OL_DEVICE_OK
