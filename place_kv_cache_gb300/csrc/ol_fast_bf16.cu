@@ -143,6 +143,37 @@ int max_cluster() {
   return cs;
 }
 
+// Clusters of cs CTAs of this kernel the device holds at once (0 if none).
+template <int NWARPS, int STAGES, bool PAGED>
+int active_clusters(int cs) {
+  static int cached[17] = {0};
+  static bool done[17] = {false};
+  if (cs < 1 || cs > 16) return 0;
+  if (!done[cs]) {
+    int n = 0;
+    if (ensure_attrs<NWARPS, STAGES, PAGED>() == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(cs, 1, 1);
+      cfg.blockDim = dim3(NWARPS * 32, 1, 1);
+      cfg.dynamicSmemBytes = FastLayout<NWARPS, STAGES>::kTotal;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = cs;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, fast_bf16_kernel<NWARPS, STAGES, PAGED>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+      }
+    }
+    cached[cs] = n;
+    done[cs] = true;
+  }
+  return cached[cs];
+}
+
 template <int NWARPS, int STAGES, bool PAGED, bool CHUNK>
 cudaError_t launch_cfg(const CUtensorMap& map, const AttnParams& p, cudaStream_t s) {
   auto kern = kernel_of<NWARPS, STAGES, PAGED, CHUNK>();
@@ -176,6 +207,7 @@ cudaError_t launch_variant(const CUtensorMap& map, const AttnParams& p, cudaStre
     case 1: return launch_cfg<4, 3, PAGED, false>(map, p, s);
     case 2: return launch_cfg<4, 2, PAGED, false>(map, p, s);
     case 3: return launch_cfg<8, 2, PAGED, false>(map, p, s);
+    case 4: return launch_cfg<6, 2, PAGED, false>(map, p, s);
     default: return launch_cfg<4, 4, PAGED, false>(map, p, s);
   }
 }
@@ -187,18 +219,30 @@ int fast_bf16_smem(int variant) {
     case 1: return FastLayout<4, 3>::kTotal;
     case 2: return FastLayout<4, 2>::kTotal;
     case 3: return FastLayout<8, 2>::kTotal;
+    case 4: return FastLayout<6, 2>::kTotal;
     default: return FastLayout<4, 4>::kTotal;
   }
 }
 
-int fast_bf16_warps(int variant) { return variant == 3 ? 8 : 4; }
+int fast_bf16_warps(int variant) { return variant == 3 ? 8 : variant == 4 ? 6 : 4; }
 
 int fast_bf16_max_cluster(int variant, bool paged) {
   switch (variant) {
     case 1: return paged ? max_cluster<4, 3, true>() : max_cluster<4, 3, false>();
     case 2: return paged ? max_cluster<4, 2, true>() : max_cluster<4, 2, false>();
     case 3: return paged ? max_cluster<8, 2, true>() : max_cluster<8, 2, false>();
+    case 4: return paged ? max_cluster<6, 2, true>() : max_cluster<6, 2, false>();
     default: return paged ? max_cluster<4, 4, true>() : max_cluster<4, 4, false>();
+  }
+}
+
+int fast_bf16_active_clusters(int variant, bool paged, int cs) {
+  switch (variant) {
+    case 1: return paged ? active_clusters<4, 3, true>(cs) : active_clusters<4, 3, false>(cs);
+    case 2: return paged ? active_clusters<4, 2, true>(cs) : active_clusters<4, 2, false>(cs);
+    case 3: return paged ? active_clusters<8, 2, true>(cs) : active_clusters<8, 2, false>(cs);
+    case 4: return paged ? active_clusters<6, 2, true>(cs) : active_clusters<6, 2, false>(cs);
+    default: return paged ? active_clusters<4, 4, true>(cs) : active_clusters<4, 4, false>(cs);
   }
 }
 

@@ -145,6 +145,7 @@ bool fast_bf16_supported(const AttnParams& p);
 int fast_bf16_smem(int variant);
 int fast_bf16_warps(int variant);
 int fast_bf16_max_cluster(int variant, bool paged);
+int fast_bf16_active_clusters(int variant, bool paged, int cs);  // clusters of cs CTAs resident at once
 cudaError_t launch_fast_bf16(const AttnParams& p, cudaStream_t s);
 bool fast_int4_supported(const AttnParams& p);
 int fast_int4_smem(int variant);
