@@ -246,16 +246,22 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
       qz[b] = c == 0 ? pack_f16x2(-qhi, -(qs - qhi)) : 0u;
     }
   }
-  // loop-invariant shared-memory offsets of the lane's reads from a stage:
-  // K word of token n, block b (token n + 8: +512); V half-words of tokens
-  // 2c, 2c+1, 2c+8, 2c+9 at dims 32b + 4n .. +3 (+0, +64, +512, +576); the
-  // warp's tile is rows 16*warp .. +15 of each plane (the 64-byte swizzle
-  // pattern repeats every 8 rows, so a tile's offsets do not depend on warp)
-  uint32_t koff[4], voff[4];
+  // The code words come from ldmatrix: the 16 bytes of block b in a token's
+  // 64-byte row are one 8 x b16 matrix row, b16 k holding dims 32b + 4k .. +3.
+  // Matrix m of a x4 load covers tokens 8(m & 1) .. +7 of block 2h + (m >> 1)
+  // (block pair h); lane l gives the address of row l % 8 of matrix l / 8 in
+  // the warp's tile (rows 16*warp .. +15 of each plane, 64-byte swizzle).
+  //   K, plain: lane (c, n) gets bytes 4c .. 4c+3 of token n (matrices 0, 2)
+  //     and of token n + 8 (1, 3): the A words of S^T = K q^T.
+  //   V, transposed: lane (c, n) gets the b16 n (dims 32b + 4n .. +3) of
+  //     tokens 2c and 2c + 1 (matrices 0, 2; tokens 2c + 8, 2c + 9 from 1, 3)
+  //     in the low and high halves: the A words of O^T += V^T P^T.
+  uint32_t kaddr[2], vaddr[2];
 #pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    koff[b] = 1024 * warp + swz64(n, 16 * b + 4 * c);
-    voff[b] = S::kCodes + 1024 * warp + swz64(2 * c, 16 * b + 2 * n);
+  for (int h = 0; h < 2; ++h) {
+    const int tok = (lane & 7) + 8 * ((lane >> 3) & 1), blk = 2 * h + (lane >> 4);
+    kaddr[h] = 1024 * warp + swz64(tok, 16 * blk);
+    vaddr[h] = S::kCodes + 1024 * warp + swz64(tok, 16 * blk);
   }
 
   float o[8][4];
@@ -279,11 +285,14 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
 
     // ---- S^T = K q^T, one accumulator per 32-dim block
     const uint32_t zda = lds_u16(kz + 2 * n) * 0x10001u, zdb = lds_u16(kz + 2 * n + 16) * 0x10001u;
+    uint32_t kw[4][2];  // [block][tokens n, n + 8]
+    ldsm_x4(sg + kaddr[0], kw[0][0], kw[0][1], kw[1][0], kw[1][1]);
+    ldsm_x4(sg + kaddr[1], kw[2][0], kw[2][1], kw[3][0], kw[3][1]);
     float sacc[4][4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       sacc[b][0] = sacc[b][1] = sacc[b][2] = sacc[b][3] = 0.f;
-      const uint32_t wa = lds_u32(sg + koff[b]), wb = lds_u32(sg + koff[b] + 512);
+      const uint32_t wa = kw[b][0], wb = kw[b][1];
       const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
       mma_f16_16816(sacc[b], wa & kLoNib, wb & kLoNib, wa & kHiNib, wb & kHiNib, qf[b][0][0], qf[b][0][1]);
       mma_f16_16816(sacc[b], wa8 & kLoNib, wb8 & kLoNib, wa8 & kHiNib, wb8 & kHiNib, qf[b][1][0], qf[b][1][1]);
@@ -352,6 +361,9 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
     // zero points of the lane's V^T columns: tokens (2c, 2c+1) and (2c+8, 2c+9)
     // in the two 16-bit halves
     const uint32_t zv01 = lds_u32(vz + 4 * c), zv89 = lds_u32(vz + 4 * c + 16);
+    uint32_t vw[4][2];  // [block][tokens (2c, 2c+1), (2c+8, 2c+9)]
+    ldsm_x4_trans(sg + vaddr[0], vw[0][0], vw[0][1], vw[1][0], vw[1][1]);
+    ldsm_x4_trans(sg + vaddr[1], vw[2][0], vw[2][1], vw[3][0], vw[3][1]);
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       const float sca = b == 0 ? va01.x : b == 1 ? va01.y : b == 2 ? va23.x : va23.y;
@@ -362,9 +374,7 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
       const uint32_t l1 = pack_bf16x2(q10 - __uint_as_float(h1 << 16), q11 - __uint_as_float(h1 & 0xffff0000u));
       const uint32_t ph0 = movmatrix_trans(h0), ph1 = movmatrix_trans(h1);
       const uint32_t pl0 = movmatrix_trans(l0), pl1 = movmatrix_trans(l1);
-      const uint32_t vrow = sg + voff[b];
-      const uint32_t w01 = __byte_perm(lds_u16(vrow), lds_u16(vrow + 64), 0x5410);
-      const uint32_t w89 = __byte_perm(lds_u16(vrow + 512), lds_u16(vrow + 576), 0x5410);
+      const uint32_t w01 = vw[b][0], w89 = vw[b][1];
       const uint32_t z01 = code_pair(zv01, 4 * b), z89 = code_pair(zv89, 4 * b);  // (128 + zp) per token
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
