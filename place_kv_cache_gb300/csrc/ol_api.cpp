@@ -56,7 +56,7 @@ bool valid_dtype(int d) { return d == OL_F32 || d == OL_BF16; }
 // Launch tuning: OL_TUNE="waves=<w>,minchunk=<c>,cfg=<variant>,cluster=<cs>,cpu=<k>,generic=<0|1>,hpwaves=<w>,
 // cwaves=<w>" (read once).
 struct Tune {
-  int waves = 2;
+  int waves = -1;  // CTA waves of a split plan without clusters; -1 = by layout (measured best)
   int min_chunk = 16;
   int cfg = -1;      // tensor-core kernel variant; -1 = default
   int cluster = -1;  // cluster size cap; -1 = automatic
@@ -178,7 +178,10 @@ void plan_fast(AttnParams& p, const int32_t* lens_host, int sms, int force_varia
     }
   }
   if (units >= sms || units == 0) {
-    plan_splits(p, lens_host, slots * (p.nq > 1 ? tune().chunk_waves : tune().waves), 1);
+    // CTA waves: contiguous caches 2 (ragged_b32: 83.6 us/step; 1 wave 86.8, 3 85.5);
+    // paged pools 4 (paged_b64: 352.5; 2 waves 364, 3 354.4, 5 356.2)
+    const int waves = tune().waves > 0 ? tune().waves : (p.layout == OL_LAYOUT_PAGED ? 4 : 2);
+    plan_splits(p, lens_host, slots * (p.nq > 1 ? tune().chunk_waves : waves), 1);
     return;
   }
   int cs = pow2_floor(slots / units);
