@@ -221,6 +221,24 @@ void plan_fast(AttnParams& p, const int32_t* lens_host, int sms, int force_varia
   }
 }
 
+// Launch order of the rows of a split plan (lengths carried by value): rows
+// by descending tiles per CTA, so the longest CTAs start in the first wave and
+// the short ones fill the tail (longest first). Stream-K plans balance by
+// construction and keep row order.
+void order_rows(AttnParams& p, const int32_t* lens_host) {
+  p.ordered = 0;
+  if (!p.inline_lens || p.streamk || p.batch < 2) return;
+  std::vector<std::pair<int, int>> key(p.batch);  // (tiles per CTA, row)
+  for (int b = 0; b < p.batch; ++b) {
+    const RowSplit rs = row_split(lens_host[b], p.window, p.chunk, p.cluster);
+    key[b] = {rs.nsplit > 0 ? (rs.ntiles + rs.nsplit - 1) / rs.nsplit : 0, b};
+  }
+  std::stable_sort(key.begin(), key.end(),
+                   [](const std::pair<int, int>& x, const std::pair<int, int>& y) { return x.first > y.first; });
+  for (int i = 0; i < p.batch; ++i) p.row_order[i] = (int16_t)key[i].second;
+  p.ordered = 1;
+}
+
 int sm_count_cached() {
   static int cached[64] = {0};
   int dev = 0;
@@ -745,16 +763,20 @@ ol_status run_attention(int layout, const void* desc, const CacheView& v, const 
     // a chunk's query tokens share a CTA as extra MMA columns: 8 / group of them
     if (nq > 1) p.tq = std::max(1, std::min(nq, 8 / p.group));
     plan_fast(p, lens_host, sms);
+    order_rows(p, lens_host);
     e = launch_fast_bf16(p, stream);
   } else if (layout == OL_LAYOUT_INT4 && fast_int4_supported(p)) {
     plan_fast(p, lens_host, sms);
+    order_rows(p, lens_host);
     e = launch_fast_int4(p, stream);
   } else if (layout == OL_LAYOUT_HPAGED && fast_hpaged_supported(p) && !tune().generic) {
     plan_splits(p, lens_host, (long long)sms * fast_hpaged_ctas_per_sm() * tune().hp_waves, 1);
+    order_rows(p, lens_host);
     p.variant = 0;
     e = launch_fast_hpaged(p, stream);
   } else {
     plan_splits(p, lens_host, (long long)sms * 4, 1);
+    order_rows(p, lens_host);
     p.variant = 0;
     e = launch_generic_attention(p, stream);
   }

@@ -206,10 +206,13 @@ struct Work {
   int valid;
 };
 
-// Computed by one full warp; every lane returns the same Work.
+// Computed by one full warp; every lane returns the same Work. CTAs go to the
+// rows in the order `order` (a permutation of 0 .. batch - 1; NULL = row
+// index order), the splits of one (row, kv head) on consecutive CTAs.
 __device__ __forceinline__ Work map_cta_warp(const int32_t* __restrict__ lens, int batch, int kv_heads,
                                              int capacity, int window, int chunk, int cta,
-                                             int32_t* status, int cluster = 1) {
+                                             int32_t* status, int cluster = 1,
+                                             const int16_t* __restrict__ order = nullptr) {
   const int lane = threadIdx.x & 31;
   Work w;
   w.valid = 0;
@@ -220,9 +223,17 @@ __device__ __forceinline__ Work map_cta_warp(const int32_t* __restrict__ lens, i
   w.next = -1;
   int running = 0;
   for (int base = 0; base < batch; base += 32) {
-    int b = base + lane;
+    const int i = base + lane;  // position in the launch order
+    int b = i;
+    if (order && i < batch) {
+      b = order[i];
+      if (b < 0 || b >= batch) {
+        set_status(status, OL_DEVICE_GUARD);
+        b = 0;
+      }
+    }
     int n = 0;
-    if (b < batch) {
+    if (i < batch) {
       n = lens[b];
       if (n < 0 || n > capacity) {
         set_status(status, OL_DEVICE_GUARD);
@@ -230,7 +241,7 @@ __device__ __forceinline__ Work map_cta_warp(const int32_t* __restrict__ lens, i
       }
     }
     RowSplit rs = row_split(n, window, chunk, cluster);
-    int cnt = (b < batch) ? rs.nsplit * kv_heads : 0;
+    int cnt = (i < batch) ? rs.nsplit * kv_heads : 0;
     int incl = cnt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -243,7 +254,7 @@ __device__ __forceinline__ Work map_cta_warp(const int32_t* __restrict__ lens, i
       unsigned hit = __ballot_sync(0xffffffffu, cnt > 0 && cta >= running + excl && cta < running + incl);
       int src = __ffs(hit) - 1;
       int within = cta - running - __shfl_sync(0xffffffffu, excl, src);
-      w.b = base + src;
+      w.b = __shfl_sync(0xffffffffu, b, src);
       w.nsplit = __shfl_sync(0xffffffffu, rs.nsplit, src);
       w.lo = __shfl_sync(0xffffffffu, rs.lo, src);
       w.hi = __shfl_sync(0xffffffffu, rs.hi, src);

@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
   pdl_launch_dependents();
   if (warp == 0) {
     Work w = p.inline_lens ? map_cta_warp(p.lens_inline, p.batch, p.kv_heads, p.capacity, p.window, p.chunk,
-                                          blockIdx.x, nullptr)
+                                          blockIdx.x, nullptr, 1, p.ordered ? p.row_order : nullptr)
                            : map_cta_warp(p.lens, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, blockIdx.x,
                                           p.status);
     if (lane == 0) *sw = w;

@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
     Work w = p.streamk ? map_streamk_warp(lens, p.batch, p.kv_heads, p.capacity, p.window, p.total_ctas,
                                           blockIdx.x, next, lens_status)
                        : map_cta_warp(lens, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, blockIdx.x,
-                                      lens_status, CS);
+                                      lens_status, CS, p.inline_lens && p.ordered ? p.row_order : nullptr);
     if (lane == 0) *sw = w;
   }
   __syncthreads();

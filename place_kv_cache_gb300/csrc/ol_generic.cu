@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kGenWarps * 32) generic_attn_kernel(const __gr
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 0) {
     Work w = p.inline_lens ? map_cta_warp(p.lens_inline, p.batch, p.kv_heads, p.capacity, p.window, p.chunk,
-                                          cta_index(p), nullptr)
+                                          cta_index(p), nullptr, 1, p.ordered ? p.row_order : nullptr)
                            : map_cta_warp(p.lens, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, cta_index(p),
                                           p.status);
     const int row_hi = w.hi;  // the row's length: its new tokens are the last max(nq, 1)

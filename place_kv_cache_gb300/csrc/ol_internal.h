@@ -88,6 +88,8 @@ struct AttnParams {
   int inputs_ready;     // 1: q and new_kv are complete at launch (host data, or written by copies
                         // ordered before the launch), so they may be read before the dependency wait
   int32_t lens_inline[kInlineRows];
+  int ordered;          // 1: row_order holds the launch order of the rows (inline lengths only)
+  int16_t row_order[kInlineRows];  // CTAs are assigned to rows in this order (longest work first)
 
   int32_t* status;      // device status word
   uint32_t* counters;   // [B * Hkv]
