@@ -62,7 +62,8 @@ struct Tune {
   int cluster = -1;  // cluster size cap; -1 = automatic
   int clusters_per_unit = -1;  // cap on clusters per (row, kv head) for small batches
   bool generic = false;        // heterogeneous pages: the CUDA-core kernel even where the tensor-core one applies
-  int hp_waves = 4;            // heterogeneous pages: CTA waves of the split plan (measured best on hpaged_b64)
+  int hp_waves = 1;            // heterogeneous pages: CTA waves of the split plan (hpaged_b64, rows
+                               // longest-first: 1 wave 287.5 us/step, 2 299.1, 3 310.3, 4 308.3)
   int chunk_waves = 1;         // chunked steps on tensor cores (measured best on chunk4_b32)
 };
 const Tune& tune() {
@@ -178,9 +179,11 @@ void plan_fast(AttnParams& p, const int32_t* lens_host, int sms, int force_varia
     }
   }
   if (units >= sms || units == 0) {
-    // CTA waves: contiguous caches 2 (ragged_b32: 83.6 us/step; 1 wave 86.8, 3 85.5);
-    // paged pools 4 (paged_b64: 352.5; 2 waves 364, 3 354.4, 5 356.2)
-    const int waves = tune().waves > 0 ? tune().waves : (p.layout == OL_LAYOUT_PAGED ? 4 : 2);
+    // CTA waves, measured with the rows launched longest-first: contiguous
+    // caches 1 (ragged_b32: 79.5 us/step; 2 waves 84.1, 3 87.5), paged pools 2
+    // (paged_b64: 345.4; 3 waves 345.4, 4 346.8, 6 350.7), INT4 2
+    const int waves = tune().waves > 0 ? tune().waves
+                                       : (p.layout == OL_LAYOUT_CONTIGUOUS ? 1 : 2);
     plan_splits(p, lens_host, slots * (p.nq > 1 ? tune().chunk_waves : waves), 1);
     return;
   }
