@@ -388,38 +388,10 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
     }
   };
 
-  for (int j = 0; j < nstage; ++j) {
-    const int tile_idx = j * NWARPS + warp;
-    if (tile_idx >= nsub) break;  // the last stage may hold fewer tiles
-    const int st = (jbase + j) % STAGES;
-    if (!mbar_wait_bounded(bar0 + 8 * st, ((jbase + j) / STAGES) & 1)) {
-      if (lane == 0) set_status(p.status, OL_DEVICE_GUARD);
-      break;
-    }
-    const int t0 = w.t_begin + tile_idx * kTok;
-    const uint32_t sg = smem_u32(stages + st * S::kBytes);
-    if (t0 >= w.lo && t0 + kTok <= t_stop)
-      tile(sg, t0, std::true_type{});
-    else
-      tile(sg, t0, std::false_type{});
-    if (j + STAGES < nstage) {  // every warp has a tile in this stage
-      __syncwarp();
-      if (lane == 0) {
-        __threadfence_block();  // this warp's reads of the stage come first
-        if (atomicAdd(freed + st, 1) == NWARPS - 1) {
-          freed[st] = 0;
-          fence_proxy_async_smem();  // the generic reads before the async-proxy refill
-          issue(j + STAGES);
-        }
-      }
-    }
-  }
-  __syncthreads();  // all stages consumed: they now hold the warps' states
-
-  store_warp_state<true>(reinterpret_cast<float*>(stages + warp * kStateBytes), ms, warp, o, m_run0, m_run1, l_run0, l_run1);
-
   // The token being appended (if this CTA's range holds it): attended from
-  // new_kv uncompressed as one more merge state, and quantized into the cache.
+  // new_kv uncompressed as one more merge state (formed here, before the
+  // tiles, so its loads overlap theirs), and quantized into the cache after
+  // every tile is consumed.
   const int cur = p.cur_from_new ? w.hi - 1 : -1;
   const bool has_cur = w.valid && cur >= w.t_begin && cur < w.t_end;
   if (has_cur && warp == 0) {
@@ -450,6 +422,36 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
       }
     }
   }
+  for (int j = 0; j < nstage; ++j) {
+    const int tile_idx = j * NWARPS + warp;
+    if (tile_idx >= nsub) break;  // the last stage may hold fewer tiles
+    const int st = (jbase + j) % STAGES;
+    if (!mbar_wait_bounded(bar0 + 8 * st, ((jbase + j) / STAGES) & 1)) {
+      if (lane == 0) set_status(p.status, OL_DEVICE_GUARD);
+      break;
+    }
+    const int t0 = w.t_begin + tile_idx * kTok;
+    const uint32_t sg = smem_u32(stages + st * S::kBytes);
+    if (t0 >= w.lo && t0 + kTok <= t_stop)
+      tile(sg, t0, std::true_type{});
+    else
+      tile(sg, t0, std::false_type{});
+    if (j + STAGES < nstage) {  // every warp has a tile in this stage
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();  // this warp's reads of the stage come first
+        if (atomicAdd(freed + st, 1) == NWARPS - 1) {
+          freed[st] = 0;
+          fence_proxy_async_smem();  // the generic reads before the async-proxy refill
+          issue(j + STAGES);
+        }
+      }
+    }
+  }
+  __syncthreads();  // all stages consumed: they now hold the warps' states
+
+  store_warp_state<true>(reinterpret_cast<float*>(stages + warp * kStateBytes), ms, warp, o, m_run0, m_run1, l_run0, l_run1);
+
   __syncthreads();  // every tile is consumed: the appended row may be rewritten
   if (has_cur && p.append && warp < 2) {
     const int plane = warp;
