@@ -1166,6 +1166,10 @@ ol_status ol_decode_step_host(int32_t layout, const void* cache_desc, void* upda
   const size_t q_bytes = (size_t)v.batch * q_heads * v.head_dim * in_elt;
   const size_t kv_bytes = 2ull * v.batch * v.kv_heads * v.head_dim * in_elt;
   const size_t out_bytes = (size_t)v.batch * q_heads * v.head_dim * elt_bytes(out_dtype);
+  // y must not overlap the step's inputs, whichever way each buffer travels
+  if (overlaps(range_of(out_host, out_bytes), range_of(q_host, q_bytes)) ||
+      overlaps(range_of(out_host, out_bytes), range_of(new_kv_host, kv_bytes)))
+    return OL_ERR_ALIAS;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // Mapped page-locked buffers are used in place: the step's kernels load q

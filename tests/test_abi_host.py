@@ -272,6 +272,11 @@ def test_host_step_rejects_before_any_copy():
     assert status_of(host_step, ws=WS + 8) == ol.OL_ERR_ALIGN
     ro = ol.kv_cache(CACHE, dims=(B, HKV, C, D), dtype=ol.OL_BF16, access=ol.OL_READ_ONLY)
     assert status_of(host_step, desc=ro) == ol.OL_ERR_READONLY
+    # y overlapping q or the new K/V in host memory
+    shared = np.zeros((2, B, HQ, D), np.uint16)
+    assert status_of(host_step, q=shared[0], out=shared[0]) == ol.OL_ERR_ALIAS
+    assert status_of(host_step, kv=shared.reshape(-1)[: 2 * B * HKV * D].reshape(2, B, HKV, 1, D),
+                     out=shared[0]) == ol.OL_ERR_ALIAS
     lib = ol.load()
     d = ol.kv_cache(CACHE, dims=(B, HKV, C, D), dtype=ol.OL_BF16)
     import ctypes
