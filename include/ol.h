@@ -500,7 +500,7 @@ OL_API size_t ol_workspace_size_host(int32_t batch, int32_t q_heads, int32_t kv_
  * The lengths travel in the launch for up to 160 rows, else by one copy.
  * Everything is asynchronous: out_host holds y once `stream` has been
  * synchronized, and the host buffers must stay valid and unchanged until
- * then; out_host must not overlap q_host or new_kv_host. The cache stays in
+ * then; out_host overlapping q_host or new_kv_host is OL_ERR_ALIAS. The cache stays in
  * device memory, described as for ol_decode_step. ws_bytes must be at least
  * ol_workspace_size_host(batch, q_heads, kv_heads, head_dim).
  * Errors: those of ol_decode_step (the descriptor, host pointers, lengths and
