@@ -3,7 +3,9 @@ invariants checked over drawn shapes (batch, kv heads, query group, head_dim,
 capacity, per-row lengths, window), so that an index or stride mistake that
 one fixed shape happens to hide (rows and kv heads mixed up, a group mapped
 to the wrong kv head, a window off by one at a row boundary) fails here.
-Every expected value is a closed form of the definition, not the oracle.
+Every expected value is a closed form of the definition, an invariant, or
+(for chunked steps) a masked-softmax brute force written here, not the
+oracle.
 """
 import numpy as np
 import pytest
@@ -138,3 +140,35 @@ def test_paged_layout_equals_contiguous_for_any_page_placement(s, S):
             pool[:, table[b, t // S], :, t % S] = cache[:, b, :, t]
     np.testing.assert_array_equal(O.paged_attention(q, pool, table, lens, window=window),
                                   O.decode_attention(q, cache, lens, window=window))
+
+
+def _masked_softmax_attention(q, k, v, pos, scale, window):
+    """Score matrix with a causal (and left-window) mask, row softmax, weighted
+    sum, in float64; written independently of the oracle. q [T, D]; k, v
+    [C, D]; pos [T] query positions."""
+    s = (q @ k.T) * scale
+    t = np.arange(k.shape[0])[None, :]
+    lo = pos[:, None] - (window if window >= 0 else 10 ** 9)
+    s = np.where((t <= pos[:, None]) & (t >= lo), s, -np.inf)
+    w = np.exp(s - s.max(axis=1, keepdims=True))
+    return (w / w.sum(axis=1, keepdims=True)) @ v
+
+
+@SETTINGS
+@given(shapes(), st.integers(1, 5), st.floats(0.05, 2.0))
+def test_chunk_attention_equals_masked_softmax_over_drawn_shapes(s, T, scale):
+    # a chunk of T tokens per row (rows at least T long), any explicit scale
+    B, Hkv, G, D, C, lens, window, seed = s
+    C = max(C, T)
+    lens = np.maximum(np.minimum(lens, C), T).astype(np.int32)
+    rng = np.random.default_rng(seed)
+    cache = rng.uniform(-2, 2, size=(2, B, Hkv, C, D)).astype(np.float32)
+    q = rng.uniform(-2, 2, size=(B, Hkv * G, T, D)).astype(np.float32)
+    y = O.chunk_attention(q, cache, lens, T, scale=scale, window=window)
+    for b in range(B):
+        pos = lens[b] - T + np.arange(T)
+        for h in range(Hkv * G):
+            g = h // G
+            want = _masked_softmax_attention(q[b, h].astype(np.float64), cache[0, b, g].astype(np.float64),
+                                             cache[1, b, g].astype(np.float64), pos, scale, window)
+            np.testing.assert_allclose(y[b, h], want, rtol=0, atol=1e-12)
