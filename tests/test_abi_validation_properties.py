@@ -1,0 +1,100 @@
+"""Randomised CPU tests of the host validation of ol_decode_step (row a1 of
+the path: pointer identity, capacity, no buffer over the cache, alignment,
+workspace size): drawn shapes and lengths, with at most one violation
+planted per request, must give exactly the status the rule names, and every
+clean request must pass validation. No GPU is touched: device pointers are
+fake aligned addresses, and requests that pass validation stop at the host
+fault-injection switch (OL_FAULT_INJECT) before any CUDA call.
+"""
+import numpy as np
+import pytest
+
+hyp = pytest.importorskip("hypothesis")
+from hypothesis import given, settings, strategies as st  # noqa: E402
+
+import place_kv_cache_gb300 as ol  # noqa: E402
+
+BASE = 0x7E0000000000   # fake device address space
+GB = 1 << 30
+
+VIOLATIONS = {
+    "none": ol.OL_ERR_INJECTED,
+    "len_zero": ol.OL_ERR_CAPACITY,
+    "len_over_capacity": ol.OL_ERR_CAPACITY,
+    "updated_is_another_pointer": ol.OL_ERR_ALIAS,
+    "q_inside_cache": ol.OL_ERR_ALIAS,
+    "new_kv_inside_cache": ol.OL_ERR_ALIAS,
+    "out_inside_cache": ol.OL_ERR_ALIAS,
+    "workspace_inside_cache": ol.OL_ERR_ALIAS,
+    "out_over_q": ol.OL_ERR_ALIAS,
+    "q_misaligned": ol.OL_ERR_ALIGN,
+    "out_misaligned": ol.OL_ERR_ALIGN,
+    "workspace_too_small": ol.OL_ERR_WORKSPACE,
+    "q_heads_not_a_multiple": ol.OL_ERR_SHAPE,
+}
+
+
+@pytest.fixture(autouse=True)
+def _inject(monkeypatch):
+    monkeypatch.setenv("OL_FAULT_INJECT", "after_validate")
+    yield
+
+
+@st.composite
+def requests(draw):
+    B = draw(st.integers(1, 6))
+    Hkv = draw(st.integers(1, 4))
+    G = draw(st.integers(1, 8))
+    D = draw(st.sampled_from([64, 128]))
+    C = draw(st.integers(16, 4096))
+    lens = draw(st.lists(st.integers(1, C), min_size=B, max_size=B))
+    violation = draw(st.sampled_from(sorted(VIOLATIONS)))
+    row = draw(st.integers(0, B - 1))
+    offset = draw(st.integers(0, 1 << 20))       # where inside the cache a stray buffer starts
+    return B, Hkv, G, D, C, lens, violation, row, offset
+
+
+@settings(max_examples=300, deadline=None, derandomize=True)
+@given(requests())
+def test_each_rule_gives_its_status(r):
+    B, Hkv, G, D, C, lens, violation, row, offset = r
+    cache_bytes = 2 * B * Hkv * C * D * 2
+    cache = BASE
+    q, new_kv, out, lens_dev, ws = (BASE + k * GB for k in (1, 2, 3, 4, 5))
+    ws_bytes = ol.ol_workspace_size(B, Hkv * G, Hkv, D)
+    q_heads = Hkv * G
+    updated = cache
+    inside = cache + (offset % cache_bytes) // 16 * 16    # an aligned address inside the cache
+    lens = list(lens)
+    if violation == "len_zero":
+        lens[row] = 0
+    elif violation == "len_over_capacity":
+        lens[row] = C + 1
+    elif violation == "updated_is_another_pointer":
+        updated = cache + 16 * (1 + offset % 64)
+    elif violation == "q_inside_cache":
+        q = inside
+    elif violation == "new_kv_inside_cache":
+        new_kv = inside
+    elif violation == "out_inside_cache":
+        out = inside
+    elif violation == "workspace_inside_cache":
+        ws = inside
+    elif violation == "out_over_q":
+        out = q + 16 * (offset % 8)
+    elif violation == "q_misaligned":
+        q += 8
+    elif violation == "out_misaligned":
+        out += 4
+    elif violation == "workspace_too_small":
+        ws_bytes -= 1 + offset % 64
+    elif violation == "q_heads_not_a_multiple":
+        q_heads = Hkv * G + 1 if Hkv > 1 else 0
+    desc = ol.kv_cache(cache, dims=(B, Hkv, C, D), dtype=ol.OL_BF16)
+    try:
+        ol.ol_decode_step(ol.OL_LAYOUT_CONTIGUOUS, desc, updated, q, q_heads, new_kv, np.array(lens, np.int32),
+                          lens_dev, 0.0, -1, out, ol.OL_BF16, ws, ws_bytes, stream=0)
+        status = ol.OL_OK
+    except ol.OlError as e:
+        status = e.status
+    assert status == VIOLATIONS[violation], (violation, status)
