@@ -98,3 +98,66 @@ def test_each_rule_gives_its_status(r):
     except ol.OlError as e:
         status = e.status
     assert status == VIOLATIONS[violation], (violation, status)
+
+
+@st.composite
+def paged_requests(draw):
+    B = draw(st.integers(1, 4))
+    Hkv = draw(st.integers(1, 3))
+    G = draw(st.integers(1, 4))
+    S = draw(st.sampled_from([16, 32]))
+    M = draw(st.integers(1, 8))
+    P = B * M + draw(st.integers(0, 16))
+    lens = draw(st.lists(st.integers(1, M * S), min_size=B, max_size=B))
+    case = draw(st.sampled_from(["none", "page_out_of_pool", "page_out_of_pool_not_reached", "append_page_shared",
+                                 "history_page_shared", "over_capacity", "updated_is_another_pointer"]))
+    seed = draw(st.integers(0, 2**31 - 1))
+    return B, Hkv, G, S, M, P, lens, case, seed
+
+
+@settings(max_examples=300, deadline=None, derandomize=True)
+@given(paged_requests())
+def test_paged_page_rules_give_their_status(r):
+    # a fused step appends at lens - 1 and reads [0, lens - 1): every page a
+    # row reaches must lie in the pool, and no row may append into a page
+    # another row also reaches; pages beyond a row's length are never looked at
+    # and rows may share pages they only read
+    B, Hkv, G, S, M, P, lens, case, seed = r
+    rng = np.random.default_rng(seed)
+    D = 128
+    table = rng.permutation(P)[:B * M].reshape(B, M).astype(np.int32)   # distinct pages
+    lens = list(lens)
+    reached = [(n - 1) // S for n in lens]                               # last page index each row reaches
+    pool, bt = BASE, BASE + 6 * GB
+    updated = pool
+    want = ol.OL_ERR_INJECTED
+    b = int(rng.integers(B))
+    if case == "page_out_of_pool":
+        table[b, int(rng.integers(reached[b] + 1))] = P if rng.integers(2) else -1
+        want = ol.OL_ERR_PAGE
+    elif case == "page_out_of_pool_not_reached" and reached[b] + 1 < M:
+        table[b, int(rng.integers(reached[b] + 1, M))] = P
+    elif case == "append_page_shared" and B > 1:
+        other = (b + 1 + int(rng.integers(B - 1))) % B
+        table[other, int(rng.integers(reached[other] + 1))] = table[b, reached[b]]
+        want = ol.OL_ERR_PAGE
+    elif case == "history_page_shared" and B > 1:
+        other = (b + 1 + int(rng.integers(B - 1))) % B
+        if reached[b] >= 1 and reached[other] >= 1:                      # neither row appends into it
+            table[other, int(rng.integers(reached[other]))] = table[b, int(rng.integers(reached[b]))]
+    elif case == "over_capacity":
+        lens[b] = M * S + 1
+        want = ol.OL_ERR_CAPACITY
+    elif case == "updated_is_another_pointer":
+        updated = pool + 16
+        want = ol.OL_ERR_ALIAS
+    desc = ol.paged_kv(pool, bt, table, dims=(P, Hkv, S, D), dtype=ol.OL_BF16)
+    q, new_kv, out, lens_dev, ws = (BASE + k * GB for k in (1, 2, 3, 4, 5))
+    try:
+        ol.ol_decode_step(ol.OL_LAYOUT_PAGED, desc, updated, q, Hkv * G, new_kv, np.array(lens, np.int32),
+                          lens_dev, 0.0, -1, out, ol.OL_BF16, ws, ol.ol_workspace_size(B, Hkv * G, Hkv, D),
+                          stream=0)
+        status = ol.OL_OK
+    except ol.OlError as e:
+        status = e.status
+    assert status == want, (case, status)
