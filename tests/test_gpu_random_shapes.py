@@ -1,0 +1,90 @@
+"""A seeded random sweep of the fused decode step on the GPU against the CPU
+oracle: contiguous caches and paged pools with drawn batch, kv heads, query
+group (1-8, the tensor-core range), head_dim (128, and 64 on the CUDA-core
+kernel), capacity or page geometry, ragged lengths (1 and the full capacity
+included), windows and the history-stable access bit. The planner picks the
+kernel variant, cluster size, split count and launch order per shape, so the
+sweep reaches combinations the hand-picked shapes do not. Every cache byte
+must match the oracle's append and every output the oracle's attention within
+the tolerance of the other parity tests.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+import place_kv_cache_gb300 as ol
+from workloads import Workload, block_table, contiguous_cache, make_case, poisoned_pool
+from tests.gpu_util import check_out, out_as_f64, out_tensor, to_dev, to_host, workspace
+
+pytestmark = pytest.mark.gpu
+
+
+def draw_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        layout = "paged" if rng.integers(2) else "contiguous"
+        B = int(rng.integers(1, 7))
+        Hkv = int(rng.integers(1, 9))
+        G = int(rng.integers(1, 9))
+        D = 128 if rng.random() < 0.85 else 64
+        window = int(rng.choice([-1, -1, 0, 1, 15, 100]))
+        stable = bool(rng.integers(2))
+        if layout == "contiguous":
+            C = int(rng.integers(16, 2049))
+            S = M = P = 0
+        else:
+            S = int(rng.choice([16, 32]))
+            M = int(rng.integers(1, 65))
+            C = S * M
+            P = B * M + int(rng.integers(0, 32))
+        lens = rng.integers(1, C + 1, size=B)
+        if B > 1:                      # edge rows: a single token, and a full row
+            lens[int(rng.integers(B))] = 1
+            lens[int(rng.integers(B))] = C
+        cases.append(dict(id=f"{i:02d}-{layout}-B{B}-H{Hkv}x{G}-D{D}-C{C}-w{window}{'-stable' if stable else ''}",
+                          layout=layout, B=B, Hkv=Hkv, G=G, D=D, C=C, S=S, M=M, P=P,
+                          lens=lens.astype(np.int32), window=window, stable=stable, seed=int(rng.integers(1 << 30))))
+    return cases
+
+
+CASES = draw_cases(48, 2026)
+
+
+@pytest.mark.parametrize("c", CASES, ids=[c["id"] for c in CASES])
+def test_random_shape_fused_step(c):
+    B, Hkv, G, D, C, lens, window = c["B"], c["Hkv"], c["G"], c["D"], c["C"], c["lens"], c["window"]
+    Hq = Hkv * G
+    access = ol.OL_READ_WRITE | (ol.OL_HISTORY_STABLE if c["stable"] else 0)
+    ws, n = workspace(B, Hq, Hkv, D)
+    out = out_tensor(B, Hq, D, ol.OL_BF16)
+    if c["layout"] == "contiguous":
+        w = Workload("rnd", "bf16", B, Hq, Hkv, D, C, "contiguous", seed=c["seed"])
+        case = make_case(w, lens=lens)
+        cache = contiguous_cache(case)
+        cache_d = to_dev(cache)
+        ol.ol_decode_step(ol.OL_LAYOUT_CONTIGUOUS, ol.kv_cache(cache_d, access=access), cache_d, to_dev(case.q), Hq,
+                          to_dev(case.new_kv), lens, to_dev(lens), 0.0, window, out, ol.OL_BF16, ws, n)
+        got = out_as_f64(out)
+        O.cache_update(cache, case.new_kv, lens - 1)
+        np.testing.assert_array_equal(to_host(cache_d), cache)
+        want = O.decode_attention(case.q, cache, lens, window=window)
+    else:
+        w = Workload("rnd", "bf16", B, Hq, Hkv, D, C, "paged", seed=c["seed"], page_size=c["S"], num_pages=c["P"],
+                     lens_range=(1, C))
+        case = make_case(w, lens=lens)
+        table = block_table(case)
+        pool = poisoned_pool(w)
+        for b, h in enumerate(case.history):
+            if h.shape[2]:
+                O.paged_update(pool, table[b:b + 1], h[:, None], [0])
+        pool_d = to_dev(pool)
+        desc = ol.paged_kv(pool_d, to_dev(table), table, access=access)
+        ol.ol_decode_step(ol.OL_LAYOUT_PAGED, desc, pool_d, to_dev(case.q), Hq, to_dev(case.new_kv), lens,
+                          to_dev(lens), 0.0, window, out, ol.OL_BF16, ws, n)
+        got = out_as_f64(out)
+        O.paged_update(pool, table, case.new_kv, lens - 1)
+        np.testing.assert_array_equal(to_host(pool_d), pool)
+        want = O.paged_attention(case.q, pool, table, lens, window=window)
+    assert ol.ol_workspace_status(ws) == ol.OL_DEVICE_OK
+    check_out(got, want, ol.OL_BF16)
