@@ -1,4 +1,4 @@
-"""A seeded random sweep of the fused decode step on the GPU against the CPU
+"""Seeded random sweeps of the fused decode step on the GPU against the CPU
 oracle: contiguous caches and paged pools with drawn batch, kv heads, query
 group (1-8, the tensor-core range), head_dim (128, and 64 on the CUDA-core
 kernel), capacity or page geometry, ragged lengths (1 and the full capacity
@@ -88,3 +88,58 @@ def test_random_shape_fused_step(c):
         want = O.paged_attention(case.q, pool, table, lens, window=window)
     assert ol.ol_workspace_status(ws) == ol.OL_DEVICE_OK
     check_out(got, want, ol.OL_BF16)
+
+
+def draw_int4_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        B = int(rng.integers(1, 7))
+        Hkv = int(rng.integers(1, 9))
+        G = int(rng.integers(1, 9))
+        D = 128 if rng.random() < 0.8 else 64
+        C = int(rng.integers(16, 1501))
+        window = int(rng.choice([-1, -1, 0, 3, 40]))
+        mode = O.Q_FIXED if rng.random() < 0.3 else O.Q_DYNAMIC
+        lens = rng.integers(1, C + 1, size=B)
+        if B > 1:
+            lens[int(rng.integers(B))] = 1
+            lens[int(rng.integers(B))] = C
+        cases.append(dict(id=f"{i:02d}-int4-B{B}-H{Hkv}x{G}-D{D}-C{C}-w{window}-{'fixed' if mode == O.Q_FIXED else 'dyn'}",
+                          B=B, Hkv=Hkv, G=G, D=D, C=C, lens=lens.astype(np.int32), window=window, mode=mode,
+                          seed=int(rng.integers(1 << 30))))
+    return cases
+
+
+INT4_CASES = draw_int4_cases(24, 2027)
+
+
+@pytest.mark.parametrize("c", INT4_CASES, ids=[c["id"] for c in INT4_CASES])
+def test_random_shape_int4_step(c):
+    # the fused INT4 step: the new token quantized into the planes (bit-exact
+    # with the oracle's encoding), history attended from the codes, the
+    # current token uncompressed
+    B, Hkv, G, D, C, lens, window, mode = c["B"], c["Hkv"], c["G"], c["D"], c["C"], c["lens"], c["window"], c["mode"]
+    Hq = Hkv * G
+    w = Workload("rnd4", "bf16", B, Hq, Hkv, D, C, "int4", seed=c["seed"])
+    case = make_case(w, lens=lens)
+    planes = O.int4_planes(B, Hkv, C, D)
+    for b, h in enumerate(case.history):
+        if h.shape[2]:
+            sub = O.int4_planes(1, Hkv, C, D)
+            O.int4_append(*sub, h[:, None], [0], mode=mode)
+            for full, part in zip(planes, sub):
+                full[:, b] = part[:, 0]
+    dplanes = tuple(to_dev(p) for p in planes)
+    ws, n = workspace(B, Hq, Hkv, D)
+    out = out_tensor(B, Hq, D, ol.OL_F32)
+    ol.ol_decode_step(ol.OL_LAYOUT_INT4, ol.int4_kv(*dplanes, head_dim=D, quant_mode=mode), dplanes[0],
+                      to_dev(case.q), Hq, to_dev(case.new_kv), lens, to_dev(lens), 0.0, window, out, ol.OL_F32,
+                      ws, n)
+    got = out_as_f64(out)
+    assert ol.ol_workspace_status(ws) == ol.OL_DEVICE_OK
+    O.int4_append(*planes, case.new_kv, lens - 1, mode=mode)
+    for g, r in zip((to_host(p) for p in dplanes), planes):
+        np.testing.assert_array_equal(g, r)
+    want = O.int4_attention(case.q, *planes, lens, cur_kv=case.new_kv, window=window)
+    check_out(got, want, ol.OL_F32)
