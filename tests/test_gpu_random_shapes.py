@@ -6,14 +6,16 @@ included), windows and the history-stable access bit. The planner picks the
 kernel variant, cluster size, split count and launch order per shape, so the
 sweep reaches combinations the hand-picked shapes do not. Every cache byte
 must match the oracle's append and every output the oracle's attention within
-the tolerance of the other parity tests.
+the tolerance of the other parity tests. The INT4 and heterogeneous-page
+sweeps do the same for those layouts (codes, scales, zero points, page
+formats bit-exact).
 """
 import numpy as np
 import pytest
 
 import oracle as O
 import place_kv_cache_gb300 as ol
-from workloads import Workload, block_table, contiguous_cache, make_case, poisoned_pool
+from workloads import Workload, bf16_from_f32, block_table, contiguous_cache, make_case, poisoned_pool
 from tests.gpu_util import check_out, out_as_f64, out_tensor, to_dev, to_host, workspace
 
 pytestmark = pytest.mark.gpu
@@ -142,4 +144,51 @@ def test_random_shape_int4_step(c):
     for g, r in zip((to_host(p) for p in dplanes), planes):
         np.testing.assert_array_equal(g, r)
     want = O.int4_attention(case.q, *planes, lens, cur_kv=case.new_kv, window=window)
+    check_out(got, want, ol.OL_F32)
+
+
+def draw_hpaged_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        B = int(rng.integers(1, 5))
+        H = int(rng.integers(1, 5))
+        G = int(rng.integers(1, 9))
+        S = int(rng.choice([16, 32]))
+        D = 128 if rng.random() < 0.75 else 64
+        M = int(rng.integers(1, 9))
+        window = int(rng.choice([-1, -1, 0, 5, 40]))
+        lens = rng.integers(1, M * S + 1, size=B)
+        cases.append(dict(id=f"{i:02d}-hpaged-B{B}-H{H}x{G}-S{S}-D{D}-M{M}-w{window}", B=B, H=H, G=G, S=S, D=D, M=M,
+                          lens=lens.astype(np.int32), window=window, seed=int(rng.integers(1 << 30))))
+    return cases
+
+
+HPAGED_CASES = draw_hpaged_cases(16, 2028)
+
+
+@pytest.mark.parametrize("c", HPAGED_CASES, ids=[c["id"] for c in HPAGED_CASES])
+def test_random_shape_hpaged_step(c):
+    # history written page by page in drawn formats (every page its own K/V
+    # formats), then one fused step whose new page (if it starts one) takes
+    # the call's formats: pool bytes, format table and mirror bit-exact,
+    # outputs against the oracle
+    from tests.test_gpu_hpaged import FORMATS, Pair, fmt_pair
+    B, H, G, S, D, M, lens, window = c["B"], c["H"], c["G"], c["S"], c["D"], c["M"], c["lens"], c["window"]
+    Hq = H * G
+    pr = Pair(B, H, S, D, M, B * M + 2, seed=c["seed"])
+    pick = pr.rng.integers(0, len(FORMATS), size=(B, M))
+    pr.fill(lens - 1, lambda b, j: int(pick[b, j]))
+    q = bf16_from_f32(pr.rng.standard_normal((B, Hq, D)).astype(np.float32))
+    new_kv = pr.values(1)
+    od, gd = fmt_pair(int(pr.rng.integers(len(FORMATS))))
+    want = O.hpaged_attention(q, pr.pool, pr.desc, pr.table, lens, H, cur_kv=new_kv, window=window)
+    O.hpaged_append(pr.pool, pr.desc, pr.table, new_kv, lens - 1, od)
+    ws, n = workspace(B, Hq, H, D)
+    out = out_tensor(B, Hq, D, ol.OL_F32)
+    ol.ol_hpaged_decode_step(pr.kv, pr.pool_d, to_dev(q), Hq, to_dev(new_kv), gd, lens, to_dev(lens), 0.0, window,
+                             out, ol.OL_F32, ws, n)
+    got = out_as_f64(out)
+    assert ol.ol_workspace_status(ws) == ol.OL_DEVICE_OK
+    pr.check_state()
     check_out(got, want, ol.OL_F32)
