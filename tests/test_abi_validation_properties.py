@@ -161,3 +161,50 @@ def test_paged_page_rules_give_their_status(r):
     except ol.OlError as e:
         status = e.status
     assert status == want, (case, status)
+
+
+# the integer ranges of the affine formats (QuantizeLinear's output types)
+AFFINE_RANGE = {ol.OL_FMT_I8: (-128, 127), ol.OL_FMT_U8: (0, 255), ol.OL_FMT_I4: (-8, 7), ol.OL_FMT_U4: (0, 15),
+                ol.OL_FMT_I2: (-2, 1), ol.OL_FMT_U2: (0, 3)}
+FLOAT_FORMATS = (ol.OL_FMT_F32, ol.OL_FMT_F16, ol.OL_FMT_BF16)
+
+
+@st.composite
+def plane_formats(draw):
+    f = draw(st.integers(-1, 9))
+    scale = draw(st.sampled_from([0.0, -0.5, float("inf"), float("nan"), 1e-30, 0.03125, 0.5, 3.0]))
+    zp = draw(st.integers(-300, 300))
+    return f, scale, zp
+
+
+def plane_ok(f, scale, zp):
+    if f in FLOAT_FORMATS:
+        return True                                   # scale and zero point unused
+    if f not in AFFINE_RANGE:
+        return False
+    lo, hi = AFFINE_RANGE[f]
+    return scale > 0 and np.isfinite(scale) and lo <= zp <= hi
+
+
+@settings(max_examples=400, deadline=None, derandomize=True)
+@given(plane_formats(), plane_formats())
+def test_page_format_rules(kf, vf):
+    # the formats a heterogeneous append starts its pages in: a known format;
+    # for the affine ones a positive finite scale and a zero point inside the
+    # format's integer range
+    B, H, S, M, D = 2, 2, 16, 8, 128
+    P = B * M
+    mirror = np.zeros(P, ol.PAGE_FORMAT_DTYPE)
+    mirror["kf"], mirror["ks"], mirror["vf"], mirror["vs"] = ol.OL_FMT_BF16, 1.0, ol.OL_FMT_BF16, 1.0
+    pool, fmt_dev, bt = BASE, BASE + 7 * GB, BASE + 8 * GB
+    kv = ol.hpaged_kv(pool, fmt_dev, mirror, bt, np.arange(P, dtype=np.int32).reshape(B, M), kv_heads=H,
+                      page_size=S, head_dim=D)
+    fmt = ol.page_format(k=kf, v=vf)
+    pos = np.array([0, 3 * S], np.int32)           # both rows start a page
+    try:
+        ol.ol_hpaged_append(kv, pool, BASE + GB, 1, pos, BASE + 2 * GB, fmt, stream=0)
+        status = ol.OL_OK
+    except ol.OlError as e:
+        status = e.status
+    want = ol.OL_ERR_INJECTED if plane_ok(*kf) and plane_ok(*vf) else ol.OL_ERR_SHAPE
+    assert status == want, (kf, vf, status)
