@@ -4,10 +4,18 @@ step (in-place append + GQA decode attention) over a caller-owned KV cache.
 
 One step = one ``ol_decode_step`` over the whole batch of the workload: host
 validation, the append of one token per row and attention over every row's
-valid prefix, in one kernel launch. Steps are replayed from CUDA graphs so
-the host never limits a microsecond-scale step; when one step's cache fits in
-L2, consecutive steps rotate over enough independent cache replicas that the
-data of a step is never L2-resident from the previous visit.
+valid prefix, in one kernel launch (a chunked step: the append, then the
+attention). Steps are replayed from CUDA graphs so the host never limits a
+microsecond-scale step; when one step's cache fits in L2, consecutive steps
+rotate over enough independent cache replicas that the data of a step is never
+L2-resident from the previous visit.
+
+Without --workload the headline line is the paged pool of 64 rows (the largest
+workload that fits one GPU) and ``per_config`` carries the same figures for
+every other workload: the single-row GQA-7 step, the ragged batch of 32 rows,
+the INT4 cache over its 64-step chain, the chunked step of 4 tokens and the
+heterogeneous pages. Every workload times exactly --steps steps (a chained
+workload at least its whole chain).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                        [--impl ours|reference]
@@ -44,7 +52,8 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="qwen_b1_gqa7", choices=[k for k in WORKLOADS if k != "tiny_f32"])
+    ap.add_argument("--workload", default=None, choices=[k for k in WORKLOADS if k != "tiny_f32"],
+                    help="one workload only (default: the headline workload and per_config for the others)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -380,116 +389,167 @@ class Setup:
                                self.ws_bytes, stream=stream)
 
 
-def workload_of(args):
-    """The named workload, or its first --rows rows (pages sized to those rows)."""
+# ------------------------------------------------------------- driver
+
+# The headline workload is the largest one that fits one GPU (the paged pool of
+# 64 rows); every other workload is measured in the same run under per_config.
+HEADLINE = "paged_b64"
+PER_CONFIG = ("qwen_b1_gqa7", "ragged_b32", "int4_b16", "chunk4_b32", "hpaged_b64")
+
+
+def workload_of(name, rows=None):
+    """The named workload, or its first `rows` rows (pages sized to those rows)."""
     from workloads import scaled
-    w = WORKLOADS[args.workload]
-    if args.rows is not None and args.rows < w.batch:
-        w = scaled(w, batch=args.rows)
+    w = WORKLOADS[name]
+    if rows is not None and rows < w.batch:
+        w = scaled(w, batch=rows)
         if w.layout in ("paged", "hpaged"):
-            w = scaled(w, num_pages=args.rows * w.max_pages_per_row)
+            w = scaled(w, num_pages=rows * w.max_pages_per_row)
     return w
 
 
-def run_ours(args, rank, world, dist):
+def launches_per_step(w) -> int:
+    """Kernel launches of one step: a chunked step appends and attends in two
+    launches; a decode step is one fused launch."""
+    return 2 if w.chunk > 1 else 1
+
+
+def measure(w, args, rank, world, dist, dev, K_req):
+    """Time exactly K_req steps of workload w (K_req None: about --seconds).
+
+    Steps are replayed from CUDA graphs: full graphs of `per_graph` steps (a
+    whole number of cache-replica rotations and chain positions) and, for the
+    remainder, one graph of the first K mod per_graph steps of the rotation, so
+    the timed region holds exactly K steps. The region is bracketed by a
+    barrier and a stream synchronize on both sides and timed with CUDA events
+    on the launching stream. The spread comes from further full graphs timed
+    one by one after the region."""
     import torch
-    dev = f"cuda:{int(os.environ.get('LOCAL_RANK', 0))}"
-    torch.cuda.set_device(dev)
-    import place_kv_cache_gb300 as ol
-    ol.load()
-    w = workload_of(args)
     s = Setup(w, dev, seed_offset=rank)
     stream = torch.cuda.Stream(device=dev)
-    R = s.replicas
-    per_graph = max(R * s.chain, 32)
-    per_graph = (per_graph + R * s.chain - 1) // (R * s.chain) * (R * s.chain)
-    with torch.cuda.stream(stream):
-        for i in range(max(args.warmup, 3) * R * s.chain):
-            s.step(i)
-        stream.synchronize()
+    unit = s.replicas * s.chain
+    per_graph = -(-max(unit, 32) // unit) * unit
+
+    def capture(n):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            for i in range(per_graph):
+            for i in range(n):
                 s.step(i)
-        g.replay()
+        return g
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3) * unit):
+            s.step(i)
         stream.synchronize()
-    # calibrate the step time to size the timed region
+        g_full = capture(per_graph)
+        g_full.replay()
+        stream.synchronize()
     t = time.perf_counter()
     with torch.cuda.stream(stream):
         for _ in range(5):
-            g.replay()
+            g_full.replay()
     stream.synchronize()
     est = (time.perf_counter() - t) / (5 * per_graph)
-    if args.steps is None:
-        K = max(per_graph, int(args.seconds / max(est, 1e-7)) // per_graph * per_graph)
-    else:
-        K = max(per_graph, (args.steps + per_graph - 1) // per_graph * per_graph)
-    n_graphs = K // per_graph
+    K = K_req if K_req is not None else max(per_graph, int(args.seconds / max(est, 1e-7)) // per_graph * per_graph)
+    n_full, rem = divmod(K, per_graph)
+    g_tail = None
+    if rem:
+        with torch.cuda.stream(stream):
+            g_tail = capture(rem)
+            g_tail.replay()
+            stream.synchronize()
+    local = int(os.environ.get("LOCAL_RANK", 0))
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(int(os.environ.get("LOCAL_RANK", 0))) as clk:
+    n_sp = max(5, min(50, int(0.3 / max(est * per_graph, 1e-7))))
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(n_sp + 1)]
+    with ClockSampler(local) as clk:
         with torch.cuda.stream(stream):
-            for _ in range(max(1, int(0.3 / max(est * per_graph, 1e-6)))):
-                g.replay()                       # keep the GPU busy while the sampler settles
+            for _ in range(max(1, int(0.3 / max(est * per_graph, 1e-7)))):
+                g_full.replay()                  # keep the GPU busy while the sampler settles
         if dist is not None:
             dist.barrier()
         stream.synchronize()
         clk.mark_start()
-        # one event between consecutive graphs (recorded on the same stream, no
-        # synchronization between them): per-graph step times for the spread
-        marks = [torch.cuda.Event(enable_timing=True) for _ in range(n_graphs - 1)]
         with torch.cuda.stream(stream):
             e0.record(stream)
-            for k in range(n_graphs):
-                g.replay()
-                if k < n_graphs - 1:
-                    marks[k].record(stream)
+            for _ in range(n_full):
+                g_full.replay()
+            if g_tail is not None:
+                g_tail.replay()
             e1.record(stream)
         stream.synchronize()
         clk.mark_end()
         if dist is not None:
             dist.barrier()
+        with torch.cuda.stream(stream):            # spread: full graphs timed one by one
+            marks[0].record(stream)
+            for k in range(n_sp):
+                g_full.replay()
+                marks[k + 1].record(stream)
+        stream.synchronize()
     ms = e0.elapsed_time(e1)
-    bounds = [e0] + marks + [e1]
-    per_graph_us = sorted(bounds[k].elapsed_time(bounds[k + 1]) * 1e3 / per_graph for k in range(n_graphs))
-    spread = {"graphs": n_graphs,
-              "p10": round(float(np.percentile(per_graph_us, 10)), 3),
-              "median": round(float(np.percentile(per_graph_us, 50)), 3),
-              "p90": round(float(np.percentile(per_graph_us, 90)), 3)}
+    per_us = sorted(marks[k].elapsed_time(marks[k + 1]) * 1e3 / per_graph for k in range(n_sp))
     ms_per_step, gbs = combine_ranks(ms, K, s.bytes_per_step, world, dist, device=dev)
+    import place_kv_cache_gb300 as ol
     status = ol.ol_workspace_status(s.ws, stream=stream)
     peak, peak_src = measured_peaks()
-    result = {
-        "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": {"int4": "u4+bf16", "hpaged": "bf16+i8+i4/u4 pages, f32 math"}.get(w.layout, "bf16"), "data": "synthetic",
+    frac = gbs / world / peak
+    res = {
+        "value": round(gbs, 2), "unit": "GB/s", "steps": K, "ms_per_step": ms_per_step,
         "us_per_step": round(ms_per_step * 1e3, 3),
-        "us_per_step_spread": dict(spread, note=f"per graph of {per_graph} steps, rank {rank}"),
-        "rows_tok_per_s": round(w.batch * world / (ms_per_step * 1e-3), 1),
-        "pct_of_hbm_roofline": round(100.0 * gbs / world / peak, 2),
+        "us_per_step_spread": {"p10": round(float(np.percentile(per_us, 10)), 3),
+                               "median": round(float(np.percentile(per_us, 50)), 3),
+                               "p90": round(float(np.percentile(per_us, 90)), 3),
+                               "graphs": n_sp, "graph_steps": per_graph},
+        "rows_tok_per_s": round(w.batch * w.chunk * world / (ms_per_step * 1e-3), 1),
+        "pct_of_hbm_roofline": round(100.0 * frac, 2),
+        "dtype": {"int4": "u4+bf16", "hpaged": "bf16+i8+i4/u4 pages, f32 math"}.get(w.layout, "bf16"),
         "config": {"workload": w.name, "layout": w.layout, "batch": w.batch, "q_heads": w.q_heads,
                    "kv_heads": w.kv_heads, "head_dim": w.head_dim, "capacity": w.capacity,
-                   "lens_mean": float(np.mean(s.lens)), "bytes_per_step": s.bytes_per_step,
-                   "l2": s.l2_note, "graph_steps": per_graph, "chained_steps": s.chain,
-                   "history_stable": s.chain == 1,
-                   "parallelism": f"rows x{world} (independent)"},
+                   "lens_mean": float(np.mean(s.lens)), "bytes_per_step": s.bytes_per_step, "l2": s.l2_note,
+                   "graph_steps": per_graph, "tail_graph_steps": rem, "chained_steps": s.chain,
+                   "history_stable": s.chain == 1, "parallelism": f"rows x{world} (independent)"},
         "roofline": {"bound": "hbm", "achieved": round(gbs / world, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(gbs / world / peak, 4), "traffic": recorded_traffic(w.name),
+                     "frac": round(frac, 4), "traffic": recorded_traffic(w.name),
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else
                      "fallback 6.8 TB/s"},
-        "gpu_launches": K,
+        "gpu_launches": K * launches_per_step(w),
         "device_status": status,
         "clocks": clk.summary(),
     }
-    if not args.no_e2e and w.chunk == 1 and w.layout != "hpaged":
-        result["e2e"] = run_e2e(s, stream, K_e2e=min(K, 200 * R))
-    elif not args.no_e2e:
-        # the host-buffer call serves the decode step of the uniform layouts; chunked
-        # steps and heterogeneous pages run from device buffers
-        result["e2e"] = None
     if w.chunk > 1:
-        result["config"]["chunk"] = w.chunk
-    return result
+        res["config"]["chunk"] = w.chunk
+    if not args.no_e2e and w.chunk == 1 and w.layout != "hpaged":
+        res["e2e"] = run_e2e(s, stream, K)
+    elif not args.no_e2e:
+        # the host-buffer call serves the decode step of the uniform layouts;
+        # chunked steps and heterogeneous pages run from device buffers
+        res["e2e"] = None
+    del s, g_full, g_tail
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def compact(r):
+    """The per-workload figures of a measure() result, for per_config."""
+    out = {"value": r["value"], "unit": r["unit"], "us_per_step": r["us_per_step"], "steps": r["steps"],
+           "spread_us": [r["us_per_step_spread"][k] for k in ("p10", "median", "p90")],
+           "rows_tok_per_s": r["rows_tok_per_s"], "frac": r["roofline"]["frac"],
+           "traffic": r["roofline"]["traffic"], "bytes_per_step": r["config"]["bytes_per_step"],
+           "lens_mean": r["config"]["lens_mean"], "gpu_launches": r["gpu_launches"],
+           "device_status": r["device_status"], "dtype": r["dtype"],
+           "clocks": {k: r["clocks"][k] for k in ("sm_mhz", "reasons")}}
+    e = r.get("e2e")
+    out["e2e"] = None if not e else {"value": e["value"], "us_per_step": e["us_per_step"],
+                                     "h2d_bytes_per_step": e["h2d_bytes_per_step"],
+                                     "d2h_bytes_per_step": e["d2h_bytes_per_step"]}
+    cb = r.get("cpu_baseline")
+    if cb:
+        out["cpu_baseline"] = {"value": cb["value"], "cores": cb["cores"], "us_per_step": cb["us_per_step"],
+                               "single_core_us_per_step": cb["single_core"]["us_per_step"]}
+    return out
 
 
 def run_e2e(s, stream, K_e2e):
@@ -537,106 +597,198 @@ def run_e2e(s, stream, K_e2e):
 
 # --------------------------------------------------------------- oracle
 
-def oracle_step_inputs(w, max_rows):
-    """A bounded sample of the workload for the CPU oracle: the first max_rows rows."""
+def host_threads() -> int:
+    """Host cores this process may run on (at most 32)."""
+    try:
+        n = len(os.sched_getaffinity(0))
+    except AttributeError:
+        n = os.cpu_count() or 1
+    return max(1, min(n, 32))
+
+
+def oracle_units(w, n_threads):
+    """A bounded sample of the workload for the CPU oracle, cut into independent
+    units of one step (append + attention), one per host thread: the first
+    min(batch, n_threads) rows, a unit per row; a single-row workload is cut by
+    kv head instead. Every unit works on its own arrays (or, for the paged
+    pools, on its own row's pages of one shared pool), so the units of a step
+    run side by side. Returns (units, sample workload, bytes of one step of the
+    whole sample, description)."""
     import oracle as O
-    from workloads import scaled
-    rows = min(w.batch, max_rows)
+    from workloads import block_table, contiguous_cache, poisoned_pool, scaled
+    by_head = w.batch == 1
+    rows = 1 if by_head else min(w.batch, n_threads)
     ws = scaled(w, batch=rows)
-    if w.layout == "hpaged":   # the sample's rows own their pages; a pool of the full size is not needed
+    if w.layout in ("paged", "hpaged"):
         ws = scaled(ws, num_pages=rows * w.max_pages_per_row)
-    case = make_case(ws, seed=w.seed, history_len_offset=w.chunk)
-    return O, ws, case
-
-
-def run_oracle_steps(w, budget_s, max_rows):
-    """Time the oracle's decode step (append + attention) on a sample of the workload."""
-    from workloads import block_table, contiguous_cache, poisoned_pool
-    O, ws, case = oracle_step_inputs(w, max_rows)
-    if w.layout == "contiguous" and w.chunk > 1:
-        cache = contiguous_cache(case)
-        T = w.chunk
+    T = w.chunk
+    case = make_case(ws, seed=w.seed, history_len_offset=T)
+    lens = case.lens
+    H, G, D = ws.kv_heads, ws.group, ws.head_dim
+    units = []
+    if T > 1:
         rng = np.random.default_rng(w.seed + 7)
-        q = bf16_from_f32(rng.standard_normal((ws.batch, ws.q_heads, T, ws.head_dim)).astype(np.float32))
-        kv = bf16_from_f32(rng.standard_normal((2, ws.batch, ws.kv_heads, T, ws.head_dim)).astype(np.float32))
+        q = bf16_from_f32(rng.standard_normal((rows, ws.q_heads, T, D)).astype(np.float32))
+        kv = bf16_from_f32(rng.standard_normal((2, rows, H, T, D)).astype(np.float32))
+    else:
+        q, kv = case.q, case.new_kv
+    # (row, kv heads) pieces: a row, or one kv head of the single row
+    pieces = [(0, g) for g in range(H)] if by_head else [(b, None) for b in range(rows)]
 
-        def one():
-            O.cache_update(cache, kv, case.lens - T)
-            return O.chunk_attention(q, cache, case.lens, T)
-    elif w.layout == "contiguous":
+    def sl_heads(a, g, axis):       # kv head g's slice along `axis` (None: all heads)
+        if g is None:
+            return a
+        idx = [slice(None)] * a.ndim
+        idx[axis] = slice(g, g + 1)
+        return a[tuple(idx)]
+
+    def sl_q(b, g):
+        qb = q[b:b + 1]
+        return np.ascontiguousarray(qb if g is None else qb[:, g * G:(g + 1) * G])
+
+    def build(fn, items):          # per-unit set-up work on the host threads (the oracle is C)
+        import concurrent.futures
+        with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, min(len(items), n_threads))) as ex:
+            return list(ex.map(fn, items))
+
+    if w.layout == "contiguous":
         cache = contiguous_cache(case)
-
-        def one():
-            O.cache_update(cache, case.new_kv, case.lens - 1)
-            return O.decode_attention(case.q, cache, case.lens)
+        for b, g in pieces:
+            c = np.ascontiguousarray(sl_heads(cache[:, b:b + 1], g, 2))
+            k = np.ascontiguousarray(sl_heads(kv[:, b:b + 1], g, 2))
+            qq, lb = sl_q(b, g), np.ascontiguousarray(lens[b:b + 1])
+            if T > 1:
+                units.append(lambda c=c, k=k, qq=qq, lb=lb: (O.cache_update(c, k, lb - T),
+                                                             O.chunk_attention(qq, c, lb, T)))
+            else:
+                units.append(lambda c=c, k=k, qq=qq, lb=lb: (O.cache_update(c, k, lb - 1),
+                                                             O.decode_attention(qq, c, lb)))
+        del cache
+    elif w.layout == "int4":
+        def quantized(piece):
+            b, g = piece
+            hb = case.history[b] if g is None else case.history[b][:, g:g + 1]
+            planes = O.int4_planes(1, hb.shape[1], ws.capacity, D)
+            O.int4_append(*planes, np.ascontiguousarray(hb[:, None]), [0])
+            return planes
+        for (b, g), planes in zip(pieces, build(quantized, pieces)):
+            k = np.ascontiguousarray(sl_heads(kv[:, b:b + 1], g, 2))
+            qq, lb = sl_q(b, g), np.ascontiguousarray(lens[b:b + 1])
+            units.append(lambda pl=planes, k=k, qq=qq, lb=lb: (O.int4_append(*pl, k, lb - 1),
+                                                               O.int4_attention(qq, *pl, lb, cur_kv=k)))
     elif w.layout == "paged":
         pool = poisoned_pool(ws)
         table = block_table(case)
-        for b, h in enumerate(case.history):
+
+        def fill(b):               # rows own disjoint pages of the shared pool
+            h = case.history[b]
             if h.shape[2]:
                 O.paged_update(pool, table[b:b + 1], h[:, None], [0])
-
-        def one():
-            O.paged_update(pool, table, case.new_kv, case.lens - 1)
-            return O.paged_attention(case.q, pool, table, case.lens)
-    elif w.layout == "hpaged":
-        S, M, H, D = ws.page_size, ws.max_pages_per_row, ws.kv_heads, ws.head_dim
+        build(fill, list(range(rows)))
+        for b, _ in pieces:
+            tb, k = np.ascontiguousarray(table[b:b + 1]), np.ascontiguousarray(kv[:, b:b + 1])
+            qq, lb = sl_q(b, None), np.ascontiguousarray(lens[b:b + 1])
+            units.append(lambda tb=tb, k=k, qq=qq, lb=lb: (O.paged_update(pool, tb, k, lb - 1),
+                                                           O.paged_attention(qq, pool, tb, lb)))
+    else:  # heterogeneous pages
+        S, M = ws.page_size, ws.max_pages_per_row
         pool, desc = O.hpaged_pool(ws.num_pages, H, S, D)
         table = block_table(case)
-        cls = page_format_classes(case.lens, S, M)
-        for b, h in enumerate(case.history):
-            for j in range((h.shape[2] + S - 1) // S):
-                k, v = AGE_FORMATS[cls[b, j]][1]
-                O.hpaged_append(pool, desc, table[b:b + 1], h[:, None, :, j * S:(j + 1) * S], [j * S],
-                                O.page_desc(k=k, v=v))
+        cls = page_format_classes(lens, S, M)
+
+        def fill(b):               # one append per run of pages of one format class
+            h = case.history[b]
+            hist, j = h.shape[2], 0
+            npages = (hist + S - 1) // S
+            while j < npages:
+                j1 = j
+                while j1 < npages and cls[b, j1] == cls[b, j]:
+                    j1 += 1
+                kf, vf = AGE_FORMATS[cls[b, j]][1]
+                O.hpaged_append(pool, desc, table[b:b + 1], h[:, None, :, j * S:min(j1 * S, hist)], [j * S],
+                                O.page_desc(k=kf, v=vf))
+                j = j1
+        build(fill, list(range(rows)))
         new_fmt = O.page_desc(*AGE_FORMATS[0][1])
+        for b, _ in pieces:
+            tb, k = np.ascontiguousarray(table[b:b + 1]), np.ascontiguousarray(kv[:, b:b + 1])
+            qq, lb = sl_q(b, None), np.ascontiguousarray(lens[b:b + 1])
+            units.append(lambda tb=tb, k=k, qq=qq, lb=lb: (O.hpaged_attention(qq, pool, desc, tb, lb, H, cur_kv=k),
+                                                           O.hpaged_append(pool, desc, tb, k, lb - 1, new_fmt)))
+    case.history = None
+    what = (f"the {H} kv heads of the single row" if by_head else f"the first {rows} of {w.batch} rows")
+    return units, ws, step_bytes(ws, lens), what
 
-        def one():
-            y = O.hpaged_attention(case.q, pool, desc, table, case.lens, H, cur_kv=case.new_kv)
-            O.hpaged_append(pool, desc, table, case.new_kv, case.lens - 1, new_fmt)
-            return y
-    else:
-        planes = O.int4_planes(ws.batch, ws.kv_heads, ws.capacity, ws.head_dim)
-        for b, h in enumerate(case.history):
-            sub = O.int4_planes(1, ws.kv_heads, ws.capacity, ws.head_dim)
-            O.int4_append(*sub, h[:, None], [0])
-            for full, part in zip(planes, sub):
-                full[:, b] = part[:, 0]
 
-        def one():
-            O.int4_append(*planes, case.new_kv, case.lens - 1)
-            return O.int4_attention(case.q, *planes, case.lens, cur_kv=case.new_kv)
-    times = []
-    t_all = time.perf_counter()
-    while True:
+def measure_oracle(w, budget_s, n_threads=None):
+    """The oracle as it stands (plain C, fp64) on the host cores: one step of a
+    bounded sample of the workload (oracle_units) with one host thread per
+    unit, repeated for about budget_s seconds (median step time), and the same
+    units run one after another on one thread (single_core)."""
+    import concurrent.futures
+    n = n_threads or host_threads()
+    units, ws, nbytes, what = oracle_units(w, n)
+    t_serial = 0.0
+    for u in units:                       # single core: every unit once, in turn
         t = time.perf_counter()
-        one()
-        times.append(time.perf_counter() - t)
-        if time.perf_counter() - t_all > budget_s or len(times) >= 1000:
-            break
-    sec = statistics.median(times)
-    nbytes = step_bytes(ws, case.lens)
-    return {"value": round(nbytes / sec / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{len(times)} oracle {'chunked' if w.chunk > 1 else 'decode'} steps (append + attention, "
-                      f"fp64) on the first {ws.batch} of "
-                      f"{w.batch} rows of {w.name}; median {sec * 1e3:.1f} ms/step",
-            "us_per_step": round(sec * 1e6, 1), "rows_tok_per_s": round(ws.batch / sec, 2)}
+        u()
+        t_serial += time.perf_counter() - t
+    walls = []
+    with concurrent.futures.ThreadPoolExecutor(max_workers=len(units)) as ex:
+        t_all = time.perf_counter()
+        while True:
+            t = time.perf_counter()
+            for f in [ex.submit(u) for u in units]:
+                f.result()
+            walls.append(time.perf_counter() - t)
+            if time.perf_counter() - t_all > budget_s or len(walls) >= 200:
+                break
+    sec = statistics.median(walls)
+    kind = "chunked" if w.chunk > 1 else "decode"
+    return {"value": round(nbytes / sec / 1e9, 4), "unit": "GB/s", "cores": len(units), "kind": "oracle",
+            "sample": f"{len(walls)} oracle {kind} steps (append + attention, fp64) on {what} of {w.name}, "
+                      f"{len(units)} host threads (one per {'kv head' if w.batch == 1 else 'row'}); "
+                      f"median {sec * 1e3:.1f} ms/step",
+            "us_per_step": round(sec * 1e6, 1), "rows_tok_per_s": round(ws.batch * w.chunk / sec, 2),
+            "single_core": {"value": round(nbytes / t_serial / 1e9, 4), "cores": 1,
+                            "us_per_step": round(t_serial * 1e6, 1)}}
 
 
-def run_reference(args, rank, world):
-    w = WORKLOADS[args.workload]
-    max_rows = {"qwen_b1_gqa7": 1, "ragged_b32": 4, "paged_b64": 2, "int4_b16": 1, "chunk4_b32": 1,
-                "hpaged_b64": 2}[w.name]
+def run_reference(args, world):
+    """The reference arm: the oracle, as it stands, on the host cores, for the
+    headline workload (or --workload): W untimed steps, then K timed steps, each
+    one step of the bounded sample with one host thread per unit."""
+    import concurrent.futures
+    w = workload_of(args.workload or HEADLINE)
     K = args.steps if args.steps is not None else 3
-    budget = 60.0
-    res = run_oracle_steps(w, budget_s=min(budget, 10.0 * max(1, K)), max_rows=max_rows)
-    return {"impl": "reference", "metric": METRIC, "value": res["value"], "unit": "GB/s", "n_gpus": world,
-            "steps": K, "warmup": args.warmup, "ms_per_step": res["us_per_step"] / 1e3, "higher_is_better": True,
+    units, ws, nbytes, what = oracle_units(w, host_threads())
+    with concurrent.futures.ThreadPoolExecutor(max_workers=len(units)) as ex:
+        def step():
+            for f in [ex.submit(u) for u in units]:
+                f.result()
+        for _ in range(args.warmup):
+            step()
+        t = time.perf_counter()
+        for _ in range(K):
+            step()
+        sec = (time.perf_counter() - t) / K
+    value = round(nbytes / sec / 1e9, 4)
+    kind = "chunked" if w.chunk > 1 else "decode"
+    cb = {"value": value, "unit": "GB/s", "cores": len(units), "kind": "oracle",
+          "sample": f"{K} timed oracle {kind} steps (append + attention, fp64) on {what} of {w.name}, "
+                    f"{len(units)} host threads (one per {'kv head' if w.batch == 1 else 'row'}); "
+                    f"{sec * 1e3:.1f} ms/step",
+          "us_per_step": round(sec * 1e6, 1), "rows_tok_per_s": round(ws.batch * w.chunk / sec, 2)}
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "layout": w.layout, "batch": w.batch, "q_heads": w.q_heads,
                        "kv_heads": w.kv_heads, "head_dim": w.head_dim, "capacity": w.capacity},
-            "cpu_baseline": res,
-            "e2e": {"value": res["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+ORACLE_BUDGET_S = 4.0   # seconds of oracle steps per workload (after its one-thread pass)
 
 
 def main():
@@ -645,19 +797,41 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(run_reference(args, rank, world)), flush=True)
+            print(json.dumps(run_reference(args, world)), flush=True)
         return
     dist = None
     if world > 1:
         import torch.distributed as dist_mod
         dist_mod.init_process_group("nccl")
         dist = dist_mod
-    result = run_ours(args, rank, world, dist)
+    import torch
+    dev = f"cuda:{int(os.environ.get('LOCAL_RANK', 0))}"
+    torch.cuda.set_device(dev)
+    import place_kv_cache_gb300 as ol
+    ol.load()
+    head = workload_of(args.workload or HEADLINE, args.rows)
+    r = measure(head, args, rank, world, dist, dev, args.steps)
+    result = {"metric": METRIC, "value": r["value"], "unit": "GB/s", "n_gpus": world, "steps": r["steps"],
+              "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True,
+              "scaling": "weak", "vs_baseline": None, "dtype": r["dtype"], "data": "synthetic"}
+    for k in ("us_per_step", "us_per_step_spread", "rows_tok_per_s", "pct_of_hbm_roofline", "config", "roofline",
+              "gpu_launches", "device_status", "clocks"):
+        result[k] = r[k]
+    if "e2e" in r:
+        result["e2e"] = r["e2e"]
     if rank == 0 and not args.no_cpu_baseline:
-        w = WORKLOADS[args.workload]
-        max_rows = {"qwen_b1_gqa7": 1, "ragged_b32": 4, "paged_b64": 2, "int4_b16": 1, "chunk4_b32": 1,
-                "hpaged_b64": 2}[w.name]
-        result["cpu_baseline"] = run_oracle_steps(w, budget_s=10.0, max_rows=max_rows)
+        result["cpu_baseline"] = measure_oracle(head, ORACLE_BUDGET_S)
+    if args.workload is None:
+        per = {}
+        for name in PER_CONFIG:
+            w = workload_of(name, args.rows)
+            # a chained workload is timed over its whole chain at least
+            K = None if args.steps is None else (max(args.steps, w.steps) if w.steps > 1 else args.steps)
+            rr = measure(w, args, rank, world, dist, dev, K)
+            if rank == 0 and not args.no_cpu_baseline:
+                rr["cpu_baseline"] = measure_oracle(w, ORACLE_BUDGET_S)
+            per[name] = compact(rr)
+        result["per_config"] = per
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()

@@ -29,9 +29,15 @@ F32_NAN = np.float32(np.nan)
 def bf16_from_f32(a) -> np.ndarray:
     """Round float32 values to bf16 (round to nearest, ties to even); returns uint16 bit patterns."""
     a = np.ascontiguousarray(np.asarray(a, dtype=np.float32))
-    u = a.view(np.uint32).astype(np.uint64)
-    rounded = (u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
-    out = rounded.astype(np.uint16)
+    u = a.view(np.uint32)
+    # u + 0x7FFF + (bit 16 of u), shifted down 16: in uint32 this cannot wrap
+    # for any non-NaN pattern (at most 0xFF800000 + 0x8000); NaNs are replaced below
+    r = u >> np.uint32(16)
+    r &= np.uint32(1)
+    r += np.uint32(0x7FFF)
+    r += u
+    r >>= np.uint32(16)
+    out = r.astype(np.uint16)
     nan = np.isnan(a)
     if nan.any():
         out[nan] = BF16_NAN
