@@ -58,6 +58,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--seconds", type=float, default=1.0, help="target timed seconds when --steps is not given")
+    ap.add_argument("--phase-stamps", action="store_true",
+                    help="timing build: per-CTA phase stamps of the decode kernel over one graph of steps")
+    ap.add_argument("--phase-out", default=None, help="with --phase-stamps: save the raw stamps (.npy) here")
     ap.add_argument("--rows", type=int, default=None,
                     help="the workload's first ROWS rows only (a smaller device footprint, for profiling)")
     return ap.parse_args()
@@ -788,6 +791,80 @@ def run_reference(args, world):
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+PHASES = ("entry", "wait", "inputs", "first_tile", "warp0_tiles", "all_tiles", "cta_merged", "cluster", "end")
+
+
+def phase_report(w, dev, raw_out=None):
+    """Run one CUDA graph of consecutive steps with the timing build (libol_phase.so)
+    and reduce its per-CTA phase stamps (%globaltimer ns and clock64 cycles at:
+    entry, after the dependency wait, q and the new token loaded, first tile
+    landed, warp 0's tiles done, every warp's tiles done, CTA merge done (before
+    the cluster barrier), after the cluster barrier, y stored). Times are medians
+    over the steps after the first: `since_prev_end` is relative to the moment the
+    previous step's last CTA stored y; `per_cta` are medians over CTAs of the
+    intervals between consecutive phases, from clock64."""
+    import ctypes
+    import torch
+    import place_kv_cache_gb300 as ol
+    L = ol.load(variant="phase")
+    fn = L.ol_debug_phase_stamps
+    fn.restype, fn.argtypes = ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32]
+    s = Setup(w, dev)
+    stream = torch.cuda.Stream(device=dev)
+    unit = s.replicas * s.chain
+    n = min(64, -(-max(unit, 32) // unit) * unit)
+    with torch.cuda.stream(stream):
+        for i in range(3 * unit):
+            s.step(i)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                s.step(i)
+        g.replay()
+        stream.synchronize()
+    assert fn(None, 0, 1) == 0
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    buf = np.zeros((64, 256, len(PHASES), 2), np.uint64)
+    assert fn(buf.ctypes.data, buf.nbytes, 0) == 0
+    if raw_out:
+        np.save(raw_out, buf)
+    st = buf.astype(np.int64)
+    steps = [k for k in range(n) if (st[k, :, 0, 0] > 0).any()]
+    ctas = [c for c in range(256) if st[steps[0], c, 0, 0] > 0]
+    sub = st[:, ctas]                                     # [launch, cta, phase, 2]
+    ns, cyc = sub[..., 0], sub[..., 1]
+    done = ns[:, :, -1] > 0                               # CTAs that stored (mapped ones)
+    # SM clock from the CTAs' own (clock64, globaltimer) spans
+    span_ns = ns[steps, :, -1] - ns[steps, :, 0]
+    span_cy = cyc[steps, :, -1] - cyc[steps, :, 0]
+    ok = (span_ns > 0) & done[steps]
+    mhz = float(np.median(span_cy[ok] / span_ns[ok] * 1e3))
+    gt = np.diff(np.sort(np.unique(ns[steps][ns[steps] > 0])))
+    rel = {ph: [] for ph in ("entry_first", "entry_last", "wait_first", "wait_last", "end_first", "end_last")}
+    period, per_cta = [], {f"{a}->{b}": [] for a, b in zip(PHASES[1:-1], PHASES[2:])}
+    for k0, k in zip(steps[:-1], steps[1:]):
+        prev_end = ns[k0, done[k0], -1].max()
+        m = done[k]
+        period.append(ns[k, m, -1].max() - prev_end)
+        for name, ph, f in (("entry", 0, None), ("wait", 1, None), ("end", -1, None)):
+            rel[name + "_first"].append(ns[k, m, ph].min() - prev_end)
+            rel[name + "_last"].append(ns[k, m, ph].max() - prev_end)
+        for i, key in enumerate(per_cta):
+            a, b = cyc[k, m, i + 1], cyc[k, m, i + 2]
+            if (a > 0).all() and (b > 0).all():           # phases a plan without clusters skips stay empty
+                per_cta[key].append(float(np.median(b - a)) / mhz * 1e3)
+    med = lambda v: round(float(np.median(v)), 1)
+    return {"workload": w.name, "phase_stamps": {
+        "steps": len(steps), "ctas_per_step": len(ctas), "sm_mhz_from_clock64": round(mhz, 1),
+        "globaltimer_min_step_ns": int(gt[gt > 0].min()) if (gt > 0).any() else None,
+        "step_period_ns": med(period),
+        "since_prev_end_ns": {k: med(v) for k, v in rel.items()},
+        "per_cta_ns": {k: med(v) for k, v in per_cta.items() if v}}}
+
+
 ORACLE_BUDGET_S = 4.0   # seconds of oracle steps per workload (after its one-thread pass)
 
 
@@ -807,6 +884,11 @@ def main():
     import torch
     dev = f"cuda:{int(os.environ.get('LOCAL_RANK', 0))}"
     torch.cuda.set_device(dev)
+    if args.phase_stamps:
+        if rank == 0:
+            print(json.dumps(phase_report(workload_of(args.workload or HEADLINE, args.rows), dev, args.phase_out)),
+                  flush=True)
+        return
     import place_kv_cache_gb300 as ol
     ol.load()
     head = workload_of(args.workload or HEADLINE, args.rows)

@@ -104,21 +104,27 @@ class HPagedKV(ctypes.Structure):
 _lib = None
 
 
-def load(build_if_missing: bool = True):
-    """Load libol.so (building it in-tree first if it is missing or stale)."""
+def load(build_if_missing: bool = True, variant: str = ""):
+    """Load libol.so (building it in-tree first if it is missing or stale).
+    variant="phase" loads the timing build libol_phase.so instead (same API plus
+    ol_debug_phase_stamps); it must be the first load of the process."""
     global _lib
     if _lib is not None:
+        if variant and getattr(_lib, "_variant", "") != variant:
+            raise RuntimeError(f"library already loaded without variant {variant!r}")
         return _lib
+    path = LIB_PATH if not variant else os.path.join(_HERE, f"libol_{variant}.so")
     if build_if_missing:
         from . import _build
         try:
-            _build.build()
+            _build.build(variant=variant)
         except Exception as e:  # no nvcc, compile error: fail loudly, never fall back
-            if not os.path.exists(LIB_PATH):
+            if not os.path.exists(path):
                 raise RuntimeError(f"the CUDA library could not be built: {e}") from e
-    if not os.path.exists(LIB_PATH):
-        raise RuntimeError(f"{LIB_PATH} is missing: run __graft_entry__.build()")
-    L = ctypes.CDLL(LIB_PATH)
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: run __graft_entry__.build()")
+    L = ctypes.CDLL(path)
+    L._variant = variant
     vp, i32, i64, u64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float,
                                   ctypes.c_size_t)
     st = ctypes.c_int

@@ -18,6 +18,60 @@
 //   O^T[128 dims x 8 heads] += V^T[128 x 16] * P^T  8 mma, V via ldmatrix.trans
 // Warps merge in shared memory; CTAs of one (row, kv head) merge through
 // fp32 partials in the workspace and an atomic ticket (finish_split).
+#if defined(OL_PHASE_STAMPS) && OL_PHASE_STAMPS
+// Timing build: thread 0 of every decode-kernel CTA records (%globaltimer,
+// clock64) at each phase boundary into a ring of 64 launches x 256 CTAs. The
+// launch index is a running CTA count divided by the grid size: every CTA of a
+// launch starts (and counts itself) before any CTA of the next launch, which
+// programmatic dependent launch starts only once all of them have triggered.
+namespace ol {
+enum { OL_PH_ENTRY, OL_PH_WAIT, OL_PH_INPUTS, OL_PH_FIRST_TILE, OL_PH_TILES, OL_PH_ALL_TILES, OL_PH_CTA_MERGED,
+       OL_PH_CLUSTER, OL_PH_END, OL_PH_COUNT };
+constexpr int kStampSteps = 64, kStampCtas = 256;
+__device__ unsigned long long g_stamps[kStampSteps][kStampCtas][OL_PH_COUNT][2];
+__device__ unsigned int g_stamp_seq;
+__shared__ unsigned int s_stamp_slot;
+__device__ __forceinline__ void stamp_record(int ph) {
+  const unsigned slot = s_stamp_slot;
+  if (slot == 0xffffffffu) return;
+  unsigned long long t, c;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(c));
+  g_stamps[slot / kStampCtas][slot % kStampCtas][ph][0] = t;
+  g_stamps[slot / kStampCtas][slot % kStampCtas][ph][1] = c;
+}
+__device__ __forceinline__ void stamp_begin(bool on) {
+  if (threadIdx.x != 0) return;
+  unsigned slot = 0xffffffffu;
+  if (on && blockIdx.x < (unsigned)kStampCtas) {
+    const unsigned seq = atomicAdd(&g_stamp_seq, 1u);
+    slot = (seq / (gridDim.x * gridDim.y * gridDim.z)) % kStampSteps * kStampCtas + blockIdx.x;
+  }
+  s_stamp_slot = slot;
+  stamp_record(OL_PH_ENTRY);
+}
+}  // namespace ol
+#define OL_STAMP(ph) \
+  do {               \
+    if (threadIdx.x == 0) ::ol::stamp_record(::ol::ph); \
+  } while (0)
+// the stamp waits for `reg` (a loaded value) to arrive
+#define OL_STAMP_AFTER(ph, reg)                                  \
+  do {                                                           \
+    if (threadIdx.x == 0) {                                      \
+      uint32_t dep_;                                             \
+      asm volatile("mov.b32 %0, %1;" : "=r"(dep_) : "r"(reg));   \
+      ::ol::stamp_record(::ol::ph);                              \
+    }                                                            \
+  } while (0)
+#define OL_STAMP_BEGIN(on) ::ol::stamp_begin(on)
+#define OL_STAMP_END()  \
+  do {                  \
+    __syncthreads();    \
+    OL_STAMP(OL_PH_END); \
+  } while (0)
+#endif
+
 #include "ol_merge.cuh"
 
 namespace ol {
@@ -269,3 +323,24 @@ cudaError_t launch_fast_bf16(const AttnParams& p, cudaStream_t s) {
 }
 
 }  // namespace ol
+
+#if defined(OL_PHASE_STAMPS) && OL_PHASE_STAMPS
+// Copy the timing build's stamp ring to host memory ([64][256][9][2] uint64:
+// launch slot, CTA, phase, {%globaltimer ns, clock64}); with reset != 0 then
+// zero it and restart the launch count (synchronizes the device).
+extern "C" OL_API ol_status ol_debug_phase_stamps(void* host_out, size_t bytes, int32_t reset) {
+  if (host_out && bytes > 0) {
+    if (bytes > sizeof(ol::g_stamps)) bytes = sizeof(ol::g_stamps);
+    if (cudaMemcpyFromSymbol(host_out, ol::g_stamps, bytes) != cudaSuccess) return OL_ERR_CUDA;
+  }
+  if (reset) {
+    static unsigned long long zeros[ol::kStampCtas * ol::OL_PH_COUNT * 2];
+    for (int s = 0; s < ol::kStampSteps; ++s)
+      if (cudaMemcpyToSymbol(ol::g_stamps, zeros, sizeof(zeros), (size_t)s * sizeof(zeros)) != cudaSuccess)
+        return OL_ERR_CUDA;
+    const unsigned int z = 0;
+    if (cudaMemcpyToSymbol(ol::g_stamp_seq, &z, sizeof(z)) != cudaSuccess) return OL_ERR_CUDA;
+  }
+  return cudaDeviceSynchronize() == cudaSuccess ? OL_OK : OL_ERR_CUDA;
+}
+#endif

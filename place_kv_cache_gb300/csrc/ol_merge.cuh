@@ -5,6 +5,14 @@
 
 #include "ol_common.cuh"
 
+// Phase stamps of the timing build (see ol_fast_bf16.cu); no code otherwise.
+#ifndef OL_STAMP
+#define OL_STAMP(ph)
+#define OL_STAMP_AFTER(ph, reg)
+#define OL_STAMP_BEGIN(on)
+#define OL_STAMP_END()
+#endif
+
 namespace ol {
 
 constexpr int kOStride = 132;  // fp32 row stride of an [8 heads][128 dims] state in shared memory
@@ -72,8 +80,60 @@ __device__ __forceinline__ void st_shared_cluster_v4(uint32_t addr, float4 v) {
                : "memory");
 }
 
+// The last level of a cluster merge when the cluster covers its (row, kv head)
+// alone: thread (column j, 4 dims) of this CTA's slice [rank*128/CS, +128/CS)
+// forms M = max_q m_q, the weights 2^(m_q - M) and L = sum_q l_q 2^(m_q - M)
+// over the CS received states and stores y = sum_q o_q 2^(m_q - M) / L.
+template <int CS>
+__device__ __forceinline__ void cluster_store_y(const AttnParams& p, const Work& w, const MergeScratch& ms, int G,
+                                                int zs) {
+  constexpr int dspan = 128 / CS, nd4 = dspan / 4;
+  const int d0 = (int)cluster_ctarank() * dspan;
+  if (zs < 0) zs = query_index(p);
+  const int D = p.head_dim, Gq = p.group;
+  const int nq = p.nq > 1 ? p.nq : 1, z0 = slice_first(p, zs), c_live = Gq * slice_tokens(p, zs);
+  const size_t head_base = (size_t)w.b * p.q_heads + (size_t)w.g * Gq;
+  for (int idx = threadIdx.x; idx < G * nd4; idx += blockDim.x) {
+    const int j = idx / nd4, dd = (idx % nd4) * 4;
+    float mq[CS];
+    float M = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < CS; ++q) {
+      mq[q] = ms.recv_m[q * 8 + j];
+      M = fmaxf(M, mq[q]);
+    }
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < CS; ++q) {
+      const float wq = (mq[q] == -INFINITY) ? 0.f : fast_exp2(mq[q] - M);
+      L += wq * ms.recv_l[q * 8 + j];
+      const float4 v = *reinterpret_cast<const float4*>(ms.recv_o + (q * 8 + j) * dspan + dd);
+      acc.x += wq * v.x;
+      acc.y += wq * v.y;
+      acc.z += wq * v.z;
+      acc.w += wq * v.w;
+    }
+    if (j >= c_live) continue;
+    const size_t o = (nq == 1 ? (head_base + j) : ((head_base + j % Gq) * nq + z0 + j / Gq)) * D + d0 + dd;
+    const float y0 = L > 0.f ? acc.x / L : 0.f, y1 = L > 0.f ? acc.y / L : 0.f;
+    const float y2 = L > 0.f ? acc.z / L : 0.f, y3 = L > 0.f ? acc.w / L : 0.f;
+    if (p.out_dtype == OL_F32) {
+      *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o) = make_float4(y0, y1, y2, y3);
+    } else {
+      *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.out) + o) =
+          make_uint2(pack_bf16x2(y0, y1), pack_bf16x2(y2, y3));
+    }
+  }
+}
+
 // Merge `nstates` (<= 32) states (state s has O at state_o(s)) into the CTA
-// state and finish. Weights 2^(m_s - M) are formed once per (state, head).
+// state and finish.
+//   CTA level: thread (head j, 8 dims d..d+7) forms head j's maximum M over the
+//     states, the weights 2^(m_s - M) and L = sum_s l_s 2^(m_s - M) in its own
+//     registers (every thread of a head recomputes them from shared memory: no
+//     barrier between the reduction and its use), then its 8 dims of
+//     sum_s o_s 2^(m_s - M).
 //   p.cluster == 1: the CTA state goes to `merged` ([8][kOStride]) and
 //     finish_split.
 //   p.cluster == CS > 1: the CTAs of a cluster hold consecutive splits of one
@@ -81,7 +141,10 @@ __device__ __forceinline__ void st_shared_cluster_v4(uint32_t addr, float4 v) {
 //     its state straight into the owners' receive buffers (remote shared-memory
 //     stores), one cluster barrier makes them visible, and every CTA merges its
 //     own slice from local shared memory. No remote loads, one barrier; after
-//     the barrier a CTA touches only its own shared memory and may exit.
+//     the barrier a CTA touches only its own shared memory and may exit. When
+//     the cluster covers its (row, kv head) alone, thread (head j, 4 dims)
+//     forms the merge weights in registers and stores y directly (no further
+//     barrier); otherwise the cluster state goes to finish_split.
 // Every thread of every CTA of the cluster must call it.
 template <typename StateO>
 __device__ __forceinline__ void merge_and_finish(const AttnParams& p, const Work& w, int nstates, StateO state_o,
@@ -90,47 +153,50 @@ __device__ __forceinline__ void merge_and_finish(const AttnParams& p, const Work
   const int G = state_cols(p);  // state columns: the heads, or (query token, head) pairs
   const int CS = p.cluster;
   __syncthreads();
-  if (threadIdx.x < 8) {  // one thread per head: maximum, weights 2^(m_s - M), sum
-    const int j = threadIdx.x;
+  OL_STAMP(OL_PH_ALL_TILES);
+  const uint32_t rank = CS > 1 ? cluster_ctarank() : 0;
+  const int dspan = 128 / CS;
+  for (int idx = threadIdx.x; idx < G * 16; idx += blockDim.x) {
+    const int j = idx >> 4, d = (idx & 15) * 8;
     float M = -INFINITY;
+#pragma unroll 8
     for (int s = 0; s < nstates; ++s) M = fmaxf(M, ms.wm[s * 8 + j]);
     float L = 0.f;
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+#pragma unroll 8
     for (int s = 0; s < nstates; ++s) {
       const float mw = ms.wm[s * 8 + j];
       const float wt = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
-      ms.wt[s * 8 + j] = wt;
       L += wt * ms.wl[s * 8 + j];
-    }
-    ms.m[j] = M;
-    ms.l[j] = L;
-  }
-  __syncthreads();
-  const uint32_t rank = CS > 1 ? cluster_ctarank() : 0;
-  const int dspan = 128 / CS;
-  if (CS > 1 && threadIdx.x < CS * 8) {  // (m, l) of head j to CTA q
-    const int q = threadIdx.x >> 3, j = threadIdx.x & 7;
-    st_shared_cluster(map_shared_rank(smem_u32(ms.recv_m + rank * 8 + j), q), ms.m[j]);
-    st_shared_cluster(map_shared_rank(smem_u32(ms.recv_l + rank * 8 + j), q), ms.l[j]);
-  }
-  for (int idx = threadIdx.x; idx < G * 32; idx += blockDim.x) {
-    const int j = idx >> 5, d = (idx & 31) * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < nstates; ++s) {
-      const float wt = ms.wt[s * 8 + j];
       if (wt != 0.f) {
-        const float4 v = *reinterpret_cast<const float4*>(state_o(s) + j * kOStride + d);
-        acc.x += wt * v.x;
-        acc.y += wt * v.y;
-        acc.z += wt * v.z;
-        acc.w += wt * v.w;
+        const float4 v0 = *reinterpret_cast<const float4*>(state_o(s) + j * kOStride + d);
+        const float4 v1 = *reinterpret_cast<const float4*>(state_o(s) + j * kOStride + d + 4);
+        a0.x += wt * v0.x;
+        a0.y += wt * v0.y;
+        a0.z += wt * v0.z;
+        a0.w += wt * v0.w;
+        a1.x += wt * v1.x;
+        a1.y += wt * v1.y;
+        a1.z += wt * v1.z;
+        a1.w += wt * v1.w;
       }
     }
     if (CS == 1) {
-      *reinterpret_cast<float4*>(merged + j * kOStride + d) = acc;
+      *reinterpret_cast<float4*>(merged + j * kOStride + d) = a0;
+      *reinterpret_cast<float4*>(merged + j * kOStride + d + 4) = a1;
+      if (d == 0) {
+        ms.m[j] = M;
+        ms.l[j] = L;
+      }
     } else {
-      const int owner = d / dspan;
-      const uint32_t dst = smem_u32(ms.recv_o + (rank * 8 + j) * dspan + (d - owner * dspan));
-      st_shared_cluster_v4(map_shared_rank(dst, owner), acc);
+      const int owner = d / dspan, off = d - owner * dspan;
+      const uint32_t dst = smem_u32(ms.recv_o + (rank * 8 + j) * dspan + off);
+      st_shared_cluster_v4(map_shared_rank(dst, owner), a0);
+      st_shared_cluster_v4(map_shared_rank(dst + 16, owner), a1);
+      if (off == 0) {  // the owner of these dims also needs this CTA's (m, l) of head j
+        st_shared_cluster(map_shared_rank(smem_u32(ms.recv_m + rank * 8 + j), owner), M);
+        st_shared_cluster(map_shared_rank(smem_u32(ms.recv_l + rank * 8 + j), owner), L);
+      }
     }
   }
   if (CS == 1) {
@@ -140,8 +206,21 @@ __device__ __forceinline__ void merge_and_finish(const AttnParams& p, const Work
                  ms.flag, ms.scr, zs);
     return;
   }
+  OL_STAMP(OL_PH_CTA_MERGED);
   cluster_sync();  // every push of every CTA of the cluster is visible
+  OL_STAMP(OL_PH_CLUSTER);
   const int d0 = (int)rank * dspan;
+  const int nd4 = dspan / 4;
+  if (w.nsplit == CS) {
+    // the cluster is the whole (row, kv head): y for this CTA's dims, straight from registers
+    if (!w.valid) return;
+    switch (CS) {  // a compile-time source count lets every source's loads issue together
+      case 16: cluster_store_y<16>(p, w, ms, G, zs); return;
+      case 8: cluster_store_y<8>(p, w, ms, G, zs); return;
+      case 4: cluster_store_y<4>(p, w, ms, G, zs); return;
+      default: cluster_store_y<2>(p, w, ms, G, zs); return;
+    }
+  }
   if (threadIdx.x < 8) {
     const int j = threadIdx.x;
     float M = -INFINITY;
@@ -157,7 +236,6 @@ __device__ __forceinline__ void merge_and_finish(const AttnParams& p, const Work
     ms.cl[j] = L;
   }
   __syncthreads();
-  const int nd4 = dspan / 4;
   for (int idx = threadIdx.x; idx < G * nd4; idx += blockDim.x) {
     const int j = idx / nd4, dd = (idx % nd4) * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
