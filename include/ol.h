@@ -525,21 +525,35 @@ OL_API ol_status ol_decode_step_host(int32_t layout, const void* cache_desc, voi
  * file-scope device array of OL_NOALLOC_SCRATCH_BYTES inside this library;
  * every GPU that loads the library holds it until the process exits. The
  * first call on a device looks up that array's device address (with the
- * device current); make that first call before any stream capture. Every call
- * clears the counters and status word on `stream` (cudaMemsetAsync of the
- * array itself, no allocation) and then runs ol_decode_step with the array as
- * its workspace. Requests whose worst-case workspace,
- * ol_workspace_size(batch, q_heads, kv_heads, head_dim), exceeds
- * OL_NOALLOC_SCRATCH_BYTES are rejected with OL_ERR_WORKSPACE before anything
- * runs. All calls share the one array: calls that overlap on the GPU (on
+ * device current); make that first call before any stream capture. Every
+ * check of ol_decode_step runs first, with the array as the workspace: a
+ * request whose worst-case workspace, ol_workspace_size(batch, q_heads,
+ * kv_heads, head_dim), exceeds OL_NOALLOC_SCRATCH_BYTES is OL_ERR_WORKSPACE,
+ * and any rejected call returns ol_decode_step's status for the same
+ * arguments with nothing enqueued. A call that passes clears the array's
+ * counters and status word on `stream` (cudaMemsetAsync of the array itself,
+ * no allocation) and then runs ol_decode_step with the array as its
+ * workspace. All calls share the one array: calls that overlap on the GPU (on
  * different streams, or from different threads) race on it and must not be
- * issued. Arguments and errors are otherwise those of ol_decode_step.
+ * issued. The heterogeneous-page layout is not taken (as by ol_decode_step,
+ * which has no format choice for the pages it would start).
  */
 #define OL_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 OL_API ol_status ol_decode_step_noalloc(int32_t layout, const void* cache_desc, void* updated, const void* q,
                                         int32_t q_heads, const void* new_kv, const int32_t* lens_host,
                                         const int32_t* lens_dev, float scale, int32_t window, void* out,
                                         int32_t out_dtype, ol_stream stream);
+
+/*
+ * Read and clear the device status word of the current device's
+ * allocation-free scratch (synchronizes `stream`): OL_DEVICE_OK, or
+ * OL_DEVICE_GUARD if a kernel of an ol_decode_step_noalloc call skipped an
+ * access because a device-side index disagreed with the validated sizes (as
+ * ol_workspace_status for a caller's workspace). Every ol_decode_step_noalloc
+ * call clears the word before it runs, so the word reports the calls since the
+ * last one that started, i.e. the most recent call.
+ */
+OL_API ol_status ol_noalloc_status(int32_t* status_out, ol_stream stream);
 
 #ifdef __cplusplus
 }

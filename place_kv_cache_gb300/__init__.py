@@ -36,7 +36,7 @@ OL_DEVICE_OK, OL_DEVICE_GUARD = 0, 1
 SYMBOLS = ("ol_status_string", "ol_version", "ol_workspace_size", "ol_workspace_init", "ol_workspace_status",
            "ol_cache_bind", "ol_cache_unbind", "ol_cache_update", "ol_cache_update_rows",
            "ol_paged_cache_update", "ol_decode_attention", "ol_paged_decode_attention", "ol_int4kv_append",
-           "ol_int4kv_decode_attention", "ol_decode_step", "ol_decode_step_noalloc", "ol_workspace_size_host",
+           "ol_int4kv_decode_attention", "ol_decode_step", "ol_decode_step_noalloc", "ol_noalloc_status", "ol_workspace_size_host",
            "ol_decode_step_host", "ol_last_call_stats", "ol_total_stats", "ol_reset_stats",
            "ol_workspace_size_chunk", "ol_chunk_step", "ol_hpaged_append", "ol_hpaged_decode_attention",
            "ol_hpaged_decode_step", "ol_hpaged_quantize", "ol_hpaged_chunk_step")
@@ -146,6 +146,7 @@ def load(build_if_missing: bool = True, variant: str = ""):
                                             vp]),
         "ol_decode_step": (st, [i32, vp, vp, vp, i32, vp, vp, vp, f32, i32, vp, i32, vp, sz, vp]),
         "ol_decode_step_noalloc": (st, [i32, vp, vp, vp, i32, vp, vp, vp, f32, i32, vp, i32, vp]),
+        "ol_noalloc_status": (st, [ctypes.POINTER(i32), vp]),
         "ol_workspace_size_host": (sz, [i32, i32, i32, i32]),
         "ol_workspace_size_chunk": (sz, [i32, i32, i32, i32, i32]),
         "ol_chunk_step": (st, [i32, vp, vp, vp, i32, i32, vp, vp, vp, f32, i32, vp, i32, vp, sz, vp]),
@@ -461,6 +462,13 @@ def ol_decode_step_noalloc(layout: int, desc, updated, q, q_heads: int, new_kv, 
     _check(load().ol_decode_step_noalloc(layout, ctypes.byref(desc), _ptr(updated), _ptr(q), q_heads, _ptr(new_kv),
                                          _ptr(lh), _ptr(lens_dev), scale, window, _ptr(out), out_dtype,
                                          _stream(stream)), "ol_decode_step_noalloc")
+
+
+def ol_noalloc_status(stream=None) -> int:
+    """Read and clear the status word of the allocation-free step's scratch (current device)."""
+    out = ctypes.c_int32(0)
+    _check(load().ol_noalloc_status(ctypes.byref(out), _stream(stream)), "ol_noalloc_status")
+    return out.value
 
 
 def ol_hpaged_append(kv: HPagedKV, updated, values, new_len: int, positions_host, positions_dev,

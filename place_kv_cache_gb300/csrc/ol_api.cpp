@@ -787,6 +787,20 @@ ol_status run_attention(int layout, const void* desc, const CacheView& v, const 
 }
 
 }  // namespace
+
+ol_status decode_step_impl(int32_t layout, const void* cache_desc, void* updated, const void* q, int32_t q_heads,
+                           const void* new_kv, const int32_t* lens_host, const int32_t* lens_dev, float scale,
+                           int32_t window, void* out, int32_t out_dtype, void* workspace, size_t ws_bytes,
+                           ol_stream stream, bool check_only) {
+  CacheView v;
+  ol_status st = view_of(layout, cache_desc, v);
+  if (st != OL_OK) return st;
+  if ((st = writable(v, updated)) != OL_OK) return st;
+  if (!new_kv) return OL_ERR_NULL;
+  return run_attention(layout, cache_desc, v, q, q_heads, lens_host, lens_dev, new_kv, 1, 1, scale, window, out,
+                       out_dtype, workspace, ws_bytes, static_cast<cudaStream_t>(stream), 1, check_only);
+}
+
 }  // namespace ol
 
 using namespace ol;
@@ -1041,13 +1055,8 @@ ol_status ol_decode_step(int32_t layout, const void* cache_desc, void* updated, 
                          const void* new_kv, const int32_t* lens_host, const int32_t* lens_dev, float scale,
                          int32_t window, void* out, int32_t out_dtype, void* workspace, size_t ws_bytes,
                          ol_stream stream) {
-  CacheView v;
-  ol_status st = view_of(layout, cache_desc, v);
-  if (st != OL_OK) return st;
-  if ((st = writable(v, updated)) != OL_OK) return st;
-  if (!new_kv) return OL_ERR_NULL;
-  return run_attention(layout, cache_desc, v, q, q_heads, lens_host, lens_dev, new_kv, 1, 1, scale, window, out,
-                       out_dtype, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+  return ol::decode_step_impl(layout, cache_desc, updated, q, q_heads, new_kv, lens_host, lens_dev, scale, window,
+                              out, out_dtype, workspace, ws_bytes, stream, false);
 }
 
 // Staging offsets inside the workspace for ol_decode_step_host, after the

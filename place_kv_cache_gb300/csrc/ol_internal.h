@@ -139,6 +139,13 @@ struct QuantizeParams {
 cudaError_t launch_hpaged_quantize(const QuantizeParams& p, cudaStream_t s);
 cudaError_t launch_hpaged_append(const AppendParams& p, cudaStream_t s);
 
+// ol_decode_step; with check_only every check runs and nothing is recorded or
+// launched (OL_OK: the call would enqueue its launch).
+ol_status decode_step_impl(int32_t layout, const void* cache_desc, void* updated, const void* q, int32_t q_heads,
+                           const void* new_kv, const int32_t* lens_host, const int32_t* lens_dev, float scale,
+                           int32_t window, void* out, int32_t out_dtype, void* workspace, size_t ws_bytes,
+                           ol_stream stream, bool check_only);
+
 // Launchers (return cudaSuccess or the launch error).
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_generic_attention(const AttnParams& p, cudaStream_t s);

@@ -29,47 +29,48 @@ void* scratch_for_current_device() {
   return g_scratch_ptr[dev];
 }
 
-ol_status sizes_of(int32_t layout, const void* desc, int32_t* batch, int32_t* kv_heads, int32_t* head_dim) {
-  if (!desc) return OL_ERR_NULL;
-  switch (layout) {
-    case OL_LAYOUT_CONTIGUOUS: {
-      const ol_kv_cache* c = static_cast<const ol_kv_cache*>(desc);
-      *batch = c->batch, *kv_heads = c->kv_heads, *head_dim = c->head_dim;
-      return OL_OK;
-    }
-    case OL_LAYOUT_PAGED: {
-      const ol_paged_kv* c = static_cast<const ol_paged_kv*>(desc);
-      *batch = c->batch, *kv_heads = c->kv_heads, *head_dim = c->head_dim;
-      return OL_OK;
-    }
-    case OL_LAYOUT_INT4: {
-      const ol_int4_kv* c = static_cast<const ol_int4_kv*>(desc);
-      *batch = c->batch, *kv_heads = c->kv_heads, *head_dim = c->head_dim;
-      return OL_OK;
-    }
-    default:
-      return OL_ERR_UNSUPPORTED;
-  }
-}
-
 }  // namespace
 
 extern "C" ol_status ol_decode_step_noalloc(int32_t layout, const void* cache_desc, void* updated, const void* q,
                                             int32_t q_heads, const void* new_kv, const int32_t* lens_host,
                                             const int32_t* lens_dev, float scale, int32_t window, void* out,
                                             int32_t out_dtype, ol_stream stream) {
-  int32_t batch = 0, kv_heads = 0, head_dim = 0;
-  ol_status st = sizes_of(layout, cache_desc, &batch, &kv_heads, &head_dim);
-  if (st != OL_OK) return st;
-  if (batch < 0 || kv_heads <= 0 || head_dim <= 0 || q_heads <= 0 || q_heads % kv_heads != 0) return OL_ERR_SHAPE;
-  const size_t need = ol::workspace_bytes(batch, q_heads, kv_heads, head_dim);
-  if (need > OL_NOALLOC_SCRATCH_BYTES) return OL_ERR_WORKSPACE;
   void* scratch = scratch_for_current_device();
   if (!scratch) return OL_ERR_CUDA;
-  // The ticket counters and status word must start at zero; the partials are
-  // always written before they are read.
+  // Every check of ol_decode_step first (the scratch size included: a request
+  // whose workspace exceeds it is OL_ERR_WORKSPACE), so a rejected call
+  // enqueues nothing and returns what ol_decode_step would.
+  ol_status st = ol::decode_step_impl(layout, cache_desc, updated, q, q_heads, new_kv, lens_host, lens_dev, scale,
+                                      window, out, out_dtype, scratch, OL_NOALLOC_SCRATCH_BYTES, stream, true);
+  if (st != OL_OK) return st;
+  // The status word and the ticket counters must start at zero (an earlier
+  // call may have been cut short); the partials are written before they are read.
+  int32_t batch = 0, kv_heads = 0;
+  switch (layout) {
+    case OL_LAYOUT_CONTIGUOUS:
+      batch = static_cast<const ol_kv_cache*>(cache_desc)->batch;
+      kv_heads = static_cast<const ol_kv_cache*>(cache_desc)->kv_heads;
+      break;
+    case OL_LAYOUT_PAGED:
+      batch = static_cast<const ol_paged_kv*>(cache_desc)->batch;
+      kv_heads = static_cast<const ol_paged_kv*>(cache_desc)->kv_heads;
+      break;
+    case OL_LAYOUT_INT4:
+      batch = static_cast<const ol_int4_kv*>(cache_desc)->batch;
+      kv_heads = static_cast<const ol_int4_kv*>(cache_desc)->kv_heads;
+      break;
+    default:  // not reached: the checks above accept only the three layouts
+      return OL_ERR_UNSUPPORTED;
+  }
   const size_t zero_bytes = ol::partials_offset(batch, kv_heads);
   if (cudaMemsetAsync(scratch, 0, zero_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess) return OL_ERR_CUDA;
   return ol_decode_step(layout, cache_desc, updated, q, q_heads, new_kv, lens_host, lens_dev, scale, window, out,
                         out_dtype, scratch, OL_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+extern "C" ol_status ol_noalloc_status(int32_t* status_out, ol_stream stream) {
+  if (!status_out) return OL_ERR_NULL;
+  void* scratch = scratch_for_current_device();
+  if (!scratch) return OL_ERR_CUDA;
+  return ol_workspace_status(scratch, status_out, stream);
 }
