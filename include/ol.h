@@ -107,6 +107,20 @@ typedef enum ol_quant_mode {
   OL_Q_FIXED = 1    /* scale = fp16(fixed_scale), zp = fixed_zp for every block */
 } ol_quant_mode;
 
+/*
+ * Launch tuning. The library plans every launch itself (kernel variant, split
+ * length, cluster size, CTA waves) from the call's sizes and the device. For
+ * measurement and for test coverage of the plans it does not pick by default,
+ * the environment variable OL_TUNE, read once per process at the first call
+ * that plans a launch, overrides parts of the plan: a comma-separated list of
+ * key=value with keys waves (CTA waves of a split plan), minchunk (smallest
+ * split, tokens), cfg (tensor-core variant 0..4), cluster (largest cluster
+ * size), cpu (clusters per row and kv head), generic (1: CUDA-core kernel for
+ * heterogeneous pages), hpwaves and cwaves (CTA waves of heterogeneous-page and
+ * chunked plans). Unknown keys and out-of-range values are ignored. Results
+ * stay within the same tolerances under every setting; only speed changes.
+ */
+
 /* Device status word values (ol_workspace_status). */
 enum { OL_DEVICE_OK = 0, OL_DEVICE_GUARD = 1 };
 
@@ -291,19 +305,36 @@ OL_API ol_status ol_paged_cache_update(const ol_paged_kv* kv, void* updated_pool
                                 const int32_t* positions_dev, ol_stream stream);
 
 /*
- * Decode attention over a contiguous cache (read-only use of the cache).
+ * Decode attention over a contiguous cache (read-only use of the cache): the
+ * Attention contract of page "Persistent input/output feedback", sections
+ * Optional heterogeneous paged KV and Versioned operator schema (causal by
+ * default, left_window_size, query heads a multiple of the KV heads, online
+ * softmax over the valid and visible tokens only, Y in the dtype of Q unless
+ * fp32 is asked for) over the cache layout of page "Mutable execution cache",
+ * section Model example.
  * q [batch, q_heads, head_dim] (cache dtype); out [batch, q_heads, head_dim]
  * in out_dtype. Query head h reads kv head h / (q_heads / kv_heads). Row b
  * attends its visible tokens: [0, lens[b]) if window < 0, else
  * [max(0, lens[b] - 1 - window), lens[b]). lens[b] == 0 gives out = 0.
  * scale <= 0 selects 1/sqrt(head_dim).
+ * Errors: NULL, ALIAS (q, out, lens_dev or workspace overlapping the cache;
+ * out overlapping q or the workspace), CAPACITY (lens[b] outside
+ * [0, capacity]), SHAPE, DTYPE, WORKSPACE, BUSY, ALIGN, UNSUPPORTED
+ * (head_dim > 256), CUDA.
  */
 OL_API ol_status ol_decode_attention(const ol_kv_cache* cache, const void* q, int32_t q_heads,
                               const int32_t* lens_host, const int32_t* lens_dev, float scale,
                               int32_t window, void* out, int32_t out_dtype, void* workspace,
                               size_t ws_bytes, ol_stream stream);
 
-/* Decode attention over a paged cache; as ol_decode_attention. */
+/*
+ * Decode attention over a paged cache: the same Attention contract (page
+ * "Persistent input/output feedback", section Optional heterogeneous paged
+ * KV) over a fixed pool addressed through the block table (page "Mutable
+ * execution cache", section ONNX Runtime GenAI: logical pages map to slices of
+ * the pool). Arguments, visibility and errors as ol_decode_attention; every
+ * page the visible range reaches must be in [0, num_pages) (OL_ERR_PAGE).
+ */
 OL_API ol_status ol_paged_decode_attention(const ol_paged_kv* kv, const void* q, int32_t q_heads,
                                     const int32_t* lens_host, const int32_t* lens_dev,
                                     float scale, int32_t window, void* out, int32_t out_dtype,
