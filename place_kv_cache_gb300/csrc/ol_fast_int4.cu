@@ -16,8 +16,10 @@
 //        c * 2^-24, or 16c * 2^-24 one nibble up, which q absorbs as q / 16);
 //        one more k-step adds zp_K * (-sum of the block's q). Then
 //        s = sum_b scale_K[t,b] * acc_b.
-//   O^T: V^T as exact bf16 (128 + c) - (128 + zp_V) per token, the V scale
-//        folded into P^T per block, P^T carried as bf16 hi + lo.
+//   O^T: the V code words masked in place as fp16 subnormals (as for K), the
+//        V scale folded into P^T per block, one fp16 per weight under a
+//        warp-uniform power of two, and zp_V taken off by one more MMA per
+//        block half with A = -zp.
 // The token being appended (fused step) takes part uncompressed from new_kv as
 // one extra merge state, and is quantized into the cache by the same CTA.
 #include <cuda_bf16.h>
@@ -36,6 +38,7 @@ constexpr uint32_t kLoNib = 0x000F000Fu;  // nibble in bits 0..3 of both 16-bit 
 constexpr uint32_t kHiNib = 0x00F000F0u;  // nibble in bits 4..7 of both halves
 constexpr int kStateBytes = 8 * kOStride * 4;  // one warp's [8][kOStride] fp32 state
 constexpr float kLazy = 8.f;  // log2 headroom of the lazy softmax maximum
+constexpr int kNoExp = -1000;  // no V exponent chosen yet (no tile seen)
 
 // A stage: NWARPS tiles of 16 tokens. Byte offsets (NW = NWARPS):
 //   K codes [16NW][64] @0, V codes @1024NW, K scales [16NW][4] fp16 @2048NW,
@@ -268,6 +271,7 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   float m_run0 = -INFINITY, m_run1 = -INFINITY, l_run0 = 0.f, l_run1 = 0.f;
+  int ev = kNoExp;  // O is held in units of 2^(ev - 24) (V side, see the tile)
   const int codes_hi = p.cur_from_new ? w.hi - 1 : w.hi;  // tokens below this come from the codes
   const int t_stop = min(w.t_end, codes_hi);
 
@@ -349,15 +353,48 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
     l_run0 += p00 + p10;
     l_run1 += p01 + p11;
 
-    // ---- O^T += V^T P^T, block by block: A = exact bf16 (c - zp_V), the V
-    // scale folded into P^T, P^T carried as bf16 hi + lo
+    // ---- O^T += V^T P^T, block by block. A = the V code words masked in
+    // place: fp16 subnormals c * 2^-24 (rows n: dims 32b + 4n + 2h), or
+    // 16c * 2^-24 for a code in bits 4..7 (rows n + 8: dims 32b + 4n + 2h + 1,
+    // which therefore hold 16 O and are scaled back when the state is
+    // stored). B = P^T times the token's V scale and 2^ev, one fp16 per
+    // weight. One more MMA per (block, half) with A = -zp (the same in every
+    // row, x16 in rows n + 8) adds -zp * P^T, so A needs no subtraction.
+    // ev is warp-uniform: 2^kLazy * (largest V scale of the tile) * 2^ev stays
+    // below 2^15, and O is held in units of 2^(ev - 24); it is rescaled only
+    // when the tile needs a smaller ev, or a much larger one.
     const uint2 sva = lds_v2(vsc + 8 * n), svb = lds_v2(vsc + 8 * n + 64);
-    float2 va01 = half2_bits_to_float2(sva.x), va23 = half2_bits_to_float2(sva.y);
-    float2 vb01 = half2_bits_to_float2(svb.x), vb23 = half2_bits_to_float2(svb.y);
+    uint32_t sa0 = sva.x, sa1 = sva.y, sb0 = svb.x, sb1 = svb.y;
     if (!FULL) {  // a hidden token's scale may be anything: its weight is exactly 0
-      if (!va) va01 = va23 = make_float2(0.f, 0.f);
-      if (!vb) vb01 = vb23 = make_float2(0.f, 0.f);
+      if (!va) sa0 = sa1 = 0u;
+      if (!vb) sb0 = sb1 = 0u;
     }
+    {
+      // largest scale of the tile (positive fp16 order as unsigned integers)
+      uint32_t mx = __vmaxu2(__vmaxu2(sa0, sa1), __vmaxu2(sb0, sb1));
+      mx = max(mx & 0xffffu, mx >> 16);
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const int e_want = 21 - (int)((mx >> 10) & 31u);  // scale < 2^(field - 14)
+      if (e_want < ev || e_want > ev + 6) {
+        if (ev != kNoExp) {
+          const float f = ldexpf(1.f, e_want - ev);
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            o[mt][0] *= f;
+            o[mt][1] *= f;
+            o[mt][2] *= f;
+            o[mt][3] *= f;
+          }
+        }
+        ev = e_want;
+      }
+    }
+    const float pe = ldexpf(1.f, ev);
+    const float pa0 = p00 * pe, pa1 = p01 * pe, pb0 = p10 * pe, pb1 = p11 * pe;
+    const float2 va01 = half2_bits_to_float2(sa0), va23 = half2_bits_to_float2(sa1);
+    const float2 vb01 = half2_bits_to_float2(sb0), vb23 = half2_bits_to_float2(sb1);
     // zero points of the lane's V^T columns: tokens (2c, 2c+1) and (2c+8, 2c+9)
     // in the two 16-bit halves
     const uint32_t zv01 = lds_u32(vz + 4 * c), zv89 = lds_u32(vz + 4 * c + 16);
@@ -368,22 +405,17 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
     for (int b = 0; b < 4; ++b) {
       const float sca = b == 0 ? va01.x : b == 1 ? va01.y : b == 2 ? va23.x : va23.y;
       const float scb = b == 0 ? vb01.x : b == 1 ? vb01.y : b == 2 ? vb23.x : vb23.y;
-      const float q00 = p00 * sca, q01 = p01 * sca, q10 = p10 * scb, q11 = p11 * scb;
-      const uint32_t h0 = pack_bf16x2(q00, q01), h1 = pack_bf16x2(q10, q11);
-      const uint32_t l0 = pack_bf16x2(q00 - __uint_as_float(h0 << 16), q01 - __uint_as_float(h0 & 0xffff0000u));
-      const uint32_t l1 = pack_bf16x2(q10 - __uint_as_float(h1 << 16), q11 - __uint_as_float(h1 & 0xffff0000u));
+      const uint32_t h0 = pack_f16x2(pa0 * sca, pa1 * sca), h1 = pack_f16x2(pb0 * scb, pb1 * scb);
       const uint32_t ph0 = movmatrix_trans(h0), ph1 = movmatrix_trans(h1);
-      const uint32_t pl0 = movmatrix_trans(l0), pl1 = movmatrix_trans(l1);
-      const uint32_t w01 = vw[b][0], w89 = vw[b][1];
-      const uint32_t z01 = code_pair(zv01, 4 * b), z89 = code_pair(zv89, 4 * b);  // (128 + zp) per token
+      // -zp as fp16 subnormals: rows n (x1) and n + 8 (x16)
+      const uint32_t t01 = zv01 >> (4 * b), t89 = zv89 >> (4 * b);
+      const uint32_t zl01 = (t01 & kLoNib) | 0x80008000u, zh01 = ((t01 << 4) & kHiNib) | 0x80008000u;
+      const uint32_t zl89 = (t89 & kLoNib) | 0x80008000u, zh89 = ((t89 << 4) & kHiNib) | 0x80008000u;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const uint32_t a0 = hsub2_bf16(code_pair(w01, 8 * h), z01);
-        const uint32_t a1 = hsub2_bf16(code_pair(w01, 8 * h + 4), z01);
-        const uint32_t a2 = hsub2_bf16(code_pair(w89, 8 * h), z89);
-        const uint32_t a3 = hsub2_bf16(code_pair(w89, 8 * h + 4), z89);
-        mma_bf16_16816(o[2 * b + h], a0, a1, a2, a3, ph0, ph1);
-        mma_bf16_16816(o[2 * b + h], a0, a1, a2, a3, pl0, pl1);
+        const uint32_t w01 = vw[b][0] >> (8 * h), w89 = vw[b][1] >> (8 * h);
+        mma_f16_16816(o[2 * b + h], w01 & kLoNib, w01 & kHiNib, w89 & kLoNib, w89 & kHiNib, ph0, ph1);
+        mma_f16_16816(o[2 * b + h], zl01, zh01, zl89, zh89, ph0, ph1);
       }
     }
   };
@@ -450,6 +482,16 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
   }
   __syncthreads();  // all stages consumed: they now hold the warps' states
 
+  if (ev != kNoExp) {  // O to plain units: 2^(24 - ev), and 1/16 more for the rows of upper-nibble dims
+    const float f = ldexpf(1.f, 24 - ev), f16 = f * 0.0625f;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      o[mt][0] *= f;
+      o[mt][1] *= f;
+      o[mt][2] *= f16;
+      o[mt][3] *= f16;
+    }
+  }
   store_warp_state<true>(reinterpret_cast<float*>(stages + warp * kStateBytes), ms, warp, o, m_run0, m_run1, l_run0, l_run1);
 
   __syncthreads();  // every tile is consumed: the appended row may be rewritten
