@@ -114,6 +114,12 @@ def step_bytes(w, lens):
     elt = 2 if w.dtype == "bf16" else 4
     D = w.head_dim
     T = w.chunk
+    if T > 1 and w.layout == "int4":
+        # history codes, scales and zero points; the chunk read uncompressed (bf16) and
+        # written quantized; T queries and outputs
+        kv_tok = 2 * (D // 2 + (D // 32) * 2 + D // 64)
+        hist = float(np.sum(lens - T)) * w.kv_heads * kv_tok
+        return hist + w.batch * w.kv_heads * T * (2 * D * 2 + kv_tok) + 2 * w.batch * w.q_heads * T * D * 2
     if T > 1:
         hist = float(np.sum(lens - T)) * w.kv_heads * 2 * D * elt
         new = w.batch * w.kv_heads * T * 2 * D * elt
@@ -397,7 +403,10 @@ class Setup:
 # The headline workload is the largest one that fits one GPU (the paged pool of
 # 64 rows); every other workload is measured in the same run under per_config.
 HEADLINE = "paged_b64"
-PER_CONFIG = ("qwen_b1_gqa7", "ragged_b32", "int4_b16", "chunk4_b32", "hpaged_b64")
+PER_CONFIG = ("qwen_b1_gqa7", "ragged_b32", "int4_b16", "chunk4_b32", "int4chunk4_b16", "hpaged_b64")
+# oracle samples cut to fewer rows where the oracle's own composition is slow
+# (the INT4 chunked attention decodes the history row by row in Python)
+ORACLE_ROWS = {"int4chunk4_b16": 2}
 
 
 def workload_of(name, rows=None):
@@ -620,7 +629,7 @@ def oracle_units(w, n_threads):
     import oracle as O
     from workloads import block_table, contiguous_cache, poisoned_pool, scaled
     by_head = w.batch == 1
-    rows = 1 if by_head else min(w.batch, n_threads)
+    rows = 1 if by_head else min(w.batch, n_threads, ORACLE_ROWS.get(w.name, w.batch))
     ws = scaled(w, batch=rows)
     if w.layout in ("paged", "hpaged"):
         ws = scaled(ws, num_pages=rows * w.max_pages_per_row)
@@ -667,6 +676,16 @@ def oracle_units(w, n_threads):
                 units.append(lambda c=c, k=k, qq=qq, lb=lb: (O.cache_update(c, k, lb - 1),
                                                              O.decode_attention(qq, c, lb)))
         del cache
+    elif w.layout == "int4" and T > 1:
+        def quantized(b):
+            planes = O.int4_planes(1, H, ws.capacity, D)
+            O.int4_append(*planes, np.ascontiguousarray(case.history[b][:, None]), [0])
+            return planes
+        for b, planes in zip(range(rows), build(quantized, list(range(rows)))):
+            k = np.ascontiguousarray(kv[:, b:b + 1])
+            qq, lb = sl_q(b, None), np.ascontiguousarray(lens[b:b + 1])
+            units.append(lambda pl=planes, k=k, qq=qq, lb=lb: (O.int4_chunk_attention(qq, *pl, lb, T, k),
+                                                               O.int4_append(*pl, k, lb - T)))
     elif w.layout == "int4":
         def quantized(piece):
             b, g = piece

@@ -157,7 +157,7 @@ void plan_fast(AttnParams& p, const int32_t* lens_host, int sms, int force_varia
   if (per_sm < 1) per_sm = 1;
   const long long slots = (long long)sms * per_sm;
   p.streamk = 0;
-  if (int4 && units > 0 && slots <= 4096 && tune().cluster <= 0) {
+  if (int4 && p.nq == 1 && units > 0 && slots <= 4096 && tune().cluster <= 0) {
     // Stream-K: the INT4 kernel is bound by instruction throughput, so every
     // SM gets the same number of tiles (whole CTAs per (row, kv head) leave
     // some SMs with more). Used when every row has tiles and a CTA gets at
@@ -638,6 +638,13 @@ void record_hpaged(const ol_hpaged_kv* c, const int32_t* read_lo, const int32_t*
   record(s);
 }
 
+// The INT4 tensor-core kernel takes the step: a chunked step's query tokens
+// share a CTA as extra MMA columns, 8 / group of them (p.tq).
+bool int4_fast_path(AttnParams& p) {
+  p.tq = p.nq > 1 ? std::max(1, std::min(p.nq, 8 / std::max(1, p.group))) : 1;
+  return fast_int4_supported(p);
+}
+
 // nq > 1: a chunked step's attention (query tokens z = 0..nq-1 per row, token z
 // at position lens - nq + z; q and y are [B, Hq, nq, D]). check_only: stop
 // after validation (nothing recorded, nothing launched).
@@ -768,7 +775,7 @@ ol_status run_attention(int layout, const void* desc, const CacheView& v, const 
     plan_fast(p, lens_host, sms);
     order_rows(p, lens_host);
     e = launch_fast_bf16(p, stream);
-  } else if (layout == OL_LAYOUT_INT4 && fast_int4_supported(p)) {
+  } else if (layout == OL_LAYOUT_INT4 && int4_fast_path(p)) {
     plan_fast(p, lens_host, sms);
     order_rows(p, lens_host);
     e = launch_fast_int4(p, stream);
@@ -778,6 +785,7 @@ ol_status run_attention(int layout, const void* desc, const CacheView& v, const 
     p.variant = 0;
     e = launch_fast_hpaged(p, stream);
   } else {
+    p.tq = 1;  // the CUDA-core kernel serves one query token per grid slice
     plan_splits(p, lens_host, (long long)sms * 4, 1);
     order_rows(p, lens_host);
     p.variant = 0;

@@ -88,7 +88,12 @@ __device__ __forceinline__ int swz64(int r, int x) {
   return r * 64 + ((((x >> 4) ^ (r >> 1)) & 3) << 4) + (x & 15);
 }
 
-template <int NWARPS, int STAGES>
+// CHUNK: a chunked step's attention (grid x = slice of query tokens, y = the
+// plan's CTA): state columns are (query token, head) pairs, each masked to its
+// token's window; the history ends where the chunk starts, and the chunk's
+// tokens take part uncompressed from new_kv as one causal extra state per
+// column. Its own instantiation: the decode kernel keeps its own code.
+template <int NWARPS, int STAGES, bool CHUNK = false>
 __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerSm)
     fast_int4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
                      const __grid_constant__ CUtensorMap tm_zps, const __grid_constant__ AttnParams p) {
@@ -145,8 +150,9 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
   if (warp == 0) {
     Work w = p.streamk ? map_streamk_warp(lens, p.batch, p.kv_heads, p.capacity, p.window, p.total_ctas,
                                           blockIdx.x, next, lens_status)
-                       : map_cta_warp(lens, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, blockIdx.x,
+                       : map_cta_warp(lens, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, cta_index(p),
                                       lens_status, CS, p.inline_lens && p.ordered ? p.row_order : nullptr);
+    if (CHUNK) slice_query(w, p);
     if (lane == 0) *sw = w;
   }
   __syncthreads();
@@ -160,7 +166,9 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
   const int C = p.capacity;
   const int nsub = w.valid ? (w.t_end - w.t_begin + kTok - 1) / kTok : 0;  // tiles of the CTA
   const int nstage = (nsub + NWARPS - 1) / NWARPS;                              // stages of the CTA
-  const uint64_t pol = policy_evict_first();
+  // a decode step reads each byte once; a chunked step's slices (adjacent in
+  // launch order) read the same tiles, the later ones from L2
+  const uint64_t pol = CHUNK ? policy_evict_normal() : policy_evict_first();
   const int row0 = (w.b * p.kv_heads + w.g) * C;  // row of token 0 within a plane
   const int rowK0 = row0, rowV0 = p.batch * p.kv_heads * C + row0;
 
@@ -204,10 +212,16 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
   const int c = lane & 3, n = lane >> 2;
   uint32_t qf[4][2][2], qz[4];
   float sfac;  // converts an accumulator (units 2^-24 * 2^eq) to the exp2 domain
+  // A chunked step's column n is head n % G of the slice's query token n / G.
+  const int zs = CHUNK ? query_index(p) : 0;
+  const int ncols = CHUNK ? G * slice_tokens(p, zs) : G;
   {
-    const bool live = n < G && w.valid;
+    const bool live = n < ncols && w.valid;
+    const int nl = live ? n : 0;
     const uint16_t* qp = reinterpret_cast<const uint16_t*>(p.q) +
-                         ((size_t)w.b * p.q_heads + (size_t)w.g * G + (n < G ? n : 0)) * 128;
+                         (CHUNK ? (((size_t)w.b * p.q_heads + (size_t)w.g * G + nl % G) * p.nq + slice_first(p, zs) +
+                                   nl / G) * 128
+                                : ((size_t)w.b * p.q_heads + (size_t)w.g * G + nl) * 128);
     float qv[4][8];
     float mx = 0.f;
 #pragma unroll
@@ -272,8 +286,23 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
   for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   float m_run0 = -INFINITY, m_run1 = -INFINITY, l_run0 = 0.f, l_run1 = 0.f;
   int ev = kNoExp;  // O is held in units of 2^(ev - 24) (V side, see the tile)
-  const int codes_hi = p.cur_from_new ? w.hi - 1 : w.hi;  // tokens below this come from the codes
+  // tokens below codes_hi come from the codes: a decode step's history ends
+  // before its current token, a chunked step's before its chunk (w.hi is one
+  // past the slice's last query token, at position codes_hi + zlast)
+  const int zlast = CHUNK ? slice_first(p, zs) + slice_tokens(p, zs) - 1 : 0;
+  const int codes_hi = CHUNK ? w.hi - 1 - zlast : (p.cur_from_new ? w.hi - 1 : w.hi);
   const int t_stop = min(w.t_end, codes_hi);
+  // visible history of the lane's columns 2c, 2c + 1 (chunked step): from its
+  // query token's window start; a tile is FULL only if it starts at or past
+  // every column's start (the slice's last token has the latest one)
+  int clo0 = w.lo, clo1 = w.lo, lo_full = w.lo;
+  if (CHUNK && p.window_q >= 0) {
+    const int ti0 = min((2 * c) / G, slice_tokens(p, zs) - 1), ti1 = min((2 * c + 1) / G, slice_tokens(p, zs) - 1);
+    const int base = codes_hi + slice_first(p, zs);  // position of the slice's first query token
+    clo0 = max(w.lo, base + ti0 - p.window_q);
+    clo1 = max(w.lo, base + ti1 - p.window_q);
+    lo_full = max(w.lo, codes_hi + zlast - p.window_q);
+  }
 
   // One 16-token tile in stage base sg. FULL: every token of the tile is
   // visible (no masking of scores or scales).
@@ -281,7 +310,7 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
     constexpr bool FULL = decltype(full_tag)::value;
     const uint32_t ksc = sg + S::kOffSk + 128 * warp, vsc = sg + S::kOffSv + 128 * warp;
     const uint32_t kz = sg + S::kOffZk + 32 * warp, vz = sg + S::kOffZv + 32 * warp;
-    bool va = true, vb = true;  // the lane's S^T rows (tokens n, n + 8) are visible
+    bool va = true, vb = true;  // the lane's S^T rows (tokens n, n + 8) are visible (to some column)
     if (!FULL) {
       va = t0 + n >= w.lo && t0 + n < t_stop;
       vb = t0 + n + 8 >= w.lo && t0 + n + 8 < t_stop;
@@ -315,10 +344,17 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
     s10 *= sfac;
     s11 *= sfac;
     if (!FULL) {
-      s00 = va ? s00 : -INFINITY;
-      s01 = va ? s01 : -INFINITY;
-      s10 = vb ? s10 : -INFINITY;
-      s11 = vb ? s11 : -INFINITY;
+      if (CHUNK) {  // each column from its own window start
+        s00 = va && t0 + n >= clo0 ? s00 : -INFINITY;
+        s01 = va && t0 + n >= clo1 ? s01 : -INFINITY;
+        s10 = vb && t0 + n + 8 >= clo0 ? s10 : -INFINITY;
+        s11 = vb && t0 + n + 8 >= clo1 ? s11 : -INFINITY;
+      } else {
+        s00 = va ? s00 : -INFINITY;
+        s01 = va ? s01 : -INFINITY;
+        s10 = vb ? s10 : -INFINITY;
+        s11 = vb ? s11 : -INFINITY;
+      }
     }
 
     // ---- online softmax (exp2 domain) with a lazy maximum: the weights are
@@ -427,6 +463,53 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
   const int cur = p.cur_from_new ? w.hi - 1 : -1;
   const bool has_cur = w.valid && cur >= w.t_begin && cur < w.t_end;
   if (has_cur && warp == 0) {
+    if (CHUNK) {
+      // column j (query token ti = j / G of the slice, head j % G) attends the
+      // chunk's tokens 0 .. ti within its window, uncompressed: scores, then
+      // (m, l, o) of that softmax as the column's extra state
+      const int nq = p.nq, z0 = slice_first(p, zs);
+      const size_t kv_row = ((size_t)w.b * p.kv_heads + w.g) * nq;
+      const uint16_t* nk = reinterpret_cast<const uint16_t*>(p.new_kv) + kv_row * 128;
+      const uint16_t* nv = reinterpret_cast<const uint16_t*>(p.new_kv) +
+                           ((size_t)p.batch * p.kv_heads * nq + kv_row) * 128;
+      for (int j = 0; j < 8; ++j) {
+        float mj = -INFINITY, lj = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+        if (j < ncols) {
+          const int ti = z0 + j / G, h = j % G;
+          const uint16_t* qj = reinterpret_cast<const uint16_t*>(p.q) +
+                               (((size_t)w.b * p.q_heads + (size_t)w.g * G + h) * nq + ti) * 128;
+          const uint2 qq = *reinterpret_cast<const uint2*>(qj + 4 * lane);
+          const float q0 = __uint_as_float(qq.x << 16), q1 = __uint_as_float(qq.x & 0xffff0000u);
+          const float q2 = __uint_as_float(qq.y << 16), q3 = __uint_as_float(qq.y & 0xffff0000u);
+          const int t_first = p.window_q < 0 ? 0 : max(0, ti - p.window_q);
+          for (int t = t_first; t <= ti; ++t) {
+            const uint2 kk = *reinterpret_cast<const uint2*>(nk + (size_t)t * 128 + 4 * lane);
+            float acc = q0 * __uint_as_float(kk.x << 16) + q1 * __uint_as_float(kk.x & 0xffff0000u) +
+                        q2 * __uint_as_float(kk.y << 16) + q3 * __uint_as_float(kk.y & 0xffff0000u);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            const float st = acc * p.scale_log2;
+            const float mn = fmaxf(mj, st);
+            const float al = fast_exp2(mj - mn), pt = fast_exp2(st - mn);
+            const uint2 vv = *reinterpret_cast<const uint2*>(nv + (size_t)t * 128 + 4 * lane);
+            lj = lj * al + pt;
+            o0 = o0 * al + pt * __uint_as_float(vv.x << 16);
+            o1 = o1 * al + pt * __uint_as_float(vv.x & 0xffff0000u);
+            o2 = o2 * al + pt * __uint_as_float(vv.y << 16);
+            o3 = o3 * al + pt * __uint_as_float(vv.y & 0xffff0000u);
+            mj = mn;
+          }
+        }
+        extra_o[j * kOStride + 4 * lane + 0] = o0;
+        extra_o[j * kOStride + 4 * lane + 1] = o1;
+        extra_o[j * kOStride + 4 * lane + 2] = o2;
+        extra_o[j * kOStride + 4 * lane + 3] = o3;
+        if (lane == 0) {
+          ms.wm[NWARPS * 8 + j] = mj;
+          ms.wl[NWARPS * 8 + j] = lj;
+        }
+      }
+    } else {
     const uint16_t* nk = reinterpret_cast<const uint16_t*>(p.new_kv) + ((size_t)w.b * p.kv_heads + w.g) * 128;
     const uint16_t* nv = reinterpret_cast<const uint16_t*>(p.new_kv) + (((size_t)p.batch + w.b) * p.kv_heads + w.g) * 128;
     const uint2 kk = *reinterpret_cast<const uint2*>(nk + 4 * lane);
@@ -453,6 +536,7 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
         ms.wl[NWARPS * 8 + j] = j < G ? 1.f : 0.f;
       }
     }
+    }
   }
   for (int j = 0; j < nstage; ++j) {
     const int tile_idx = j * NWARPS + warp;
@@ -464,7 +548,7 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
     }
     const int t0 = w.t_begin + tile_idx * kTok;
     const uint32_t sg = smem_u32(stages + st * S::kBytes);
-    if (t0 >= w.lo && t0 + kTok <= t_stop)
+    if (t0 >= lo_full && t0 + kTok <= t_stop)
       tile(sg, t0, std::true_type{});
     else
       tile(sg, t0, std::false_type{});
@@ -509,7 +593,7 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
         return s < NWARPS ? reinterpret_cast<const float*>(stages + s * kStateBytes)
                           : static_cast<const float*>(extra_o);
       },
-      merged, cmerged, ms);
+      merged, cmerged, ms, CHUNK ? zs : -1);
   jbase += nstage;
   if (!p.streamk || w.next < 0) break;
   next = w.next;
@@ -559,10 +643,10 @@ bool encode_int4_maps(CUtensorMap (&maps)[3], const AttnParams& p, int nwarps) {
          encode_planes(&maps[2], p.zps, 16, rows / 8, tok / 8, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-template <int NWARPS, int STAGES>
+template <int NWARPS, int STAGES, bool CHUNK = false>
 cudaError_t ensure_attrs() {
   static cudaError_t state = [] {
-    auto kern = fast_int4_kernel<NWARPS, STAGES>;
+    auto kern = fast_int4_kernel<NWARPS, STAGES, CHUNK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Int4Layout<NWARPS, STAGES>::kTotal);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -597,14 +681,16 @@ int max_cluster() {
   return cs;
 }
 
-template <int NWARPS, int STAGES>
+template <int NWARPS, int STAGES, bool CHUNK>
 cudaError_t launch_cfg(const AttnParams& p, cudaStream_t s) {
   CUtensorMap maps[3];
   if (!encode_int4_maps(maps, p, NWARPS)) return cudaErrorInvalidValue;
-  cudaError_t e = ensure_attrs<NWARPS, STAGES>();
+  cudaError_t e = ensure_attrs<NWARPS, STAGES, CHUNK>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.total_ctas, 1, 1);
+  // a chunked step: slices of query tokens along x, the plan's CTAs (and clusters) along y
+  const int slices = CHUNK ? (p.nq + p.tq - 1) / p.tq : 1;
+  cfg.gridDim = CHUNK ? dim3(slices, p.total_ctas, 1) : dim3(p.total_ctas, 1, 1);
   cfg.blockDim = dim3(NWARPS * 32, 1, 1);
   cfg.dynamicSmemBytes = Int4Layout<NWARPS, STAGES>::kTotal;
   cfg.stream = s;
@@ -612,18 +698,20 @@ cudaError_t launch_cfg(const AttnParams& p, cudaStream_t s) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = p.cluster;
-  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.x = CHUNK ? 1 : p.cluster;
+  attr[1].val.clusterDim.y = CHUNK ? p.cluster : 1;
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, fast_int4_kernel<NWARPS, STAGES>, maps[0], maps[1], maps[2], p);
+  return cudaLaunchKernelEx(&cfg, fast_int4_kernel<NWARPS, STAGES, CHUNK>, maps[0], maps[1], maps[2], p);
 }
 
 }  // namespace
 
 bool fast_int4_supported(const AttnParams& p) {
-  if (p.layout != OL_LAYOUT_INT4 || p.head_dim != 128 || p.group > 8 || p.nq != 1) return false;
+  if (p.layout != OL_LAYOUT_INT4 || p.head_dim != 128 || p.group > 8) return false;
+  // a chunked step: query tokens share a CTA as extra columns (at most 8)
+  if (p.nq > 1 && (p.tq < 1 || p.group * p.tq > 8)) return false;
   // every (row, kv head) starts on a 16-token boundary, so a stage's scale
   // and zero-point boxes start on whole 16-byte rows of their maps
   if (p.capacity % 16 != 0) return false;
@@ -649,10 +737,17 @@ int fast_int4_max_cluster(int variant) {
 
 cudaError_t launch_fast_int4(const AttnParams& p, cudaStream_t s) {
   if (p.total_ctas <= 0) return cudaSuccess;
+  if (p.nq > 1) {
+    switch (p.variant) {
+      case 1: return launch_cfg<4, 4, true>(p, s);
+      case 2: return launch_cfg<8, 2, true>(p, s);
+      default: return launch_cfg<8, 4, true>(p, s);
+    }
+  }
   switch (p.variant) {
-    case 1: return launch_cfg<4, 4>(p, s);
-    case 2: return launch_cfg<8, 2>(p, s);
-    default: return launch_cfg<8, 4>(p, s);
+    case 1: return launch_cfg<4, 4, false>(p, s);
+    case 2: return launch_cfg<8, 2, false>(p, s);
+    default: return launch_cfg<8, 4, false>(p, s);
   }
 }
 

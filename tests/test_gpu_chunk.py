@@ -130,10 +130,15 @@ def test_chunk_of_one_token_is_the_decode_step():
 
 
 INT4 = [
-    # name, B, Hq, Hkv, D, C, lens, T, quant mode
+    # name, B, Hq, Hkv, D, C, lens, T, quant mode (head_dim 128: tensor-core kernel, 8 / group query
+    # tokens per CTA as MMA columns; head_dim 64: CUDA-core kernel)
     ("int4_gqa4_t4", 3, 16, 4, 128, 96, [4, 37, 96], 4, ol.OL_Q_DYNAMIC),
     ("int4_gqa7_t2_fixed", 1, 28, 4, 128, 64, [50], 2, ol.OL_Q_FIXED),
     ("int4_d64_t8", 2, 8, 2, 64, 48, [8, 48], 8, ol.OL_Q_DYNAMIC),
+    ("int4_gqa4_t4_long", 3, 32, 8, 128, 2048, [5, 700, 2048], 4, ol.OL_Q_DYNAMIC),
+    ("int4_gqa8_t3", 2, 16, 2, 128, 512, [300, 512], 3, ol.OL_Q_FIXED),
+    ("int4_gqa2_t8", 2, 4, 2, 128, 272, [8, 200], 8, ol.OL_Q_DYNAMIC),
+    ("int4_gqa1_t5_wide", 1, 6, 6, 128, 1024, [1000], 5, ol.OL_Q_DYNAMIC),
 ]
 
 

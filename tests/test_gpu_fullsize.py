@@ -282,3 +282,52 @@ def test_hpaged_full_size_sampled_rows():
     assert bad.size == 0, f"{len(bad)} pool bytes differ, first at page/byte {bad[0].tolist()}"
     for code, _ in OUTS:
         check(got[code][rows], want, code)
+
+
+def test_int4_chunk4_full_size_sampled_rows():
+    # the INT4 cache of 16 rows taking 4 tokens per row (bench.py's int4chunk4_b16):
+    # attention on the tensor-core kernel with 2 query tokens per CTA (GQA 4), then
+    # the quantized append; every plane byte compared, outputs on two rows
+    w = WORKLOADS["int4chunk4_b16"]
+    T = w.chunk
+    case = make_case(w, history_len_offset=T)
+    rng = np.random.default_rng(w.seed + 7)
+    q = bf16_from_f32(rng.standard_normal((w.batch, w.q_heads, T, w.head_dim)).astype(np.float32))
+    kv = bf16_from_f32(rng.standard_normal((2, w.batch, w.kv_heads, T, w.head_dim)).astype(np.float32))
+
+    def quantized(b):
+        sub = O.int4_planes(1, w.kv_heads, w.capacity, w.head_dim)
+        O.int4_append(*sub, case.history[b][:, None], [0])
+        return sub
+    subs = threaded(quantized, list(range(w.batch)))
+    planes = O.int4_planes(w.batch, w.kv_heads, w.capacity, w.head_dim)
+    for b, sub in enumerate(subs):
+        for full, part in zip(planes, sub):
+            full[:, b] = part[:, 0]
+    del subs
+    case.history = None
+    dplanes = tuple(to_dev(p) for p in planes)
+    desc = ol.int4_kv(*dplanes, head_dim=w.head_dim, access=STABLE)
+    n = ol.ol_workspace_size_chunk(w.batch, w.q_heads, w.kv_heads, w.head_dim, T)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    ol.ol_workspace_init(ws, n)
+    q_d, kv_d, lens_d = to_dev(q), to_dev(kv), to_dev(case.lens)
+    got = {}
+    for code, dt in OUTS:
+        out = torch.full((w.batch, w.q_heads, T, w.head_dim), float("nan"), dtype=dt, device="cuda")
+        ol.ol_chunk_step(ol.OL_LAYOUT_INT4, desc, dplanes[0], q_d, w.q_heads, T, kv_d, case.lens, lens_d, 0.0, -1,
+                         out, code, ws, n)
+        torch.cuda.synchronize()
+        got[code] = out_as_f64(out)
+    assert ol.ol_workspace_status(ws) == ol.OL_DEVICE_OK
+    rows = [0, w.batch - 1]
+
+    def row(b):
+        sub = tuple(np.ascontiguousarray(p[:, b:b + 1]) for p in planes)
+        return O.int4_chunk_attention(q[b:b + 1], *sub, case.lens[b:b + 1], T, np.ascontiguousarray(kv[:, b:b + 1]))[0]
+    want = np.stack(threaded(row, rows))
+    O.int4_append(*planes, kv, case.lens - T)
+    for g, r in zip(dplanes, planes):
+        np.testing.assert_array_equal(to_host(g), r)
+    for code, _ in OUTS:
+        check(got[code][rows], want, code)

@@ -104,6 +104,10 @@ WORKLOADS = {
     # appends and scores its drafted tokens
     "chunk4_b32": Workload("chunk4_b32", "bf16", 32, 32, 8, 128, 8192, "contiguous",
                            seed=6, lens_range=(512, 8192), chunk=4),
+    # the INT4 cache of int4_b16 taking 4 tokens per row per step (chunked step:
+    # the chunk attended uncompressed, then quantized into the cache)
+    "int4chunk4_b16": Workload("int4chunk4_b16", "bf16", 16, 32, 8, 128, 32768, "int4", seed=8,
+                               lens_fixed=16388, chunk=4),
     # heterogeneous pages: the paged shape with every page's K/V formats chosen
     # by its age (AGE_FORMATS): recent pages BFLOAT16, older INT8, oldest 4-bit
     "hpaged_b64": Workload("hpaged_b64", "bf16", 64, 32, 8, 128, 16384, "hpaged", seed=7,
