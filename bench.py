@@ -114,6 +114,24 @@ def step_bytes(w, lens):
     elt = 2 if w.dtype == "bf16" else 4
     D = w.head_dim
     T = w.chunk
+    if w.layout == "hpaged":
+        # each history token in its page's formats (K and V rows of D * bits / 8
+        # bytes), plus a block-table entry and a 24-byte format pair per page;
+        # the T new tokens read uncompressed (bf16) and written in the format of
+        # the pages they start (age 0); T queries and outputs
+        S, M = w.page_size, w.max_pages_per_row
+        cls = page_format_classes(lens, S, M)
+        row = [D * (FORMAT_BITS[k[0]] + FORMAT_BITS[v[0]]) // 8 for _, (k, v) in AGE_FORMATS]
+        hist = 0.0
+        for b, n in enumerate(lens):
+            h = int(n) - T
+            for j in range((h + S - 1) // S):
+                hist += min(S, h - j * S) * row[cls[b, j]]
+        hist = hist * w.kv_heads + float(np.sum(np.ceil(lens / S))) * (4 + 24)
+        cur = w.batch * w.kv_heads * T * 2 * D * 2
+        written = w.batch * w.kv_heads * T * row[0]
+        q = w.batch * w.q_heads * T * D * 2
+        return hist + cur + written + q + q
     if T > 1 and w.layout == "int4":
         # history codes, scales and zero points; the chunk read uncompressed (bf16) and
         # written quantized; T queries and outputs
@@ -124,22 +142,6 @@ def step_bytes(w, lens):
         hist = float(np.sum(lens - T)) * w.kv_heads * 2 * D * elt
         new = w.batch * w.kv_heads * T * 2 * D * elt
         return hist + 2 * new + 2 * w.batch * w.q_heads * T * D * 2   # new K/V written and read; q and y
-    if w.layout == "hpaged":
-        # each history token in its page's formats (K and V rows of D * bits / 8
-        # bytes), plus a block-table entry and a 24-byte format pair per page
-        S, M = w.page_size, w.max_pages_per_row
-        cls = page_format_classes(lens, S, M)
-        row = [D * (FORMAT_BITS[k[0]] + FORMAT_BITS[v[0]]) // 8 for _, (k, v) in AGE_FORMATS]
-        hist = 0.0
-        for b, n in enumerate(lens):
-            h = int(n) - 1
-            for j in range((h + S - 1) // S):
-                hist += min(S, h - j * S) * row[cls[b, j]]
-        hist = hist * w.kv_heads + float(np.sum(np.ceil(lens / S))) * (4 + 24)
-        cur = w.batch * w.kv_heads * 2 * D * 2
-        written = w.batch * w.kv_heads * row[0]
-        q = w.batch * w.q_heads * D * 2
-        return hist + cur + written + q + q
     if w.layout == "int4":
         kv_tok = 2 * (D // 2 + (D // 32) * 2 + D // 64)         # codes + fp16 scales + zero points, K and V
         hist = float(np.sum(lens - 1)) * w.kv_heads * kv_tok
@@ -356,7 +358,7 @@ class Setup:
         bt_d = torch.from_numpy(table).to(self.dev)
         cls = page_format_classes(self.lens, S, M)
         for b in range(B):
-            hist = int(self.lens[b]) - 1
+            hist = int(self.lens[b]) - w.chunk
             row_t = np.ascontiguousarray(table[b:b + 1])
             row_kv = ol.hpaged_kv(pool, fmt_d, mirror, bt_d[b:b + 1], row_t, kv_heads=H, page_size=S, head_dim=D)
             j = 0
@@ -383,6 +385,11 @@ class Setup:
     def step(self, i, stream=None):
         """Step i of the rotation: replica i % replicas, chain position i % chain."""
         r, c = i % self.replicas, i % self.chain
+        if self.w.chunk > 1 and self.w.layout == "hpaged":
+            self.ol.ol_hpaged_chunk_step(self.descs[r], self.updated[r], self.q, self.w.q_heads, self.w.chunk,
+                                         self.new_kv, self.new_pages, self.lens_list[c], self.lens_d_list[c], 0.0, -1,
+                                         self.out, self.ol.OL_BF16, self.ws, self.ws_bytes, stream=stream)
+            return
         if self.w.chunk > 1:
             self.ol.ol_chunk_step(self.layout, self.descs[r], self.updated[r], self.q, self.w.q_heads, self.w.chunk,
                                   self.new_kv, self.lens_list[c], self.lens_d_list[c], 0.0, -1, self.out,
@@ -403,10 +410,11 @@ class Setup:
 # The headline workload is the largest one that fits one GPU (the paged pool of
 # 64 rows); every other workload is measured in the same run under per_config.
 HEADLINE = "paged_b64"
-PER_CONFIG = ("qwen_b1_gqa7", "ragged_b32", "int4_b16", "chunk4_b32", "int4chunk4_b16", "hpaged_b64")
+PER_CONFIG = ("qwen_b1_gqa7", "ragged_b32", "int4_b16", "chunk4_b32", "int4chunk4_b16", "hpaged_b64",
+              "hpchunk4_b64")
 # oracle samples cut to fewer rows where the oracle's own composition is slow
 # (the INT4 chunked attention decodes the history row by row in Python)
-ORACLE_ROWS = {"int4chunk4_b16": 2}
+ORACLE_ROWS = {"int4chunk4_b16": 2, "hpchunk4_b64": 2}
 
 
 def workload_of(name, rows=None):
@@ -735,8 +743,14 @@ def oracle_units(w, n_threads):
         for b, _ in pieces:
             tb, k = np.ascontiguousarray(table[b:b + 1]), np.ascontiguousarray(kv[:, b:b + 1])
             qq, lb = sl_q(b, None), np.ascontiguousarray(lens[b:b + 1])
-            units.append(lambda tb=tb, k=k, qq=qq, lb=lb: (O.hpaged_attention(qq, pool, desc, tb, lb, H, cur_kv=k),
-                                                           O.hpaged_append(pool, desc, tb, k, lb - 1, new_fmt)))
+            if T > 1:
+                units.append(lambda tb=tb, k=k, qq=qq, lb=lb: (
+                    O.hpaged_chunk_attention(qq, pool, desc, tb, lb, H, T, k),
+                    O.hpaged_append(pool, desc, tb, k, lb - T, new_fmt)))
+            else:
+                units.append(lambda tb=tb, k=k, qq=qq, lb=lb: (
+                    O.hpaged_attention(qq, pool, desc, tb, lb, H, cur_kv=k),
+                    O.hpaged_append(pool, desc, tb, k, lb - 1, new_fmt)))
     case.history = None
     what = (f"the {H} kv heads of the single row" if by_head else f"the first {rows} of {w.batch} rows")
     return units, ws, step_bytes(ws, lens), what

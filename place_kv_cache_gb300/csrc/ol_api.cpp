@@ -645,6 +645,13 @@ bool int4_fast_path(AttnParams& p) {
   return fast_int4_supported(p);
 }
 
+// The heterogeneous-page tensor-core kernel takes the step (query tokens of a
+// chunked step as extra columns, as for INT4).
+bool hpaged_fast_path(AttnParams& p) {
+  p.tq = p.nq > 1 ? std::max(1, std::min(p.nq, 8 / std::max(1, p.group))) : 1;
+  return fast_hpaged_supported(p);
+}
+
 // nq > 1: a chunked step's attention (query tokens z = 0..nq-1 per row, token z
 // at position lens - nq + z; q and y are [B, Hq, nq, D]). check_only: stop
 // after validation (nothing recorded, nothing launched).
@@ -779,7 +786,7 @@ ol_status run_attention(int layout, const void* desc, const CacheView& v, const 
     plan_fast(p, lens_host, sms);
     order_rows(p, lens_host);
     e = launch_fast_int4(p, stream);
-  } else if (layout == OL_LAYOUT_HPAGED && fast_hpaged_supported(p) && !tune().generic) {
+  } else if (layout == OL_LAYOUT_HPAGED && hpaged_fast_path(p) && !tune().generic) {
     plan_splits(p, lens_host, (long long)sms * fast_hpaged_ctas_per_sm() * tune().hp_waves, 1);
     order_rows(p, lens_host);
     p.variant = 0;

@@ -160,7 +160,13 @@ __device__ __forceinline__ int map_row(const AttnParams& p, int page, int plane,
 
 // -------------------------------------------------------------- the kernel
 
-template <int NWARPS, int STAGES>
+// CHUNK: a chunked step's attention (grid x = slice of query tokens, y = the
+// split): state columns are (query token, head) pairs, each masked to its
+// token's window; the history ends where the chunk starts, and the chunk's
+// tokens take part uncompressed from new_kv, folded causally into warp 0's
+// state after the tile loop. Its own instantiation: the decode kernel keeps
+// its own code.
+template <int NWARPS, int STAGES, bool CHUNK = false>
 __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
     fast_hpaged_kernel(const __grid_constant__ CUtensorMap tm16, const __grid_constant__ CUtensorMap tm8,
                        const __grid_constant__ CUtensorMap tm4, const __grid_constant__ CUtensorMap tm2,
@@ -206,9 +212,10 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
   pdl_launch_dependents();
   if (warp == 0) {
     Work w = p.inline_lens ? map_cta_warp(p.lens_inline, p.batch, p.kv_heads, p.capacity, p.window, p.chunk,
-                                          blockIdx.x, nullptr, 1, p.ordered ? p.row_order : nullptr)
-                           : map_cta_warp(p.lens, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, blockIdx.x,
+                                          cta_index(p), nullptr, 1, p.ordered ? p.row_order : nullptr)
+                           : map_cta_warp(p.lens, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, cta_index(p),
                                           p.status);
+    if (CHUNK) slice_query(w, p);
     if (lane == 0) *sw = w;
   }
   __syncthreads();
@@ -216,15 +223,20 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
   if (!w.valid) return;
 
   const int G = p.group;
+  // a chunked step's slice zs: query tokens z0 .. zlast; w.hi is one past zlast's position
+  const int zs = CHUNK ? query_index(p) : 0;
+  const int z0 = CHUNK ? slice_first(p, zs) : 0, zlast = CHUNK ? z0 + slice_tokens(p, zs) - 1 : 0;
   const int cur = p.cur_from_new ? w.hi - 1 : -1;
-  // history tiles: [t_begin, tend); the current token (from new_kv) is not read from the cache
-  const int hist_end = p.cur_from_new ? w.hi - 1 : w.hi;
+  // history tiles: [t_begin, tend); the current token (a chunk: the chunk's
+  // tokens up to the slice's last one, from new_kv) is not read from the cache
+  const int hist_end = CHUNK ? w.hi - 1 - zlast : (p.cur_from_new ? w.hi - 1 : w.hi);
   const int tend = min(w.t_end, hist_end);
   const int nsub = tend > w.t_begin ? (tend - w.t_begin + kTok - 1) / kTok : 0;
   const int my_n = nsub > warp ? (nsub - warp + NWARPS - 1) / NWARPS : 0;
   uint8_t* my_stages = stages + warp * STAGES * kStage;
   int* my_info = info + warp * STAGES * kInfo;
-  const uint64_t pol = policy_evict_first();
+  // a chunked step's slices (adjacent in launch order) read the same tiles, the later ones from L2
+  const uint64_t pol = CHUNK ? policy_evict_normal() : policy_evict_first();
   const ol_page_format* __restrict__ fmts = p.page_fmt;
 
   // Look-ahead: lane j holds what the warp needs of its tile la_base + j, so one
@@ -314,11 +326,16 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
   };
   for (int i = 0; i < min(my_n, STAGES); ++i) issue(i);
 
-  // ---- q operands (lane: c = lane % 4, n = lane / 4 = head), written once per CTA by warp 0
+  // ---- q operands (lane: c = lane % 4, n = lane / 4 = state column: the head,
+  // or for a chunked step head n % G of query token z0 + n / G), written once
+  // per CTA by warp 0
   const int c = lane & 3, n = lane >> 2;
-  const bool live = n < G;
-  const uint16_t* qp = reinterpret_cast<const uint16_t*>(p.q) + ((size_t)w.b * p.q_heads + (size_t)w.g * G +
-                                                                 (live ? n : 0)) * 128;
+  const int ncols = CHUNK ? G * (zlast - z0 + 1) : G;
+  const bool live = n < ncols;
+  const int nl = live ? n : 0;
+  const uint16_t* qp = reinterpret_cast<const uint16_t*>(p.q) +
+                       (CHUNK ? (((size_t)w.b * p.q_heads + (size_t)w.g * G + nl % G) * p.nq + z0 + nl / G) * 128
+                              : ((size_t)w.b * p.q_heads + (size_t)w.g * G + nl) * 128);
   if (warp == 0) {
     // this lane's 32 dims 32c .. 32c + 31 of head n: head n's exponent e and sum
     uint32_t qraw[16];
@@ -389,6 +406,15 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
   const float pne0 = pow2f(-e0), pne1 = pow2f(-e1);  // 2^-e of this lane's state columns
   const uint32_t qbase = smem_u32(qsm) + lane * 8;
   auto qop = [&](int order, int kk) { return lds_v2(qbase + (order * 8 + kk) * 256); };
+
+  // visible history of this lane's state columns 2c, 2c + 1: a chunked step's
+  // column from its own query token's window start
+  int clo0 = w.lo, clo1 = w.lo;
+  if (CHUNK && p.window_q >= 0) {
+    const int t0c = min((2 * c) / G, zlast - z0), t1c = min((2 * c + 1) / G, zlast - z0);
+    clo0 = max(w.lo, hist_end + z0 + t0c - p.window_q);
+    clo1 = max(w.lo, hist_end + z0 + t1c - p.window_q);
+  }
 
   float o[8][4];
 #pragma unroll
@@ -539,11 +565,11 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
     // running maximum moves only when a score passes it by more than kLazy, so
     // most tiles skip the warp reduction and the rescale (weights stay <= 2^kLazy)
     const int ta_ = t0 + n, tb_ = ta_ + 8;
-    const bool va_ = ta_ >= w.lo && ta_ < tend, vb_ = tb_ >= w.lo && tb_ < tend;
-    const float s00 = va_ ? fmaf(sa[0] + sb[0], kmul0, -kb0) : -INFINITY;
-    const float s01 = va_ ? fmaf(sa[1] + sb[1], kmul1, -kb1) : -INFINITY;
-    const float s10 = vb_ ? fmaf(sa[2] + sb[2], kmul0, -kb0) : -INFINITY;
-    const float s11 = vb_ ? fmaf(sa[3] + sb[3], kmul1, -kb1) : -INFINITY;
+    const bool va_ = ta_ < tend, vb_ = tb_ < tend;
+    const float s00 = va_ && ta_ >= clo0 ? fmaf(sa[0] + sb[0], kmul0, -kb0) : -INFINITY;
+    const float s01 = va_ && ta_ >= clo1 ? fmaf(sa[1] + sb[1], kmul1, -kb1) : -INFINITY;
+    const float s10 = vb_ && tb_ >= clo0 ? fmaf(sa[2] + sb[2], kmul0, -kb0) : -INFINITY;
+    const float s11 = vb_ && tb_ >= clo1 ? fmaf(sa[3] + sb[3], kmul1, -kb1) : -INFINITY;
     if (__any_sync(0xffffffffu, fmaxf(s00, s10) > m_run0 + kLazy || fmaxf(s01, s11) > m_run1 + kLazy)) {
       float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
 #pragma unroll
@@ -743,7 +769,49 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
     const uint16_t* nk = reinterpret_cast<const uint16_t*>(p.new_kv) + ((size_t)w.b * p.kv_heads + w.g) * 128;
     const uint16_t* nv = reinterpret_cast<const uint16_t*>(p.new_kv) +
                          (((size_t)p.batch + w.b) * p.kv_heads + w.g) * 128;
-    if (warp == 0) {
+    if (warp == 0 && CHUNK) {
+      // the chunk's tokens 0 .. zlast, uncompressed: token t is visible to
+      // column j (query token zj = z0 + j / G) if t <= zj and, with a window,
+      // t >= zj - window
+      const size_t kv_row = ((size_t)w.b * p.kv_heads + w.g) * p.nq;
+      const uint16_t* ck = reinterpret_cast<const uint16_t*>(p.new_kv) + kv_row * 128;
+      const uint16_t* cv = reinterpret_cast<const uint16_t*>(p.new_kv) +
+                           ((size_t)p.batch * p.kv_heads * p.nq + kv_row) * 128;
+      const int zc0 = z0 + (2 * c) / G, zc1 = z0 + (2 * c + 1) / G;
+      for (int t = 0; t <= zlast; ++t) {
+        const uint16_t* kt = ck + (size_t)t * 128;
+        const uint16_t* vt = cv + (size_t)t * 128;
+        float part = 0.f;
+        if (live) {
+#pragma unroll 8
+          for (int d = 32 * c; d < 32 * c + 32; ++d) part = fmaf(bf16_bits_to_float(qp[d]), bf16_bits_to_float(kt[d]), part);
+        }
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        const float sc0 = __shfl_sync(0xffffffffu, part, 8 * c) * sl2;
+        const float sc1 = __shfl_sync(0xffffffffu, part, 8 * c + 4) * sl2;
+        const bool v0 = 2 * c < ncols && t <= zc0 && (p.window_q < 0 || t >= zc0 - p.window_q);
+        const bool v1 = 2 * c + 1 < ncols && t <= zc1 && (p.window_q < 0 || t >= zc1 - p.window_q);
+        const float s0c = v0 ? sc0 : -INFINITY, s1c = v1 ? sc1 : -INFINITY;
+        const float mn0 = fmaxf(m_run0, s0c), mn1 = fmaxf(m_run1, s1c);
+        const float b0 = mn0 == -INFINITY ? 0.f : mn0, b1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = fast_exp2(m_run0 - b0), al1 = fast_exp2(m_run1 - b1);
+        const float pc0 = fast_exp2(s0c - b0), pc1 = fast_exp2(s1c - b1);
+        l_run0 = l_run0 * al0 + (n == 0 ? pc0 : 0.f);
+        l_run1 = l_run1 * al1 + (n == 0 ? pc1 : 0.f);
+        m_run0 = mn0;
+        m_run1 = mn1;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          const int da = 32 * (mt >> 1) + 4 * n + 2 * (mt & 1);
+          const float va = bf16_bits_to_float(vt[da]), vb = bf16_bits_to_float(vt[da + 1]);
+          o[mt][0] = fmaf(pc0, va, o[mt][0] * al0);
+          o[mt][1] = fmaf(pc1, va, o[mt][1] * al1);
+          o[mt][2] = fmaf(pc0, vb, o[mt][2] * al0);
+          o[mt][3] = fmaf(pc1, vb, o[mt][3] * al1);
+        }
+      }
+    } else if (warp == 0) {
       float part = 0.f;
       if (live) {
 #pragma unroll 8
@@ -802,7 +870,7 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
   float* merged = reinterpret_cast<float*>(stages + kStage);  // warp 0's second stage
   merge_and_finish(
       p, w, NWARPS, [&](int st) { return reinterpret_cast<const float*>(stages + st * STAGES * kStage); }, merged,
-      nullptr, ms);
+      nullptr, ms, CHUNK ? zs : -1);
 }
 
 // ------------------------------------------------------------------ host
@@ -843,8 +911,9 @@ bool encode_width(CUtensorMap* map, void* base, uint64_t pool_bytes, int width) 
 
 constexpr int kWarps = 6, kStages = 2;
 
+template <bool CHUNK>
 cudaError_t ensure_attrs() {
-  static cudaError_t state = cudaFuncSetAttribute(fast_hpaged_kernel<kWarps, kStages>,
+  static cudaError_t state = cudaFuncSetAttribute(fast_hpaged_kernel<kWarps, kStages, CHUNK>,
                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                   HpLayout<kWarps, kStages>::kTotal);
   return state;
@@ -853,7 +922,9 @@ cudaError_t ensure_attrs() {
 }  // namespace
 
 bool fast_hpaged_supported(const AttnParams& p) {
-  if (p.layout != OL_LAYOUT_HPAGED || p.head_dim != 128 || p.group > 8 || p.nq != 1) return false;
+  if (p.layout != OL_LAYOUT_HPAGED || p.head_dim != 128 || p.group > 8) return false;
+  // a chunked step: query tokens share a CTA as extra columns (at most 8)
+  if (p.nq > 1 && (p.tq < 1 || p.group * p.tq > 8)) return false;
   if (p.page_size % kTok != 0) return false;
   // TMA row coordinates are 32-bit: the 32-byte-row view has the most rows
   const unsigned long long rows32 = (unsigned long long)p.num_pages * p.kv_heads * p.page_size * 128 * 8 / 32;
@@ -869,10 +940,12 @@ cudaError_t launch_fast_hpaged(const AttnParams& p, cudaStream_t s) {
   if (!encode_width(&maps[0], p.pool, bytes, 256) || !encode_width(&maps[1], p.pool, bytes, 128) ||
       !encode_width(&maps[2], p.pool, bytes, 64) || !encode_width(&maps[3], p.pool, bytes, 32))
     return cudaErrorInvalidValue;
-  cudaError_t e = ensure_attrs();
+  const bool chunk = p.nq > 1;
+  cudaError_t e = chunk ? ensure_attrs<true>() : ensure_attrs<false>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.total_ctas, 1, 1);
+  // a chunked step: slices of query tokens along x, the split plan's CTAs along y
+  cfg.gridDim = chunk ? dim3((p.nq + p.tq - 1) / p.tq, p.total_ctas, 1) : dim3(p.total_ctas, 1, 1);
   cfg.blockDim = dim3(kWarps * 32, 1, 1);
   cfg.dynamicSmemBytes = HpLayout<kWarps, kStages>::kTotal;
   cfg.stream = s;
@@ -881,7 +954,9 @@ cudaError_t launch_fast_hpaged(const AttnParams& p, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fast_hpaged_kernel<kWarps, kStages>, maps[0], maps[1], maps[2], maps[3], p);
+  if (chunk)
+    return cudaLaunchKernelEx(&cfg, fast_hpaged_kernel<kWarps, kStages, true>, maps[0], maps[1], maps[2], maps[3], p);
+  return cudaLaunchKernelEx(&cfg, fast_hpaged_kernel<kWarps, kStages, false>, maps[0], maps[1], maps[2], maps[3], p);
 }
 
 }  // namespace ol

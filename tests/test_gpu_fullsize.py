@@ -331,3 +331,64 @@ def test_int4_chunk4_full_size_sampled_rows():
         np.testing.assert_array_equal(to_host(g), r)
     for code, _ in OUTS:
         check(got[code][rows], want, code)
+
+
+def test_hpaged_chunk4_full_size_sampled_rows():
+    # heterogeneous pages taking 4 tokens per row (bench.py's hpchunk4_b64): attention on the
+    # tensor-core kernel with 2 query tokens per CTA, then the chunk encoded into its pages
+    w = WORKLOADS["hpchunk4_b64"]
+    T = w.chunk
+    case = make_case(w, history_len_offset=T)
+    rng = np.random.default_rng(w.seed + 7)
+    q = bf16_from_f32(rng.standard_normal((w.batch, w.q_heads, T, w.head_dim)).astype(np.float32))
+    kv = bf16_from_f32(rng.standard_normal((2, w.batch, w.kv_heads, T, w.head_dim)).astype(np.float32))
+    S, M, H, D = w.page_size, w.max_pages_per_row, w.kv_heads, w.head_dim
+    pool, desc = O.hpaged_pool(w.num_pages, H, S, D)
+    table = block_table(case)
+    cls = page_format_classes(case.lens, S, M)
+
+    def fill(b):  # one append per run of pages of one format class; rows own disjoint pages
+        h = case.history[b]
+        hist, j = h.shape[2], 0
+        npages = (hist + S - 1) // S
+        while j < npages:
+            j1 = j
+            while j1 < npages and cls[b, j1] == cls[b, j]:
+                j1 += 1
+            kf, vf = AGE_FORMATS[cls[b, j]][1]
+            O.hpaged_append(pool, desc, table[b:b + 1], h[:, None, :, j * S:min(j1 * S, hist)], [j * S],
+                            O.page_desc(k=kf, v=vf))
+            j = j1
+    threaded(fill, list(range(w.batch)))
+    case.history = None
+    new_o = O.page_desc(*AGE_FORMATS[0][1])
+    new_g = ol.page_format(*AGE_FORMATS[0][1])
+    pool_d, fmt_d = to_dev(pool), to_dev(desc.view(np.uint8).copy())
+    mirror = desc.copy().view(ol.PAGE_FORMAT_DTYPE)
+    kvd = ol.hpaged_kv(pool_d, fmt_d, mirror, to_dev(table), table, kv_heads=H, page_size=S, head_dim=D,
+                       access=STABLE)
+    n = ol.ol_workspace_size_chunk(w.batch, w.q_heads, H, D, T)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    ol.ol_workspace_init(ws, n)
+    q_d, kv_d, lens_d = to_dev(q), to_dev(kv), to_dev(case.lens)
+    got = {}
+    for code, dt in OUTS:
+        out = torch.full((w.batch, w.q_heads, T, D), float("nan"), dtype=dt, device="cuda")
+        ol.ol_hpaged_chunk_step(kvd, pool_d, q_d, w.q_heads, T, kv_d, new_g, case.lens, lens_d, 0.0, -1, out, code,
+                                ws, n)
+        torch.cuda.synchronize()
+        got[code] = out_as_f64(out)
+    assert ol.ol_workspace_status(ws) == ol.OL_DEVICE_OK
+    rows = [int(np.argmin(case.lens)), int(np.argmax(case.lens))]
+
+    def row(b):
+        return O.hpaged_chunk_attention(q[b:b + 1], pool, desc, table[b:b + 1], case.lens[b:b + 1], H, T,
+                                        np.ascontiguousarray(kv[:, b:b + 1]))[0]
+    want = np.stack(threaded(row, rows))                      # before the append: history only from the pages
+    O.hpaged_append(pool, desc, table, kv, case.lens - T, new_o)
+    np.testing.assert_array_equal(to_host(fmt_d).view(np.uint8), desc.view(np.uint8))
+    got_pool = to_host(pool_d)
+    bad = np.argwhere(got_pool != pool)
+    assert bad.size == 0, f"{len(bad)} pool bytes differ, first at page/byte {bad[0].tolist()}"
+    for code, _ in OUTS:
+        check(got[code][rows], want, code)

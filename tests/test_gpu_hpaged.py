@@ -249,9 +249,13 @@ def test_long_rows_with_every_format_match_oracle(shape):
 
 
 CHUNKS = [  # B, H, S, D, Hq, lens (before the chunk is counted in), chunk length
+    # head_dim 128, pages of 16: tensor-core kernel, 8 / group query tokens per CTA
     (3, 2, 16, 128, 8, [16, 21, 40], 4),
     (2, 1, 4, 64, 4, [3, 9], 5),
     (1, 2, 16, 128, 14, [100], 16),
+    (2, 2, 16, 128, 16, [300, 777], 3),
+    (2, 4, 32, 128, 8, [64, 500], 8),
+    (1, 3, 16, 128, 3, [250], 6),
 ]
 
 

@@ -112,6 +112,10 @@ WORKLOADS = {
     # by its age (AGE_FORMATS): recent pages BFLOAT16, older INT8, oldest 4-bit
     "hpaged_b64": Workload("hpaged_b64", "bf16", 64, 32, 8, 128, 16384, "hpaged", seed=7,
                            lens_range=(1, 16384), page_size=16, num_pages=65536),
+    # the heterogeneous pages taking 4 tokens per row per step (chunked step:
+    # the chunk attended uncompressed, then encoded into its pages)
+    "hpchunk4_b64": Workload("hpchunk4_b64", "bf16", 64, 32, 8, 128, 16384, "hpaged", seed=9,
+                             lens_range=(8, 16384), page_size=16, num_pages=65536, chunk=4),
 }
 
 # Page formats of the heterogeneous workloads, as (format, scale, zero point)
