@@ -553,22 +553,22 @@ def measure(w, args, rank, world, dist, dev, K_req):
 
 
 def compact(r):
-    """The per-workload figures of a measure() result, for per_config."""
-    out = {"value": r["value"], "unit": r["unit"], "us_per_step": r["us_per_step"], "steps": r["steps"],
+    """The per-workload figures of a measure() result, for per_config: CUDA-event
+    time of exactly `steps` steps, the spread over further graphs (p10, median,
+    p90), roofline fraction and recorded DRAM traffic, clocks, the host-buffer
+    time, and the oracle's time on the host cores."""
+    out = {"value": r["value"], "us_per_step": r["us_per_step"], "steps": r["steps"],
            "spread_us": [r["us_per_step_spread"][k] for k in ("p10", "median", "p90")],
-           "rows_tok_per_s": r["rows_tok_per_s"], "frac": r["roofline"]["frac"],
-           "traffic": r["roofline"]["traffic"], "bytes_per_step": r["config"]["bytes_per_step"],
-           "lens_mean": r["config"]["lens_mean"], "gpu_launches": r["gpu_launches"],
-           "device_status": r["device_status"], "dtype": r["dtype"],
-           "clocks": {k: r["clocks"][k] for k in ("sm_mhz", "reasons")}}
+           "frac": r["roofline"]["frac"], "traffic": r["roofline"]["traffic"],
+           "bytes_per_step": r["config"]["bytes_per_step"], "rows_tok_per_s": r["rows_tok_per_s"],
+           "gpu_launches": r["gpu_launches"], "device_status": r["device_status"],
+           "clocks": [r["clocks"]["sm_mhz"], r["clocks"]["reasons"]]}
     e = r.get("e2e")
-    out["e2e"] = None if not e else {"value": e["value"], "us_per_step": e["us_per_step"],
-                                     "h2d_bytes_per_step": e["h2d_bytes_per_step"],
-                                     "d2h_bytes_per_step": e["d2h_bytes_per_step"]}
+    out["e2e_us_per_step"] = e["us_per_step"] if e else None
     cb = r.get("cpu_baseline")
     if cb:
         out["cpu_baseline"] = {"value": cb["value"], "cores": cb["cores"], "us_per_step": cb["us_per_step"],
-                               "single_core_us_per_step": cb["single_core"]["us_per_step"]}
+                               "one_core_us": cb["single_core"]["us_per_step"]}
     return out
 
 
@@ -611,8 +611,8 @@ def run_e2e(s, stream, K_e2e):
     ms = e0.elapsed_time(e1) / K_e2e
     return {"value": round(s.bytes_per_step / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "us_per_step": round(ms * 1e3, 3),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": K_e2e,
-            "call": "ol_decode_step_host (one C-ABI call per step, pinned host buffers)",
-            "transfer": "q, new K/V loaded and y stored by the step's kernels from/to mapped pinned host memory"}
+            "call": "ol_decode_step_host per step; q, new K/V read and y written by its kernels in mapped pinned "
+                    "host memory"}
 
 
 # --------------------------------------------------------------- oracle
@@ -951,7 +951,7 @@ def main():
         dist.barrier()
         dist.destroy_process_group()
     if rank == 0:
-        print(json.dumps(result), flush=True)
+        print(json.dumps(result, separators=(",", ":")), flush=True)
 
 
 if __name__ == "__main__":
