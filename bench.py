@@ -75,33 +75,41 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def kernel_sources_sha() -> str:
-    """sha256 over the library's device-code sources (.cu, .cuh, .h, .inc: file name
-    and content, in name order): a recorded DRAM traffic figure holds only for
-    the kernel sources it was measured on."""
+# Device-code sources each layout's timed kernel is built from (the shared
+# headers included): a recorded DRAM traffic figure holds only while these are
+# unchanged.
+_SHARED = ("ol_common.cuh", "ol_merge.cuh", "ol_internal.h")
+KERNEL_SOURCES = {"contiguous": ("ol_fast_bf16.cu", "ol_fast_bf16_kernel.inc") + _SHARED,
+                  "paged": ("ol_fast_bf16.cu", "ol_fast_bf16_kernel.inc") + _SHARED,
+                  "int4": ("ol_fast_int4.cu",) + _SHARED,
+                  "hpaged": ("ol_fast_hpaged.cu", "ol_hpaged.cuh") + _SHARED}
+
+
+def kernel_sources_sha(layout: str) -> str:
+    """sha256 over the device-code sources of a layout's kernel (file name and
+    content, in name order)."""
     import hashlib
     d = os.path.join(ROOT, "place_kv_cache_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(d)):
-        if name.endswith((".cu", ".cuh", ".h", ".inc")):
-            h.update(name.encode() + b"\0")
-            with open(os.path.join(d, name), "rb") as f:
-                h.update(f.read())
+    for name in sorted(KERNEL_SOURCES[layout]):
+        h.update(name.encode() + b"\0")
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(w):
     """DRAM bytes (read + write) per launch of the workload's kernel from one ncu
     capture, as listed in profiles/dram_traffic.txt; None when none was recorded
     or it was recorded on other kernel sources."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    sha = kernel_sources_sha()
+    sha = kernel_sources_sha(w.layout)
     with open(path) as f:
         for line in f:
             parts = line.split()
-            if len(parts) == 4 and not line.startswith("#") and parts[0] == workload and parts[3] == sha:
+            if len(parts) == 4 and not line.startswith("#") and parts[0] == w.name and parts[3] == sha:
                 return int(parts[2])
     return None
 
@@ -531,7 +539,7 @@ def measure(w, args, rank, world, dist, dev, K_req):
                    "graph_steps": per_graph, "tail_graph_steps": rem, "chained_steps": s.chain,
                    "history_stable": s.chain == 1, "parallelism": f"rows x{world} (independent)"},
         "roofline": {"bound": "hbm", "achieved": round(gbs / world, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(frac, 4), "traffic": recorded_traffic(w.name),
+                     "frac": round(frac, 4), "traffic": recorded_traffic(w),
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else
                      "fallback 6.8 TB/s"},
         "gpu_launches": K * launches_per_step(w),
