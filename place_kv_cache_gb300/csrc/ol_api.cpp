@@ -154,10 +154,11 @@ void plan_fast(AttnParams& p, const int32_t* lens_host, int sms, int force_varia
   int per_sm = (228 * 1024) / smem;
   if (per_sm > 64 / warps) per_sm = 64 / warps;
   if (int4 && per_sm > 16 / warps) per_sm = 16 / warps;  // 128 registers per thread
+  if (int4 && p.nq > 1) per_sm = std::max(1, 8 / warps);   // chunked: two column groups, up to 255 registers
   if (per_sm < 1) per_sm = 1;
   const long long slots = (long long)sms * per_sm;
   p.streamk = 0;
-  if (int4 && p.nq == 1 && units > 0 && slots <= 4096 && tune().cluster <= 0) {
+  if (int4 && units > 0 && slots <= 4096 && tune().cluster <= 0) {
     // Stream-K: the INT4 kernel is bound by instruction throughput, so every
     // SM gets the same number of tiles (whole CTAs per (row, kv head) leave
     // some SMs with more). Used when every row has tiles and a CTA gets at

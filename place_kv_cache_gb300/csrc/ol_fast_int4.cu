@@ -51,20 +51,23 @@ struct Int4Stage {
   static constexpr int kBytes = (kTx + 1023) / 1024 * 1024;  // 1024-aligned stride
 };
 
-template <int NWARPS, int STAGES>
+template <int NWARPS, int STAGES, int NG = 1>
 struct Int4Layout {
   static constexpr int kStages = STAGES * Int4Stage<NWARPS>::kBytes;
-  // extra state O, then one region that is either the CTA-merged state (no
-  // cluster) or the cluster receive buffers + cmerged (cluster): never both
+  // extra state O of each column group, then one region that is either the
+  // CTA-merged state (no cluster) or the cluster receive buffers + cmerged
+  // (cluster): never both
   static constexpr int kUnion = (1024 + 2 * 128 + 8 * 64) * 4 > kStateBytes ? (1024 + 2 * 128 + 8 * 64) * 4
                                                                          : kStateBytes;
-  static constexpr int kExtra = kStateBytes + kUnion;
+  static constexpr int kExtra = NG * kStateBytes + kUnion;
   static constexpr int kBars = STAGES * 8 + STAGES * 4;  // full barriers, release counters
-  static constexpr int kMisc = 256 + (NWARPS + 1) * 8 * 4 * 2 + 8 * 4 * 6 + 16 * 4 + 2 * 16 * 8 * 4 + 16;
+  static constexpr int kMisc = 256 + (NWARPS + NG) * 8 * 4 * 2 + 8 * 4 * 6 + 16 * 4 + 2 * 16 * 8 * 4 + 16;
   static constexpr int kTotal = 1024 + kStages + kExtra + (kBars + 15) / 16 * 16 + kMisc;
-  // CTAs per SM: shared memory, and 128 registers per thread
+  // CTAs per SM: shared memory, and registers (128 per thread for one column
+  // group; two groups take up to 255, one CTA per SM)
   static constexpr int kBySmem = (228 * 1024) / (kTotal + 1024) > 0 ? (228 * 1024) / (kTotal + 1024) : 1;
-  static constexpr int kPerSm = kBySmem < 16 / NWARPS ? kBySmem : 16 / NWARPS;
+  static constexpr int kByRegs = NG > 1 ? 8 / NWARPS : 16 / NWARPS;
+  static constexpr int kPerSm = kBySmem < kByRegs ? kBySmem : (kByRegs > 0 ? kByRegs : 1);
   static_assert(kStages >= NWARPS * kStateBytes, "the warps' states fit in the stages");
 };
 
@@ -94,16 +97,17 @@ __device__ __forceinline__ int swz64(int r, int x) {
 // tokens take part uncompressed from new_kv as one causal extra state per
 // column. Its own instantiation: the decode kernel keeps its own code.
 template <int NWARPS, int STAGES, bool CHUNK = false>
-__global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerSm)
+__global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES, CHUNK ? 2 : 1>::kPerSm)
     fast_int4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
                      const __grid_constant__ CUtensorMap tm_zps, const __grid_constant__ AttnParams p) {
-  using L = Int4Layout<NWARPS, STAGES>;
+  constexpr int NG = CHUNK ? 2 : 1;  // column groups a warp carries (a chunked step: two slices)
+  using L = Int4Layout<NWARPS, STAGES, NG>;
   using S = Int4Stage<NWARPS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* stages = smem;
-  float* extra_o = reinterpret_cast<float*>(smem + L::kStages);
-  float* merged = extra_o + 8 * kOStride;  // no cluster: the CTA state
+  float* extra_o = reinterpret_cast<float*>(smem + L::kStages);  // [NG][8][kOStride]
+  float* merged = extra_o + NG * 8 * kOStride;  // no cluster: the CTA state
   float* recv = merged;                    // cluster: receive buffers, then cmerged
   float* cmerged = recv + 1024 + 256;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kStages + L::kExtra);
@@ -111,9 +115,9 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
   Work* sw = reinterpret_cast<Work*>(smem + L::kStages + L::kExtra + (L::kBars + 15) / 16 * 16);
   float* misc = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(sw) + 256);
   MergeScratch ms;
-  ms.wm = misc;                        // [NWARPS + 1][8]
-  ms.wl = ms.wm + (NWARPS + 1) * 8;    // [NWARPS + 1][8]
-  ms.m = ms.wl + (NWARPS + 1) * 8;
+  ms.wm = misc;                        // [NWARPS + NG][8]: warps, then the extra states
+  ms.wl = ms.wm + (NWARPS + NG) * 8;   // [NWARPS + NG][8]
+  ms.m = ms.wl + (NWARPS + NG) * 8;
   ms.l = ms.m + 8;
   ms.cm = ms.l + 8;
   ms.cl = ms.cm + 8;
@@ -141,6 +145,10 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
   if (!p.inline_lens) pdl_wait();
   const int32_t* lens = p.inline_lens ? p.lens_inline : p.lens;
   int32_t* const lens_status = p.inline_lens ? nullptr : p.status;
+  // a chunked step's CTA serves NG consecutive slices of query tokens, zs0 .. zs0 + nsl - 1
+  const int nslices = CHUNK ? (p.nq + slice_tq(p) - 1) / slice_tq(p) : 1;
+  const int zs0 = CHUNK ? NG * query_index(p) : 0;
+  const int nsl = CHUNK ? min(NG, nslices - zs0) : 1;
   int jbase = 0;  // stages consumed by earlier segments: ring slot and mbarrier phase
   int next = -1;  // stream-K: global tile where the next segment starts
   // One pass per segment: a split of one (row, kv head). Without stream-K a
@@ -149,10 +157,10 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
   if (seg > 0) __syncthreads();  // the previous segment's Work and states are done with
   if (warp == 0) {
     Work w = p.streamk ? map_streamk_warp(lens, p.batch, p.kv_heads, p.capacity, p.window, p.total_ctas,
-                                          blockIdx.x, next, lens_status)
+                                          cta_index(p), next, lens_status)
                        : map_cta_warp(lens, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, cta_index(p),
                                       lens_status, CS, p.inline_lens && p.ordered ? p.row_order : nullptr);
-    if (CHUNK) slice_query(w, p);
+    if (CHUNK) slice_query(w, p, zs0, zs0 + nsl - 1);
     if (lane == 0) *sw = w;
   }
   __syncthreads();
@@ -209,30 +217,34 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
   //             k-step 1:            b0 = (i2, i6), b1 = (i3, i7) / 16.
   // A third k-step per block adds zp * (-Q_b), Q_b the sum of the block's
   // fp16 q carried as two fp16 (rows 0 and 1 of lane c = 0).
+  // Column group g (a chunked step: slice zs0 + g) has its own q operands,
+  // scores, softmax state and O; the code-word operands of a tile serve all.
   const int c = lane & 3, n = lane >> 2;
-  uint32_t qf[4][2][2], qz[4];
+  uint32_t qf[NG][4][2][2], qz[NG][4];
   float sfac;  // converts an accumulator (units 2^-24 * 2^eq) to the exp2 domain
-  // A chunked step's column n is head n % G of the slice's query token n / G.
-  const int zs = CHUNK ? query_index(p) : 0;
-  const int ncols = CHUNK ? G * slice_tokens(p, zs) : G;
+  // A chunked step's column n of group g is head n % G of slice zs0 + g's query token n / G.
   {
-    const bool live = n < ncols && w.valid;
-    const int nl = live ? n : 0;
-    const uint16_t* qp = reinterpret_cast<const uint16_t*>(p.q) +
-                         (CHUNK ? (((size_t)w.b * p.q_heads + (size_t)w.g * G + nl % G) * p.nq + slice_first(p, zs) +
-                                   nl / G) * 128
-                                : ((size_t)w.b * p.q_heads + (size_t)w.g * G + nl) * 128);
-    float qv[4][8];
+    float qv[NG][4][8];
     float mx = 0.f;
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const uint4 v = live ? __ldg(reinterpret_cast<const uint4*>(qp + 32 * b + 8 * c)) : make_uint4(0, 0, 0, 0);
-      const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+    for (int g = 0; g < NG; ++g) {
+      const int zs = zs0 + g;
+      const bool live = g < nsl && n < (CHUNK ? G * slice_tokens(p, zs) : G) && w.valid;
+      const int nl = live ? n : 0;
+      const uint16_t* qp = reinterpret_cast<const uint16_t*>(p.q) +
+                           (CHUNK ? (((size_t)w.b * p.q_heads + (size_t)w.g * G + nl % G) * p.nq + slice_first(p, zs) +
+                                     nl / G) * 128
+                                  : ((size_t)w.b * p.q_heads + (size_t)w.g * G + nl) * 128);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        qv[b][2 * k] = __uint_as_float(wd[k] << 16);
-        qv[b][2 * k + 1] = __uint_as_float(wd[k] & 0xffff0000u);
-        mx = fmaxf(mx, fmaxf(fabsf(qv[b][2 * k]), fabsf(qv[b][2 * k + 1])));
+      for (int b = 0; b < 4; ++b) {
+        const uint4 v = live ? __ldg(reinterpret_cast<const uint4*>(qp + 32 * b + 8 * c)) : make_uint4(0, 0, 0, 0);
+        const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          qv[g][b][2 * k] = __uint_as_float(wd[k] << 16);
+          qv[g][b][2 * k + 1] = __uint_as_float(wd[k] & 0xffff0000u);
+          mx = fmaxf(mx, fmaxf(fabsf(qv[g][b][2 * k]), fabsf(qv[g][b][2 * k + 1])));
+        }
       }
     }
     mx = warp_max(mx);
@@ -245,23 +257,25 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
     const float qscale = ldexpf(1.f, eq);
     sfac = ldexpf(p.scale_log2, 24 - eq);
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      float qh[8];
-      float qs = 0.f;
+    for (int g = 0; g < NG; ++g)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        qh[i] = __half2float(__float2half_rn(qv[b][i] * qscale));
-        qs += qh[i];
+      for (int b = 0; b < 4; ++b) {
+        float qh[8];
+        float qs = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          qh[i] = __half2float(__float2half_rn(qv[g][b][i] * qscale));
+          qs += qh[i];
+        }
+        qf[g][b][0][0] = pack_f16x2(qh[0], qh[4]);
+        qf[g][b][0][1] = pack_f16x2(qh[1] * 0.0625f, qh[5] * 0.0625f);
+        qf[g][b][1][0] = pack_f16x2(qh[2], qh[6]);
+        qf[g][b][1][1] = pack_f16x2(qh[3] * 0.0625f, qh[7] * 0.0625f);
+        qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+        qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+        const float qhi = __half2float(__float2half_rn(qs));
+        qz[g][b] = c == 0 ? pack_f16x2(-qhi, -(qs - qhi)) : 0u;
       }
-      qf[b][0][0] = pack_f16x2(qh[0], qh[4]);
-      qf[b][0][1] = pack_f16x2(qh[1] * 0.0625f, qh[5] * 0.0625f);
-      qf[b][1][0] = pack_f16x2(qh[2], qh[6]);
-      qf[b][1][1] = pack_f16x2(qh[3] * 0.0625f, qh[7] * 0.0625f);
-      qs += __shfl_xor_sync(0xffffffffu, qs, 1);
-      qs += __shfl_xor_sync(0xffffffffu, qs, 2);
-      const float qhi = __half2float(__float2half_rn(qs));
-      qz[b] = c == 0 ? pack_f16x2(-qhi, -(qs - qhi)) : 0u;
-    }
   }
   // The code words come from ldmatrix: the 16 bytes of block b in a token's
   // 64-byte row are one 8 x b16 matrix row, b16 k holding dims 32b + 4k .. +3.
@@ -281,26 +295,37 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
     vaddr[h] = S::kCodes + 1024 * warp + swz64(tok, 16 * blk);
   }
 
-  float o[8][4];
+  float o[NG][8][4];
+  float mr[NG][2], lr[NG][2];  // running maximum and sum of the lane's columns 2c, 2c + 1
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-  float m_run0 = -INFINITY, m_run1 = -INFINITY, l_run0 = 0.f, l_run1 = 0.f;
+  for (int g = 0; g < NG; ++g) {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) o[g][mt][0] = o[g][mt][1] = o[g][mt][2] = o[g][mt][3] = 0.f;
+    mr[g][0] = mr[g][1] = -INFINITY;
+    lr[g][0] = lr[g][1] = 0.f;
+  }
   int ev = kNoExp;  // O is held in units of 2^(ev - 24) (V side, see the tile)
   // tokens below codes_hi come from the codes: a decode step's history ends
   // before its current token, a chunked step's before its chunk (w.hi is one
-  // past the slice's last query token, at position codes_hi + zlast)
-  const int zlast = CHUNK ? slice_first(p, zs) + slice_tokens(p, zs) - 1 : 0;
+  // past the last query token of the CTA's last slice, at codes_hi + zlast)
+  const int zlast = CHUNK ? slice_first(p, zs0 + nsl - 1) + slice_tokens(p, zs0 + nsl - 1) - 1 : 0;
   const int codes_hi = CHUNK ? w.hi - 1 - zlast : (p.cur_from_new ? w.hi - 1 : w.hi);
   const int t_stop = min(w.t_end, codes_hi);
-  // visible history of the lane's columns 2c, 2c + 1 (chunked step): from its
-  // query token's window start; a tile is FULL only if it starts at or past
-  // every column's start (the slice's last token has the latest one)
-  int clo0 = w.lo, clo1 = w.lo, lo_full = w.lo;
+  // visible history of the lane's columns 2c, 2c + 1 of each group (chunked
+  // step): from its query token's window start; a tile is FULL only if it
+  // starts at or past every column's start (the last token has the latest one)
+  int clo[NG][2], lo_full = w.lo;
+#pragma unroll
+  for (int g = 0; g < NG; ++g) clo[g][0] = clo[g][1] = w.lo;
   if (CHUNK && p.window_q >= 0) {
-    const int ti0 = min((2 * c) / G, slice_tokens(p, zs) - 1), ti1 = min((2 * c + 1) / G, slice_tokens(p, zs) - 1);
-    const int base = codes_hi + slice_first(p, zs);  // position of the slice's first query token
-    clo0 = max(w.lo, base + ti0 - p.window_q);
-    clo1 = max(w.lo, base + ti1 - p.window_q);
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      const int zs = zs0 + min(g, nsl - 1);
+      const int last = slice_tokens(p, zs) - 1;
+      const int base = codes_hi + slice_first(p, zs);  // position of the slice's first query token
+      clo[g][0] = max(w.lo, base + min((2 * c) / G, last) - p.window_q);
+      clo[g][1] = max(w.lo, base + min((2 * c + 1) / G, last) - p.window_q);
+    }
     lo_full = max(w.lo, codes_hi + zlast - p.window_q);
   }
 
@@ -316,78 +341,90 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
       vb = t0 + n + 8 >= w.lo && t0 + n + 8 < t_stop;
     }
 
-    // ---- S^T = K q^T, one accumulator per 32-dim block
+    // ---- S^T = K q^T, one accumulator per 32-dim block (and column group)
     const uint32_t zda = lds_u16(kz + 2 * n) * 0x10001u, zdb = lds_u16(kz + 2 * n + 16) * 0x10001u;
     uint32_t kw[4][2];  // [block][tokens n, n + 8]
     ldsm_x4(sg + kaddr[0], kw[0][0], kw[0][1], kw[1][0], kw[1][1]);
     ldsm_x4(sg + kaddr[1], kw[2][0], kw[2][1], kw[3][0], kw[3][1]);
-    float sacc[4][4];
+    float sacc[NG][4][4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      sacc[b][0] = sacc[b][1] = sacc[b][2] = sacc[b][3] = 0.f;
       const uint32_t wa = kw[b][0], wb = kw[b][1];
       const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
-      mma_f16_16816(sacc[b], wa & kLoNib, wb & kLoNib, wa & kHiNib, wb & kHiNib, qf[b][0][0], qf[b][0][1]);
-      mma_f16_16816(sacc[b], wa8 & kLoNib, wb8 & kLoNib, wa8 & kHiNib, wb8 & kHiNib, qf[b][1][0], qf[b][1][1]);
+      const uint32_t a0 = wa & kLoNib, a1 = wb & kLoNib, a2 = wa & kHiNib, a3 = wb & kHiNib;
+      const uint32_t c0 = wa8 & kLoNib, c1 = wb8 & kLoNib, c2 = wa8 & kHiNib, c3 = wb8 & kHiNib;
       const uint32_t za = (zda >> (4 * b)) & kLoNib, zb = (zdb >> (4 * b)) & kLoNib;
-      mma_f16_16816(sacc[b], za, zb, za, zb, qz[b], 0u);
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        sacc[g][b][0] = sacc[g][b][1] = sacc[g][b][2] = sacc[g][b][3] = 0.f;
+        mma_f16_16816(sacc[g][b], a0, a1, a2, a3, qf[g][b][0][0], qf[g][b][0][1]);
+        mma_f16_16816(sacc[g][b], c0, c1, c2, c3, qf[g][b][1][0], qf[g][b][1][1]);
+        mma_f16_16816(sacc[g][b], za, zb, za, zb, qz[g][b], 0u);
+      }
     }
     const uint2 ska = lds_v2(ksc + 8 * n), skb = lds_v2(ksc + 8 * n + 64);
     const float2 ka01 = half2_bits_to_float2(ska.x), ka23 = half2_bits_to_float2(ska.y);
     const float2 kb01 = half2_bits_to_float2(skb.x), kb23 = half2_bits_to_float2(skb.y);
-    float s00 = ka01.x * sacc[0][0] + ka01.y * sacc[1][0] + ka23.x * sacc[2][0] + ka23.y * sacc[3][0];
-    float s01 = ka01.x * sacc[0][1] + ka01.y * sacc[1][1] + ka23.x * sacc[2][1] + ka23.y * sacc[3][1];
-    float s10 = kb01.x * sacc[0][2] + kb01.y * sacc[1][2] + kb23.x * sacc[2][2] + kb23.y * sacc[3][2];
-    float s11 = kb01.x * sacc[0][3] + kb01.y * sacc[1][3] + kb23.x * sacc[2][3] + kb23.y * sacc[3][3];
-    s00 *= sfac;
-    s01 *= sfac;
-    s10 *= sfac;
-    s11 *= sfac;
-    if (!FULL) {
-      if (CHUNK) {  // each column from its own window start
-        s00 = va && t0 + n >= clo0 ? s00 : -INFINITY;
-        s01 = va && t0 + n >= clo1 ? s01 : -INFINITY;
-        s10 = vb && t0 + n + 8 >= clo0 ? s10 : -INFINITY;
-        s11 = vb && t0 + n + 8 >= clo1 ? s11 : -INFINITY;
-      } else {
-        s00 = va ? s00 : -INFINITY;
-        s01 = va ? s01 : -INFINITY;
-        s10 = vb ? s10 : -INFINITY;
-        s11 = vb ? s11 : -INFINITY;
+    float pw[NG][4];  // weights: (token n, column 2c), (n, 2c + 1), (n + 8, 2c), (n + 8, 2c + 1)
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      const float(&sc)[4][4] = sacc[g];
+      float s00 = ka01.x * sc[0][0] + ka01.y * sc[1][0] + ka23.x * sc[2][0] + ka23.y * sc[3][0];
+      float s01 = ka01.x * sc[0][1] + ka01.y * sc[1][1] + ka23.x * sc[2][1] + ka23.y * sc[3][1];
+      float s10 = kb01.x * sc[0][2] + kb01.y * sc[1][2] + kb23.x * sc[2][2] + kb23.y * sc[3][2];
+      float s11 = kb01.x * sc[0][3] + kb01.y * sc[1][3] + kb23.x * sc[2][3] + kb23.y * sc[3][3];
+      s00 *= sfac;
+      s01 *= sfac;
+      s10 *= sfac;
+      s11 *= sfac;
+      if (!FULL) {
+        if (CHUNK) {  // each column from its own window start
+          s00 = va && t0 + n >= clo[g][0] ? s00 : -INFINITY;
+          s01 = va && t0 + n >= clo[g][1] ? s01 : -INFINITY;
+          s10 = vb && t0 + n + 8 >= clo[g][0] ? s10 : -INFINITY;
+          s11 = vb && t0 + n + 8 >= clo[g][1] ? s11 : -INFINITY;
+        } else {
+          s00 = va ? s00 : -INFINITY;
+          s01 = va ? s01 : -INFINITY;
+          s10 = vb ? s10 : -INFINITY;
+          s11 = vb ? s11 : -INFINITY;
+        }
       }
-    }
 
-    // ---- online softmax (exp2 domain) with a lazy maximum: the weights are
-    // taken against the running maximum m as long as no score exceeds it by
-    // more than kLazy (weights stay below 2^kLazy); only then is the tile's
-    // maximum reduced across the lanes and the state rescaled
-    if (__any_sync(0xffffffffu, fmaxf(s00, s10) > m_run0 + kLazy || fmaxf(s01, s11) > m_run1 + kLazy)) {
-      float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+      // ---- online softmax (exp2 domain) with a lazy maximum: the weights are
+      // taken against the running maximum m as long as no score exceeds it by
+      // more than kLazy (weights stay below 2^kLazy); only then is the tile's
+      // maximum reduced across the lanes and the state rescaled
+      if (__any_sync(0xffffffffu, fmaxf(s00, s10) > mr[g][0] + kLazy || fmaxf(s01, s11) > mr[g][1] + kLazy)) {
+        float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-      }
-      const float mn0 = fmaxf(m_run0, mx0), mn1 = fmaxf(m_run1, mx1);
-      const float al0 = mn0 == m_run0 ? 1.f : fast_exp2(m_run0 - mn0);
-      const float al1 = mn1 == m_run1 ? 1.f : fast_exp2(m_run1 - mn1);
-      l_run0 *= al0;
-      l_run1 *= al1;
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(mr[g][0], mx0), mn1 = fmaxf(mr[g][1], mx1);
+        const float al0 = mn0 == mr[g][0] ? 1.f : fast_exp2(mr[g][0] - mn0);
+        const float al1 = mn1 == mr[g][1] ? 1.f : fast_exp2(mr[g][1] - mn1);
+        lr[g][0] *= al0;
+        lr[g][1] *= al1;
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        o[mt][0] *= al0;
-        o[mt][1] *= al1;
-        o[mt][2] *= al0;
-        o[mt][3] *= al1;
+        for (int mt = 0; mt < 8; ++mt) {
+          o[g][mt][0] *= al0;
+          o[g][mt][1] *= al1;
+          o[g][mt][2] *= al0;
+          o[g][mt][3] *= al1;
+        }
+        mr[g][0] = mn0;
+        mr[g][1] = mn1;
       }
-      m_run0 = mn0;
-      m_run1 = mn1;
+      const float r0 = mr[g][0] == -INFINITY ? 0.f : mr[g][0], r1 = mr[g][1] == -INFINITY ? 0.f : mr[g][1];
+      pw[g][0] = fast_exp2(s00 - r0);
+      pw[g][1] = fast_exp2(s01 - r1);
+      pw[g][2] = fast_exp2(s10 - r0);
+      pw[g][3] = fast_exp2(s11 - r1);
+      lr[g][0] += pw[g][0] + pw[g][2];
+      lr[g][1] += pw[g][1] + pw[g][3];
     }
-    const float r0 = m_run0 == -INFINITY ? 0.f : m_run0, r1 = m_run1 == -INFINITY ? 0.f : m_run1;
-    const float p00 = fast_exp2(s00 - r0), p01 = fast_exp2(s01 - r1);
-    const float p10 = fast_exp2(s10 - r0), p11 = fast_exp2(s11 - r1);
-    l_run0 += p00 + p10;
-    l_run1 += p01 + p11;
 
     // ---- O^T += V^T P^T, block by block. A = the V code words masked in
     // place: fp16 subnormals c * 2^-24 (rows n: dims 32b + 4n + 2h), or
@@ -417,18 +454,24 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
         if (ev != kNoExp) {
           const float f = ldexpf(1.f, e_want - ev);
 #pragma unroll
-          for (int mt = 0; mt < 8; ++mt) {
-            o[mt][0] *= f;
-            o[mt][1] *= f;
-            o[mt][2] *= f;
-            o[mt][3] *= f;
-          }
+          for (int g = 0; g < NG; ++g)
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+              o[g][mt][0] *= f;
+              o[g][mt][1] *= f;
+              o[g][mt][2] *= f;
+              o[g][mt][3] *= f;
+            }
         }
         ev = e_want;
       }
     }
     const float pe = ldexpf(1.f, ev);
-    const float pa0 = p00 * pe, pa1 = p01 * pe, pb0 = p10 * pe, pb1 = p11 * pe;
+    float pa[NG][4];
+#pragma unroll
+    for (int g = 0; g < NG; ++g)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) pa[g][k] = pw[g][k] * pe;
     const float2 va01 = half2_bits_to_float2(sa0), va23 = half2_bits_to_float2(sa1);
     const float2 vb01 = half2_bits_to_float2(sb0), vb23 = half2_bits_to_float2(sb1);
     // zero points of the lane's V^T columns: tokens (2c, 2c+1) and (2c+8, 2c+9)
@@ -441,8 +484,12 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
     for (int b = 0; b < 4; ++b) {
       const float sca = b == 0 ? va01.x : b == 1 ? va01.y : b == 2 ? va23.x : va23.y;
       const float scb = b == 0 ? vb01.x : b == 1 ? vb01.y : b == 2 ? vb23.x : vb23.y;
-      const uint32_t h0 = pack_f16x2(pa0 * sca, pa1 * sca), h1 = pack_f16x2(pb0 * scb, pb1 * scb);
-      const uint32_t ph0 = movmatrix_trans(h0), ph1 = movmatrix_trans(h1);
+      uint32_t ph0[NG], ph1[NG];
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        ph0[g] = movmatrix_trans(pack_f16x2(pa[g][0] * sca, pa[g][1] * sca));
+        ph1[g] = movmatrix_trans(pack_f16x2(pa[g][2] * scb, pa[g][3] * scb));
+      }
       // -zp as fp16 subnormals: rows n (x1) and n + 8 (x16)
       const uint32_t t01 = zv01 >> (4 * b), t89 = zv89 >> (4 * b);
       const uint32_t zl01 = (t01 & kLoNib) | 0x80008000u, zh01 = ((t01 << 4) & kHiNib) | 0x80008000u;
@@ -450,8 +497,12 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint32_t w01 = vw[b][0] >> (8 * h), w89 = vw[b][1] >> (8 * h);
-        mma_f16_16816(o[2 * b + h], w01 & kLoNib, w01 & kHiNib, w89 & kLoNib, w89 & kHiNib, ph0, ph1);
-        mma_f16_16816(o[2 * b + h], zl01, zh01, zl89, zh89, ph0, ph1);
+        const uint32_t a0 = w01 & kLoNib, a1 = w01 & kHiNib, a2 = w89 & kLoNib, a3 = w89 & kHiNib;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          mma_f16_16816(o[g][2 * b + h], a0, a1, a2, a3, ph0[g], ph1[g]);
+          mma_f16_16816(o[g][2 * b + h], zl01, zh01, zl89, zh89, ph0[g], ph1[g]);
+        }
       }
     }
   };
@@ -459,83 +510,90 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
   // The token being appended (if this CTA's range holds it): attended from
   // new_kv uncompressed as one more merge state (formed here, before the
   // tiles, so its loads overlap theirs), and quantized into the cache after
-  // every tile is consumed.
+  // every tile is consumed. A chunked step: the chunk's tokens, causally, as
+  // one more state per column group.
   const int cur = p.cur_from_new ? w.hi - 1 : -1;
   const bool has_cur = w.valid && cur >= w.t_begin && cur < w.t_end;
   if (has_cur && warp == 0) {
     if (CHUNK) {
-      // column j (query token ti = j / G of the slice, head j % G) attends the
-      // chunk's tokens 0 .. ti within its window, uncompressed: scores, then
-      // (m, l, o) of that softmax as the column's extra state
-      const int nq = p.nq, z0 = slice_first(p, zs);
+      // column j of group g (query token ti = slice_first + j / G of slice
+      // zs0 + g, head j % G) attends the chunk's tokens 0 .. ti within its
+      // window, uncompressed: (m, l, o) of that softmax as its extra state
+      const int nq = p.nq;
       const size_t kv_row = ((size_t)w.b * p.kv_heads + w.g) * nq;
       const uint16_t* nk = reinterpret_cast<const uint16_t*>(p.new_kv) + kv_row * 128;
       const uint16_t* nv = reinterpret_cast<const uint16_t*>(p.new_kv) +
                            ((size_t)p.batch * p.kv_heads * nq + kv_row) * 128;
-      for (int j = 0; j < 8; ++j) {
-        float mj = -INFINITY, lj = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-        if (j < ncols) {
-          const int ti = z0 + j / G, h = j % G;
-          const uint16_t* qj = reinterpret_cast<const uint16_t*>(p.q) +
-                               (((size_t)w.b * p.q_heads + (size_t)w.g * G + h) * nq + ti) * 128;
-          const uint2 qq = *reinterpret_cast<const uint2*>(qj + 4 * lane);
-          const float q0 = __uint_as_float(qq.x << 16), q1 = __uint_as_float(qq.x & 0xffff0000u);
-          const float q2 = __uint_as_float(qq.y << 16), q3 = __uint_as_float(qq.y & 0xffff0000u);
-          const int t_first = p.window_q < 0 ? 0 : max(0, ti - p.window_q);
-          for (int t = t_first; t <= ti; ++t) {
-            const uint2 kk = *reinterpret_cast<const uint2*>(nk + (size_t)t * 128 + 4 * lane);
-            float acc = q0 * __uint_as_float(kk.x << 16) + q1 * __uint_as_float(kk.x & 0xffff0000u) +
-                        q2 * __uint_as_float(kk.y << 16) + q3 * __uint_as_float(kk.y & 0xffff0000u);
+      for (int g = 0; g < nsl; ++g) {
+        const int zs = zs0 + g, ncols = G * slice_tokens(p, zs);
+        float* xo = extra_o + g * 8 * kOStride;
+        for (int j = 0; j < 8; ++j) {
+          float mj = -INFINITY, lj = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+          if (j < ncols) {
+            const int ti = slice_first(p, zs) + j / G, h = j % G;
+            const uint16_t* qj = reinterpret_cast<const uint16_t*>(p.q) +
+                                 (((size_t)w.b * p.q_heads + (size_t)w.g * G + h) * nq + ti) * 128;
+            const uint2 qq = *reinterpret_cast<const uint2*>(qj + 4 * lane);
+            const float q0 = __uint_as_float(qq.x << 16), q1 = __uint_as_float(qq.x & 0xffff0000u);
+            const float q2 = __uint_as_float(qq.y << 16), q3 = __uint_as_float(qq.y & 0xffff0000u);
+            const int t_first = p.window_q < 0 ? 0 : max(0, ti - p.window_q);
+            for (int t = t_first; t <= ti; ++t) {
+              const uint2 kk = *reinterpret_cast<const uint2*>(nk + (size_t)t * 128 + 4 * lane);
+              float acc = q0 * __uint_as_float(kk.x << 16) + q1 * __uint_as_float(kk.x & 0xffff0000u) +
+                          q2 * __uint_as_float(kk.y << 16) + q3 * __uint_as_float(kk.y & 0xffff0000u);
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-            const float st = acc * p.scale_log2;
-            const float mn = fmaxf(mj, st);
-            const float al = fast_exp2(mj - mn), pt = fast_exp2(st - mn);
-            const uint2 vv = *reinterpret_cast<const uint2*>(nv + (size_t)t * 128 + 4 * lane);
-            lj = lj * al + pt;
-            o0 = o0 * al + pt * __uint_as_float(vv.x << 16);
-            o1 = o1 * al + pt * __uint_as_float(vv.x & 0xffff0000u);
-            o2 = o2 * al + pt * __uint_as_float(vv.y << 16);
-            o3 = o3 * al + pt * __uint_as_float(vv.y & 0xffff0000u);
-            mj = mn;
+              for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+              const float st = acc * p.scale_log2;
+              const float mn = fmaxf(mj, st);
+              const float al = fast_exp2(mj - mn), pt = fast_exp2(st - mn);
+              const uint2 vv = *reinterpret_cast<const uint2*>(nv + (size_t)t * 128 + 4 * lane);
+              lj = lj * al + pt;
+              o0 = o0 * al + pt * __uint_as_float(vv.x << 16);
+              o1 = o1 * al + pt * __uint_as_float(vv.x & 0xffff0000u);
+              o2 = o2 * al + pt * __uint_as_float(vv.y << 16);
+              o3 = o3 * al + pt * __uint_as_float(vv.y & 0xffff0000u);
+              mj = mn;
+            }
           }
-        }
-        extra_o[j * kOStride + 4 * lane + 0] = o0;
-        extra_o[j * kOStride + 4 * lane + 1] = o1;
-        extra_o[j * kOStride + 4 * lane + 2] = o2;
-        extra_o[j * kOStride + 4 * lane + 3] = o3;
-        if (lane == 0) {
-          ms.wm[NWARPS * 8 + j] = mj;
-          ms.wl[NWARPS * 8 + j] = lj;
+          xo[j * kOStride + 4 * lane + 0] = o0;
+          xo[j * kOStride + 4 * lane + 1] = o1;
+          xo[j * kOStride + 4 * lane + 2] = o2;
+          xo[j * kOStride + 4 * lane + 3] = o3;
+          if (lane == 0) {
+            ms.wm[(NWARPS + g) * 8 + j] = mj;
+            ms.wl[(NWARPS + g) * 8 + j] = lj;
+          }
         }
       }
     } else {
-    const uint16_t* nk = reinterpret_cast<const uint16_t*>(p.new_kv) + ((size_t)w.b * p.kv_heads + w.g) * 128;
-    const uint16_t* nv = reinterpret_cast<const uint16_t*>(p.new_kv) + (((size_t)p.batch + w.b) * p.kv_heads + w.g) * 128;
-    const uint2 kk = *reinterpret_cast<const uint2*>(nk + 4 * lane);
-    const uint2 vv = *reinterpret_cast<const uint2*>(nv + 4 * lane);
-    const float k0 = __uint_as_float(kk.x << 16), k1 = __uint_as_float(kk.x & 0xffff0000u);
-    const float k2 = __uint_as_float(kk.y << 16), k3 = __uint_as_float(kk.y & 0xffff0000u);
-    for (int j = 0; j < 8; ++j) {
-      float sj = -INFINITY;
-      if (j < G) {
-        const uint16_t* qj = reinterpret_cast<const uint16_t*>(p.q) + ((size_t)w.b * p.q_heads + (size_t)w.g * G + j) * 128;
-        const uint2 qq = *reinterpret_cast<const uint2*>(qj + 4 * lane);
-        float acc = __uint_as_float(qq.x << 16) * k0 + __uint_as_float(qq.x & 0xffff0000u) * k1 +
-                    __uint_as_float(qq.y << 16) * k2 + __uint_as_float(qq.y & 0xffff0000u) * k3;
+      const uint16_t* nk = reinterpret_cast<const uint16_t*>(p.new_kv) + ((size_t)w.b * p.kv_heads + w.g) * 128;
+      const uint16_t* nv =
+          reinterpret_cast<const uint16_t*>(p.new_kv) + (((size_t)p.batch + w.b) * p.kv_heads + w.g) * 128;
+      const uint2 kk = *reinterpret_cast<const uint2*>(nk + 4 * lane);
+      const uint2 vv = *reinterpret_cast<const uint2*>(nv + 4 * lane);
+      const float k0 = __uint_as_float(kk.x << 16), k1 = __uint_as_float(kk.x & 0xffff0000u);
+      const float k2 = __uint_as_float(kk.y << 16), k3 = __uint_as_float(kk.y & 0xffff0000u);
+      for (int j = 0; j < 8; ++j) {
+        float sj = -INFINITY;
+        if (j < G) {
+          const uint16_t* qj =
+              reinterpret_cast<const uint16_t*>(p.q) + ((size_t)w.b * p.q_heads + (size_t)w.g * G + j) * 128;
+          const uint2 qq = *reinterpret_cast<const uint2*>(qj + 4 * lane);
+          float acc = __uint_as_float(qq.x << 16) * k0 + __uint_as_float(qq.x & 0xffff0000u) * k1 +
+                      __uint_as_float(qq.y << 16) * k2 + __uint_as_float(qq.y & 0xffff0000u) * k3;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        sj = acc * p.scale_log2;
-        extra_o[j * kOStride + 4 * lane + 0] = __uint_as_float(vv.x << 16);
-        extra_o[j * kOStride + 4 * lane + 1] = __uint_as_float(vv.x & 0xffff0000u);
-        extra_o[j * kOStride + 4 * lane + 2] = __uint_as_float(vv.y << 16);
-        extra_o[j * kOStride + 4 * lane + 3] = __uint_as_float(vv.y & 0xffff0000u);
+          for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+          sj = acc * p.scale_log2;
+          extra_o[j * kOStride + 4 * lane + 0] = __uint_as_float(vv.x << 16);
+          extra_o[j * kOStride + 4 * lane + 1] = __uint_as_float(vv.x & 0xffff0000u);
+          extra_o[j * kOStride + 4 * lane + 2] = __uint_as_float(vv.y << 16);
+          extra_o[j * kOStride + 4 * lane + 3] = __uint_as_float(vv.y & 0xffff0000u);
+        }
+        if (lane == 0) {
+          ms.wm[NWARPS * 8 + j] = sj;
+          ms.wl[NWARPS * 8 + j] = j < G ? 1.f : 0.f;
+        }
       }
-      if (lane == 0) {
-        ms.wm[NWARPS * 8 + j] = sj;
-        ms.wl[NWARPS * 8 + j] = j < G ? 1.f : 0.f;
-      }
-    }
     }
   }
   for (int j = 0; j < nstage; ++j) {
@@ -569,31 +627,63 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES>::kPerS
   if (ev != kNoExp) {  // O to plain units: 2^(24 - ev), and 1/16 more for the rows of upper-nibble dims
     const float f = ldexpf(1.f, 24 - ev), f16 = f * 0.0625f;
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      o[mt][0] *= f;
-      o[mt][1] *= f;
-      o[mt][2] *= f16;
-      o[mt][3] *= f16;
+    for (int g = 0; g < NG; ++g)
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        o[g][mt][0] *= f;
+        o[g][mt][1] *= f;
+        o[g][mt][2] *= f16;
+        o[g][mt][3] *= f16;
+      }
+  }
+  if (!CHUNK) {
+    store_warp_state<true>(reinterpret_cast<float*>(stages + warp * kStateBytes), ms, warp, o[0], mr[0][0], mr[0][1],
+                           lr[0][0], lr[0][1]);
+
+    __syncthreads();  // every tile is consumed: the appended row may be rewritten
+    if (has_cur && p.append && warp < 2) {
+      const int plane = warp;
+      const size_t row = (size_t)(plane == 0 ? rowK0 : rowV0) + cur;
+      const uint16_t* src = reinterpret_cast<const uint16_t*>(p.new_kv) +
+                            (((size_t)plane * p.batch + w.b) * p.kv_heads + w.g) * 128;
+      int4_quantize_row_warp(src, 128, p.quant_mode, p.fixed_scale, p.fixed_zp, p.codes + row * 64,
+                             p.scales + row * 4, p.zps + row * 2);
+    }
+    merge_and_finish(
+        p, w, has_cur ? NWARPS + 1 : NWARPS,
+        [&](int s) {
+          return s < NWARPS ? reinterpret_cast<const float*>(stages + s * kStateBytes)
+                            : static_cast<const float*>(extra_o);
+        },
+        merged, cmerged, ms);
+  } else {
+    // a chunked step: each column group (slice) merged and finished on its own
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      if (g >= nsl) break;
+      if (g > 0) {
+        // the previous group's merge is complete everywhere (cluster receive
+        // buffers read, states and scratch free) before this one reuses them
+        if (CS > 1)
+          cluster_sync();
+        else
+          __syncthreads();
+        if (threadIdx.x < 8) {  // this group's extra state in the merge's extra slot
+          ms.wm[NWARPS * 8 + threadIdx.x] = ms.wm[(NWARPS + g) * 8 + threadIdx.x];
+          ms.wl[NWARPS * 8 + threadIdx.x] = ms.wl[(NWARPS + g) * 8 + threadIdx.x];
+        }
+      }
+      store_warp_state<true>(reinterpret_cast<float*>(stages + warp * kStateBytes), ms, warp, o[g], mr[g][0],
+                             mr[g][1], lr[g][0], lr[g][1]);
+      merge_and_finish(
+          p, w, has_cur ? NWARPS + 1 : NWARPS,
+          [&](int s) {
+            return s < NWARPS ? reinterpret_cast<const float*>(stages + s * kStateBytes)
+                              : static_cast<const float*>(extra_o + g * 8 * kOStride);
+          },
+          merged, cmerged, ms, zs0 + g);
     }
   }
-  store_warp_state<true>(reinterpret_cast<float*>(stages + warp * kStateBytes), ms, warp, o, m_run0, m_run1, l_run0, l_run1);
-
-  __syncthreads();  // every tile is consumed: the appended row may be rewritten
-  if (has_cur && p.append && warp < 2) {
-    const int plane = warp;
-    const size_t row = (size_t)(plane == 0 ? rowK0 : rowV0) + cur;
-    const uint16_t* src = reinterpret_cast<const uint16_t*>(p.new_kv) +
-                          (((size_t)plane * p.batch + w.b) * p.kv_heads + w.g) * 128;
-    int4_quantize_row_warp(src, 128, p.quant_mode, p.fixed_scale, p.fixed_zp, p.codes + row * 64, p.scales + row * 4,
-                           p.zps + row * 2);
-  }
-  merge_and_finish(
-      p, w, has_cur ? NWARPS + 1 : NWARPS,
-      [&](int s) {
-        return s < NWARPS ? reinterpret_cast<const float*>(stages + s * kStateBytes)
-                          : static_cast<const float*>(extra_o);
-      },
-      merged, cmerged, ms, CHUNK ? zs : -1);
   jbase += nstage;
   if (!p.streamk || w.next < 0) break;
   next = w.next;
@@ -648,7 +738,7 @@ cudaError_t ensure_attrs() {
   static cudaError_t state = [] {
     auto kern = fast_int4_kernel<NWARPS, STAGES, CHUNK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Int4Layout<NWARPS, STAGES>::kTotal);
+                                         Int4Layout<NWARPS, STAGES, CHUNK ? 2 : 1>::kTotal);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     return e;
   }();
@@ -688,11 +778,12 @@ cudaError_t launch_cfg(const AttnParams& p, cudaStream_t s) {
   cudaError_t e = ensure_attrs<NWARPS, STAGES, CHUNK>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  // a chunked step: slices of query tokens along x, the plan's CTAs (and clusters) along y
+  // a chunked step: pairs of slices of query tokens along x (a CTA carries two
+  // slices' columns), the plan's CTAs (and clusters) along y
   const int slices = CHUNK ? (p.nq + p.tq - 1) / p.tq : 1;
-  cfg.gridDim = CHUNK ? dim3(slices, p.total_ctas, 1) : dim3(p.total_ctas, 1, 1);
+  cfg.gridDim = CHUNK ? dim3((slices + 1) / 2, p.total_ctas, 1) : dim3(p.total_ctas, 1, 1);
   cfg.blockDim = dim3(NWARPS * 32, 1, 1);
-  cfg.dynamicSmemBytes = Int4Layout<NWARPS, STAGES>::kTotal;
+  cfg.dynamicSmemBytes = Int4Layout<NWARPS, STAGES, CHUNK ? 2 : 1>::kTotal;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
