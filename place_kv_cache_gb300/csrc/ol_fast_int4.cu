@@ -16,10 +16,10 @@
 //        c * 2^-24, or 16c * 2^-24 one nibble up, which q absorbs as q / 16);
 //        one more k-step adds zp_K * (-sum of the block's q). Then
 //        s = sum_b scale_K[t,b] * acc_b.
-//   O^T: the V code words masked in place as fp16 subnormals (as for K), the
-//        V scale folded into P^T per block, one fp16 per weight under a
-//        warp-uniform power of two, and zp_V taken off by one more MMA per
-//        block half with A = -zp.
+//   O^T: the V code words masked in place as fp16 subnormals (as for K)
+//        minus the zero point (an exact subnormal difference), the V scale
+//        folded into P^T per block, P^T as fp16 hi + lo under a warp-uniform
+//        power of two.
 // The token being appended (fused step) takes part uncompressed from new_kv as
 // one extra merge state, and is quantized into the cache by the same CTA.
 #include <cuda_bf16.h>
@@ -33,7 +33,6 @@ namespace ol {
 namespace {
 
 constexpr int kTok = 16;
-constexpr uint32_t kMagic = 0x43004300u;  // bf16 pair (128, 128)
 constexpr uint32_t kLoNib = 0x000F000Fu;  // nibble in bits 0..3 of both 16-bit halves
 constexpr uint32_t kHiNib = 0x00F000F0u;  // nibble in bits 4..7 of both halves
 constexpr int kStateBytes = 8 * kOStride * 4;  // one warp's [8][kOStride] fp32 state
@@ -71,12 +70,9 @@ struct Int4Layout {
   static_assert(kStages >= NWARPS * kStateBytes, "the warps' states fit in the stages");
 };
 
-__device__ __forceinline__ uint32_t code_pair(uint32_t w, int shift) {
-  return ((w >> shift) & 0x000F000Fu) | kMagic;
-}
-__device__ __forceinline__ uint32_t hsub2_bf16(uint32_t a, uint32_t b) {
-  __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a), y = *reinterpret_cast<__nv_bfloat162*>(&b);
-  __nv_bfloat162 r = __hsub2(x, y);
+// fp16 pair difference (exact for the subnormal code and zero-point values used here)
+__device__ __forceinline__ uint32_t hsub2_f16(uint32_t a, uint32_t b) {
+  __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
   return *reinterpret_cast<uint32_t*>(&r);
 }
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
@@ -430,12 +426,13 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES, CHUNK 
     // place: fp16 subnormals c * 2^-24 (rows n: dims 32b + 4n + 2h), or
     // 16c * 2^-24 for a code in bits 4..7 (rows n + 8: dims 32b + 4n + 2h + 1,
     // which therefore hold 16 O and are scaled back when the state is
-    // stored). B = P^T times the token's V scale and 2^ev, one fp16 per
-    // weight. One more MMA per (block, half) with A = -zp (the same in every
-    // row, x16 in rows n + 8) adds -zp * P^T, so A needs no subtraction.
-    // ev is warp-uniform: 2^kLazy * (largest V scale of the tile) * 2^ev stays
-    // below 2^15, and O is held in units of 2^(ev - 24); it is rescaled only
-    // when the tile needs a smaller ev, or a much larger one.
+    // stored), minus the zero point in the same units: (c - zp) * 2^-24, a
+    // subnormal difference, exact. B = P^T times the token's V scale and
+    // 2^ev as fp16 hi + lo (about 22 significant bits per weight: the error
+    // does not grow with the size of the values). ev is warp-uniform:
+    // 2^kLazy * (largest V scale of the tile) * 2^ev stays below 2^15, and O
+    // is held in units of 2^(ev - 24); it is rescaled only when the tile
+    // needs a smaller ev, or a much larger one.
     const uint2 sva = lds_v2(vsc + 8 * n), svb = lds_v2(vsc + 8 * n + 64);
     uint32_t sa0 = sva.x, sa1 = sva.y, sb0 = svb.x, sb1 = svb.y;
     if (!FULL) {  // a hidden token's scale may be anything: its weight is exactly 0
@@ -445,10 +442,7 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES, CHUNK 
     {
       // largest scale of the tile (positive fp16 order as unsigned integers)
       uint32_t mx = __vmaxu2(__vmaxu2(sa0, sa1), __vmaxu2(sb0, sb1));
-      mx = max(mx & 0xffffu, mx >> 16);
-      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      mx = __reduce_max_sync(0xffffffffu, max(mx & 0xffffu, mx >> 16));
       const int e_want = 21 - (int)((mx >> 10) & 31u);  // scale < 2^(field - 14)
       if (e_want < ev || e_want > ev + 6) {
         if (ev != kNoExp) {
@@ -484,24 +478,30 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES, CHUNK 
     for (int b = 0; b < 4; ++b) {
       const float sca = b == 0 ? va01.x : b == 1 ? va01.y : b == 2 ? va23.x : va23.y;
       const float scb = b == 0 ? vb01.x : b == 1 ? vb01.y : b == 2 ? vb23.x : vb23.y;
-      uint32_t ph0[NG], ph1[NG];
+      uint32_t ph0[NG], ph1[NG], pl0[NG], pl1[NG];
 #pragma unroll
       for (int g = 0; g < NG; ++g) {
-        ph0[g] = movmatrix_trans(pack_f16x2(pa[g][0] * sca, pa[g][1] * sca));
-        ph1[g] = movmatrix_trans(pack_f16x2(pa[g][2] * scb, pa[g][3] * scb));
+        const float q00 = pa[g][0] * sca, q01 = pa[g][1] * sca, q10 = pa[g][2] * scb, q11 = pa[g][3] * scb;
+        const uint32_t h0 = pack_f16x2(q00, q01), h1 = pack_f16x2(q10, q11);
+        const float2 f0 = half2_bits_to_float2(h0), f1 = half2_bits_to_float2(h1);
+        ph0[g] = movmatrix_trans(h0);
+        ph1[g] = movmatrix_trans(h1);
+        pl0[g] = movmatrix_trans(pack_f16x2(q00 - f0.x, q01 - f0.y));
+        pl1[g] = movmatrix_trans(pack_f16x2(q10 - f1.x, q11 - f1.y));
       }
-      // -zp as fp16 subnormals: rows n (x1) and n + 8 (x16)
+      // zp as fp16 subnormals in the A layout: rows n (x1) and n + 8 (x16)
       const uint32_t t01 = zv01 >> (4 * b), t89 = zv89 >> (4 * b);
-      const uint32_t zl01 = (t01 & kLoNib) | 0x80008000u, zh01 = ((t01 << 4) & kHiNib) | 0x80008000u;
-      const uint32_t zl89 = (t89 & kLoNib) | 0x80008000u, zh89 = ((t89 << 4) & kHiNib) | 0x80008000u;
+      const uint32_t zl01 = t01 & kLoNib, zh01 = (t01 << 4) & kHiNib;
+      const uint32_t zl89 = t89 & kLoNib, zh89 = (t89 << 4) & kHiNib;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint32_t w01 = vw[b][0] >> (8 * h), w89 = vw[b][1] >> (8 * h);
-        const uint32_t a0 = w01 & kLoNib, a1 = w01 & kHiNib, a2 = w89 & kLoNib, a3 = w89 & kHiNib;
+        const uint32_t a0 = hsub2_f16(w01 & kLoNib, zl01), a1 = hsub2_f16(w01 & kHiNib, zh01);
+        const uint32_t a2 = hsub2_f16(w89 & kLoNib, zl89), a3 = hsub2_f16(w89 & kHiNib, zh89);
 #pragma unroll
         for (int g = 0; g < NG; ++g) {
           mma_f16_16816(o[g][2 * b + h], a0, a1, a2, a3, ph0[g], ph1[g]);
-          mma_f16_16816(o[g][2 * b + h], zl01, zh01, zl89, zh89, ph0[g], ph1[g]);
+          mma_f16_16816(o[g][2 * b + h], a0, a1, a2, a3, pl0[g], pl1[g]);
         }
       }
     }
