@@ -153,8 +153,8 @@ void plan_fast(AttnParams& p, const int32_t* lens_host, int sms, int force_varia
   const int warps = int4 ? fast_int4_warps(p.variant) : fast_bf16_warps(p.variant);
   int per_sm = (228 * 1024) / smem;
   if (per_sm > 64 / warps) per_sm = 64 / warps;
-  if (int4 && per_sm > 16 / warps) per_sm = 16 / warps;  // 128 registers per thread
-  if (int4 && p.nq > 1) per_sm = std::max(1, 8 / warps);   // chunked: two column groups, up to 255 registers
+  // INT4: the CTAs per SM its launch bounds promise (registers and shared memory)
+  if (int4) per_sm = fast_int4_ctas_per_sm(p.variant, p.nq > 1);
   if (per_sm < 1) per_sm = 1;
   const long long slots = (long long)sms * per_sm;
   p.streamk = 0;

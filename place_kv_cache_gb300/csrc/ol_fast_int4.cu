@@ -92,10 +92,16 @@ __device__ __forceinline__ int swz64(int r, int x) {
 // token's window; the history ends where the chunk starts, and the chunk's
 // tokens take part uncompressed from new_kv as one causal extra state per
 // column. Its own instantiation: the decode kernel keeps its own code.
-template <int NWARPS, int STAGES, bool CHUNK = false>
+// DUP (a decode step with at most 4 heads per kv head): MMA columns 4..7
+// repeat the heads of columns 0..3, so the two halves of P^T (fp16 hi and lo)
+// travel in one MMA, hi in columns 0..3 and lo in 4..7, added when the state
+// is stored; and the V zero point leaves the code operands: its term
+// sum_t P'[t] * zp[t] is one fp32 sum per (block, column), subtracted at the end.
+template <int NWARPS, int STAGES, bool CHUNK = false, bool DUP = false>
 __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES, CHUNK ? 2 : 1>::kPerSm)
     fast_int4_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
                      const __grid_constant__ CUtensorMap tm_zps, const __grid_constant__ AttnParams p) {
+  static_assert(!(CHUNK && DUP), "duplicated columns serve a decode step only");
   constexpr int NG = CHUNK ? 2 : 1;  // column groups a warp carries (a chunked step: two slices)
   using L = Int4Layout<NWARPS, STAGES, NG>;
   using S = Int4Stage<NWARPS>;
@@ -216,6 +222,7 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES, CHUNK 
   // Column group g (a chunked step: slice zs0 + g) has its own q operands,
   // scores, softmax state and O; the code-word operands of a tile serve all.
   const int c = lane & 3, n = lane >> 2;
+  const int ncol = DUP ? (n & 3) : n;  // the head (or token-head pair) of MMA column n
   uint32_t qf[NG][4][2][2], qz[NG][4];
   float sfac;  // converts an accumulator (units 2^-24 * 2^eq) to the exp2 domain
   // A chunked step's column n of group g is head n % G of slice zs0 + g's query token n / G.
@@ -225,8 +232,8 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES, CHUNK 
 #pragma unroll
     for (int g = 0; g < NG; ++g) {
       const int zs = zs0 + g;
-      const bool live = g < nsl && n < (CHUNK ? G * slice_tokens(p, zs) : G) && w.valid;
-      const int nl = live ? n : 0;
+      const bool live = g < nsl && ncol < (CHUNK ? G * slice_tokens(p, zs) : G) && w.valid;
+      const int nl = live ? ncol : 0;
       const uint16_t* qp = reinterpret_cast<const uint16_t*>(p.q) +
                            (CHUNK ? (((size_t)w.b * p.q_heads + (size_t)w.g * G + nl % G) * p.nq + slice_first(p, zs) +
                                      nl / G) * 128
@@ -301,6 +308,18 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES, CHUNK 
     lr[g][0] = lr[g][1] = 0.f;
   }
   int ev = kNoExp;  // O is held in units of 2^(ev - 24) (V side, see the tile)
+  float pe = 0.f;   // 2^ev
+  // the running maximum as the exp2 offset: 0 while no score is finite
+  float rz[NG][2];
+#pragma unroll
+  for (int g = 0; g < NG; ++g) rz[g][0] = rz[g][1] = 0.f;
+  // DUP: the V zero-point term of the lane's columns 2c, 2c + 1 per block b,
+  // over its tokens n, n + 8, times 16^b (units of O times 2^24)
+  float zc[DUP ? 4 : 1][2];
+#pragma unroll
+  for (int b = 0; b < (DUP ? 4 : 1); ++b) zc[b][0] = zc[b][1] = 0.f;
+  // DUP: 1 on the lanes of columns 4..7, whose P^T operand is the lo half
+  const float hsel = DUP && c >= 2 ? 1.f : 0.f;
   // tokens below codes_hi come from the codes: a decode step's history ends
   // before its current token, a chunked step's before its chunk (w.hi is one
   // past the last query token of the CTA's last slice, at codes_hi + zlast)
@@ -410,10 +429,19 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES, CHUNK 
           o[g][mt][2] *= al0;
           o[g][mt][3] *= al1;
         }
+        if constexpr (DUP) {
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            zc[b][0] *= al0;
+            zc[b][1] *= al1;
+          }
+        }
         mr[g][0] = mn0;
         mr[g][1] = mn1;
+        rz[g][0] = mn0 == -INFINITY ? 0.f : mn0;
+        rz[g][1] = mn1 == -INFINITY ? 0.f : mn1;
       }
-      const float r0 = mr[g][0] == -INFINITY ? 0.f : mr[g][0], r1 = mr[g][1] == -INFINITY ? 0.f : mr[g][1];
+      const float r0 = rz[g][0], r1 = rz[g][1];
       pw[g][0] = fast_exp2(s00 - r0);
       pw[g][1] = fast_exp2(s01 - r1);
       pw[g][2] = fast_exp2(s10 - r0);
@@ -456,11 +484,18 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES, CHUNK 
               o[g][mt][2] *= f;
               o[g][mt][3] *= f;
             }
+          if constexpr (DUP) {
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              zc[b][0] *= f;
+              zc[b][1] *= f;
+            }
+          }
         }
         ev = e_want;
+        pe = __int_as_float((127 + e_want) << 23);  // e_want in [-10, 21]
       }
     }
-    const float pe = ldexpf(1.f, ev);
     float pa[NG][4];
 #pragma unroll
     for (int g = 0; g < NG; ++g)
@@ -468,12 +503,39 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES, CHUNK 
       for (int k = 0; k < 4; ++k) pa[g][k] = pw[g][k] * pe;
     const float2 va01 = half2_bits_to_float2(sa0), va23 = half2_bits_to_float2(sa1);
     const float2 vb01 = half2_bits_to_float2(sb0), vb23 = half2_bits_to_float2(sb1);
-    // zero points of the lane's V^T columns: tokens (2c, 2c+1) and (2c+8, 2c+9)
-    // in the two 16-bit halves
-    const uint32_t zv01 = lds_u32(vz + 4 * c), zv89 = lds_u32(vz + 4 * c + 16);
     uint32_t vw[4][2];  // [block][tokens (2c, 2c+1), (2c+8, 2c+9)]
     ldsm_x4_trans(sg + vaddr[0], vw[0][0], vw[0][1], vw[1][0], vw[1][1]);
     ldsm_x4_trans(sg + vaddr[1], vw[2][0], vw[2][1], vw[3][0], vw[3][1]);
+    if constexpr (DUP) {
+      // zero points of the lane's weights' tokens n and n + 8 (all four
+      // blocks in one 16-bit word each)
+      const uint32_t zn = lds_u16(vz + 2 * n), zn8 = lds_u16(vz + 2 * n + 16);
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const float sca = b == 0 ? va01.x : b == 1 ? va01.y : b == 2 ? va23.x : va23.y;
+        const float scb = b == 0 ? vb01.x : b == 1 ? vb01.y : b == 2 ? vb23.x : vb23.y;
+        const float q00 = pa[0][0] * sca, q01 = pa[0][1] * sca, q10 = pa[0][2] * scb, q11 = pa[0][3] * scb;
+        // hi on the lanes of columns 0..3, lo = what hi leaves on those of 4..7
+        const float2 f0 = half2_bits_to_float2(pack_f16x2(q00, q01));
+        const float2 f1 = half2_bits_to_float2(pack_f16x2(q10, q11));
+        const uint32_t pb0 = movmatrix_trans(pack_f16x2(fmaf(-hsel, f0.x, q00), fmaf(-hsel, f0.y, q01)));
+        const uint32_t pb1 = movmatrix_trans(pack_f16x2(fmaf(-hsel, f1.x, q10), fmaf(-hsel, f1.y, q11)));
+        // zp * 16^b as an exact fp32 integer (the nibble in place, 2^23 bias off)
+        const float za = __uint_as_float(0x4B000000u | (zn & (0xFu << (4 * b)))) - 8388608.f;
+        const float zb = __uint_as_float(0x4B000000u | (zn8 & (0xFu << (4 * b)))) - 8388608.f;
+        zc[b][0] = fmaf(q00, za, fmaf(q10, zb, zc[b][0]));
+        zc[b][1] = fmaf(q01, za, fmaf(q11, zb, zc[b][1]));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t w01 = vw[b][0] >> (8 * h), w89 = vw[b][1] >> (8 * h);
+          mma_f16_16816(o[0][2 * b + h], w01 & kLoNib, w01 & kHiNib, w89 & kLoNib, w89 & kHiNib, pb0, pb1);
+        }
+      }
+      return;
+    }
+    // zero points of the lane's V^T columns: tokens (2c, 2c+1) and (2c+8, 2c+9)
+    // in the two 16-bit halves
+    const uint32_t zv01 = lds_u32(vz + 4 * c), zv89 = lds_u32(vz + 4 * c + 16);
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       const float sca = b == 0 ? va01.x : b == 1 ? va01.y : b == 2 ? va23.x : va23.y;
@@ -599,8 +661,9 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES, CHUNK 
   for (int j = 0; j < nstage; ++j) {
     const int tile_idx = j * NWARPS + warp;
     if (tile_idx >= nsub) break;  // the last stage may hold fewer tiles
-    const int st = (jbase + j) % STAGES;
-    if (!mbar_wait_bounded(bar0 + 8 * st, ((jbase + j) / STAGES) & 1)) {
+    const uint32_t jj = (uint32_t)(jbase + j);
+    const int st = (int)(jj % STAGES);
+    if (!mbar_wait_bounded(bar0 + 8 * st, (jj / STAGES) & 1)) {
       if (lane == 0) set_status(p.status, OL_DEVICE_GUARD);
       break;
     }
@@ -624,6 +687,31 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES, CHUNK 
   }
   __syncthreads();  // all stages consumed: they now hold the warps' states
 
+  if constexpr (DUP) {
+    // the zero-point term, summed over the tile rows (lanes n), off every dim
+    // of its block on the hi lanes (units of O: 2^-24, 16^-b; 16 times more
+    // on the rows of upper-nibble dims); then the lo columns added in
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        float v = zc[b][k];
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        v += __shfl_xor_sync(0xffffffffu, v, 8);
+        v += __shfl_xor_sync(0xffffffffu, v, 16);
+        zc[b][k] = c < 2 ? v * ldexpf(1.f, -24 - 4 * b) : 0.f;
+      }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const int b = mt >> 1;
+      o[0][mt][0] -= zc[b][0];
+      o[0][mt][1] -= zc[b][1];
+      o[0][mt][2] -= 16.f * zc[b][0];
+      o[0][mt][3] -= 16.f * zc[b][1];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) o[0][mt][k] += __shfl_xor_sync(0xffffffffu, o[0][mt][k], 2);
+    }
+  }
   if (ev != kNoExp) {  // O to plain units: 2^(24 - ev), and 1/16 more for the rows of upper-nibble dims
     const float f = ldexpf(1.f, 24 - ev), f16 = f * 0.0625f;
 #pragma unroll
@@ -733,10 +821,10 @@ bool encode_int4_maps(CUtensorMap (&maps)[3], const AttnParams& p, int nwarps) {
          encode_planes(&maps[2], p.zps, 16, rows / 8, tok / 8, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-template <int NWARPS, int STAGES, bool CHUNK = false>
+template <int NWARPS, int STAGES, bool CHUNK = false, bool DUP = false>
 cudaError_t ensure_attrs() {
   static cudaError_t state = [] {
-    auto kern = fast_int4_kernel<NWARPS, STAGES, CHUNK>;
+    auto kern = fast_int4_kernel<NWARPS, STAGES, CHUNK, DUP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Int4Layout<NWARPS, STAGES, CHUNK ? 2 : 1>::kTotal);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -771,11 +859,11 @@ int max_cluster() {
   return cs;
 }
 
-template <int NWARPS, int STAGES, bool CHUNK>
+template <int NWARPS, int STAGES, bool CHUNK, bool DUP = false>
 cudaError_t launch_cfg(const AttnParams& p, cudaStream_t s) {
   CUtensorMap maps[3];
   if (!encode_int4_maps(maps, p, NWARPS)) return cudaErrorInvalidValue;
-  cudaError_t e = ensure_attrs<NWARPS, STAGES, CHUNK>();
+  cudaError_t e = ensure_attrs<NWARPS, STAGES, CHUNK, DUP>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   // a chunked step: pairs of slices of query tokens along x (a CTA carries two
@@ -794,7 +882,7 @@ cudaError_t launch_cfg(const AttnParams& p, cudaStream_t s) {
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, fast_int4_kernel<NWARPS, STAGES, CHUNK>, maps[0], maps[1], maps[2], p);
+  return cudaLaunchKernelEx(&cfg, fast_int4_kernel<NWARPS, STAGES, CHUNK, DUP>, maps[0], maps[1], maps[2], p);
 }
 
 }  // namespace
@@ -818,6 +906,13 @@ int fast_int4_smem(int variant) {
   }
 }
 int fast_int4_warps(int variant) { return variant == 1 ? 4 : 8; }
+int fast_int4_ctas_per_sm(int variant, bool chunk) {
+  switch (variant) {
+    case 1: return chunk ? Int4Layout<4, 4, 2>::kPerSm : Int4Layout<4, 4>::kPerSm;
+    case 2: return chunk ? Int4Layout<8, 2, 2>::kPerSm : Int4Layout<8, 2>::kPerSm;
+    default: return chunk ? Int4Layout<8, 4, 2>::kPerSm : Int4Layout<8, 4>::kPerSm;
+  }
+}
 int fast_int4_max_cluster(int variant) {
   switch (variant) {
     case 1: return max_cluster<4, 4>();
@@ -833,6 +928,13 @@ cudaError_t launch_fast_int4(const AttnParams& p, cudaStream_t s) {
       case 1: return launch_cfg<4, 4, true>(p, s);
       case 2: return launch_cfg<8, 2, true>(p, s);
       default: return launch_cfg<8, 4, true>(p, s);
+    }
+  }
+  if (p.group <= 4) {  // the lo half of P^T in the free MMA columns
+    switch (p.variant) {
+      case 1: return launch_cfg<4, 4, false, true>(p, s);
+      case 2: return launch_cfg<8, 2, false, true>(p, s);
+      default: return launch_cfg<8, 4, false, true>(p, s);
     }
   }
   switch (p.variant) {

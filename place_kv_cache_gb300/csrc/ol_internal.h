@@ -159,6 +159,7 @@ cudaError_t launch_fast_bf16(const AttnParams& p, cudaStream_t s);
 bool fast_int4_supported(const AttnParams& p);
 int fast_int4_smem(int variant);
 int fast_int4_warps(int variant);
+int fast_int4_ctas_per_sm(int variant, bool chunk);
 int fast_int4_max_cluster(int variant);
 cudaError_t launch_fast_int4(const AttnParams& p, cudaStream_t s);
 bool fast_hpaged_supported(const AttnParams& p);

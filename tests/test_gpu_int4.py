@@ -49,6 +49,9 @@ def desc_of(dplanes, w, mode, access=ol.OL_READ_WRITE):  # noqa: D401
 @pytest.mark.parametrize("shape", [
     ("b3_gqa4", 3, 32, 8, 128, 300, [1, 17, 300]),
     ("b2_gqa7", 2, 28, 4, 128, 160, [160, 64]),
+    ("b2_gqa5", 2, 10, 2, 128, 150, [150, 20]),
+    ("b2_gqa2", 2, 8, 4, 128, 200, [200, 33]),
+    ("b2_gqa1", 2, 4, 4, 128, 130, [130, 5]),
     ("b2_d64", 2, 8, 2, 64, 96, [96, 33]),
     ("b1_d256_gqa1", 1, 2, 2, 256, 64, [50]),
 ], ids=lambda s: s[0])
@@ -183,5 +186,35 @@ def test_int4_streamk_matches_oracle(shape):
     O.int4_append(*planes, case.new_kv, case.lens - 1, mode=O.Q_DYNAMIC)
     for g, r in zip(host_planes(dplanes), planes):
         np.testing.assert_array_equal(g, r)
+    want = O.int4_attention(case.q, *planes, case.lens, cur_kv=case.new_kv, window=window)
+    assert max_abs_err(out_as_f64(out), want) <= TOL
+
+
+def scaled_bf16(x, std):
+    """bf16 bit patterns of std times the bf16 values x (rounded to nearest even)."""
+    f = (x.astype(np.uint32) << 16).view(np.float32) * np.float32(std)
+    return bf16_from_f32(f.astype(np.float32))
+
+
+@pytest.mark.parametrize("heads", [(32, 8), (28, 4)], ids=["gqa4", "gqa7"])
+@pytest.mark.parametrize("window", [0, 1, 3, -1])
+def test_int4_large_values_short_windows(heads, window):
+    # values N(0, 3): with few visible tokens nothing averages the rounding of
+    # the weights, so the V side's error shows at its full size (a single fp16
+    # P^T times the V scale put it at about 2e-3 here)
+    Hq, Hkv = heads
+    B, D, C = 4, 128, 512
+    w = Workload("i4big", "bf16", B, Hq, Hkv, D, C, "int4", seed=37)
+    case = make_case(w, lens=np.array([512, 300, 17, 2], np.int32))
+    case.history = [scaled_bf16(h, 3.0) for h in case.history]
+    case.new_kv = scaled_bf16(case.new_kv, 3.0)
+    planes = oracle_planes(case, O.Q_DYNAMIC)
+    dplanes = dev_planes(planes)
+    ws, n = workspace(B, Hq, Hkv, D)
+    out = out_tensor(B, Hq, D, ol.OL_F32)
+    ol.ol_int4kv_decode_attention(desc_of(dplanes, w, O.Q_DYNAMIC, access=ol.OL_READ_ONLY), to_dev(case.q), Hq,
+                                  case.lens, to_dev(case.lens), to_dev(case.new_kv), 0.0, window, out, ol.OL_F32,
+                                  ws, n)
+    torch.cuda.synchronize()
     want = O.int4_attention(case.q, *planes, case.lens, cur_kv=case.new_kv, window=window)
     assert max_abs_err(out_as_f64(out), want) <= TOL
