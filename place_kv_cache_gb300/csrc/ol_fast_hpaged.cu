@@ -166,11 +166,18 @@ __device__ __forceinline__ int map_row(const AttnParams& p, int page, int plane,
 // tokens take part uncompressed from new_kv, folded causally into warp 0's
 // state after the tile loop. Its own instantiation: the decode kernel keeps
 // its own code.
-template <int NWARPS, int STAGES, bool CHUNK = false>
+// DUP (a decode step with at most 4 heads per kv head): MMA columns 4..7
+// repeat the heads of columns 0..3, so the two halves of P^T (hi and lo)
+// travel in one MMA, hi in columns 0..3 and lo in 4..7, added when the state
+// is stored. Affine V codes then enter as exact fp16 subnormals c' * 2^-24
+// (O in units of 2^(k + 24) on those tiles) and the page's zero point is one
+// fp32 sum per column, zp' * sum_t P'[t], subtracted at the end.
+template <int NWARPS, int STAGES, bool CHUNK = false, bool DUP = false>
 __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
     fast_hpaged_kernel(const __grid_constant__ CUtensorMap tm16, const __grid_constant__ CUtensorMap tm8,
                        const __grid_constant__ CUtensorMap tm4, const __grid_constant__ CUtensorMap tm2,
                        const __grid_constant__ AttnParams p) {
+  static_assert(!(CHUNK && DUP), "duplicated columns serve a decode step only");
   using L = HpLayout<NWARPS, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -268,6 +275,7 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
       if (fmt_affine(fv)) {
         kv = log2_floor(fv_.scale);
         mv = fv_.scale * pow2f(-kv);
+        if (DUP) kv += 24;  // the codes enter as c' * 2^-24
         vz = fv_.zero_point + code_offset(fv);
       }
       la_page = page;
@@ -331,8 +339,9 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
   // per CTA by warp 0
   const int c = lane & 3, n = lane >> 2;
   const int ncols = CHUNK ? G * (zlast - z0 + 1) : G;
-  const bool live = n < ncols;
-  const int nl = live ? n : 0;
+  const int ncol = DUP ? (n & 3) : n;  // the state column of MMA column n
+  const bool live = ncol < ncols;
+  const int nl = live ? ncol : 0;
   const uint16_t* qp = reinterpret_cast<const uint16_t*>(p.q) +
                        (CHUNK ? (((size_t)w.b * p.q_heads + (size_t)w.g * G + nl % G) * p.nq + z0 + nl / G) * 128
                               : ((size_t)w.b * p.q_heads + (size_t)w.g * G + nl) * 128);
@@ -421,6 +430,10 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
   for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   float m_run0 = -INFINITY, m_run1 = -INFINITY, l_run0 = 0.f, l_run1 = 0.f;
   int ko = 0;  // O is held in units of 2^ko
+  // DUP: the zero-point term of the lane's columns 2c, 2c + 1 over its tokens
+  // (units of O times 2^24), and 1 on the lanes of columns 4..7 (the lo half)
+  float zc0 = 0.f, zc1 = 0.f;
+  const float hsel = DUP && c >= 2 ? 1.f : 0.f;
 
   const int mi = lane >> 3, r8 = lane & 7;
   const int rK = r8 + 8 * (mi & 1), cK = mi >> 1;  // ldmatrix roles for 16-bit K
@@ -589,6 +602,10 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
         o[mt][2] *= al0;
         o[mt][3] *= al1;
       }
+      if constexpr (DUP) {
+        zc0 *= al0;
+        zc1 *= al1;
+      }
       m_run0 = mn0;
       m_run1 = mn1;
     }
@@ -604,14 +621,39 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
       for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
         for (int j = 0; j < 4; ++j) o[mt][j] *= f;
+      if constexpr (DUP) {
+        zc0 *= f;
+        zc1 *= f;
+      }
       ko = kv;
     }
 
     // ---- O^T += V^T P^T (dimension order: m-tile 2bb + hh, row n -> 32bb + 4n + 2hh, row n + 8 -> + 1)
     const int TA = 2 * c, TB = 2 * c + 1, TC = 2 * c + 8, TD = 2 * c + 9;  // this lane's tokens (k rows)
     const bool half_p = fv != OL_FMT_BF16 && fv != OL_FMT_F32;  // P^T in fp16 (else bf16)
-    uint32_t ph0, ph1, pl0, pl1;
-    {
+    uint32_t ph0, ph1, pl0 = 0u, pl1 = 0u;
+    if constexpr (DUP) {
+      // hi on the lanes of columns 0..3, lo = what hi leaves on those of 4..7
+      if (half_p) {
+        const float x0 = p00 * mv, x1 = p01 * mv, x2 = p10 * mv, x3 = p11 * mv;
+        uint32_t h0 = pack_f16x2(x0, x1), h1 = pack_f16x2(x2, x3);
+        const float2 f0 = __half22float2(*reinterpret_cast<__half2*>(&h0));
+        const float2 f1 = __half22float2(*reinterpret_cast<__half2*>(&h1));
+        ph0 = movmatrix_trans(pack_f16x2(fmaf(-hsel, f0.x, x0), fmaf(-hsel, f0.y, x1)));
+        ph1 = movmatrix_trans(pack_f16x2(fmaf(-hsel, f1.x, x2), fmaf(-hsel, f1.y, x3)));
+        if (fmt_affine(fv)) {  // the page's zero point, times the weights as they are
+          const float z = (float)vz;
+          zc0 = fmaf(z, x0 + x2, zc0);
+          zc1 = fmaf(z, x1 + x3, zc1);
+        }
+      } else {
+        const uint32_t h0 = pack_bf16x2(p00, p01), h1 = pack_bf16x2(p10, p11);
+        ph0 = movmatrix_trans(pack_bf16x2(fmaf(-hsel, __uint_as_float(h0 << 16), p00),
+                                          fmaf(-hsel, __uint_as_float(h0 & 0xffff0000u), p01)));
+        ph1 = movmatrix_trans(pack_bf16x2(fmaf(-hsel, __uint_as_float(h1 << 16), p10),
+                                          fmaf(-hsel, __uint_as_float(h1 & 0xffff0000u), p11)));
+      }
+    } else {
       uint32_t h0, l0, h1, l1;
       if (half_p) {
         split_f16(p00 * mv, p01 * mv, h0, l0);
@@ -649,7 +691,7 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
           split_bf16(xc0, xd0, a2h, a2l);
           split_bf16(xc1, xd1, a3h, a3l);
           mma_bf16_16816(o[2 * bb + hh], a0h, a1h, a2h, a3h, ph0, ph1);
-          mma_bf16_16816(o[2 * bb + hh], a0h, a1h, a2h, a3h, pl0, pl1);
+          if (!DUP) mma_bf16_16816(o[2 * bb + hh], a0h, a1h, a2h, a3h, pl0, pl1);
           mma_bf16_16816(o[2 * bb + hh], a0l, a1l, a2l, a3l, ph0, ph1);
         }
       }
@@ -673,10 +715,10 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
           const uint32_t a2 = prmt(xc, xd, 0x5410u), a3 = prmt(xc, xd, 0x7632u);
           if (h16) {
             mma_f16_16816(o[2 * bb + hh], a0, a1, a2, a3, ph0, ph1);
-            mma_f16_16816(o[2 * bb + hh], a0, a1, a2, a3, pl0, pl1);
+            if (!DUP) mma_f16_16816(o[2 * bb + hh], a0, a1, a2, a3, pl0, pl1);
           } else {
             mma_bf16_16816(o[2 * bb + hh], a0, a1, a2, a3, ph0, ph1);
-            mma_bf16_16816(o[2 * bb + hh], a0, a1, a2, a3, pl0, pl1);
+            if (!DUP) mma_bf16_16816(o[2 * bb + hh], a0, a1, a2, a3, pl0, pl1);
           }
         }
       }
@@ -687,6 +729,10 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
       const uint32_t zf = (uint32_t)__half_as_ushort(__int2half_rn(1024 + vz));
       const uint32_t zpair = zf | (zf << 16);
       auto add_tile = [&](int mt, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
+        if constexpr (DUP) {  // c' * 2^-24 as they are; the zero point is in zc
+          mma_f16_16816(o[mt], a0, a1, a2, a3, ph0, ph1);
+          return;
+        }
         a0 = hsub2_f16(a0, zpair);
         a1 = hsub2_f16(a1, zpair);
         a2 = hsub2_f16(a2, zpair);
@@ -694,8 +740,10 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
         mma_f16_16816(o[mt], a0, a1, a2, a3, ph0, ph1);
         mma_f16_16816(o[mt], a0, a1, a2, a3, pl0, pl1);
       };
+      // the offset-binary flip of signed codes, and (not DUP) the fp16 1024 around them
+      const uint32_t hi1024 = DUP ? 0u : 0x64006400u;
       if (bits == 8) {
-        const uint32_t magic = sgn ? 0x64806480u : 0x64006400u;
+        const uint32_t magic = (sgn ? 0x00800080u : 0u) | hi1024;
 #pragma unroll
         for (int bb = 0; bb < 4; ++bb) {
           const int ch = 2 * bb + (n >> 2), sub = 4 * (n & 3);
@@ -712,7 +760,7 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
           }
         }
       } else if (bits == 4) {
-        const uint32_t magic = sgn ? 0x64086408u : 0x64006400u;
+        const uint32_t magic = (sgn ? 0x00080008u : 0u) | hi1024;
 #pragma unroll
         for (int bp = 0; bp < 2; ++bp) {
           // matrices (tokens 0-7 | 8-15) x (32-dim blocks 2bp | 2bp + 1)
@@ -732,7 +780,7 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
           }
         }
       } else {
-        const uint32_t magic = sgn ? 0x64026402u : 0x64006400u;
+        const uint32_t magic = (sgn ? 0x00020002u : 0u) | hi1024;
 #pragma unroll
         for (int bb = 0; bb < 4; ++bb) {
           // byte 8bb + n of each token row: dims 32bb + 4n .. + 3
@@ -755,6 +803,27 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
     __syncwarp();
   }
 
+  if constexpr (DUP) {
+    // the zero-point term, summed over the tile rows (lanes n), off every dim
+    // on the hi lanes (units of O: 2^-24); then the lo columns added in
+    float z0s = zc0, z1s = zc1;
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      z0s += __shfl_xor_sync(0xffffffffu, z0s, off);
+      z1s += __shfl_xor_sync(0xffffffffu, z1s, off);
+    }
+    z0s = c < 2 ? z0s * 5.9604644775390625e-8f : 0.f;
+    z1s = c < 2 ? z1s * 5.9604644775390625e-8f : 0.f;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      o[mt][0] -= z0s;
+      o[mt][1] -= z1s;
+      o[mt][2] -= z0s;
+      o[mt][3] -= z1s;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o[mt][j] += __shfl_xor_sync(0xffffffffu, o[mt][j], 2);
+    }
+  }
   if (ko != 0) {
     const float f = pow2f(ko);
 #pragma unroll
@@ -911,9 +980,9 @@ bool encode_width(CUtensorMap* map, void* base, uint64_t pool_bytes, int width) 
 
 constexpr int kWarps = 6, kStages = 2;
 
-template <bool CHUNK>
+template <bool CHUNK, bool DUP = false>
 cudaError_t ensure_attrs() {
-  static cudaError_t state = cudaFuncSetAttribute(fast_hpaged_kernel<kWarps, kStages, CHUNK>,
+  static cudaError_t state = cudaFuncSetAttribute(fast_hpaged_kernel<kWarps, kStages, CHUNK, DUP>,
                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                   HpLayout<kWarps, kStages>::kTotal);
   return state;
@@ -940,8 +1009,8 @@ cudaError_t launch_fast_hpaged(const AttnParams& p, cudaStream_t s) {
   if (!encode_width(&maps[0], p.pool, bytes, 256) || !encode_width(&maps[1], p.pool, bytes, 128) ||
       !encode_width(&maps[2], p.pool, bytes, 64) || !encode_width(&maps[3], p.pool, bytes, 32))
     return cudaErrorInvalidValue;
-  const bool chunk = p.nq > 1;
-  cudaError_t e = chunk ? ensure_attrs<true>() : ensure_attrs<false>();
+  const bool chunk = p.nq > 1, dup = !chunk && p.group <= 4;
+  cudaError_t e = chunk ? ensure_attrs<true>() : dup ? ensure_attrs<false, true>() : ensure_attrs<false>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   // a chunked step: slices of query tokens along x, the split plan's CTAs along y
@@ -956,6 +1025,9 @@ cudaError_t launch_fast_hpaged(const AttnParams& p, cudaStream_t s) {
   cfg.numAttrs = 1;
   if (chunk)
     return cudaLaunchKernelEx(&cfg, fast_hpaged_kernel<kWarps, kStages, true>, maps[0], maps[1], maps[2], maps[3], p);
+  if (dup)  // the lo half of P^T in the free MMA columns
+    return cudaLaunchKernelEx(&cfg, fast_hpaged_kernel<kWarps, kStages, false, true>, maps[0], maps[1], maps[2],
+                              maps[3], p);
   return cudaLaunchKernelEx(&cfg, fast_hpaged_kernel<kWarps, kStages, false>, maps[0], maps[1], maps[2], maps[3], p);
 }
 
