@@ -788,7 +788,7 @@ ol_status run_attention(int layout, const void* desc, const CacheView& v, const 
     order_rows(p, lens_host);
     e = launch_fast_int4(p, stream);
   } else if (layout == OL_LAYOUT_HPAGED && hpaged_fast_path(p) && !tune().generic) {
-    plan_splits(p, lens_host, (long long)sms * fast_hpaged_ctas_per_sm() * tune().hp_waves, 1);
+    plan_splits(p, lens_host, (long long)sms * fast_hpaged_ctas_per_sm(p.nq > 1) * tune().hp_waves, 1);
     order_rows(p, lens_host);
     p.variant = 0;
     e = launch_fast_hpaged(p, stream);

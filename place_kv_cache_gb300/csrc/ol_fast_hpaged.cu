@@ -50,17 +50,19 @@ constexpr int kHalf = 2048;           // a 16-bit tile's second 64-dimension hal
 constexpr int kInfo = 8;              // ints of tile information per stage
 constexpr float kLazy = 8.f;          // log2 headroom of the lazy softmax maximum
 
-template <int NWARPS, int STAGES>
+template <int NWARPS, int STAGES, int NG = 1>
 struct HpLayout {
   static constexpr int kStages = NWARPS * STAGES * kStage;
-  static constexpr int kQ = 4 * 8 * 32 * 8;  // q operands: 4 orders x 8 k-steps x 32 lanes x 2 registers
-  static constexpr int kQAux = 2 * 8 * 4;    // per head: exponent e and sum of q
+  // q operands of each column group: 4 orders x 8 k-steps x 32 lanes x 2 registers
+  static constexpr int kQ = NG * 4 * 8 * 32 * 8;
+  static constexpr int kQAux = NG * 2 * 8 * 4;  // per column: exponent e and sum of q
   static constexpr int kInfoBytes = NWARPS * STAGES * kInfo * 4;
   static constexpr int kBars = NWARPS * STAGES * 8;
   static constexpr int kMisc = 256 + NWARPS * 8 * 4 * 2 + 8 * 4 * 6 + 2 * 16 * 8 * 4 + 16;
   static constexpr int kTotal = 1024 + kStages + kQ + kQAux + kInfoBytes + kBars + kMisc;
   static constexpr int kBySmem = (228 * 1024) / (kTotal + 1024) > 0 ? (228 * 1024) / (kTotal + 1024) : 1;
-  static constexpr int kPerSm = kBySmem < 2 ? kBySmem : 2;
+  // two column groups take up to 255 registers: one CTA per SM
+  static constexpr int kPerSm = NG > 1 ? 1 : (kBySmem < 2 ? kBySmem : 2);
   static_assert(STAGES >= 2, "the merged O lives in warp 0's second stage");
   static_assert(8 * kOStride * 4 <= kStage, "a warp state fits one stage");
 };
@@ -160,12 +162,14 @@ __device__ __forceinline__ int map_row(const AttnParams& p, int page, int plane,
 
 // -------------------------------------------------------------- the kernel
 
-// CHUNK: a chunked step's attention (grid x = slice of query tokens, y = the
-// split): state columns are (query token, head) pairs, each masked to its
-// token's window; the history ends where the chunk starts, and the chunk's
-// tokens take part uncompressed from new_kv, folded causally into warp 0's
-// state after the tile loop. Its own instantiation: the decode kernel keeps
-// its own code.
+// CHUNK: a chunked step's attention (grid x = pair of slices of query tokens,
+// y = the split): state columns are (query token, head) pairs, each masked to
+// its token's window; the history ends where the chunk starts, and the
+// chunk's tokens take part uncompressed from new_kv, folded causally into
+// warp 0's state after the tile loop. A warp carries two slices' columns (two
+// column groups: their own q operands, scores, softmax states and O) and
+// decodes each tile's operands once for both. Its own instantiation: the
+// decode kernel keeps its own code.
 // DUP (a decode step with at most 4 heads per kv head): MMA columns 4..7
 // repeat the heads of columns 0..3, so the two halves of P^T (hi and lo)
 // travel in one MMA, hi in columns 0..3 and lo in 4..7, added when the state
@@ -173,18 +177,19 @@ __device__ __forceinline__ int map_row(const AttnParams& p, int page, int plane,
 // (O in units of 2^(k + 24) on those tiles) and the page's zero point is one
 // fp32 sum per column, zp' * sum_t P'[t], subtracted at the end.
 template <int NWARPS, int STAGES, bool CHUNK = false, bool DUP = false>
-__global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
+__global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES, CHUNK ? 2 : 1>::kPerSm)
     fast_hpaged_kernel(const __grid_constant__ CUtensorMap tm16, const __grid_constant__ CUtensorMap tm8,
                        const __grid_constant__ CUtensorMap tm4, const __grid_constant__ CUtensorMap tm2,
                        const __grid_constant__ AttnParams p) {
   static_assert(!(CHUNK && DUP), "duplicated columns serve a decode step only");
-  using L = HpLayout<NWARPS, STAGES>;
+  constexpr int NG = CHUNK ? 2 : 1;  // column groups a warp carries (a chunked step: two slices)
+  using L = HpLayout<NWARPS, STAGES, NG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* stages = smem;
-  uint2* qsm = reinterpret_cast<uint2*>(smem + L::kStages);            // [order][kk][lane]
-  int* qexp = reinterpret_cast<int*>(smem + L::kStages + L::kQ);       // [8] per head
-  float* qsum_h = reinterpret_cast<float*>(qexp + 8);                  // [8] per head
+  uint2* qsm = reinterpret_cast<uint2*>(smem + L::kStages);            // [group][order][kk][lane]
+  int* qexp = reinterpret_cast<int*>(smem + L::kStages + L::kQ);       // [group][8] per column
+  float* qsum_h = reinterpret_cast<float*>(qexp + NG * 8);             // [group][8] per column
   uint8_t* after_q = smem + L::kStages + L::kQ + L::kQAux;
   int* info = reinterpret_cast<int*>(after_q);
   uint64_t* bars = reinterpret_cast<uint64_t*>(after_q + L::kInfoBytes);
@@ -217,12 +222,16 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
   }
   pdl_wait();
   pdl_launch_dependents();
+  // a chunked step's CTA serves NG consecutive slices of query tokens, zs0 .. zs0 + nsl - 1
+  const int nslices = CHUNK ? (p.nq + slice_tq(p) - 1) / slice_tq(p) : 1;
+  const int zs0 = CHUNK ? NG * query_index(p) : 0;
+  const int nsl = CHUNK ? min(NG, nslices - zs0) : 1;
   if (warp == 0) {
     Work w = p.inline_lens ? map_cta_warp(p.lens_inline, p.batch, p.kv_heads, p.capacity, p.window, p.chunk,
                                           cta_index(p), nullptr, 1, p.ordered ? p.row_order : nullptr)
                            : map_cta_warp(p.lens, p.batch, p.kv_heads, p.capacity, p.window, p.chunk, cta_index(p),
                                           p.status);
-    if (CHUNK) slice_query(w, p);
+    if (CHUNK) slice_query(w, p, zs0, zs0 + nsl - 1);
     if (lane == 0) *sw = w;
   }
   __syncthreads();
@@ -230,9 +239,15 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
   if (!w.valid) return;
 
   const int G = p.group;
-  // a chunked step's slice zs: query tokens z0 .. zlast; w.hi is one past zlast's position
-  const int zs = CHUNK ? query_index(p) : 0;
-  const int z0 = CHUNK ? slice_first(p, zs) : 0, zlast = CHUNK ? z0 + slice_tokens(p, zs) - 1 : 0;
+  // column group g: slice zs0 + g, query tokens gz0[g] .. gzl[g] (a group past the
+  // last slice has none: gzl = gz0 - 1); w.hi is one past the last slice's last token
+  int gz0[NG], gzl[NG];
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    gz0[g] = CHUNK ? slice_first(p, zs0 + g) : 0;
+    gzl[g] = CHUNK ? (g < nsl ? gz0[g] + slice_tokens(p, zs0 + g) - 1 : gz0[g] - 1) : 0;
+  }
+  const int zlast = gzl[nsl - 1];
   const int cur = p.cur_from_new ? w.hi - 1 : -1;
   // history tiles: [t_begin, tend); the current token (a chunk: the chunk's
   // tokens up to the slice's last one, from new_kv) is not read from the cache
@@ -334,19 +349,26 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
   };
   for (int i = 0; i < min(my_n, STAGES); ++i) issue(i);
 
-  // ---- q operands (lane: c = lane % 4, n = lane / 4 = state column: the head,
-  // or for a chunked step head n % G of query token z0 + n / G), written once
-  // per CTA by warp 0
+  // ---- q operands of each column group (lane: c = lane % 4, n = lane / 4 =
+  // state column: the head, or for a chunked step head n % G of the slice's
+  // query token n / G), written once per CTA, group g by warp g
   const int c = lane & 3, n = lane >> 2;
-  const int ncols = CHUNK ? G * (zlast - z0 + 1) : G;
   const int ncol = DUP ? (n & 3) : n;  // the state column of MMA column n
-  const bool live = ncol < ncols;
-  const int nl = live ? ncol : 0;
-  const uint16_t* qp = reinterpret_cast<const uint16_t*>(p.q) +
-                       (CHUNK ? (((size_t)w.b * p.q_heads + (size_t)w.g * G + nl % G) * p.nq + z0 + nl / G) * 128
-                              : ((size_t)w.b * p.q_heads + (size_t)w.g * G + nl) * 128);
-  if (warp == 0) {
-    // this lane's 32 dims 32c .. 32c + 31 of head n: head n's exponent e and sum
+  auto gcols = [&](int g) { return CHUNK ? G * (gzl[g] - gz0[g] + 1) : G; };  // live columns of group g
+  // the q row of this lane's column in group g (live: the column exists)
+  auto gq = [&](int g, bool& live) -> const uint16_t* {
+    live = ncol < gcols(g);
+    const int nl = live ? ncol : 0;
+    return reinterpret_cast<const uint16_t*>(p.q) +
+           (CHUNK ? (((size_t)w.b * p.q_heads + (size_t)w.g * G + nl % G) * p.nq + gz0[g] + nl / G) * 128
+                  : ((size_t)w.b * p.q_heads + (size_t)w.g * G + nl) * 128);
+  };
+  if (warp < NG) {
+    const int g = warp;
+    bool live;
+    const uint16_t* qp = gq(g, live);
+    uint2* qg = qsm + g * 4 * 8 * 32;
+    // this lane's 32 dims 32c .. 32c + 31 of column n: its exponent e and sum
     uint32_t qraw[16];
     const uint4* src = reinterpret_cast<const uint4*>(qp + 32 * c);
 #pragma unroll
@@ -368,11 +390,11 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
     qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 2));
     qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
     qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
-    const int qe = qmax > 0.f ? 14 - log2_floor(qmax) : 0;  // head n's largest |q| * 2^e in [2^14, 2^15)
+    const int qe = qmax > 0.f ? 14 - log2_floor(qmax) : 0;  // column n's largest |q| * 2^e in [2^14, 2^15)
     const float s2e_n = pow2f(qe);
     if (c == 0) {
-      qexp[n] = qe;
-      qsum_h[n] = qsum;
+      qexp[g * 8 + n] = qe;
+      qsum_h[g * 8 + n] = qsum;
     }
     auto qd = [&](int j) {  // q[n][32c + j] * 2^e as float (j < 32)
       const uint32_t wd = qraw[j >> 1];
@@ -384,18 +406,18 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
       uint2 b;
       b.x = live ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * kk + 2 * c)) : 0u;
       b.y = live ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * kk + 2 * c + 8)) : 0u;
-      qsm[(0 * 8 + kk) * 32 + lane] = b;
+      qg[(0 * 8 + kk) * 32 + lane] = b;
       // order 1, 4-bit codes: kk = 2i + h, e_j = 8i + j: (e_2h, e_2h+4) | (e_2h+1, e_2h+5) / 16
       {
         const int i = kk >> 1, h = kk & 1, e = 8 * i;
         b.x = pack_f16x2(qd(e + 2 * h), qd(e + 2 * h + 4));
         b.y = pack_f16x2(qd(e + 2 * h + 1) * 0.0625f, qd(e + 2 * h + 5) * 0.0625f);
-        qsm[(1 * 8 + kk) * 32 + lane] = b;
+        qg[(1 * 8 + kk) * 32 + lane] = b;
       }
       // order 2, 8-bit codes: d_j = 4kk + j: (d0, d2) | (d1, d3)
       b.x = pack_f16x2(qd(4 * kk), qd(4 * kk + 2));
       b.y = pack_f16x2(qd(4 * kk + 1), qd(4 * kk + 3));
-      qsm[(2 * 8 + kk) * 32 + lane] = b;
+      qg[(2 * 8 + kk) * 32 + lane] = b;
       // order 3, 2-bit codes: word w = kk / 4, pairs j = 2(kk % 4) (+1): (16w + j, 16w + j + 8) / 4^f(j),
       // f(j) = j below 5, j - 5 from 5 (the bit position / 2 of the masked code)
       {
@@ -403,32 +425,47 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
         const float f0 = pow2f(-2 * (j0 < 5 ? j0 : j0 - 5)), f1 = pow2f(-2 * (j1 < 5 ? j1 : j1 - 5));
         b.x = pack_f16x2(qd(16 * wv + j0) * f0, qd(16 * wv + j0 + 8) * f0);
         b.y = pack_f16x2(qd(16 * wv + j1) * f1, qd(16 * wv + j1 + 8) * f1);
-        qsm[(3 * 8 + kk) * 32 + lane] = b;
+        qg[(3 * 8 + kk) * 32 + lane] = b;
       }
     }
   }
   __syncthreads();
-  const int e_own = qexp[n];                                      // this lane's head (B-operand column n)
-  const float s2e = pow2f(e_own);
-  const int e0 = qexp[2 * c], e1 = qexp[2 * c + 1];               // this lane's state columns 2c, 2c + 1
-  const float qs0 = qsum_h[2 * c], qs1 = qsum_h[2 * c + 1];
-  const float pne0 = pow2f(-e0), pne1 = pow2f(-e1);  // 2^-e of this lane's state columns
+  // per group: 2^e of this lane's B-operand column n; 2^-e and sum(q) of its
+  // state columns 2c, 2c + 1
+  float s2e[NG], qs0[NG], qs1[NG], pne0[NG], pne1[NG];
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    s2e[g] = pow2f(qexp[g * 8 + n]);
+    qs0[g] = qsum_h[g * 8 + 2 * c];
+    qs1[g] = qsum_h[g * 8 + 2 * c + 1];
+    pne0[g] = pow2f(-qexp[g * 8 + 2 * c]);
+    pne1[g] = pow2f(-qexp[g * 8 + 2 * c + 1]);
+  }
   const uint32_t qbase = smem_u32(qsm) + lane * 8;
-  auto qop = [&](int order, int kk) { return lds_v2(qbase + (order * 8 + kk) * 256); };
+  auto qop = [&](int order, int kk, int g) { return lds_v2(qbase + ((g * 4 + order) * 8 + kk) * 256); };
 
-  // visible history of this lane's state columns 2c, 2c + 1: a chunked step's
-  // column from its own query token's window start
-  int clo0 = w.lo, clo1 = w.lo;
-  if (CHUNK && p.window_q >= 0) {
-    const int t0c = min((2 * c) / G, zlast - z0), t1c = min((2 * c + 1) / G, zlast - z0);
-    clo0 = max(w.lo, hist_end + z0 + t0c - p.window_q);
-    clo1 = max(w.lo, hist_end + z0 + t1c - p.window_q);
+  // visible history of this lane's state columns 2c, 2c + 1 of each group: a
+  // chunked step's column from its own query token's window start
+  int clo0[NG], clo1[NG];
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    clo0[g] = clo1[g] = w.lo;
+    if (CHUNK && p.window_q >= 0) {
+      const int t0c = min((2 * c) / G, gzl[g] - gz0[g]), t1c = min((2 * c + 1) / G, gzl[g] - gz0[g]);
+      clo0[g] = max(w.lo, hist_end + gz0[g] + t0c - p.window_q);
+      clo1[g] = max(w.lo, hist_end + gz0[g] + t1c - p.window_q);
+    }
   }
 
-  float o[8][4];
+  float o[NG][8][4];
+  float mr[NG][2], lr[NG][2];  // running maximum and sum of the lane's columns 2c, 2c + 1 of each group
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-  float m_run0 = -INFINITY, m_run1 = -INFINITY, l_run0 = 0.f, l_run1 = 0.f;
+  for (int g = 0; g < NG; ++g) {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) o[g][mt][0] = o[g][mt][1] = o[g][mt][2] = o[g][mt][3] = 0.f;
+    mr[g][0] = mr[g][1] = -INFINITY;
+    lr[g][0] = lr[g][1] = 0.f;
+  }
   int ko = 0;  // O is held in units of 2^ko
   // DUP: the zero-point term of the lane's columns 2c, 2c + 1 over its tokens
   // (units of O times 2^24), and 1 on the lanes of columns 4..7 (the lo half)
@@ -471,12 +508,13 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
     }
     __syncwarp();
 
-    // ---- S^T = K q^T, even and odd k-steps in two accumulators (shorter MMA chains)
-    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-    // S scale per column: kbase, times 2^-e for fp16-q formats; codes subtract kbias * sum(q)
-    const bool kq16 = fk != OL_FMT_BF16 && fk != OL_FMT_F32;
-    const float kmul0 = kq16 ? kbase * pne0 : kbase, kmul1 = kq16 ? kbase * pne1 : kbase;
-    const float kb0 = kbias * qs0, kb1 = kbias * qs1;
+    // ---- S^T = K q^T, even and odd k-steps in two accumulators (shorter MMA
+    // chains), one pair per column group; a tile's K operands serve every group
+    float sa[NG][4], sb[NG][4];
+#pragma unroll
+    for (int g = 0; g < NG; ++g)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sa[g][j] = sb[g][j] = 0.f;
     if (fk == OL_FMT_BF16 || fk == OL_FMT_F16) {
       const bool h16 = fk == OL_FMT_F16;
 #pragma unroll
@@ -484,14 +522,18 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
         const int ch = 2 * kk + cK;
         uint32_t a0, a1, a2, a3;
         ldsm_x4(sK + (ch >> 3) * kHalf + rK * 128 + (((ch & 7) ^ r8) << 4), a0, a1, a2, a3);
-        const uint2 q = qop(0, kk);
-        float(&acc)[4] = (kk & 1) ? sb : sa;
-        if (h16) {
-          const uint32_t b0 = pack_f16x2(__uint_as_float(q.x << 16) * s2e, __uint_as_float(q.x & 0xffff0000u) * s2e);
-          const uint32_t b1 = pack_f16x2(__uint_as_float(q.y << 16) * s2e, __uint_as_float(q.y & 0xffff0000u) * s2e);
-          mma_f16_16816(acc, a0, a1, a2, a3, b0, b1);
-        } else {
-          mma_bf16_16816(acc, a0, a1, a2, a3, q.x, q.y);
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          const uint2 q = qop(0, kk, g);
+          float(&acc)[4] = (kk & 1) ? sb[g] : sa[g];
+          if (h16) {
+            const float e = s2e[g];
+            const uint32_t b0 = pack_f16x2(__uint_as_float(q.x << 16) * e, __uint_as_float(q.x & 0xffff0000u) * e);
+            const uint32_t b1 = pack_f16x2(__uint_as_float(q.y << 16) * e, __uint_as_float(q.y & 0xffff0000u) * e);
+            mma_f16_16816(acc, a0, a1, a2, a3, b0, b1);
+          } else {
+            mma_bf16_16816(acc, a0, a1, a2, a3, q.x, q.y);
+          }
         }
       }
     } else if (fk == OL_FMT_F32) {
@@ -508,9 +550,12 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
         split_bf16(x1.x, x1.y, h1, l1);
         split_bf16(x2.x, x2.y, h2, l2);
         split_bf16(x3.x, x3.y, h3, l3);
-        const uint2 q = qop(0, kk);
-        mma_bf16_16816(sa, h0, h1, h2, h3, q.x, q.y);
-        mma_bf16_16816(sb, l0, l1, l2, l3, q.x, q.y);
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          const uint2 q = qop(0, kk, g);
+          mma_bf16_16816(sa[g], h0, h1, h2, h3, q.x, q.y);
+          mma_bf16_16816(sb[g], l0, l1, l2, l3, q.x, q.y);
+        }
       }
     } else {
       // affine codes: A = the code bits masked in place (fp16 subnormals), in the width's q order
@@ -530,9 +575,13 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t x = ya[kk] ^ flip, y = yb[kk] ^ flip;
-          const uint2 q = qop(2, kk);
-          mma_f16_16816((kk & 1) ? sb : sa, x & 0x00FF00FFu, y & 0x00FF00FFu, (x >> 8) & 0x00FF00FFu,
-                        (y >> 8) & 0x00FF00FFu, q.x, q.y);
+          const uint32_t a0 = x & 0x00FF00FFu, a1 = y & 0x00FF00FFu, a2 = (x >> 8) & 0x00FF00FFu,
+                         a3 = (y >> 8) & 0x00FF00FFu;
+#pragma unroll
+          for (int g = 0; g < NG; ++g) {
+            const uint2 q = qop(2, kk, g);
+            mma_f16_16816((kk & 1) ? sb[g] : sa[g], a0, a1, a2, a3, q.x, q.y);
+          }
         }
       } else if (bits == 4) {
         const int sw = (n >> 1) & 3;  // rows n and n + 8 share the 64-byte swizzle phase
@@ -544,11 +593,16 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
 #pragma unroll
         for (int ii = 0; ii < 4; ++ii) {
           // nibbles j = 0, 4 | 1, 5 (x16) in place; then 2, 6 | 3, 7 (x16) after a shift by 8
-          const uint2 q0 = qop(1, 2 * ii), q1 = qop(1, 2 * ii + 1);
-          mma_f16_16816(sa, xa[ii] & 0x000F000Fu, xb[ii] & 0x000F000Fu, xa[ii] & 0x00F000F0u, xb[ii] & 0x00F000F0u,
-                        q0.x, q0.y);
           const uint32_t ta = xa[ii] >> 8, tb = xb[ii] >> 8;
-          mma_f16_16816(sb, ta & 0x000F000Fu, tb & 0x000F000Fu, ta & 0x00F000F0u, tb & 0x00F000F0u, q1.x, q1.y);
+          const uint32_t a0 = xa[ii] & 0x000F000Fu, a1 = xb[ii] & 0x000F000Fu, a2 = xa[ii] & 0x00F000F0u,
+                         a3 = xb[ii] & 0x00F000F0u;
+          const uint32_t c0 = ta & 0x000F000Fu, c1 = tb & 0x000F000Fu, c2 = ta & 0x00F000F0u, c3 = tb & 0x00F000F0u;
+#pragma unroll
+          for (int g = 0; g < NG; ++g) {
+            const uint2 q0 = qop(1, 2 * ii, g), q1 = qop(1, 2 * ii + 1, g);
+            mma_f16_16816(sa[g], a0, a1, a2, a3, q0.x, q0.y);
+            mma_f16_16816(sb[g], c0, c1, c2, c3, q1.x, q1.y);
+          }
         }
       } else {
         const int sw = (n >> 2) & 1;  // rows n and n + 8 share the 32-byte swizzle phase
@@ -567,8 +621,11 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
             const uint32_t m1 = 0x00030003u << (2 * (j1 < 5 ? j1 : j1 - 5));
             const uint32_t a0 = (j0 < 5 ? za[wv] : ta) & m0, a1 = (j0 < 5 ? zb[wv] : tb) & m0;
             const uint32_t a2 = (j1 < 5 ? za[wv] : ta) & m1, a3 = (j1 < 5 ? zb[wv] : tb) & m1;
-            const uint2 q = qop(3, 4 * wv + k2);
-            mma_f16_16816((k2 & 1) ? sb : sa, a0, a1, a2, a3, q.x, q.y);
+#pragma unroll
+            for (int g = 0; g < NG; ++g) {
+              const uint2 q = qop(3, 4 * wv + k2, g);
+              mma_f16_16816((k2 & 1) ? sb[g] : sa[g], a0, a1, a2, a3, q.x, q.y);
+            }
           }
         }
       }
@@ -579,48 +636,60 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
     // most tiles skip the warp reduction and the rescale (weights stay <= 2^kLazy)
     const int ta_ = t0 + n, tb_ = ta_ + 8;
     const bool va_ = ta_ < tend, vb_ = tb_ < tend;
-    const float s00 = va_ && ta_ >= clo0 ? fmaf(sa[0] + sb[0], kmul0, -kb0) : -INFINITY;
-    const float s01 = va_ && ta_ >= clo1 ? fmaf(sa[1] + sb[1], kmul1, -kb1) : -INFINITY;
-    const float s10 = vb_ && tb_ >= clo0 ? fmaf(sa[2] + sb[2], kmul0, -kb0) : -INFINITY;
-    const float s11 = vb_ && tb_ >= clo1 ? fmaf(sa[3] + sb[3], kmul1, -kb1) : -INFINITY;
-    if (__any_sync(0xffffffffu, fmaxf(s00, s10) > m_run0 + kLazy || fmaxf(s01, s11) > m_run1 + kLazy)) {
-      float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+    // S scale per column: kbase, times 2^-e for fp16-q formats; codes subtract kbias * sum(q)
+    const bool kq16 = fk != OL_FMT_BF16 && fk != OL_FMT_F32;
+    float pw[NG][4];  // weights: (token n, column 2c), (n, 2c + 1), (n + 8, 2c), (n + 8, 2c + 1)
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-      }
-      const float mn0 = fmaxf(m_run0, mx0), mn1 = fmaxf(m_run1, mx1);
-      const float b0 = mn0 == -INFINITY ? 0.f : mn0, b1 = mn1 == -INFINITY ? 0.f : mn1;
-      const float al0 = fast_exp2(m_run0 - b0), al1 = fast_exp2(m_run1 - b1);
-      l_run0 *= al0;
-      l_run1 *= al1;
+    for (int g = 0; g < NG; ++g) {
+      const float kmul0 = kq16 ? kbase * pne0[g] : kbase, kmul1 = kq16 ? kbase * pne1[g] : kbase;
+      const float kb0 = kbias * qs0[g], kb1 = kbias * qs1[g];
+      const float s00 = va_ && ta_ >= clo0[g] ? fmaf(sa[g][0] + sb[g][0], kmul0, -kb0) : -INFINITY;
+      const float s01 = va_ && ta_ >= clo1[g] ? fmaf(sa[g][1] + sb[g][1], kmul1, -kb1) : -INFINITY;
+      const float s10 = vb_ && tb_ >= clo0[g] ? fmaf(sa[g][2] + sb[g][2], kmul0, -kb0) : -INFINITY;
+      const float s11 = vb_ && tb_ >= clo1[g] ? fmaf(sa[g][3] + sb[g][3], kmul1, -kb1) : -INFINITY;
+      if (__any_sync(0xffffffffu, fmaxf(s00, s10) > mr[g][0] + kLazy || fmaxf(s01, s11) > mr[g][1] + kLazy)) {
+        float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        o[mt][0] *= al0;
-        o[mt][1] *= al1;
-        o[mt][2] *= al0;
-        o[mt][3] *= al1;
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(mr[g][0], mx0), mn1 = fmaxf(mr[g][1], mx1);
+        const float b0 = mn0 == -INFINITY ? 0.f : mn0, b1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = fast_exp2(mr[g][0] - b0), al1 = fast_exp2(mr[g][1] - b1);
+        lr[g][0] *= al0;
+        lr[g][1] *= al1;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          o[g][mt][0] *= al0;
+          o[g][mt][1] *= al1;
+          o[g][mt][2] *= al0;
+          o[g][mt][3] *= al1;
+        }
+        if constexpr (DUP) {
+          zc0 *= al0;
+          zc1 *= al1;
+        }
+        mr[g][0] = mn0;
+        mr[g][1] = mn1;
       }
-      if constexpr (DUP) {
-        zc0 *= al0;
-        zc1 *= al1;
-      }
-      m_run0 = mn0;
-      m_run1 = mn1;
+      const float b0 = mr[g][0] == -INFINITY ? 0.f : mr[g][0], b1 = mr[g][1] == -INFINITY ? 0.f : mr[g][1];
+      pw[g][0] = fast_exp2(s00 - b0);
+      pw[g][1] = fast_exp2(s01 - b1);
+      pw[g][2] = fast_exp2(s10 - b0);
+      pw[g][3] = fast_exp2(s11 - b1);
+      lr[g][0] += pw[g][0] + pw[g][2];
+      lr[g][1] += pw[g][1] + pw[g][3];
     }
-    const float b0 = m_run0 == -INFINITY ? 0.f : m_run0, b1 = m_run1 == -INFINITY ? 0.f : m_run1;
-    const float p00 = fast_exp2(s00 - b0), p01 = fast_exp2(s01 - b1);
-    const float p10 = fast_exp2(s10 - b0), p11 = fast_exp2(s11 - b1);
-    l_run0 += p00 + p10;
-    l_run1 += p01 + p11;
     // O is held in units of 2^kv of the tile's V scale exponent (dense: 0)
     if (kv != ko) {
       const float f = pow2f(ko - kv);
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt)
+      for (int g = 0; g < NG; ++g)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) o[mt][j] *= f;
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) o[g][mt][j] *= f;
       if constexpr (DUP) {
         zc0 *= f;
         zc1 *= f;
@@ -631,16 +700,18 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
     // ---- O^T += V^T P^T (dimension order: m-tile 2bb + hh, row n -> 32bb + 4n + 2hh, row n + 8 -> + 1)
     const int TA = 2 * c, TB = 2 * c + 1, TC = 2 * c + 8, TD = 2 * c + 9;  // this lane's tokens (k rows)
     const bool half_p = fv != OL_FMT_BF16 && fv != OL_FMT_F32;  // P^T in fp16 (else bf16)
-    uint32_t ph0, ph1, pl0 = 0u, pl1 = 0u;
+    uint32_t ph0[NG], ph1[NG], pl0[NG], pl1[NG];  // per group: P^T hi and lo (DUP: hi | lo in ph)
     if constexpr (DUP) {
       // hi on the lanes of columns 0..3, lo = what hi leaves on those of 4..7
+      const float p00 = pw[0][0], p01 = pw[0][1], p10 = pw[0][2], p11 = pw[0][3];
+      pl0[0] = pl1[0] = 0u;
       if (half_p) {
         const float x0 = p00 * mv, x1 = p01 * mv, x2 = p10 * mv, x3 = p11 * mv;
         uint32_t h0 = pack_f16x2(x0, x1), h1 = pack_f16x2(x2, x3);
         const float2 f0 = __half22float2(*reinterpret_cast<__half2*>(&h0));
         const float2 f1 = __half22float2(*reinterpret_cast<__half2*>(&h1));
-        ph0 = movmatrix_trans(pack_f16x2(fmaf(-hsel, f0.x, x0), fmaf(-hsel, f0.y, x1)));
-        ph1 = movmatrix_trans(pack_f16x2(fmaf(-hsel, f1.x, x2), fmaf(-hsel, f1.y, x3)));
+        ph0[0] = movmatrix_trans(pack_f16x2(fmaf(-hsel, f0.x, x0), fmaf(-hsel, f0.y, x1)));
+        ph1[0] = movmatrix_trans(pack_f16x2(fmaf(-hsel, f1.x, x2), fmaf(-hsel, f1.y, x3)));
         if (fmt_affine(fv)) {  // the page's zero point, times the weights as they are
           const float z = (float)vz;
           zc0 = fmaf(z, x0 + x2, zc0);
@@ -648,24 +719,27 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
         }
       } else {
         const uint32_t h0 = pack_bf16x2(p00, p01), h1 = pack_bf16x2(p10, p11);
-        ph0 = movmatrix_trans(pack_bf16x2(fmaf(-hsel, __uint_as_float(h0 << 16), p00),
-                                          fmaf(-hsel, __uint_as_float(h0 & 0xffff0000u), p01)));
-        ph1 = movmatrix_trans(pack_bf16x2(fmaf(-hsel, __uint_as_float(h1 << 16), p10),
-                                          fmaf(-hsel, __uint_as_float(h1 & 0xffff0000u), p11)));
+        ph0[0] = movmatrix_trans(pack_bf16x2(fmaf(-hsel, __uint_as_float(h0 << 16), p00),
+                                             fmaf(-hsel, __uint_as_float(h0 & 0xffff0000u), p01)));
+        ph1[0] = movmatrix_trans(pack_bf16x2(fmaf(-hsel, __uint_as_float(h1 << 16), p10),
+                                             fmaf(-hsel, __uint_as_float(h1 & 0xffff0000u), p11)));
       }
     } else {
-      uint32_t h0, l0, h1, l1;
-      if (half_p) {
-        split_f16(p00 * mv, p01 * mv, h0, l0);
-        split_f16(p10 * mv, p11 * mv, h1, l1);
-      } else {
-        split_bf16(p00, p01, h0, l0);
-        split_bf16(p10, p11, h1, l1);
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        uint32_t h0, l0, h1, l1;
+        if (half_p) {
+          split_f16(pw[g][0] * mv, pw[g][1] * mv, h0, l0);
+          split_f16(pw[g][2] * mv, pw[g][3] * mv, h1, l1);
+        } else {
+          split_bf16(pw[g][0], pw[g][1], h0, l0);
+          split_bf16(pw[g][2], pw[g][3], h1, l1);
+        }
+        ph0[g] = movmatrix_trans(h0);
+        ph1[g] = movmatrix_trans(h1);
+        pl0[g] = movmatrix_trans(l0);
+        pl1[g] = movmatrix_trans(l1);
       }
-      ph0 = movmatrix_trans(h0);
-      ph1 = movmatrix_trans(h1);
-      pl0 = movmatrix_trans(l0);
-      pl1 = movmatrix_trans(l1);
     }
     if (fv == OL_FMT_F32) {
       // V from global memory; rows at or past the history end count as zero
@@ -690,9 +764,12 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
           split_bf16(xa1, xb1, a1h, a1l);
           split_bf16(xc0, xd0, a2h, a2l);
           split_bf16(xc1, xd1, a3h, a3l);
-          mma_bf16_16816(o[2 * bb + hh], a0h, a1h, a2h, a3h, ph0, ph1);
-          if (!DUP) mma_bf16_16816(o[2 * bb + hh], a0h, a1h, a2h, a3h, pl0, pl1);
-          mma_bf16_16816(o[2 * bb + hh], a0l, a1l, a2l, a3l, ph0, ph1);
+#pragma unroll
+          for (int g = 0; g < NG; ++g) {
+            mma_bf16_16816(o[g][2 * bb + hh], a0h, a1h, a2h, a3h, ph0[g], ph1[g]);
+            if (!DUP) mma_bf16_16816(o[g][2 * bb + hh], a0h, a1h, a2h, a3h, pl0[g], pl1[g]);
+            mma_bf16_16816(o[g][2 * bb + hh], a0l, a1l, a2l, a3l, ph0[g], ph1[g]);
+          }
         }
       }
     } else if (fv == OL_FMT_BF16 || fv == OL_FMT_F16) {
@@ -713,12 +790,15 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
           const uint32_t xc = hh ? wc.y : wc.x, xd = hh ? wd.y : wd.x;
           const uint32_t a0 = prmt(xa, xb, 0x5410u), a1 = prmt(xa, xb, 0x7632u);
           const uint32_t a2 = prmt(xc, xd, 0x5410u), a3 = prmt(xc, xd, 0x7632u);
-          if (h16) {
-            mma_f16_16816(o[2 * bb + hh], a0, a1, a2, a3, ph0, ph1);
-            if (!DUP) mma_f16_16816(o[2 * bb + hh], a0, a1, a2, a3, pl0, pl1);
-          } else {
-            mma_bf16_16816(o[2 * bb + hh], a0, a1, a2, a3, ph0, ph1);
-            if (!DUP) mma_bf16_16816(o[2 * bb + hh], a0, a1, a2, a3, pl0, pl1);
+#pragma unroll
+          for (int g = 0; g < NG; ++g) {
+            if (h16) {
+              mma_f16_16816(o[g][2 * bb + hh], a0, a1, a2, a3, ph0[g], ph1[g]);
+              if (!DUP) mma_f16_16816(o[g][2 * bb + hh], a0, a1, a2, a3, pl0[g], pl1[g]);
+            } else {
+              mma_bf16_16816(o[g][2 * bb + hh], a0, a1, a2, a3, ph0[g], ph1[g]);
+              if (!DUP) mma_bf16_16816(o[g][2 * bb + hh], a0, a1, a2, a3, pl0[g], pl1[g]);
+            }
           }
         }
       }
@@ -730,15 +810,18 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
       const uint32_t zpair = zf | (zf << 16);
       auto add_tile = [&](int mt, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
         if constexpr (DUP) {  // c' * 2^-24 as they are; the zero point is in zc
-          mma_f16_16816(o[mt], a0, a1, a2, a3, ph0, ph1);
+          mma_f16_16816(o[0][mt], a0, a1, a2, a3, ph0[0], ph1[0]);
           return;
         }
         a0 = hsub2_f16(a0, zpair);
         a1 = hsub2_f16(a1, zpair);
         a2 = hsub2_f16(a2, zpair);
         a3 = hsub2_f16(a3, zpair);
-        mma_f16_16816(o[mt], a0, a1, a2, a3, ph0, ph1);
-        mma_f16_16816(o[mt], a0, a1, a2, a3, pl0, pl1);
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          mma_f16_16816(o[g][mt], a0, a1, a2, a3, ph0[g], ph1[g]);
+          mma_f16_16816(o[g][mt], a0, a1, a2, a3, pl0[g], pl1[g]);
+        }
       };
       // the offset-binary flip of signed codes, and (not DUP) the fp16 1024 around them
       const uint32_t hi1024 = DUP ? 0u : 0x64006400u;
@@ -816,20 +899,22 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
     z1s = c < 2 ? z1s * 5.9604644775390625e-8f : 0.f;
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
-      o[mt][0] -= z0s;
-      o[mt][1] -= z1s;
-      o[mt][2] -= z0s;
-      o[mt][3] -= z1s;
+      o[0][mt][0] -= z0s;
+      o[0][mt][1] -= z1s;
+      o[0][mt][2] -= z0s;
+      o[0][mt][3] -= z1s;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) o[mt][j] += __shfl_xor_sync(0xffffffffu, o[mt][j], 2);
+      for (int j = 0; j < 4; ++j) o[0][mt][j] += __shfl_xor_sync(0xffffffffu, o[0][mt][j], 2);
     }
   }
   if (ko != 0) {
     const float f = pow2f(ko);
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt)
+    for (int g = 0; g < NG; ++g)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) o[mt][j] *= f;
+      for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[g][mt][j] *= f;
   }
 
   // ---- the current token, uncompressed from new_kv, in warp 0's state; the
@@ -839,48 +924,58 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
     const uint16_t* nv = reinterpret_cast<const uint16_t*>(p.new_kv) +
                          (((size_t)p.batch + w.b) * p.kv_heads + w.g) * 128;
     if (warp == 0 && CHUNK) {
-      // the chunk's tokens 0 .. zlast, uncompressed: token t is visible to
-      // column j (query token zj = z0 + j / G) if t <= zj and, with a window,
-      // t >= zj - window
+      // group g: the chunk's tokens 0 .. gzl[g], uncompressed: token t is
+      // visible to column j (query token zj = gz0[g] + j / G) if t <= zj and,
+      // with a window, t >= zj - window
       const size_t kv_row = ((size_t)w.b * p.kv_heads + w.g) * p.nq;
       const uint16_t* ck = reinterpret_cast<const uint16_t*>(p.new_kv) + kv_row * 128;
       const uint16_t* cv = reinterpret_cast<const uint16_t*>(p.new_kv) +
                            ((size_t)p.batch * p.kv_heads * p.nq + kv_row) * 128;
-      const int zc0 = z0 + (2 * c) / G, zc1 = z0 + (2 * c + 1) / G;
-      for (int t = 0; t <= zlast; ++t) {
-        const uint16_t* kt = ck + (size_t)t * 128;
-        const uint16_t* vt = cv + (size_t)t * 128;
-        float part = 0.f;
-        if (live) {
-#pragma unroll 8
-          for (int d = 32 * c; d < 32 * c + 32; ++d) part = fmaf(bf16_bits_to_float(qp[d]), bf16_bits_to_float(kt[d]), part);
-        }
-        part += __shfl_xor_sync(0xffffffffu, part, 1);
-        part += __shfl_xor_sync(0xffffffffu, part, 2);
-        const float sc0 = __shfl_sync(0xffffffffu, part, 8 * c) * sl2;
-        const float sc1 = __shfl_sync(0xffffffffu, part, 8 * c + 4) * sl2;
-        const bool v0 = 2 * c < ncols && t <= zc0 && (p.window_q < 0 || t >= zc0 - p.window_q);
-        const bool v1 = 2 * c + 1 < ncols && t <= zc1 && (p.window_q < 0 || t >= zc1 - p.window_q);
-        const float s0c = v0 ? sc0 : -INFINITY, s1c = v1 ? sc1 : -INFINITY;
-        const float mn0 = fmaxf(m_run0, s0c), mn1 = fmaxf(m_run1, s1c);
-        const float b0 = mn0 == -INFINITY ? 0.f : mn0, b1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float al0 = fast_exp2(m_run0 - b0), al1 = fast_exp2(m_run1 - b1);
-        const float pc0 = fast_exp2(s0c - b0), pc1 = fast_exp2(s1c - b1);
-        l_run0 = l_run0 * al0 + (n == 0 ? pc0 : 0.f);
-        l_run1 = l_run1 * al1 + (n == 0 ? pc1 : 0.f);
-        m_run0 = mn0;
-        m_run1 = mn1;
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          const int da = 32 * (mt >> 1) + 4 * n + 2 * (mt & 1);
-          const float va = bf16_bits_to_float(vt[da]), vb = bf16_bits_to_float(vt[da + 1]);
-          o[mt][0] = fmaf(pc0, va, o[mt][0] * al0);
-          o[mt][1] = fmaf(pc1, va, o[mt][1] * al1);
-          o[mt][2] = fmaf(pc0, vb, o[mt][2] * al0);
-          o[mt][3] = fmaf(pc1, vb, o[mt][3] * al1);
+      for (int g = 0; g < NG; ++g) {
+        if (g >= nsl) break;
+        bool live;
+        const uint16_t* qp = gq(g, live);
+        const int ncols = gcols(g);
+        const int zc0 = gz0[g] + (2 * c) / G, zc1 = gz0[g] + (2 * c + 1) / G;
+        for (int t = 0; t <= gzl[g]; ++t) {
+          const uint16_t* kt = ck + (size_t)t * 128;
+          const uint16_t* vt = cv + (size_t)t * 128;
+          float part = 0.f;
+          if (live) {
+#pragma unroll 8
+            for (int d = 32 * c; d < 32 * c + 32; ++d)
+              part = fmaf(bf16_bits_to_float(qp[d]), bf16_bits_to_float(kt[d]), part);
+          }
+          part += __shfl_xor_sync(0xffffffffu, part, 1);
+          part += __shfl_xor_sync(0xffffffffu, part, 2);
+          const float sc0 = __shfl_sync(0xffffffffu, part, 8 * c) * sl2;
+          const float sc1 = __shfl_sync(0xffffffffu, part, 8 * c + 4) * sl2;
+          const bool v0 = 2 * c < ncols && t <= zc0 && (p.window_q < 0 || t >= zc0 - p.window_q);
+          const bool v1 = 2 * c + 1 < ncols && t <= zc1 && (p.window_q < 0 || t >= zc1 - p.window_q);
+          const float s0c = v0 ? sc0 : -INFINITY, s1c = v1 ? sc1 : -INFINITY;
+          const float mn0 = fmaxf(mr[g][0], s0c), mn1 = fmaxf(mr[g][1], s1c);
+          const float b0 = mn0 == -INFINITY ? 0.f : mn0, b1 = mn1 == -INFINITY ? 0.f : mn1;
+          const float al0 = fast_exp2(mr[g][0] - b0), al1 = fast_exp2(mr[g][1] - b1);
+          const float pc0 = fast_exp2(s0c - b0), pc1 = fast_exp2(s1c - b1);
+          lr[g][0] = lr[g][0] * al0 + (n == 0 ? pc0 : 0.f);
+          lr[g][1] = lr[g][1] * al1 + (n == 0 ? pc1 : 0.f);
+          mr[g][0] = mn0;
+          mr[g][1] = mn1;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            const int da = 32 * (mt >> 1) + 4 * n + 2 * (mt & 1);
+            const float va = bf16_bits_to_float(vt[da]), vb = bf16_bits_to_float(vt[da + 1]);
+            o[g][mt][0] = fmaf(pc0, va, o[g][mt][0] * al0);
+            o[g][mt][1] = fmaf(pc1, va, o[g][mt][1] * al1);
+            o[g][mt][2] = fmaf(pc0, vb, o[g][mt][2] * al0);
+            o[g][mt][3] = fmaf(pc1, vb, o[g][mt][3] * al1);
+          }
         }
       }
     } else if (warp == 0) {
+      bool live;
+      const uint16_t* qp = gq(0, live);
       float part = 0.f;
       if (live) {
 #pragma unroll 8
@@ -892,23 +987,23 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
       const float sc0 = __shfl_sync(0xffffffffu, part, 8 * c) * sl2;
       const float sc1 = __shfl_sync(0xffffffffu, part, 8 * c + 4) * sl2;
       const float s0c = 2 * c < G ? sc0 : -INFINITY, s1c = 2 * c + 1 < G ? sc1 : -INFINITY;
-      const float mn0 = fmaxf(m_run0, s0c), mn1 = fmaxf(m_run1, s1c);
+      const float mn0 = fmaxf(mr[0][0], s0c), mn1 = fmaxf(mr[0][1], s1c);
       const float b0 = mn0 == -INFINITY ? 0.f : mn0, b1 = mn1 == -INFINITY ? 0.f : mn1;
-      const float al0 = fast_exp2(m_run0 - b0), al1 = fast_exp2(m_run1 - b1);
+      const float al0 = fast_exp2(mr[0][0] - b0), al1 = fast_exp2(mr[0][1] - b1);
       const float pc0 = fast_exp2(s0c - b0), pc1 = fast_exp2(s1c - b1);
       // l is summed over the 8 lanes of a column when the state is stored: add p once
-      l_run0 = l_run0 * al0 + (n == 0 ? pc0 : 0.f);
-      l_run1 = l_run1 * al1 + (n == 0 ? pc1 : 0.f);
-      m_run0 = mn0;
-      m_run1 = mn1;
+      lr[0][0] = lr[0][0] * al0 + (n == 0 ? pc0 : 0.f);
+      lr[0][1] = lr[0][1] * al1 + (n == 0 ? pc1 : 0.f);
+      mr[0][0] = mn0;
+      mr[0][1] = mn1;
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         const int da = 32 * (mt >> 1) + 4 * n + 2 * (mt & 1);
         const float va = bf16_bits_to_float(nv[da]), vb = bf16_bits_to_float(nv[da + 1]);
-        o[mt][0] = fmaf(pc0, va, o[mt][0] * al0);
-        o[mt][1] = fmaf(pc1, va, o[mt][1] * al1);
-        o[mt][2] = fmaf(pc0, vb, o[mt][2] * al0);
-        o[mt][3] = fmaf(pc1, vb, o[mt][3] * al1);
+        o[0][mt][0] = fmaf(pc0, va, o[0][mt][0] * al0);
+        o[0][mt][1] = fmaf(pc1, va, o[0][mt][1] * al1);
+        o[0][mt][2] = fmaf(pc0, vb, o[0][mt][2] * al0);
+        o[0][mt][3] = fmaf(pc1, vb, o[0][mt][3] * al1);
       }
     } else if (warp == 1 && p.append) {
       const int page = __ldg(p.block_table + (size_t)w.b * p.max_pages + cur / p.page_size);
@@ -935,11 +1030,18 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES>::kPerSm)
     }
   }
 
-  store_warp_state<true>(reinterpret_cast<float*>(my_stages), ms, warp, o, m_run0, m_run1, l_run0, l_run1);
   float* merged = reinterpret_cast<float*>(stages + kStage);  // warp 0's second stage
-  merge_and_finish(
-      p, w, NWARPS, [&](int st) { return reinterpret_cast<const float*>(stages + st * STAGES * kStage); }, merged,
-      nullptr, ms, CHUNK ? zs : -1);
+  // each column group (a chunked step: each slice) merged and finished on its own
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    if (g >= nsl) break;
+    if (g > 0) __syncthreads();  // the previous group's merge is done with the states and scratch
+    store_warp_state<true>(reinterpret_cast<float*>(my_stages), ms, warp, o[g], mr[g][0], mr[g][1], lr[g][0],
+                           lr[g][1]);
+    merge_and_finish(
+        p, w, NWARPS, [&](int st) { return reinterpret_cast<const float*>(stages + st * STAGES * kStage); }, merged,
+        nullptr, ms, CHUNK ? zs0 + g : -1);
+  }
 }
 
 // ------------------------------------------------------------------ host
@@ -978,13 +1080,16 @@ bool encode_width(CUtensorMap* map, void* base, uint64_t pool_bytes, int width) 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr int kWarps = 6, kStages = 2;
+// decode steps: 6 warps x 2 stages, two CTAs per SM; chunked steps (two
+// column groups, up to 255 registers): one CTA of kWarpsC warps per SM
+constexpr int kWarps = 6, kStages = 2, kWarpsC = 8, kStagesC = 2;
 
 template <bool CHUNK, bool DUP = false>
 cudaError_t ensure_attrs() {
-  static cudaError_t state = cudaFuncSetAttribute(fast_hpaged_kernel<kWarps, kStages, CHUNK, DUP>,
+  constexpr int W = CHUNK ? kWarpsC : kWarps, S = CHUNK ? kStagesC : kStages;
+  static cudaError_t state = cudaFuncSetAttribute(fast_hpaged_kernel<W, S, CHUNK, DUP>,
                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                  HpLayout<kWarps, kStages>::kTotal);
+                                                  HpLayout<W, S, CHUNK ? 2 : 1>::kTotal);
   return state;
 }
 
@@ -1000,7 +1105,9 @@ bool fast_hpaged_supported(const AttnParams& p) {
   return rows32 < (1ull << 31);
 }
 
-int fast_hpaged_ctas_per_sm() { return HpLayout<kWarps, kStages>::kPerSm; }
+int fast_hpaged_ctas_per_sm(bool chunk) {
+  return chunk ? HpLayout<kWarpsC, kStagesC, 2>::kPerSm : HpLayout<kWarps, kStages>::kPerSm;
+}
 
 cudaError_t launch_fast_hpaged(const AttnParams& p, cudaStream_t s) {
   if (p.total_ctas <= 0) return cudaSuccess;
@@ -1013,10 +1120,12 @@ cudaError_t launch_fast_hpaged(const AttnParams& p, cudaStream_t s) {
   cudaError_t e = chunk ? ensure_attrs<true>() : dup ? ensure_attrs<false, true>() : ensure_attrs<false>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  // a chunked step: slices of query tokens along x, the split plan's CTAs along y
-  cfg.gridDim = chunk ? dim3((p.nq + p.tq - 1) / p.tq, p.total_ctas, 1) : dim3(p.total_ctas, 1, 1);
-  cfg.blockDim = dim3(kWarps * 32, 1, 1);
-  cfg.dynamicSmemBytes = HpLayout<kWarps, kStages>::kTotal;
+  // a chunked step: pairs of slices of query tokens along x (a CTA carries two
+  // slices' columns), the split plan's CTAs along y
+  const int slices = (p.nq + p.tq - 1) / p.tq;
+  cfg.gridDim = chunk ? dim3((slices + 1) / 2, p.total_ctas, 1) : dim3(p.total_ctas, 1, 1);
+  cfg.blockDim = dim3((chunk ? kWarpsC : kWarps) * 32, 1, 1);
+  cfg.dynamicSmemBytes = chunk ? HpLayout<kWarpsC, kStagesC, 2>::kTotal : HpLayout<kWarps, kStages>::kTotal;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1024,7 +1133,8 @@ cudaError_t launch_fast_hpaged(const AttnParams& p, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (chunk)
-    return cudaLaunchKernelEx(&cfg, fast_hpaged_kernel<kWarps, kStages, true>, maps[0], maps[1], maps[2], maps[3], p);
+    return cudaLaunchKernelEx(&cfg, fast_hpaged_kernel<kWarpsC, kStagesC, true>, maps[0], maps[1], maps[2], maps[3],
+                              p);
   if (dup)  // the lo half of P^T in the free MMA columns
     return cudaLaunchKernelEx(&cfg, fast_hpaged_kernel<kWarps, kStages, false, true>, maps[0], maps[1], maps[2],
                               maps[3], p);

@@ -163,7 +163,7 @@ int fast_int4_ctas_per_sm(int variant, bool chunk);
 int fast_int4_max_cluster(int variant);
 cudaError_t launch_fast_int4(const AttnParams& p, cudaStream_t s);
 bool fast_hpaged_supported(const AttnParams& p);
-int fast_hpaged_ctas_per_sm();
+int fast_hpaged_ctas_per_sm(bool chunk);
 cudaError_t launch_fast_hpaged(const AttnParams& p, cudaStream_t s);
 
 // Visible range and split plan of one row, shared by the host planner and the
