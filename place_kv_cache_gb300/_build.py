@@ -17,7 +17,7 @@ OBJ_PHASE = os.path.join(HERE, "_objs_phase")
 LIB_PHASE = os.path.join(HERE, "libol_phase.so")
 SOURCES = ["ol_api.cpp", "ol_append.cu", "ol_generic.cu", "ol_fast_bf16.cu", "ol_fast_int4.cu", "ol_noalloc.cu",
            "ol_hpaged.cu", "ol_fast_hpaged.cu"]
-HEADERS = ["ol_internal.h", "ol_common.cuh", "ol_merge.cuh", "ol_fast_bf16_kernel.inc", "ol_hpaged.cuh",
+HEADERS = ["ol_internal.h", "ol_launch.h", "ol_common.cuh", "ol_merge.cuh", "ol_fast_bf16_kernel.inc", "ol_hpaged.cuh",
            os.path.join("..", "..", "include", "ol.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

@@ -15,6 +15,7 @@
 #include <vector>
 
 #include "ol_internal.h"
+#include "ol_launch.h"
 
 namespace ol {
 namespace {

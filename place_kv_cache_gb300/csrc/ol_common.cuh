@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include "ol_internal.h"
+#include "ol_launch.h"
 
 namespace ol {
 
