@@ -571,12 +571,13 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES, CHUNK ? 
           ya[4 * m] = va.x; ya[4 * m + 1] = va.y; ya[4 * m + 2] = va.z; ya[4 * m + 3] = va.w;
           yb[4 * m] = vb.x; yb[4 * m + 1] = vb.y; yb[4 * m + 2] = vb.z; yb[4 * m + 3] = vb.w;
         }
-        const uint32_t flip = sgn ? 0x80808080u : 0u;
+        // the offset-binary flip of signed codes inside the mask: (x ^ f) & m = (x & m) ^ (f & m)
+        const uint32_t fm = sgn ? 0x00800080u : 0u;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t x = ya[kk] ^ flip, y = yb[kk] ^ flip;
-          const uint32_t a0 = x & 0x00FF00FFu, a1 = y & 0x00FF00FFu, a2 = (x >> 8) & 0x00FF00FFu,
-                         a3 = (y >> 8) & 0x00FF00FFu;
+          const uint32_t x = ya[kk], y = yb[kk];
+          const uint32_t a0 = and_xor(x, 0x00FF00FFu, fm), a1 = and_xor(y, 0x00FF00FFu, fm);
+          const uint32_t a2 = and_xor(x >> 8, 0x00FF00FFu, fm), a3 = and_xor(y >> 8, 0x00FF00FFu, fm);
 #pragma unroll
           for (int g = 0; g < NG; ++g) {
             const uint2 q = qop(2, kk, g);
@@ -587,16 +588,17 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES, CHUNK ? 
         const int sw = (n >> 1) & 3;  // rows n and n + 8 share the 64-byte swizzle phase
         const uint4 va = lds_v4(sK + n * 64 + ((c ^ sw) << 4));
         const uint4 vb = lds_v4(sK + (n + 8) * 64 + ((c ^ sw) << 4));
-        const uint32_t flip = sgn ? 0x88888888u : 0u;
-        const uint32_t xa[4] = {va.x ^ flip, va.y ^ flip, va.z ^ flip, va.w ^ flip};
-        const uint32_t xb[4] = {vb.x ^ flip, vb.y ^ flip, vb.z ^ flip, vb.w ^ flip};
+        // the flip of signed codes inside the masks, as for 8 bits
+        const uint32_t fl = sgn ? 0x00080008u : 0u, fh = sgn ? 0x00800080u : 0u;
+        const uint32_t xa[4] = {va.x, va.y, va.z, va.w}, xb[4] = {vb.x, vb.y, vb.z, vb.w};
 #pragma unroll
         for (int ii = 0; ii < 4; ++ii) {
           // nibbles j = 0, 4 | 1, 5 (x16) in place; then 2, 6 | 3, 7 (x16) after a shift by 8
           const uint32_t ta = xa[ii] >> 8, tb = xb[ii] >> 8;
-          const uint32_t a0 = xa[ii] & 0x000F000Fu, a1 = xb[ii] & 0x000F000Fu, a2 = xa[ii] & 0x00F000F0u,
-                         a3 = xb[ii] & 0x00F000F0u;
-          const uint32_t c0 = ta & 0x000F000Fu, c1 = tb & 0x000F000Fu, c2 = ta & 0x00F000F0u, c3 = tb & 0x00F000F0u;
+          const uint32_t a0 = and_xor(xa[ii], 0x000F000Fu, fl), a1 = and_xor(xb[ii], 0x000F000Fu, fl);
+          const uint32_t a2 = and_xor(xa[ii], 0x00F000F0u, fh), a3 = and_xor(xb[ii], 0x00F000F0u, fh);
+          const uint32_t c0 = and_xor(ta, 0x000F000Fu, fl), c1 = and_xor(tb, 0x000F000Fu, fl);
+          const uint32_t c2 = and_xor(ta, 0x00F000F0u, fh), c3 = and_xor(tb, 0x00F000F0u, fh);
 #pragma unroll
           for (int g = 0; g < NG; ++g) {
             const uint2 q0 = qop(1, 2 * ii, g), q1 = qop(1, 2 * ii + 1, g);
@@ -608,8 +610,10 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES, CHUNK ? 
         const int sw = (n >> 2) & 1;  // rows n and n + 8 share the 32-byte swizzle phase
         const uint2 va = lds_v2(sK + n * 32 + (((c >> 1) ^ sw) << 4) + 8 * (c & 1));
         const uint2 vb = lds_v2(sK + (n + 8) * 32 + (((c >> 1) ^ sw) << 4) + 8 * (c & 1));
+        // the flip of signed codes inside the masks, as for 8 bits (0xAA.. >> 10 keeps its
+        // pattern on the masked bits)
         const uint32_t flip = sgn ? 0xAAAAAAAAu : 0u;
-        const uint32_t za[2] = {va.x ^ flip, va.y ^ flip}, zb[2] = {vb.x ^ flip, vb.y ^ flip};
+        const uint32_t za[2] = {va.x, va.y}, zb[2] = {vb.x, vb.y};
 #pragma unroll
         for (int wv = 0; wv < 2; ++wv) {
           // code pairs (j, j + 8) of the word: j < 5 masked in place (bit 2j), j >= 5 after a shift by 10
@@ -619,8 +623,10 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES, CHUNK ? 
             const int j0 = 2 * k2, j1 = j0 + 1;
             const uint32_t m0 = 0x00030003u << (2 * (j0 < 5 ? j0 : j0 - 5));
             const uint32_t m1 = 0x00030003u << (2 * (j1 < 5 ? j1 : j1 - 5));
-            const uint32_t a0 = (j0 < 5 ? za[wv] : ta) & m0, a1 = (j0 < 5 ? zb[wv] : tb) & m0;
-            const uint32_t a2 = (j1 < 5 ? za[wv] : ta) & m1, a3 = (j1 < 5 ? zb[wv] : tb) & m1;
+            const uint32_t a0 = and_xor(j0 < 5 ? za[wv] : ta, m0, flip & m0);
+            const uint32_t a1 = and_xor(j0 < 5 ? zb[wv] : tb, m0, flip & m0);
+            const uint32_t a2 = and_xor(j1 < 5 ? za[wv] : ta, m1, flip & m1);
+            const uint32_t a3 = and_xor(j1 < 5 ? zb[wv] : tb, m1, flip & m1);
 #pragma unroll
             for (int g = 0; g < NG; ++g) {
               const uint2 q = qop(3, 4 * wv + k2, g);
