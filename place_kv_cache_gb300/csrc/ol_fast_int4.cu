@@ -82,6 +82,8 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 __device__ __forceinline__ float2 half2_bits_to_float2(uint32_t x) {
   return __half22float2(*reinterpret_cast<__half2*>(&x));
 }
+// packed pairs of fp32 (one instruction for two lanes' columns 2c, 2c + 1)
+__device__ __forceinline__ float2 bc2(float x) { return make_float2(x, x); }
 // byte offset of logical byte x of 64-byte row r in a SWIZZLE_64B tile
 __device__ __forceinline__ int swz64(int r, int x) {
   return r * 64 + ((((x >> 4) ^ (r >> 1)) & 3) << 4) + (x & 15);
@@ -384,14 +386,18 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES, CHUNK 
 #pragma unroll
     for (int g = 0; g < NG; ++g) {
       const float(&sc)[4][4] = sacc[g];
-      float s00 = ka01.x * sc[0][0] + ka01.y * sc[1][0] + ka23.x * sc[2][0] + ka23.y * sc[3][0];
-      float s01 = ka01.x * sc[0][1] + ka01.y * sc[1][1] + ka23.x * sc[2][1] + ka23.y * sc[3][1];
-      float s10 = kb01.x * sc[0][2] + kb01.y * sc[1][2] + kb23.x * sc[2][2] + kb23.y * sc[3][2];
-      float s11 = kb01.x * sc[0][3] + kb01.y * sc[1][3] + kb23.x * sc[2][3] + kb23.y * sc[3][3];
-      s00 *= sfac;
-      s01 *= sfac;
-      s10 *= sfac;
-      s11 *= sfac;
+      // columns (2c, 2c + 1) of tokens n and n + 8 as pairs
+      float2 sa2 = __fmul2_rn(bc2(ka01.x), make_float2(sc[0][0], sc[0][1]));
+      float2 sb2 = __fmul2_rn(bc2(kb01.x), make_float2(sc[0][2], sc[0][3]));
+      sa2 = __ffma2_rn(bc2(ka01.y), make_float2(sc[1][0], sc[1][1]), sa2);
+      sb2 = __ffma2_rn(bc2(kb01.y), make_float2(sc[1][2], sc[1][3]), sb2);
+      sa2 = __ffma2_rn(bc2(ka23.x), make_float2(sc[2][0], sc[2][1]), sa2);
+      sb2 = __ffma2_rn(bc2(kb23.x), make_float2(sc[2][2], sc[2][3]), sb2);
+      sa2 = __ffma2_rn(bc2(ka23.y), make_float2(sc[3][0], sc[3][1]), sa2);
+      sb2 = __ffma2_rn(bc2(kb23.y), make_float2(sc[3][2], sc[3][3]), sb2);
+      sa2 = __fmul2_rn(sa2, bc2(sfac));
+      sb2 = __fmul2_rn(sb2, bc2(sfac));
+      float s00 = sa2.x, s01 = sa2.y, s10 = sb2.x, s11 = sb2.y;
       if (!FULL) {
         if (CHUNK) {  // each column from its own window start
           s00 = va && t0 + n >= clo[g][0] ? s00 : -INFINITY;
@@ -500,7 +506,11 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES, CHUNK 
 #pragma unroll
     for (int g = 0; g < NG; ++g)
 #pragma unroll
-      for (int k = 0; k < 4; ++k) pa[g][k] = pw[g][k] * pe;
+      for (int k = 0; k < 4; k += 2) {
+        const float2 x = __fmul2_rn(make_float2(pw[g][k], pw[g][k + 1]), bc2(pe));
+        pa[g][k] = x.x;
+        pa[g][k + 1] = x.y;
+      }
     const float2 va01 = half2_bits_to_float2(sa0), va23 = half2_bits_to_float2(sa1);
     const float2 vb01 = half2_bits_to_float2(sb0), vb23 = half2_bits_to_float2(sb1);
     uint32_t vw[4][2];  // [block][tokens (2c, 2c+1), (2c+8, 2c+9)]
@@ -514,17 +524,23 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES, CHUNK 
       for (int b = 0; b < 4; ++b) {
         const float sca = b == 0 ? va01.x : b == 1 ? va01.y : b == 2 ? va23.x : va23.y;
         const float scb = b == 0 ? vb01.x : b == 1 ? vb01.y : b == 2 ? vb23.x : vb23.y;
-        const float q00 = pa[0][0] * sca, q01 = pa[0][1] * sca, q10 = pa[0][2] * scb, q11 = pa[0][3] * scb;
+        // P^T times the V scale, columns (2c, 2c + 1) of tokens n and n + 8 as pairs
+        const float2 qa = __fmul2_rn(make_float2(pa[0][0], pa[0][1]), bc2(sca));
+        const float2 qb = __fmul2_rn(make_float2(pa[0][2], pa[0][3]), bc2(scb));
         // hi on the lanes of columns 0..3, lo = what hi leaves on those of 4..7
-        const float2 f0 = half2_bits_to_float2(pack_f16x2(q00, q01));
-        const float2 f1 = half2_bits_to_float2(pack_f16x2(q10, q11));
-        const uint32_t pb0 = movmatrix_trans(pack_f16x2(fmaf(-hsel, f0.x, q00), fmaf(-hsel, f0.y, q01)));
-        const uint32_t pb1 = movmatrix_trans(pack_f16x2(fmaf(-hsel, f1.x, q10), fmaf(-hsel, f1.y, q11)));
-        // zp * 16^b as an exact fp32 integer (the nibble in place, 2^23 bias off)
-        const float za = __uint_as_float(0x4B000000u | (zn & (0xFu << (4 * b)))) - 8388608.f;
-        const float zb = __uint_as_float(0x4B000000u | (zn8 & (0xFu << (4 * b)))) - 8388608.f;
-        zc[b][0] = fmaf(q00, za, fmaf(q10, zb, zc[b][0]));
-        zc[b][1] = fmaf(q01, za, fmaf(q11, zb, zc[b][1]));
+        const float2 f0 = half2_bits_to_float2(pack_f16x2(qa.x, qa.y));
+        const float2 f1 = half2_bits_to_float2(pack_f16x2(qb.x, qb.y));
+        const float2 y0 = __ffma2_rn(bc2(-hsel), f0, qa), y1 = __ffma2_rn(bc2(-hsel), f1, qb);
+        const uint32_t pb0 = movmatrix_trans(pack_f16x2(y0.x, y0.y));
+        const uint32_t pb1 = movmatrix_trans(pack_f16x2(y1.x, y1.y));
+        // zp * 16^b of tokens n and n + 8 as exact fp32 integers (the nibble in place, 2^23 bias off)
+        const float2 zz = __fadd2_rn(make_float2(__uint_as_float(0x4B000000u | (zn & (0xFu << (4 * b)))),
+                                                 __uint_as_float(0x4B000000u | (zn8 & (0xFu << (4 * b))))),
+                                     bc2(-8388608.f));
+        float2 z2 = __ffma2_rn(qb, bc2(zz.y), make_float2(zc[b][0], zc[b][1]));
+        z2 = __ffma2_rn(qa, bc2(zz.x), z2);
+        zc[b][0] = z2.x;
+        zc[b][1] = z2.y;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const uint32_t w01 = vw[b][0] >> (8 * h), w89 = vw[b][1] >> (8 * h);
