@@ -111,10 +111,18 @@ __device__ __forceinline__ void split_bf16(float x, float y, uint32_t& hi, uint3
   hi = pack_bf16x2(x, y);
   lo = pack_bf16x2(x - __uint_as_float(hi << 16), y - __uint_as_float(hi & 0xffff0000u));
 }
-__device__ __forceinline__ void split_f16(float x, float y, uint32_t& hi, uint32_t& lo) {
-  hi = pack_f16x2(x, y);
-  const float2 h = __half22float2(*reinterpret_cast<__half2*>(&hi));
-  lo = pack_f16x2(x - h.x, y - h.y);
+__device__ __forceinline__ float2 bc2(float x) { return make_float2(x, x); }
+// the same for a packed pair (the remainders by one paired fma: v - hi)
+__device__ __forceinline__ void split_bf16(float2 v, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16x2(v.x, v.y);
+  const float2 r =
+      __ffma2_rn(make_float2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u)), bc2(-1.f), v);
+  lo = pack_bf16x2(r.x, r.y);
+}
+__device__ __forceinline__ void split_f16(float2 v, uint32_t& hi, uint32_t& lo) {
+  hi = pack_f16x2(v.x, v.y);
+  const float2 r = __ffma2_rn(__half22float2(*reinterpret_cast<__half2*>(&hi)), bc2(-1.f), v);
+  lo = pack_f16x2(r.x, r.y);
 }
 
 // 2^k as a float: the exponent field directly where it is in range
@@ -647,12 +655,26 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES, CHUNK ? 
     float pw[NG][4];  // weights: (token n, column 2c), (n, 2c + 1), (n + 8, 2c), (n + 8, 2c + 1)
 #pragma unroll
     for (int g = 0; g < NG; ++g) {
-      const float kmul0 = kq16 ? kbase * pne0[g] : kbase, kmul1 = kq16 ? kbase * pne1[g] : kbase;
-      const float kb0 = kbias * qs0[g], kb1 = kbias * qs1[g];
-      const float s00 = va_ && ta_ >= clo0[g] ? fmaf(sa[g][0] + sb[g][0], kmul0, -kb0) : -INFINITY;
-      const float s01 = va_ && ta_ >= clo1[g] ? fmaf(sa[g][1] + sb[g][1], kmul1, -kb1) : -INFINITY;
-      const float s10 = vb_ && tb_ >= clo0[g] ? fmaf(sa[g][2] + sb[g][2], kmul0, -kb0) : -INFINITY;
-      const float s11 = vb_ && tb_ >= clo1[g] ? fmaf(sa[g][3] + sb[g][3], kmul1, -kb1) : -INFINITY;
+      float s00, s01, s10, s11;
+      if constexpr (CHUNK) {  // columns (2c, 2c + 1) as packed pairs (measured: faster for chunks only)
+        const float2 km = kq16 ? __fmul2_rn(bc2(kbase), make_float2(pne0[g], pne1[g])) : bc2(kbase);
+        const float2 kbn = __fmul2_rn(bc2(-kbias), make_float2(qs0[g], qs1[g]));
+        const float2 ra =
+            __ffma2_rn(__fadd2_rn(make_float2(sa[g][0], sa[g][1]), make_float2(sb[g][0], sb[g][1])), km, kbn);
+        const float2 rb =
+            __ffma2_rn(__fadd2_rn(make_float2(sa[g][2], sa[g][3]), make_float2(sb[g][2], sb[g][3])), km, kbn);
+        s00 = va_ && ta_ >= clo0[g] ? ra.x : -INFINITY;
+        s01 = va_ && ta_ >= clo1[g] ? ra.y : -INFINITY;
+        s10 = vb_ && tb_ >= clo0[g] ? rb.x : -INFINITY;
+        s11 = vb_ && tb_ >= clo1[g] ? rb.y : -INFINITY;
+      } else {
+        const float kmul0 = kq16 ? kbase * pne0[g] : kbase, kmul1 = kq16 ? kbase * pne1[g] : kbase;
+        const float kb0 = kbias * qs0[g], kb1 = kbias * qs1[g];
+        s00 = va_ && ta_ >= clo0[g] ? fmaf(sa[g][0] + sb[g][0], kmul0, -kb0) : -INFINITY;
+        s01 = va_ && ta_ >= clo1[g] ? fmaf(sa[g][1] + sb[g][1], kmul1, -kb1) : -INFINITY;
+        s10 = vb_ && tb_ >= clo0[g] ? fmaf(sa[g][2] + sb[g][2], kmul0, -kb0) : -INFINITY;
+        s11 = vb_ && tb_ >= clo1[g] ? fmaf(sa[g][3] + sb[g][3], kmul1, -kb1) : -INFINITY;
+      }
       if (__any_sync(0xffffffffu, fmaxf(s00, s10) > mr[g][0] + kLazy || fmaxf(s01, s11) > mr[g][1] + kLazy)) {
         float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
 #pragma unroll
@@ -735,11 +757,11 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES, CHUNK ? 
       for (int g = 0; g < NG; ++g) {
         uint32_t h0, l0, h1, l1;
         if (half_p) {
-          split_f16(pw[g][0] * mv, pw[g][1] * mv, h0, l0);
-          split_f16(pw[g][2] * mv, pw[g][3] * mv, h1, l1);
+          split_f16(__fmul2_rn(make_float2(pw[g][0], pw[g][1]), bc2(mv)), h0, l0);
+          split_f16(__fmul2_rn(make_float2(pw[g][2], pw[g][3]), bc2(mv)), h1, l1);
         } else {
-          split_bf16(pw[g][0], pw[g][1], h0, l0);
-          split_bf16(pw[g][2], pw[g][3], h1, l1);
+          split_bf16(make_float2(pw[g][0], pw[g][1]), h0, l0);
+          split_bf16(make_float2(pw[g][2], pw[g][3]), h1, l1);
         }
         ph0[g] = movmatrix_trans(h0);
         ph1[g] = movmatrix_trans(h1);
