@@ -559,13 +559,16 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES, CHUNK 
       uint32_t ph0[NG], ph1[NG], pl0[NG], pl1[NG];
 #pragma unroll
       for (int g = 0; g < NG; ++g) {
-        const float q00 = pa[g][0] * sca, q01 = pa[g][1] * sca, q10 = pa[g][2] * scb, q11 = pa[g][3] * scb;
-        const uint32_t h0 = pack_f16x2(q00, q01), h1 = pack_f16x2(q10, q11);
-        const float2 f0 = half2_bits_to_float2(h0), f1 = half2_bits_to_float2(h1);
+        // columns (2c, 2c + 1) of tokens n and n + 8 as packed pairs
+        const float2 qa = __fmul2_rn(make_float2(pa[g][0], pa[g][1]), bc2(sca));
+        const float2 qb = __fmul2_rn(make_float2(pa[g][2], pa[g][3]), bc2(scb));
+        const uint32_t h0 = pack_f16x2(qa.x, qa.y), h1 = pack_f16x2(qb.x, qb.y);
+        const float2 r0 = __ffma2_rn(half2_bits_to_float2(h0), bc2(-1.f), qa);  // what hi leaves
+        const float2 r1 = __ffma2_rn(half2_bits_to_float2(h1), bc2(-1.f), qb);
         ph0[g] = movmatrix_trans(h0);
         ph1[g] = movmatrix_trans(h1);
-        pl0[g] = movmatrix_trans(pack_f16x2(q00 - f0.x, q01 - f0.y));
-        pl1[g] = movmatrix_trans(pack_f16x2(q10 - f1.x, q11 - f1.y));
+        pl0[g] = movmatrix_trans(pack_f16x2(r0.x, r0.y));
+        pl1[g] = movmatrix_trans(pack_f16x2(r1.x, r1.y));
       }
       // zp as fp16 subnormals in the A layout: rows n (x1) and n + 8 (x16)
       const uint32_t t01 = zv01 >> (4 * b), t89 = zv89 >> (4 * b);
