@@ -139,7 +139,7 @@ void plan_fast(AttnParams& p, const int32_t* lens_host, int sms, int force_varia
   const bool int4 = p.layout == OL_LAYOUT_INT4;
   // measured defaults: 8 warps x 2 stages for contiguous caches and small
   // batches, 4 warps x 2 stages (three CTAs per SM) for paged pools; INT4:
-  // 6 warps x 4 stages (chunked steps 8)
+  // 6 warps x 6 stages (chunked steps 8 x 4)
   if (force_variant >= 0)
     p.variant = force_variant;
   else if (tune().cfg >= 0)

@@ -921,25 +921,26 @@ int fast_int4_smem(int variant) {
   switch (variant) {
     case 1: return Int4Layout<4, 4>::kTotal;
     case 2: return Int4Layout<8, 2>::kTotal;
-    default: return Int4Layout<6, 4>::kTotal;
+    default: return Int4Layout<6, 6>::kTotal;
   }
 }
-// variant 0 (the default): decode steps 6 warps x 4 stages, two CTAs per SM at
-// up to 168 registers (int4_b16 89.3 us/step against 91.6 with 8 warps at 128);
-// chunked steps keep 8 warps (two column groups, one CTA per SM)
+// variant 0 (the default): decode steps 6 warps x 6 stages, two CTAs per SM at
+// up to 168 registers (int4_b16 88.2 us/step; 4 stages 89.2, 8 warps x 4 at
+// 128 registers 91.6); chunked steps keep 8 warps x 4 stages (two column
+// groups, one CTA per SM)
 int fast_int4_warps(int variant) { return variant == 1 ? 4 : variant == 0 ? 6 : 8; }
 int fast_int4_ctas_per_sm(int variant, bool chunk) {
   switch (variant) {
     case 1: return chunk ? Int4Layout<4, 4, 2>::kPerSm : Int4Layout<4, 4>::kPerSm;
     case 2: return chunk ? Int4Layout<8, 2, 2>::kPerSm : Int4Layout<8, 2>::kPerSm;
-    default: return chunk ? Int4Layout<8, 4, 2>::kPerSm : Int4Layout<6, 4>::kPerSm;
+    default: return chunk ? Int4Layout<8, 4, 2>::kPerSm : Int4Layout<6, 6>::kPerSm;
   }
 }
 int fast_int4_max_cluster(int variant) {
   switch (variant) {
     case 1: return max_cluster<4, 4>();
     case 2: return max_cluster<8, 2>();
-    default: return max_cluster<6, 4>();
+    default: return max_cluster<6, 6>();
   }
 }
 
@@ -956,13 +957,13 @@ cudaError_t launch_fast_int4(const AttnParams& p, cudaStream_t s) {
     switch (p.variant) {
       case 1: return launch_cfg<4, 4, false, true>(p, s);
       case 2: return launch_cfg<8, 2, false, true>(p, s);
-      default: return launch_cfg<6, 4, false, true>(p, s);
+      default: return launch_cfg<6, 6, false, true>(p, s);
     }
   }
   switch (p.variant) {
     case 1: return launch_cfg<4, 4, false>(p, s);
     case 2: return launch_cfg<8, 2, false>(p, s);
-    default: return launch_cfg<6, 4, false>(p, s);
+    default: return launch_cfg<6, 6, false>(p, s);
   }
 }
 
