@@ -113,7 +113,9 @@ def test_append_sequence_matches_oracle(shape):
 
 
 GQA = [  # B, H, S, D, Hq
-    (1, 2, 16, 128, 8), (2, 2, 16, 128, 14), (3, 1, 8, 64, 16), (2, 2, 4, 4, 4), (1, 2, 16, 256, 32)]
+    (1, 2, 16, 128, 8), (2, 2, 16, 128, 14), (3, 1, 8, 64, 16), (2, 2, 4, 4, 4), (1, 2, 16, 256, 32),
+    # tensor-core kernel: groups 1-3 (duplicated columns with dead ones), 5 and 8 (P^T hi and lo apart)
+    (1, 4, 16, 128, 4), (1, 2, 16, 128, 4), (2, 2, 16, 128, 6), (1, 2, 16, 128, 10), (1, 1, 16, 128, 8)]
 
 
 @pytest.mark.parametrize("shape", GQA, ids=[f"b{s[0]}h{s[1]}s{s[2]}d{s[3]}g{s[4] // s[1]}" for s in GQA])

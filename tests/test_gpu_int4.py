@@ -50,6 +50,7 @@ def desc_of(dplanes, w, mode, access=ol.OL_READ_WRITE):  # noqa: D401
     ("b3_gqa4", 3, 32, 8, 128, 300, [1, 17, 300]),
     ("b2_gqa7", 2, 28, 4, 128, 160, [160, 64]),
     ("b2_gqa5", 2, 10, 2, 128, 150, [150, 20]),
+    ("b2_gqa3", 2, 12, 4, 128, 180, [180, 40]),
     ("b2_gqa2", 2, 8, 4, 128, 200, [200, 33]),
     ("b2_gqa1", 2, 4, 4, 128, 130, [130, 5]),
     ("b2_d64", 2, 8, 2, 64, 96, [96, 33]),
