@@ -107,6 +107,8 @@ __device__ __forceinline__ int tile_row(const AttnParams& p, bool paged, int pla
 }
 
 #define OL_CHUNK 0
+constexpr float kLazy = 8.f;  // log2 headroom of the lazy softmax maximum
+
 #define OL_FAST_KERNEL fast_bf16_kernel
 #include "ol_fast_bf16_kernel.inc"
 #undef OL_FAST_KERNEL
