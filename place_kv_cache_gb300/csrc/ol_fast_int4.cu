@@ -279,7 +279,9 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES, CHUNK 
         qs += __shfl_xor_sync(0xffffffffu, qs, 1);
         qs += __shfl_xor_sync(0xffffffffu, qs, 2);
         const float qhi = __half2float(__float2half_rn(qs));
-        qz[g][b] = c == 0 ? pack_f16x2(-qhi, -(qs - qhi)) : 0u;
+        // blocks 1 and 3 meet their zero point in bits 4..7 (16 zp): Q / 16
+        const float zf = (b & 1) ? 0.0625f : 1.f;
+        qz[g][b] = c == 0 ? pack_f16x2(-qhi * zf, -(qs - qhi) * zf) : 0u;
       }
   }
   // The code words come from ldmatrix: the 16 bytes of block b in a token's
@@ -364,13 +366,16 @@ __global__ void __launch_bounds__(NWARPS * 32, Int4Layout<NWARPS, STAGES, CHUNK 
     ldsm_x4(sg + kaddr[0], kw[0][0], kw[0][1], kw[1][0], kw[1][1]);
     ldsm_x4(sg + kaddr[1], kw[2][0], kw[2][1], kw[3][0], kw[3][1]);
     float sacc[NG][4][4];
+    // zero points of blocks 0 / 1 in bits 0..3 / 4..7 of each half, blocks 2 / 3 one byte up
+    const uint32_t zda8 = zda >> 8, zdb8 = zdb >> 8;
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       const uint32_t wa = kw[b][0], wb = kw[b][1];
       const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
       const uint32_t a0 = wa & kLoNib, a1 = wb & kLoNib, a2 = wa & kHiNib, a3 = wb & kHiNib;
       const uint32_t c0 = wa8 & kLoNib, c1 = wb8 & kLoNib, c2 = wa8 & kHiNib, c3 = wb8 & kHiNib;
-      const uint32_t za = (zda >> (4 * b)) & kLoNib, zb = (zdb >> (4 * b)) & kLoNib;
+      const uint32_t zm = (b & 1) ? kHiNib : kLoNib;  // block b's nibble in place (x16 for odd b)
+      const uint32_t za = (b < 2 ? zda : zda8) & zm, zb = (b < 2 ? zdb : zdb8) & zm;
 #pragma unroll
       for (int g = 0; g < NG; ++g) {
         sacc[g][b][0] = sacc[g][b][1] = sacc[g][b][2] = sacc[g][b][3] = 0.f;
