@@ -100,10 +100,11 @@ def kernel_sources_sha(layout: str) -> str:
 
 def recorded_traffic(w):
     """DRAM bytes (read + write) per launch of the workload's kernel from one ncu
-    capture, as listed in profiles/dram_traffic.txt; None when none was recorded
-    or it was recorded on other kernel sources."""
+    capture, as listed in profiles/dram_traffic.txt; None when none was recorded,
+    it was recorded on other kernel sources, or the workload is a reduced copy
+    (--rows) of the recorded one."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-    if not os.path.exists(path):
+    if not os.path.exists(path) or WORKLOADS.get(w.name) != w:
         return None
     sha = kernel_sources_sha(w.layout)
     with open(path) as f:

@@ -71,3 +71,15 @@ def test_compact_carries_the_per_config_fields():
     assert c["spread_us"] == [1.9, 2.0, 2.1] and c["frac"] == 0.5 and c["traffic"] == 10
     assert c["clocks"] == [2070.0, []] and c["e2e_us_per_step"] == 2.5
     assert c["cpu_baseline"] == {"value": 0.1, "cores": 16, "us_per_step": 9.0, "one_core_us": 90.0}
+
+
+def test_recorded_traffic_only_for_the_recorded_workload_and_sources():
+    """A traffic figure belongs to one full-size workload on one version of its
+    kernel sources: every line of the record resolves on the current sources,
+    and a reduced copy of the same workload (--rows) gets none."""
+    for name in ("qwen_b1_gqa7", "paged_b64", "int4_b16", "hpaged_b64"):
+        w = bench.workload_of(name)
+        t = bench.recorded_traffic(w)
+        assert t is not None and t > 0, name
+        if w.batch > 1:
+            assert bench.recorded_traffic(bench.workload_of(name, w.batch // 2)) is None, name
