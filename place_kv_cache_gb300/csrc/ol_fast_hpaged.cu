@@ -1066,7 +1066,7 @@ __global__ void __launch_bounds__(NWARPS * 32, HpLayout<NWARPS, STAGES, CHUNK ? 
     if (g > 0) __syncthreads();  // the previous group's merge is done with the states and scratch
     store_warp_state<true>(reinterpret_cast<float*>(my_stages), ms, warp, o[g], mr[g][0], mr[g][1], lr[g][0],
                            lr[g][1]);
-    merge_and_finish(
+    merge_and_finish<NWARPS>(
         p, w, NWARPS, [&](int st) { return reinterpret_cast<const float*>(stages + st * STAGES * kStage); }, merged,
         nullptr, ms, CHUNK ? zs0 + g : -1);
   }

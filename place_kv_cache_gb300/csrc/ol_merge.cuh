@@ -145,8 +145,12 @@ __device__ __forceinline__ void cluster_store_y(const AttnParams& p, const Work&
 //     the cluster covers its (row, kv head) alone, thread (head j, 4 dims)
 //     forms the merge weights in registers and stores y directly (no further
 //     barrier); otherwise the cluster state goes to finish_split.
+// NS > 0: the caller passes exactly NS states, every one with its O written
+// (zero for a state that saw no visible token), so the CTA level needs no
+// data-dependent branch and the loads of all states issue together; NS = 0:
+// nstates is known only at run time, and a state of weight 0 is skipped.
 // Every thread of every CTA of the cluster must call it.
-template <typename StateO>
+template <int NS = 0, typename StateO>
 __device__ __forceinline__ void merge_and_finish(const AttnParams& p, const Work& w, int nstates, StateO state_o,
                                                  float* merged, float* cmerged, const MergeScratch& ms,
                                                  int zs = -1) {
@@ -159,26 +163,43 @@ __device__ __forceinline__ void merge_and_finish(const AttnParams& p, const Work
   for (int idx = threadIdx.x; idx < G * 16; idx += blockDim.x) {
     const int j = idx >> 4, d = (idx & 15) * 8;
     float M = -INFINITY;
-#pragma unroll 8
-    for (int s = 0; s < nstates; ++s) M = fmaxf(M, ms.wm[s * 8 + j]);
     float L = 0.f;
     float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+    // state s's 8 dims of head j, weighted
+    auto add = [&](int s, float wt) {
+      const float4 v0 = *reinterpret_cast<const float4*>(state_o(s) + j * kOStride + d);
+      const float4 v1 = *reinterpret_cast<const float4*>(state_o(s) + j * kOStride + d + 4);
+      a0.x += wt * v0.x;
+      a0.y += wt * v0.y;
+      a0.z += wt * v0.z;
+      a0.w += wt * v0.w;
+      a1.x += wt * v1.x;
+      a1.y += wt * v1.y;
+      a1.z += wt * v1.z;
+      a1.w += wt * v1.w;
+    };
+    if constexpr (NS > 0) {
+      float mw[NS];
+#pragma unroll
+      for (int s = 0; s < NS; ++s) {
+        mw[s] = ms.wm[s * 8 + j];
+        M = fmaxf(M, mw[s]);
+      }
+#pragma unroll
+      for (int s = 0; s < NS; ++s) {
+        const float wt = (mw[s] == -INFINITY) ? 0.f : fast_exp2(mw[s] - M);
+        L += wt * ms.wl[s * 8 + j];
+        add(s, wt);
+      }
+    } else {
 #pragma unroll 8
-    for (int s = 0; s < nstates; ++s) {
-      const float mw = ms.wm[s * 8 + j];
-      const float wt = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
-      L += wt * ms.wl[s * 8 + j];
-      if (wt != 0.f) {
-        const float4 v0 = *reinterpret_cast<const float4*>(state_o(s) + j * kOStride + d);
-        const float4 v1 = *reinterpret_cast<const float4*>(state_o(s) + j * kOStride + d + 4);
-        a0.x += wt * v0.x;
-        a0.y += wt * v0.y;
-        a0.z += wt * v0.z;
-        a0.w += wt * v0.w;
-        a1.x += wt * v1.x;
-        a1.y += wt * v1.y;
-        a1.z += wt * v1.z;
-        a1.w += wt * v1.w;
+      for (int s = 0; s < nstates; ++s) M = fmaxf(M, ms.wm[s * 8 + j]);
+#pragma unroll 8
+      for (int s = 0; s < nstates; ++s) {
+        const float mw = ms.wm[s * 8 + j];
+        const float wt = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
+        L += wt * ms.wl[s * 8 + j];
+        if (wt != 0.f) add(s, wt);
       }
     }
     if (CS == 1) {
