@@ -546,7 +546,7 @@ OL_API ol_status ol_decode_step_host(int32_t layout, const void* cache_desc, voi
 
 /*
  * The fused decode step with no allocation by anyone: no workspace argument.
- * The paper has no counterpart; it exists for callers that cannot call
+ * The method's pages describe no such call; it exists for callers that cannot call
  * cudaMalloc -- code running inside a host engine that owns all device memory
  * and forbids allocation while it executes (an inference-engine plugin's
  * enqueue, a fixed-arena runtime), or a latency-critical decode loop that
