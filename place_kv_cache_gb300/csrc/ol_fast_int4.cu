@@ -62,8 +62,9 @@ struct Int4Layout {
   static constexpr int kBars = STAGES * 8 + STAGES * 4;  // full barriers, release counters
   static constexpr int kMisc = 256 + (NWARPS + NG) * 8 * 4 * 2 + 8 * 4 * 6 + 16 * 4 + 2 * 16 * 8 * 4 + 16;
   static constexpr int kTotal = 1024 + kStages + kExtra + (kBars + 15) / 16 * 16 + kMisc;
-  // CTAs per SM: shared memory, and registers (128 per thread for one column
-  // group; two groups take up to 255, one CTA per SM)
+  // CTAs per SM: shared memory, and registers (one column group: up to 16
+  // warps per SM, i.e. 128 registers per thread at 8 warps per CTA and up to
+  // 168 at 6; two groups take up to 255, one CTA per SM)
   static constexpr int kBySmem = (228 * 1024) / (kTotal + 1024) > 0 ? (228 * 1024) / (kTotal + 1024) : 1;
   static constexpr int kByRegs = NG > 1 ? 8 / NWARPS : 16 / NWARPS;
   static constexpr int kPerSm = kBySmem < kByRegs ? kBySmem : (kByRegs > 0 ? kByRegs : 1);

@@ -95,29 +95,34 @@ __device__ __forceinline__ void cluster_store_y(const AttnParams& p, const Work&
   const size_t head_base = (size_t)w.b * p.q_heads + (size_t)w.g * Gq;
   for (int idx = threadIdx.x; idx < G * nd4; idx += blockDim.x) {
     const int j = idx / nd4, dd = (idx % nd4) * 4;
-    float mq[CS];
-    float M = -INFINITY;
+    float mq[CS], t[CS];
 #pragma unroll
-    for (int q = 0; q < CS; ++q) {
-      mq[q] = ms.recv_m[q * 8 + j];
-      M = fmaxf(M, mq[q]);
-    }
-    float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < CS; ++q) t[q] = mq[q] = ms.recv_m[q * 8 + j];
+#pragma unroll
+    for (int h = CS / 2; h >= 1; h >>= 1)  // the maximum as a tree
+#pragma unroll
+      for (int q = 0; q < h; ++q) t[q] = fmaxf(t[q], t[q + h]);
+    const float M = t[0];
+    // two partial sums per quantity: half the dependent chain
+    float L2[2] = {0.f, 0.f};
+    float4 acc2[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
 #pragma unroll
     for (int q = 0; q < CS; ++q) {
       const float wq = (mq[q] == -INFINITY) ? 0.f : fast_exp2(mq[q] - M);
-      L += wq * ms.recv_l[q * 8 + j];
+      L2[q & 1] += wq * ms.recv_l[q * 8 + j];
       const float4 v = *reinterpret_cast<const float4*>(ms.recv_o + (q * 8 + j) * dspan + dd);
-      acc.x += wq * v.x;
-      acc.y += wq * v.y;
-      acc.z += wq * v.z;
-      acc.w += wq * v.w;
+      acc2[q & 1].x += wq * v.x;
+      acc2[q & 1].y += wq * v.y;
+      acc2[q & 1].z += wq * v.z;
+      acc2[q & 1].w += wq * v.w;
     }
+    const float L = L2[0] + L2[1];
+    const float4 acc = make_float4(acc2[0].x + acc2[1].x, acc2[0].y + acc2[1].y, acc2[0].z + acc2[1].z,
+                                   acc2[0].w + acc2[1].w);
     if (j >= c_live) continue;
     const size_t o = (nq == 1 ? (head_base + j) : ((head_base + j % Gq) * nq + z0 + j / Gq)) * D + d0 + dd;
-    const float y0 = L > 0.f ? acc.x / L : 0.f, y1 = L > 0.f ? acc.y / L : 0.f;
-    const float y2 = L > 0.f ? acc.z / L : 0.f, y3 = L > 0.f ? acc.w / L : 0.f;
+    const float rl = L > 0.f ? 1.f / L : 0.f;  // one division, four products
+    const float y0 = acc.x * rl, y1 = acc.y * rl, y2 = acc.z * rl, y3 = acc.w * rl;
     if (p.out_dtype == OL_F32) {
       *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o) = make_float4(y0, y1, y2, y3);
     } else {
